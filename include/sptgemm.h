@@ -1,0 +1,118 @@
+/*
+ * sptgemm.h -- C ABI of the software-pipelined tiled GEMM library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the tiled matrix multiply C = A * B of "Hiding Memory
+ * Latency in CUDA: Asynchronous Loads and Software Pipelines" (opening
+ * section: load A and B tiles, stage them in shared memory, multiply on the
+ * tensor cores, advance to the next K tile), software-pipelined so that the
+ * load of K-tile k+1 overlaps the multiply-accumulate of K-tile k (same
+ * page, sections 1, 5 and 11; "Pipeline GPU Kernel", Step 3). Pipelining
+ * reorders loads and leaves the arithmetic alone ("Pipeline GPU Kernel",
+ * Step 5 item 4): the result is the plain product.
+ *
+ * Layouts (all dense, leading dimensions implied by the shape):
+ *   A  row-major    M x K : element (i, k) at A[i*K + k]
+ *   B  column-major K x N : element (k, j) at B[j*K + k]
+ *   C  row-major    M x N : element (i, j) at C[i*N + j]
+ *
+ * Ownership: the caller owns A, B and C, which are device pointers (any
+ * allocation the CUDA runtime can address on the current device). The
+ * library keeps no pointer past a call. It owns one cached scratch area per
+ * (device, stream) for the paths that need one (int8 operand conversion,
+ * split-K partial sums), grown on demand and released at unload.
+ *
+ * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and never synchronizes. Inputs must stay valid
+ * and C untouched by others until the stream reaches the call.
+ *
+ * Errors: functions return an int status, 0 on success, a negative
+ * SPTG_ERR_* code otherwise. No call aborts the process and there is no CPU
+ * fallback: on a machine without an sm_103 device the call fails.
+ */
+#ifndef SPTGEMM_H
+#define SPTGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Input/output element pairs. Float inputs accumulate in fp32; int8 inputs
+ * accumulate exactly and return int32. */
+typedef enum {
+  SPTG_F16_F32 = 0,   /* binary16 A, B -> fp32 C                 */
+  SPTG_F16_F16 = 1,   /* binary16 A, B -> binary16 C (RN-even)   */
+  SPTG_S8_S32 = 2,    /* int8 A, B -> int32 C, bit-exact         */
+  SPTG_BF16_BF16 = 3, /* bfloat16 A, B -> bfloat16 C (RN-even)   */
+  SPTG_BF16_F32 = 4   /* bfloat16 A, B -> fp32 C                 */
+} sptg_dtype;
+
+enum {
+  SPTG_OK = 0,
+  SPTG_ERR_ARG = -1,         /* null pointer with a nonzero extent, negative or
+                                too-large dimension, unknown dtype or option   */
+  SPTG_ERR_ALIGN = -2,       /* a pointer not 16-byte aligned, or a row pitch
+                                (K*sizeof(in), N*sizeof(out)) not a multiple
+                                of 16 bytes, as the tensor-copy engine needs  */
+  SPTG_ERR_UNSUPPORTED = -3, /* no CUDA device of compute capability 10.3    */
+  SPTG_ERR_LAUNCH = -4,      /* a CUDA runtime error; see sptg_last_error()  */
+  SPTG_ERR_TIMEOUT = -5,     /* a kernel gave up a bounded wait (reported by
+                                sptg_device_error)                            */
+  SPTG_ERR_NOMEM = -6,       /* scratch memory could not be allocated        */
+  SPTG_ERR_CONFIG = -7       /* a forced configuration does not fit          */
+};
+
+/*
+ * C = A * B.  M, N, K >= 0.  M == 0 or N == 0: nothing is done.  K == 0:
+ * C is set to zero (the empty sum).  Shapes need not be multiples of any
+ * tile: edges are zero-filled on load and clipped on store.
+ *
+ * Alignment: A, B, C 16-byte aligned; K * sizeof(input) and
+ * N * sizeof(output) multiples of 16 bytes.  Otherwise SPTG_ERR_ALIGN.
+ */
+int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype,
+              const void* A, const void* B, void* C, void* stream);
+
+/* Kernel selection for sptg_gemm_ex; fields left at 0 mean "choose". */
+typedef struct {
+  int kernel;   /* 0 auto, 1 square (tile rows 128), 2 skinny swap-AB        */
+  int bn;       /* square: tile columns (multiple of 16, 16..256)           */
+  int stages;   /* shared-memory ring depth (1 = synchronous load/compute)  */
+  int splits;   /* skinny: number of CTAs sharing the work (0 = SM count)   */
+  int timeout_ms; /* bounded-wait limit inside the kernel (0 = default 2000) */
+  int inject_stall; /* test hook: 1 makes the producer withhold one k-tile so
+                       the consumer's bounded wait runs out; 0 = off          */
+} sptg_config;
+
+/* sptg_gemm with an explicit configuration (NULL = sptg_gemm). */
+int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype,
+                 const void* A, const void* B, void* C, void* stream,
+                 const sptg_config* cfg);
+
+/* Static text for a status code. */
+const char* sptg_status_string(int status);
+
+/* Text of the last CUDA runtime error seen by this thread ("" if none). */
+const char* sptg_last_error(void);
+
+/* Writes "kernel=... bm=... bn=... bk=... stages=... ..." for the last call
+ * made by this thread into buf (NUL-terminated, truncated to len).
+ * Returns the length the full text needs. */
+int sptg_last_config(char* buf, size_t len);
+
+/* Synchronizes `stream`, then reads and clears the current device's error
+ * word written by timed-out waits. Returns SPTG_OK or SPTG_ERR_TIMEOUT
+ * (or SPTG_ERR_LAUNCH if synchronization itself failed). */
+int sptg_device_error(void* stream);
+
+/* Library ABI version (major*100 + minor). */
+int sptg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPTGEMM_H */

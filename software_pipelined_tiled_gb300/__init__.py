@@ -1,0 +1,164 @@
+"""Python binding of the software-pipelined tiled GEMM library (libsptgemm.so).
+
+Argument marshalling only: every step of the product runs in the library's
+CUDA kernels.  PyTorch is used for device memory and streams.  There is no
+fallback: if the library is missing or no sm_103 device is present, calls
+raise.
+
+    import software_pipelined_tiled_gb300 as sptg
+    C = sptg.gemm(A, Bcm, out_dtype=torch.float16)   # C = A @ Bcm.T
+
+A is M x K row-major; B is K x N column-major, passed as its storage, the
+N x K row-major tensor ``Bcm`` (``Bcm[j, k] = B[k, j]``); C is M x N row-major.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from ._build import LIB_PATH, build
+
+__all__ = ["DTYPES", "SptgError", "Config", "load", "gemm", "gemm_raw", "last_config",
+           "last_error", "device_error", "status_string", "LIB_PATH", "build"]
+
+# sptg_dtype values of include/sptgemm.h
+DTYPES = {"f16_f32": 0, "f16_f16": 1, "s8_s32": 2, "bf16_bf16": 3, "bf16_f32": 4}
+STATUS = {0: "SPTG_OK", -1: "SPTG_ERR_ARG", -2: "SPTG_ERR_ALIGN", -3: "SPTG_ERR_UNSUPPORTED",
+          -4: "SPTG_ERR_LAUNCH", -5: "SPTG_ERR_TIMEOUT", -6: "SPTG_ERR_NOMEM",
+          -7: "SPTG_ERR_CONFIG"}
+KERNELS = {"auto": 0, "square": 1, "skinny": 2}
+
+# the C functions every build must export (checked by the tests)
+EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_status_string", "sptg_last_error",
+           "sptg_last_config", "sptg_device_error", "sptg_version")
+
+
+class SptgError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    """sptg_config: 0 in a field means "let the library choose"."""
+    _fields_ = [("kernel", ctypes.c_int), ("bn", ctypes.c_int), ("stages", ctypes.c_int),
+                ("splits", ctypes.c_int), ("timeout_ms", ctypes.c_int),
+                ("inject_stall", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Loads libsptgemm.so (building it first if the sources are newer)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if path is None and not os.path.exists(p):
+            build()
+        lib = ctypes.CDLL(p)
+        i64, vp = ctypes.c_int64, ctypes.c_void_p
+        lib.sptg_gemm.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
+        lib.sptg_gemm.restype = ctypes.c_int
+        lib.sptg_gemm_ex.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp,
+                                     ctypes.POINTER(Config)]
+        lib.sptg_gemm_ex.restype = ctypes.c_int
+        lib.sptg_status_string.argtypes = [ctypes.c_int]
+        lib.sptg_status_string.restype = ctypes.c_char_p
+        lib.sptg_last_error.argtypes = []
+        lib.sptg_last_error.restype = ctypes.c_char_p
+        lib.sptg_last_config.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
+        lib.sptg_last_config.restype = ctypes.c_int
+        lib.sptg_device_error.argtypes = [vp]
+        lib.sptg_device_error.restype = ctypes.c_int
+        lib.sptg_version.argtypes = []
+        lib.sptg_version.restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().sptg_status_string(int(status)).decode()
+
+
+def last_error() -> str:
+    return load().sptg_last_error().decode()
+
+
+def last_config() -> str:
+    lib = load()
+    buf = ctypes.create_string_buffer(512)
+    lib.sptg_last_config(buf, len(buf))
+    return buf.value.decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def gemm_raw(M: int, N: int, K: int, dtype: str | int, A_ptr: int, B_ptr: int, C_ptr: int,
+             stream: int = 0, config: Config | None = None) -> int:
+    """Calls sptg_gemm_ex with raw device pointers; returns the status code."""
+    d = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    cfg = ctypes.byref(config) if config is not None else None
+    return int(load().sptg_gemm_ex(M, N, K, d, A_ptr, B_ptr, C_ptr, stream, cfg))
+
+
+def _dtype_key(in_dtype, out_dtype) -> str:
+    import torch
+    names = {torch.float16: "f16", torch.bfloat16: "bf16", torch.int8: "s8",
+             torch.float32: "f32", torch.int32: "s32"}
+    key = f"{names.get(in_dtype, '?')}_{names.get(out_dtype, '?')}"
+    if key not in DTYPES:
+        raise ValueError(f"unsupported input/output dtype pair {in_dtype} -> {out_dtype}")
+    return key
+
+
+def gemm(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = None,
+         kernel: str | None = None, stages: int = 0, bn: int = 0, splits: int = 0):
+    """C = A * B on the GPU, with A (M x K) and Bcm (N x K) CUDA tensors.
+
+    out_dtype defaults to the input type for binary16/bfloat16 and int32 for
+    int8.  Returns C.  Raises SptgError on any failure.
+    """
+    import torch
+    if A.dim() != 2 or Bcm.dim() != 2 or A.shape[1] != Bcm.shape[1]:
+        raise ValueError("A must be M x K and Bcm N x K")
+    if A.dtype != Bcm.dtype:
+        raise ValueError("A and Bcm must have the same dtype")
+    if not (A.is_cuda and Bcm.is_cuda):
+        raise ValueError("A and Bcm must be CUDA tensors")
+    if not (A.is_contiguous() and Bcm.is_contiguous()):
+        raise ValueError("A and Bcm must be contiguous")
+    M, K = A.shape
+    N = Bcm.shape[0]
+    if out_dtype is None:
+        out_dtype = C.dtype if C is not None else (torch.int32 if A.dtype == torch.int8 else A.dtype)
+    key = _dtype_key(A.dtype, out_dtype)
+    if C is None:
+        C = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    elif C.shape != (M, N) or C.dtype != out_dtype or not C.is_contiguous() or not C.is_cuda:
+        raise ValueError("C must be a contiguous M x N CUDA tensor of the output dtype")
+    if config is None and (kernel or stages or bn or splits):
+        config = Config(KERNELS[kernel or "auto"], bn, stages, splits, 0, 0)
+    with torch.cuda.device(A.device):
+        rc = gemm_raw(M, N, K, key, A.data_ptr(), Bcm.data_ptr(), C.data_ptr(),
+                      _stream_handle(stream), config)
+    if rc != 0:
+        raise SptgError(rc, last_error() or status_string(rc))
+    return C
+
+
+def device_error(stream=None) -> int:
+    """Synchronizes the stream and returns (and clears) the device error status."""
+    return int(load().sptg_device_error(_stream_handle(stream)))

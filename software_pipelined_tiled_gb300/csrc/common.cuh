@@ -1,0 +1,106 @@
+// common.cuh -- shared device-side pieces of the GEMM kernels: the bounded
+// mbarrier wait, the output conversions and the tile raster.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace sptg {
+
+// Output element kinds of the epilogue.
+enum OutKind : int { OUT_F32 = 0, OUT_F16 = 1, OUT_BF16 = 2, OUT_S32 = 3 };
+
+template <int OUT>
+struct OutTraits {
+  static constexpr int bytes = (OUT == OUT_F16 || OUT == OUT_BF16) ? 2 : 4;
+};
+
+// Codes or-ed into the device error word when a bounded wait runs out; the
+// bit names the wait that gave up.
+enum WaitSite : unsigned int {
+  WAIT_PRODUCER_EMPTY = 1u << 0,
+  WAIT_MMA_FULL = 1u << 1,
+  WAIT_MMA_TMEM_EMPTY = 1u << 2,
+  WAIT_EPI_TMEM_FULL = 1u << 3,
+  WAIT_DRAIN = 1u << 4,
+};
+
+// Everything a bounded wait needs: the limit, where to report, and the
+// CTA-wide abort flag that lets the other roles stop early once one gave up.
+struct WaitCtl {
+  uint64_t timeout_ns;
+  unsigned int* error_word;
+  volatile int* abort_flag;  // in shared memory
+};
+
+// Waits for the phase of `bar` with parity `parity` to complete, for at most
+// ctl.timeout_ns. On time-out it records `site` in the error word, raises the
+// CTA's abort flag and returns false; it also returns false as soon as
+// another role of the CTA has raised the flag.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
+                                             unsigned int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((spin & 63u) == 0) {
+      if (*ctl.abort_flag) return false;
+      if (global_timer_ns() - t0 > ctl.timeout_ns) {
+        *ctl.abort_flag = 1;
+        atomicOr(ctl.error_word, site);
+        return false;
+      }
+    }
+  }
+}
+
+// Barrier over `nthreads` threads (named barrier `id`) that also returns the
+// AND of every participant's `pred`, so a group of warps takes one decision.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pin, pout;\n\t"
+      "setp.ne.u32 pin, %1, 0;\n\t"
+      "bar.red.and.pred pout, %2, %3, pin;\n\t"
+      "selp.u32 %0, 1, 0, pout;\n\t}"
+      : "=r"(out)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Packs two fp32 values into one 32-bit word of the 16-bit output type
+// (round to nearest even; `lo` lands at the lower address).
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (OUT == OUT_F16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// Tile index -> (m tile, n tile). Tiles are visited in column strips of
+// `group` m-tiles so that CTAs running at the same time share A and B tiles
+// in L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_m_tiles, int num_n_tiles, int group,
+                                            int& m_tile, int& n_tile) {
+  const int per_group = group * num_n_tiles;
+  const int g = tile / per_group;
+  const int first_m = g * group;
+  const int rows = min(group, num_m_tiles - first_m);
+  const int r = tile - g * per_group;
+  m_tile = first_m + r % rows;
+  n_tile = r / rows;
+}
+
+}  // namespace sptg

@@ -1,0 +1,554 @@
+// sptgemm.cu -- the C ABI of the library (declared in include/sptgemm.h):
+// argument checks, kernel choice, tensor-map encoding and launch.
+//
+// All device work runs in the kernels of square_gemm.cuh, skinny_gemm.cuh and
+// convert.cuh; this file only validates, plans and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <set>
+#include <string>
+#include <utility>
+
+#include "sptgemm.h"
+
+#include "convert.cuh"
+#include "skinny_gemm.cuh"
+#include "square_gemm.cuh"
+
+// Device error word: a timed-out bounded wait ors its site code in here.
+__device__ unsigned int g_sptg_error_word;
+
+namespace {
+
+using namespace sptg;
+
+thread_local std::string t_last_error;
+thread_local std::string t_last_config;
+
+void set_config_text(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_config = buf;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  t_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return SPTG_ERR_LAUNCH;
+}
+
+// ------------------------------------------------------------ driver entry
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// ------------------------------------------------------------ device state
+struct DeviceInfo {
+  bool ok = false;
+  int sm_count = 0;
+  int major = 0, minor = 0;
+  unsigned int* error_word = nullptr;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::set<std::pair<int, const void*>> g_smem_set;
+
+int device_info(DeviceInfo& out, int& dev) {
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    t_last_error = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+    return SPTG_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_devices.find(dev);
+  if (it != g_devices.end()) {
+    out = it->second;
+    return out.ok ? SPTG_OK : SPTG_ERR_UNSUPPORTED;
+  }
+  DeviceInfo d;
+  cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+  d.ok = (d.major == 10 && d.minor == 3);
+  if (d.ok) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_sptg_error_word);
+    if (e != cudaSuccess) {
+      t_last_error = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
+      return SPTG_ERR_LAUNCH;
+    }
+    d.error_word = static_cast<unsigned int*>(p);
+  } else {
+    char b[128];
+    snprintf(b, sizeof(b), "device %d has compute capability %d.%d; this library needs 10.3", dev,
+             d.major, d.minor);
+    t_last_error = b;
+  }
+  g_devices[dev] = d;
+  out = d;
+  return d.ok ? SPTG_OK : SPTG_ERR_UNSUPPORTED;
+}
+
+int ensure_smem(int dev, const void* kernel, int bytes) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_smem_set.count({dev, kernel})) return SPTG_OK;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_smem_set.insert({dev, kernel});
+  return SPTG_OK;
+}
+
+// ------------------------------------------------------------ scratch space
+// One stream-ordered scratch area per (device, stream), grown on demand.
+struct Scratch {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
+
+int scratch_for(int dev, cudaStream_t stream, size_t need, void** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Scratch& s = g_scratch[{dev, stream}];
+  if (s.bytes < need) {
+    if (s.ptr) cudaFreeAsync(s.ptr, stream);
+    s.ptr = nullptr;
+    s.bytes = 0;
+    size_t grow = std::max(need, static_cast<size_t>(1) << 20);
+    cudaError_t e = cudaMallocAsync(&s.ptr, grow, stream);
+    if (e != cudaSuccess) {
+      s.ptr = nullptr;
+      t_last_error = std::string("cudaMallocAsync: ") + cudaGetErrorString(e);
+      return SPTG_ERR_NOMEM;
+    }
+    s.bytes = grow;
+  }
+  *out = s.ptr;
+  return SPTG_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+int make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
+                uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+  auto enc = tensor_map_encoder();
+  if (!enc) {
+    t_last_error = "cuTensorMapEncodeTiled is not available from the driver";
+    return SPTG_ERR_UNSUPPORTED;
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char b[160];
+    snprintf(b, sizeof(b), "cuTensorMapEncodeTiled failed (%d) for %llux%llu box %ux%u", (int)r,
+             (unsigned long long)outer, (unsigned long long)inner, box_outer, box_inner);
+    t_last_error = b;
+    return SPTG_ERR_ARG;
+  }
+  return SPTG_OK;
+}
+
+// ------------------------------------------------------------ dtype table
+struct DtypeInfo {
+  int in_bytes, out_bytes;
+  bool in_bf16, is_int8;
+  int out_kind;
+  CUtensorMapDataType in_tma, out_tma;
+  const char* name;
+};
+
+bool dtype_info(int dtype, DtypeInfo& d) {
+  switch (dtype) {
+    case SPTG_F16_F32:
+      d = {2, 4, false, false, OUT_F32, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+           CU_TENSOR_MAP_DATA_TYPE_FLOAT32, "f16_f32"};
+      return true;
+    case SPTG_F16_F16:
+      d = {2, 2, false, false, OUT_F16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+           CU_TENSOR_MAP_DATA_TYPE_FLOAT16, "f16_f16"};
+      return true;
+    case SPTG_S8_S32:
+      d = {1, 4, false, true, OUT_S32, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+           CU_TENSOR_MAP_DATA_TYPE_INT32, "s8_s32"};
+      return true;
+    case SPTG_BF16_BF16:
+      d = {2, 2, true, false, OUT_BF16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+           CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, "bf16_bf16"};
+      return true;
+    case SPTG_BF16_F32:
+      d = {2, 4, true, false, OUT_F32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+           CU_TENSOR_MAP_DATA_TYPE_FLOAT32, "bf16_f32"};
+      return true;
+    default:
+      return false;
+  }
+}
+
+// ------------------------------------------------------------ square path
+using SquareKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, SquareParams);
+
+struct SquareVariant {
+  SquareKernel fn;
+  int bn, stages, smem;
+};
+
+template <int BN, int ST, bool BF, int OUT, bool IE>
+SquareVariant square_variant() {
+  return {reinterpret_cast<SquareKernel>(&square_gemm_kernel<BN, ST, BF, OUT, IE>), BN, ST,
+          SquareLayout<BN, ST, IE>::SMEM_BYTES};
+}
+
+// Ring depth choices per dtype: the deepest ring that fits next to the
+// epilogue staging (4 stages of 48 KiB at BN = 256) plus the shallower ones
+// for the pipelining ablation (1 = synchronous load then compute).
+bool pick_square(const DtypeInfo& d, int stages_req, int bn_req, SquareVariant& v) {
+  const int st = stages_req;
+  if (d.is_int8) {
+    if (bn_req && bn_req != 128) return false;
+    switch (st ? st : 6) {
+      case 6: v = square_variant<128, 6, false, OUT_S32, true>(); return true;
+      default: return false;
+    }
+  }
+  if (bn_req && bn_req != 256) return false;
+  const int s = st ? st : 4;
+  switch (d.out_kind) {
+    case OUT_F16:
+      switch (s) {
+        case 1: v = square_variant<256, 1, false, OUT_F16, false>(); return true;
+        case 2: v = square_variant<256, 2, false, OUT_F16, false>(); return true;
+        case 3: v = square_variant<256, 3, false, OUT_F16, false>(); return true;
+        case 4: v = square_variant<256, 4, false, OUT_F16, false>(); return true;
+        default: return false;
+      }
+    case OUT_BF16:
+      if (s != 4) return false;
+      v = square_variant<256, 4, true, OUT_BF16, false>();
+      return true;
+    case OUT_F32:
+      if (s != 4) return false;
+      if (d.in_bf16)
+        v = square_variant<256, 4, true, OUT_F32, false>();
+      else
+        v = square_variant<256, 4, false, OUT_F32, false>();
+      return true;
+    default:
+      return false;
+  }
+}
+
+int run_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N, int64_t K,
+               const void* A16, const void* B16, void* C, cudaStream_t stream,
+               const sptg_config& cfg) {
+  SquareVariant v;
+  if (!pick_square(d, cfg.stages, cfg.bn, v)) {
+    t_last_error = "no square-kernel variant for the requested stages/bn";
+    return SPTG_ERR_CONFIG;
+  }
+  const int BM = 128, BK = 64;
+  CUtensorMap ta, tb, tc;
+  int rc = make_map_2d(&ta, d.in_tma, 2, A16, K, M, BK, BM);
+  if (rc) return rc;
+  rc = make_map_2d(&tb, d.in_tma, 2, B16, K, N, BK, v.bn);
+  if (rc) return rc;
+  rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, 128 / d.out_bytes, 32);
+  if (rc) return rc;
+  rc = ensure_smem(dev, reinterpret_cast<const void*>(v.fn), v.smem);
+  if (rc) return rc;
+
+  SquareParams p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_m_tiles = static_cast<int>((M + BM - 1) / BM);
+  p.num_n_tiles = static_cast<int>((N + v.bn - 1) / v.bn);
+  p.num_k_tiles = static_cast<int>((K + BK - 1) / BK);
+  p.k_tiles_per_chunk = d.is_int8 ? 1024 / BK : p.num_k_tiles;
+  p.group_m = 8;
+  p.error_word = di.error_word;
+  p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
+  p.inject_stall = cfg.inject_stall;
+  const int tiles = p.num_m_tiles * p.num_n_tiles;
+  const int grid = std::min(tiles, cfg.splits > 0 ? cfg.splits : di.sm_count);
+  v.fn<<<grid, 192, v.smem, stream>>>(ta, tb, tc, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "square_gemm launch");
+  set_config_text(
+      "kernel=square dtype=%s bm=%d bn=%d bk=%d stages=%d grid=%d tiles=%d k_tiles=%d "
+      "chunk_k_tiles=%d smem=%d",
+      d.name, BM, v.bn, BK, v.stages, grid, tiles, p.num_k_tiles, p.k_tiles_per_chunk, v.smem);
+  return SPTG_OK;
+}
+
+// ------------------------------------------------------------ skinny path
+using SkinnyKernel = void (*)(CUtensorMap, CUtensorMap, SkinnyParams);
+
+struct SkinnyVariant {
+  SkinnyKernel fn;
+  int mn, stages, smem;
+};
+
+template <int MN, int ST, bool BF, int OUT>
+SkinnyVariant skinny_variant() {
+  return {reinterpret_cast<SkinnyKernel>(&skinny_gemm_kernel<MN, ST, BF, OUT>), MN, ST,
+          SkinnyLayout<MN, ST>::SMEM_BYTES};
+}
+
+bool pick_skinny(const DtypeInfo& d, int stages_req, SkinnyVariant& v) {
+  const int s = stages_req ? stages_req : 8;
+  if (d.is_int8) return false;
+#define SPTG_SKINNY_CASES(ST)                                                     \
+  case ST:                                                                        \
+    if (d.out_kind == OUT_BF16) v = skinny_variant<64, ST, true, OUT_BF16>();      \
+    else if (d.out_kind == OUT_F16) v = skinny_variant<64, ST, false, OUT_F16>();  \
+    else if (d.in_bf16) v = skinny_variant<64, ST, true, OUT_F32>();               \
+    else v = skinny_variant<64, ST, false, OUT_F32>();                             \
+    return true;
+  switch (s) {
+    SPTG_SKINNY_CASES(8)
+    case 1:
+    case 2:
+    case 4:
+      if (d.out_kind != OUT_BF16) return false;
+      v = s == 1 ? skinny_variant<64, 1, true, OUT_BF16>()
+                 : s == 2 ? skinny_variant<64, 2, true, OUT_BF16>()
+                          : skinny_variant<64, 4, true, OUT_BF16>();
+      return true;
+    default:
+      return false;
+  }
+#undef SPTG_SKINNY_CASES
+}
+
+int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N, int64_t K,
+               const void* A, const void* B, void* C, cudaStream_t stream,
+               const sptg_config& cfg) {
+  SkinnyVariant v;
+  if (!pick_skinny(d, cfg.stages, v) || M > v.mn) {
+    t_last_error = "no skinny-kernel variant for the requested dtype/stages/M";
+    return SPTG_ERR_CONFIG;
+  }
+  const int BNT = 128, BK = 64;
+  CUtensorMap tb, ta;
+  // MMA operand A is the B^T tile (128 output columns x 64 k), operand B is the A tile.
+  int rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT);
+  if (rc) return rc;
+  rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.mn);
+  if (rc) return rc;
+  rc = ensure_smem(dev, reinterpret_cast<const void*>(v.fn), v.smem);
+  if (rc) return rc;
+
+  SkinnyParams p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_n_tiles = static_cast<int>((N + BNT - 1) / BNT);
+  p.num_k_tiles = static_cast<int>((K + BK - 1) / BK);
+  const int64_t units = static_cast<int64_t>(p.num_n_tiles) * p.num_k_tiles;
+  int grid = cfg.splits > 0 ? cfg.splits : di.sm_count;
+  grid = static_cast<int>(std::min<int64_t>(grid, units));
+  p.num_ctas = grid;
+  p.total_units = units;
+  // Largest number of CTAs that can share one n-tile: ceil(kt / per_cta) + 1.
+  const int64_t per_cta_min = units / grid;
+  int max_contrib = per_cta_min > 0 ? static_cast<int>((p.num_k_tiles + per_cta_min - 1) / per_cta_min) + 1
+                                    : grid;
+  max_contrib = std::min(max_contrib, grid);
+  p.max_contrib = max_contrib;
+  p.C = C;
+  p.error_word = di.error_word;
+  p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
+  p.inject_stall = cfg.inject_stall;
+
+  // Scratch: fp32 partial tiles [n_tile][contributor][MN x 128] then one
+  // arrival counter per n-tile (zeroed here, and re-zeroed by the last arrival).
+  const bool split = grid > p.num_n_tiles;
+  size_t partial_bytes = 0, counter_bytes = 0;
+  if (split) {
+    partial_bytes = static_cast<size_t>(p.num_n_tiles) * max_contrib * v.mn * BNT * sizeof(float);
+    counter_bytes = static_cast<size_t>(p.num_n_tiles) * sizeof(unsigned int);
+    void* ws = nullptr;
+    rc = scratch_for(dev, stream, partial_bytes + counter_bytes + 256, &ws);
+    if (rc) return rc;
+    p.partials = static_cast<float*>(ws);
+    p.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + partial_bytes);
+    cudaError_t e = cudaMemsetAsync(p.counters, 0, counter_bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  } else {
+    p.partials = nullptr;
+    p.counters = nullptr;
+  }
+  v.fn<<<grid, 192, v.smem, stream>>>(tb, ta, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "skinny_gemm launch");
+  set_config_text(
+      "kernel=skinny dtype=%s mma_m=%d mma_n=%d bk=%d stages=%d grid=%d n_tiles=%d k_tiles=%d "
+      "units=%lld max_contrib=%d smem=%d",
+      d.name, BNT, v.mn, BK, v.stages, grid, p.num_n_tiles, p.num_k_tiles, (long long)units,
+      max_contrib, v.smem);
+  return SPTG_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// ================================================================ C ABI
+extern "C" {
+
+int sptg_version(void) { return 100; }
+
+const char* sptg_status_string(int status) {
+  switch (status) {
+    case SPTG_OK: return "ok";
+    case SPTG_ERR_ARG: return "invalid argument";
+    case SPTG_ERR_ALIGN: return "pointer or row pitch not 16-byte aligned";
+    case SPTG_ERR_UNSUPPORTED: return "no sm_103 (compute capability 10.3) device";
+    case SPTG_ERR_LAUNCH: return "CUDA runtime error";
+    case SPTG_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    case SPTG_ERR_NOMEM: return "scratch memory allocation failed";
+    case SPTG_ERR_CONFIG: return "requested configuration not available";
+    default: return "unknown status";
+  }
+}
+
+const char* sptg_last_error(void) { return t_last_error.c_str(); }
+
+int sptg_last_config(char* buf, size_t len) {
+  if (buf && len) {
+    size_t n = std::min(len - 1, t_last_config.size());
+    memcpy(buf, t_last_config.data(), n);
+    buf[n] = '\0';
+  }
+  return static_cast<int>(t_last_config.size());
+}
+
+int sptg_device_error(void* stream) {
+  int dev = 0;
+  DeviceInfo di;
+  int rc = device_info(di, dev);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int word = 0, zero = 0;
+  e = cudaMemcpy(&word, di.error_word, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+  e = cudaMemcpy(di.error_word, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word reset)");
+  if (word) {
+    char b[96];
+    snprintf(b, sizeof(b), "bounded wait ran out (site mask 0x%x)", word);
+    t_last_error = b;
+    return SPTG_ERR_TIMEOUT;
+  }
+  return SPTG_OK;
+}
+
+int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B,
+                 void* C, void* stream, const sptg_config* cfg_in) {
+  sptg_config cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  if (cfg_in) cfg = *cfg_in;
+  DtypeInfo d;
+  if (!dtype_info(dtype, d)) {
+    t_last_error = "unknown dtype";
+    return SPTG_ERR_ARG;
+  }
+  if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) {
+    t_last_error = "dimensions must be in [0, 2^31)";
+    return SPTG_ERR_ARG;
+  }
+  if (cfg.kernel < 0 || cfg.kernel > 2 || cfg.stages < 0 || cfg.bn < 0 || cfg.splits < 0 ||
+      cfg.timeout_ms < 0 || (cfg.inject_stall != 0 && cfg.inject_stall != 1)) {
+    t_last_error = "invalid configuration field";
+    return SPTG_ERR_ARG;
+  }
+  if (M == 0 || N == 0) {
+    set_config_text("kernel=none dtype=%s (empty output)", d.name);
+    return SPTG_OK;
+  }
+  if (!C || (K > 0 && (!A || !B))) {
+    t_last_error = "null pointer";
+    return SPTG_ERR_ARG;
+  }
+  if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))) ||
+      (K * d.in_bytes) % 16 != 0 || (N * d.out_bytes) % 16 != 0) {
+    t_last_error = "TMA needs 16-byte aligned bases and row pitches";
+    return SPTG_ERR_ALIGN;
+  }
+  int dev = 0;
+  DeviceInfo di;
+  int rc = device_info(di, dev);
+  if (rc) return rc;
+  cudaStream_t stream_h = static_cast<cudaStream_t>(stream);
+
+  if (K == 0) {  // the empty sum
+    cudaError_t e = cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * d.out_bytes, stream_h);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    set_config_text("kernel=zero-fill dtype=%s", d.name);
+    return SPTG_OK;
+  }
+
+  // Shape class: few output rows and a float type -> the memory-bound
+  // swap-AB kernel; everything else -> the square tile kernel.
+  int kernel = cfg.kernel;
+  if (kernel == 0) kernel = (!d.is_int8 && M <= 64 && N >= 1024) ? 2 : 1;
+  if (kernel == 2) return run_skinny(dev, di, d, M, N, K, A, B, C, stream_h, cfg);
+
+  if (d.is_int8) {
+    // Widen both operands to binary16 in scratch, then run the exact path.
+    const size_t a_bytes = static_cast<size_t>(M) * K * 2, b_bytes = static_cast<size_t>(N) * K * 2;
+    const size_t a_pad = (a_bytes + 255) & ~static_cast<size_t>(255);
+    void* ws = nullptr;
+    rc = scratch_for(dev, stream_h, a_pad + b_bytes, &ws);
+    if (rc) return rc;
+    void* A16 = ws;
+    void* B16 = static_cast<char*>(ws) + a_pad;
+    const int64_t na = M * K / 16, nb = N * K / 16;
+    const int blocks_a = static_cast<int>(std::min<int64_t>((na + 255) / 256, 8 * di.sm_count));
+    const int blocks_b = static_cast<int>(std::min<int64_t>((nb + 255) / 256, 8 * di.sm_count));
+    s8_to_f16_kernel<<<blocks_a, 256, 0, stream_h>>>(static_cast<const int4*>(A),
+                                                     static_cast<uint4*>(A16), na);
+    s8_to_f16_kernel<<<blocks_b, 256, 0, stream_h>>>(static_cast<const int4*>(B),
+                                                     static_cast<uint4*>(B16), nb);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "s8_to_f16 launch");
+    return run_square(dev, di, d, M, N, K, A16, B16, C, stream_h, cfg);
+  }
+  return run_square(dev, di, d, M, N, K, A, B, C, stream_h, cfg);
+}
+
+int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B, void* C,
+              void* stream) {
+  return sptg_gemm_ex(M, N, K, dtype, A, B, C, stream, nullptr);
+}
+
+}  // extern "C"

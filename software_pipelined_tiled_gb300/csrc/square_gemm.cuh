@@ -1,0 +1,338 @@
+// square_gemm.cuh -- the software-pipelined tiled GEMM for sm_103a.
+//
+// C (M x N, row-major) = A (M x K, row-major) * B (K x N, column-major), i.e.
+// both operands K-major.  One CTA per SM, persistent over output tiles of
+// 128 x BN, with three roles in warp specialisation:
+//
+//   warp 0     producer: for every K-tile, waits until its ring stage is free
+//              (the stage's "empty" mbarrier), then has the tensor-copy engine
+//              load the A tile (128 x 64) and the B tile (BN x 64) into it;
+//              the copy completes the stage's "full" mbarrier by byte count.
+//   warp 1     MMA issuer: waits for "full", issues four tcgen05.mma (K = 16
+//              each) into a tensor-memory accumulator, then tcgen05.commit
+//              arrives on "empty" once those MMAs have read the stage.
+//   warps 2-5  epilogue: wait until an accumulator is complete, read it from
+//              tensor memory (each warp owns 32 of the 128 lanes), convert,
+//              stage 32-row blocks in shared memory and store them with the
+//              tensor-copy engine; then hand the accumulator back.
+//
+// This is the producer/consumer ring of "Hiding Memory Latency in CUDA:
+// Asynchronous Loads and Software Pipelines" (sections 5, 6 and 11): stage =
+// k-tile mod STAGES, separate read and write positions each with its own
+// wrap, "producer never overwrites an in-use stage" enforced by the empty
+// barrier and "consumer never reads an incomplete stage" by the full barrier.
+// The prologue is the producer running up to STAGES tiles ahead, the steady
+// state is the overlap, and the drain is the final commit of a tile's last
+// MMA ("Pipeline GPU Kernel", Step 3).  The register-fragment pipeline of the
+// Ampere design (section 7) has no counterpart: tcgen05.mma reads both
+// operands from shared memory and accumulates in tensor memory; its place is
+// taken by two accumulators, so the epilogue of one tile overlaps the K-loop
+// of the next.
+//
+// INT_EXACT mode computes an int8 product exactly on the fp16 tensor path: the
+// inputs are int8 values held as binary16 (exact), every product is an integer
+// of magnitude <= 2^14 and every partial sum of at most 1024 products is an
+// integer of magnitude <= 2^24, which fp32 holds exactly.  The K-loop is cut
+// into chunks of 1024; each chunk's fp32 accumulator is converted to int32 and
+// added to an int32 running sum kept in tensor memory.
+#pragma once
+
+#include "common.cuh"
+
+namespace sptg {
+
+struct SquareParams {
+  int M, N, K;
+  int num_m_tiles, num_n_tiles, num_k_tiles;
+  int k_tiles_per_chunk;  // accumulation chunk (all K-tiles unless INT_EXACT)
+  int group_m;            // raster strip height in m-tiles
+  unsigned int* error_word;
+  uint64_t timeout_ns;
+  int inject_stall;  // test hook: withhold the load of the second K-tile
+};
+
+template <int BN, int STAGES, bool INT_EXACT>
+struct SquareLayout {
+  static constexpr int BM = 128;
+  static constexpr int BK = 64;  // 64 16-bit elements = one 128-byte swizzle row
+  static constexpr int A_STAGE = BM * BK * 2;
+  static constexpr int B_STAGE = BN * BK * 2;
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_BUF = 32 * 128;  // 32 rows x 128 bytes
+  static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+  static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int BYTES_USED = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = BYTES_USED + 1024;  // slack to align the base to 1024
+  static constexpr int TMEM_NEEDED = 2 * BN + (INT_EXACT ? BN : 0);
+  static constexpr int TMEM_COLS = TMEM_NEEDED <= 32    ? 32
+                                   : TMEM_NEEDED <= 64  ? 64
+                                   : TMEM_NEEDED <= 128 ? 128
+                                   : TMEM_NEEDED <= 256 ? 256
+                                                        : 512;
+  static_assert(TMEM_NEEDED <= 512, "accumulators exceed tensor memory");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
+};
+
+template <int BN, int STAGES, bool IN_BF16, int OUT, bool INT_EXACT>
+__global__ void __launch_bounds__(192, 1)
+    square_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC, const SquareParams p) {
+  using L = SquareLayout<BN, STAGES, INT_EXACT>;
+  constexpr int BM = L::BM, BK = L::BK;
+  constexpr int OBYTES = OutTraits<OUT>::bytes;
+  constexpr int COLS_PER_STORE = 128 / OBYTES;  // output columns per 128-byte row block
+  constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, BM, BN);
+  static_assert(!INT_EXACT || OUT == OUT_S32, "exact integer mode writes int32");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t sA = sbase + L::OFF_A;
+  const uint32_t sB = sbase + L::OFF_B;
+  uint8_t* epi_buf = smem + L::OFF_EPI;
+  const uint32_t bar0 = sbase + L::OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), L::EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const WaitCtl ctl{p.timeout_ns, p.error_word, abort_flag};
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+  const int num_chunks = (p.num_k_tiles + p.k_tiles_per_chunk - 1) / p.k_tiles_per_chunk;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensor_map(&tmA);
+      prefetch_tensor_map(&tmB);
+      const uint64_t pol = policy_evict_last();  // operands are re-read by other tiles
+      int issued_round[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
+      bool ok = true;
+      uint32_t it = 0;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        int mt, nt;
+        tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+        for (int kt = 0; kt < p.num_k_tiles; ++kt, ++it) {
+          const int s = it % STAGES;
+          const uint32_t round = it / STAGES;
+          if (!wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl, WAIT_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          if (p.inject_stall && it == 1) continue;  // test hook: this stage never fills
+          mbar_arrive_expect_tx(full_bar(s), L::A_STAGE + L::B_STAGE);
+          tma_load_2d(sA + s * L::A_STAGE, &tmA, full_bar(s), kt * BK, mt * BM, pol);
+          tma_load_2d(sB + s * L::B_STAGE, &tmB, full_bar(s), kt * BK, nt * BN, pol);
+          issued_round[s] = static_cast<int>(round);
+        }
+      }
+      if (!ok) {
+        // Let every copy already issued land before the CTA can exit.
+        const WaitCtl drain{ctl.timeout_ns, ctl.error_word, ctl.abort_flag};
+        for (int s = 0; s < STAGES; ++s) {
+          if (issued_round[s] < 0) continue;
+          const uint32_t bar = full_bar(s), par = static_cast<uint32_t>(issued_round[s]) & 1u;
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(bar, par) && global_timer_ns() - t0 < drain.timeout_ns) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t it = 0, unit = 0;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int c = 0; ok && c < num_chunks; ++c, ++unit) {
+          const uint32_t b = unit & 1u;
+          const uint32_t use = unit >> 1;
+          if (!wait_bounded(tempty_bar(b), (use & 1u) ^ 1u, ctl, WAIT_MMA_TMEM_EMPTY)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + b * BN;
+          const int kt0 = c * p.k_tiles_per_chunk;
+          const int kt1 = min(p.num_k_tiles, kt0 + p.k_tiles_per_chunk);
+          for (int kt = kt0; kt < kt1; ++kt, ++it) {
+            const int s = it % STAGES;
+            const uint32_t round = it / STAGES;
+            if (!wait_bounded(full_bar(s), round & 1u, ctl, WAIT_MMA_FULL)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = sA + s * L::A_STAGE;
+            const uint32_t b_addr = sB + s * L::B_STAGE;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              mma_f16(d_tmem, sdesc_k_major_sw128(a_addr + 32 * k),
+                      sdesc_k_major_sw128(b_addr + 32 * k), IDESC,
+                      (kt > kt0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(empty_bar(s));  // stage s may be refilled once these MMAs have read it
+          }
+          if (ok) mma_commit(tfull_bar(b));  // accumulator b holds the finished chunk
+        }
+      }
+      // Drain: every MMA issued above has completed before tensor memory is freed.
+      mma_commit(drain_bar);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < ctl.timeout_ns) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // tensor-memory lane quadrant this warp may access
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    uint8_t* bufs = epi_buf + (warp - 2) * 2 * L::EPI_BUF;
+    uint32_t stores = 0, unit = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      int mt, nt;
+      tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+      for (int c = 0; c < num_chunks; ++c, ++unit) {
+        const uint32_t b = unit & 1u;
+        const uint32_t use = unit >> 1;
+        // every lane waits, and the warp leaves together: the tensor-memory
+        // loads below are warp-collective
+        ok = __all_sync(0xffffffffu, wait_bounded(tfull_bar(b), use & 1u, ctl, WAIT_EPI_TMEM_FULL));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t t_acc = tmem_base + lane_base + b * BN;
+        const bool last_chunk = (c == num_chunks - 1);
+
+        if constexpr (INT_EXACT) {
+          const uint32_t t_sum = tmem_base + lane_base + 2 * BN;
+#pragma unroll 1
+          for (int cb = 0; cb < BN / 32; ++cb) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_acc + 32 * cb, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+            if (c > 0) {
+              uint32_t s[32];
+              tmem_ld_32x32b_x32(t_sum + 32 * cb, s);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(static_cast<int32_t>(v[i]) + static_cast<int32_t>(s[i]));
+            }
+            if (!last_chunk) {
+              tmem_st_32x32b_x32(t_sum + 32 * cb, v);
+            } else {
+              // 32 int32 columns = one 128-byte row block
+              uint8_t* buf = bufs + (stores & 1u) * L::EPI_BUF;
+              if (lane == 0) bulk_wait_group_read<1>();
+              __syncwarp();
+              uint8_t* row = buf + lane * 128;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint4 w = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = w;
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmC, smem_addr(buf), nt * BN + 32 * cb, mt * BM + 32 * q);
+                bulk_commit_group();
+              }
+              ++stores;
+            }
+          }
+          if (!last_chunk) tmem_wait_st();
+        } else {
+#pragma unroll 1
+          for (int cb = 0; cb < BN / COLS_PER_STORE; ++cb) {
+            uint32_t w[32];  // one 128-byte output row for this lane
+            if constexpr (OBYTES == 4) {
+              tmem_ld_32x32b_x32(t_acc + 32 * cb, w);
+              tmem_wait_ld();
+              if constexpr (OUT == OUT_S32) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) w[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(w[i])));
+              }
+            } else {
+              uint32_t v0[32], v1[32];
+              tmem_ld_32x32b_x32(t_acc + 64 * cb, v0);
+              tmem_ld_32x32b_x32(t_acc + 64 * cb + 32, v1);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                w[i] = pack2<OUT>(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+                w[16 + i] = pack2<OUT>(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+              }
+            }
+            uint8_t* buf = bufs + (stores & 1u) * L::EPI_BUF;
+            if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf is done reading
+            __syncwarp();
+            uint8_t* row = buf + lane * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+              *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, smem_addr(buf), nt * BN + COLS_PER_STORE * cb, mt * BM + 32 * q);
+              bulk_commit_group();
+            }
+            ++stores;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(b));
+      }
+    }
+    if (lane == 0) bulk_wait_group_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+}  // namespace sptg

@@ -1,0 +1,64 @@
+"""Shared helpers of the GPU parity tests: run the library, ask the oracle, compare.
+
+The float bar is the per-element bound |C - C_ref| <= 1e-3 * sum_k |A_ik B_kj|
+(C_ref the oracle's fp64 sum, not rounded to the output type); the int8 bar
+is equality with the oracle's int64 sum.
+"""
+import numpy as np
+import torch
+
+import oracle
+import software_pipelined_tiled_gb300 as sptg
+
+TOL = 1e-3  # relative to sum_k |A_ik B_kj|
+
+IN_TYPE = {torch.float16: oracle.IN_F16, torch.bfloat16: oracle.IN_BF16}
+
+
+def run(A, Bcm, out_dtype, **kw):
+    """Runs the library on CPU tensors A, Bcm; returns C on the CPU."""
+    dA, dB = A.cuda(), Bcm.cuda()
+    C = sptg.gemm(dA, dB, out_dtype=out_dtype, **kw)
+    torch.cuda.synchronize()
+    assert sptg.device_error() == 0
+    return C.cpu()
+
+
+def assert_float_parity(C, A, Bcm, rows=None, cols=None):
+    """Element-wise bound against the oracle (full, or at sampled positions)."""
+    it = IN_TYPE[A.dtype]
+    got = C.to(torch.float64).numpy()
+    if rows is None:
+        ref, S = oracle.gemm_float(A, Bcm, it)
+    else:
+        ref, S = oracle.gemm_float_at(A, Bcm, it, rows, cols)
+        got = got[rows, cols]
+    assert np.isfinite(got).all(), "non-finite output"
+    err = np.abs(got - ref)
+    ratio = err / np.maximum(S, np.finfo(np.float64).tiny)
+    worst = float(ratio.max()) if ratio.size else 0.0
+    bad = err > TOL * S
+    assert not bad.any(), (f"{int(bad.sum())} elements outside the bound; "
+                           f"max |err|/S = {worst:.3e}")
+    return worst
+
+
+def assert_int_parity(C, A, Bcm, rows=None, cols=None):
+    got = C.to(torch.int64).numpy()
+    if rows is None:
+        ref = oracle.gemm_s8(A, Bcm)
+    else:
+        ref = oracle.gemm_s8_at(A, Bcm, rows, cols)
+        got = got[rows, cols]
+    mism = got != ref
+    assert not mism.any(), f"{int(mism.sum())} int8 results differ from the oracle"
+
+
+def sample_positions(M, N, n, seed=0):
+    """n positions: the four corners, tile edges, and uniform random ones."""
+    g = np.random.default_rng(seed)
+    fixed_r = [0, 0, M - 1, M - 1, min(127, M - 1), min(128, M - 1)]
+    fixed_c = [0, N - 1, 0, N - 1, min(255, N - 1), min(256, N - 1)]
+    r = np.concatenate([fixed_r, g.integers(0, M, n)])
+    c = np.concatenate([fixed_c, g.integers(0, N, n)])
+    return r.astype(np.int64), c.astype(np.int64)

@@ -1,0 +1,225 @@
+"""GPU parity of the pipelined GEMM against the CPU oracle, through the C ABI.
+
+Covers the five measured workloads (full comparison where the oracle finishes
+in seconds, sampled positions for the 8192 x 8192 x 16384 product), the
+pipeline-structure cases the method's pitfalls name (a dropped, doubled or
+misplaced K-tile; ring wrap and phase flips; the last tile), ragged edges and
+degenerate shapes, and the bounded-wait error path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import software_pipelined_tiled_gb300 as sptg
+from gpu_helpers import (assert_float_parity, assert_int_parity, run, sample_positions)
+from workloads import WORKLOADS, make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+F16, BF16, F32, I8, I32 = torch.float16, torch.bfloat16, torch.float32, torch.int8, torch.int32
+
+
+# ----------------------------------------------------------------- workloads
+def test_workload_f16_256_f32out():
+    w = WORKLOADS["f16_256x256x256_f32out"]
+    A, B = workload_inputs(w)
+    C = run(A, B, F32)
+    assert "kernel=square" in sptg.last_config()
+    assert_float_parity(C, A, B)
+
+
+def test_workload_f16_4096_f16out():
+    w = WORKLOADS["f16_4096x4096x4096_f16out"]
+    A, B = workload_inputs(w)
+    C = run(A, B, F16)
+    assert_float_parity(C, A, B)
+
+
+def test_workload_s8_4096_bit_exact():
+    w = WORKLOADS["s8_4096x4096x4096_s32out"]
+    A, B = workload_inputs(w)
+    C = run(A, B, I32)
+    assert_int_parity(C, A, B)
+
+
+def test_workload_bf16_skinny():
+    w = WORKLOADS["bf16_skinny_64x8192x8192_bf16out"]
+    A, B = workload_inputs(w)
+    C = run(A, B, BF16)
+    assert "kernel=skinny" in sptg.last_config()
+    assert_float_parity(C, A, B)
+
+
+def test_workload_bf16_8192x8192x16384_sampled():
+    w = WORKLOADS["bf16_8192x8192x16384_f32out"]
+    A, B = workload_inputs(w)
+    C = run(A, B, F32)
+    rows, cols = sample_positions(w.M, w.N, 4000, seed=5)
+    assert_float_parity(C, A, B, rows, cols)
+    # a whole row and a whole column as well
+    r = np.full(w.N, 4097, dtype=np.int64)
+    assert_float_parity(C, A, B, r, np.arange(w.N, dtype=np.int64))
+    c = np.full(w.M, 8191, dtype=np.int64)
+    assert_float_parity(C, A, B, np.arange(w.M, dtype=np.int64), c)
+
+
+# ---------------------------------------------------------- pipeline structure
+def _marker_inputs(M, N, T, BK=64, dtype=F16):
+    # A = 1, B[k][j] = floor(k / BK) + 1: C = BK * T (T + 1) / 2 exactly
+    K = BK * T
+    A = torch.ones(M, K, dtype=dtype)
+    Bcm = (torch.arange(K) // BK + 1).to(dtype).repeat(N, 1).contiguous()
+    return A, Bcm, BK * T * (T + 1) // 2
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 9, 17])
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+def test_k_tile_marker_square(T, stages):
+    # K/BK around the ring depth: fewer, equal, one more, wraps twice
+    A, B, expect = _marker_inputs(256, 512, T)
+    C = run(A, B, F16 if stages != 4 else F32, stages=stages, splits=3)
+    assert (C.to(torch.float64) == expect).all()
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 8, 9, 17])
+def test_k_tile_marker_skinny(T):
+    A, B, expect = _marker_inputs(64, 1024, T, dtype=BF16)
+    C = run(A, B, F32, kernel="skinny", splits=24)
+    assert (C.to(torch.float64) == expect).all()
+
+
+def test_only_last_k_tile_nonzero():
+    # a dropped final tile ("Pipeline GPU Kernel", pitfalls) shows up as zeros
+    M, N, K = 128, 256, 64 * 7
+    A = torch.zeros(M, K, dtype=F16)
+    B = torch.zeros(N, K, dtype=F16)
+    A[:, -64:] = 1
+    B[:, -64:] = 0.5
+    C = run(A, B, F32)
+    assert (C == 32.0).all()
+
+
+def test_identity_and_ones():
+    A, _ = make_inputs(256, 1, 256, "f16", "uniform", 3)
+    eye = torch.eye(256, dtype=F16)
+    C = run(A, eye, F32)
+    assert torch.equal(C, A.to(F32))
+    ones = torch.ones(128, 4096, dtype=BF16)
+    C = run(ones, torch.ones(256, 4096, dtype=BF16), F32)
+    assert (C == 4096).all()
+
+
+def test_permutation_selects_columns():
+    A, _ = make_inputs(256, 1, 512, "bf16", "normal", 4)
+    perm = torch.randperm(512, generator=torch.Generator().manual_seed(1))[:384]
+    Bcm = torch.zeros(384, 512, dtype=BF16)
+    Bcm[torch.arange(384), perm] = 1
+    C = run(A, Bcm, BF16)
+    assert torch.equal(C, A[:, perm])
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3])
+def test_stage_count_does_not_change_the_arithmetic(stages):
+    # pipelining reorders loads only ("Pipeline GPU Kernel", Step 5): any
+    # ring depth gives the same bits as the default one
+    A, B = make_inputs(384, 512, 1024, "f16", "uniform", 12)
+    ref = run(A, B, F16)
+    got = run(A, B, F16, stages=stages)
+    assert torch.equal(ref, got)
+
+
+# --------------------------------------------------------- ragged and edges
+@pytest.mark.parametrize("M,N,K,dt,out", [
+    (200, 136, 200, F16, F32),
+    (1, 8, 8, F16, F16),
+    (129, 264, 72, BF16, BF16),
+    (300, 520, 1032, BF16, F32),
+    (77, 4, 4104, F16, F32),
+])
+def test_ragged_shapes(M, N, K, dt, out):
+    A, B = make_inputs(M, N, K, "f16" if dt == F16 else "bf16", "uniform", M + N + K)
+    C = run(A, B, out, kernel="square")
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 2048), (129, 260, 1040), (64, 64, 16)])
+def test_int8_exact_small(M, N, K):
+    A, B = make_inputs(M, N, K, "s8", "int8", 7 + K)
+    C = run(A, B, I32)
+    assert_int_parity(C, A, B)
+
+
+@pytest.mark.parametrize("K", [1024, 1040, 4096])
+def test_int8_extremes_exact(K):
+    # every chunk of 1024 products reaches 2^24 exactly
+    A = torch.full((130, K), -128, dtype=I8)
+    B = torch.full((136, K), -128, dtype=I8)
+    C = run(A, B, I32)
+    assert (C.to(torch.int64) == 16384 * K).all()
+    alt = torch.tensor([-128 if k % 2 == 0 else 127 for k in range(K)], dtype=I8)
+    C = run(alt.repeat(128, 1), (-alt.to(torch.int16)).clamp(-128, 127).to(I8).repeat(128, 1), I32)
+    assert (C.to(torch.int64) == (K // 2) * (-128 * 127) + (K // 2) * (127 * -127)).all()
+
+
+def test_zero_k_gives_zero_and_empty_is_noop():
+    A = torch.zeros(64, 0, dtype=F16).cuda()
+    B = torch.zeros(128, 0, dtype=F16).cuda()
+    C = torch.full((64, 128), 7.0, dtype=F32).cuda()
+    sptg.gemm(A, B, C=C)
+    torch.cuda.synchronize()
+    assert (C == 0).all()
+    E = torch.empty(0, 128, dtype=F32).cuda()
+    sptg.gemm(torch.zeros(0, 16, dtype=F16).cuda(), torch.zeros(128, 16, dtype=F16).cuda(), C=E)
+
+
+# ----------------------------------------------------------------- skinny
+@pytest.mark.parametrize("M,N,K,splits", [
+    (64, 8192, 1024, 0), (1, 1024, 2048, 0), (17, 1000, 1000, 7), (64, 512, 4096, 200),
+    (33, 2048, 520, 5), (64, 256, 64, 3)])
+def test_skinny_split_and_ragged(M, N, K, splits):
+    A, B = make_inputs(M, N, K, "bf16", "normal", M * 7 + K)
+    C = run(A, B, BF16, kernel="skinny", splits=splits)
+    assert_float_parity(C, A, B)
+
+
+def test_skinny_is_deterministic():
+    A, B = make_inputs(64, 4096, 4096, "bf16", "normal", 9)
+    c1 = run(A, B, F32, kernel="skinny")
+    c2 = run(A, B, F32, kernel="skinny")
+    assert torch.equal(c1, c2)
+
+
+def test_skinny_f16_out_and_f32_out():
+    A, B = make_inputs(40, 2048, 2048, "f16", "uniform", 10)
+    assert_float_parity(run(A, B, F16, kernel="skinny"), A, B)
+    assert_float_parity(run(A, B, F32, kernel="skinny"), A, B)
+
+
+# ------------------------------------------------------------ stream / errors
+def test_async_on_a_side_stream():
+    A, B = make_inputs(512, 512, 512, "f16", "uniform", 21)
+    dA, dB = A.cuda(), B.cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        C = sptg.gemm(dA, dB, out_dtype=F32, stream=s)
+    s.synchronize()
+    assert_float_parity(C.cpu(), A, B)
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_bounded_wait_reports_timeout_and_context_survives(kernel):
+    # The producer withholds one K-tile; the consumer's wait runs out after
+    # 100 ms, the kernel tears down, and the host reads SPTG_ERR_TIMEOUT.
+    M = 256 if kernel == 1 else 64
+    A, B = make_inputs(M, 1024, 1024, "bf16", "normal", 30)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty(M, 1024, dtype=BF16, device="cuda")
+    cfg = sptg.Config(kernel, 0, 0, 4, 100, 1)
+    rc = sptg.gemm_raw(M, 1024, 1024, "bf16_bf16", dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
+                       torch.cuda.current_stream().cuda_stream, cfg)
+    assert rc == 0
+    assert sptg.device_error() == -5
+    assert sptg.device_error() == 0  # the word was cleared
+    # the context still works
+    C = run(A, B, BF16, kernel="square" if kernel == 1 else "skinny")
+    assert_float_parity(C, A, B)
