@@ -1,0 +1,416 @@
+"""Benchmark of the software-pipelined tiled GEMM (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--stages S] [--no-e2e]
+
+A step is one GEMM of the workload on one set of inputs already resident in
+device memory. The default workload is the binary16 4096 x 4096 x 4096
+product with a binary16 output; the metric is TFLOPS (TOPS for int8).
+
+L2 policy: the inputs and outputs rotate over several device copies whose
+total size is well above the 129 MB L2, so every step reads its operands from
+HBM, not from what the previous step left in L2.
+
+`value` is timed with CUDA events on the launching stream around exactly K
+steps, between a barrier + synchronize on each side, max over ranks. `e2e`
+is the same metric through the public API from pinned host buffers, the
+host->device copies of A and B and the device->host copy of C inside the
+timed region. `cpu_baseline` is the CPU oracle (fp64 triple loop) timed on the
+host cores on a bounded sample of the same workload.
+
+--impl reference times that oracle as the reference arm on the same
+workload, each step a bounded sample (a block of output rows).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, TORCH_DTYPE, workload_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "f16_4096x4096x4096_f16out"
+L2_BYTES = 129 * 10 ** 6
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def metric_for(w):
+    if w.in_type == "s8":
+        return "int8 GEMM TOPS", "TOPS"
+    return "GEMM TFLOPS", "TFLOPS"
+
+
+def algorithmic_bytes(w):
+    isz = 1 if w.in_type == "s8" else 2
+    osz = {"f32": 4, "s32": 4, "f16": 2, "bf16": 2}[w.out_type]
+    return (w.M * w.K + w.N * w.K) * isz + w.M * w.N * osz
+
+
+def bound_for(w):
+    # arithmetic intensity against the machine balance decides the roof
+    peaks, _ = measured_peaks()
+    balance = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    ai = w.flops / algorithmic_bytes(w)
+    return "tensor" if ai >= balance else "hbm"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        sm_sorted = sorted(sm)
+        # the median over samples taken under load
+        loaded = [x for x in sm_sorted if x > 0.3 * (mx or x)] or sm_sorted
+        return {"sm_mhz": loaded[len(loaded) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "software_pipelined_tiled_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get(f"{kernel}/{workload}")
+        if rec and rec.get("sources") == sources_hash():
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------- CPU oracle leg
+def oracle_sample(w, A, B, target_s: float = 12.0):
+    """Times the CPU oracle on a leading block of output rows (about target_s seconds)."""
+    import oracle
+    it = {"f16": oracle.IN_F16, "bf16": oracle.IN_BF16}.get(w.in_type)
+
+    def run_rows(r):
+        t0 = time.perf_counter()
+        if w.in_type == "s8":
+            oracle.gemm_s8(A[:r], B)
+        else:
+            oracle.gemm_float(A[:r], B, it)
+        return time.perf_counter() - t0
+
+    probe = min(w.M, max(1, 2 * oracle.threads()))
+    run_rows(probe)  # loads the oracle library and warms the caches
+    t = run_rows(probe)
+    rows = int(min(w.M, max(probe, probe * target_s / max(t, 1e-6))))
+    return rows, oracle.threads()
+
+
+def cpu_baseline(w, A, B, target_s: float = 12.0):
+    import oracle
+    rows, cores = oracle_sample(w, A, B, target_s)
+    t0 = time.perf_counter()
+    if w.in_type == "s8":
+        oracle.gemm_s8(A[:rows], B)
+    else:
+        oracle.gemm_float(A[:rows], B, {"f16": oracle.IN_F16, "bf16": oracle.IN_BF16}[w.in_type])
+    dt = time.perf_counter() - t0
+    _, unit = metric_for(w)
+    return {"value": 2.0 * rows * w.N * w.K / dt / 1e12, "unit": unit, "cores": cores,
+            "kind": "oracle",
+            "sample": f"output rows 0..{rows - 1} of {w.M} ({rows}x{w.N}x{w.K}), {dt:.1f} s"}
+
+
+# ------------------------------------------------------------- GPU leg
+def init_dist(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args, w):
+    import software_pipelined_tiled_gb300 as sptg
+
+    rank, world, local = init_dist(args.gpus)
+    sptg.load()
+    metric, unit = metric_for(w)
+    A, B = workload_inputs(w)
+    out_dtype = TORCH_DTYPE[w.out_type]
+    set_bytes = algorithmic_bytes(w)
+    n_sets = max(2, -(-3 * L2_BYTES // set_bytes) + 1)  # total well above L2
+    dev = torch.device("cuda", local)
+    As = [A.to(dev) for _ in range(n_sets)]
+    Bs = [B.to(dev) for _ in range(n_sets)]
+    Cs = [torch.empty(w.M, w.N, dtype=out_dtype, device=dev) for _ in range(n_sets)]
+    cfg = sptg.Config(0, 0, args.stages, 0, 0, 0) if args.stages else None
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        j = i % n_sets
+        sptg.gemm(As[j], Bs[j], C=Cs[j], config=cfg)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if sptg.device_error() != 0:
+        raise RuntimeError("kernel reported a timed-out wait during warm-up")
+    launches_per_step = int(sptg.last_config().split("launches=")[-1].split()[0])
+    kernel_name = sptg.last_config().split()[0].split("=")[1]
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if rank == 0:
+        sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, world)
+    ms_per_step = ms / args.steps
+    value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+    if sptg.device_error() != 0:
+        raise RuntimeError("kernel reported a timed-out wait in the timed region")
+
+    # ---- end to end through the public API from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        hA, hB = A.pin_memory(), B.pin_memory()
+        hC = torch.empty(w.M, w.N, dtype=out_dtype).pin_memory()
+        dA, dB, dC = As[0], Bs[0], Cs[0]
+        e2e_steps = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            sptg.gemm(dA, dB, C=dC, config=cfg)
+            hC.copy_(dC, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+        isz = A.element_size()
+        e2e = {"value": world * w.flops / (e_ms * 1e-3) / 1e12, "unit": unit,
+               "h2d_bytes_per_step": (A.numel() + B.numel()) * isz,
+               "d2h_bytes_per_step": hC.numel() * hC.element_size(),
+               "ms_per_step": e_ms}
+
+    if rank != 0:
+        return None
+
+    peaks, peak_src = measured_peaks()
+    bound = bound_for(w)
+    # the timed region runs the kernel back to back; over a second the sustained
+    # figure is the matching denominator, else the burst one
+    sustained = ms > 1000.0
+    if bound == "tensor":
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        achieved = w.flops / (ms_per_step * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_source": f"{peak_src} bf16 {'sustained' if sustained else 'burst'} "
+                               f"(binary16 runs at the bfloat16 rate)"}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = set_bytes / (ms_per_step * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth"}
+    roof["traffic"] = recorded_traffic(kernel_name, w.name)
+    roof["algorithmic_bytes"] = set_bytes
+    roof["kernel"] = kernel_name
+
+    cpu = None if args.no_cpu_baseline else cpu_baseline(w, A, B)
+    clocks = sampler.summary()
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.in_type, "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype_pair": w.dtype,
+                   "distribution": w.dist, "seed": w.seed, "kernel": sptg.last_config(),
+                   "l2": f"{n_sets} rotating input/output sets of {set_bytes / 2**20:.0f} MiB "
+                         f"(> L2)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+    }
+    return line
+
+
+def run_reference(args, w):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return None
+    import oracle
+    metric, unit = metric_for(w)
+    A, B = workload_inputs(w)
+    total_budget = 150.0  # seconds for warm-up + timed steps together
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    rows, cores = oracle_sample(w, A, B, target_s=min(12.0, per_step))
+    it = {"f16": oracle.IN_F16, "bf16": oracle.IN_BF16}.get(w.in_type)
+
+    def step():
+        if w.in_type == "s8":
+            oracle.gemm_s8(A[:rows], B)
+        else:
+            oracle.gemm_float(A[:rows], B, it)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 2.0 * rows * w.N * w.K / dt / 1e12
+    sample = f"each step: output rows 0..{rows - 1} of {w.M} ({rows}x{w.N}x{w.K})"
+    return {
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.in_type,
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype_pair": w.dtype,
+                   "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--stages", type=int, default=0, help="force the ring depth (ablation)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    w = WORKLOADS[args.workload]
+    line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if args.impl == "ours" and int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

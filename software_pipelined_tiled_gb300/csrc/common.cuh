@@ -26,6 +26,7 @@ enum WaitSite : unsigned int {
   WAIT_MMA_TMEM_EMPTY = 1u << 2,
   WAIT_EPI_TMEM_FULL = 1u << 3,
   WAIT_DRAIN = 1u << 4,
+  WAIT_PLAN = 1u << 5,  // not a wait: a launch whose scratch plan does not fit
 };
 
 // Everything a bounded wait needs: the limit, where to report, and the

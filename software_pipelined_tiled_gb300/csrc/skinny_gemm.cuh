@@ -250,6 +250,9 @@ __global__ void __launch_bounds__(192, 1)
           for (int m = 0; m < MN; ++m)
             if (m < M) store_out<OUT>(p.C, static_cast<int64_t>(m) * p.N + n, acc[m]);
         }
+      } else if (p.partials == nullptr || count > p.max_contrib) {
+        // the host planned no room for this split: report instead of writing
+        if (threadIdx.x == 64) atomicOr(p.error_word, WAIT_PLAN);
       } else {
         const int j = static_cast<int>(blockIdx.x) - c_first;
         float* slot = p.partials + (static_cast<int64_t>(nt) * p.max_contrib + j) * (MN * BNT);

@@ -32,6 +32,7 @@ using namespace sptg;
 
 thread_local std::string t_last_error;
 thread_local std::string t_last_config;
+thread_local int t_launches = 0;  // kernels this library launched in the current call
 
 void set_config_text(const char* fmt, ...) {
   char buf[512];
@@ -40,6 +41,7 @@ void set_config_text(const char* fmt, ...) {
   vsnprintf(buf, sizeof(buf), fmt, ap);
   va_end(ap);
   t_last_config = buf;
+  t_last_config += " launches=" + std::to_string(t_launches);
 }
 
 int cuda_fail(cudaError_t e, const char* what) {
@@ -298,6 +300,7 @@ int run_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   const int grid = std::min(tiles, cfg.splits > 0 ? cfg.splits : di.sm_count);
   v.fn<<<grid, 192, v.smem, stream>>>(ta, tb, tc, p);
+  ++t_launches;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "square_gemm launch");
   set_config_text(
@@ -389,7 +392,10 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
 
   // Scratch: fp32 partial tiles [n_tile][contributor][MN x 128] then one
   // arrival counter per n-tile (zeroed here, and re-zeroed by the last arrival).
-  const bool split = grid > p.num_n_tiles;
+  // Partials are needed as soon as one CTA boundary falls inside an n-tile.
+  bool split = false;
+  for (int c = 1; c < grid && !split; ++c)
+    split = ((static_cast<int64_t>(c) * units / grid) % p.num_k_tiles) != 0;
   size_t partial_bytes = 0, counter_bytes = 0;
   if (split) {
     partial_bytes = static_cast<size_t>(p.num_n_tiles) * max_contrib * v.mn * BNT * sizeof(float);
@@ -406,6 +412,7 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
     p.counters = nullptr;
   }
   v.fn<<<grid, 192, v.smem, stream>>>(tb, ta, p);
+  ++t_launches;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "skinny_gemm launch");
   set_config_text(
@@ -474,6 +481,7 @@ int sptg_device_error(void* stream) {
 
 int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B,
                  void* C, void* stream, const sptg_config* cfg_in) {
+  t_launches = 0;
   sptg_config cfg;
   memset(&cfg, 0, sizeof(cfg));
   if (cfg_in) cfg = *cfg_in;
@@ -539,6 +547,7 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
                                                      static_cast<uint4*>(A16), na);
     s8_to_f16_kernel<<<blocks_b, 256, 0, stream_h>>>(static_cast<const int4*>(B),
                                                      static_cast<uint4*>(B16), nb);
+    t_launches += 2;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "s8_to_f16 launch");
     return run_square(dev, di, d, M, N, K, A16, B16, C, stream_h, cfg);
