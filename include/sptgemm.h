@@ -108,6 +108,40 @@ int sptg_last_config(char* buf, size_t len);
  * (or SPTG_ERR_LAUNCH if synchronization itself failed). */
 int sptg_device_error(void* stream);
 
+/*
+ * Allocation-free variant of the skinny (M <= 64) kernel.
+ *
+ * This call has no counterpart in the paper. It exists for callers that
+ * cannot let a library allocate device memory: a serving process that reserves the GPU's
+ * memory for its own pool up front (a library cudaMalloc would then fail or
+ * fragment that pool), and latency-critical code that cannot accept the
+ * device-wide synchronisation a cudaMalloc or cudaFree may imply.
+ *
+ * It computes exactly what sptg_gemm computes for the same arguments, with
+ * the same kernel, but keeps its split-K partial sums and arrival counters in
+ * one fixed array compiled into the library (SPTG_NOALLOC_PARTIAL_BYTES +
+ * SPTG_NOALLOC_COUNTER_BYTES of device memory, held on every GPU that loads
+ * the library until the process exits). It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *
+ *  - dtype: the float pairs only (not SPTG_S8_S32), and M <= 64; otherwise
+ *    SPTG_ERR_CONFIG. A, B, C, stream, alignment and return codes as for
+ *    sptg_gemm.
+ *  - A shape whose split needs more partial-tile bytes (column tiles of 128 x
+ *    contributing CTAs x 32 KiB) or counter bytes than the fixed array holds
+ *    is rejected with SPTG_ERR_CONFIG; sptg_last_error() gives the sizes.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call uses the same array and clears the counters it needs at its
+ *    start; the array keeps the last call's partial sums. Calls whose kernels
+ *    overlap on the GPU (two streams, or two threads) race on it: serialise
+ *    them.
+ */
+#define SPTG_NOALLOC_PARTIAL_BYTES (8u << 20)
+#define SPTG_NOALLOC_COUNTER_BYTES (64u << 10)
+int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype,
+                             const void* A, const void* B, void* C, void* stream);
+
 /* Library ABI version (major*100 + minor). */
 int sptg_version(void);
 

@@ -19,7 +19,8 @@ import threading
 
 from ._build import LIB_PATH, build
 
-__all__ = ["DTYPES", "SptgError", "Config", "load", "gemm", "gemm_raw", "last_config",
+__all__ = ["DTYPES", "SptgError", "Config", "load", "gemm", "gemm_raw", "gemm_skinny_noalloc_raw",
+           "last_config",
            "last_error", "device_error", "status_string", "LIB_PATH", "build"]
 
 # sptg_dtype values of include/sptgemm.h
@@ -31,7 +32,7 @@ KERNELS = {"auto": 0, "square": 1, "skinny": 2}
 
 # the C functions every build must export (checked by the tests)
 EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_status_string", "sptg_last_error",
-           "sptg_last_config", "sptg_device_error", "sptg_version")
+           "sptg_last_config", "sptg_device_error", "sptg_version", "sptg_gemm_skinny_noalloc")
 
 
 class SptgError(RuntimeError):
@@ -75,6 +76,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sptg_last_config.restype = ctypes.c_int
         lib.sptg_device_error.argtypes = [vp]
         lib.sptg_device_error.restype = ctypes.c_int
+        lib.sptg_gemm_skinny_noalloc.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
+        lib.sptg_gemm_skinny_noalloc.restype = ctypes.c_int
         lib.sptg_version.argtypes = []
         lib.sptg_version.restype = ctypes.c_int
         if path is None:
@@ -112,6 +115,15 @@ def gemm_raw(M: int, N: int, K: int, dtype: str | int, A_ptr: int, B_ptr: int, C
     d = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
     cfg = ctypes.byref(config) if config is not None else None
     return int(load().sptg_gemm_ex(M, N, K, d, A_ptr, B_ptr, C_ptr, stream, cfg))
+
+
+def gemm_skinny_noalloc_raw(M: int, N: int, K: int, dtype: str | int, A_ptr: int, B_ptr: int,
+                            C_ptr: int, stream: int = 0) -> int:
+    """Calls sptg_gemm_skinny_noalloc (the skinny kernel with its split-K
+    scratch in a fixed array inside the library, so the call allocates
+    nothing); returns the status code."""
+    d = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    return int(load().sptg_gemm_skinny_noalloc(M, N, K, d, A_ptr, B_ptr, C_ptr, stream))
 
 
 def _dtype_key(in_dtype, out_dtype) -> str:

@@ -350,9 +350,19 @@ bool pick_skinny(const DtypeInfo& d, int stages_req, SkinnyVariant& v) {
 #undef SPTG_SKINNY_CASES
 }
 
+// Caller-provided scratch for the skinny kernel's split-K partials and
+// arrival counters (used by sptg_gemm_skinny_noalloc); null = the cached
+// per-stream scratch of scratch_for().
+struct FixedScratch {
+  void* partials;
+  size_t partial_bytes;
+  void* counters;
+  size_t counter_bytes;
+};
+
 int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N, int64_t K,
                const void* A, const void* B, void* C, cudaStream_t stream,
-               const sptg_config& cfg) {
+               const sptg_config& cfg, const FixedScratch* fixed = nullptr) {
   SkinnyVariant v;
   if (!pick_skinny(d, cfg.stages, v) || M > v.mn) {
     t_last_error = "no skinny-kernel variant for the requested dtype/stages/M";
@@ -400,11 +410,25 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   if (split) {
     partial_bytes = static_cast<size_t>(p.num_n_tiles) * max_contrib * v.mn * BNT * sizeof(float);
     counter_bytes = static_cast<size_t>(p.num_n_tiles) * sizeof(unsigned int);
-    void* ws = nullptr;
-    rc = scratch_for(dev, stream, partial_bytes + counter_bytes + 256, &ws);
-    if (rc) return rc;
-    p.partials = static_cast<float*>(ws);
-    p.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + partial_bytes);
+    if (fixed) {
+      if (partial_bytes > fixed->partial_bytes || counter_bytes > fixed->counter_bytes) {
+        char b[200];
+        snprintf(b, sizeof(b),
+                 "shape needs %zu bytes of split-K partials and %zu of counters; the fixed "
+                 "scratch holds %zu and %zu",
+                 partial_bytes, counter_bytes, fixed->partial_bytes, fixed->counter_bytes);
+        t_last_error = b;
+        return SPTG_ERR_CONFIG;
+      }
+      p.partials = static_cast<float*>(fixed->partials);
+      p.counters = static_cast<unsigned int*>(fixed->counters);
+    } else {
+      void* ws = nullptr;
+      rc = scratch_for(dev, stream, partial_bytes + counter_bytes + 256, &ws);
+      if (rc) return rc;
+      p.partials = static_cast<float*>(ws);
+      p.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + partial_bytes);
+    }
     cudaError_t e = cudaMemsetAsync(p.counters, 0, counter_bytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   } else {
@@ -424,6 +448,37 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------ allocation-free entry
+// Fixed device scratch of sptg_gemm_skinny_noalloc: split-K partial tiles
+// followed by the per-n-tile arrival counters. Every device that loads the
+// library holds it until the process exits.
+constexpr size_t kNoAllocPartialBytes = SPTG_NOALLOC_PARTIAL_BYTES;
+constexpr size_t kNoAllocCounterBytes = SPTG_NOALLOC_COUNTER_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocPartialBytes +
+                                                                 kNoAllocCounterBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current. In host code the array's name is only a host-side stand-in.
+std::map<int, unsigned char*> g_noalloc_addr;
+
+int noalloc_scratch(int dev, unsigned char** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_noalloc_addr.find(dev);
+  if (it != g_noalloc_addr.end()) {
+    *out = it->second;
+    return SPTG_OK;
+  }
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    t_last_error = std::string("cudaGetSymbolAddress(noalloc scratch): ") + cudaGetErrorString(e);
+    return SPTG_ERR_LAUNCH;
+  }
+  g_noalloc_addr[dev] = static_cast<unsigned char*>(p);
+  *out = static_cast<unsigned char*>(p);
+  return SPTG_OK;
+}
 
 }  // namespace
 
@@ -558,6 +613,56 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
 int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B, void* C,
               void* stream) {
   return sptg_gemm_ex(M, N, K, dtype, A, B, C, stream, nullptr);
+}
+
+int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype, const void* A,
+                             const void* B, void* C, void* stream) {
+  t_launches = 0;
+  DtypeInfo d;
+  if (!dtype_info(dtype, d)) {
+    t_last_error = "unknown dtype";
+    return SPTG_ERR_ARG;
+  }
+  if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) {
+    t_last_error = "dimensions must be in [0, 2^31)";
+    return SPTG_ERR_ARG;
+  }
+  if (d.is_int8 || M > 64) {
+    t_last_error = "the allocation-free entry covers float dtypes with M <= 64 only";
+    return SPTG_ERR_CONFIG;
+  }
+  if (M == 0 || N == 0) {
+    set_config_text("kernel=none dtype=%s (empty output)", d.name);
+    return SPTG_OK;
+  }
+  if (!C || (K > 0 && (!A || !B))) {
+    t_last_error = "null pointer";
+    return SPTG_ERR_ARG;
+  }
+  if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))) ||
+      (K * d.in_bytes) % 16 != 0 || (N * d.out_bytes) % 16 != 0) {
+    t_last_error = "TMA needs 16-byte aligned bases and row pitches";
+    return SPTG_ERR_ALIGN;
+  }
+  int dev = 0;
+  DeviceInfo di;
+  int rc = device_info(di, dev);
+  if (rc) return rc;
+  cudaStream_t stream_h = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    cudaError_t e = cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * d.out_bytes, stream_h);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    set_config_text("kernel=zero-fill dtype=%s", d.name);
+    return SPTG_OK;
+  }
+  unsigned char* base = nullptr;
+  rc = noalloc_scratch(dev, &base);
+  if (rc) return rc;
+  const FixedScratch fixed{base, kNoAllocPartialBytes, base + kNoAllocPartialBytes,
+                           kNoAllocCounterBytes};
+  sptg_config cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  return run_skinny(dev, di, d, M, N, K, A, B, C, stream_h, cfg, &fixed);
 }
 
 }  // extern "C"
