@@ -132,10 +132,12 @@ int sptg_device_error(void* stream);
  *    is rejected with SPTG_ERR_CONFIG; sptg_last_error() gives the sizes.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
- *  - Every call uses the same array and clears the counters it needs at its
- *    start; the array keeps the last call's partial sums. Calls whose kernels
- *    overlap on the GPU (two streams, or two threads) race on it: serialise
- *    them.
+ *  - Every call uses the same array, which keeps the last call's partial
+ *    sums and counters. Each call tags the counters it uses with a new call
+ *    number, so whatever an earlier call left there (even one whose kernel
+ *    gave up a wait) is never taken for this call's. Calls whose kernels
+ *    overlap on the GPU (two streams, or two threads) race on the array:
+ *    serialise them.
  */
 #define SPTG_NOALLOC_PARTIAL_BYTES (8u << 20)
 #define SPTG_NOALLOC_COUNTER_BYTES (64u << 10)

@@ -36,7 +36,8 @@ struct SkinnyParams {
   int max_contrib;            // partial slots per n-tile
   void* C;                    // row-major M x N output
   float* partials;            // [n_tile][max_contrib][MN][128] fp32, or null if unsplit
-  unsigned int* counters;     // [n_tile] arrival counters, zero between calls
+  unsigned long long* counters;  // [n_tile] (generation << 32 | arrivals)
+  unsigned int generation;    // this call's tag for the counters, never 0
   unsigned int* error_word;
   uint64_t timeout_ns;
   int inject_stall;
@@ -73,6 +74,38 @@ __device__ __forceinline__ void store_out(void* C, int64_t idx, float v) {
   } else {
     static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
   }
+}
+
+// Four consecutive outputs; idx is a multiple of 4 and the row pitch keeps
+// the group inside one row (N is a multiple of 4 for every output type).
+template <int OUT>
+__device__ __forceinline__ void store_out4(void* C, int64_t idx, float4 v) {
+  if constexpr (OUT == OUT_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(C) + idx) = v;
+  } else {
+    uint2 w = make_uint2(pack2<OUT>(v.x, v.y), pack2<OUT>(v.z, v.w));
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(C) + idx) = w;
+  }
+}
+
+// Counts one arrival at an n-tile's counter and returns whether it was the
+// last of `count`. The 64-bit counter holds (call generation << 32 | arrivals):
+// a value left by an earlier call (or by one that gave up) carries another
+// generation and is replaced, so no call has to clear the counters first.
+// The compare-and-swap retries only when another contributor got in first.
+__device__ __forceinline__ int arrive_generation(unsigned long long* ctr, unsigned int gen,
+                                                 int count, unsigned int* error_word) {
+  unsigned long long cur = atomicAdd(ctr, 0ull);
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    const unsigned long long base =
+        (static_cast<unsigned int>(cur >> 32) == gen) ? cur : (static_cast<unsigned long long>(gen) << 32);
+    const unsigned long long want = base + 1;
+    const unsigned long long prev = atomicCAS(ctr, cur, want);
+    if (prev == cur) return static_cast<int>(want & 0xffffffffull) == count;
+    cur = prev;
+  }
+  atomicOr(error_word, WAIT_PLAN);
+  return 0;
 }
 
 template <int MN, int STAGES, bool IN_BF16, int OUT>
@@ -260,22 +293,40 @@ __global__ void __launch_bounds__(192, 1)
         for (int m = 0; m < MN; ++m) __stcg(slot + m * BNT + n_local, acc[m]);
         __threadfence();
         named_barrier_sync(1, 128);
-        if (threadIdx.x == 64) {
-          const unsigned int prev = atomicAdd(p.counters + nt, 1u);
-          const int last = (prev == static_cast<unsigned int>(count - 1));
-          if (last) p.counters[nt] = 0;  // ready for the next call
-          *last_flag = last;
-        }
+        if (threadIdx.x == 64) *last_flag = arrive_generation(p.counters + nt, p.generation, count,
+                                                              p.error_word);
         named_barrier_sync(1, 128);
         if (*last_flag) {
+          // Sum the partial tiles in contributor order (increasing k), 16-byte
+          // loads with every contributor's loads in flight together.
           __threadfence();
-          const float* base = p.partials + static_cast<int64_t>(nt) * p.max_contrib * (MN * BNT);
-          if (n < p.N) {
-            for (int m = 0; m < M && m < MN; ++m) {
-              float s = __ldcg(base + m * BNT + n_local);
-              for (int jj = 1; jj < count; ++jj) s += __ldcg(base + jj * (MN * BNT) + m * BNT + n_local);
-              store_out<OUT>(p.C, static_cast<int64_t>(m) * p.N + n, s);
+          constexpr int F4_PER_ROW = BNT / 4;
+          constexpr int PER_THREAD = MN * F4_PER_ROW / 128;
+          const int tid = threadIdx.x - 64;
+          const float4* base = reinterpret_cast<const float4*>(
+              p.partials + static_cast<int64_t>(nt) * p.max_contrib * (MN * BNT));
+          float4 sum[PER_THREAD];
+#pragma unroll
+          for (int i = 0; i < PER_THREAD; ++i) sum[i] = __ldcg(base + tid + 128 * i);
+          for (int jj = 1; jj < count; ++jj) {
+            const float4* pj = base + static_cast<int64_t>(jj) * (MN * BNT / 4);
+            float4 v[PER_THREAD];
+#pragma unroll
+            for (int i = 0; i < PER_THREAD; ++i) v[i] = __ldcg(pj + tid + 128 * i);
+#pragma unroll
+            for (int i = 0; i < PER_THREAD; ++i) {
+              sum[i].x += v[i].x;
+              sum[i].y += v[i].y;
+              sum[i].z += v[i].z;
+              sum[i].w += v[i].w;
             }
+          }
+#pragma unroll
+          for (int i = 0; i < PER_THREAD; ++i) {
+            const int f = tid + 128 * i;
+            const int m = f / F4_PER_ROW;
+            const int n0 = nt * BNT + 4 * (f % F4_PER_ROW);
+            if (m < M && n0 < p.N) store_out4<OUT>(p.C, static_cast<int64_t>(m) * p.N + n0, sum[i]);
           }
         }
         named_barrier_sync(1, 128);  // last_flag is reused by the next segment

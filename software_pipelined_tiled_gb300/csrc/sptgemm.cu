@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -125,16 +126,30 @@ int ensure_smem(int dev, const void* kernel, int bytes) {
 }
 
 // ------------------------------------------------------------ scratch space
-// One stream-ordered scratch area per (device, stream), grown on demand.
+// One stream-ordered scratch area per (device, stream), grown on demand. Its
+// first kCounterArea bytes hold the skinny kernel's split-K arrival counters
+// (zeroed whenever the area is (re)allocated, never used by anything else);
+// the rest holds a call's data (int8 operands widened to binary16, or split-K
+// partial tiles).
+constexpr size_t kCounterArea = static_cast<size_t>(1) << 16;
+
 struct Scratch {
   void* ptr = nullptr;
   size_t bytes = 0;
+  unsigned int generation = 0;  // tag of the last call that used the counters
 };
 std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
 
-int scratch_for(int dev, cudaStream_t stream, size_t need, void** out) {
+struct ScratchView {
+  void* data;
+  unsigned long long* counters;
+  unsigned int generation;  // a new non-zero tag for this call's counters
+};
+
+int scratch_for(int dev, cudaStream_t stream, size_t data_bytes, ScratchView* out) {
   std::lock_guard<std::mutex> lk(g_mu);
   Scratch& s = g_scratch[{dev, stream}];
+  const size_t need = kCounterArea + data_bytes;
   if (s.bytes < need) {
     if (s.ptr) cudaFreeAsync(s.ptr, stream);
     s.ptr = nullptr;
@@ -146,15 +161,21 @@ int scratch_for(int dev, cudaStream_t stream, size_t need, void** out) {
       t_last_error = std::string("cudaMallocAsync: ") + cudaGetErrorString(e);
       return SPTG_ERR_NOMEM;
     }
+    e = cudaMemsetAsync(s.ptr, 0, kCounterArea, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     s.bytes = grow;
   }
-  *out = s.ptr;
+  s.generation = s.generation + 1 ? s.generation + 1 : 1;
+  out->counters = static_cast<unsigned long long*>(s.ptr);
+  out->data = static_cast<char*>(s.ptr) + kCounterArea;
+  out->generation = s.generation;
   return SPTG_OK;
 }
 
 // ------------------------------------------------------------ tensor maps
 int make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
-                uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+                uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tensor_map_encoder();
   if (!enc) {
     t_last_error = "cuTensorMapEncodeTiled is not available from the driver";
@@ -165,7 +186,7 @@ int make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void*
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char b[160];
@@ -227,42 +248,82 @@ SquareVariant square_variant() {
           SquareLayout<BN, ST, IE>::SMEM_BYTES};
 }
 
-// Ring depth choices per dtype: the deepest ring that fits next to the
-// epilogue staging (4 stages of 48 KiB at BN = 256) plus the shallower ones
-// for the pipelining ablation (1 = synchronous load then compute).
-bool pick_square(const DtypeInfo& d, int stages_req, int bn_req, SquareVariant& v) {
-  const int st = stages_req;
-  if (d.is_int8) {
-    if (bn_req && bn_req != 128) return false;
-    switch (st ? st : 6) {
-      case 6: v = square_variant<128, 6, false, OUT_S32, true>(); return true;
-      default: return false;
-    }
-  }
-  if (bn_req && bn_req != 256) return false;
-  const int s = st ? st : 4;
-  switch (d.out_kind) {
-    case OUT_F16:
-      switch (s) {
-        case 1: v = square_variant<256, 1, false, OUT_F16, false>(); return true;
-        case 2: v = square_variant<256, 2, false, OUT_F16, false>(); return true;
-        case 3: v = square_variant<256, 3, false, OUT_F16, false>(); return true;
-        case 4: v = square_variant<256, 4, false, OUT_F16, false>(); return true;
-        default: return false;
-      }
-    case OUT_BF16:
-      if (s != 4) return false;
-      v = square_variant<256, 4, true, OUT_BF16, false>();
-      return true;
-    case OUT_F32:
-      if (s != 4) return false;
-      if (d.in_bf16)
-        v = square_variant<256, 4, true, OUT_F32, false>();
-      else
-        v = square_variant<256, 4, false, OUT_F32, false>();
-      return true;
+// The square-kernel variants compiled into the library: for every float
+// dtype pair the tile widths BN in {256, 224, 192, 160, 128} at the deepest
+// ring that fits (square_max_stages); for binary16 -> binary16 at BN 256 and
+// 224 also the shallower rings 1-3 (1 = load, then compute, no overlap) for
+// the pipelining ablation; int8 (exact mode) at BN 128.
+template <bool BF, int OUT>
+bool square_float_variant(int bn, int stages, SquareVariant& v) {
+#define SPTG_SQ(BNV)                                                           \
+  case BNV:                                                                    \
+    if (stages == 0 || stages == square_max_stages<BNV>()) {                   \
+      v = square_variant<BNV, square_max_stages<BNV>(), BF, OUT, false>();     \
+      return true;                                                             \
+    }                                                                          \
+    break;
+  switch (bn) {
+    SPTG_SQ(256)
+    SPTG_SQ(224)
+    SPTG_SQ(192)
+    SPTG_SQ(160)
+    SPTG_SQ(128)
     default:
       return false;
+  }
+#undef SPTG_SQ
+  if constexpr (!BF && OUT == OUT_F16) {
+    if (bn == 256 && stages >= 1 && stages <= 3) {
+      v = stages == 1 ? square_variant<256, 1, false, OUT_F16, false>()
+                      : stages == 2 ? square_variant<256, 2, false, OUT_F16, false>()
+                                    : square_variant<256, 3, false, OUT_F16, false>();
+      return true;
+    }
+    if (bn == 224 && stages >= 1 && stages <= 3) {
+      v = stages == 1 ? square_variant<224, 1, false, OUT_F16, false>()
+                      : stages == 2 ? square_variant<224, 2, false, OUT_F16, false>()
+                                    : square_variant<224, 3, false, OUT_F16, false>();
+      return true;
+    }
+  }
+  return false;
+}
+
+// Tile width against wave quantisation: the persistent grid runs
+// ceil(tiles / SMs) rounds of 128 x BN tiles, and a tile costs about
+// BN + 64 column-units (the 64 stands for the A-operand traffic every tile
+// carries whatever its width). The cheapest estimate wins; ties keep the
+// wider tile.
+int choose_square_bn(int64_t M, int64_t N, int sm_count) {
+  static const int cands[] = {256, 224, 192, 160, 128};
+  int best = 256;
+  int64_t best_cost = INT64_MAX;
+  const int64_t mt = (M + 127) / 128;
+  for (int bn : cands) {
+    const int64_t tiles = mt * ((N + bn - 1) / bn);
+    const int64_t rounds = (tiles + sm_count - 1) / sm_count;
+    const int64_t cost = rounds * (bn + 64);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+bool pick_square(const DtypeInfo& d, int stages_req, int bn, SquareVariant& v) {
+  if (d.is_int8) {
+    if (bn != 128 || (stages_req && stages_req != 6)) return false;
+    v = square_variant<128, 6, false, OUT_S32, true>();
+    return true;
+  }
+  switch (d.out_kind) {
+    case OUT_F16: return square_float_variant<false, OUT_F16>(bn, stages_req, v);
+    case OUT_BF16: return d.in_bf16 && square_float_variant<true, OUT_BF16>(bn, stages_req, v);
+    case OUT_F32:
+      return d.in_bf16 ? square_float_variant<true, OUT_F32>(bn, stages_req, v)
+                       : square_float_variant<false, OUT_F32>(bn, stages_req, v);
+    default: return false;
   }
 }
 
@@ -270,7 +331,8 @@ int run_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
                const void* A16, const void* B16, void* C, cudaStream_t stream,
                const sptg_config& cfg) {
   SquareVariant v;
-  if (!pick_square(d, cfg.stages, cfg.bn, v)) {
+  const int bn = cfg.bn ? cfg.bn : (d.is_int8 ? 128 : choose_square_bn(M, N, di.sm_count));
+  if (!pick_square(d, cfg.stages, bn, v)) {
     t_last_error = "no square-kernel variant for the requested stages/bn";
     return SPTG_ERR_CONFIG;
   }
@@ -280,7 +342,10 @@ int run_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   if (rc) return rc;
   rc = make_map_2d(&tb, d.in_tma, 2, B16, K, N, BK, v.bn);
   if (rc) return rc;
-  rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, 128 / d.out_bytes, 32);
+  // C blocks of 32 columns x 32 rows: 128-byte rows for 4-byte outputs,
+  // 64-byte rows for 16-bit ones (matching the kernel's staging swizzle)
+  rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, 32, 32,
+                   d.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
   rc = ensure_smem(dev, reinterpret_cast<const void*>(v.fn), v.smem);
   if (rc) return rc;
@@ -358,7 +423,15 @@ struct FixedScratch {
   size_t partial_bytes;
   void* counters;
   size_t counter_bytes;
+  std::atomic<unsigned int>* generation;
 };
+
+// Next non-zero call generation of a scratch area.
+unsigned int next_generation(std::atomic<unsigned int>* g) {
+  unsigned int v = g->fetch_add(1) + 1;
+  if (v == 0) v = g->fetch_add(1) + 1;
+  return v;
+}
 
 int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N, int64_t K,
                const void* A, const void* B, void* C, cudaStream_t stream,
@@ -409,7 +482,7 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   size_t partial_bytes = 0, counter_bytes = 0;
   if (split) {
     partial_bytes = static_cast<size_t>(p.num_n_tiles) * max_contrib * v.mn * BNT * sizeof(float);
-    counter_bytes = static_cast<size_t>(p.num_n_tiles) * sizeof(unsigned int);
+    counter_bytes = static_cast<size_t>(p.num_n_tiles) * sizeof(unsigned long long);
     if (fixed) {
       if (partial_bytes > fixed->partial_bytes || counter_bytes > fixed->counter_bytes) {
         char b[200];
@@ -421,19 +494,24 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
         return SPTG_ERR_CONFIG;
       }
       p.partials = static_cast<float*>(fixed->partials);
-      p.counters = static_cast<unsigned int*>(fixed->counters);
+      p.counters = static_cast<unsigned long long*>(fixed->counters);
+      p.generation = next_generation(fixed->generation);
     } else {
-      void* ws = nullptr;
-      rc = scratch_for(dev, stream, partial_bytes + counter_bytes + 256, &ws);
+      if (counter_bytes > kCounterArea) {
+        t_last_error = "too many column tiles for the split-K counter area";
+        return SPTG_ERR_CONFIG;
+      }
+      ScratchView ws;
+      rc = scratch_for(dev, stream, partial_bytes, &ws);
       if (rc) return rc;
-      p.partials = static_cast<float*>(ws);
-      p.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + partial_bytes);
+      p.partials = static_cast<float*>(ws.data);
+      p.counters = ws.counters;
+      p.generation = ws.generation;
     }
-    cudaError_t e = cudaMemsetAsync(p.counters, 0, counter_bytes, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   } else {
     p.partials = nullptr;
     p.counters = nullptr;
+    p.generation = 0;
   }
   v.fn<<<grid, 192, v.smem, stream>>>(tb, ta, p);
   ++t_launches;
@@ -461,6 +539,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocPartial
 // Device address of g_noalloc_scratch, looked up once per device with that
 // device current. In host code the array's name is only a host-side stand-in.
 std::map<int, unsigned char*> g_noalloc_addr;
+std::atomic<unsigned int> g_noalloc_generation{0};
 
 int noalloc_scratch(int dev, unsigned char** out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -590,11 +669,11 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
     // Widen both operands to binary16 in scratch, then run the exact path.
     const size_t a_bytes = static_cast<size_t>(M) * K * 2, b_bytes = static_cast<size_t>(N) * K * 2;
     const size_t a_pad = (a_bytes + 255) & ~static_cast<size_t>(255);
-    void* ws = nullptr;
+    ScratchView ws;
     rc = scratch_for(dev, stream_h, a_pad + b_bytes, &ws);
     if (rc) return rc;
-    void* A16 = ws;
-    void* B16 = static_cast<char*>(ws) + a_pad;
+    void* A16 = ws.data;
+    void* B16 = static_cast<char*>(ws.data) + a_pad;
     const int64_t na = M * K / 16, nb = N * K / 16;
     const int blocks_a = static_cast<int>(std::min<int64_t>((na + 255) / 256, 8 * di.sm_count));
     const int blocks_b = static_cast<int>(std::min<int64_t>((nb + 255) / 256, 8 * di.sm_count));
@@ -659,7 +738,7 @@ int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype, const v
   rc = noalloc_scratch(dev, &base);
   if (rc) return rc;
   const FixedScratch fixed{base, kNoAllocPartialBytes, base + kNoAllocPartialBytes,
-                           kNoAllocCounterBytes};
+                           kNoAllocCounterBytes, &g_noalloc_generation};
   sptg_config cfg;
   memset(&cfg, 0, sizeof(cfg));
   return run_skinny(dev, di, d, M, N, K, A, B, C, stream_h, cfg, &fixed);

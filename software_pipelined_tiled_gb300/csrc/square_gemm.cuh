@@ -76,8 +76,16 @@ struct SquareLayout {
                                                         : 512;
   static_assert(TMEM_NEEDED <= 512, "accumulators exceed tensor memory");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
+  static_assert(STAGES >= 1, "at least one stage");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 };
+
+// Deepest ring that fits the 227 KB per-CTA budget next to the epilogue
+// staging (32 KB), the barriers and the 1 KB alignment slack.
+template <int BN>
+constexpr int square_max_stages() {
+  return (232448 - 1024 - 4 * 2 * 32 * 128 - 256) / (128 * 64 * 2 + BN * 64 * 2);
+}
 
 template <int BN, int STAGES, bool IN_BF16, int OUT, bool INT_EXACT>
 __global__ void __launch_bounds__(192, 1)
@@ -87,7 +95,6 @@ __global__ void __launch_bounds__(192, 1)
   using L = SquareLayout<BN, STAGES, INT_EXACT>;
   constexpr int BM = L::BM, BK = L::BK;
   constexpr int OBYTES = OutTraits<OUT>::bytes;
-  constexpr int COLS_PER_STORE = 128 / OBYTES;  // output columns per 128-byte row block
   constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, BM, BN);
   static_assert(!INT_EXACT || OUT == OUT_S32, "exact integer mode writes int32");
 
@@ -280,40 +287,44 @@ __global__ void __launch_bounds__(192, 1)
           }
           if (!last_chunk) tmem_wait_st();
         } else {
+          // One block = 32 output columns of this warp's 32 rows: 128-byte
+          // rows (128-byte swizzle) for 4-byte outputs, 64-byte rows (64-byte
+          // swizzle) for 16-bit outputs; the TMA store unswizzles.
 #pragma unroll 1
-          for (int cb = 0; cb < BN / COLS_PER_STORE; ++cb) {
-            uint32_t w[32];  // one 128-byte output row for this lane
-            if constexpr (OBYTES == 4) {
-              tmem_ld_32x32b_x32(t_acc + 32 * cb, w);
-              tmem_wait_ld();
-              if constexpr (OUT == OUT_S32) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) w[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(w[i])));
-              }
-            } else {
-              uint32_t v0[32], v1[32];
-              tmem_ld_32x32b_x32(t_acc + 64 * cb, v0);
-              tmem_ld_32x32b_x32(t_acc + 64 * cb + 32, v1);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                w[i] = pack2<OUT>(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
-                w[16 + i] = pack2<OUT>(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
-              }
-            }
+          for (int cb = 0; cb < BN / 32; ++cb) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_acc + 32 * cb, v);
+            tmem_wait_ld();
             uint8_t* buf = bufs + (stores & 1u) * L::EPI_BUF;
             if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf is done reading
             __syncwarp();
-            uint8_t* row = buf + lane * 128;
+            if constexpr (OBYTES == 4) {
+              if constexpr (OUT == OUT_S32) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-              *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
+                for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+              }
+              uint8_t* row = buf + lane * 128;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint4 q4 = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
+              }
+            } else {
+              uint32_t w[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                w[i] = pack2<OUT>(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+              uint8_t* row = buf + lane * 64;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                *reinterpret_cast<uint4*>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = q4;
+              }
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmC, smem_addr(buf), nt * BN + COLS_PER_STORE * cb, mt * BM + 32 * q);
+              tma_store_2d(&tmC, smem_addr(buf), nt * BN + 32 * cb, mt * BM + 32 * q);
               bulk_commit_group();
             }
             ++stores;

@@ -74,11 +74,24 @@ def _marker_inputs(M, N, T, BK=64, dtype=F16):
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 9, 17])
 @pytest.mark.parametrize("stages", [1, 2, 3, 4])
-def test_k_tile_marker_square(T, stages):
-    # K/BK around the ring depth: fewer, equal, one more, wraps twice
+@pytest.mark.parametrize("bn", [256, 224])
+def test_k_tile_marker_square(T, stages, bn):
+    # K/BK around the ring depth: fewer, equal, one more, wraps twice; three
+    # CTAs over several tiles each, so accumulators and phases wrap as well
     A, B, expect = _marker_inputs(256, 512, T)
-    C = run(A, B, F16 if stages != 4 else F32, stages=stages, splits=3)
+    C = run(A, B, F16, stages=stages, splits=3, bn=bn)
     assert (C.to(torch.float64) == expect).all()
+
+
+@pytest.mark.parametrize("bn", [256, 224, 192, 160, 128])
+@pytest.mark.parametrize("pair", ["f16_f32", "f16_f16", "bf16_bf16", "bf16_f32"])
+def test_every_tile_width(bn, pair):
+    it, ot = pair.split("_")
+    dt = {"f16": F16, "bf16": BF16, "f32": F32}
+    A, B = make_inputs(300, 680, 328, it, "uniform", bn)
+    C = run(A, B, dt[ot], kernel="square", bn=bn)
+    assert f"bn={bn}" in sptg.last_config()
+    assert_float_parity(C, A, B)
 
 
 @pytest.mark.parametrize("T", [1, 2, 7, 8, 9, 17])
@@ -123,8 +136,8 @@ def test_stage_count_does_not_change_the_arithmetic(stages):
     # pipelining reorders loads only ("Pipeline GPU Kernel", Step 5): any
     # ring depth gives the same bits as the default one
     A, B = make_inputs(384, 512, 1024, "f16", "uniform", 12)
-    ref = run(A, B, F16)
-    got = run(A, B, F16, stages=stages)
+    ref = run(A, B, F16, bn=224)
+    got = run(A, B, F16, stages=stages, bn=224)
     assert torch.equal(ref, got)
 
 
