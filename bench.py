@@ -396,6 +396,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K,dtype_pair: time another shape (uniform inputs, seed 1)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--stages", type=int, default=0, help="force the ring depth (ablation)")
     ap.add_argument("--bn", type=int, default=0, help="force the square tile width")
@@ -404,7 +406,13 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
-    w = WORKLOADS[args.workload]
+    if args.shape:
+        from workloads import Workload
+        m, n, k, pair = args.shape.split(",")
+        w = Workload(f"{pair}_{m}x{n}x{k}", int(m), int(n), int(k), pair,
+                     "int8" if pair.startswith("s8") else "uniform", 1.0, 1)
+    else:
+        w = WORKLOADS[args.workload]
     line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)
