@@ -241,7 +241,8 @@ def run_ours(args, w):
     As = [A.to(dev) for _ in range(n_sets)]
     Bs = [B.to(dev) for _ in range(n_sets)]
     Cs = [torch.empty(w.M, w.N, dtype=out_dtype, device=dev) for _ in range(n_sets)]
-    cfg = sptg.Config(0, args.bn, args.stages, 0, 0, 0) if (args.stages or args.bn) else None
+    cfg = (sptg.Config(0, args.bn, args.stages, 0, 0, 0, args.cta_pair)
+           if (args.stages or args.bn or args.cta_pair) else None)
     stream = torch.cuda.current_stream()
 
     def step(i):
@@ -401,6 +402,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--stages", type=int, default=0, help="force the ring depth (ablation)")
     ap.add_argument("--bn", type=int, default=0, help="force the square tile width")
+    ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
+                    help="square kernel: 0 choose, 1 one CTA per tile, 2 CTA pair (2-SM MMA)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -85,6 +85,8 @@ typedef struct {
   int timeout_ms; /* bounded-wait limit inside the kernel (0 = default 2000) */
   int inject_stall; /* test hook: 1 makes the producer withhold one k-tile so
                        the consumer's bounded wait runs out; 0 = off          */
+  int cta_pair; /* square: 0 choose, 1 one CTA (128-row tiles), 2 a CTA pair on
+                   two SMs with the 2-SM MMA (256-row tiles)                 */
 } sptg_config;
 
 /* sptg_gemm with an explicit configuration (NULL = sptg_gemm). */

@@ -1,0 +1,34 @@
+// skinny.cu -- instantiations of the skinny (swap-AB, stream-K) kernel.
+#include "skinny_gemm.cuh"
+#include "variants.h"
+
+namespace sptg {
+
+template <int MN, int ST, bool BF, int OUT>
+KernelVariant make_skinny() {
+  return {reinterpret_cast<const void*>(&skinny_gemm_kernel<MN, ST, BF, OUT>), MN, ST,
+          SkinnyLayout<MN, ST>::SMEM_BYTES, false};
+}
+
+// MMA N = 64 (up to 64 rows of A) at an 8-stage ring for every float dtype
+// pair; bfloat16 -> bfloat16 also at rings 1, 2 and 4 for the ablation.
+bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v) {
+  const int s = stages ? stages : 8;
+  if (s == 8) {
+    if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny<64, 8, true, OUT_BF16>();
+    else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny<64, 8, false, OUT_F16>();
+    else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny<64, 8, true, OUT_F32>();
+    else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny<64, 8, false, OUT_F32>();
+    else return false;
+    return true;
+  }
+  if (!(in_bf16 && out_kind == OUT_BF16)) return false;
+  switch (s) {
+    case 1: *v = make_skinny<64, 1, true, OUT_BF16>(); return true;
+    case 2: *v = make_skinny<64, 2, true, OUT_BF16>(); return true;
+    case 4: *v = make_skinny<64, 4, true, OUT_BF16>(); return true;
+    default: return false;
+  }
+}
+
+}  // namespace sptg

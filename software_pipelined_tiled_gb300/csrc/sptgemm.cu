@@ -20,9 +20,9 @@
 
 #include "sptgemm.h"
 
-#include "convert.cuh"
-#include "skinny_gemm.cuh"
-#include "square_gemm.cuh"
+#include "skinny_gemm.cuh"  // SkinnyParams
+#include "square_gemm.cuh"  // SquareParams
+#include "variants.h"
 
 // Device error word: a timed-out bounded wait ors its site code in here.
 __device__ unsigned int g_sptg_error_word;
@@ -234,127 +234,141 @@ bool dtype_info(int dtype, DtypeInfo& d) {
   }
 }
 
+// ------------------------------------------------------------ launching
+// Launches a kernel variant with the given arguments; a CTA-pair variant
+// goes out as clusters of two.
+cudaError_t launch_variant(const KernelVariant& v, int grid, cudaStream_t stream, void** args) {
+  cudaLaunchConfig_t lc;
+  memset(&lc, 0, sizeof(lc));
+  lc.gridDim = dim3(grid, 1, 1);
+  lc.blockDim = dim3(192, 1, 1);
+  lc.dynamicSmemBytes = v.smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (v.pair) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+  }
+  return cudaLaunchKernelExC(&lc, v.fn, args);
+}
+
+// How many CTA pairs of a pair variant can be resident at once.
+std::map<std::pair<int, const void*>, int> g_pair_slots;
+
+int pair_slots(int dev, const KernelVariant& v, int sm_count) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_pair_slots.find({dev, v.fn});
+    if (it != g_pair_slots.end()) return it->second;
+  }
+  cudaLaunchConfig_t lc;
+  memset(&lc, 0, sizeof(lc));
+  lc.gridDim = dim3(2 * (sm_count / 2), 1, 1);
+  lc.blockDim = dim3(192, 1, 1);
+  lc.dynamicSmemBytes = v.smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, v.fn, &lc) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sm_count / 2;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_pair_slots[{dev, v.fn}] = n;
+  return n;
+}
+
 // ------------------------------------------------------------ square path
-using SquareKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, SquareParams);
-
-struct SquareVariant {
-  SquareKernel fn;
-  int bn, stages, smem;
-};
-
-template <int BN, int ST, bool BF, int OUT, bool IE>
-SquareVariant square_variant() {
-  return {reinterpret_cast<SquareKernel>(&square_gemm_kernel<BN, ST, BF, OUT, IE>), BN, ST,
-          SquareLayout<BN, ST, IE>::SMEM_BYTES};
-}
-
-// The square-kernel variants compiled into the library: for every float
-// dtype pair the tile widths BN in {256, 224, 192, 160, 128} at the deepest
-// ring that fits (square_max_stages); for binary16 -> binary16 at BN 256 and
-// 224 also the shallower rings 1-3 (1 = load, then compute, no overlap) for
-// the pipelining ablation; int8 (exact mode) at BN 128.
-template <bool BF, int OUT>
-bool square_float_variant(int bn, int stages, SquareVariant& v) {
-#define SPTG_SQ(BNV)                                                           \
-  case BNV:                                                                    \
-    if (stages == 0 || stages == square_max_stages<BNV>()) {                   \
-      v = square_variant<BNV, square_max_stages<BNV>(), BF, OUT, false>();     \
-      return true;                                                             \
-    }                                                                          \
-    break;
-  switch (bn) {
-    SPTG_SQ(256)
-    SPTG_SQ(224)
-    SPTG_SQ(192)
-    SPTG_SQ(160)
-    SPTG_SQ(128)
-    default:
-      return false;
-  }
-#undef SPTG_SQ
-  if constexpr (!BF && OUT == OUT_F16) {
-    if (bn == 256 && stages >= 1 && stages <= 3) {
-      v = stages == 1 ? square_variant<256, 1, false, OUT_F16, false>()
-                      : stages == 2 ? square_variant<256, 2, false, OUT_F16, false>()
-                                    : square_variant<256, 3, false, OUT_F16, false>();
-      return true;
-    }
-    if (bn == 224 && stages >= 1 && stages <= 3) {
-      v = stages == 1 ? square_variant<224, 1, false, OUT_F16, false>()
-                      : stages == 2 ? square_variant<224, 2, false, OUT_F16, false>()
-                                    : square_variant<224, 3, false, OUT_F16, false>();
-      return true;
-    }
-  }
-  return false;
-}
-
-// Tile width against wave quantisation: the persistent grid runs
-// ceil(tiles / SMs) rounds of 128 x BN tiles, and a tile costs about
-// BN + 64 column-units (the 64 stands for the A-operand traffic every tile
-// carries whatever its width). The cheapest estimate wins; ties keep the
-// wider tile.
-int choose_square_bn(int64_t M, int64_t N, int sm_count) {
-  static const int cands[] = {256, 224, 192, 160, 128};
-  int best = 256;
-  int64_t best_cost = INT64_MAX;
-  const int64_t mt = (M + 127) / 128;
-  for (int bn : cands) {
-    const int64_t tiles = mt * ((N + bn - 1) / bn);
-    const int64_t rounds = (tiles + sm_count - 1) / sm_count;
-    const int64_t cost = rounds * (bn + 64);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = bn;
-    }
-  }
-  return best;
-}
-
-bool pick_square(const DtypeInfo& d, int stages_req, int bn, SquareVariant& v) {
-  if (d.is_int8) {
-    if (bn != 128 || (stages_req && stages_req != 6)) return false;
-    v = square_variant<128, 6, false, OUT_S32, true>();
-    return true;
-  }
+bool pick_square(const DtypeInfo& d, int bn, int stages, bool pair, KernelVariant* v) {
+  if (d.is_int8) return square_variant_s8(bn, stages, pair, v);
   switch (d.out_kind) {
-    case OUT_F16: return square_float_variant<false, OUT_F16>(bn, stages_req, v);
-    case OUT_BF16: return d.in_bf16 && square_float_variant<true, OUT_BF16>(bn, stages_req, v);
+    case OUT_F16: return !d.in_bf16 && square_variant_f16_f16(bn, stages, pair, v);
+    case OUT_BF16: return d.in_bf16 && square_variant_bf16_bf16(bn, stages, pair, v);
     case OUT_F32:
-      return d.in_bf16 ? square_float_variant<true, OUT_F32>(bn, stages_req, v)
-                       : square_float_variant<false, OUT_F32>(bn, stages_req, v);
+      return d.in_bf16 ? square_variant_bf16_f32(bn, stages, pair, v)
+                       : square_variant_f16_f32(bn, stages, pair, v);
     default: return false;
+  }
+}
+
+// Tile shape against wave quantisation. The persistent grid runs
+// ceil(tiles / workers) rounds, a worker being one SM (128 x BN tiles) or a
+// CTA pair on two SMs (256 x BN tiles). Per SM a tile costs about BN + 64
+// column-units (the 64 stands for the A-operand traffic every tile carries
+// whatever its width); a pair's 2-SM MMA reads half of B per SM, which is
+// credited as a 10 % cheaper tile. The cheapest estimate wins; ties keep the
+// wider tile.
+void choose_square_shape(int64_t M, int64_t N, int sm_count, int bn_req, int pair_req,
+                         bool int8, int* bn_out, bool* pair_out) {
+  static const int cands[] = {256, 224, 192, 160, 128};
+  int64_t best_cost = INT64_MAX;
+  *bn_out = 256;
+  *pair_out = false;
+  for (int pair = 0; pair < 2; ++pair) {
+    if ((pair_req == 1 && pair) || (pair_req == 2 && !pair)) continue;
+    if (pair && M <= 128 && pair_req != 2) continue;  // one CTA already covers all rows
+    const int64_t rows = pair ? 256 : 128;
+    const int64_t workers = pair ? sm_count / 2 : sm_count;
+    for (int bn : cands) {
+      if (bn_req && bn != bn_req) continue;
+      if (int8 && bn != 128) continue;
+      const int64_t tiles = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
+      const int64_t rounds = (tiles + workers - 1) / workers;
+      const int64_t cost = rounds * (bn + 64) * (pair ? 9 : 10);
+      if (cost < best_cost) {
+        best_cost = cost;
+        *bn_out = bn;
+        *pair_out = pair != 0;
+      }
+    }
   }
 }
 
 int run_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N, int64_t K,
                const void* A16, const void* B16, void* C, cudaStream_t stream,
                const sptg_config& cfg) {
-  SquareVariant v;
-  const int bn = cfg.bn ? cfg.bn : (d.is_int8 ? 128 : choose_square_bn(M, N, di.sm_count));
-  if (!pick_square(d, cfg.stages, bn, v)) {
-    t_last_error = "no square-kernel variant for the requested stages/bn";
-    return SPTG_ERR_CONFIG;
+  int bn = 0;
+  bool pair = false;
+  choose_square_shape(M, N, di.sm_count, cfg.bn, cfg.cta_pair, d.is_int8, &bn, &pair);
+  KernelVariant v;
+  if (!pick_square(d, bn, cfg.stages, pair, &v)) {
+    // a forced ring depth may exist for the other tile mode only
+    if (cfg.cta_pair == 0 && pick_square(d, bn, cfg.stages, !pair, &v)) {
+      pair = !pair;
+    } else {
+      t_last_error = "no square-kernel variant for the requested bn/stages/pairing";
+      return SPTG_ERR_CONFIG;
+    }
   }
   const int BM = 128, BK = 64;
+  const int tile_m = pair ? 256 : 128;
   CUtensorMap ta, tb, tc;
   int rc = make_map_2d(&ta, d.in_tma, 2, A16, K, M, BK, BM);
   if (rc) return rc;
-  rc = make_map_2d(&tb, d.in_tma, 2, B16, K, N, BK, v.bn);
+  rc = make_map_2d(&tb, d.in_tma, 2, B16, K, N, BK, pair ? v.bn / 2 : v.bn);
   if (rc) return rc;
   // C blocks of 32 columns x 32 rows: 128-byte rows for 4-byte outputs,
   // 64-byte rows for 16-bit ones (matching the kernel's staging swizzle)
   rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, 32, 32,
                    d.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
-  rc = ensure_smem(dev, reinterpret_cast<const void*>(v.fn), v.smem);
+  rc = ensure_smem(dev, v.fn, v.smem);
   if (rc) return rc;
 
   SquareParams p;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.num_m_tiles = static_cast<int>((M + BM - 1) / BM);
+  p.num_m_tiles = static_cast<int>((M + tile_m - 1) / tile_m);
   p.num_n_tiles = static_cast<int>((N + v.bn - 1) / v.bn);
   p.num_k_tiles = static_cast<int>((K + BK - 1) / BK);
   p.k_tiles_per_chunk = d.is_int8 ? 1024 / BK : p.num_k_tiles;
@@ -363,58 +377,23 @@ int run_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;
   const int tiles = p.num_m_tiles * p.num_n_tiles;
-  const int grid = std::min(tiles, cfg.splits > 0 ? cfg.splits : di.sm_count);
-  v.fn<<<grid, 192, v.smem, stream>>>(ta, tb, tc, p);
+  int workers = pair ? pair_slots(dev, v, di.sm_count) : di.sm_count;
+  if (cfg.splits > 0) workers = std::min(workers, cfg.splits);
+  workers = std::min(workers, tiles);
+  const int grid = pair ? 2 * workers : workers;
+  void* args[] = {&ta, &tb, &tc, &p};
+  cudaError_t e = launch_variant(v, grid, stream, args);
   ++t_launches;
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "square_gemm launch");
   set_config_text(
-      "kernel=square dtype=%s bm=%d bn=%d bk=%d stages=%d grid=%d tiles=%d k_tiles=%d "
-      "chunk_k_tiles=%d smem=%d",
-      d.name, BM, v.bn, BK, v.stages, grid, tiles, p.num_k_tiles, p.k_tiles_per_chunk, v.smem);
+      "kernel=square dtype=%s tile_m=%d bn=%d bk=%d stages=%d pair=%d grid=%d tiles=%d "
+      "k_tiles=%d chunk_k_tiles=%d smem=%d",
+      d.name, tile_m, v.bn, BK, v.stages, pair ? 1 : 0, grid, tiles, p.num_k_tiles,
+      p.k_tiles_per_chunk, v.smem);
   return SPTG_OK;
 }
 
 // ------------------------------------------------------------ skinny path
-using SkinnyKernel = void (*)(CUtensorMap, CUtensorMap, SkinnyParams);
-
-struct SkinnyVariant {
-  SkinnyKernel fn;
-  int mn, stages, smem;
-};
-
-template <int MN, int ST, bool BF, int OUT>
-SkinnyVariant skinny_variant() {
-  return {reinterpret_cast<SkinnyKernel>(&skinny_gemm_kernel<MN, ST, BF, OUT>), MN, ST,
-          SkinnyLayout<MN, ST>::SMEM_BYTES};
-}
-
-bool pick_skinny(const DtypeInfo& d, int stages_req, SkinnyVariant& v) {
-  const int s = stages_req ? stages_req : 8;
-  if (d.is_int8) return false;
-#define SPTG_SKINNY_CASES(ST)                                                     \
-  case ST:                                                                        \
-    if (d.out_kind == OUT_BF16) v = skinny_variant<64, ST, true, OUT_BF16>();      \
-    else if (d.out_kind == OUT_F16) v = skinny_variant<64, ST, false, OUT_F16>();  \
-    else if (d.in_bf16) v = skinny_variant<64, ST, true, OUT_F32>();               \
-    else v = skinny_variant<64, ST, false, OUT_F32>();                             \
-    return true;
-  switch (s) {
-    SPTG_SKINNY_CASES(8)
-    case 1:
-    case 2:
-    case 4:
-      if (d.out_kind != OUT_BF16) return false;
-      v = s == 1 ? skinny_variant<64, 1, true, OUT_BF16>()
-                 : s == 2 ? skinny_variant<64, 2, true, OUT_BF16>()
-                          : skinny_variant<64, 4, true, OUT_BF16>();
-      return true;
-    default:
-      return false;
-  }
-#undef SPTG_SKINNY_CASES
-}
-
 // Caller-provided scratch for the skinny kernel's split-K partials and
 // arrival counters (used by sptg_gemm_skinny_noalloc); null = the cached
 // per-stream scratch of scratch_for().
@@ -436,8 +415,8 @@ unsigned int next_generation(std::atomic<unsigned int>* g) {
 int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N, int64_t K,
                const void* A, const void* B, void* C, cudaStream_t stream,
                const sptg_config& cfg, const FixedScratch* fixed = nullptr) {
-  SkinnyVariant v;
-  if (!pick_skinny(d, cfg.stages, v) || M > v.mn) {
+  KernelVariant v;
+  if (d.is_int8 || !skinny_variant(d.in_bf16, d.out_kind, cfg.stages, &v) || M > v.bn) {
     t_last_error = "no skinny-kernel variant for the requested dtype/stages/M";
     return SPTG_ERR_CONFIG;
   }
@@ -446,9 +425,9 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   // MMA operand A is the B^T tile (128 output columns x 64 k), operand B is the A tile.
   int rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT);
   if (rc) return rc;
-  rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.mn);
+  rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.bn);
   if (rc) return rc;
-  rc = ensure_smem(dev, reinterpret_cast<const void*>(v.fn), v.smem);
+  rc = ensure_smem(dev, v.fn, v.smem);
   if (rc) return rc;
 
   SkinnyParams p;
@@ -481,7 +460,7 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
     split = ((static_cast<int64_t>(c) * units / grid) % p.num_k_tiles) != 0;
   size_t partial_bytes = 0, counter_bytes = 0;
   if (split) {
-    partial_bytes = static_cast<size_t>(p.num_n_tiles) * max_contrib * v.mn * BNT * sizeof(float);
+    partial_bytes = static_cast<size_t>(p.num_n_tiles) * max_contrib * v.bn * BNT * sizeof(float);
     counter_bytes = static_cast<size_t>(p.num_n_tiles) * sizeof(unsigned long long);
     if (fixed) {
       if (partial_bytes > fixed->partial_bytes || counter_bytes > fixed->counter_bytes) {
@@ -513,14 +492,14 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
     p.counters = nullptr;
     p.generation = 0;
   }
-  v.fn<<<grid, 192, v.smem, stream>>>(tb, ta, p);
+  void* args[] = {&tb, &ta, &p};
+  cudaError_t e = launch_variant(v, grid, stream, args);
   ++t_launches;
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "skinny_gemm launch");
   set_config_text(
       "kernel=skinny dtype=%s mma_m=%d mma_n=%d bk=%d stages=%d grid=%d n_tiles=%d k_tiles=%d "
       "units=%lld max_contrib=%d smem=%d",
-      d.name, BNT, v.mn, BK, v.stages, grid, p.num_n_tiles, p.num_k_tiles, (long long)units,
+      d.name, BNT, v.bn, BK, v.stages, grid, p.num_n_tiles, p.num_k_tiles, (long long)units,
       max_contrib, v.smem);
   return SPTG_OK;
 }
@@ -629,7 +608,8 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
     return SPTG_ERR_ARG;
   }
   if (cfg.kernel < 0 || cfg.kernel > 2 || cfg.stages < 0 || cfg.bn < 0 || cfg.splits < 0 ||
-      cfg.timeout_ms < 0 || (cfg.inject_stall != 0 && cfg.inject_stall != 1)) {
+      cfg.timeout_ms < 0 || (cfg.inject_stall != 0 && cfg.inject_stall != 1) ||
+      cfg.cta_pair < 0 || cfg.cta_pair > 2) {
     t_last_error = "invalid configuration field";
     return SPTG_ERR_ARG;
   }
@@ -677,12 +657,9 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
     const int64_t na = M * K / 16, nb = N * K / 16;
     const int blocks_a = static_cast<int>(std::min<int64_t>((na + 255) / 256, 8 * di.sm_count));
     const int blocks_b = static_cast<int>(std::min<int64_t>((nb + 255) / 256, 8 * di.sm_count));
-    s8_to_f16_kernel<<<blocks_a, 256, 0, stream_h>>>(static_cast<const int4*>(A),
-                                                     static_cast<uint4*>(A16), na);
-    s8_to_f16_kernel<<<blocks_b, 256, 0, stream_h>>>(static_cast<const int4*>(B),
-                                                     static_cast<uint4*>(B16), nb);
+    cudaError_t e = launch_s8_to_f16(A, A16, na, blocks_a, stream_h);
+    if (e == cudaSuccess) e = launch_s8_to_f16(B, B16, nb, blocks_b, stream_h);
     t_launches += 2;
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "s8_to_f16 launch");
     return run_square(dev, di, d, M, N, K, A16, B16, C, stream_h, cfg);
   }

@@ -29,6 +29,16 @@
 // taken by two accumulators, so the epilogue of one tile overlaps the K-loop
 // of the next.
 //
+// PAIR mode runs the same roles on a cluster of two CTAs (two SMs) with the
+// 2-SM tensor-core instruction (tcgen05.mma.cta_group::2): a tile is 256 x BN,
+// each CTA loads its own 128 rows of A and its own BN/2 rows of B, the leader
+// CTA's MMA warp multiplies the whole 256 x BN tile reading both CTAs' shared
+// memory, and each CTA's tensor memory receives its 128 rows of the result.
+// Per SM this halves the B traffic of a 128 x BN tile. The copies of both
+// CTAs complete on the leader's "full" barrier; the leader's commits arrive
+// on both CTAs' "empty" and "tmem_full" barriers; both CTAs' epilogue warps
+// release the accumulator on the leader's "tmem_empty" barrier.
+//
 // INT_EXACT mode computes an int8 product exactly on the fp16 tensor path: the
 // inputs are int8 values held as binary16 (exact), every product is an integer
 // of magnitude <= 2^14 and every partial sum of at most 1024 products is an
@@ -51,12 +61,14 @@ struct SquareParams {
   int inject_stall;  // test hook: withhold the load of the second K-tile
 };
 
-template <int BN, int STAGES, bool INT_EXACT>
+template <int BN, int STAGES, bool INT_EXACT, bool PAIR>
 struct SquareLayout {
-  static constexpr int BM = 128;
+  static constexpr int BM = 128;         // rows of A (and of C) per CTA
+  static constexpr int TILE_M = PAIR ? 256 : 128;
+  static constexpr int BN_CTA = PAIR ? BN / 2 : BN;  // rows of B per CTA
   static constexpr int BK = 64;  // 64 16-bit elements = one 128-byte swizzle row
   static constexpr int A_STAGE = BM * BK * 2;
-  static constexpr int B_STAGE = BN * BK * 2;
+  static constexpr int B_STAGE = BN_CTA * BK * 2;
   static constexpr int EPI_WARPS = 4;
   static constexpr int EPI_BUF = 32 * 128;  // 32 rows x 128 bytes
   static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
@@ -74,28 +86,31 @@ struct SquareLayout {
                                    : TMEM_NEEDED <= 128 ? 128
                                    : TMEM_NEEDED <= 256 ? 256
                                                         : 512;
+  // bytes that complete one stage's "full" barrier (both CTAs' copies in PAIR mode)
+  static constexpr uint32_t STAGE_TX = (PAIR ? 2 : 1) * (A_STAGE + B_STAGE);
   static_assert(TMEM_NEEDED <= 512, "accumulators exceed tensor memory");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
+  static_assert(!PAIR || BN_CTA % 16 == 0, "each CTA's B rows must be a multiple of 16");
   static_assert(STAGES >= 1, "at least one stage");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 };
 
 // Deepest ring that fits the 227 KB per-CTA budget next to the epilogue
 // staging (32 KB), the barriers and the 1 KB alignment slack.
-template <int BN>
+template <int BN, bool PAIR = false>
 constexpr int square_max_stages() {
-  return (232448 - 1024 - 4 * 2 * 32 * 128 - 256) / (128 * 64 * 2 + BN * 64 * 2);
+  return (232448 - 1024 - 4 * 2 * 32 * 128 - 256) / (128 * 64 * 2 + (PAIR ? BN / 2 : BN) * 64 * 2);
 }
 
-template <int BN, int STAGES, bool IN_BF16, int OUT, bool INT_EXACT>
+template <int BN, int STAGES, bool IN_BF16, int OUT, bool INT_EXACT, bool PAIR = false>
 __global__ void __launch_bounds__(192, 1)
     square_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const SquareParams p) {
-  using L = SquareLayout<BN, STAGES, INT_EXACT>;
+  using L = SquareLayout<BN, STAGES, INT_EXACT, PAIR>;
   constexpr int BM = L::BM, BK = L::BK;
   constexpr int OBYTES = OutTraits<OUT>::bytes;
-  constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, BM, BN);
+  constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, L::TILE_M, BN);
   static_assert(!INT_EXACT || OUT == OUT_S32, "exact integer mode writes int32");
 
   extern __shared__ uint8_t smem_raw[];
@@ -116,6 +131,8 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA rank within the pair (0 = leader, which issues the MMAs)
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -124,24 +141,30 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), L::EPI_WARPS);
+      mbar_init(tempty_bar(b), (PAIR ? 2 : 1) * L::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_g<PAIR>(smem_addr(tmem_slot), L::TMEM_COLS);
+    tmem_relinquish_g<PAIR>();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // both CTAs' barriers exist before any cross-CTA use
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitCtl ctl{p.timeout_ns, p.error_word, abort_flag};
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
   const int num_chunks = (p.num_k_tiles + p.k_tiles_per_chunk - 1) / p.k_tiles_per_chunk;
+  // the persistent work unit is a CTA, or a CTA pair in PAIR mode
+  const int worker = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -153,9 +176,11 @@ __global__ void __launch_bounds__(192, 1)
       for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
       bool ok = true;
       uint32_t it = 0;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int tile = worker; ok && tile < num_tiles; tile += workers) {
         int mt, nt;
         tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+        const int a_row = mt * L::TILE_M + static_cast<int>(rank) * BM;
+        const int b_row = nt * BN + static_cast<int>(rank) * L::BN_CTA;
         for (int kt = 0; kt < p.num_k_tiles; ++kt, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
@@ -163,31 +188,47 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          if (p.inject_stall && it == 1) continue;  // test hook: this stage never fills
-          mbar_arrive_expect_tx(full_bar(s), L::A_STAGE + L::B_STAGE);
-          tma_load_2d(sA + s * L::A_STAGE, &tmA, full_bar(s), kt * BK, mt * BM, pol);
-          tma_load_2d(sB + s * L::B_STAGE, &tmB, full_bar(s), kt * BK, nt * BN, pol);
+          if (p.inject_stall && it == 1 && rank == 0) continue;  // test hook: stage never fills
+          if constexpr (PAIR) {
+            // both CTAs' copies complete on the leader's barrier; the leader
+            // announces the bytes of both
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), L::STAGE_TX);
+            const uint32_t leader_full = map_to_cta(full_bar(s), 0);
+            tma_load_2d_pair(sA + s * L::A_STAGE, &tmA, leader_full, kt * BK, a_row, pol);
+            tma_load_2d_pair(sB + s * L::B_STAGE, &tmB, leader_full, kt * BK, b_row, pol);
+          } else {
+            mbar_arrive_expect_tx(full_bar(s), L::STAGE_TX);
+            tma_load_2d(sA + s * L::A_STAGE, &tmA, full_bar(s), kt * BK, a_row, pol);
+            tma_load_2d(sB + s * L::B_STAGE, &tmB, full_bar(s), kt * BK, b_row, pol);
+          }
           issued_round[s] = static_cast<int>(round);
         }
       }
       if (!ok) {
         // Let every copy already issued land before the CTA can exit.
-        const WaitCtl drain{ctl.timeout_ns, ctl.error_word, ctl.abort_flag};
-        for (int s = 0; s < STAGES; ++s) {
-          if (issued_round[s] < 0) continue;
-          const uint32_t bar = full_bar(s), par = static_cast<uint32_t>(issued_round[s]) & 1u;
+        if (!PAIR || rank == 0) {
+          for (int s = 0; s < STAGES; ++s) {
+            if (issued_round[s] < 0) continue;
+            const uint32_t bar = full_bar(s), par = static_cast<uint32_t>(issued_round[s]) & 1u;
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(bar, par) && global_timer_ns() - t0 < ctl.timeout_ns) {
+            }
+          }
+        } else {
+          // the peer's copies complete on the leader's barriers, which this
+          // CTA cannot wait on: give them a fixed 100 us to land
           const uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(bar, par) && global_timer_ns() - t0 < drain.timeout_ns) {
+          while (global_timer_ns() - t0 < 100000ull) {
           }
         }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       bool ok = true;
       uint32_t it = 0, unit = 0;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int tile = worker; ok && tile < num_tiles; tile += workers) {
         for (int c = 0; ok && c < num_chunks; ++c, ++unit) {
           const uint32_t b = unit & 1u;
           const uint32_t use = unit >> 1;
@@ -211,17 +252,17 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t b_addr = sB + s * L::B_STAGE;
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              mma_f16(d_tmem, sdesc_k_major_sw128(a_addr + 32 * k),
-                      sdesc_k_major_sw128(b_addr + 32 * k), IDESC,
-                      (kt > kt0 || k > 0) ? 1u : 0u);
+              mma_f16_g<PAIR>(d_tmem, sdesc_k_major_sw128(a_addr + 32 * k),
+                              sdesc_k_major_sw128(b_addr + 32 * k), IDESC,
+                              (kt > kt0 || k > 0) ? 1u : 0u);
             }
-            mma_commit(empty_bar(s));  // stage s may be refilled once these MMAs have read it
+            mma_commit_g<PAIR>(empty_bar(s));  // stage s may be refilled (in both CTAs)
           }
-          if (ok) mma_commit(tfull_bar(b));  // accumulator b holds the finished chunk
+          if (ok) mma_commit_g<PAIR>(tfull_bar(b));  // accumulator b holds the finished chunk
         }
       }
       // Drain: every MMA issued above has completed before tensor memory is freed.
-      mma_commit(drain_bar);
+      mma_commit_local_g<PAIR>(drain_bar);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < ctl.timeout_ns) {
       }
@@ -233,9 +274,10 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t* bufs = epi_buf + (warp - 2) * 2 * L::EPI_BUF;
     uint32_t stores = 0, unit = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+    for (int tile = worker; ok && tile < num_tiles; tile += workers) {
       int mt, nt;
       tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+      const int c_row = mt * L::TILE_M + static_cast<int>(rank) * BM + 32 * q;
       for (int c = 0; c < num_chunks; ++c, ++unit) {
         const uint32_t b = unit & 1u;
         const uint32_t use = unit >> 1;
@@ -279,7 +321,9 @@ __global__ void __launch_bounds__(192, 1)
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&tmC, smem_addr(buf), nt * BN + 32 * cb, mt * BM + 32 * q);
+                // a block that starts past the matrix (ragged edge) stores nothing
+                if (c_row < p.M && nt * BN + 32 * cb < p.N)
+                  tma_store_2d(&tmC, smem_addr(buf), nt * BN + 32 * cb, c_row);
                 bulk_commit_group();
               }
               ++stores;
@@ -324,7 +368,9 @@ __global__ void __launch_bounds__(192, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmC, smem_addr(buf), nt * BN + 32 * cb, mt * BM + 32 * q);
+              // a block that starts past the matrix (ragged edge) stores nothing
+              if (c_row < p.M && nt * BN + 32 * cb < p.N)
+                tma_store_2d(&tmC, smem_addr(buf), nt * BN + 32 * cb, c_row);
               bulk_commit_group();
             }
             ++stores;
@@ -332,17 +378,25 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(b));
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster(map_to_cta(tempty_bar(b), 0));  // the leader's barrier
+          else
+            mbar_arrive(tempty_bar(b));
+        }
       }
     }
     if (lane == 0) bulk_wait_group_all();
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // no CTA leaves while its peer may still signal its barriers
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, L::TMEM_COLS);
+    tmem_dealloc_g<PAIR>(tmem_base, L::TMEM_COLS);
   }
 }
 

@@ -1,0 +1,29 @@
+// square_s8.cu -- the square kernel in exact-integer mode (int8 operands held
+// as binary16, fp32 chunk accumulators of at most 1024 products, int32 sums),
+// and the int8 -> binary16 widening kernel it runs after.
+#include "convert.cuh"
+#include "square_variants.cuh"
+
+namespace sptg {
+
+bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v) {
+  if (bn != 128) return false;
+  if (!pair && (stages == 0 || stages == square_max_stages<128, false>())) {
+    *v = make_square<128, square_max_stages<128, false>(), false, OUT_S32, true, false>();
+    return true;
+  }
+  if (pair && (stages == 0 || stages == square_max_stages<128, true>())) {
+    *v = make_square<128, square_max_stages<128, true>(), false, OUT_S32, true, true>();
+    return true;
+  }
+  return false;
+}
+
+cudaError_t launch_s8_to_f16(const void* src, void* dst, int64_t n16, int blocks,
+                             cudaStream_t stream) {
+  s8_to_f16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const int4*>(src),
+                                               static_cast<uint4*>(dst), n16);
+  return cudaGetLastError();
+}
+
+}  // namespace sptg

@@ -1,0 +1,68 @@
+// square_variants.cuh -- the instantiation table of the square kernel,
+// included by one translation unit per dtype pair.
+#pragma once
+
+#include "square_gemm.cuh"
+#include "variants.h"
+
+namespace sptg {
+
+template <int BN, int ST, bool BF, int OUT, bool IE, bool PAIR>
+KernelVariant make_square() {
+  return {reinterpret_cast<const void*>(&square_gemm_kernel<BN, ST, BF, OUT, IE, PAIR>), BN, ST,
+          SquareLayout<BN, ST, IE, PAIR>::SMEM_BYTES, PAIR};
+}
+
+// Tile widths BN in {256, 224, 192, 160, 128}, one CTA or a CTA pair per
+// tile, each at the deepest ring that fits (square_max_stages). For
+// binary16 -> binary16 also the shallower rings of BN 256 and 224 for the
+// pipelining ablation (1 = load, then compute, no overlap).
+template <bool BF, int OUT>
+bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v) {
+#define SPTG_SQ(BNV)                                                                 \
+  case BNV:                                                                          \
+    if (!pair && (stages == 0 || stages == square_max_stages<BNV, false>())) {       \
+      *v = make_square<BNV, square_max_stages<BNV, false>(), BF, OUT, false, false>(); \
+      return true;                                                                   \
+    }                                                                                \
+    if (pair && (stages == 0 || stages == square_max_stages<BNV, true>())) {         \
+      *v = make_square<BNV, square_max_stages<BNV, true>(), BF, OUT, false, true>();   \
+      return true;                                                                   \
+    }                                                                                \
+    break;
+  switch (bn) {
+    SPTG_SQ(256)
+    SPTG_SQ(224)
+    SPTG_SQ(192)
+    SPTG_SQ(160)
+    SPTG_SQ(128)
+    default:
+      return false;
+  }
+#undef SPTG_SQ
+  if constexpr (!BF && OUT == OUT_F16) {
+    if (!pair && (bn == 256 || bn == 224) && stages >= 1 && stages <= 3) {
+      if (bn == 256)
+        *v = stages == 1 ? make_square<256, 1, false, OUT_F16, false, false>()
+                         : stages == 2 ? make_square<256, 2, false, OUT_F16, false, false>()
+                                       : make_square<256, 3, false, OUT_F16, false, false>();
+      else
+        *v = stages == 1 ? make_square<224, 1, false, OUT_F16, false, false>()
+                         : stages == 2 ? make_square<224, 2, false, OUT_F16, false, false>()
+                                       : make_square<224, 3, false, OUT_F16, false, false>();
+      return true;
+    }
+    if (pair && bn == 224 && stages >= 1 && stages <= 5) {
+      switch (stages) {
+        case 1: *v = make_square<224, 1, false, OUT_F16, false, true>(); return true;
+        case 2: *v = make_square<224, 2, false, OUT_F16, false, true>(); return true;
+        case 3: *v = make_square<224, 3, false, OUT_F16, false, true>(); return true;
+        case 4: *v = make_square<224, 4, false, OUT_F16, false, true>(); return true;
+        default: *v = make_square<224, 5, false, OUT_F16, false, true>(); return true;
+      }
+    }
+  }
+  return false;
+}
+
+}  // namespace sptg

@@ -1,0 +1,35 @@
+// variants.h -- host-side catalogue of the compiled kernel variants.
+//
+// Each kernel template instantiation lives in one of the square_*.cu /
+// skinny.cu translation units (compiled in parallel); the host API finds
+// them through these lookups and launches them with cudaLaunchKernelExC.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sptg {
+
+struct KernelVariant {
+  const void* fn;  // the __global__ function
+  int bn;          // square: tile columns; skinny: MMA N (rows of A covered)
+  int stages;      // shared-memory ring depth
+  int smem;        // dynamic shared memory per CTA, bytes
+  bool pair;       // square: 2-SM CTA-pair variant (cluster of 2)
+};
+
+// Square kernel for binary16 inputs (out_kind OUT_F16 or OUT_F32).
+bool square_variant_f16_f16(int bn, int stages, bool pair, KernelVariant* v);
+bool square_variant_f16_f32(int bn, int stages, bool pair, KernelVariant* v);
+// Square kernel for bfloat16 inputs (out_kind OUT_BF16 or OUT_F32).
+bool square_variant_bf16_bf16(int bn, int stages, bool pair, KernelVariant* v);
+bool square_variant_bf16_f32(int bn, int stages, bool pair, KernelVariant* v);
+// Square kernel in exact-integer mode (int8 operands widened to binary16).
+bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v);
+// Skinny kernel (in_bf16 selects bfloat16 inputs, else binary16).
+bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
+// int8 -> binary16 widening of n16 groups of 16 elements.
+cudaError_t launch_s8_to_f16(const void* src, void* dst, int64_t n16, int blocks,
+                             cudaStream_t stream);
+
+}  // namespace sptg

@@ -79,7 +79,8 @@ def test_k_tile_marker_square(T, stages, bn):
     # K/BK around the ring depth: fewer, equal, one more, wraps twice; three
     # CTAs over several tiles each, so accumulators and phases wrap as well
     A, B, expect = _marker_inputs(256, 512, T)
-    C = run(A, B, F16, stages=stages, splits=3, bn=bn)
+    C = run(A, B, F16, stages=stages, splits=3, bn=bn, cta_pair=1)
+    assert "pair=0" in sptg.last_config()
     assert (C.to(torch.float64) == expect).all()
 
 
@@ -89,9 +90,52 @@ def test_every_tile_width(bn, pair):
     it, ot = pair.split("_")
     dt = {"f16": F16, "bf16": BF16, "f32": F32}
     A, B = make_inputs(300, 680, 328, it, "uniform", bn)
-    C = run(A, B, dt[ot], kernel="square", bn=bn)
-    assert f"bn={bn}" in sptg.last_config()
+    C = run(A, B, dt[ot], kernel="square", bn=bn, cta_pair=1)
+    assert f"bn={bn}" in sptg.last_config() and "pair=0" in sptg.last_config()
     assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 6, 7, 13])
+@pytest.mark.parametrize("bn", [224, 128])
+def test_k_tile_marker_cta_pair(T, bn):
+    # 2-SM tiles: both CTAs' copies must land before the leader's MMA, and
+    # both halves of the result must come back; 3 pairs over several tiles
+    A, B, expect = _marker_inputs(512, 896, T)
+    C = run(A, B, F16, cta_pair=2, bn=bn, splits=3)
+    assert "pair=1" in sptg.last_config()
+    assert (C.to(torch.float64) == expect).all()
+
+
+@pytest.mark.parametrize("bn", [256, 224, 192, 160, 128])
+@pytest.mark.parametrize("pair", ["f16_f32", "f16_f16", "bf16_bf16", "bf16_f32"])
+def test_every_tile_width_cta_pair(bn, pair):
+    it, ot = pair.split("_")
+    dt = {"f16": F16, "bf16": BF16, "f32": F32}
+    # M = 300: the second pair-tile's peer CTA sees only out-of-range rows
+    A, B = make_inputs(300, 680, 328, it, "uniform", bn + 1)
+    C = run(A, B, dt[ot], kernel="square", bn=bn, cta_pair=2)
+    assert f"bn={bn}" in sptg.last_config() and "pair=1" in sptg.last_config()
+    assert_float_parity(C, A, B)
+
+
+def test_cta_pair_operand_halves_are_not_swapped():
+    # rows of A and columns of B differ everywhere: a swapped half or a
+    # misplaced peer tile changes the result
+    M, N, K = 256, 224, 64
+    A = (torch.arange(M).unsqueeze(1) + 1).to(F32).expand(M, K).contiguous() / 256
+    Bcm = (torch.arange(N).unsqueeze(1) + 1).to(F32).expand(N, K).contiguous() / 256
+    A, Bcm = A.to(F16), Bcm.to(F16)
+    C = run(A, Bcm, F32, cta_pair=2, bn=224)
+    expect = (A.to(torch.float64) @ Bcm.to(torch.float64).t()).to(F32)
+    assert torch.equal(C, expect)
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3, 4, 5])
+def test_cta_pair_stage_count_does_not_change_the_arithmetic(stages):
+    A, B = make_inputs(512, 448, 640, "f16", "uniform", 13)
+    ref = run(A, B, F16, bn=224, cta_pair=2)
+    got = run(A, B, F16, stages=stages, bn=224, cta_pair=2)
+    assert torch.equal(ref, got)
 
 
 @pytest.mark.parametrize("T", [1, 2, 7, 8, 9, 17])
@@ -136,8 +180,8 @@ def test_stage_count_does_not_change_the_arithmetic(stages):
     # pipelining reorders loads only ("Pipeline GPU Kernel", Step 5): any
     # ring depth gives the same bits as the default one
     A, B = make_inputs(384, 512, 1024, "f16", "uniform", 12)
-    ref = run(A, B, F16, bn=224)
-    got = run(A, B, F16, stages=stages, bn=224)
+    ref = run(A, B, F16, bn=224, cta_pair=1)
+    got = run(A, B, F16, stages=stages, bn=224, cta_pair=1)
     assert torch.equal(ref, got)
 
 
@@ -159,6 +203,14 @@ def test_ragged_shapes(M, N, K, dt, out):
 def test_int8_exact_small(M, N, K):
     A, B = make_inputs(M, N, K, "s8", "int8", 7 + K)
     C = run(A, B, I32)
+    assert_int_parity(C, A, B)
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 384, 2080), (300, 136, 1024)])
+def test_int8_exact_cta_pair(M, N, K):
+    A, B = make_inputs(M, N, K, "s8", "int8", 11 + K)
+    C = run(A, B, I32, cta_pair=2)
+    assert "pair=1" in sptg.last_config()
     assert_int_parity(C, A, B)
 
 
@@ -219,15 +271,15 @@ def test_async_on_a_side_stream():
     assert_float_parity(C.cpu(), A, B)
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
-def test_bounded_wait_reports_timeout_and_context_survives(kernel):
+@pytest.mark.parametrize("kernel,pair", [(1, 1), (1, 2), (2, 0)])
+def test_bounded_wait_reports_timeout_and_context_survives(kernel, pair):
     # The producer withholds one K-tile; the consumer's wait runs out after
     # 100 ms, the kernel tears down, and the host reads SPTG_ERR_TIMEOUT.
-    M = 256 if kernel == 1 else 64
+    M = 512 if kernel == 1 else 64
     A, B = make_inputs(M, 1024, 1024, "bf16", "normal", 30)
     dA, dB = A.cuda(), B.cuda()
     C = torch.empty(M, 1024, dtype=BF16, device="cuda")
-    cfg = sptg.Config(kernel, 0, 0, 4, 100, 1)
+    cfg = sptg.Config(kernel, 0, 0, 4, 100, 1, pair)
     rc = sptg.gemm_raw(M, 1024, 1024, "bf16_bf16", dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
                        torch.cuda.current_stream().cuda_stream, cfg)
     assert rc == 0
