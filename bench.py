@@ -241,8 +241,8 @@ def run_ours(args, w):
     As = [A.to(dev) for _ in range(n_sets)]
     Bs = [B.to(dev) for _ in range(n_sets)]
     Cs = [torch.empty(w.M, w.N, dtype=out_dtype, device=dev) for _ in range(n_sets)]
-    cfg = (sptg.Config(0, args.bn, args.stages, 0, 0, 0, args.cta_pair)
-           if (args.stages or args.bn or args.cta_pair) else None)
+    cfg = (sptg.Config(0, args.bn, args.stages, 0, 0, 0, args.cta_pair, int(args.no_overlap))
+           if (args.stages or args.bn or args.cta_pair or args.no_overlap) else None)
     stream = torch.cuda.current_stream()
 
     def step(i):
@@ -257,16 +257,38 @@ def run_ours(args, w):
     launches_per_step = int(sptg.last_config().split("launches=")[-1].split()[0])
     kernel_name = sptg.last_config().split()[0].split("=")[1]
 
+    graph = None
+    if args.graph:
+        # the K timed steps captured once as a CUDA graph on a side stream
+        # (warm-up on that stream first, so its scratch exists before capture)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for i in range(args.warmup):
+                step(i)
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(args.steps):
+                step(i)
+        torch.cuda.synchronize()
+        # replay() launches on the current stream, where the events are recorded
+
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
     barrier(world)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0 = time.perf_counter()
     ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            step(i)
     ev1.record(stream)
+    host_us = (time.perf_counter() - h0) * 1e6 / args.steps
     torch.cuda.synchronize()
     barrier(world)
     if rank == 0:
@@ -333,6 +355,10 @@ def run_ours(args, w):
     roof["algorithmic_bytes"] = set_bytes
     roof["kernel"] = kernel_name
 
+    tl = None
+    if args.trace:
+        fields = (0, args.bn, args.stages, 0, 0, 0, args.cta_pair)
+        tl = timeline(sptg, As[0], Bs[0], Cs[0], fields)
     cpu = None if args.no_cpu_baseline else cpu_baseline(w, A, B)
     clocks = sampler.summary()
     line = {
@@ -346,8 +372,51 @@ def run_ours(args, w):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+        "launch": {"mode": "cuda-graph" if graph is not None else "stream",
+                   "host_us_per_step": host_us,
+                   "overlap_previous": not args.no_overlap},
     }
+    if tl is not None:
+        line["timeline"] = tl
     return line
+
+
+TRACE_EVENTS = ["setup", "first_load", "first_data", "last_load", "last_mma", "epi_done",
+                "exit", "fixup_done"]
+TRACE_WORDS = 8 * 1024 + 2 * 64
+
+
+def timeline(sptg, A, B, C, cfg_fields):
+    """One traced call: per-event spread over CTAs and CTA 0's K-tile detail."""
+    import numpy as np
+    buf = torch.zeros(TRACE_WORDS, dtype=torch.int64, device=A.device)
+    cfg = sptg.Config(*cfg_fields)
+    cfg.trace = buf.data_ptr()
+    sptg.gemm(A, B, C=C, config=cfg)
+    torch.cuda.synchronize()
+    t = buf.cpu().numpy().astype(np.int64)
+    grid = int(sptg.last_config().split("grid=")[1].split()[0])
+    ev = t[:8 * 1024].reshape(1024, 8)[:grid]
+    t0 = ev[:, 0][ev[:, 0] > 0].min()
+    out = {"ctas": grid}
+    for i, name in enumerate(TRACE_EVENTS):
+        col = ev[:, i][ev[:, i] > 0]
+        if len(col):
+            us = (col - t0) / 1e3
+            out[name + "_us"] = [round(float(us.min()), 2), round(float(np.median(us)), 2),
+                                 round(float(us.max()), 2)]
+    issue = t[8 * 1024: 8 * 1024 + 64]
+    full = t[8 * 1024 + 64: 8 * 1024 + 128]
+    n = int(min((issue > 0).sum(), (full > 0).sum()))
+    if n:
+        lat = (full[:n] - issue[:n]) / 1e3
+        ahead = [int(((issue[:n] > 0) & (issue[:n] <= full[i])).sum()) - (i + 1) for i in range(n)]
+        out["cta0_ktiles"] = n
+        out["cta0_issue_to_full_us"] = [round(float(lat.min()), 2), round(float(np.median(lat)), 2),
+                                        round(float(lat.max()), 2)]
+        out["cta0_tiles_in_flight_at_consume"] = [int(min(ahead)), int(np.median(ahead)),
+                                                  int(max(ahead))]
+    return out
 
 
 def run_reference(args, w):
@@ -405,6 +474,12 @@ def main(argv=None):
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="square kernel: 0 choose, 1 one CTA per tile, 2 CTA pair (2-SM MMA)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the timed steps as one CUDA graph and replay it")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="launch without programmatic dependent launch")
+    ap.add_argument("--trace", action="store_true",
+                    help="add one traced call's in-kernel timeline to the JSON line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

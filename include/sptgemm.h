@@ -78,16 +78,33 @@ int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype,
 
 /* Kernel selection for sptg_gemm_ex; fields left at 0 mean "choose". */
 typedef struct {
-  int kernel;   /* 0 auto, 1 square (tile rows 128), 2 skinny swap-AB        */
+  int kernel;   /* 0 auto, 1 square, 2 skinny swap-AB with stream-K split,
+                   3 skinny swap-AB with the K split inside thread-block
+                   clusters (splits = cluster size 1, 2, 4 or 8)              */
   int bn;       /* square: tile columns (multiple of 16, 16..256)           */
   int stages;   /* shared-memory ring depth (1 = synchronous load/compute)  */
-  int splits;   /* skinny: number of CTAs sharing the work (0 = SM count)   */
+  int splits;   /* square: cap on persistent workers; skinny stream-K: CTAs
+                   sharing the work (0 = SM count); skinny cluster: cluster
+                   size                                                      */
   int timeout_ms; /* bounded-wait limit inside the kernel (0 = default 2000) */
   int inject_stall; /* test hook: 1 makes the producer withhold one k-tile so
                        the consumer's bounded wait runs out; 0 = off          */
   int cta_pair; /* square: 0 choose, 1 one CTA (128-row tiles), 2 a CTA pair on
                    two SMs with the 2-SM MMA (256-row tiles)                 */
+  int no_overlap; /* 1: launch without programmatic dependent launch (the
+                     kernel then starts only after the previous one ends)    */
+  void* trace;  /* optional device buffer of SPTG_TRACE_WORDS uint64 (8-byte
+                   aligned, zeroed by the caller): word [8*cta + e] is the
+                   %globaltimer ns of event e of CTA cta (first 1024 CTAs):
+                   0 set-up done, 1 first copy issued, 2 first stage full at
+                   the MMA issuer, 3 last copy issued, 4 last MMA committed,
+                   5 epilogue done, 6 exit, 7 last split-K reduction; then
+                   for CTA 0, the issue time of K-tiles 0..63 (words 8192..)
+                   and the time the MMA issuer found each full (8256..);
+                   NULL = off                                               */
 } sptg_config;
+
+#define SPTG_TRACE_WORDS (8 * 1024 + 2 * 64)
 
 /* sptg_gemm with an explicit configuration (NULL = sptg_gemm). */
 int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype,

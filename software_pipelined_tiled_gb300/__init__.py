@@ -28,7 +28,7 @@ DTYPES = {"f16_f32": 0, "f16_f16": 1, "s8_s32": 2, "bf16_bf16": 3, "bf16_f32": 4
 STATUS = {0: "SPTG_OK", -1: "SPTG_ERR_ARG", -2: "SPTG_ERR_ALIGN", -3: "SPTG_ERR_UNSUPPORTED",
           -4: "SPTG_ERR_LAUNCH", -5: "SPTG_ERR_TIMEOUT", -6: "SPTG_ERR_NOMEM",
           -7: "SPTG_ERR_CONFIG"}
-KERNELS = {"auto": 0, "square": 1, "skinny": 2}
+KERNELS = {"auto": 0, "square": 1, "skinny": 2, "skinny_cluster": 3}
 
 # the C functions every build must export (checked by the tests)
 EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_status_string", "sptg_last_error",
@@ -45,7 +45,8 @@ class Config(ctypes.Structure):
     """sptg_config: 0 in a field means "let the library choose"."""
     _fields_ = [("kernel", ctypes.c_int), ("bn", ctypes.c_int), ("stages", ctypes.c_int),
                 ("splits", ctypes.c_int), ("timeout_ms", ctypes.c_int),
-                ("inject_stall", ctypes.c_int), ("cta_pair", ctypes.c_int)]
+                ("inject_stall", ctypes.c_int), ("cta_pair", ctypes.c_int),
+                ("no_overlap", ctypes.c_int), ("trace", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -114,7 +115,7 @@ def gemm_raw(M: int, N: int, K: int, dtype: str | int, A_ptr: int, B_ptr: int, C
     """Calls sptg_gemm_ex with raw device pointers; returns the status code."""
     d = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
     cfg = ctypes.byref(config) if config is not None else None
-    return int(load().sptg_gemm_ex(M, N, K, d, A_ptr, B_ptr, C_ptr, stream, cfg))
+    return int((_lib or load()).sptg_gemm_ex(M, N, K, d, A_ptr, B_ptr, C_ptr, stream, cfg))
 
 
 def gemm_skinny_noalloc_raw(M: int, N: int, K: int, dtype: str | int, A_ptr: int, B_ptr: int,
@@ -164,9 +165,13 @@ def gemm(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = No
         raise ValueError("C must be a contiguous M x N CUDA tensor of the output dtype")
     if config is None and (kernel or stages or bn or splits or cta_pair):
         config = Config(KERNELS[kernel or "auto"], bn, stages, splits, 0, 0, cta_pair)
-    with torch.cuda.device(A.device):
+    if A.device.index == torch.cuda.current_device():
         rc = gemm_raw(M, N, K, key, A.data_ptr(), Bcm.data_ptr(), C.data_ptr(),
                       _stream_handle(stream), config)
+    else:
+        with torch.cuda.device(A.device):
+            rc = gemm_raw(M, N, K, key, A.data_ptr(), Bcm.data_ptr(), C.data_ptr(),
+                          _stream_handle(stream), config)
     if rc != 0:
         raise SptgError(rc, last_error() or status_string(rc))
     return C

@@ -29,6 +29,37 @@ enum WaitSite : unsigned int {
   WAIT_PLAN = 1u << 5,  // not a wait: a launch whose scratch plan does not fit
 };
 
+// Optional timeline: with a trace buffer, chosen threads stamp %globaltimer
+// (ns) at these points into trace[cta * TR_SLOTS + event] (CTAs < TR_MAX_CTAS).
+enum TraceEvent : int {
+  TR_SETUP = 0,       // barriers, tensor memory and the dependency wait done
+  TR_FIRST_LOAD = 1,  // producer issued its first copy
+  TR_FIRST_DATA = 2,  // MMA issuer saw its first full stage
+  TR_LAST_LOAD = 3,   // producer issued its last copy
+  TR_LAST_MMA = 4,    // MMA issuer committed its last MMA
+  TR_EPI_DONE = 5,    // epilogue finished its last tile (stores complete)
+  TR_EXIT = 6,        // every role of the CTA (and of its pair) is done
+  TR_FIXUP_DONE = 7,  // skinny: last split-K reduction this CTA did, if any
+  TR_SLOTS = 8,
+  TR_MAX_CTAS = 1024,
+  // detail of CTA 0: when the producer issued K-tile i and when the MMA
+  // issuer found it full, for the first TR_DETAIL K-tiles of the CTA
+  TR_DETAIL = 64,
+  TR_DETAIL_BASE = TR_SLOTS * TR_MAX_CTAS,
+  TR_WORDS = TR_DETAIL_BASE + 2 * TR_DETAIL
+};
+
+__device__ __forceinline__ void trace_mark(unsigned long long* trace, int event) {
+  if (trace != nullptr && blockIdx.x < TR_MAX_CTAS)
+    trace[blockIdx.x * TR_SLOTS + event] = global_timer_ns();
+}
+
+// role 0 = producer issued K-tile `it`, role 1 = MMA issuer found it full
+__device__ __forceinline__ void trace_ktile(unsigned long long* trace, int role, uint32_t it) {
+  if (trace != nullptr && blockIdx.x == 0 && it < TR_DETAIL)
+    trace[TR_DETAIL_BASE + role * TR_DETAIL + it] = global_timer_ns();
+}
+
 // Everything a bounded wait needs: the limit, where to report, and the
 // CTA-wide abort flag that lets the other roles stop early once one gave up.
 struct WaitCtl {
@@ -87,6 +118,31 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   } else {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// One output element of the given kind from an fp32 value (round to nearest
+// even for the 16-bit kinds).
+template <int OUT>
+__device__ __forceinline__ void store_out(void* C, int64_t idx, float v) {
+  if constexpr (OUT == OUT_F32) {
+    static_cast<float*>(C)[idx] = v;
+  } else if constexpr (OUT == OUT_F16) {
+    static_cast<__half*>(C)[idx] = __float2half_rn(v);
+  } else {
+    static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
+  }
+}
+
+// Four consecutive outputs; idx is a multiple of 4 and the row pitch keeps
+// the group inside one row (N is a multiple of 4 for every output type).
+template <int OUT>
+__device__ __forceinline__ void store_out4(void* C, int64_t idx, float4 v) {
+  if constexpr (OUT == OUT_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(C) + idx) = v;
+  } else {
+    uint2 w = make_uint2(pack2<OUT>(v.x, v.y), pack2<OUT>(v.z, v.w));
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(C) + idx) = w;
   }
 }
 

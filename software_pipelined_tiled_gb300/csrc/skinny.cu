@@ -1,4 +1,5 @@
 // skinny.cu -- instantiations of the skinny (swap-AB, stream-K) kernel.
+#include "skinny_cluster_gemm.cuh"
 #include "skinny_gemm.cuh"
 #include "variants.h"
 
@@ -29,6 +30,23 @@ bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v) {
     case 4: *v = make_skinny<64, 4, true, OUT_BF16>(); return true;
     default: return false;
   }
+}
+
+template <int MN, int ST, bool BF, int OUT>
+KernelVariant make_skinny_cluster() {
+  return {reinterpret_cast<const void*>(&skinny_cluster_gemm_kernel<MN, ST, BF, OUT>), MN, ST,
+          SkinnyClusterLayout<MN, ST>::SMEM_BYTES, false};
+}
+
+// MMA N = 64 at an 8-stage ring for every float dtype pair.
+bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v) {
+  if (stages != 0 && stages != 8) return false;
+  if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny_cluster<64, 8, true, OUT_BF16>();
+  else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny_cluster<64, 8, false, OUT_F16>();
+  else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny_cluster<64, 8, true, OUT_F32>();
+  else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny_cluster<64, 8, false, OUT_F32>();
+  else return false;
+  return true;
 }
 
 }  // namespace sptg

@@ -41,6 +41,7 @@ struct SkinnyParams {
   unsigned int* error_word;
   uint64_t timeout_ns;
   int inject_stall;
+  unsigned long long* trace;  // optional timeline (see TraceEvent), or null
 };
 
 template <int MN, int STAGES>
@@ -63,29 +64,6 @@ struct SkinnyLayout {
 // CTA whose unit range [c*T/G, (c+1)*T/G) holds unit u.
 __device__ __forceinline__ int cta_of_unit(int64_t u, int G, int64_t T) {
   return static_cast<int>(((u + 1) * G - 1) / T);
-}
-
-template <int OUT>
-__device__ __forceinline__ void store_out(void* C, int64_t idx, float v) {
-  if constexpr (OUT == OUT_F32) {
-    static_cast<float*>(C)[idx] = v;
-  } else if constexpr (OUT == OUT_F16) {
-    static_cast<__half*>(C)[idx] = __float2half_rn(v);
-  } else {
-    static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
-  }
-}
-
-// Four consecutive outputs; idx is a multiple of 4 and the row pitch keeps
-// the group inside one row (N is a multiple of 4 for every output type).
-template <int OUT>
-__device__ __forceinline__ void store_out4(void* C, int64_t idx, float4 v) {
-  if constexpr (OUT == OUT_F32) {
-    *reinterpret_cast<float4*>(static_cast<float*>(C) + idx) = v;
-  } else {
-    uint2 w = make_uint2(pack2<OUT>(v.x, v.y), pack2<OUT>(v.z, v.w));
-    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(C) + idx) = w;
-  }
 }
 
 // Counts one arrival at an n-tile's counter and returns whether it was the
@@ -148,6 +126,9 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // kernel parameters, not written by earlier kernels: fetch them early
+    prefetch_tensor_map(&tmBt);
+    prefetch_tensor_map(&tmA);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);
@@ -157,6 +138,10 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Set-up above may overlap the previous kernel in the stream; no global
+  // memory is touched before that kernel has completed.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) trace_mark(p.trace, TR_SETUP);
 
   const WaitCtl ctl{p.timeout_ns, p.error_word, abort_flag};
   const int G = p.num_ctas;
@@ -168,8 +153,6 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tensor_map(&tmBt);
-      prefetch_tensor_map(&tmA);
       const uint64_t pol_stream = policy_evict_first();  // B is read once
       const uint64_t pol_keep = policy_evict_last();     // A is read by every CTA
       int issued_round[STAGES];
@@ -190,7 +173,11 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_2d(stage_bt(s), &tmBt, full_bar(s), kt * BK, nt * BNT, pol_stream);
         tma_load_2d(stage_a(s), &tmA, full_bar(s), kt * BK, 0, pol_keep);
         issued_round[s] = static_cast<int>(round);
+        if (it == 0) trace_mark(p.trace, TR_FIRST_LOAD);
+          trace_ktile(p.trace, 0, it);
       }
+      trace_mark(p.trace, TR_LAST_LOAD);
+      grid_launch_dependents();  // the next kernel may start its set-up
       if (!ok) {
         for (int s = 0; s < STAGES; ++s) {
           if (issued_round[s] < 0) continue;
@@ -226,6 +213,8 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after();
+          if (it == 0) trace_mark(p.trace, TR_FIRST_DATA);
+            trace_ktile(p.trace, 1, it);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             mma_f16(d_tmem, sdesc_k_major_sw128(stage_bt(s) + 32 * k),
@@ -237,6 +226,7 @@ __global__ void __launch_bounds__(192, 1)
         u = seg_end;
         ++seg;
       }
+      trace_mark(p.trace, TR_LAST_MMA);
       mma_commit(drain_bar);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < ctl.timeout_ns) {
@@ -305,39 +295,67 @@ __global__ void __launch_bounds__(192, 1)
           const int tid = threadIdx.x - 64;
           const float4* base = reinterpret_cast<const float4*>(
               p.partials + static_cast<int64_t>(nt) * p.max_contrib * (MN * BNT));
-          float4 sum[PER_THREAD];
+          // two halves of the tile; in each, the loads of up to four
+          // contributors are issued together, then added in order
+          constexpr int HALF = PER_THREAD / 2;
+          constexpr int64_t SLOT4 = MN * BNT / 4;
 #pragma unroll
-          for (int i = 0; i < PER_THREAD; ++i) sum[i] = __ldcg(base + tid + 128 * i);
-          for (int jj = 1; jj < count; ++jj) {
-            const float4* pj = base + static_cast<int64_t>(jj) * (MN * BNT / 4);
-            float4 v[PER_THREAD];
+          for (int h = 0; h < 2; ++h) {
+            float4 v[4][HALF];
 #pragma unroll
-            for (int i = 0; i < PER_THREAD; ++i) v[i] = __ldcg(pj + tid + 128 * i);
+            for (int jj = 0; jj < 4; ++jj) {
+              if (jj < count) {
 #pragma unroll
-            for (int i = 0; i < PER_THREAD; ++i) {
-              sum[i].x += v[i].x;
-              sum[i].y += v[i].y;
-              sum[i].z += v[i].z;
-              sum[i].w += v[i].w;
+                for (int i = 0; i < HALF; ++i)
+                  v[jj][i] = __ldcg(base + jj * SLOT4 + tid + 128 * (h * HALF + i));
+              }
+            }
+            float4 sum[HALF];
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) sum[i] = v[0][i];
+#pragma unroll
+            for (int jj = 1; jj < 4; ++jj) {
+              if (jj < count) {
+#pragma unroll
+                for (int i = 0; i < HALF; ++i) {
+                  sum[i].x += v[jj][i].x;
+                  sum[i].y += v[jj][i].y;
+                  sum[i].z += v[jj][i].z;
+                  sum[i].w += v[jj][i].w;
+                }
+              }
+            }
+            for (int jj = 4; jj < count; ++jj) {  // more than four contributors: rare
+#pragma unroll
+              for (int i = 0; i < HALF; ++i) {
+                const float4 w = __ldcg(base + jj * SLOT4 + tid + 128 * (h * HALF + i));
+                sum[i].x += w.x;
+                sum[i].y += w.y;
+                sum[i].z += w.z;
+                sum[i].w += w.w;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) {
+              const int f = tid + 128 * (h * HALF + i);
+              const int m = f / F4_PER_ROW;
+              const int n0 = nt * BNT + 4 * (f % F4_PER_ROW);
+              if (m < M && n0 < p.N) store_out4<OUT>(p.C, static_cast<int64_t>(m) * p.N + n0, sum[i]);
             }
           }
-#pragma unroll
-          for (int i = 0; i < PER_THREAD; ++i) {
-            const int f = tid + 128 * i;
-            const int m = f / F4_PER_ROW;
-            const int n0 = nt * BNT + 4 * (f % F4_PER_ROW);
-            if (m < M && n0 < p.N) store_out4<OUT>(p.C, static_cast<int64_t>(m) * p.N + n0, sum[i]);
-          }
+          if (threadIdx.x == 64) trace_mark(p.trace, TR_FIXUP_DONE);
         }
         named_barrier_sync(1, 128);  // last_flag is reused by the next segment
       }
       u = seg_end;
       ++seg;
     }
+    if (threadIdx.x == 64) trace_mark(p.trace, TR_EPI_DONE);
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) trace_mark(p.trace, TR_EXIT);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, L::TMEM_COLS);

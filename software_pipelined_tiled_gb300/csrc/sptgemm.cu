@@ -12,14 +12,17 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <map>
 #include <mutex>
 #include <set>
+#include <tuple>
 #include <string>
 #include <utility>
 
 #include "sptgemm.h"
 
+#include "skinny_cluster_gemm.cuh"  // SkinnyClusterParams
 #include "skinny_gemm.cuh"  // SkinnyParams
 #include "square_gemm.cuh"  // SquareParams
 #include "variants.h"
@@ -32,17 +35,35 @@ namespace {
 using namespace sptg;
 
 thread_local std::string t_last_error;
-thread_local std::string t_last_config;
 thread_local int t_launches = 0;  // kernels this library launched in the current call
 
-void set_config_text(const char* fmt, ...) {
+// What the last call of this thread chose, formatted only when asked for
+// (sptg_last_config), so that a call pays no string formatting.
+struct LastConfig {
+  const char* fmt = "";
+  const char* name = "";
+  long long v[12] = {};
+  int launches = 0;
+};
+thread_local LastConfig t_config;
+
+void set_config(const char* fmt, const char* name, std::initializer_list<long long> vals) {
+  t_config.fmt = fmt;
+  t_config.name = name;
+  int i = 0;
+  for (long long x : vals) {
+    if (i < 12) t_config.v[i++] = x;
+  }
+  for (; i < 12; ++i) t_config.v[i] = 0;
+  t_config.launches = t_launches;
+}
+
+std::string config_text() {
   char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(buf, sizeof(buf), fmt, ap);
-  va_end(ap);
-  t_last_config = buf;
-  t_last_config += " launches=" + std::to_string(t_launches);
+  const long long* v = t_config.v;
+  snprintf(buf, sizeof(buf), t_config.fmt, t_config.name, v[0], v[1], v[2], v[3], v[4], v[5], v[6],
+           v[7], v[8], v[9], v[10], v[11]);
+  return std::string(buf) + " launches=" + std::to_string(t_config.launches);
 }
 
 int cuda_fail(cudaError_t e, const char* what) {
@@ -173,9 +194,56 @@ int scratch_for(int dev, cudaStream_t stream, size_t data_bytes, ScratchView* ou
 }
 
 // ------------------------------------------------------------ tensor maps
+// The last tensor maps this thread encoded, keyed by everything that goes
+// into them: a call on the same buffers and shape reuses them.
+struct MapKey {
+  const void* base;
+  uint64_t inner, outer;
+  uint32_t box_inner, box_outer;
+  int dt, esize, swizzle;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && inner == o.inner && outer == o.outer && box_inner == o.box_inner &&
+           box_outer == o.box_outer && dt == o.dt && esize == o.esize && swizzle == o.swizzle;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool valid = false;
+};
+constexpr int kMapCache = 32;
+thread_local MapEntry t_maps[kMapCache];
+thread_local int t_map_next = 0;
+
+int encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
+                  uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                  CUtensorMapSwizzle swizzle);
+
 int make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
                 uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+  const MapKey key{base, inner, outer, box_inner, box_outer, static_cast<int>(dt), esize,
+                   static_cast<int>(swizzle)};
+  for (const MapEntry& e : t_maps) {
+    if (e.valid && e.key == key) {
+      *map = e.map;
+      return SPTG_OK;
+    }
+  }
+  int rc = encode_map_2d(map, dt, esize, base, inner, outer, box_inner, box_outer, swizzle);
+  if (rc == SPTG_OK) {
+    MapEntry& e = t_maps[t_map_next];
+    t_map_next = (t_map_next + 1) % kMapCache;
+    e.key = key;
+    e.map = *map;
+    e.valid = true;
+  }
+  return rc;
+}
+
+int encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
+                  uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                  CUtensorMapSwizzle swizzle) {
   auto enc = tensor_map_encoder();
   if (!enc) {
     t_last_error = "cuTensorMapEncodeTiled is not available from the driver";
@@ -237,42 +305,54 @@ bool dtype_info(int dtype, DtypeInfo& d) {
 // ------------------------------------------------------------ launching
 // Launches a kernel variant with the given arguments; a CTA-pair variant
 // goes out as clusters of two.
-cudaError_t launch_variant(const KernelVariant& v, int grid, cudaStream_t stream, void** args) {
+// Every launch allows programmatic dependent launch: the kernel may start its
+// set-up while the previous kernel of the stream drains, and waits for that
+// kernel (griddepcontrol.wait) before touching global memory.
+cudaError_t launch_variant(const KernelVariant& v, int grid, cudaStream_t stream, void** args,
+                           bool overlap_previous, int cluster = 0) {
   cudaLaunchConfig_t lc;
   memset(&lc, 0, sizeof(lc));
   lc.gridDim = dim3(grid, 1, 1);
   lc.blockDim = dim3(192, 1, 1);
   lc.dynamicSmemBytes = v.smem;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
-  if (v.pair) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (v.pair || cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = v.pair ? 2 : cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
   }
+  if (overlap_previous) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  lc.attrs = n ? attr : nullptr;
+  lc.numAttrs = n;
   return cudaLaunchKernelExC(&lc, v.fn, args);
 }
 
 // How many CTA pairs of a pair variant can be resident at once.
-std::map<std::pair<int, const void*>, int> g_pair_slots;
+// How many clusters of `cluster` CTAs of a variant can be resident at once.
+std::map<std::tuple<int, const void*, int>, int> g_cluster_slots;
 
-int pair_slots(int dev, const KernelVariant& v, int sm_count) {
+int cluster_slots(int dev, const KernelVariant& v, int cluster, int sm_count) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_pair_slots.find({dev, v.fn});
-    if (it != g_pair_slots.end()) return it->second;
+    auto it = g_cluster_slots.find({dev, v.fn, cluster});
+    if (it != g_cluster_slots.end()) return it->second;
   }
   cudaLaunchConfig_t lc;
   memset(&lc, 0, sizeof(lc));
-  lc.gridDim = dim3(2 * (sm_count / 2), 1, 1);
+  lc.gridDim = dim3(cluster * (sm_count / cluster), 1, 1);
   lc.blockDim = dim3(192, 1, 1);
   lc.dynamicSmemBytes = v.smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   lc.attrs = attr;
@@ -280,11 +360,15 @@ int pair_slots(int dev, const KernelVariant& v, int sm_count) {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, v.fn, &lc) != cudaSuccess || n <= 0) {
     cudaGetLastError();
-    n = sm_count / 2;
+    n = sm_count / cluster;
   }
   std::lock_guard<std::mutex> lk(g_mu);
-  g_pair_slots[{dev, v.fn}] = n;
+  g_cluster_slots[{dev, v.fn, cluster}] = n;
   return n;
+}
+
+int pair_slots(int dev, const KernelVariant& v, int sm_count) {
+  return cluster_slots(dev, v, 2, sm_count);
 }
 
 // ------------------------------------------------------------ square path
@@ -376,20 +460,21 @@ int run_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   p.error_word = di.error_word;
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;
+  p.trace = static_cast<unsigned long long*>(cfg.trace);
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   int workers = pair ? pair_slots(dev, v, di.sm_count) : di.sm_count;
   if (cfg.splits > 0) workers = std::min(workers, cfg.splits);
   workers = std::min(workers, tiles);
   const int grid = pair ? 2 * workers : workers;
   void* args[] = {&ta, &tb, &tc, &p};
-  cudaError_t e = launch_variant(v, grid, stream, args);
+  cudaError_t e = launch_variant(v, grid, stream, args, !cfg.no_overlap);
   ++t_launches;
   if (e != cudaSuccess) return cuda_fail(e, "square_gemm launch");
-  set_config_text(
-      "kernel=square dtype=%s tile_m=%d bn=%d bk=%d stages=%d pair=%d grid=%d tiles=%d "
-      "k_tiles=%d chunk_k_tiles=%d smem=%d",
-      d.name, tile_m, v.bn, BK, v.stages, pair ? 1 : 0, grid, tiles, p.num_k_tiles,
-      p.k_tiles_per_chunk, v.smem);
+  set_config(
+      "kernel=square dtype=%s tile_m=%lld bn=%lld bk=%lld stages=%lld pair=%lld grid=%lld "
+      "tiles=%lld k_tiles=%lld chunk_k_tiles=%lld smem=%lld",
+      d.name, {tile_m, v.bn, BK, v.stages, pair ? 1 : 0, grid, tiles, p.num_k_tiles,
+               p.k_tiles_per_chunk, v.smem});
   return SPTG_OK;
 }
 
@@ -451,6 +536,7 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   p.error_word = di.error_word;
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;
+  p.trace = static_cast<unsigned long long*>(cfg.trace);
 
   // Scratch: fp32 partial tiles [n_tile][contributor][MN x 128] then one
   // arrival counter per n-tile (zeroed here, and re-zeroed by the last arrival).
@@ -493,14 +579,78 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
     p.generation = 0;
   }
   void* args[] = {&tb, &ta, &p};
-  cudaError_t e = launch_variant(v, grid, stream, args);
+  cudaError_t e = launch_variant(v, grid, stream, args, !cfg.no_overlap);
   ++t_launches;
   if (e != cudaSuccess) return cuda_fail(e, "skinny_gemm launch");
-  set_config_text(
-      "kernel=skinny dtype=%s mma_m=%d mma_n=%d bk=%d stages=%d grid=%d n_tiles=%d k_tiles=%d "
-      "units=%lld max_contrib=%d smem=%d",
-      d.name, BNT, v.bn, BK, v.stages, grid, p.num_n_tiles, p.num_k_tiles, (long long)units,
-      max_contrib, v.smem);
+  set_config(
+      "kernel=skinny dtype=%s mma_m=%lld mma_n=%lld bk=%lld stages=%lld grid=%lld n_tiles=%lld "
+      "k_tiles=%lld units=%lld max_contrib=%lld smem=%lld",
+      d.name, {BNT, v.bn, BK, v.stages, grid, p.num_n_tiles, p.num_k_tiles, (long long)units,
+               max_contrib, v.smem});
+  return SPTG_OK;
+}
+
+// The skinny product with K split inside clusters: one cluster of `cs` CTAs
+// per 128-column tile. Returns SPTG_ERR_CONFIG (and launches nothing) when
+// the shape does not suit it, so that the caller can use the stream-K kernel.
+int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N,
+                       int64_t K, const void* A, const void* B, void* C, cudaStream_t stream,
+                       const sptg_config& cfg, bool forced) {
+  KernelVariant v;
+  if (d.is_int8 || !skinny_cluster_variant(d.in_bf16, d.out_kind, cfg.stages, &v) || M > v.bn) {
+    if (forced) t_last_error = "no cluster-split skinny variant for the requested dtype/stages/M";
+    return SPTG_ERR_CONFIG;
+  }
+  const int BNT = 128, BK = 64;
+  const int n_tiles = static_cast<int>((N + BNT - 1) / BNT);
+  const int k_tiles = static_cast<int>((K + BK - 1) / BK);
+  // cluster size: forced (splits), else the largest of 8, 4, 2, 1 whose grid
+  // fits the SMs, taken only if it fills at least three quarters of them
+  int cs = 0;
+  if (forced && cfg.splits > 0) {
+    cs = cfg.splits;
+    if (cs > 8 || (cs & (cs - 1)) != 0) {
+      t_last_error = "cluster size must be 1, 2, 4 or 8";
+      return SPTG_ERR_CONFIG;
+    }
+  } else {
+    for (int c : {8, 4, 2, 1}) {
+      if (static_cast<int64_t>(n_tiles) * c <= di.sm_count && k_tiles >= 2 * c) {
+        cs = c;
+        break;
+      }
+    }
+    if (cs == 0 || (!forced && static_cast<int64_t>(n_tiles) * cs * 4 < 3 * di.sm_count))
+      return SPTG_ERR_CONFIG;
+  }
+  int rc = ensure_smem(dev, v.fn, v.smem);
+  if (rc) return rc;
+  if (cs > 1 && !forced && cluster_slots(dev, v, cs, di.sm_count) < n_tiles) return SPTG_ERR_CONFIG;
+  CUtensorMap tb, ta;
+  rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT);
+  if (rc) return rc;
+  rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.bn);
+  if (rc) return rc;
+  SkinnyClusterParams p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_n_tiles = n_tiles;
+  p.num_k_tiles = k_tiles;
+  p.C = C;
+  p.error_word = di.error_word;
+  p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
+  p.inject_stall = cfg.inject_stall;
+  p.trace = static_cast<unsigned long long*>(cfg.trace);
+  const int grid = n_tiles * cs;
+  void* args[] = {&tb, &ta, &p};
+  cudaError_t e = launch_variant(v, grid, stream, args, !cfg.no_overlap, cs);
+  ++t_launches;
+  if (e != cudaSuccess) return cuda_fail(e, "skinny_cluster_gemm launch");
+  set_config(
+      "kernel=skinny-cluster dtype=%s mma_m=%lld mma_n=%lld bk=%lld stages=%lld grid=%lld "
+      "cluster=%lld n_tiles=%lld k_tiles=%lld smem=%lld",
+      d.name, {BNT, v.bn, BK, v.stages, grid, cs, n_tiles, k_tiles, v.smem});
   return SPTG_OK;
 }
 
@@ -562,12 +712,13 @@ const char* sptg_status_string(int status) {
 const char* sptg_last_error(void) { return t_last_error.c_str(); }
 
 int sptg_last_config(char* buf, size_t len) {
+  const std::string text = config_text();
   if (buf && len) {
-    size_t n = std::min(len - 1, t_last_config.size());
-    memcpy(buf, t_last_config.data(), n);
+    size_t n = std::min(len - 1, text.size());
+    memcpy(buf, text.data(), n);
     buf[n] = '\0';
   }
-  return static_cast<int>(t_last_config.size());
+  return static_cast<int>(text.size());
 }
 
 int sptg_device_error(void* stream) {
@@ -607,14 +758,15 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
     t_last_error = "dimensions must be in [0, 2^31)";
     return SPTG_ERR_ARG;
   }
-  if (cfg.kernel < 0 || cfg.kernel > 2 || cfg.stages < 0 || cfg.bn < 0 || cfg.splits < 0 ||
+  if (cfg.kernel < 0 || cfg.kernel > 3 || cfg.stages < 0 || cfg.bn < 0 || cfg.splits < 0 ||
       cfg.timeout_ms < 0 || (cfg.inject_stall != 0 && cfg.inject_stall != 1) ||
-      cfg.cta_pair < 0 || cfg.cta_pair > 2) {
+      cfg.cta_pair < 0 || cfg.cta_pair > 2 || (cfg.no_overlap != 0 && cfg.no_overlap != 1) ||
+      (cfg.trace && (reinterpret_cast<uintptr_t>(cfg.trace) & 7u))) {
     t_last_error = "invalid configuration field";
     return SPTG_ERR_ARG;
   }
   if (M == 0 || N == 0) {
-    set_config_text("kernel=none dtype=%s (empty output)", d.name);
+    set_config("kernel=none dtype=%s (empty output)", d.name, {});
     return SPTG_OK;
   }
   if (!C || (K > 0 && (!A || !B))) {
@@ -635,14 +787,21 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
   if (K == 0) {  // the empty sum
     cudaError_t e = cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * d.out_bytes, stream_h);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
-    set_config_text("kernel=zero-fill dtype=%s", d.name);
+    set_config("kernel=zero-fill dtype=%s", d.name, {});
     return SPTG_OK;
   }
 
   // Shape class: few output rows and a float type -> the memory-bound
   // swap-AB kernel; everything else -> the square tile kernel.
   int kernel = cfg.kernel;
-  if (kernel == 0) kernel = (!d.is_int8 && M <= 64 && N >= 1024) ? 2 : 1;
+  if (kernel == 0 && !d.is_int8 && M <= 64 && N >= 1024) {
+    // memory-bound: the cluster split when it fills the GPU, else stream-K
+    rc = run_skinny_cluster(dev, di, d, M, N, K, A, B, C, stream_h, cfg, false);
+    if (rc != SPTG_ERR_CONFIG) return rc;
+    kernel = 2;
+  }
+  if (kernel == 0) kernel = 1;
+  if (kernel == 3) return run_skinny_cluster(dev, di, d, M, N, K, A, B, C, stream_h, cfg, true);
   if (kernel == 2) return run_skinny(dev, di, d, M, N, K, A, B, C, stream_h, cfg);
 
   if (d.is_int8) {
@@ -688,7 +847,7 @@ int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype, const v
     return SPTG_ERR_CONFIG;
   }
   if (M == 0 || N == 0) {
-    set_config_text("kernel=none dtype=%s (empty output)", d.name);
+    set_config("kernel=none dtype=%s (empty output)", d.name, {});
     return SPTG_OK;
   }
   if (!C || (K > 0 && (!A || !B))) {
@@ -708,7 +867,7 @@ int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype, const v
   if (K == 0) {
     cudaError_t e = cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * d.out_bytes, stream_h);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
-    set_config_text("kernel=zero-fill dtype=%s", d.name);
+    set_config("kernel=zero-fill dtype=%s", d.name, {});
     return SPTG_OK;
   }
   unsigned char* base = nullptr;

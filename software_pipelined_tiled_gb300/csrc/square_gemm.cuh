@@ -58,7 +58,8 @@ struct SquareParams {
   int group_m;            // raster strip height in m-tiles
   unsigned int* error_word;
   uint64_t timeout_ns;
-  int inject_stall;  // test hook: withhold the load of the second K-tile
+  int inject_stall;
+  unsigned long long* trace;  // optional timeline (see TraceEvent), or null  // test hook: withhold the load of the second K-tile
 };
 
 template <int BN, int STAGES, bool INT_EXACT, bool PAIR>
@@ -146,6 +147,10 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // kernel parameters, not written by earlier kernels: fetch them early
+    prefetch_tensor_map(&tmA);
+    prefetch_tensor_map(&tmB);
+    prefetch_tensor_map(&tmC);
   }
   if (warp == 1) {
     tmem_alloc_g<PAIR>(smem_addr(tmem_slot), L::TMEM_COLS);
@@ -158,6 +163,10 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Set-up above may overlap the previous kernel in the stream; no global
+  // memory is touched before that kernel has completed.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) trace_mark(p.trace, TR_SETUP);
 
   const WaitCtl ctl{p.timeout_ns, p.error_word, abort_flag};
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
@@ -169,8 +178,6 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tensor_map(&tmA);
-      prefetch_tensor_map(&tmB);
       const uint64_t pol = policy_evict_last();  // operands are re-read by other tiles
       int issued_round[STAGES];
       for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
@@ -202,8 +209,12 @@ __global__ void __launch_bounds__(192, 1)
             tma_load_2d(sB + s * L::B_STAGE, &tmB, full_bar(s), kt * BK, b_row, pol);
           }
           issued_round[s] = static_cast<int>(round);
+          if (it == 0) trace_mark(p.trace, TR_FIRST_LOAD);
+          trace_ktile(p.trace, 0, it);
         }
       }
+      trace_mark(p.trace, TR_LAST_LOAD);
+      grid_launch_dependents();  // the next kernel may start its set-up
       if (!ok) {
         // Let every copy already issued land before the CTA can exit.
         if (!PAIR || rank == 0) {
@@ -248,6 +259,8 @@ __global__ void __launch_bounds__(192, 1)
               break;
             }
             tc_fence_after();
+            if (it == 0) trace_mark(p.trace, TR_FIRST_DATA);
+            trace_ktile(p.trace, 1, it);
             const uint32_t a_addr = sA + s * L::A_STAGE;
             const uint32_t b_addr = sB + s * L::B_STAGE;
 #pragma unroll
@@ -261,6 +274,7 @@ __global__ void __launch_bounds__(192, 1)
           if (ok) mma_commit_g<PAIR>(tfull_bar(b));  // accumulator b holds the finished chunk
         }
       }
+      trace_mark(p.trace, TR_LAST_MMA);
       // Drain: every MMA issued above has completed before tensor memory is freed.
       mma_commit_local_g<PAIR>(drain_bar);
       const uint64_t t0 = global_timer_ns();
@@ -387,6 +401,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     if (lane == 0) bulk_wait_group_all();
+    if (warp == 2 && lane == 0) trace_mark(p.trace, TR_EPI_DONE);
   }
 
   tc_fence_before();
@@ -394,6 +409,7 @@ __global__ void __launch_bounds__(192, 1)
     cluster_sync();  // no CTA leaves while its peer may still signal its barriers
   else
     __syncthreads();
+  if (threadIdx.x == 0) trace_mark(p.trace, TR_EXIT);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_g<PAIR>(tmem_base, L::TMEM_COLS);

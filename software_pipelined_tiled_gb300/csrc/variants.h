@@ -28,6 +28,8 @@ bool square_variant_bf16_f32(int bn, int stages, bool pair, KernelVariant* v);
 bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v);
 // Skinny kernel (in_bf16 selects bfloat16 inputs, else binary16).
 bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
+// Skinny kernel with K split inside a cluster (launched in clusters of 2-8).
+bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
 // int8 -> binary16 widening of n16 groups of 16 elements.
 cudaError_t launch_s8_to_f16(const void* src, void* dst, int64_t n16, int blocks,
                              cudaStream_t stream);

@@ -247,6 +247,36 @@ def test_skinny_split_and_ragged(M, N, K, splits):
     assert_float_parity(C, A, B)
 
 
+@pytest.mark.parametrize("M,N,K,cs", [
+    (64, 8192, 4096, 2), (64, 4096, 2048, 4), (17, 1000, 1000, 2), (1, 2048, 1040, 8),
+    (40, 768, 520, 1), (64, 256, 64, 2)])
+def test_skinny_cluster_split(M, N, K, cs):
+    A, B = make_inputs(M, N, K, "bf16", "normal", M * 3 + K)
+    C = run(A, B, BF16, kernel="skinny_cluster", splits=cs)
+    assert "kernel=skinny-cluster" in sptg.last_config() and f"cluster={cs}" in sptg.last_config()
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("T", [2, 3, 8, 17])
+@pytest.mark.parametrize("cs", [2, 4])
+def test_k_tile_marker_skinny_cluster(T, cs):
+    # every rank's K-range lands in the sum exactly once
+    A, B, expect = _marker_inputs(64, 1024, T * cs, dtype=BF16)
+    C = run(A, B, F32, kernel="skinny_cluster", splits=cs)
+    assert (C.to(torch.float64) == expect).all()
+
+
+def test_skinny_cluster_matches_stream_k_and_is_deterministic():
+    A, B = make_inputs(64, 8192, 8192, "bf16", "normal", 19)
+    c1 = run(A, B, F32, kernel="skinny_cluster", splits=2)
+    c2 = run(A, B, F32, kernel="skinny_cluster", splits=2)
+    assert torch.equal(c1, c2)
+    assert_float_parity(c1, A, B)
+    for pair in (("f16", F16), ("f16", F32)):
+        A2, B2 = make_inputs(48, 4096, 2048, pair[0], "uniform", 20)
+        assert_float_parity(run(A2, B2, pair[1], kernel="skinny_cluster", splits=4), A2, B2)
+
+
 def test_skinny_is_deterministic():
     A, B = make_inputs(64, 4096, 4096, "bf16", "normal", 9)
     c1 = run(A, B, F32, kernel="skinny")
@@ -271,7 +301,7 @@ def test_async_on_a_side_stream():
     assert_float_parity(C.cpu(), A, B)
 
 
-@pytest.mark.parametrize("kernel,pair", [(1, 1), (1, 2), (2, 0)])
+@pytest.mark.parametrize("kernel,pair", [(1, 1), (1, 2), (2, 0), (3, 0)])
 def test_bounded_wait_reports_timeout_and_context_survives(kernel, pair):
     # The producer withholds one K-tile; the consumer's wait runs out after
     # 100 ms, the kernel tears down, and the host reads SPTG_ERR_TIMEOUT.
@@ -279,12 +309,44 @@ def test_bounded_wait_reports_timeout_and_context_survives(kernel, pair):
     A, B = make_inputs(M, 1024, 1024, "bf16", "normal", 30)
     dA, dB = A.cuda(), B.cuda()
     C = torch.empty(M, 1024, dtype=BF16, device="cuda")
-    cfg = sptg.Config(kernel, 0, 0, 4, 100, 1, pair)
+    cfg = sptg.Config(kernel, 0, 0, 2 if kernel == 3 else 4, 100, 1, pair)
     rc = sptg.gemm_raw(M, 1024, 1024, "bf16_bf16", dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
                        torch.cuda.current_stream().cuda_stream, cfg)
     assert rc == 0
     assert sptg.device_error() == -5
     assert sptg.device_error() == 0  # the word was cleared
     # the context still works
-    C = run(A, B, BF16, kernel="square" if kernel == 1 else "skinny")
+    C = run(A, B, BF16, kernel={1: "square", 2: "skinny", 3: "skinny_cluster"}[kernel])
     assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("kernel,cta_pair", [("square", 1), ("square", 2), ("skinny", 0),
+                                             ("skinny_cluster", 0)])
+def test_timeline_trace_is_ordered(kernel, cta_pair):
+    # the optional in-kernel timeline: per CTA the events come in pipeline
+    # order, and CTA 0's K-tiles are consumed after they were issued
+    M = 64 if kernel.startswith("skinny") else 512
+    A, B = make_inputs(M, 2048, 2048, "bf16", "normal", 31)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty(M, 2048, dtype=BF16, device="cuda")
+    buf = torch.zeros(8 * 1024 + 128, dtype=torch.int64, device="cuda")
+    cfg = sptg.Config(sptg.KERNELS[kernel], 0, 0, 2 if kernel == "skinny_cluster" else 0, 0, 0,
+                      cta_pair)
+    cfg.trace = buf.data_ptr()
+    sptg.gemm(dA, dB, C=C, config=cfg)
+    torch.cuda.synchronize()
+    assert sptg.device_error() == 0
+    grid = int(sptg.last_config().split("grid=")[1].split()[0])
+    t = buf.cpu().numpy()
+    ev = t[:8 * 1024].reshape(1024, 8)[:grid]
+    assert (ev[:, 0] > 0).all() and (ev[:, 6] > 0).all()
+    for row in ev:
+        assert row[0] <= row[1] <= row[3], row       # set-up, first copy, last copy
+        assert row[6] >= row[5] >= row[0], row       # epilogue done before exit
+    leaders = ev[:, 2] > 0
+    assert (ev[leaders, 1] <= ev[leaders, 2]).all()  # data after its copy
+    assert (ev[leaders, 2] <= ev[leaders, 4]).all()
+    issue, full = t[8192:8256], t[8256:8320]
+    n = int((full > 0).sum())
+    assert n > 0 and (full[:n] >= issue[:n]).all()
+    assert_float_parity(C.cpu(), A, B)
