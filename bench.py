@@ -241,8 +241,9 @@ def run_ours(args, w):
     As = [A.to(dev) for _ in range(n_sets)]
     Bs = [B.to(dev) for _ in range(n_sets)]
     Cs = [torch.empty(w.M, w.N, dtype=out_dtype, device=dev) for _ in range(n_sets)]
-    cfg = (sptg.Config(0, args.bn, args.stages, 0, 0, 0, args.cta_pair, int(args.no_overlap))
-           if (args.stages or args.bn or args.cta_pair or args.no_overlap) else None)
+    cfg = (sptg.Config(args.kernel, args.bn, args.stages, 0, 0, 0, args.cta_pair,
+                       int(args.no_overlap))
+           if (args.kernel or args.stages or args.bn or args.cta_pair or args.no_overlap) else None)
     stream = torch.cuda.current_stream()
 
     def step(i):
@@ -357,7 +358,7 @@ def run_ours(args, w):
 
     tl = None
     if args.trace:
-        fields = (0, args.bn, args.stages, 0, 0, 0, args.cta_pair)
+        fields = (args.kernel, args.bn, args.stages, 0, 0, 0, args.cta_pair, int(args.no_overlap))
         tl = timeline(sptg, As[0], Bs[0], Cs[0], fields)
     cpu = None if args.no_cpu_baseline else cpu_baseline(w, A, B)
     clocks = sampler.summary()
@@ -471,6 +472,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--stages", type=int, default=0, help="force the ring depth (ablation)")
     ap.add_argument("--bn", type=int, default=0, help="force the square tile width")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="0 choose, 1 square, 2 skinny stream-K, 3 skinny cluster split")
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="square kernel: 0 choose, 1 one CTA per tile, 2 CTA pair (2-SM MMA)")
     ap.add_argument("--no-e2e", action="store_true")

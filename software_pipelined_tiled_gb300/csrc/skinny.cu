@@ -32,19 +32,21 @@ bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v) {
   }
 }
 
-template <int MN, int ST, bool BF, int OUT>
+template <int MN, bool BF, int OUT>
 KernelVariant make_skinny_cluster() {
+  constexpr int ST = skinny_cluster_stages<MN>();
   return {reinterpret_cast<const void*>(&skinny_cluster_gemm_kernel<MN, ST, BF, OUT>), MN, ST,
-          SkinnyClusterLayout<MN, ST>::SMEM_BYTES, false};
+          SkinnyClusterLayout<MN, ST, OutTraits<OUT>::bytes>::SMEM_BYTES, false};
 }
 
-// MMA N = 64 at an 8-stage ring for every float dtype pair.
+// MMA N = 64 at the deepest ring next to the receive buffer (7 stages), for
+// every float dtype pair.
 bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v) {
-  if (stages != 0 && stages != 8) return false;
-  if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny_cluster<64, 8, true, OUT_BF16>();
-  else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny_cluster<64, 8, false, OUT_F16>();
-  else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny_cluster<64, 8, true, OUT_F32>();
-  else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny_cluster<64, 8, false, OUT_F32>();
+  if (stages != 0 && stages != skinny_cluster_stages<64>()) return false;
+  if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny_cluster<64, true, OUT_BF16>();
+  else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny_cluster<64, false, OUT_F16>();
+  else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny_cluster<64, true, OUT_F32>();
+  else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny_cluster<64, false, OUT_F32>();
   else return false;
   return true;
 }

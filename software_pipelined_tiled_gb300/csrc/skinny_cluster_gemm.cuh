@@ -1,19 +1,21 @@
 // skinny_cluster_gemm.cuh -- the memory-bound skinny product (M <= 64) with
-// its K split inside a thread-block cluster.
+// its K split across the two CTAs of a thread-block cluster.
 //
 // Same arithmetic as skinny_gemm.cuh (swap-AB: D^T[n, m] = sum_k Bcm[n, k] *
 // A[m, k], MMA M = 128 over N, MMA N = MN over the rows of A), but the work
-// is cut along whole column tiles: one cluster of CS CTAs per 128-column tile,
-// CTA rank r streaming the contiguous K-range [r*KT/CS, (r+1)*KT/CS). Each
-// CTA accumulates its range in tensor memory. When all have finished, ranks
-// 1..CS-1 leave their fp32 partial tile in their own shared memory and rank 0
-// reads them through distributed shared memory, adds them in rank order
-// (= increasing k, a fixed order) to its own, converts and writes C.
+// is cut along whole column tiles: one cluster of CS (1 or 2) CTAs per
+// 128-column tile, CTA rank r streaming the contiguous K-range
+// [r*KT/CS, (r+1)*KT/CS). Each CTA accumulates its range in tensor memory.
+// Then each rank finalises one half of the columns: it pushes the partial of
+// the other half straight into the peer's receive buffer (distributed shared
+// memory stores) and arrives on a barrier there, adds the half it received to
+// its own (two fp32 terms: the same bits in either order), converts, stages
+// its output block in shared memory and writes it with one tensor-copy store.
 //
 // Compared with the stream-K kernel this needs no global scratch and no
-// atomics, and the final reduction is one exchange between SMs of a cluster
-// instead of a round trip through L2. The price is that the grid is
-// (column tiles x CS) CTAs, which the host uses when that fills the GPU.
+// atomics: the reduction is one push between the two SMs of a cluster. The
+// grid is (column tiles x CS) CTAs, which the host uses when that fills the
+// GPU.
 #pragma once
 
 #include "common.cuh"
@@ -23,47 +25,50 @@ namespace sptg {
 struct SkinnyClusterParams {
   int M, N, K;
   int num_n_tiles, num_k_tiles;
-  void* C;  // row-major M x N output
   unsigned int* error_word;
   uint64_t timeout_ns;
   int inject_stall;
   unsigned long long* trace;
 };
 
-template <int MN, int STAGES>
+template <int MN, int STAGES, int OBYTES>
 struct SkinnyClusterLayout {
   static constexpr int BNT = 128;
   static constexpr int BK = 64;
   static constexpr int BT_STAGE = BNT * BK * 2;
   static constexpr int A_STAGE = MN * BK * 2;
   static constexpr int STAGE = BT_STAGE + A_STAGE;
-  // partial tile in shared memory, rows of MN floats + 16 bytes of padding
-  // so that 16-byte accesses of 8 consecutive rows hit 8 distinct bank groups
+  // receive buffer for the peer's partial: a row of MN floats per output
+  // column, plus 16 bytes so that 16-byte accesses of 8 consecutive rows hit
+  // 8 distinct bank groups
   static constexpr int PART_ROW = MN * 4 + 16;
   static constexpr int PART_BYTES = BNT * PART_ROW;
-  static constexpr int OFF_BAR = STAGES * STAGE;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 + 1;
+  // output staging (reuses the receive buffer once it has been read): MN rows
+  // of 128 outputs, the layout of C
+  static constexpr int OUT_BYTES = MN * BNT * OBYTES;
+  static constexpr int OFF_PART = STAGES * STAGE;
+  static constexpr int OFF_BAR = OFF_PART + PART_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 3;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int TMEM_COLS = MN <= 32 ? 32 : MN <= 64 ? 64 : 128;
-  static_assert(PART_BYTES <= STAGES * STAGE, "the partial tile reuses the ring's memory");
+  static_assert(OUT_BYTES <= PART_BYTES, "output staging reuses the receive buffer");
+  static_assert(OFF_PART % 1024 == 0, "receive buffer alignment");
   static_assert(MN % 32 == 0 && MN >= 32 && MN <= 128, "MN must be 32, 64, 96 or 128");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 };
 
-__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t cluster_addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(cluster_addr)
-               : "memory");
-  return v;
+// Deepest ring next to the receive buffer within the 227 KB budget.
+template <int MN>
+constexpr int skinny_cluster_stages() {
+  return (232448 - 1024 - 128 * (MN * 4 + 16) - 512) / (128 * 64 * 2 + MN * 64 * 2);
 }
 
-__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-  return v;
+// 16-byte store into the shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_shared_cluster_f4(uint32_t cluster_addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_nctarank() {
@@ -76,8 +81,10 @@ template <int MN, int STAGES, bool IN_BF16, int OUT>
 __global__ void __launch_bounds__(192, 1)
     skinny_cluster_gemm_kernel(const __grid_constant__ CUtensorMap tmBt,
                                const __grid_constant__ CUtensorMap tmA,
+                               const __grid_constant__ CUtensorMap tmC,
                                const SkinnyClusterParams p) {
-  using L = SkinnyClusterLayout<MN, STAGES>;
+  constexpr int OBYTES = OutTraits<OUT>::bytes;
+  using L = SkinnyClusterLayout<MN, STAGES, OBYTES>;
   constexpr int BNT = L::BNT, BK = L::BK;
   constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, BNT, MN);
   static_assert(OUT != OUT_S32, "float outputs only");
@@ -87,19 +94,21 @@ __global__ void __launch_bounds__(192, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bar0 = sbase + L::OFF_BAR;
+  uint8_t* part = smem + L::OFF_PART;
   auto stage_bt = [&](int s) { return sbase + s * L::STAGE; };
   auto stage_a = [&](int s) { return sbase + s * L::STAGE + L::BT_STAGE; };
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 1);
+  const uint32_t recv_bar = bar0 + 8u * (2 * STAGES + 2);  // the peer's half partial is in
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t cs = cluster_nctarank();
+  const uint32_t cs = cluster_nctarank();  // 1 or 2
   const uint32_t rank = cluster_ctarank();
   const int nt = static_cast<int>(blockIdx.x / cs);
   const int KT = p.num_k_tiles;
@@ -113,20 +122,34 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
+    mbar_init(recv_bar, 64);  // one arrival per pushing thread of the peer
     *abort_flag = 0;
     *failed = 0;
     fence_mbar_init();
     prefetch_tensor_map(&tmBt);
     prefetch_tensor_map(&tmA);
+    prefetch_tensor_map(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (cs > 1)
+    cluster_sync();  // rank 0's receive barrier exists before the peer can arrive on it
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Warm L2 with this CTA's first stages while the previous kernel drains.
+  // L2 is where writes become coherent, so this is safe even if that kernel
+  // writes these operands: the loads proper come after the dependency wait.
+  if (threadIdx.x == 0) {
+    for (int kt = kt0; kt < min(kt1, kt0 + STAGES); ++kt) {
+      tma_prefetch_l2_2d(&tmBt, kt * BK, nt * BNT);
+      tma_prefetch_l2_2d(&tmA, kt * BK, 0);
+    }
+  }
   grid_dependency_wait();
   if (threadIdx.x == 0) trace_mark(p.trace, TR_SETUP);
 
@@ -198,17 +221,15 @@ __global__ void __launch_bounds__(192, 1)
       while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < ctl.timeout_ns) {
       }
     }
-  }
-
-  // ---------------------------------------------------------- epilogue part 1
-  // warps 2-5 read this CTA's partial tile (their 32 lanes each = 32 output
-  // columns, MN values per column) out of tensor memory
-  float acc[MN];
-  const int q = warp & 3;
-  const int n_local = 32 * q + lane;
-  if (warp >= 2) {
-    const bool done =
-        __all_sync(0xffffffffu, wait_bounded(tfull_bar, 0, ctl, WAIT_EPI_TMEM_FULL));
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // warps 2-5: each lane owns one output column (a row of D^T) and reads its
+    // MN fp32 values out of tensor memory
+    const int q = warp & 3;
+    const int n_local = 32 * q + lane;
+    float acc[MN];
+    const bool done = __all_sync(0xffffffffu, wait_bounded(tfull_bar, 0, ctl, WAIT_EPI_TMEM_FULL));
+    const bool mine_ok = __all_sync(0xffffffffu, done && !*failed);
     if (done) {
       tc_fence_after();
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
@@ -216,55 +237,88 @@ __global__ void __launch_bounds__(192, 1)
       for (int cb = 0; cb < MN / 32; ++cb) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_lane + 32 * cb, r);
-        tmem_wait_ld();
+        tmem_wait_ld_regs(r);
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           acc[32 * cb + i] = (kt1 > kt0) ? __uint_as_float(r[i]) : 0.0f;
       }
-      if (rank != 0) {
-        // leave the partial in this CTA's own shared memory (the ring is idle:
-        // every stage has been consumed) for rank 0 to read
-        uint8_t* row = smem + n_local * L::PART_ROW;
+    }
+    // With two ranks each finalises half of the 128 columns: rank 0 columns
+    // 0-63, rank 1 columns 64-127. A warp whose 32 columns belong to the other
+    // rank pushes its partial into that rank's receive buffer (distributed
+    // shared memory stores) and arrives on its barrier (release, cluster
+    // scope: each thread covers its own stores); the two halves move at once.
+    // A rank that failed does not arrive, and the peer's bounded wait gives up.
+    const int half = q >> 1;              // which 64 columns this warp holds
+    const bool keep = (cs == 1) || (half == static_cast<int>(rank));
+    const int col = (cs == 1) ? n_local : (n_local & 63);  // column within the kept block
+    const int keep_threads = (cs == 1) ? 128 : 64;
+    if (!keep) {
+      if (mine_ok) {
+        const uint32_t dst = map_to_cta(smem_addr(part + col * L::PART_ROW), rank ^ 1u);
 #pragma unroll
         for (int i = 0; i < MN / 4; ++i)
-          *reinterpret_cast<float4*>(row + 16 * i) =
-              make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+          st_shared_cluster_f4(dst + 16 * i,
+                               make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]));
+        mbar_arrive_cluster(map_to_cta(recv_bar, rank ^ 1u));
       }
-    } else if (lane == 0) {
-      *failed = 1;
-    }
-  }
-  tc_fence_before();
-  cluster_sync();  // every partial and every failure flag of the cluster is visible
-
-  // ---------------------------------------------------------- epilogue part 2
-  if (warp >= 2 && rank == 0) {
-    // the result is written only when no CTA of the cluster gave up a wait
-    bool all_ok = (*failed == 0);
-    for (uint32_t r = 1; r < cs; ++r)
-      all_ok = all_ok && ld_shared_cluster_u32(map_to_cta(smem_addr(const_cast<int*>(failed)), r)) == 0;
-    if (all_ok) {
-      for (uint32_t r = 1; r < cs; ++r) {  // rank order = increasing k: a fixed sum order
-        const uint32_t peer_row = map_to_cta(smem_addr(smem + n_local * L::PART_ROW), r);
+    } else {
+      bool ok = mine_ok;
+      if (cs > 1) {
+        ok = named_barrier_and(1, keep_threads,
+                               ok && wait_bounded(recv_bar, 0, ctl, WAIT_EPI_TMEM_FULL));
+        if (ok) {
+          // two partials: their fp32 sum is the same in either order
+          const uint8_t* row = part + col * L::PART_ROW;
+          float4 v[MN / 4];
 #pragma unroll
-        for (int i = 0; i < MN / 4; ++i) {
-          const float4 v = ld_shared_cluster_f4(peer_row + 16 * i);
-          acc[4 * i] += v.x;
-          acc[4 * i + 1] += v.y;
-          acc[4 * i + 2] += v.z;
-          acc[4 * i + 3] += v.w;
+          for (int i = 0; i < MN / 4; ++i) v[i] = *reinterpret_cast<const float4*>(row + 16 * i);
+#pragma unroll
+          for (int i = 0; i < MN / 4; ++i) {
+            acc[4 * i] += v[i].x;
+            acc[4 * i + 1] += v[i].y;
+            acc[4 * i + 2] += v[i].z;
+            acc[4 * i + 3] += v[i].w;
+          }
+        }
+        named_barrier_sync(1, keep_threads);  // the receive buffer is read: reuse it for staging
+      } else {
+        ok = named_barrier_and(1, keep_threads, ok);
+      }
+      if (ok) {
+        // stage the kept MN x (128 / cs) block of C (row m holds consecutive
+        // outputs) and store it with one tensor copy; rows past M and
+        // columns past N clip
+        const int width = BNT / static_cast<int>(cs);
+        uint8_t* stage = part;
+#pragma unroll
+        for (int m = 0; m < MN; ++m) {
+          if constexpr (OBYTES == 4) {
+            reinterpret_cast<float*>(stage)[m * width + col] = acc[m];
+          } else if constexpr (OUT == OUT_F16) {
+            reinterpret_cast<__half*>(stage)[m * width + col] = __float2half_rn(acc[m]);
+          } else {
+            reinterpret_cast<__nv_bfloat16*>(stage)[m * width + col] = __float2bfloat16_rn(acc[m]);
+          }
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, keep_threads);
+        const int x0 = nt * BNT + (cs == 1 ? 0 : static_cast<int>(rank) * 64);
+        if (col == 0 && x0 < p.N) {
+          tma_store_2d(&tmC, smem_addr(stage), x0, 0);
+          bulk_commit_group();
+          bulk_wait_group_read<0>();  // the staging may go once the copy has read it
         }
       }
-      const int n = nt * BNT + n_local;
-      if (n < p.N) {
-#pragma unroll
-        for (int m = 0; m < MN; ++m)
-          if (m < p.M) store_out<OUT>(p.C, static_cast<int64_t>(m) * p.N + n, acc[m]);
-      }
+      if (col == 0) trace_mark(p.trace, TR_EPI_DONE);
     }
   }
-  if (threadIdx.x == 64) trace_mark(p.trace, TR_EPI_DONE);
-  cluster_sync();  // peers keep their shared memory until rank 0 has read it
+
+  tc_fence_before();
+  if (cs > 1)
+    cluster_sync();  // the peer's pushes have landed before either CTA leaves
+  else
+    __syncthreads();
   if (threadIdx.x == 0) trace_mark(p.trace, TR_EXIT);
   if (warp == 1) {
     tc_fence_after();

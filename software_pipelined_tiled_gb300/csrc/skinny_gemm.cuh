@@ -138,8 +138,20 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int64_t u_begin0 = static_cast<int64_t>(blockIdx.x) * p.total_units / p.num_ctas;
+  const int64_t u_end0 = static_cast<int64_t>(blockIdx.x + 1) * p.total_units / p.num_ctas;
+  // Warm L2 with this CTA's first stages while the previous kernel drains
+  // (safe: L2 is where writes become coherent; the loads proper wait).
+  if (threadIdx.x == 0) {
+    for (int64_t u = u_begin0; u < min(u_end0, u_begin0 + STAGES); ++u) {
+      const int nt = static_cast<int>(u / p.num_k_tiles);
+      const int kt = static_cast<int>(u - static_cast<int64_t>(nt) * p.num_k_tiles);
+      tma_prefetch_l2_2d(&tmBt, kt * L::BK, nt * L::BNT);
+      tma_prefetch_l2_2d(&tmA, kt * L::BK, 0);
+    }
+  }
   // Set-up above may overlap the previous kernel in the stream; no global
-  // memory is touched before that kernel has completed.
+  // memory is read for use before that kernel has completed.
   grid_dependency_wait();
   if (threadIdx.x == 0) trace_mark(p.trace, TR_SETUP);
 
@@ -255,7 +267,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int cb = 0; cb < MN / 32; ++cb) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_lane + b * MN + 32 * cb, r);
-        tmem_wait_ld();
+        tmem_wait_ld_regs(r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[32 * cb + i] = __uint_as_float(r[i]);
       }

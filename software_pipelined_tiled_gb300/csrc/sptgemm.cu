@@ -604,17 +604,18 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   const int BNT = 128, BK = 64;
   const int n_tiles = static_cast<int>((N + BNT - 1) / BNT);
   const int k_tiles = static_cast<int>((K + BK - 1) / BK);
-  // cluster size: forced (splits), else the largest of 8, 4, 2, 1 whose grid
-  // fits the SMs, taken only if it fills at least three quarters of them
+  // cluster size: forced (splits), else 2 when two CTAs per column tile fit
+  // the SMs, else 1; taken only if the grid fills at least three quarters of
+  // the SMs
   int cs = 0;
   if (forced && cfg.splits > 0) {
     cs = cfg.splits;
-    if (cs > 8 || (cs & (cs - 1)) != 0) {
-      t_last_error = "cluster size must be 1, 2, 4 or 8";
+    if (cs > 2) {
+      t_last_error = "cluster size must be 1 or 2";
       return SPTG_ERR_CONFIG;
     }
   } else {
-    for (int c : {8, 4, 2, 1}) {
+    for (int c : {2, 1}) {
       if (static_cast<int64_t>(n_tiles) * c <= di.sm_count && k_tiles >= 2 * c) {
         cs = c;
         break;
@@ -626,10 +627,15 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   int rc = ensure_smem(dev, v.fn, v.smem);
   if (rc) return rc;
   if (cs > 1 && !forced && cluster_slots(dev, v, cs, di.sm_count) < n_tiles) return SPTG_ERR_CONFIG;
-  CUtensorMap tb, ta;
+  CUtensorMap tb, ta, tc;
   rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT);
   if (rc) return rc;
   rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.bn);
+  if (rc) return rc;
+  // the output block a rank stores: v.bn rows of 128 / cs consecutive
+  // outputs, unswizzled
+  rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, BNT / cs, v.bn,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc) return rc;
   SkinnyClusterParams p;
   p.M = static_cast<int>(M);
@@ -637,13 +643,12 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   p.K = static_cast<int>(K);
   p.num_n_tiles = n_tiles;
   p.num_k_tiles = k_tiles;
-  p.C = C;
   p.error_word = di.error_word;
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;
   p.trace = static_cast<unsigned long long*>(cfg.trace);
   const int grid = n_tiles * cs;
-  void* args[] = {&tb, &ta, &p};
+  void* args[] = {&tb, &ta, &tc, &p};
   cudaError_t e = launch_variant(v, grid, stream, args, !cfg.no_overlap, cs);
   ++t_launches;
   if (e != cudaSuccess) return cuda_fail(e, "skinny_cluster_gemm launch");

@@ -163,17 +163,28 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // Set-up above may overlap the previous kernel in the stream; no global
-  // memory is touched before that kernel has completed.
-  grid_dependency_wait();
-  if (threadIdx.x == 0) trace_mark(p.trace, TR_SETUP);
-
-  const WaitCtl ctl{p.timeout_ns, p.error_word, abort_flag};
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
   const int num_chunks = (p.num_k_tiles + p.k_tiles_per_chunk - 1) / p.k_tiles_per_chunk;
   // the persistent work unit is a CTA, or a CTA pair in PAIR mode
   const int worker = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  // Warm L2 with the first stages of this CTA's first tile while the previous
+  // kernel drains (safe: L2 is where writes become coherent; the loads proper
+  // wait for the dependency).
+  if (threadIdx.x == 0 && worker < num_tiles) {
+    int mt, nt;
+    tile_coords(worker, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+    for (int kt = 0; kt < min(p.num_k_tiles, STAGES); ++kt) {
+      tma_prefetch_l2_2d(&tmA, kt * BK, mt * L::TILE_M + static_cast<int>(rank) * BM);
+      tma_prefetch_l2_2d(&tmB, kt * BK, nt * BN + static_cast<int>(rank) * L::BN_CTA);
+    }
+  }
+  // Set-up above may overlap the previous kernel in the stream; no global
+  // memory is read for use before that kernel has completed.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) trace_mark(p.trace, TR_SETUP);
+
+  const WaitCtl ctl{p.timeout_ns, p.error_word, abort_flag};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -309,13 +320,13 @@ __global__ void __launch_bounds__(192, 1)
           for (int cb = 0; cb < BN / 32; ++cb) {
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_acc + 32 * cb, v);
-            tmem_wait_ld();
+            tmem_wait_ld_regs(v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
             if (c > 0) {
               uint32_t s[32];
               tmem_ld_32x32b_x32(t_sum + 32 * cb, s);
-              tmem_wait_ld();
+              tmem_wait_ld_regs(s);
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(static_cast<int32_t>(v[i]) + static_cast<int32_t>(s[i]));
             }
@@ -348,11 +359,16 @@ __global__ void __launch_bounds__(192, 1)
           // One block = 32 output columns of this warp's 32 rows: 128-byte
           // rows (128-byte swizzle) for 4-byte outputs, 64-byte rows (64-byte
           // swizzle) for 16-bit outputs; the TMA store unswizzles.
+          // The tensor-memory load of block cb+1 is in flight while block cb is
+          // converted, staged and stored.
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_acc, v);
+          tmem_wait_ld_regs(v);
 #pragma unroll 1
           for (int cb = 0; cb < BN / 32; ++cb) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(t_acc + 32 * cb, v);
-            tmem_wait_ld();
+            const bool more = cb + 1 < BN / 32;
+            uint32_t nxt[32];
+            if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
             uint8_t* buf = bufs + (stores & 1u) * L::EPI_BUF;
             if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf is done reading
             __syncwarp();
@@ -388,6 +404,11 @@ __global__ void __launch_bounds__(192, 1)
               bulk_commit_group();
             }
             ++stores;
+            if (more) {
+              tmem_wait_ld_regs(nxt);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = nxt[i];
+            }
           }
         }
         tc_fence_before();
@@ -400,7 +421,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
-    if (lane == 0) bulk_wait_group_all();
+    if (lane == 0) bulk_wait_group_read<0>();  // staging is free once the stores have read it
     if (warp == 2 && lane == 0) trace_mark(p.trace, TR_EPI_DONE);
   }
 

@@ -248,8 +248,8 @@ def test_skinny_split_and_ragged(M, N, K, splits):
 
 
 @pytest.mark.parametrize("M,N,K,cs", [
-    (64, 8192, 4096, 2), (64, 4096, 2048, 4), (17, 1000, 1000, 2), (1, 2048, 1040, 8),
-    (40, 768, 520, 1), (64, 256, 64, 2)])
+    (64, 8192, 4096, 2), (64, 4096, 2048, 2), (17, 1000, 1000, 2), (1, 2048, 1040, 2),
+    (40, 768, 520, 1), (64, 256, 64, 2), (33, 1024, 64, 1)])
 def test_skinny_cluster_split(M, N, K, cs):
     A, B = make_inputs(M, N, K, "bf16", "normal", M * 3 + K)
     C = run(A, B, BF16, kernel="skinny_cluster", splits=cs)
@@ -257,8 +257,8 @@ def test_skinny_cluster_split(M, N, K, cs):
     assert_float_parity(C, A, B)
 
 
-@pytest.mark.parametrize("T", [2, 3, 8, 17])
-@pytest.mark.parametrize("cs", [2, 4])
+@pytest.mark.parametrize("T", [1, 2, 3, 8, 17])
+@pytest.mark.parametrize("cs", [1, 2])
 def test_k_tile_marker_skinny_cluster(T, cs):
     # every rank's K-range lands in the sum exactly once
     A, B, expect = _marker_inputs(64, 1024, T * cs, dtype=BF16)
@@ -274,7 +274,7 @@ def test_skinny_cluster_matches_stream_k_and_is_deterministic():
     assert_float_parity(c1, A, B)
     for pair in (("f16", F16), ("f16", F32)):
         A2, B2 = make_inputs(48, 4096, 2048, pair[0], "uniform", 20)
-        assert_float_parity(run(A2, B2, pair[1], kernel="skinny_cluster", splits=4), A2, B2)
+        assert_float_parity(run(A2, B2, pair[1], kernel="skinny_cluster", splits=2), A2, B2)
 
 
 def test_skinny_is_deterministic():
