@@ -4,7 +4,8 @@ TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the CPU
 baseline of ``bench.py`` may import this package; the library itself never
 does, and the two share no code.
 
-The arithmetic lives in ``oracle_gemm.c`` (a plain triple loop, fp64 sums for
+The arithmetic lives in ``oracle_gemm.c`` (and, for the streaming pipeline
+``out = alpha * in``, ``oracle_stream.c``) (a plain triple loop, fp64 sums for
 binary16/bfloat16 inputs, int64 sums for int8 inputs).  This module builds
 that file with the host C compiler and marshals numpy arrays to it.
 
@@ -31,7 +32,7 @@ IN_F16 = 0
 IN_BF16 = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "oracle_gemm.c")
+_SRCS = [os.path.join(_HERE, "oracle_gemm.c"), os.path.join(_HERE, "oracle_stream.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_gemm.so")
 _lock = threading.Lock()
@@ -42,11 +43,11 @@ def build(force: bool = False) -> str:
     """Compiles oracle_gemm.c for the host (no fast-math, no FMA contraction)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(s) for s in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-           "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+           "-shared", "-fPIC", "-o", tmp, *_SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -67,6 +68,8 @@ def _load():
         lib.oracle_decode_f16.restype = ctypes.c_double
         lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
         lib.oracle_decode_bf16.restype = ctypes.c_double
+        lib.oracle_scale_f32.argtypes = [i64, ctypes.c_float, p, p]
+        lib.oracle_scale_f32.restype = None
         lib.oracle_threads.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         for f in (lib.oracle_gemm_float, lib.oracle_gemm_float_at,
@@ -185,4 +188,15 @@ def gemm_s8_at(A, Bcm, rows, cols):
         raise IndexError("sample position out of range")
     out = np.empty(len(r), dtype=np.int64)
     _load().oracle_gemm_s8_at(M, N, K, _ptr(a), _ptr(b), len(r), _ptr(r), _ptr(c), _ptr(out))
+    return out
+
+
+def scale_f32(x, alpha: float):
+    """out[i] = alpha * in[i] in binary32, one rounding per element."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().contiguous().numpy()
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(a)
+    if a.size:
+        _load().oracle_scale_f32(a.size, float(alpha), _ptr(a), _ptr(out))
     return out
