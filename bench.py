@@ -420,6 +420,56 @@ def timeline(sptg, A, B, C, cfg_fields):
     return out
 
 
+def run_stream(args):
+    """The streaming ring on its own (out = alpha * in, binary32): HBM roofline probe."""
+    import software_pipelined_tiled_gb300 as sptg
+    torch.cuda.set_device(0)
+    n = args.stream
+    nbytes = 8 * n  # read + write
+    n_sets = max(2, -(-3 * L2_BYTES // nbytes) + 1)
+    g = torch.Generator("cpu").manual_seed(1)
+    x = torch.randn(n, generator=g)
+    xs = [x.cuda() for _ in range(n_sets)]
+    ys = [torch.empty_like(xs[0]) for _ in range(n_sets)]
+    for i in range(args.warmup):
+        sptg.stream_scale(xs[i % n_sets], 2.0, out=ys[i % n_sets])
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(0)
+    sampler.start()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        sptg.stream_scale(xs[i % n_sets], 2.0, out=ys[i % n_sets])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    if sptg.device_error() != 0:
+        raise RuntimeError("kernel reported a timed-out wait")
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks, src = measured_peaks()
+    tl = None
+    if args.trace:
+        buf = torch.zeros(TRACE_WORDS, dtype=torch.int64, device="cuda")
+        cfg = sptg.Config()
+        cfg.trace = buf.data_ptr()
+        sptg.stream_scale(xs[0], 2.0, out=ys[0], config=cfg)
+        torch.cuda.synchronize()
+        tl = buf[:16].cpu().tolist()
+    return {"metric": "stream scale GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"stream_scale_f32_n{n}", "kernel": sptg.last_config(),
+                       "l2": f"{n_sets} rotating buffer pairs of {nbytes / 2**20:.0f} MiB"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{src} copy bandwidth",
+                         "traffic": None, "algorithmic_bytes": nbytes},
+            "clocks": sampler.summary(), "gpu_launches": args.steps}
+
+
 def run_reference(args, w):
     """The CPU oracle as the reference arm (rank 0 only)."""
     rank = int(os.environ.get("RANK", "0"))
@@ -477,6 +527,8 @@ def main(argv=None):
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="square kernel: 0 choose, 1 one CTA per tile, 2 CTA pair (2-SM MMA)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--stream", type=int, default=0,
+                    help="time the streaming ring out = 2 * in over this many binary32 values")
     ap.add_argument("--graph", action="store_true",
                     help="capture the timed steps as one CUDA graph and replay it")
     ap.add_argument("--no-overlap", action="store_true",
@@ -494,7 +546,10 @@ def main(argv=None):
                      "int8" if pair.startswith("s8") else "uniform", 1.0, 1)
     else:
         w = WORKLOADS[args.workload]
-    line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if args.stream:
+        line = run_stream(args)
+    else:
+        line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)
     if args.impl == "ours" and int(os.environ.get("WORLD_SIZE", "1")) > 1:

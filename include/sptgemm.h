@@ -111,6 +111,25 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype,
                  const void* A, const void* B, void* C, void* stream,
                  const sptg_config* cfg);
 
+/*
+ * The software-pipelined ring on its own: out[i] = alpha * in[i] for
+ * i < n, binary32, one rounding per element. This is the minimal working
+ * example of "Hiding Memory Latency in CUDA: Asynchronous Loads and Software
+ * Pipelines" (section 8: a vector streamed through a multi-stage
+ * shared-memory ring and scaled by two), here for any alpha; it measures the
+ * copy pipeline against memory bandwidth.
+ *
+ * in and out are device pointers, 16-byte aligned (else SPTG_ERR_ALIGN),
+ * and may be the same buffer (in place); they must not otherwise overlap.
+ * n >= 0 of any size (n == 0: nothing). Asynchronous on `stream`.
+ */
+int sptg_stream_scale(int64_t n, float alpha, const float* in, float* out, void* stream);
+
+/* sptg_stream_scale with the timeout_ms, inject_stall, no_overlap and trace
+ * fields of a configuration (the others are ignored; NULL = defaults). */
+int sptg_stream_scale_ex(int64_t n, float alpha, const float* in, float* out, void* stream,
+                         const sptg_config* cfg);
+
 /* Static text for a status code. */
 const char* sptg_status_string(int status);
 

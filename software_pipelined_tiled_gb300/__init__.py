@@ -20,6 +20,7 @@ import threading
 from ._build import LIB_PATH, build
 
 __all__ = ["DTYPES", "SptgError", "Config", "load", "gemm", "gemm_raw", "gemm_skinny_noalloc_raw",
+           "stream_scale",
            "last_config",
            "last_error", "device_error", "status_string", "LIB_PATH", "build"]
 
@@ -32,7 +33,8 @@ KERNELS = {"auto": 0, "square": 1, "skinny": 2, "skinny_cluster": 3}
 
 # the C functions every build must export (checked by the tests)
 EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_status_string", "sptg_last_error",
-           "sptg_last_config", "sptg_device_error", "sptg_version", "sptg_gemm_skinny_noalloc")
+           "sptg_last_config", "sptg_device_error", "sptg_version", "sptg_gemm_skinny_noalloc",
+           "sptg_stream_scale", "sptg_stream_scale_ex")
 
 
 class SptgError(RuntimeError):
@@ -79,6 +81,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sptg_device_error.restype = ctypes.c_int
         lib.sptg_gemm_skinny_noalloc.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
         lib.sptg_gemm_skinny_noalloc.restype = ctypes.c_int
+        lib.sptg_stream_scale.argtypes = [i64, ctypes.c_float, vp, vp, vp]
+        lib.sptg_stream_scale.restype = ctypes.c_int
+        lib.sptg_stream_scale_ex.argtypes = [i64, ctypes.c_float, vp, vp, vp,
+                                             ctypes.POINTER(Config)]
+        lib.sptg_stream_scale_ex.restype = ctypes.c_int
         lib.sptg_version.argtypes = []
         lib.sptg_version.restype = ctypes.c_int
         if path is None:
@@ -175,6 +182,23 @@ def gemm(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = No
     if rc != 0:
         raise SptgError(rc, last_error() or status_string(rc))
     return C
+
+
+def stream_scale(x, alpha: float, out=None, stream=None, config: Config | None = None):
+    """out = alpha * x for a contiguous binary32 CUDA tensor x (out may be x)."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must match x")
+    cfg = ctypes.byref(config) if config is not None else None
+    rc = int((_lib or load()).sptg_stream_scale_ex(x.numel(), float(alpha), x.data_ptr(),
+                                                   out.data_ptr(), _stream_handle(stream), cfg))
+    if rc != 0:
+        raise SptgError(rc, last_error() or status_string(rc))
+    return out
 
 
 def device_error(stream=None) -> int:

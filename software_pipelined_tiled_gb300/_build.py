@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 
 # One translation unit per group of kernels, compiled in parallel.
 UNITS = ["sptgemm.cu", "square_f16_f16.cu", "square_f16_f32.cu", "square_bf16_bf16.cu",
-         "square_bf16_f32.cu", "square_s8.cu", "skinny.cu"]
+         "square_bf16_f32.cu", "square_s8.cu", "skinny.cu", "stream.cu"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,

@@ -25,6 +25,7 @@
 #include "skinny_cluster_gemm.cuh"  // SkinnyClusterParams
 #include "skinny_gemm.cuh"  // SkinnyParams
 #include "square_gemm.cuh"  // SquareParams
+#include "stream_scale.cuh"  // StreamParams
 #include "variants.h"
 
 // Device error word: a timed-out bounded wait ors its site code in here.
@@ -833,6 +834,75 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
 int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B, void* C,
               void* stream) {
   return sptg_gemm_ex(M, N, K, dtype, A, B, C, stream, nullptr);
+}
+
+int sptg_stream_scale_ex(int64_t n, float alpha, const float* in, float* out, void* stream,
+                         const sptg_config* cfg_in) {
+  t_launches = 0;
+  sptg_config cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  if (cfg_in) cfg = *cfg_in;
+  if (n < 0 || cfg.timeout_ms < 0 || (cfg.inject_stall != 0 && cfg.inject_stall != 1) ||
+      (cfg.no_overlap != 0 && cfg.no_overlap != 1) ||
+      (cfg.trace && (reinterpret_cast<uintptr_t>(cfg.trace) & 7u))) {
+    t_last_error = "invalid argument";
+    return SPTG_ERR_ARG;
+  }
+  if (n == 0) {
+    set_config("kernel=none (empty)", "f32", {});
+    return SPTG_OK;
+  }
+  if (!in || !out) {
+    t_last_error = "null pointer";
+    return SPTG_ERR_ARG;
+  }
+  if (!aligned16(in) || !aligned16(out)) {
+    t_last_error = "bulk copies need 16-byte aligned buffers";
+    return SPTG_ERR_ALIGN;
+  }
+  int dev = 0;
+  DeviceInfo di;
+  int rc = device_info(di, dev);
+  if (rc) return rc;
+  const KernelVariant v = stream_variant();
+  rc = ensure_smem(dev, v.fn, v.smem);
+  if (rc) return rc;
+  StreamParams p;
+  p.in = in;
+  p.out = out;
+  p.alpha = alpha;
+  p.n = n;
+  p.n_vec = n & ~static_cast<int64_t>(3);
+  p.num_tiles = (p.n_vec * 4 + v.bn - 1) / v.bn;
+  p.error_word = di.error_word;
+  p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
+  p.inject_stall = cfg.inject_stall;
+  p.trace = static_cast<unsigned long long*>(cfg.trace);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.num_tiles, di.sm_count)));
+  cudaLaunchConfig_t lc;
+  memset(&lc, 0, sizeof(lc));
+  lc.gridDim = dim3(grid, 1, 1);
+  lc.blockDim = dim3(160, 1, 1);
+  lc.dynamicSmemBytes = v.smem;
+  lc.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  if (!cfg.no_overlap) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+  }
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchKernelExC(&lc, v.fn, args);
+  ++t_launches;
+  if (e != cudaSuccess) return cuda_fail(e, "stream_scale launch");
+  set_config("kernel=stream dtype=%s tile_bytes=%lld stages=%lld grid=%lld tiles=%lld smem=%lld",
+             "f32", {v.bn, v.stages, grid, p.num_tiles, v.smem});
+  return SPTG_OK;
+}
+
+int sptg_stream_scale(int64_t n, float alpha, const float* in, float* out, void* stream) {
+  return sptg_stream_scale_ex(n, alpha, in, out, stream, nullptr);
 }
 
 int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype, const void* A,

@@ -30,6 +30,8 @@ bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v);
 bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
 // Skinny kernel with K split inside a cluster (launched in clusters of 2-8).
 bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
+// The streaming ring out = alpha * in (bn = tile bytes).
+KernelVariant stream_variant();
 // int8 -> binary16 widening of n16 groups of 16 elements.
 cudaError_t launch_s8_to_f16(const void* src, void* dst, int64_t n16, int blocks,
                              cudaStream_t stream);

@@ -230,7 +230,9 @@ def _build_mutant(tmp_path, name):
     path = tmp_path / f"{name}.c"
     path.write_text(src.replace(old, new))
     so = tmp_path / f"{name}.so"
-    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-o", str(so), str(path), "-lm"], check=True)
+    stream_src = os.path.join(os.path.dirname(oracle.__file__), "oracle_stream.c")
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-o", str(so), str(path),
+                    stream_src, "-lm"], check=True)
     return so
 
 
