@@ -199,15 +199,19 @@ def cpu_baseline(w, A, B, target_s: float = 12.0):
 
 
 # ------------------------------------------------------------- GPU leg
-def init_dist(n_gpus):
+def init_dist(n_gpus, backend: str = "nccl"):
+    """One process per GPU (torchrun env); replicas only, no data-path collective."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+    elif backend == "nccl":
         torch.cuda.set_device(0)
     return rank, world, local
 
@@ -219,12 +223,19 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time: every replica's measurement is reduced with MAX."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job rate: the units all ranks processed over the slowest rank's time (per ms)."""
+    return world * units_per_rank / ms_max
 
 
 def run_ours(args, w):
@@ -297,7 +308,7 @@ def run_ours(args, w):
     ms = ev0.elapsed_time(ev1)
     ms = max_over_ranks(ms, world)
     ms_per_step = ms / args.steps
-    value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(w.flops, world, ms_per_step) * 1e3 / 1e12
     if sptg.device_error() != 0:
         raise RuntimeError("kernel reported a timed-out wait in the timed region")
 
