@@ -252,9 +252,11 @@ def run_ours(args, w):
     As = [A.to(dev) for _ in range(n_sets)]
     Bs = [B.to(dev) for _ in range(n_sets)]
     Cs = [torch.empty(w.M, w.N, dtype=out_dtype, device=dev) for _ in range(n_sets)]
-    cfg = (sptg.Config(args.kernel, args.bn, args.stages, 0, 0, 0, args.cta_pair,
-                       int(args.no_overlap))
-           if (args.kernel or args.stages or args.bn or args.cta_pair or args.no_overlap) else None)
+    cfg = None
+    if args.kernel or args.stages or args.bn or args.cta_pair or args.no_overlap or args.stream_k:
+        cfg = sptg.Config(args.kernel, args.bn, args.stages, 0, 0, 0, args.cta_pair,
+                          int(args.no_overlap))
+        cfg.stream_k = args.stream_k
     stream = torch.cuda.current_stream()
 
     def step(i):
@@ -369,7 +371,8 @@ def run_ours(args, w):
 
     tl = None
     if args.trace:
-        fields = (args.kernel, args.bn, args.stages, 0, 0, 0, args.cta_pair, int(args.no_overlap))
+        fields = (args.kernel, args.bn, args.stages, 0, 0, 0, args.cta_pair, int(args.no_overlap),
+                  args.stream_k)
         tl = timeline(sptg, As[0], Bs[0], Cs[0], fields)
     cpu = None if args.no_cpu_baseline else cpu_baseline(w, A, B)
     clocks = sampler.summary()
@@ -402,7 +405,9 @@ def timeline(sptg, A, B, C, cfg_fields):
     """One traced call: per-event spread over CTAs and CTA 0's K-tile detail."""
     import numpy as np
     buf = torch.zeros(TRACE_WORDS, dtype=torch.int64, device=A.device)
-    cfg = sptg.Config(*cfg_fields)
+    cfg = sptg.Config(*cfg_fields[:8])
+    if len(cfg_fields) > 8:
+        cfg.stream_k = cfg_fields[8]
     cfg.trace = buf.data_ptr()
     sptg.gemm(A, B, C=C, config=cfg)
     torch.cuda.synchronize()
@@ -537,6 +542,8 @@ def main(argv=None):
                     help="0 choose, 1 square, 2 skinny stream-K, 3 skinny cluster split")
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="square kernel: 0 choose, 1 one CTA per tile, 2 CTA pair (2-SM MMA)")
+    ap.add_argument("--stream-k", type=int, default=0, choices=[0, 1, 2],
+                    help="square kernel: 0 stream-K for a partial last round, 1 never, 2 always")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--stream", type=int, default=0,
                     help="time the streaming ring out = 2 * in over this many binary32 values")

@@ -102,6 +102,9 @@ typedef struct {
                    for CTA 0, the issue time of K-tiles 0..63 (words 8192..)
                    and the time the MMA issuer found each full (8256..);
                    NULL = off                                               */
+  int stream_k; /* square kernel: 0 choose (the tiles of a partial last
+                   round are cut along K over all workers), 1 never, 2 every
+                   tile (a test setting)                                    */
 } sptg_config;
 
 #define SPTG_TRACE_WORDS (8 * 1024 + 2 * 64)

@@ -48,7 +48,8 @@ class Config(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("bn", ctypes.c_int), ("stages", ctypes.c_int),
                 ("splits", ctypes.c_int), ("timeout_ms", ctypes.c_int),
                 ("inject_stall", ctypes.c_int), ("cta_pair", ctypes.c_int),
-                ("no_overlap", ctypes.c_int), ("trace", ctypes.c_void_p)]
+                ("no_overlap", ctypes.c_int), ("trace", ctypes.c_void_p),
+                ("stream_k", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -146,7 +147,7 @@ def _dtype_key(in_dtype, out_dtype) -> str:
 
 def gemm(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = None,
          kernel: str | None = None, stages: int = 0, bn: int = 0, splits: int = 0,
-         cta_pair: int = 0):
+         cta_pair: int = 0, stream_k: int = 0):
     """C = A * B on the GPU, with A (M x K) and Bcm (N x K) CUDA tensors.
 
     out_dtype defaults to the input type for binary16/bfloat16 and int32 for
@@ -170,8 +171,9 @@ def gemm(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = No
         C = torch.empty((M, N), dtype=out_dtype, device=A.device)
     elif C.shape != (M, N) or C.dtype != out_dtype or not C.is_contiguous() or not C.is_cuda:
         raise ValueError("C must be a contiguous M x N CUDA tensor of the output dtype")
-    if config is None and (kernel or stages or bn or splits or cta_pair):
+    if config is None and (kernel or stages or bn or splits or cta_pair or stream_k):
         config = Config(KERNELS[kernel or "auto"], bn, stages, splits, 0, 0, cta_pair)
+        config.stream_k = stream_k
     if A.device.index == torch.cuda.current_device():
         rc = gemm_raw(M, N, K, key, A.data_ptr(), Bcm.data_ptr(), C.data_ptr(),
                       _stream_handle(stream), config)

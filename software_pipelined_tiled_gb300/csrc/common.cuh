@@ -27,6 +27,8 @@ enum WaitSite : unsigned int {
   WAIT_EPI_TMEM_FULL = 1u << 3,
   WAIT_DRAIN = 1u << 4,
   WAIT_PLAN = 1u << 5,  // not a wait: a launch whose scratch plan does not fit
+  WAIT_FIXUP_NOTE = 1u << 6,  // reduction warps: notice of a written partial tile
+  WAIT_FIXUP_SLOT = 1u << 7,  // epilogue: a free notice slot
 };
 
 // Optional timeline: with a trace buffer, chosen threads stamp %globaltimer
@@ -39,7 +41,7 @@ enum TraceEvent : int {
   TR_LAST_MMA = 4,    // MMA issuer committed its last MMA
   TR_EPI_DONE = 5,    // epilogue finished its last tile (stores complete)
   TR_EXIT = 6,        // every role of the CTA (and of its pair) is done
-  TR_FIXUP_DONE = 7,  // skinny: last split-K reduction this CTA did, if any
+  TR_FIXUP_DONE = 7,  // last split-K / stream-K reduction this CTA did, if any
   TR_SLOTS = 8,
   TR_MAX_CTAS = 1024,
   // detail of CTA 0: when the producer issued K-tile i and when the MMA
@@ -144,6 +146,26 @@ __device__ __forceinline__ void store_out4(void* C, int64_t idx, float4 v) {
     uint2 w = make_uint2(pack2<OUT>(v.x, v.y), pack2<OUT>(v.z, v.w));
     *reinterpret_cast<uint2*>(static_cast<uint16_t*>(C) + idx) = w;
   }
+}
+
+// Counts one arrival at a tile's split-K counter and returns whether it was the
+// last of `count`. The 64-bit counter holds (call generation << 32 | arrivals):
+// a value left by an earlier call (or by one that gave up) carries another
+// generation and is replaced, so no call has to clear the counters first.
+// The compare-and-swap retries only when another contributor got in first.
+__device__ __forceinline__ int arrive_generation(unsigned long long* ctr, unsigned int gen,
+                                                 int count, unsigned int* error_word) {
+  unsigned long long cur = atomicAdd(ctr, 0ull);
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    const unsigned long long base =
+        (static_cast<unsigned int>(cur >> 32) == gen) ? cur : (static_cast<unsigned long long>(gen) << 32);
+    const unsigned long long want = base + 1;
+    const unsigned long long prev = atomicCAS(ctr, cur, want);
+    if (prev == cur) return static_cast<int>(want & 0xffffffffull) == count;
+    cur = prev;
+  }
+  atomicOr(error_word, WAIT_PLAN);
+  return 0;
 }
 
 // Tile index -> (m tile, n tile). Tiles are visited in column strips of

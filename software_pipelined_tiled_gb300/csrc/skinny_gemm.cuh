@@ -66,26 +66,6 @@ __device__ __forceinline__ int cta_of_unit(int64_t u, int G, int64_t T) {
   return static_cast<int>(((u + 1) * G - 1) / T);
 }
 
-// Counts one arrival at an n-tile's counter and returns whether it was the
-// last of `count`. The 64-bit counter holds (call generation << 32 | arrivals):
-// a value left by an earlier call (or by one that gave up) carries another
-// generation and is replaced, so no call has to clear the counters first.
-// The compare-and-swap retries only when another contributor got in first.
-__device__ __forceinline__ int arrive_generation(unsigned long long* ctr, unsigned int gen,
-                                                 int count, unsigned int* error_word) {
-  unsigned long long cur = atomicAdd(ctr, 0ull);
-  for (int tries = 0; tries < (1 << 20); ++tries) {
-    const unsigned long long base =
-        (static_cast<unsigned int>(cur >> 32) == gen) ? cur : (static_cast<unsigned long long>(gen) << 32);
-    const unsigned long long want = base + 1;
-    const unsigned long long prev = atomicCAS(ctr, cur, want);
-    if (prev == cur) return static_cast<int>(want & 0xffffffffull) == count;
-    cur = prev;
-  }
-  atomicOr(error_word, WAIT_PLAN);
-  return 0;
-}
-
 template <int MN, int STAGES, bool IN_BF16, int OUT>
 __global__ void __launch_bounds__(192, 1)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmBt,

@@ -149,9 +149,10 @@ int ensure_smem(int dev, const void* kernel, int bytes) {
 
 // ------------------------------------------------------------ scratch space
 // One stream-ordered scratch area per (device, stream), grown on demand. Its
-// first kCounterArea bytes hold the skinny kernel's split-K arrival counters
-// (zeroed whenever the area is (re)allocated, never used by anything else);
-// the rest holds a call's data (int8 operands widened to binary16, or split-K
+// first kCounterArea bytes hold the split-K arrival counters of the skinny
+// kernel and of the square kernel's stream-K tiles (zeroed whenever the area
+// is (re)allocated; each call tags its arrivals with a new generation); the
+// rest holds a call's data (int8 operands widened to binary16, split-K
 // partial tiles).
 constexpr size_t kCounterArea = static_cast<size_t>(1) << 16;
 
@@ -314,7 +315,7 @@ cudaError_t launch_variant(const KernelVariant& v, int grid, cudaStream_t stream
   cudaLaunchConfig_t lc;
   memset(&lc, 0, sizeof(lc));
   lc.gridDim = dim3(grid, 1, 1);
-  lc.blockDim = dim3(192, 1, 1);
+  lc.blockDim = dim3(v.threads, 1, 1);
   lc.dynamicSmemBytes = v.smem;
   lc.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -349,7 +350,7 @@ int cluster_slots(int dev, const KernelVariant& v, int cluster, int sm_count) {
   cudaLaunchConfig_t lc;
   memset(&lc, 0, sizeof(lc));
   lc.gridDim = dim3(cluster * (sm_count / cluster), 1, 1);
-  lc.blockDim = dim3(192, 1, 1);
+  lc.blockDim = dim3(v.threads, 1, 1);
   lc.dynamicSmemBytes = v.smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -385,32 +386,77 @@ bool pick_square(const DtypeInfo& d, int bn, int stages, bool pair, KernelVarian
   }
 }
 
-// Tile shape against wave quantisation. The persistent grid runs
-// ceil(tiles / workers) rounds, a worker being one SM (128 x BN tiles) or a
-// CTA pair on two SMs (256 x BN tiles). Per SM a tile costs about BN + 64
-// column-units (the 64 stands for the A-operand traffic every tile carries
-// whatever its width); a pair's 2-SM MMA reads half of B per SM, which is
-// credited as a 10 % cheaper tile. The cheapest estimate wins; ties keep the
-// wider tile.
-void choose_square_shape(int64_t M, int64_t N, int sm_count, int bn_req, int pair_req,
+// Per-FLOP rate of each tile shape measured on GB300 (binary16 8192 x 8192 x
+// 4096, TFLOPS with wave quantisation and padding divided out), for BN =
+// 256, 224, 192, 160, 128: the weights of the shape model below. Narrow
+// tiles lose more than their share: each K-tile of a stage costs about the
+// same whatever its width.
+constexpr double kRatePair[5] = {1790, 1638, 1446, 1241, 988};
+constexpr double kRateSingle[5] = {1606, 1501, 1469, 1213, 1003};
+constexpr int kTileWidths[5] = {256, 224, 192, 160, 128};
+
+// Stream-K part of the schedule for T tiles over W workers, KT K-tiles each:
+// the tiles of a partial last round (mode 0, when that round is at most 90 %
+// full), none (mode 1), or every tile (mode 2, a test setting), cut over
+// enough workers that each gets at least 8 K-tiles. sk_tiles = 0: nothing
+// is cut.
+void plan_stream_k(int T, int W, int KT, int mode, int* sk_tiles, int* sk_workers,
+                   int* max_contrib) {
+  *sk_tiles = 0;
+  *sk_workers = 0;
+  *max_contrib = 1;
+  int t = 0;
+  if (mode == 2)
+    t = T;
+  else if (mode == 0 && T % W != 0 && T % W <= (9 * W) / 10)
+    t = T % W;
+  if (t == 0) return;
+  const int64_t units = static_cast<int64_t>(t) * KT;
+  int sw = static_cast<int>(std::min<int64_t>(W, units / 8));
+  if (sw < 2) {
+    if (mode != 2) return;
+    sw = 1;
+  }
+  // every worker holds at least floor(units / sw) consecutive units, so a
+  // tile of KT units meets at most ceil(KT / that) + 1 of them
+  const int64_t per = units / sw;
+  const int mc = static_cast<int>((KT + per - 1) / per) + 1;
+  *sk_tiles = t;
+  *sk_workers = sw;
+  *max_contrib = std::min(mc, sw);
+}
+
+// Tile shape: one CTA (128 x BN) or a CTA pair (256 x BN) per tile. The
+// estimate is rounds x (tile rows x BN) x workers / measured rate, with
+// rounds = ceil(tiles / workers) for a data-parallel schedule and
+// tiles / workers + 0.5 when the last round goes through stream-K (the cut
+// tiles' partial writes and reductions measured at about half a round on
+// 4096 x 4096 x 4096). The cheapest estimate wins; ties keep the wider tile.
+void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sptg_config& cfg,
                          bool int8, int* bn_out, bool* pair_out) {
-  static const int cands[] = {256, 224, 192, 160, 128};
-  int64_t best_cost = INT64_MAX;
+  double best = 1e300;
   *bn_out = 256;
   *pair_out = false;
+  const int KT = static_cast<int>((K + 63) / 64);
   for (int pair = 0; pair < 2; ++pair) {
-    if ((pair_req == 1 && pair) || (pair_req == 2 && !pair)) continue;
-    if (pair && M <= 128 && pair_req != 2) continue;  // one CTA already covers all rows
+    if ((cfg.cta_pair == 1 && pair) || (cfg.cta_pair == 2 && !pair)) continue;
+    if (pair && M <= 128 && cfg.cta_pair != 2) continue;  // one CTA already covers all rows
     const int64_t rows = pair ? 256 : 128;
-    const int64_t workers = pair ? sm_count / 2 : sm_count;
-    for (int bn : cands) {
-      if (bn_req && bn != bn_req) continue;
+    const int W = pair ? sm_count / 2 : sm_count;
+    for (int i = 0; i < 5; ++i) {
+      const int bn = kTileWidths[i];
+      if (cfg.bn && bn != cfg.bn) continue;
       if (int8 && bn != 128) continue;
-      const int64_t tiles = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
-      const int64_t rounds = (tiles + workers - 1) / workers;
-      const int64_t cost = rounds * (bn + 64) * (pair ? 9 : 10);
-      if (cost < best_cost) {
-        best_cost = cost;
+      const int64_t T64 = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
+      const int T = static_cast<int>(std::min<int64_t>(T64, INT32_MAX));
+      int skt, skw, mc;
+      plan_stream_k(T, W, KT, cfg.stream_k, &skt, &skw, &mc);
+      const double rounds = skt ? static_cast<double>(T) / W + 0.5
+                                : static_cast<double>((T + W - 1) / W);
+      const double rate = pair ? kRatePair[i] : kRateSingle[i];
+      const double cost = rounds * static_cast<double>(rows * bn) * W / rate;
+      if (cost < best) {
+        best = cost;
         *bn_out = bn;
         *pair_out = pair != 0;
       }
@@ -418,64 +464,102 @@ void choose_square_shape(int64_t M, int64_t N, int sm_count, int bn_req, int pai
   }
 }
 
-int run_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N, int64_t K,
-               const void* A16, const void* B16, void* C, cudaStream_t stream,
-               const sptg_config& cfg) {
+struct SquarePlan {
+  KernelVariant v;
+  bool pair;
+  int tile_m, m_tiles, n_tiles, k_tiles, workers, grid;
+  int sk_tiles, sk_workers, max_contrib;
+  size_t partial_bytes;  // scratch for the stream-K partial tiles (0: none)
+};
+
+int plan_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N,
+                int64_t K, const sptg_config& cfg, SquarePlan* pl) {
   int bn = 0;
   bool pair = false;
-  choose_square_shape(M, N, di.sm_count, cfg.bn, cfg.cta_pair, d.is_int8, &bn, &pair);
-  KernelVariant v;
-  if (!pick_square(d, bn, cfg.stages, pair, &v)) {
+  choose_square_shape(M, N, K, di.sm_count, cfg, d.is_int8, &bn, &pair);
+  if (!pick_square(d, bn, cfg.stages, pair, &pl->v)) {
     // a forced ring depth may exist for the other tile mode only
-    if (cfg.cta_pair == 0 && pick_square(d, bn, cfg.stages, !pair, &v)) {
+    if (cfg.cta_pair == 0 && pick_square(d, bn, cfg.stages, !pair, &pl->v)) {
       pair = !pair;
     } else {
       t_last_error = "no square-kernel variant for the requested bn/stages/pairing";
       return SPTG_ERR_CONFIG;
     }
   }
+  int rc = ensure_smem(dev, pl->v.fn, pl->v.smem);
+  if (rc) return rc;
+  pl->pair = pair;
+  pl->tile_m = pair ? 256 : 128;
+  pl->m_tiles = static_cast<int>((M + pl->tile_m - 1) / pl->tile_m);
+  pl->n_tiles = static_cast<int>((N + pl->v.bn - 1) / pl->v.bn);
+  pl->k_tiles = static_cast<int>((K + 63) / 64);
+  const int tiles = pl->m_tiles * pl->n_tiles;
+  int workers = pair ? pair_slots(dev, pl->v, di.sm_count) : di.sm_count;
+  if (cfg.splits > 0) workers = std::min(workers, cfg.splits);
+  plan_stream_k(tiles, workers, pl->k_tiles, cfg.stream_k, &pl->sk_tiles, &pl->sk_workers,
+                &pl->max_contrib);
+  if (pl->sk_tiles == 0)
+    workers = std::min(workers, tiles);
+  else if (pl->sk_tiles == tiles)
+    workers = pl->sk_workers;  // no data-parallel tiles: idle workers are not launched
+  pl->workers = workers;
+  pl->grid = pair ? 2 * workers : workers;
+  pl->partial_bytes =
+      static_cast<size_t>(pl->sk_tiles) * 2 * pl->max_contrib * 128 * pl->v.bn * 4;
+  if (static_cast<size_t>(pl->sk_tiles) * 2 * sizeof(unsigned long long) > kCounterArea) {
+    t_last_error = "too many stream-K tiles for the arrival-counter area";
+    return SPTG_ERR_CONFIG;
+  }
+  return SPTG_OK;
+}
+
+int launch_square(const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N, int64_t K,
+                  const void* A16, const void* B16, void* C, cudaStream_t stream,
+                  const sptg_config& cfg, const SquarePlan& pl, void* partials,
+                  unsigned long long* counters, unsigned int generation) {
   const int BM = 128, BK = 64;
-  const int tile_m = pair ? 256 : 128;
   CUtensorMap ta, tb, tc;
   int rc = make_map_2d(&ta, d.in_tma, 2, A16, K, M, BK, BM);
   if (rc) return rc;
-  rc = make_map_2d(&tb, d.in_tma, 2, B16, K, N, BK, pair ? v.bn / 2 : v.bn);
+  rc = make_map_2d(&tb, d.in_tma, 2, B16, K, N, BK, pl.pair ? pl.v.bn / 2 : pl.v.bn);
   if (rc) return rc;
   // C blocks of 32 columns x 32 rows: 128-byte rows for 4-byte outputs,
   // 64-byte rows for 16-bit ones (matching the kernel's staging swizzle)
   rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, 32, 32,
                    d.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
-  rc = ensure_smem(dev, v.fn, v.smem);
-  if (rc) return rc;
 
   SquareParams p;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.num_m_tiles = static_cast<int>((M + tile_m - 1) / tile_m);
-  p.num_n_tiles = static_cast<int>((N + v.bn - 1) / v.bn);
-  p.num_k_tiles = static_cast<int>((K + BK - 1) / BK);
-  p.k_tiles_per_chunk = d.is_int8 ? 1024 / BK : p.num_k_tiles;
+  p.C_out = C;
+  p.num_m_tiles = pl.m_tiles;
+  p.num_n_tiles = pl.n_tiles;
+  p.num_k_tiles = pl.k_tiles;
+  p.k_tiles_per_chunk = d.is_int8 ? 1024 / BK : pl.k_tiles;
   p.group_m = 8;
+  p.sk_tiles = pl.sk_tiles;
+  p.sk_workers = pl.sk_workers;
+  p.max_contrib = pl.max_contrib;
+  p.partials = static_cast<uint32_t*>(partials);
+  p.counters = counters;
+  p.generation = generation;
   p.error_word = di.error_word;
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;
   p.trace = static_cast<unsigned long long*>(cfg.trace);
-  const int tiles = p.num_m_tiles * p.num_n_tiles;
-  int workers = pair ? pair_slots(dev, v, di.sm_count) : di.sm_count;
-  if (cfg.splits > 0) workers = std::min(workers, cfg.splits);
-  workers = std::min(workers, tiles);
-  const int grid = pair ? 2 * workers : workers;
   void* args[] = {&ta, &tb, &tc, &p};
-  cudaError_t e = launch_variant(v, grid, stream, args, !cfg.no_overlap);
+  cudaError_t e = launch_variant(pl.v, pl.grid, stream, args, !cfg.no_overlap);
   ++t_launches;
   if (e != cudaSuccess) return cuda_fail(e, "square_gemm launch");
   set_config(
       "kernel=square dtype=%s tile_m=%lld bn=%lld bk=%lld stages=%lld pair=%lld grid=%lld "
-      "tiles=%lld k_tiles=%lld chunk_k_tiles=%lld smem=%lld",
-      d.name, {tile_m, v.bn, BK, v.stages, pair ? 1 : 0, grid, tiles, p.num_k_tiles,
-               p.k_tiles_per_chunk, v.smem});
+      "tiles=%lld k_tiles=%lld chunk_k_tiles=%lld stream_k_tiles=%lld stream_k_workers=%lld "
+      "smem=%lld",
+      d.name, {pl.tile_m, pl.v.bn, BK, pl.v.stages, pl.pair ? 1 : 0, pl.grid,
+               static_cast<long long>(pl.m_tiles) * pl.n_tiles, pl.k_tiles, p.k_tiles_per_chunk,
+               pl.sk_tiles, pl.sk_workers, pl.v.smem});
   return SPTG_OK;
 }
 
@@ -767,6 +851,7 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
   if (cfg.kernel < 0 || cfg.kernel > 3 || cfg.stages < 0 || cfg.bn < 0 || cfg.splits < 0 ||
       cfg.timeout_ms < 0 || (cfg.inject_stall != 0 && cfg.inject_stall != 1) ||
       cfg.cta_pair < 0 || cfg.cta_pair > 2 || (cfg.no_overlap != 0 && cfg.no_overlap != 1) ||
+      cfg.stream_k < 0 || cfg.stream_k > 2 ||
       (cfg.trace && (reinterpret_cast<uintptr_t>(cfg.trace) & 7u))) {
     t_last_error = "invalid configuration field";
     return SPTG_ERR_ARG;
@@ -810,12 +895,18 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
   if (kernel == 3) return run_skinny_cluster(dev, di, d, M, N, K, A, B, C, stream_h, cfg, true);
   if (kernel == 2) return run_skinny(dev, di, d, M, N, K, A, B, C, stream_h, cfg);
 
+  SquarePlan pl;
+  rc = plan_square(dev, di, d, M, N, K, cfg, &pl);
+  if (rc) return rc;
   if (d.is_int8) {
-    // Widen both operands to binary16 in scratch, then run the exact path.
+    // Widen both operands to binary16 in scratch, followed by any stream-K
+    // partials (one request: the scratch cannot move within the call), then
+    // run the exact path.
     const size_t a_bytes = static_cast<size_t>(M) * K * 2, b_bytes = static_cast<size_t>(N) * K * 2;
     const size_t a_pad = (a_bytes + 255) & ~static_cast<size_t>(255);
+    const size_t b_pad = (b_bytes + 255) & ~static_cast<size_t>(255);
     ScratchView ws;
-    rc = scratch_for(dev, stream_h, a_pad + b_bytes, &ws);
+    rc = scratch_for(dev, stream_h, a_pad + b_pad + pl.partial_bytes, &ws);
     if (rc) return rc;
     void* A16 = ws.data;
     void* B16 = static_cast<char*>(ws.data) + a_pad;
@@ -826,9 +917,17 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
     if (e == cudaSuccess) e = launch_s8_to_f16(B, B16, nb, blocks_b, stream_h);
     t_launches += 2;
     if (e != cudaSuccess) return cuda_fail(e, "s8_to_f16 launch");
-    return run_square(dev, di, d, M, N, K, A16, B16, C, stream_h, cfg);
+    return launch_square(di, d, M, N, K, A16, B16, C, stream_h, cfg, pl,
+                         static_cast<char*>(ws.data) + a_pad + b_pad, ws.counters, ws.generation);
   }
-  return run_square(dev, di, d, M, N, K, A, B, C, stream_h, cfg);
+  if (pl.partial_bytes) {
+    ScratchView ws;
+    rc = scratch_for(dev, stream_h, pl.partial_bytes, &ws);
+    if (rc) return rc;
+    return launch_square(di, d, M, N, K, A, B, C, stream_h, cfg, pl, ws.data, ws.counters,
+                         ws.generation);
+  }
+  return launch_square(di, d, M, N, K, A, B, C, stream_h, cfg, pl, nullptr, nullptr, 0);
 }
 
 int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B, void* C,

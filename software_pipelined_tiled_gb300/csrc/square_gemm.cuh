@@ -15,6 +15,7 @@
 //              tensor memory (each warp owns 32 of the 128 lanes), convert,
 //              stage 32-row blocks in shared memory and store them with the
 //              tensor-copy engine; then hand the accumulator back.
+//   warps 6-9  stream-K reduction (below); idle when no tile is cut.
 //
 // This is the producer/consumer ring of "Hiding Memory Latency in CUDA:
 // Asynchronous Loads and Software Pipelines" (sections 5, 6 and 11): stage =
@@ -39,6 +40,19 @@
 // on both CTAs' "empty" and "tmem_full" barriers; both CTAs' epilogue warps
 // release the accumulator on the leader's "tmem_empty" barrier.
 //
+// Work schedule (stream-K + data-parallel). With T tiles and W workers (CTAs,
+// or CTA pairs), T mod W tiles would leave a last round with most SMs idle.
+// Those tiles are instead cut along K into one contiguous range of
+// (tile, K-tile) units per worker and done first; the remaining T - T mod W
+// tiles follow round robin, every worker the same number. A worker whose range
+// covers only part of a tile's K writes its fp32 (int32 in INT_EXACT mode)
+// partial tile to scratch; the last contributor to arrive (an atomic counter
+// tagged with the call's generation) adds the partials in contributor order
+// (= increasing k, a fixed order) and writes C. The epilogue only writes the
+// partial and posts a notice; four reduction warps of their own take the
+// arrival and the sum, so the accumulators keep draining and the K-loop of
+// the next tiles never waits for a reduction.
+//
 // INT_EXACT mode computes an int8 product exactly on the fp16 tensor path: the
 // inputs are int8 values held as binary16 (exact), every product is an integer
 // of magnitude <= 2^14 and every partial sum of at most 1024 products is an
@@ -51,18 +65,94 @@
 
 namespace sptg {
 
+// Threads of a square-kernel CTA: producer, MMA, 4 epilogue, 4 reduction warps.
+constexpr int SQUARE_THREADS = 320;
+
 struct SquareParams {
   int M, N, K;
+  void* C_out;  // C, for the stream-K reductions' direct stores
   int num_m_tiles, num_n_tiles, num_k_tiles;
   int k_tiles_per_chunk;  // accumulation chunk (all K-tiles unless INT_EXACT)
   int group_m;            // raster strip height in m-tiles
+  // stream-K part: the last sk_tiles tile indices, cut into sk_units =
+  // sk_tiles * num_k_tiles units over the first sk_workers workers
+  int sk_tiles;
+  int sk_workers;
+  int max_contrib;              // partial slots per (tile, CTA of the pair)
+  uint32_t* partials;           // [sk_tile][rank][contributor][128][BN] 32-bit
+  unsigned long long* counters;  // [sk_tile * 2 + rank] (generation << 32 | arrivals)
+  unsigned int generation;
   unsigned int* error_word;
   uint64_t timeout_ns;
-  int inject_stall;
-  unsigned long long* trace;  // optional timeline (see TraceEvent), or null  // test hook: withhold the load of the second K-tile
+  int inject_stall;  // test hook: withhold the load of the second K-tile
+  unsigned long long* trace;  // optional timeline (see TraceEvent), or null
 };
 
-template <int BN, int STAGES, bool INT_EXACT, bool PAIR>
+// One piece of a worker's work: K-tiles [kt0, kt1) of tile `tile`. A partial
+// segment (not all of K) belongs to stream-K tile `sk`, whose contributors are
+// workers c_first .. c_first + count - 1; this worker is contributor j.
+struct Segment {
+  int tile, kt0, kt1;
+  bool partial;
+  int sk, j, count;
+};
+
+// The worker holding stream-K unit u: ranges are [w*U/G, (w+1)*U/G).
+__device__ __forceinline__ int sk_worker_of(int64_t u, int G, int64_t U) {
+  return static_cast<int>(((u + 1) * G - 1) / U);
+}
+
+// The i-th segment of `worker` (false past the last). Stream-K segments come
+// first, then the data-parallel tiles.
+__device__ __forceinline__ bool square_segment(const SquareParams& p, int worker, int workers,
+                                               int i, Segment& seg) {
+  const int KT = p.num_k_tiles;
+  const int T = p.num_m_tiles * p.num_n_tiles;
+  const int T_dp = T - p.sk_tiles;
+  int n_sk = 0;
+  int64_t u0 = 0, u1 = 0;
+  const int64_t U = static_cast<int64_t>(p.sk_tiles) * KT;
+  if (p.sk_tiles > 0 && worker < p.sk_workers) {
+    u0 = static_cast<int64_t>(worker) * U / p.sk_workers;
+    u1 = static_cast<int64_t>(worker + 1) * U / p.sk_workers;
+    if (u1 > u0) n_sk = static_cast<int>((u1 - 1) / KT - u0 / KT + 1);
+  }
+  if (i < n_sk) {
+    const int sk = static_cast<int>(u0 / KT) + i;
+    const int64_t lo = max(u0, static_cast<int64_t>(sk) * KT);
+    const int64_t hi = min(u1, static_cast<int64_t>(sk + 1) * KT);
+    seg.tile = T_dp + sk;
+    seg.kt0 = static_cast<int>(lo - static_cast<int64_t>(sk) * KT);
+    seg.kt1 = static_cast<int>(hi - static_cast<int64_t>(sk) * KT);
+    seg.partial = !(seg.kt0 == 0 && seg.kt1 == KT);
+    seg.sk = sk;
+    const int c_first = sk_worker_of(static_cast<int64_t>(sk) * KT, p.sk_workers, U);
+    const int c_last = sk_worker_of(static_cast<int64_t>(sk + 1) * KT - 1, p.sk_workers, U);
+    seg.j = worker - c_first;
+    seg.count = c_last - c_first + 1;
+    return true;
+  }
+  const int tile = worker + (i - n_sk) * workers;
+  if (tile >= T_dp) return false;
+  seg.tile = tile;
+  seg.kt0 = 0;
+  seg.kt1 = KT;
+  seg.partial = false;
+  seg.sk = seg.j = seg.count = 0;
+  return true;
+}
+
+// Epilogue staging per warp: one block of 32 rows x 32 outputs. 4-byte
+// outputs keep two such buffers (a store can read one while the next block
+// is written), 16-bit outputs one buffer of 2 KB, which leaves room for one
+// more ring stage in the pair kernels.
+template <int OBYTES>
+struct EpiStaging {
+  static constexpr int BUF = 32 * 32 * OBYTES;
+  static constexpr int NBUF = OBYTES == 4 ? 2 : 1;
+};
+
+template <int BN, int STAGES, bool INT_EXACT, bool PAIR, int OBYTES = 4>
 struct SquareLayout {
   static constexpr int BM = 128;         // rows of A (and of C) per CTA
   static constexpr int TILE_M = PAIR ? 256 : 128;
@@ -71,13 +161,14 @@ struct SquareLayout {
   static constexpr int A_STAGE = BM * BK * 2;
   static constexpr int B_STAGE = BN_CTA * BK * 2;
   static constexpr int EPI_WARPS = 4;
-  static constexpr int EPI_BUF = 32 * 128;  // 32 rows x 128 bytes
-  static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
+  static constexpr int EPI_BUF = EpiStaging<OBYTES>::BUF;
+  static constexpr int EPI_NBUF = EpiStaging<OBYTES>::NBUF;
+  static constexpr int EPI_BYTES = EPI_WARPS * EPI_NBUF * EPI_BUF;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
   static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;
   static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 4;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int BYTES_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = BYTES_USED + 1024;  // slack to align the base to 1024
@@ -97,20 +188,31 @@ struct SquareLayout {
 };
 
 // Deepest ring that fits the 227 KB per-CTA budget next to the epilogue
-// staging (32 KB), the barriers and the 1 KB alignment slack.
-template <int BN, bool PAIR = false>
+// staging, the barriers and the 1 KB alignment slack.
+template <int BN, bool PAIR = false, int OBYTES = 4>
 constexpr int square_max_stages() {
-  return (232448 - 1024 - 4 * 2 * 32 * 128 - 256) / (128 * 64 * 2 + (PAIR ? BN / 2 : BN) * 64 * 2);
+  return (232448 - 1024 - 4 * EpiStaging<OBYTES>::NBUF * EpiStaging<OBYTES>::BUF - 256) /
+         (128 * 64 * 2 + (PAIR ? BN / 2 : BN) * 64 * 2);
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_c4(void* C, int64_t idx, uint4 bits) {
+  if constexpr (OUT == OUT_S32) {
+    *reinterpret_cast<uint4*>(static_cast<int32_t*>(C) + idx) = bits;
+  } else {
+    store_out4<OUT>(C, idx, make_float4(__uint_as_float(bits.x), __uint_as_float(bits.y),
+                                        __uint_as_float(bits.z), __uint_as_float(bits.w)));
+  }
 }
 
 template <int BN, int STAGES, bool IN_BF16, int OUT, bool INT_EXACT, bool PAIR = false>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(SQUARE_THREADS, 1)
     square_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const SquareParams p) {
-  using L = SquareLayout<BN, STAGES, INT_EXACT, PAIR>;
-  constexpr int BM = L::BM, BK = L::BK;
   constexpr int OBYTES = OutTraits<OUT>::bytes;
+  using L = SquareLayout<BN, STAGES, INT_EXACT, PAIR, OBYTES>;
+  constexpr int BM = L::BM, BK = L::BK;
   constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, L::TILE_M, BN);
   static_assert(!INT_EXACT || OUT == OUT_S32, "exact integer mode writes int32");
 
@@ -127,8 +229,13 @@ __global__ void __launch_bounds__(192, 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  // notices "partial tile written" from the epilogue to the reduction warps
+  auto note_full = [&](int j) { return bar0 + 8u * (2 * STAGES + 5 + j); };
+  auto note_empty = [&](int j) { return bar0 + 8u * (2 * STAGES + 7 + j); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  // the reduction warps' decision per notice (two slots, alternating)
+  volatile int* fix_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -145,6 +252,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(tempty_bar(b), (PAIR ? 2 : 1) * L::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(note_full(j), 1);
+      mbar_init(note_empty(j), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     // kernel parameters, not written by earlier kernels: fetch them early
@@ -163,20 +274,22 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
-  const int num_chunks = (p.num_k_tiles + p.k_tiles_per_chunk - 1) / p.k_tiles_per_chunk;
+  const int kpc = p.k_tiles_per_chunk;
   // the persistent work unit is a CTA, or a CTA pair in PAIR mode
   const int worker = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  // Warm L2 with the first stages of this CTA's first tile while the previous
-  // kernel drains (safe: L2 is where writes become coherent; the loads proper
-  // wait for the dependency).
-  if (threadIdx.x == 0 && worker < num_tiles) {
-    int mt, nt;
-    tile_coords(worker, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
-    for (int kt = 0; kt < min(p.num_k_tiles, STAGES); ++kt) {
-      tma_prefetch_l2_2d(&tmA, kt * BK, mt * L::TILE_M + static_cast<int>(rank) * BM);
-      tma_prefetch_l2_2d(&tmB, kt * BK, nt * BN + static_cast<int>(rank) * L::BN_CTA);
+  // Warm L2 with the first stages of this CTA's first segment while the
+  // previous kernel drains (safe: L2 is where writes become coherent; the
+  // loads proper wait for the dependency).
+  if (threadIdx.x == 0) {
+    Segment seg;
+    if (square_segment(p, worker, workers, 0, seg)) {
+      int mt, nt;
+      tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+      for (int kt = seg.kt0; kt < min(seg.kt1, seg.kt0 + STAGES); ++kt) {
+        tma_prefetch_l2_2d(&tmA, kt * BK, mt * L::TILE_M + static_cast<int>(rank) * BM);
+        tma_prefetch_l2_2d(&tmB, kt * BK, nt * BN + static_cast<int>(rank) * L::BN_CTA);
+      }
     }
   }
   // Set-up above may overlap the previous kernel in the stream; no global
@@ -194,12 +307,13 @@ __global__ void __launch_bounds__(192, 1)
       for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
       bool ok = true;
       uint32_t it = 0;
-      for (int tile = worker; ok && tile < num_tiles; tile += workers) {
+      Segment seg;
+      for (int i = 0; ok && square_segment(p, worker, workers, i, seg); ++i) {
         int mt, nt;
-        tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+        tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
         const int a_row = mt * L::TILE_M + static_cast<int>(rank) * BM;
         const int b_row = nt * BN + static_cast<int>(rank) * L::BN_CTA;
-        for (int kt = 0; kt < p.num_k_tiles; ++kt, ++it) {
+        for (int kt = seg.kt0; kt < seg.kt1; ++kt, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
           if (!wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl, WAIT_PRODUCER_EMPTY)) {
@@ -250,8 +364,9 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0 && rank == 0) {
       bool ok = true;
       uint32_t it = 0, unit = 0;
-      for (int tile = worker; ok && tile < num_tiles; tile += workers) {
-        for (int c = 0; ok && c < num_chunks; ++c, ++unit) {
+      Segment seg;
+      for (int i = 0; ok && square_segment(p, worker, workers, i, seg); ++i) {
+        for (int c0 = seg.kt0; ok && c0 < seg.kt1; c0 += kpc, ++unit) {
           const uint32_t b = unit & 1u;
           const uint32_t use = unit >> 1;
           if (!wait_bounded(tempty_bar(b), (use & 1u) ^ 1u, ctl, WAIT_MMA_TMEM_EMPTY)) {
@@ -260,9 +375,8 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * BN;
-          const int kt0 = c * p.k_tiles_per_chunk;
-          const int kt1 = min(p.num_k_tiles, kt0 + p.k_tiles_per_chunk);
-          for (int kt = kt0; kt < kt1; ++kt, ++it) {
+          const int c1 = min(seg.kt1, c0 + kpc);
+          for (int kt = c0; kt < c1; ++kt, ++it) {
             const int s = it % STAGES;
             const uint32_t round = it / STAGES;
             if (!wait_bounded(full_bar(s), round & 1u, ctl, WAIT_MMA_FULL)) {
@@ -278,7 +392,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int k = 0; k < BK / 16; ++k) {
               mma_f16_g<PAIR>(d_tmem, sdesc_k_major_sw128(a_addr + 32 * k),
                               sdesc_k_major_sw128(b_addr + 32 * k), IDESC,
-                              (kt > kt0 || k > 0) ? 1u : 0u);
+                              (kt > c0 || k > 0) ? 1u : 0u);
             }
             mma_commit_g<PAIR>(empty_bar(s));  // stage s may be refilled (in both CTAs)
           }
@@ -292,18 +406,25 @@ __global__ void __launch_bounds__(192, 1)
       while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < ctl.timeout_ns) {
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quadrant this warp may access
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    uint8_t* bufs = epi_buf + (warp - 2) * 2 * L::EPI_BUF;
-    uint32_t stores = 0, unit = 0;
+    uint8_t* bufs = epi_buf + (warp - 2) * L::EPI_NBUF * L::EPI_BUF;
+    uint32_t stores = 0, unit = 0, notes = 0;
     bool ok = true;
-    for (int tile = worker; ok && tile < num_tiles; tile += workers) {
+    Segment seg;
+    for (int i = 0; ok && square_segment(p, worker, workers, i, seg); ++i) {
       int mt, nt;
-      tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+      tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
       const int c_row = mt * L::TILE_M + static_cast<int>(rank) * BM + 32 * q;
-      for (int c = 0; c < num_chunks; ++c, ++unit) {
+      const int n_chunks = (seg.kt1 - seg.kt0 + kpc - 1) / kpc;
+      // a partial segment's 32-bit values go to its scratch slot, rows of BN
+      uint32_t* slot = nullptr;
+      if (seg.partial)
+        slot = p.partials +
+               ((static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib + seg.j) * (128 * BN);
+      for (int c = 0; c < n_chunks; ++c, ++unit) {
         const uint32_t b = unit & 1u;
         const uint32_t use = unit >> 1;
         // every lane waits, and the warp leaves together: the tensor-memory
@@ -312,7 +433,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t t_acc = tmem_base + lane_base + b * BN;
-        const bool last_chunk = (c == num_chunks - 1);
+        const bool last_chunk = (c == n_chunks - 1);
 
         if constexpr (INT_EXACT) {
           const uint32_t t_sum = tmem_base + lane_base + 2 * BN;
@@ -322,20 +443,25 @@ __global__ void __launch_bounds__(192, 1)
             tmem_ld_32x32b_x32(t_acc + 32 * cb, v);
             tmem_wait_ld_regs(v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+            for (int i2 = 0; i2 < 32; ++i2) v[i2] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i2])));
             if (c > 0) {
               uint32_t s[32];
               tmem_ld_32x32b_x32(t_sum + 32 * cb, s);
               tmem_wait_ld_regs(s);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(static_cast<int32_t>(v[i]) + static_cast<int32_t>(s[i]));
+              for (int i2 = 0; i2 < 32; ++i2) v[i2] = static_cast<uint32_t>(static_cast<int32_t>(v[i2]) + static_cast<int32_t>(s[i2]));
             }
             if (!last_chunk) {
               tmem_st_32x32b_x32(t_sum + 32 * cb, v);
+            } else if (seg.partial) {
+              uint32_t* row = slot + (32 * q + lane) * BN + 32 * cb;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                __stcg(reinterpret_cast<uint4*>(row) + j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
             } else {
               // 32 int32 columns = one 128-byte row block
-              uint8_t* buf = bufs + (stores & 1u) * L::EPI_BUF;
-              if (lane == 0) bulk_wait_group_read<1>();
+              uint8_t* buf = bufs + (stores % L::EPI_NBUF) * L::EPI_BUF;
+              if (lane == 0) bulk_wait_group_read<L::EPI_NBUF - 1>();
               __syncwarp();
               uint8_t* row = buf + lane * 128;
 #pragma unroll
@@ -358,8 +484,8 @@ __global__ void __launch_bounds__(192, 1)
         } else {
           // One block = 32 output columns of this warp's 32 rows: 128-byte
           // rows (128-byte swizzle) for 4-byte outputs, 64-byte rows (64-byte
-          // swizzle) for 16-bit outputs; the TMA store unswizzles.
-          // The tensor-memory load of block cb+1 is in flight while block cb is
+          // swizzle) for 16-bit outputs; the TMA store unswizzles. The
+          // tensor-memory load of block cb+1 is in flight while block cb is
           // converted, staged and stored.
           uint32_t v[32];
           tmem_ld_32x32b_x32(t_acc, v);
@@ -369,45 +495,54 @@ __global__ void __launch_bounds__(192, 1)
             const bool more = cb + 1 < BN / 32;
             uint32_t nxt[32];
             if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
-            uint8_t* buf = bufs + (stores & 1u) * L::EPI_BUF;
-            if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf is done reading
-            __syncwarp();
-            if constexpr (OBYTES == 4) {
-              if constexpr (OUT == OUT_S32) {
+            if (seg.partial) {
+              // fp32 partial straight to scratch (128 contiguous bytes per lane)
+              uint32_t* row = slot + (32 * q + lane) * BN + 32 * cb;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
-              }
-              uint8_t* row = buf + lane * 128;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const uint4 q4 = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
-              }
+              for (int j = 0; j < 8; ++j)
+                __stcg(reinterpret_cast<uint4*>(row) + j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
             } else {
-              uint32_t w[16];
+              uint8_t* buf = bufs + (stores % L::EPI_NBUF) * L::EPI_BUF;
+              // the store that last used buf is done reading it
+              if (lane == 0) bulk_wait_group_read<L::EPI_NBUF - 1>();
+              __syncwarp();
+              if constexpr (OBYTES == 4) {
+                if constexpr (OUT == OUT_S32) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                w[i] = pack2<OUT>(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-              uint8_t* row = buf + lane * 64;
+                  for (int i2 = 0; i2 < 32; ++i2) v[i2] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i2])));
+                }
+                uint8_t* row = buf + lane * 128;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                *reinterpret_cast<uint4*>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = q4;
+                for (int j = 0; j < 8; ++j) {
+                  const uint4 q4 = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                  *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
+                }
+              } else {
+                uint32_t w[16];
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2)
+                  w[i2] = pack2<OUT>(__uint_as_float(v[2 * i2]), __uint_as_float(v[2 * i2 + 1]));
+                uint8_t* row = buf + lane * 64;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                  *reinterpret_cast<uint4*>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = q4;
+                }
               }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                // a block that starts past the matrix (ragged edge) stores nothing
+                if (c_row < p.M && nt * BN + 32 * cb < p.N)
+                  tma_store_2d(&tmC, smem_addr(buf), nt * BN + 32 * cb, c_row);
+                bulk_commit_group();
+              }
+              ++stores;
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              // a block that starts past the matrix (ragged edge) stores nothing
-              if (c_row < p.M && nt * BN + 32 * cb < p.N)
-                tma_store_2d(&tmC, smem_addr(buf), nt * BN + 32 * cb, c_row);
-              bulk_commit_group();
-            }
-            ++stores;
             if (more) {
               tmem_wait_ld_regs(nxt);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = nxt[i];
+              for (int i2 = 0; i2 < 32; ++i2) v[i2] = nxt[i2];
             }
           }
         }
@@ -420,9 +555,112 @@ __global__ void __launch_bounds__(192, 1)
             mbar_arrive(tempty_bar(b));
         }
       }
+      if (!ok || !seg.partial) continue;
+      // The partial is written: every writer makes its stores visible at GPU
+      // scope, then one thread posts the notice.
+      __threadfence();
+      named_barrier_sync(1, 128);
+      if (threadIdx.x == 64) {
+        const uint32_t j = notes & 1u, use = notes >> 1;
+        if (wait_bounded(note_empty(j), (use & 1u) ^ 1u, ctl, WAIT_FIXUP_SLOT))
+          mbar_arrive(note_full(j));
+      }
+      ++notes;
     }
     if (lane == 0) bulk_wait_group_read<0>();  // staging is free once the stores have read it
     if (warp == 2 && lane == 0) trace_mark(p.trace, TR_EPI_DONE);
+  } else if (p.sk_tiles > 0) {
+    // ---------------------------------------------- stream-K reduction warps
+    // For each partial tile this CTA wrote (the epilogue's notices, in
+    // segment order): count the arrival; the last of the tile's contributors
+    // adds all partials in contributor order and writes C.
+    const int tid = threadIdx.x - 192;  // 0..127
+    uint32_t notes = 0;
+    bool ok = true;
+    Segment seg;
+    for (int i = 0; ok && square_segment(p, worker, workers, i, seg); ++i) {
+      if (!seg.partial) continue;
+      const uint32_t j = notes & 1u, use = notes >> 1;
+      if (tid == 0) {
+        int flag = -1;
+        if (wait_bounded(note_full(j), use & 1u, ctl, WAIT_FIXUP_NOTE)) {
+          flag = arrive_generation(p.counters + seg.sk * 2 + rank, p.generation, seg.count,
+                                   p.error_word);
+          mbar_arrive(note_empty(j));  // the notice is consumed
+        }
+        fix_flag[j] = flag;
+      }
+      named_barrier_sync(2, 128);
+      const int flag = fix_flag[j];
+      ++notes;
+      if (flag < 0) {
+        ok = false;
+        break;
+      }
+      if (flag == 0) continue;
+      __threadfence();
+      int mt, nt;
+      tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+      const uint32_t* base =
+          p.partials + (static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib * (128 * BN);
+      constexpr int Q_PER_ROW = BN / 4;                  // 16-byte groups per row
+      constexpr int PER_THREAD = 128 * Q_PER_ROW / 128;  // groups per thread
+      constexpr int CH = 4;                              // groups per contributor in flight
+      constexpr int CB = 4;                              // contributors in flight
+      static_assert(PER_THREAD % CH == 0, "group rounds");
+      const int row0 = mt * L::TILE_M + static_cast<int>(rank) * BM;
+#pragma unroll 1
+      for (int g0 = 0; g0 < PER_THREAD; g0 += CH) {
+        uint4 acc[CH];
+#pragma unroll 1
+        for (int c0 = 0; c0 < seg.count; c0 += CB) {
+          // CB contributors' groups are loaded together, then added in order
+          uint4 v4[CB][CH];
+#pragma unroll
+          for (int cc = 0; cc < CB; ++cc) {
+            if (c0 + cc < seg.count) {
+              const uint4* pj = reinterpret_cast<const uint4*>(
+                  base + static_cast<int64_t>(c0 + cc) * (128 * BN));
+#pragma unroll
+              for (int i2 = 0; i2 < CH; ++i2) v4[cc][i2] = __ldcg(pj + tid + 128 * (g0 + i2));
+            }
+          }
+#pragma unroll
+          for (int cc = 0; cc < CB; ++cc) {
+            if (c0 + cc >= seg.count) break;
+#pragma unroll
+            for (int i2 = 0; i2 < CH; ++i2) {
+              if (c0 + cc == 0) {
+                acc[i2] = v4[cc][i2];
+              } else if constexpr (INT_EXACT) {
+                acc[i2].x = static_cast<uint32_t>(static_cast<int32_t>(acc[i2].x) + static_cast<int32_t>(v4[cc][i2].x));
+                acc[i2].y = static_cast<uint32_t>(static_cast<int32_t>(acc[i2].y) + static_cast<int32_t>(v4[cc][i2].y));
+                acc[i2].z = static_cast<uint32_t>(static_cast<int32_t>(acc[i2].z) + static_cast<int32_t>(v4[cc][i2].z));
+                acc[i2].w = static_cast<uint32_t>(static_cast<int32_t>(acc[i2].w) + static_cast<int32_t>(v4[cc][i2].w));
+              } else {
+                acc[i2].x = __float_as_uint(__uint_as_float(acc[i2].x) + __uint_as_float(v4[cc][i2].x));
+                acc[i2].y = __float_as_uint(__uint_as_float(acc[i2].y) + __uint_as_float(v4[cc][i2].y));
+                acc[i2].z = __float_as_uint(__uint_as_float(acc[i2].z) + __uint_as_float(v4[cc][i2].z));
+                acc[i2].w = __float_as_uint(__uint_as_float(acc[i2].w) + __uint_as_float(v4[cc][i2].w));
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int i2 = 0; i2 < CH; ++i2) {
+          const int g = tid + 128 * (g0 + i2);
+          const int r = row0 + g / Q_PER_ROW;
+          const int col = nt * BN + 4 * (g % Q_PER_ROW);
+          if (r < p.M && col < p.N) {
+            if constexpr (INT_EXACT || OUT == OUT_S32)
+              store_c4<OUT_S32>(p.C_out, static_cast<int64_t>(r) * p.N + col, acc[i2]);
+            else
+              store_c4<OUT>(p.C_out, static_cast<int64_t>(r) * p.N + col, acc[i2]);
+          }
+        }
+      }
+      if (tid == 0) trace_mark(p.trace, TR_FIXUP_DONE);
+    }
   }
 
   tc_fence_before();

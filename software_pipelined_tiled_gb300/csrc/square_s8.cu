@@ -8,12 +8,12 @@ namespace sptg {
 
 bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v) {
   if (bn != 128) return false;
-  if (!pair && (stages == 0 || stages == square_max_stages<128, false>())) {
-    *v = make_square<128, square_max_stages<128, false>(), false, OUT_S32, true, false>();
+  if (!pair && (stages == 0 || stages == square_max_stages<128, false, 4>())) {
+    *v = make_square<128, square_max_stages<128, false, 4>(), false, OUT_S32, true, false>();
     return true;
   }
-  if (pair && (stages == 0 || stages == square_max_stages<128, true>())) {
-    *v = make_square<128, square_max_stages<128, true>(), false, OUT_S32, true, true>();
+  if (pair && (stages == 0 || stages == square_max_stages<128, true, 4>())) {
+    *v = make_square<128, square_max_stages<128, true, 4>(), false, OUT_S32, true, true>();
     return true;
   }
   return false;

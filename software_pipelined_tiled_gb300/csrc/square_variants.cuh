@@ -10,25 +10,27 @@ namespace sptg {
 template <int BN, int ST, bool BF, int OUT, bool IE, bool PAIR>
 KernelVariant make_square() {
   return {reinterpret_cast<const void*>(&square_gemm_kernel<BN, ST, BF, OUT, IE, PAIR>), BN, ST,
-          SquareLayout<BN, ST, IE, PAIR>::SMEM_BYTES, PAIR};
+          SquareLayout<BN, ST, IE, PAIR, OutTraits<OUT>::bytes>::SMEM_BYTES, PAIR, SQUARE_THREADS};
 }
 
 // Tile widths BN in {256, 224, 192, 160, 128}, one CTA or a CTA pair per
 // tile, each at the deepest ring that fits (square_max_stages). For
-// binary16 -> binary16 also the shallower rings of BN 256 and 224 for the
-// pipelining ablation (1 = load, then compute, no overlap).
+// binary16 -> binary16 also the shallower rings of BN 256 and 224 (one CTA)
+// and of BN 224 (pair) for the pipelining ablation (1 = load, then compute,
+// no overlap).
 template <bool BF, int OUT>
 bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v) {
-#define SPTG_SQ(BNV)                                                                 \
-  case BNV:                                                                          \
-    if (!pair && (stages == 0 || stages == square_max_stages<BNV, false>())) {       \
-      *v = make_square<BNV, square_max_stages<BNV, false>(), BF, OUT, false, false>(); \
-      return true;                                                                   \
-    }                                                                                \
-    if (pair && (stages == 0 || stages == square_max_stages<BNV, true>())) {         \
-      *v = make_square<BNV, square_max_stages<BNV, true>(), BF, OUT, false, true>();   \
-      return true;                                                                   \
-    }                                                                                \
+  constexpr int OB = OutTraits<OUT>::bytes;
+#define SPTG_SQ(BNV)                                                                     \
+  case BNV:                                                                              \
+    if (!pair && (stages == 0 || stages == square_max_stages<BNV, false, OB>())) {       \
+      *v = make_square<BNV, square_max_stages<BNV, false, OB>(), BF, OUT, false, false>(); \
+      return true;                                                                       \
+    }                                                                                    \
+    if (pair && (stages == 0 || stages == square_max_stages<BNV, true, OB>())) {         \
+      *v = make_square<BNV, square_max_stages<BNV, true, OB>(), BF, OUT, false, true>();   \
+      return true;                                                                       \
+    }                                                                                    \
     break;
   switch (bn) {
     SPTG_SQ(256)
@@ -52,13 +54,14 @@ bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v) {
                                        : make_square<224, 3, false, OUT_F16, false, false>();
       return true;
     }
-    if (pair && bn == 224 && stages >= 1 && stages <= 5) {
+    if (pair && bn == 224 && stages >= 1 && stages <= 6) {
       switch (stages) {
         case 1: *v = make_square<224, 1, false, OUT_F16, false, true>(); return true;
         case 2: *v = make_square<224, 2, false, OUT_F16, false, true>(); return true;
         case 3: *v = make_square<224, 3, false, OUT_F16, false, true>(); return true;
         case 4: *v = make_square<224, 4, false, OUT_F16, false, true>(); return true;
-        default: *v = make_square<224, 5, false, OUT_F16, false, true>(); return true;
+        case 5: *v = make_square<224, 5, false, OUT_F16, false, true>(); return true;
+        default: *v = make_square<224, 6, false, OUT_F16, false, true>(); return true;
       }
     }
   }

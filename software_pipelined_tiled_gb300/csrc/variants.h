@@ -16,6 +16,7 @@ struct KernelVariant {
   int stages;      // shared-memory ring depth
   int smem;        // dynamic shared memory per CTA, bytes
   bool pair;       // square: 2-SM CTA-pair variant (cluster of 2)
+  int threads = 192;  // CTA size
 };
 
 // Square kernel for binary16 inputs (out_kind OUT_F16 or OUT_F32).

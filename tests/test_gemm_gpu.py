@@ -130,7 +130,7 @@ def test_cta_pair_operand_halves_are_not_swapped():
     assert torch.equal(C, expect)
 
 
-@pytest.mark.parametrize("stages", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("stages", [1, 2, 3, 4, 5, 6])
 def test_cta_pair_stage_count_does_not_change_the_arithmetic(stages):
     A, B = make_inputs(512, 448, 640, "f16", "uniform", 13)
     ref = run(A, B, F16, bn=224, cta_pair=2)
@@ -288,6 +288,86 @@ def test_skinny_f16_out_and_f32_out():
     A, B = make_inputs(40, 2048, 2048, "f16", "uniform", 10)
     assert_float_parity(run(A, B, F16, kernel="skinny"), A, B)
     assert_float_parity(run(A, B, F32, kernel="skinny"), A, B)
+
+
+# ------------------------------------------------------------ stream-K tiles
+def _sk_tiles():
+    return int(sptg.last_config().split("stream_k_tiles=")[1].split()[0])
+
+
+@pytest.mark.parametrize("cta_pair", [1, 2])
+@pytest.mark.parametrize("it,out", [("f16", F32), ("f16", F16), ("bf16", BF16), ("bf16", F32)])
+def test_stream_k_every_tile(cta_pair, it, out):
+    # every tile cut along K over five workers (ragged M, N and K): the
+    # partial sums go to scratch and the last contributor of each tile adds
+    # them up in contributor order
+    A, B = make_inputs(520, 776, 1096, it, "uniform", 40)
+    C = run(A, B, out, kernel="square", bn=224, cta_pair=cta_pair, stream_k=2, splits=5)
+    assert _sk_tiles() > 0 and f"pair={cta_pair - 1}" in sptg.last_config()
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("cta_pair", [1, 2])
+def test_stream_k_many_contributors(cta_pair):
+    # one tile, all workers: each holds 8 K-tiles of it, so the reduction
+    # adds dozens of partials
+    A, B = make_inputs(256, 256, 8192, "bf16", "normal", 41)
+    C = run(A, B, F32, kernel="square", bn=256, cta_pair=cta_pair, stream_k=2)
+    assert _sk_tiles() == (1 if cta_pair == 2 else 2)
+    assert "stream_k_workers=" in sptg.last_config()
+    assert int(sptg.last_config().split("stream_k_workers=")[1].split()[0]) >= 8
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("T,splits", [(17, 7), (40, 3), (9, 16)])
+def test_k_tile_marker_stream_k(T, splits):
+    # the K-tile marker through split tiles: a dropped, doubled or misplaced
+    # K-tile at a cut changes the exact result
+    A, B, expect = _marker_inputs(256, 512, T)
+    for cta_pair in (1, 2):
+        C = run(A, B, F32, kernel="square", bn=256, cta_pair=cta_pair, stream_k=2, splits=splits)
+        assert _sk_tiles() > 0
+        assert (C.to(torch.float64) == expect).all()
+
+
+@pytest.mark.parametrize("cta_pair", [1, 2])
+def test_stream_k_int8_exact(cta_pair):
+    # cuts fall inside the 1024-product chunks; the int32 partials add exactly
+    A, B = make_inputs(512, 384, 4160, "s8", "int8", 42)
+    C = run(A, B, I32, cta_pair=cta_pair, stream_k=2, splits=6)
+    assert _sk_tiles() > 0
+    assert_int_parity(C, A, B)
+    A = torch.full((130, 4096), -128, dtype=I8)
+    B = torch.full((136, 4096), -128, dtype=I8)
+    C = run(A, B, I32, cta_pair=cta_pair, stream_k=2, splits=7)
+    assert (C.to(torch.int64) == 16384 * 4096).all()
+
+
+def test_stream_k_is_deterministic_and_matches_data_parallel():
+    A, B = make_inputs(1024, 1536, 2048, "f16", "normal", 43)
+    c1 = run(A, B, F32, kernel="square", stream_k=2, splits=9)
+    c2 = run(A, B, F32, kernel="square", stream_k=2, splits=9)
+    assert torch.equal(c1, c2)
+    c3 = run(A, B, F32, kernel="square", stream_k=1)
+    assert _sk_tiles() == 0
+    assert_float_parity(c1, A, B)
+    assert_float_parity(c3, A, B)
+
+
+def test_stream_k_planned_for_a_partial_last_round():
+    # 4096 x 4096 in 256 x 256 pair tiles: 256 tiles over the pairs leave a
+    # partial last round, which the default schedule cuts along K
+    A, B = make_inputs(4096, 4096, 1024, "f16", "uniform", 44)
+    C = run(A, B, F16, bn=256, cta_pair=2)
+    cfg = sptg.last_config()
+    assert "pair=1" in cfg and "bn=256" in cfg and _sk_tiles() > 0, cfg
+    rows, cols = sample_positions(4096, 4096, 20000, seed=44)
+    # the stream-K tiles are the last tile indices, which the raster (strips
+    # of 8 m-tiles) puts in rows 2048.. and columns 3072..: sample them densely
+    extra = np.arange(2048, 4096, dtype=np.int64)
+    rows = np.concatenate([rows, extra])
+    cols = np.concatenate([cols, 3072 + extra * 37 % 1024])
+    assert_float_parity(C, A, B, rows, cols)
 
 
 # ------------------------------------------------------------ stream / errors
