@@ -29,6 +29,7 @@ enum WaitSite : unsigned int {
   WAIT_PLAN = 1u << 5,  // not a wait: a launch whose scratch plan does not fit
   WAIT_FIXUP_NOTE = 1u << 6,  // reduction warps: notice of a written partial tile
   WAIT_FIXUP_SLOT = 1u << 7,  // epilogue: a free notice slot
+  WAIT_FIXUP_PEERS = 1u << 8,  // reduction warps: the other contributors' arrivals
 };
 
 // Optional timeline: with a trace buffer, chosen threads stamp %globaltimer
@@ -166,6 +167,28 @@ __device__ __forceinline__ int arrive_generation(unsigned long long* ctr, unsign
   }
   atomicOr(error_word, WAIT_PLAN);
   return 0;
+}
+
+// Waits, for at most ctl.timeout_ns, until the counter holds `count`
+// arrivals of generation `gen` (see arrive_generation); false on time-out
+// (site WAIT_FIXUP_PEERS) or when another role raised the abort flag.
+__device__ __forceinline__ bool wait_arrivals(const unsigned long long* ctr, unsigned int gen,
+                                              int count, const WaitCtl& ctl) {
+  const unsigned long long want =
+      (static_cast<unsigned long long>(gen) << 32) | static_cast<unsigned int>(count);
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+    if (v == want) return true;
+    if (*ctl.abort_flag) return false;
+    if (global_timer_ns() - t0 > ctl.timeout_ns) {
+      *ctl.abort_flag = 1;
+      atomicOr(ctl.error_word, WAIT_FIXUP_PEERS);
+      return false;
+    }
+    __nanosleep(100);
+  }
 }
 
 // Tile index -> (m tile, n tile). Tiles are visited in column strips of

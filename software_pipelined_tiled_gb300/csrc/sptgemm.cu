@@ -429,9 +429,9 @@ void plan_stream_k(int T, int W, int KT, int mode, int* sk_tiles, int* sk_worker
 // Tile shape: one CTA (128 x BN) or a CTA pair (256 x BN) per tile. The
 // estimate is rounds x (tile rows x BN) x workers / measured rate, with
 // rounds = ceil(tiles / workers) for a data-parallel schedule and
-// tiles / workers + 0.5 when the last round goes through stream-K (the cut
-// tiles' partial writes and reductions measured at about half a round on
-// 4096 x 4096 x 4096). The cheapest estimate wins; ties keep the wider tile.
+// tiles / workers + 0.3 when the last round goes through stream-K (the cut
+// tiles' partial writes and reductions, as measured on 4096 x 4096 x 4096).
+// The cheapest estimate wins; ties keep the wider tile.
 void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sptg_config& cfg,
                          bool int8, int* bn_out, bool* pair_out) {
   double best = 1e300;
@@ -451,7 +451,7 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
       const int T = static_cast<int>(std::min<int64_t>(T64, INT32_MAX));
       int skt, skw, mc;
       plan_stream_k(T, W, KT, cfg.stream_k, &skt, &skw, &mc);
-      const double rounds = skt ? static_cast<double>(T) / W + 0.5
+      const double rounds = skt ? static_cast<double>(T) / W + 0.3
                                 : static_cast<double>((T + W - 1) / W);
       const double rate = pair ? kRatePair[i] : kRateSingle[i];
       const double cost = rounds * static_cast<double>(rows * bn) * W / rate;

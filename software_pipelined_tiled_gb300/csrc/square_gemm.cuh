@@ -46,12 +46,16 @@
 // (tile, K-tile) units per worker and done first; the remaining T - T mod W
 // tiles follow round robin, every worker the same number. A worker whose range
 // covers only part of a tile's K writes its fp32 (int32 in INT_EXACT mode)
-// partial tile to scratch; the last contributor to arrive (an atomic counter
-// tagged with the call's generation) adds the partials in contributor order
-// (= increasing k, a fixed order) and writes C. The epilogue only writes the
-// partial and posts a notice; four reduction warps of their own take the
-// arrival and the sum, so the accumulators keep draining and the K-loop of
-// the next tiles never waits for a reduction.
+// partial tile to scratch and counts its arrival (an atomic counter tagged
+// with the call's generation). Once all of a tile's contributors have
+// arrived, each contributor adds up its share of the rows over all partials
+// in contributor order (= increasing k, a fixed order) and writes C. The
+// epilogue writes the partial, counts the arrival and posts a notice; four
+// reduction warps of their own take the wait and the sum, so the
+// accumulators keep draining and the K-loop of the next tiles never waits
+// for a reduction. The wait needs every CTA of the grid resident at once,
+// which the persistent grid (one CTA, or pair, per SM slot) is; it is
+// bounded like every other wait.
 //
 // INT_EXACT mode computes an int8 product exactly on the fp16 tensor path: the
 // inputs are int8 values held as binary16 (exact), every product is an integer
@@ -79,7 +83,7 @@ struct SquareParams {
   int sk_tiles;
   int sk_workers;
   int max_contrib;              // partial slots per (tile, CTA of the pair)
-  uint32_t* partials;           // [sk_tile][rank][contributor][128][BN] 32-bit
+  uint32_t* partials;           // [sk_tile][rank][contributor][128 x BN] 32-bit
   unsigned long long* counters;  // [sk_tile * 2 + rank] (generation << 32 | arrivals)
   unsigned int generation;
   unsigned int* error_word;
@@ -419,11 +423,14 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
       const int c_row = mt * L::TILE_M + static_cast<int>(rank) * BM + 32 * q;
       const int n_chunks = (seg.kt1 - seg.kt0 + kpc - 1) / kpc;
-      // a partial segment's 32-bit values go to its scratch slot, rows of BN
-      uint32_t* slot = nullptr;
+      // A partial segment's 32-bit values go to its scratch slot as 16-byte
+      // groups in the order [32-column block][group of 4 columns][row]: the
+      // 32 lanes (32 consecutive rows) of one store write 512 contiguous bytes.
+      uint4* slot = nullptr;
       if (seg.partial)
-        slot = p.partials +
-               ((static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib + seg.j) * (128 * BN);
+        slot = reinterpret_cast<uint4*>(p.partials) +
+               ((static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib + seg.j) * (32 * BN) +
+               32 * q + lane;
       for (int c = 0; c < n_chunks; ++c, ++unit) {
         const uint32_t b = unit & 1u;
         const uint32_t use = unit >> 1;
@@ -454,10 +461,9 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
             if (!last_chunk) {
               tmem_st_32x32b_x32(t_sum + 32 * cb, v);
             } else if (seg.partial) {
-              uint32_t* row = slot + (32 * q + lane) * BN + 32 * cb;
 #pragma unroll
               for (int j = 0; j < 8; ++j)
-                __stcg(reinterpret_cast<uint4*>(row) + j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                __stcg(slot + (cb * 8 + j) * 128, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
             } else {
               // 32 int32 columns = one 128-byte row block
               uint8_t* buf = bufs + (stores % L::EPI_NBUF) * L::EPI_BUF;
@@ -496,11 +502,10 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
             uint32_t nxt[32];
             if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
             if (seg.partial) {
-              // fp32 partial straight to scratch (128 contiguous bytes per lane)
-              uint32_t* row = slot + (32 * q + lane) * BN + 32 * cb;
+              // fp32 partial straight to scratch
 #pragma unroll
               for (int j = 0; j < 8; ++j)
-                __stcg(reinterpret_cast<uint4*>(row) + j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                __stcg(slot + (cb * 8 + j) * 128, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
             } else {
               uint8_t* buf = bufs + (stores % L::EPI_NBUF) * L::EPI_BUF;
               // the store that last used buf is done reading it
@@ -557,10 +562,13 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       }
       if (!ok || !seg.partial) continue;
       // The partial is written: every writer makes its stores visible at GPU
-      // scope, then one thread posts the notice.
+      // scope, then one thread counts the arrival at the tile's counter (at
+      // once, so that no contributor waits on another's reductions) and
+      // posts the notice to the reduction warps.
       __threadfence();
       named_barrier_sync(1, 128);
       if (threadIdx.x == 64) {
+        arrive_generation(p.counters + seg.sk * 2 + rank, p.generation, seg.count, p.error_word);
         const uint32_t j = notes & 1u, use = notes >> 1;
         if (wait_bounded(note_empty(j), (use & 1u) ^ 1u, ctl, WAIT_FIXUP_SLOT))
           mbar_arrive(note_full(j));
@@ -572,8 +580,10 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   } else if (p.sk_tiles > 0) {
     // ---------------------------------------------- stream-K reduction warps
     // For each partial tile this CTA wrote (the epilogue's notices, in
-    // segment order): count the arrival; the last of the tile's contributors
-    // adds all partials in contributor order and writes C.
+    // segment order): wait until all the tile's contributors have arrived,
+    // then add up this contributor's share of this CTA's 128 rows over all
+    // partials in contributor order and write it to C. Every contributor so
+    // reduces a part of the tile, and no CTA carries a whole reduction.
     const int tid = threadIdx.x - 192;  // 0..127
     uint32_t notes = 0;
     bool ok = true;
@@ -582,35 +592,52 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       if (!seg.partial) continue;
       const uint32_t j = notes & 1u, use = notes >> 1;
       if (tid == 0) {
-        int flag = -1;
+        int flag = 0;
         if (wait_bounded(note_full(j), use & 1u, ctl, WAIT_FIXUP_NOTE)) {
-          flag = arrive_generation(p.counters + seg.sk * 2 + rank, p.generation, seg.count,
-                                   p.error_word);
           mbar_arrive(note_empty(j));  // the notice is consumed
+          flag = wait_arrivals(p.counters + seg.sk * 2 + rank, p.generation, seg.count, ctl) ? 1
+                                                                                          : 0;
         }
         fix_flag[j] = flag;
       }
       named_barrier_sync(2, 128);
       const int flag = fix_flag[j];
       ++notes;
-      if (flag < 0) {
+      if (!flag) {
         ok = false;
         break;
       }
-      if (flag == 0) continue;
       __threadfence();
       int mt, nt;
       tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
-      const uint32_t* base =
-          p.partials + (static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib * (128 * BN);
-      constexpr int Q_PER_ROW = BN / 4;                  // 16-byte groups per row
-      constexpr int PER_THREAD = 128 * Q_PER_ROW / 128;  // groups per thread
-      constexpr int CH = 4;                              // groups per contributor in flight
-      constexpr int CB = 4;                              // contributors in flight
-      static_assert(PER_THREAD % CH == 0, "group rounds");
+      const uint4* base = reinterpret_cast<const uint4*>(p.partials) +
+                          (static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib * (32 * BN);
+      // This contributor's rows: the first and the last contributor of a
+      // tile usually hold a cut of another tile as well, so they take a half
+      // share each and the ones in between a whole share (in half shares:
+      // [0, 1), [1, 3), [3, 5), ..., [2 count - 3, 2 count - 2)).
+      const int halves = 2 * seg.count - 2;
+      const int h0 = seg.j == 0 ? 0 : 2 * seg.j - 1;
+      const int h1 = seg.j == seg.count - 1 ? halves : 2 * seg.j + 1;
+      const int r0 = 128 * h0 / halves;
+      const int nr = 128 * h1 / halves - r0;
+      // Flat index f over this share: group g = f % 8 of four columns,
+      // row r0 + (f / 8) % nr, 32-column block f / (8 nr). A warp reads
+      // 64-byte runs of the partials and writes whole row segments of C.
+      const int total = nr * (BN / 4);
+      constexpr int CH = 4;  // groups per contributor in flight
+      constexpr int CB = 4;  // contributors in flight
       const int row0 = mt * L::TILE_M + static_cast<int>(rank) * BM;
 #pragma unroll 1
-      for (int g0 = 0; g0 < PER_THREAD; g0 += CH) {
+      for (int f0 = 0; f0 < total; f0 += 128 * CH) {
+        int idx[CH];
+#pragma unroll
+        for (int i2 = 0; i2 < CH; ++i2) {
+          const int f = f0 + tid + 128 * i2;
+          const int rest = f >> 3;
+          const int cb = rest / max(nr, 1);
+          idx[i2] = f < total ? ((cb * 8 + (f & 7)) * 128 + r0 + (rest - cb * nr)) : -1;
+        }
         uint4 acc[CH];
 #pragma unroll 1
         for (int c0 = 0; c0 < seg.count; c0 += CB) {
@@ -619,10 +646,10 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
 #pragma unroll
           for (int cc = 0; cc < CB; ++cc) {
             if (c0 + cc < seg.count) {
-              const uint4* pj = reinterpret_cast<const uint4*>(
-                  base + static_cast<int64_t>(c0 + cc) * (128 * BN));
+              const uint4* pj = base + static_cast<int64_t>(c0 + cc) * (32 * BN);
 #pragma unroll
-              for (int i2 = 0; i2 < CH; ++i2) v4[cc][i2] = __ldcg(pj + tid + 128 * (g0 + i2));
+              for (int i2 = 0; i2 < CH; ++i2)
+                if (idx[i2] >= 0) v4[cc][i2] = __ldcg(pj + idx[i2]);
             }
           }
 #pragma unroll
@@ -630,6 +657,7 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
             if (c0 + cc >= seg.count) break;
 #pragma unroll
             for (int i2 = 0; i2 < CH; ++i2) {
+              if (idx[i2] < 0) continue;
               if (c0 + cc == 0) {
                 acc[i2] = v4[cc][i2];
               } else if constexpr (INT_EXACT) {
@@ -648,9 +676,10 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
         }
 #pragma unroll
         for (int i2 = 0; i2 < CH; ++i2) {
-          const int g = tid + 128 * (g0 + i2);
-          const int r = row0 + g / Q_PER_ROW;
-          const int col = nt * BN + 4 * (g % Q_PER_ROW);
+          if (idx[i2] < 0) continue;
+          const int g = idx[i2] >> 7;  // cb * 8 + group
+          const int r = row0 + (idx[i2] & 127);
+          const int col = nt * BN + 4 * g;
           if (r < p.M && col < p.N) {
             if constexpr (INT_EXACT || OUT == OUT_S32)
               store_c4<OUT_S32>(p.C_out, static_cast<int64_t>(r) * p.N + col, acc[i2]);

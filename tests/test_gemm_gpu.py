@@ -354,11 +354,11 @@ def test_stream_k_is_deterministic_and_matches_data_parallel():
     assert_float_parity(c3, A, B)
 
 
-def test_stream_k_planned_for_a_partial_last_round():
+def test_stream_k_chosen_for_a_partial_last_round():
     # 4096 x 4096 in 256 x 256 pair tiles: 256 tiles over the pairs leave a
     # partial last round, which the default schedule cuts along K
     A, B = make_inputs(4096, 4096, 1024, "f16", "uniform", 44)
-    C = run(A, B, F16, bn=256, cta_pair=2)
+    C = run(A, B, F16)
     cfg = sptg.last_config()
     assert "pair=1" in cfg and "bn=256" in cfg and _sk_tiles() > 0, cfg
     rows, cols = sample_positions(4096, 4096, 20000, seed=44)
