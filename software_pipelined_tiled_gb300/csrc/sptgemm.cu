@@ -426,17 +426,19 @@ void plan_stream_k(int T, int W, int KT, int mode, int* sk_tiles, int* sk_worker
   *max_contrib = std::min(mc, sw);
 }
 
-// Tile shape: one CTA (128 x BN) or a CTA pair (256 x BN) per tile. The
-// estimate is rounds x (tile rows x BN) x workers / measured rate, with
-// rounds = ceil(tiles / workers) for a data-parallel schedule and
-// tiles / workers + 0.3 when the last round goes through stream-K (the cut
-// tiles' partial writes and reductions, as measured on 4096 x 4096 x 4096).
-// The cheapest estimate wins; ties keep the wider tile.
+// Tile shape and schedule: one CTA (128 x BN) or a CTA pair (256 x BN) per
+// tile, data-parallel or with a partial last round cut along K. The estimate
+// is rounds x (tile rows x BN) x workers / measured rate, with rounds =
+// ceil(tiles / workers) for the data-parallel schedule and tiles / workers
+// + 0.3 with stream-K (the cut tiles' partial writes and reductions, as
+// measured on 4096 x 4096 x 4096). The cheapest estimate wins; ties keep the
+// wider tile and the data-parallel schedule.
 void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sptg_config& cfg,
-                         bool int8, int* bn_out, bool* pair_out) {
+                         bool int8, int* bn_out, bool* pair_out, bool* sk_out) {
   double best = 1e300;
   *bn_out = 256;
   *pair_out = false;
+  *sk_out = false;
   const int KT = static_cast<int>((K + 63) / 64);
   for (int pair = 0; pair < 2; ++pair) {
     if ((cfg.cta_pair == 1 && pair) || (cfg.cta_pair == 2 && !pair)) continue;
@@ -446,19 +448,26 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
     for (int i = 0; i < 5; ++i) {
       const int bn = kTileWidths[i];
       if (cfg.bn && bn != cfg.bn) continue;
-      if (int8 && bn != 128) continue;
+      if (int8 && bn != 128 && bn != 160) continue;  // 3 x BN tensor-memory columns
       const int64_t T64 = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
       const int T = static_cast<int>(std::min<int64_t>(T64, INT32_MAX));
-      int skt, skw, mc;
-      plan_stream_k(T, W, KT, cfg.stream_k, &skt, &skw, &mc);
-      const double rounds = skt ? static_cast<double>(T) / W + 0.3
-                                : static_cast<double>((T + W - 1) / W);
-      const double rate = pair ? kRatePair[i] : kRateSingle[i];
-      const double cost = rounds * static_cast<double>(rows * bn) * W / rate;
-      if (cost < best) {
-        best = cost;
-        *bn_out = bn;
-        *pair_out = pair != 0;
+      const double work = static_cast<double>(rows * bn) * W / (pair ? kRatePair[i] : kRateSingle[i]);
+      for (int sk = 0; sk < 2; ++sk) {
+        double rounds = static_cast<double>((T + W - 1) / W);
+        if (sk) {
+          if (cfg.stream_k == 1) continue;
+          int skt, skw, mc;
+          plan_stream_k(T, W, KT, 0, &skt, &skw, &mc);
+          if (skt == 0) continue;
+          rounds = static_cast<double>(T) / W + 0.3;
+        }
+        const double cost = rounds * work;
+        if (cost < best) {
+          best = cost;
+          *bn_out = bn;
+          *pair_out = pair != 0;
+          *sk_out = sk != 0;
+        }
       }
     }
   }
@@ -475,8 +484,8 @@ struct SquarePlan {
 int plan_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N,
                 int64_t K, const sptg_config& cfg, SquarePlan* pl) {
   int bn = 0;
-  bool pair = false;
-  choose_square_shape(M, N, K, di.sm_count, cfg, d.is_int8, &bn, &pair);
+  bool pair = false, sk = false;
+  choose_square_shape(M, N, K, di.sm_count, cfg, d.is_int8, &bn, &pair, &sk);
   if (!pick_square(d, bn, cfg.stages, pair, &pl->v)) {
     // a forced ring depth may exist for the other tile mode only
     if (cfg.cta_pair == 0 && pick_square(d, bn, cfg.stages, !pair, &pl->v)) {
@@ -496,8 +505,8 @@ int plan_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, in
   const int tiles = pl->m_tiles * pl->n_tiles;
   int workers = pair ? pair_slots(dev, pl->v, di.sm_count) : di.sm_count;
   if (cfg.splits > 0) workers = std::min(workers, cfg.splits);
-  plan_stream_k(tiles, workers, pl->k_tiles, cfg.stream_k, &pl->sk_tiles, &pl->sk_workers,
-                &pl->max_contrib);
+  plan_stream_k(tiles, workers, pl->k_tiles, cfg.stream_k == 2 ? 2 : (sk ? 0 : 1), &pl->sk_tiles,
+                &pl->sk_workers, &pl->max_contrib);
   if (pl->sk_tiles == 0)
     workers = std::min(workers, tiles);
   else if (pl->sk_tiles == tiles)

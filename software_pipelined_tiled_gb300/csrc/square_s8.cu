@@ -6,16 +6,24 @@
 
 namespace sptg {
 
+// Tile widths 128 and 160: two accumulators and the int32 running sum,
+// 3 x BN tensor-memory columns, fit the 512 columns up to BN = 160.
 bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v) {
-  if (bn != 128) return false;
-  if (!pair && (stages == 0 || stages == square_max_stages<128, false, 4>())) {
-    *v = make_square<128, square_max_stages<128, false, 4>(), false, OUT_S32, true, false>();
-    return true;
+#define SPTG_S8(BNV)                                                                      \
+  if (bn == BNV) {                                                                        \
+    if (!pair && (stages == 0 || stages == square_max_stages<BNV, false, 4>())) {          \
+      *v = make_square<BNV, square_max_stages<BNV, false, 4>(), false, OUT_S32, true, false>(); \
+      return true;                                                                        \
+    }                                                                                     \
+    if (pair && (stages == 0 || stages == square_max_stages<BNV, true, 4>())) {            \
+      *v = make_square<BNV, square_max_stages<BNV, true, 4>(), false, OUT_S32, true, true>();   \
+      return true;                                                                        \
+    }                                                                                     \
+    return false;                                                                         \
   }
-  if (pair && (stages == 0 || stages == square_max_stages<128, true, 4>())) {
-    *v = make_square<128, square_max_stages<128, true, 4>(), false, OUT_S32, true, true>();
-    return true;
-  }
+  SPTG_S8(128)
+  SPTG_S8(160)
+#undef SPTG_S8
   return false;
 }
 

@@ -214,6 +214,14 @@ def test_int8_exact_cta_pair(M, N, K):
     assert_int_parity(C, A, B)
 
 
+@pytest.mark.parametrize("bn,cta_pair", [(160, 1), (160, 2), (128, 1), (128, 2)])
+def test_int8_exact_every_width(bn, cta_pair):
+    A, B = make_inputs(520, 488, 3136, "s8", "int8", 50 + bn)
+    C = run(A, B, I32, bn=bn, cta_pair=cta_pair)
+    assert f"bn={bn}" in sptg.last_config()
+    assert_int_parity(C, A, B)
+
+
 @pytest.mark.parametrize("K", [1024, 1040, 4096])
 def test_int8_extremes_exact(K):
     # every chunk of 1024 products reaches 2^24 exactly
