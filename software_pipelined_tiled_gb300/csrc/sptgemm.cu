@@ -443,6 +443,9 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
   for (int pair = 0; pair < 2; ++pair) {
     if ((cfg.cta_pair == 1 && pair) || (cfg.cta_pair == 2 && !pair)) continue;
     if (pair && M <= 128 && cfg.cta_pair != 2) continue;  // one CTA already covers all rows
+    // exact int8: one-CTA tiles measured faster (the chunk conversions of
+    // the epilogue weigh more against the pair's shorter K-loop)
+    if (pair && int8 && cfg.cta_pair != 2) continue;
     const int64_t rows = pair ? 256 : 128;
     const int W = pair ? sm_count / 2 : sm_count;
     for (int i = 0; i < 5; ++i) {
@@ -920,11 +923,13 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
     void* A16 = ws.data;
     void* B16 = static_cast<char*>(ws.data) + a_pad;
     const int64_t na = M * K / 16, nb = N * K / 16;
-    const int blocks_a = static_cast<int>(std::min<int64_t>((na + 255) / 256, 8 * di.sm_count));
-    const int blocks_b = static_cast<int>(std::min<int64_t>((nb + 255) / 256, 8 * di.sm_count));
-    cudaError_t e = launch_s8_to_f16(A, A16, na, blocks_a, stream_h);
-    if (e == cudaSuccess) e = launch_s8_to_f16(B, B16, nb, blocks_b, stream_h);
-    t_launches += 2;
+    // two 256-thread blocks per SM, each thread with eight loads in flight
+    const int blocks = static_cast<int>(std::min<int64_t>((na + nb + 255) / 256, 2 * di.sm_count));
+    // A plain launch: under programmatic overlap its blocks would sit on the
+    // SMs beside the previous GEMM's CTAs, which measured 14 us slower per
+    // call on 4096^3. The GEMM that follows still overlaps this kernel's tail.
+    cudaError_t e = launch_s8_to_f16(A, A16, na, B, B16, nb, blocks, stream_h, false);
+    t_launches += 1;
     if (e != cudaSuccess) return cuda_fail(e, "s8_to_f16 launch");
     return launch_square(di, d, M, N, K, A16, B16, C, stream_h, cfg, pl,
                          static_cast<char*>(ws.data) + a_pad + b_pad, ws.counters, ws.generation);

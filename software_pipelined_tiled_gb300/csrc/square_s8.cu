@@ -1,6 +1,8 @@
 // square_s8.cu -- the square kernel in exact-integer mode (int8 operands held
 // as binary16, fp32 chunk accumulators of at most 1024 products, int32 sums),
 // and the int8 -> binary16 widening kernel it runs after.
+#include <cstring>
+
 #include "convert.cuh"
 #include "square_variants.cuh"
 
@@ -27,11 +29,22 @@ bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v) {
   return false;
 }
 
-cudaError_t launch_s8_to_f16(const void* src, void* dst, int64_t n16, int blocks,
-                             cudaStream_t stream) {
-  s8_to_f16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const int4*>(src),
-                                               static_cast<uint4*>(dst), n16);
-  return cudaGetLastError();
+cudaError_t launch_s8_to_f16(const void* srcA, void* dstA, int64_t na16, const void* srcB,
+                             void* dstB, int64_t nb16, int blocks, cudaStream_t stream,
+                             bool overlap_previous) {
+  cudaLaunchConfig_t lc;
+  memset(&lc, 0, sizeof(lc));
+  lc.gridDim = dim3(blocks, 1, 1);
+  lc.blockDim = dim3(256, 1, 1);
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = overlap_previous ? attr : nullptr;
+  lc.numAttrs = overlap_previous ? 1 : 0;
+  return cudaLaunchKernelEx(&lc, s8_to_f16_kernel, static_cast<const int4*>(srcA),
+                            static_cast<uint4*>(dstA), na16, static_cast<const int4*>(srcB),
+                            static_cast<uint4*>(dstB), nb16);
 }
 
 }  // namespace sptg

@@ -33,8 +33,10 @@ bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
 bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
 // The streaming ring out = alpha * in (bn = tile bytes).
 KernelVariant stream_variant();
-// int8 -> binary16 widening of n16 groups of 16 elements.
-cudaError_t launch_s8_to_f16(const void* src, void* dst, int64_t n16, int blocks,
-                             cudaStream_t stream);
+// int8 -> binary16 widening of both operands in one launch (na16 and nb16
+// groups of 16 elements), allowed to overlap the previous kernel's tail.
+cudaError_t launch_s8_to_f16(const void* srcA, void* dstA, int64_t na16, const void* srcB,
+                             void* dstB, int64_t nb16, int blocks, cudaStream_t stream,
+                             bool overlap_previous);
 
 }  // namespace sptg
