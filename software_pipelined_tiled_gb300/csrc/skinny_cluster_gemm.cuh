@@ -31,37 +31,42 @@ struct SkinnyClusterParams {
   unsigned long long* trace;
 };
 
-template <int MN, int STAGES, int OBYTES>
+// One ring stage holds KSUB consecutive 64-wide K-chunks of B^T (128 rows)
+// and of A (MN rows), each chunk its own 128-byte-swizzled sub-tile.
+template <int MN, int STAGES, int OBYTES, int KSUB = 1>
 struct SkinnyClusterLayout {
   static constexpr int BNT = 128;
   static constexpr int BK = 64;
-  static constexpr int BT_STAGE = BNT * BK * 2;
-  static constexpr int A_STAGE = MN * BK * 2;
+  static constexpr int SUB_BT = BNT * BK * 2;
+  static constexpr int SUB_A = MN * BK * 2;
+  static constexpr int BT_STAGE = KSUB * SUB_BT;
+  static constexpr int A_STAGE = KSUB * SUB_A;
   static constexpr int STAGE = BT_STAGE + A_STAGE;
-  // receive buffer for the peer's partial: a row of MN floats per output
-  // column, plus 16 bytes so that 16-byte accesses of 8 consecutive rows hit
-  // 8 distinct bank groups
+  // receive buffer for the peer's partial: a row of MN floats for each of the
+  // 64 columns this rank finalises, plus 16 bytes so that 16-byte accesses of
+  // 8 consecutive rows hit 8 distinct bank groups
   static constexpr int PART_ROW = MN * 4 + 16;
-  static constexpr int PART_BYTES = BNT * PART_ROW;
   // output staging (reuses the receive buffer once it has been read): MN rows
-  // of 128 outputs, the layout of C
+  // of up to 128 outputs, the layout of C
   static constexpr int OUT_BYTES = MN * BNT * OBYTES;
+  static constexpr int PART_BYTES = 64 * PART_ROW > OUT_BYTES ? 64 * PART_ROW : OUT_BYTES;
   static constexpr int OFF_PART = STAGES * STAGE;
   static constexpr int OFF_BAR = OFF_PART + PART_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 3;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int TMEM_COLS = MN <= 32 ? 32 : MN <= 64 ? 64 : 128;
-  static_assert(OUT_BYTES <= PART_BYTES, "output staging reuses the receive buffer");
   static_assert(OFF_PART % 1024 == 0, "receive buffer alignment");
+  static_assert(PART_BYTES % 16 == 0, "barrier alignment");
   static_assert(MN % 32 == 0 && MN >= 32 && MN <= 128, "MN must be 32, 64, 96 or 128");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 };
 
 // Deepest ring next to the receive buffer within the 227 KB budget.
-template <int MN>
+template <int MN, int OBYTES, int KSUB = 1>
 constexpr int skinny_cluster_stages() {
-  return (232448 - 1024 - 128 * (MN * 4 + 16) - 512) / (128 * 64 * 2 + MN * 64 * 2);
+  using L1 = SkinnyClusterLayout<MN, 1, OBYTES, KSUB>;
+  return (232448 - 1024 - L1::PART_BYTES - 512) / L1::STAGE;
 }
 
 // 16-byte store into the shared memory of a CTA of the cluster.
@@ -77,14 +82,14 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   return n;
 }
 
-template <int MN, int STAGES, bool IN_BF16, int OUT>
+template <int MN, int STAGES, bool IN_BF16, int OUT, int KSUB = 1>
 __global__ void __launch_bounds__(192, 1)
     skinny_cluster_gemm_kernel(const __grid_constant__ CUtensorMap tmBt,
                                const __grid_constant__ CUtensorMap tmA,
                                const __grid_constant__ CUtensorMap tmC,
                                const SkinnyClusterParams p) {
   constexpr int OBYTES = OutTraits<OUT>::bytes;
-  using L = SkinnyClusterLayout<MN, STAGES, OBYTES>;
+  using L = SkinnyClusterLayout<MN, STAGES, OBYTES, KSUB>;
   constexpr int BNT = L::BNT, BK = L::BK;
   constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, BNT, MN);
   static_assert(OUT != OUT_S32, "float outputs only");
@@ -146,8 +151,11 @@ __global__ void __launch_bounds__(192, 1)
   // writes these operands: the loads proper come after the dependency wait.
   if (threadIdx.x == 0) {
     for (int kt = kt0; kt < min(kt1, kt0 + STAGES); ++kt) {
-      tma_prefetch_l2_2d(&tmBt, kt * BK, nt * BNT);
-      tma_prefetch_l2_2d(&tmA, kt * BK, 0);
+#pragma unroll
+      for (int j = 0; j < KSUB; ++j) {
+        tma_prefetch_l2_2d(&tmBt, (kt * KSUB + j) * BK, nt * BNT);
+        tma_prefetch_l2_2d(&tmA, (kt * KSUB + j) * BK, 0);
+      }
     }
   }
   grid_dependency_wait();
@@ -173,8 +181,13 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (p.inject_stall && it == 1) continue;  // test hook: this stage never fills
         mbar_arrive_expect_tx(full_bar(s), L::STAGE);
-        tma_load_2d(stage_bt(s), &tmBt, full_bar(s), kt * BK, nt * BNT, pol_stream);
-        tma_load_2d(stage_a(s), &tmA, full_bar(s), kt * BK, 0, pol_keep);
+#pragma unroll
+        for (int j = 0; j < KSUB; ++j) {
+          tma_load_2d(stage_bt(s) + j * L::SUB_BT, &tmBt, full_bar(s), (kt * KSUB + j) * BK,
+                      nt * BNT, pol_stream);
+          tma_load_2d(stage_a(s) + j * L::SUB_A, &tmA, full_bar(s), (kt * KSUB + j) * BK, 0,
+                      pol_keep);
+        }
         issued_round[s] = static_cast<int>(round);
         if (it == 0) trace_mark(p.trace, TR_FIRST_LOAD);
         trace_ktile(p.trace, 0, it);
@@ -207,10 +220,13 @@ __global__ void __launch_bounds__(192, 1)
         if (it == 0) trace_mark(p.trace, TR_FIRST_DATA);
         trace_ktile(p.trace, 1, it);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          mma_f16(tmem_base, sdesc_k_major_sw128(stage_bt(s) + 32 * k),
-                  sdesc_k_major_sw128(stage_a(s) + 32 * k), IDESC,
-                  (kt > kt0 || k > 0) ? 1u : 0u);
+        for (int j = 0; j < KSUB; ++j) {
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            mma_f16(tmem_base, sdesc_k_major_sw128(stage_bt(s) + j * L::SUB_BT + 32 * k),
+                    sdesc_k_major_sw128(stage_a(s) + j * L::SUB_A + 32 * k), IDESC,
+                    (kt > kt0 || j > 0 || k > 0) ? 1u : 0u);
+          }
         }
         mma_commit(empty_bar(s));
       }

@@ -700,7 +700,8 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   }
   const int BNT = 128, BK = 64;
   const int n_tiles = static_cast<int>((N + BNT - 1) / BNT);
-  const int k_tiles = static_cast<int>((K + BK - 1) / BK);
+  const int kstep = BK * v.ksub;  // K per ring stage
+  const int k_tiles = static_cast<int>((K + kstep - 1) / kstep);
   // cluster size: forced (splits), else 2 when two CTAs per column tile fit
   // the SMs, else 1; taken only if the grid fills at least three quarters of
   // the SMs
@@ -752,7 +753,7 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   set_config(
       "kernel=skinny-cluster dtype=%s mma_m=%lld mma_n=%lld bk=%lld stages=%lld grid=%lld "
       "cluster=%lld n_tiles=%lld k_tiles=%lld smem=%lld",
-      d.name, {BNT, v.bn, BK, v.stages, grid, cs, n_tiles, k_tiles, v.smem});
+      d.name, {BNT, v.bn, kstep, v.stages, grid, cs, n_tiles, k_tiles, v.smem});
   return SPTG_OK;
 }
 

@@ -17,6 +17,7 @@ struct KernelVariant {
   int smem;        // dynamic shared memory per CTA, bytes
   bool pair;       // square: 2-SM CTA-pair variant (cluster of 2)
   int threads = 192;  // CTA size
+  int ksub = 1;       // skinny cluster: 64-wide K-chunks per ring stage
 };
 
 // Square kernel for binary16 inputs (out_kind OUT_F16 or OUT_F32).
