@@ -115,6 +115,26 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype,
                  const sptg_config* cfg);
 
 /*
+ * sptg_gemm_ex on matrices inside larger row-pitched buffers ("Pipeline GPU
+ * Kernel", pitfalls: boundary handling; the tiles are read and written
+ * through the row pitch, never past a row's K or N elements).
+ *
+ *   lda  elements between rows of A        (>= K)
+ *   ldb  elements between the K-long columns of B, i.e. rows of the N x K
+ *        array Bcm                          (>= K)
+ *   ldc  elements between rows of C        (>= N)
+ *
+ * Besides the alignment rules of sptg_gemm (which still apply to K and N),
+ * lda * sizeof(in), ldb * sizeof(in) and ldc * sizeof(out) must be multiples
+ * of 16 bytes (SPTG_ERR_ALIGN), and each leading dimension must be below
+ * 2^31 (SPTG_ERR_ARG). Elements between N and ldc of a row of C are never
+ * written. lda = ldb = K and ldc = N give sptg_gemm_ex.
+ */
+int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, int dtype,
+                      const void* A, int64_t lda, const void* B, int64_t ldb,
+                      void* C, int64_t ldc, void* stream, const sptg_config* cfg);
+
+/*
  * The software-pipelined ring on its own: out[i] = alpha * in[i] for
  * i < n, binary32, one rounding per element. This is the minimal working
  * example of "Hiding Memory Latency in CUDA: Asynchronous Loads and Software

@@ -19,7 +19,8 @@ import threading
 
 from ._build import LIB_PATH, build
 
-__all__ = ["DTYPES", "SptgError", "Config", "load", "gemm", "gemm_raw", "gemm_skinny_noalloc_raw",
+__all__ = ["DTYPES", "SptgError", "Config", "load", "gemm", "gemm_raw", "gemm_strided_raw",
+           "gemm_skinny_noalloc_raw",
            "stream_scale",
            "last_config",
            "last_error", "device_error", "status_string", "LIB_PATH", "build"]
@@ -32,7 +33,7 @@ STATUS = {0: "SPTG_OK", -1: "SPTG_ERR_ARG", -2: "SPTG_ERR_ALIGN", -3: "SPTG_ERR_
 KERNELS = {"auto": 0, "square": 1, "skinny": 2, "skinny_cluster": 3}
 
 # the C functions every build must export (checked by the tests)
-EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_status_string", "sptg_last_error",
+EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_gemm_strided", "sptg_status_string", "sptg_last_error",
            "sptg_last_config", "sptg_device_error", "sptg_version", "sptg_gemm_skinny_noalloc",
            "sptg_stream_scale", "sptg_stream_scale_ex")
 
@@ -72,6 +73,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sptg_gemm_ex.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp,
                                      ctypes.POINTER(Config)]
         lib.sptg_gemm_ex.restype = ctypes.c_int
+        lib.sptg_gemm_strided.argtypes = [i64, i64, i64, ctypes.c_int, vp, i64, vp, i64, vp, i64,
+                                          vp, ctypes.POINTER(Config)]
+        lib.sptg_gemm_strided.restype = ctypes.c_int
         lib.sptg_status_string.argtypes = [ctypes.c_int]
         lib.sptg_status_string.restype = ctypes.c_char_p
         lib.sptg_last_error.argtypes = []
@@ -126,6 +130,16 @@ def gemm_raw(M: int, N: int, K: int, dtype: str | int, A_ptr: int, B_ptr: int, C
     return int((_lib or load()).sptg_gemm_ex(M, N, K, d, A_ptr, B_ptr, C_ptr, stream, cfg))
 
 
+def gemm_strided_raw(M: int, N: int, K: int, dtype: str | int, A_ptr: int, lda: int, B_ptr: int,
+                     ldb: int, C_ptr: int, ldc: int, stream: int = 0,
+                     config: Config | None = None) -> int:
+    """Calls sptg_gemm_strided (leading dimensions in elements); returns the status code."""
+    d = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    cfg = ctypes.byref(config) if config is not None else None
+    return int((_lib or load()).sptg_gemm_strided(M, N, K, d, A_ptr, lda, B_ptr, ldb, C_ptr, ldc,
+                                                  stream, cfg))
+
+
 def gemm_skinny_noalloc_raw(M: int, N: int, K: int, dtype: str | int, A_ptr: int, B_ptr: int,
                             C_ptr: int, stream: int = 0) -> int:
     """Calls sptg_gemm_skinny_noalloc (the skinny kernel with its split-K
@@ -145,13 +159,23 @@ def _dtype_key(in_dtype, out_dtype) -> str:
     return key
 
 
+def _row_pitch(t, name: str) -> int:
+    """Elements between rows of a 2-D tensor whose rows are contiguous."""
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1) or t.stride(0) < t.shape[1]:
+        raise ValueError(f"{name} must be a 2-D tensor with contiguous rows (stride(1) == 1)")
+    return max(int(t.stride(0)), int(t.shape[1]))
+
+
 def gemm(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = None,
          kernel: str | None = None, stages: int = 0, bn: int = 0, splits: int = 0,
          cta_pair: int = 0, stream_k: int = 0):
     """C = A * B on the GPU, with A (M x K) and Bcm (N x K) CUDA tensors.
 
-    out_dtype defaults to the input type for binary16/bfloat16 and int32 for
-    int8.  Returns C.  Raises SptgError on any failure.
+    Each of A, Bcm and C may be a row-strided view (contiguous rows, any row
+    pitch meeting the library's 16-byte rule), e.g. a column slice of a wider
+    matrix; C's elements outside the view are left untouched.  out_dtype
+    defaults to the input type for binary16/bfloat16 and int32 for int8.
+    Returns C.  Raises SptgError on any failure.
     """
     import torch
     if A.dim() != 2 or Bcm.dim() != 2 or A.shape[1] != Bcm.shape[1]:
@@ -160,8 +184,7 @@ def gemm(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = No
         raise ValueError("A and Bcm must have the same dtype")
     if not (A.is_cuda and Bcm.is_cuda):
         raise ValueError("A and Bcm must be CUDA tensors")
-    if not (A.is_contiguous() and Bcm.is_contiguous()):
-        raise ValueError("A and Bcm must be contiguous")
+    lda, ldb = _row_pitch(A, "A"), _row_pitch(Bcm, "Bcm")
     M, K = A.shape
     N = Bcm.shape[0]
     if out_dtype is None:
@@ -169,18 +192,19 @@ def gemm(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = No
     key = _dtype_key(A.dtype, out_dtype)
     if C is None:
         C = torch.empty((M, N), dtype=out_dtype, device=A.device)
-    elif C.shape != (M, N) or C.dtype != out_dtype or not C.is_contiguous() or not C.is_cuda:
-        raise ValueError("C must be a contiguous M x N CUDA tensor of the output dtype")
+    elif C.shape != (M, N) or C.dtype != out_dtype or not C.is_cuda:
+        raise ValueError("C must be an M x N CUDA tensor of the output dtype")
+    ldc = _row_pitch(C, "C")
     if config is None and (kernel or stages or bn or splits or cta_pair or stream_k):
         config = Config(KERNELS[kernel or "auto"], bn, stages, splits, 0, 0, cta_pair)
         config.stream_k = stream_k
+    args = (M, N, K, key, A.data_ptr(), lda, Bcm.data_ptr(), ldb, C.data_ptr(), ldc,
+            _stream_handle(stream), config)
     if A.device.index == torch.cuda.current_device():
-        rc = gemm_raw(M, N, K, key, A.data_ptr(), Bcm.data_ptr(), C.data_ptr(),
-                      _stream_handle(stream), config)
+        rc = gemm_strided_raw(*args)
     else:
         with torch.cuda.device(A.device):
-            rc = gemm_raw(M, N, K, key, A.data_ptr(), Bcm.data_ptr(), C.data_ptr(),
-                          _stream_handle(stream), config)
+            rc = gemm_strided_raw(*args)
     if rc != 0:
         raise SptgError(rc, last_error() or status_string(rc))
     return C

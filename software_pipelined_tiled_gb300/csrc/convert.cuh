@@ -32,18 +32,26 @@ __device__ __forceinline__ void widen16(const int4 v, uint32_t h[8]) {
   }
 }
 
-// Groups of 16 values: [0, na16) of A, then [0, nb16) of B. A block lets
-// the dependent GEMM launch once its own share is done (earlier, the GEMM's
-// CTAs could take the SM slots that this grid's last blocks still need); the
-// GEMM waits for this grid's completion before it reads the widened
-// operands.
-__global__ void __launch_bounds__(256) s8_to_f16_kernel(const int4* __restrict__ srcA,
-                                                        uint4* __restrict__ dstA, int64_t na16,
-                                                        const int4* __restrict__ srcB,
-                                                        uint4* __restrict__ dstB, int64_t nb16) {
+// Groups of 16 values: the rows x (K / 16) groups of A, then those of B,
+// each written densely (row pitch K) whatever the source's row pitch (lda,
+// ldb bytes, multiples of 16). A block lets the dependent GEMM launch once
+// its own share is done (earlier, the GEMM's CTAs could take the SM slots
+// that this grid's last blocks still need); the GEMM waits for this grid's
+// completion before it reads the widened operands.
+struct WidenParams {
+  const int4* srcA;
+  const int4* srcB;
+  uint4* dstA;
+  uint4* dstB;
+  int64_t lda16, ldb16;  // source row pitches in 16-byte groups
+  int64_t na16, nb16;    // groups of A and of B
+  int64_t k16;           // groups per row (K / 16)
+};
+
+__global__ void __launch_bounds__(256) s8_to_f16_kernel(const WidenParams p) {
   grid_dependency_wait();  // the previous GEMM may still read the scratch
   constexpr int U = 8;
-  const int64_t n = na16 + nb16;
+  const int64_t n = p.na16 + p.nb16;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += U * stride) {
@@ -51,7 +59,13 @@ __global__ void __launch_bounds__(256) s8_to_f16_kernel(const int4* __restrict__
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t k = i + u * stride;
-      if (k < n) v[u] = __ldcs(k < na16 ? srcA + k : srcB + (k - na16));  // streamed once
+      if (k < n) {
+        const bool is_a = k < p.na16;
+        const int64_t g = is_a ? k : k - p.na16;
+        const int64_t row = g / p.k16, col = g - row * p.k16;
+        const int4* src = is_a ? p.srcA + row * p.lda16 + col : p.srcB + row * p.ldb16 + col;
+        v[u] = __ldcs(src);  // streamed once
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -59,7 +73,7 @@ __global__ void __launch_bounds__(256) s8_to_f16_kernel(const int4* __restrict__
       if (k < n) {
         uint32_t h[8];
         widen16(v[u], h);
-        uint4* d = k < na16 ? dstA + 2 * k : dstB + 2 * (k - na16);
+        uint4* d = k < p.na16 ? p.dstA + 2 * k : p.dstB + 2 * (k - p.na16);
         d[0] = make_uint4(h[0], h[1], h[2], h[3]);
         d[1] = make_uint4(h[4], h[5], h[6], h[7]);
       }

@@ -35,6 +35,7 @@ struct SkinnyParams {
   int64_t total_units;
   int max_contrib;            // partial slots per n-tile
   void* C;                    // row-major M x N output
+  int64_t ldc;                // elements between rows of C
   float* partials;            // [n_tile][max_contrib][MN][128] fp32, or null if unsplit
   unsigned long long* counters;  // [n_tile] (generation << 32 | arrivals)
   unsigned int generation;    // this call's tag for the counters, never 0
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(192, 1)
         if (n < p.N) {
 #pragma unroll
           for (int m = 0; m < MN; ++m)
-            if (m < M) store_out<OUT>(p.C, static_cast<int64_t>(m) * p.N + n, acc[m]);
+            if (m < M) store_out<OUT>(p.C, static_cast<int64_t>(m) * p.ldc + n, acc[m]);
         }
       } else if (p.partials == nullptr || count > p.max_contrib) {
         // the host planned no room for this split: report instead of writing
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(192, 1)
               const int f = tid + 128 * (h * HALF + i);
               const int m = f / F4_PER_ROW;
               const int n0 = nt * BNT + 4 * (f % F4_PER_ROW);
-              if (m < M && n0 < p.N) store_out4<OUT>(p.C, static_cast<int64_t>(m) * p.N + n0, sum[i]);
+              if (m < M && n0 < p.N) store_out4<OUT>(p.C, static_cast<int64_t>(m) * p.ldc + n0, sum[i]);
             }
           }
           if (threadIdx.x == 64) trace_mark(p.trace, TR_FIXUP_DONE);

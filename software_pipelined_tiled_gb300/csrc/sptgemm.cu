@@ -200,11 +200,12 @@ int scratch_for(int dev, cudaStream_t stream, size_t data_bytes, ScratchView* ou
 // into them: a call on the same buffers and shape reuses them.
 struct MapKey {
   const void* base;
-  uint64_t inner, outer;
+  uint64_t inner, outer, pitch;
   uint32_t box_inner, box_outer;
   int dt, esize, swizzle;
   bool operator==(const MapKey& o) const {
-    return base == o.base && inner == o.inner && outer == o.outer && box_inner == o.box_inner &&
+    return base == o.base && inner == o.inner && outer == o.outer && pitch == o.pitch &&
+           box_inner == o.box_inner &&
            box_outer == o.box_outer && dt == o.dt && esize == o.esize && swizzle == o.swizzle;
   }
 };
@@ -218,13 +219,16 @@ thread_local MapEntry t_maps[kMapCache];
 thread_local int t_map_next = 0;
 
 int encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
-                  uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-                  CUtensorMapSwizzle swizzle);
+                  uint64_t inner, uint64_t outer, uint64_t pitch, uint32_t box_inner,
+                  uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
+// A 2-D map of `outer` rows of `inner` elements, rows `pitch` elements apart
+// (0: dense, pitch = inner).
 int make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
                 uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
-  const MapKey key{base, inner, outer, box_inner, box_outer, static_cast<int>(dt), esize,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, uint64_t pitch = 0) {
+  if (pitch == 0) pitch = inner;
+  const MapKey key{base, inner, outer, pitch, box_inner, box_outer, static_cast<int>(dt), esize,
                    static_cast<int>(swizzle)};
   for (const MapEntry& e : t_maps) {
     if (e.valid && e.key == key) {
@@ -232,7 +236,7 @@ int make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void*
       return SPTG_OK;
     }
   }
-  int rc = encode_map_2d(map, dt, esize, base, inner, outer, box_inner, box_outer, swizzle);
+  int rc = encode_map_2d(map, dt, esize, base, inner, outer, pitch, box_inner, box_outer, swizzle);
   if (rc == SPTG_OK) {
     MapEntry& e = t_maps[t_map_next];
     t_map_next = (t_map_next + 1) % kMapCache;
@@ -244,15 +248,15 @@ int make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void*
 }
 
 int encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
-                  uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-                  CUtensorMapSwizzle swizzle) {
+                  uint64_t inner, uint64_t outer, uint64_t pitch, uint32_t box_inner,
+                  uint32_t box_outer, CUtensorMapSwizzle swizzle) {
   auto enc = tensor_map_encoder();
   if (!enc) {
     t_last_error = "cuTensorMapEncodeTiled is not available from the driver";
     return SPTG_ERR_UNSUPPORTED;
   }
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
+  cuuint64_t strides[1] = {pitch * static_cast<uint64_t>(esize)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -526,19 +530,20 @@ int plan_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, in
 }
 
 int launch_square(const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N, int64_t K,
-                  const void* A16, const void* B16, void* C, cudaStream_t stream,
-                  const sptg_config& cfg, const SquarePlan& pl, void* partials,
-                  unsigned long long* counters, unsigned int generation) {
+                  const void* A16, int64_t lda, const void* B16, int64_t ldb, void* C,
+                  int64_t ldc, cudaStream_t stream, const sptg_config& cfg, const SquarePlan& pl,
+                  void* partials, unsigned long long* counters, unsigned int generation) {
   const int BM = 128, BK = 64;
   CUtensorMap ta, tb, tc;
-  int rc = make_map_2d(&ta, d.in_tma, 2, A16, K, M, BK, BM);
+  int rc = make_map_2d(&ta, d.in_tma, 2, A16, K, M, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B, lda);
   if (rc) return rc;
-  rc = make_map_2d(&tb, d.in_tma, 2, B16, K, N, BK, pl.pair ? pl.v.bn / 2 : pl.v.bn);
+  rc = make_map_2d(&tb, d.in_tma, 2, B16, K, N, BK, pl.pair ? pl.v.bn / 2 : pl.v.bn,
+                   CU_TENSOR_MAP_SWIZZLE_128B, ldb);
   if (rc) return rc;
   // C blocks of 32 columns x 32 rows: 128-byte rows for 4-byte outputs,
   // 64-byte rows for 16-bit ones (matching the kernel's staging swizzle)
   rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, 32, 32,
-                   d.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                   d.out_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, ldc);
   if (rc) return rc;
 
   SquareParams p;
@@ -546,6 +551,7 @@ int launch_square(const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.C_out = C;
+  p.ldc = ldc;
   p.num_m_tiles = pl.m_tiles;
   p.num_n_tiles = pl.n_tiles;
   p.num_k_tiles = pl.k_tiles;
@@ -595,8 +601,8 @@ unsigned int next_generation(std::atomic<unsigned int>* g) {
 }
 
 int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N, int64_t K,
-               const void* A, const void* B, void* C, cudaStream_t stream,
-               const sptg_config& cfg, const FixedScratch* fixed = nullptr) {
+               const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+               cudaStream_t stream, const sptg_config& cfg, const FixedScratch* fixed = nullptr) {
   KernelVariant v;
   if (d.is_int8 || !skinny_variant(d.in_bf16, d.out_kind, cfg.stages, &v) || M > v.bn) {
     t_last_error = "no skinny-kernel variant for the requested dtype/stages/M";
@@ -605,9 +611,9 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   const int BNT = 128, BK = 64;
   CUtensorMap tb, ta;
   // MMA operand A is the B^T tile (128 output columns x 64 k), operand B is the A tile.
-  int rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT);
+  int rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT, CU_TENSOR_MAP_SWIZZLE_128B, ldb);
   if (rc) return rc;
-  rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.bn);
+  rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.bn, CU_TENSOR_MAP_SWIZZLE_128B, lda);
   if (rc) return rc;
   rc = ensure_smem(dev, v.fn, v.smem);
   if (rc) return rc;
@@ -630,6 +636,7 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   max_contrib = std::min(max_contrib, grid);
   p.max_contrib = max_contrib;
   p.C = C;
+  p.ldc = ldc;
   p.error_word = di.error_word;
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;
@@ -691,8 +698,9 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
 // per 128-column tile. Returns SPTG_ERR_CONFIG (and launches nothing) when
 // the shape does not suit it, so that the caller can use the stream-K kernel.
 int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N,
-                       int64_t K, const void* A, const void* B, void* C, cudaStream_t stream,
-                       const sptg_config& cfg, bool forced) {
+                       int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                       void* C, int64_t ldc, cudaStream_t stream, const sptg_config& cfg,
+                       bool forced) {
   KernelVariant v;
   if (d.is_int8 || !skinny_cluster_variant(d.in_bf16, d.out_kind, cfg.stages, &v) || M > v.bn) {
     if (forced) t_last_error = "no cluster-split skinny variant for the requested dtype/stages/M";
@@ -726,14 +734,14 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   if (rc) return rc;
   if (cs > 1 && !forced && cluster_slots(dev, v, cs, di.sm_count) < n_tiles) return SPTG_ERR_CONFIG;
   CUtensorMap tb, ta, tc;
-  rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT);
+  rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT, CU_TENSOR_MAP_SWIZZLE_128B, ldb);
   if (rc) return rc;
-  rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.bn);
+  rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.bn, CU_TENSOR_MAP_SWIZZLE_128B, lda);
   if (rc) return rc;
   // the output block a rank stores: v.bn rows of 128 / cs consecutive
   // outputs, unswizzled
   rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, BNT / cs, v.bn,
-                   CU_TENSOR_MAP_SWIZZLE_NONE);
+                   CU_TENSOR_MAP_SWIZZLE_NONE, ldc);
   if (rc) return rc;
   SkinnyClusterParams p;
   p.M = static_cast<int>(M);
@@ -846,8 +854,9 @@ int sptg_device_error(void* stream) {
   return SPTG_OK;
 }
 
-int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B,
-                 void* C, void* stream, const sptg_config* cfg_in) {
+int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, int dtype, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, void* C, int64_t ldc, void* stream,
+                      const sptg_config* cfg_in) {
   t_launches = 0;
   sptg_config cfg;
   memset(&cfg, 0, sizeof(cfg));
@@ -877,8 +886,15 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
     t_last_error = "null pointer";
     return SPTG_ERR_ARG;
   }
+  if (ldc < N || (K > 0 && (lda < K || ldb < K)) || ldc > INT32_MAX || lda > INT32_MAX ||
+      ldb > INT32_MAX) {
+    t_last_error = "leading dimensions must satisfy lda >= K, ldb >= K, ldc >= N (< 2^31)";
+    return SPTG_ERR_ARG;
+  }
   if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))) ||
-      (K * d.in_bytes) % 16 != 0 || (N * d.out_bytes) % 16 != 0) {
+      (K * d.in_bytes) % 16 != 0 || (N * d.out_bytes) % 16 != 0 ||
+      (ldc * d.out_bytes) % 16 != 0 || (K > 0 && ((lda * d.in_bytes) % 16 != 0 ||
+                                                  (ldb * d.in_bytes) % 16 != 0))) {
     t_last_error = "TMA needs 16-byte aligned bases and row pitches";
     return SPTG_ERR_ALIGN;
   }
@@ -889,8 +905,9 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
   cudaStream_t stream_h = static_cast<cudaStream_t>(stream);
 
   if (K == 0) {  // the empty sum
-    cudaError_t e = cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * d.out_bytes, stream_h);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * d.out_bytes, 0,
+                                      static_cast<size_t>(N) * d.out_bytes, M, stream_h);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset2DAsync");
     set_config("kernel=zero-fill dtype=%s", d.name, {});
     return SPTG_OK;
   }
@@ -900,21 +917,22 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
   int kernel = cfg.kernel;
   if (kernel == 0 && !d.is_int8 && M <= 64 && N >= 1024) {
     // memory-bound: the cluster split when it fills the GPU, else stream-K
-    rc = run_skinny_cluster(dev, di, d, M, N, K, A, B, C, stream_h, cfg, false);
+    rc = run_skinny_cluster(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
     if (rc != SPTG_ERR_CONFIG) return rc;
     kernel = 2;
   }
   if (kernel == 0) kernel = 1;
-  if (kernel == 3) return run_skinny_cluster(dev, di, d, M, N, K, A, B, C, stream_h, cfg, true);
-  if (kernel == 2) return run_skinny(dev, di, d, M, N, K, A, B, C, stream_h, cfg);
+  if (kernel == 3)
+    return run_skinny_cluster(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, true);
+  if (kernel == 2) return run_skinny(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg);
 
   SquarePlan pl;
   rc = plan_square(dev, di, d, M, N, K, cfg, &pl);
   if (rc) return rc;
   if (d.is_int8) {
-    // Widen both operands to binary16 in scratch, followed by any stream-K
-    // partials (one request: the scratch cannot move within the call), then
-    // run the exact path.
+    // Widen both operands to dense binary16 copies in scratch, followed by
+    // any stream-K partials (one request: the scratch cannot move within the
+    // call), then run the exact path.
     const size_t a_bytes = static_cast<size_t>(M) * K * 2, b_bytes = static_cast<size_t>(N) * K * 2;
     const size_t a_pad = (a_bytes + 255) & ~static_cast<size_t>(255);
     const size_t b_pad = (b_bytes + 255) & ~static_cast<size_t>(255);
@@ -923,26 +941,33 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, cons
     if (rc) return rc;
     void* A16 = ws.data;
     void* B16 = static_cast<char*>(ws.data) + a_pad;
-    const int64_t na = M * K / 16, nb = N * K / 16;
+    const int64_t na = M * (K / 16), nb = N * (K / 16);
     // two 256-thread blocks per SM, each thread with eight loads in flight
     const int blocks = static_cast<int>(std::min<int64_t>((na + nb + 255) / 256, 2 * di.sm_count));
     // A plain launch: under programmatic overlap its blocks would sit on the
     // SMs beside the previous GEMM's CTAs, which measured 14 us slower per
     // call on 4096^3. The GEMM that follows still overlaps this kernel's tail.
-    cudaError_t e = launch_s8_to_f16(A, A16, na, B, B16, nb, blocks, stream_h, false);
+    cudaError_t e =
+        launch_s8_to_f16(A, lda, M, B, ldb, N, K, A16, B16, blocks, stream_h, false);
     t_launches += 1;
     if (e != cudaSuccess) return cuda_fail(e, "s8_to_f16 launch");
-    return launch_square(di, d, M, N, K, A16, B16, C, stream_h, cfg, pl,
+    return launch_square(di, d, M, N, K, A16, K, B16, K, C, ldc, stream_h, cfg, pl,
                          static_cast<char*>(ws.data) + a_pad + b_pad, ws.counters, ws.generation);
   }
   if (pl.partial_bytes) {
     ScratchView ws;
     rc = scratch_for(dev, stream_h, pl.partial_bytes, &ws);
     if (rc) return rc;
-    return launch_square(di, d, M, N, K, A, B, C, stream_h, cfg, pl, ws.data, ws.counters,
-                         ws.generation);
+    return launch_square(di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, pl, ws.data,
+                         ws.counters, ws.generation);
   }
-  return launch_square(di, d, M, N, K, A, B, C, stream_h, cfg, pl, nullptr, nullptr, 0);
+  return launch_square(di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, pl, nullptr, nullptr,
+                       0);
+}
+
+int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B,
+                 void* C, void* stream, const sptg_config* cfg) {
+  return sptg_gemm_strided(M, N, K, dtype, A, K, B, K, C, N, stream, cfg);
 }
 
 int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B, void* C,
@@ -1066,7 +1091,7 @@ int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype, const v
                            kNoAllocCounterBytes, &g_noalloc_generation};
   sptg_config cfg;
   memset(&cfg, 0, sizeof(cfg));
-  return run_skinny(dev, di, d, M, N, K, A, B, C, stream_h, cfg, &fixed);
+  return run_skinny(dev, di, d, M, N, K, A, K, B, K, C, N, stream_h, cfg, &fixed);
 }
 
 }  // extern "C"

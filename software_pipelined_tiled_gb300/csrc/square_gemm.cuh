@@ -74,7 +74,8 @@ constexpr int SQUARE_THREADS = 320;
 
 struct SquareParams {
   int M, N, K;
-  void* C_out;  // C, for the stream-K reductions' direct stores
+  void* C_out;   // C, for the stream-K reductions' direct stores
+  int64_t ldc;   // elements between rows of C
   int num_m_tiles, num_n_tiles, num_k_tiles;
   int k_tiles_per_chunk;  // accumulation chunk (all K-tiles unless INT_EXACT)
   int group_m;            // raster strip height in m-tiles
@@ -682,9 +683,9 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
           const int col = nt * BN + 4 * g;
           if (r < p.M && col < p.N) {
             if constexpr (INT_EXACT || OUT == OUT_S32)
-              store_c4<OUT_S32>(p.C_out, static_cast<int64_t>(r) * p.N + col, acc[i2]);
+              store_c4<OUT_S32>(p.C_out, static_cast<int64_t>(r) * p.ldc + col, acc[i2]);
             else
-              store_c4<OUT>(p.C_out, static_cast<int64_t>(r) * p.N + col, acc[i2]);
+              store_c4<OUT>(p.C_out, static_cast<int64_t>(r) * p.ldc + col, acc[i2]);
           }
         }
       }

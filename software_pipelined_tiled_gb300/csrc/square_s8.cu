@@ -29,9 +29,19 @@ bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v) {
   return false;
 }
 
-cudaError_t launch_s8_to_f16(const void* srcA, void* dstA, int64_t na16, const void* srcB,
-                             void* dstB, int64_t nb16, int blocks, cudaStream_t stream,
-                             bool overlap_previous) {
+cudaError_t launch_s8_to_f16(const void* srcA, int64_t lda, int64_t rows_a, const void* srcB,
+                             int64_t ldb, int64_t rows_b, int64_t K, void* dstA, void* dstB,
+                             int blocks, cudaStream_t stream, bool overlap_previous) {
+  WidenParams p;
+  p.srcA = static_cast<const int4*>(srcA);
+  p.srcB = static_cast<const int4*>(srcB);
+  p.dstA = static_cast<uint4*>(dstA);
+  p.dstB = static_cast<uint4*>(dstB);
+  p.lda16 = lda / 16;
+  p.ldb16 = ldb / 16;
+  p.k16 = K / 16;
+  p.na16 = rows_a * p.k16;
+  p.nb16 = rows_b * p.k16;
   cudaLaunchConfig_t lc;
   memset(&lc, 0, sizeof(lc));
   lc.gridDim = dim3(blocks, 1, 1);
@@ -42,9 +52,7 @@ cudaError_t launch_s8_to_f16(const void* srcA, void* dstA, int64_t na16, const v
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = overlap_previous ? attr : nullptr;
   lc.numAttrs = overlap_previous ? 1 : 0;
-  return cudaLaunchKernelEx(&lc, s8_to_f16_kernel, static_cast<const int4*>(srcA),
-                            static_cast<uint4*>(dstA), na16, static_cast<const int4*>(srcB),
-                            static_cast<uint4*>(dstB), nb16);
+  return cudaLaunchKernelEx(&lc, s8_to_f16_kernel, p);
 }
 
 }  // namespace sptg

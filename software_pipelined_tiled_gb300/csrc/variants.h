@@ -34,10 +34,11 @@ bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
 bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
 // The streaming ring out = alpha * in (bn = tile bytes).
 KernelVariant stream_variant();
-// int8 -> binary16 widening of both operands in one launch (na16 and nb16
-// groups of 16 elements), allowed to overlap the previous kernel's tail.
-cudaError_t launch_s8_to_f16(const void* srcA, void* dstA, int64_t na16, const void* srcB,
-                             void* dstB, int64_t nb16, int blocks, cudaStream_t stream,
-                             bool overlap_previous);
+// int8 -> binary16 widening of both operands in one launch: rows_a rows of
+// A and rows_b rows of B, K values each (a multiple of 16), read with row
+// pitches lda and ldb (multiples of 16) and written densely to dstA, dstB.
+cudaError_t launch_s8_to_f16(const void* srcA, int64_t lda, int64_t rows_a, const void* srcB,
+                             int64_t ldb, int64_t rows_b, int64_t K, void* dstA, void* dstB,
+                             int blocks, cudaStream_t stream, bool overlap_previous);
 
 }  // namespace sptg

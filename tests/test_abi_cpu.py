@@ -72,6 +72,14 @@ def test_argument_errors_before_device_work(lib):
     assert lib.sptg_gemm(4, 4, 16, 1, ok16, ok16, ok16, None) == -2           # N*2 % 16 != 0
     assert lib.sptg_gemm(4, 2, 16, 0, ok16, ok16, ok16, None) == -2           # N*4 % 16 != 0
     assert lib.sptg_gemm(4, 4, 8, 2, ok16, ok16, ok16, None) == -2            # int8 K % 16 != 0
+    # leading dimensions (elements): too small, or a pitch off the 16-byte rule
+    g = lib.sptg_gemm_strided
+    assert g(4, 8, 16, 1, ok16, 8, ok16, 16, ok16, 8, None, None) == -1        # lda < K
+    assert g(4, 8, 16, 1, ok16, 16, ok16, 8, ok16, 8, None, None) == -1        # ldb < K
+    assert g(4, 8, 16, 1, ok16, 16, ok16, 16, ok16, 4, None, None) == -1       # ldc < N
+    assert g(4, 8, 16, 1, ok16, 20, ok16, 16, ok16, 8, None, None) == -2       # lda*2 % 16
+    assert g(4, 8, 16, 1, ok16, 16, ok16, 16, ok16, 12, None, None) == -2      # ldc*2 % 16
+    assert g(4, 8, 16, 1, ok16, 1 << 31, ok16, 16, ok16, 8, None, None) == -1  # lda >= 2^31
     # empty outputs are a no-op that touches nothing
     assert lib.sptg_gemm(0, 8, 16, 1, None, None, ok16, None) == 0
     assert lib.sptg_gemm(8, 0, 16, 1, None, None, ok16, None) == 0
@@ -84,6 +92,9 @@ def test_invalid_config_fields(lib):
                 sptg.Config(0, 0, -2, 0, 0, 0), sptg.Config(0, 0, 0, 0, -5, 0),
                 sptg.Config(0, 0, 0, 0, 0, 7), sptg.Config(0, 0, 0, 0, 0, 0, 3)):
         assert lib.sptg_gemm_ex(4, 8, 16, 1, ok16, ok16, ok16, None, ctypes.byref(cfg)) == -1
+    cfg = sptg.Config()
+    cfg.stream_k = 3
+    assert lib.sptg_gemm_ex(4, 8, 16, 1, ok16, ok16, ok16, None, ctypes.byref(cfg)) == -1
 
 
 def test_no_device_is_reported_not_hidden(lib):
@@ -107,3 +118,7 @@ def test_python_binding_rejects_bad_tensors():
         sptg.gemm(A, torch.zeros(8, 16, dtype=torch.float16))  # CPU tensors
     with pytest.raises(ValueError):
         sptg._dtype_key(torch.float16, torch.int32)
+    with pytest.raises(ValueError):
+        sptg._row_pitch(torch.zeros(16, 8).t(), "A")  # columns not contiguous
+    wide = torch.zeros(4, 24)
+    assert sptg._row_pitch(wide[:, :16], "A") == 24

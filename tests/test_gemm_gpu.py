@@ -378,6 +378,59 @@ def test_stream_k_chosen_for_a_partial_last_round():
     assert_float_parity(C, A, B, rows, cols)
 
 
+# ------------------------------------------------------------ leading dimensions
+def _in_wider(X, pitch, fill):
+    """X placed in the leading columns of a rows x pitch device buffer."""
+    buf = torch.full((X.shape[0], pitch), fill, dtype=X.dtype)
+    buf[:, :X.shape[1]] = X
+    return buf.cuda()
+
+
+@pytest.mark.parametrize("kernel,M,N,K,it,ot,extra", [
+    ("square", 300, 264, 520, "f16", F32, {}),
+    ("square", 520, 776, 1096, "bf16", BF16, {"cta_pair": 2, "stream_k": 2, "splits": 5}),
+    ("square", 384, 512, 1024, "f16", F16, {"cta_pair": 1, "stream_k": 2, "splits": 7}),
+    ("skinny", 48, 2048, 1024, "bf16", BF16, {}),
+    ("skinny_cluster", 64, 4096, 2048, "f16", F16, {"splits": 2}),
+])
+def test_leading_dimensions(kernel, M, N, K, it, ot, extra):
+    # A, Bcm and C as column slices of wider buffers: the tiles are read and
+    # written through the row pitch, and C's columns past N stay untouched
+    A, B = make_inputs(M, N, K, it, "uniform", 60 + M)
+    dA = _in_wider(A, K + 64, 7)[:, :K]
+    dB = _in_wider(B, K + 32, -3)[:, :K]
+    Cbuf = torch.full((M, N + 24), 5, dtype=ot, device="cuda")
+    C = Cbuf[:, :N]
+    sptg.gemm(dA, dB, C=C, kernel=kernel, **extra)
+    torch.cuda.synchronize()
+    assert sptg.device_error() == 0
+    assert kernel.replace("_", "-") in sptg.last_config()
+    assert (Cbuf[:, N:].cpu().to(torch.float64) == 5).all()
+    assert_float_parity(C.cpu().contiguous(), A, B)
+
+
+@pytest.mark.parametrize("stream_k", [1, 2])
+def test_leading_dimensions_int8(stream_k):
+    A, B = make_inputs(264, 136, 1040, "s8", "int8", 61)
+    dA = _in_wider(A, 1040 + 48, 1)[:, :1040]
+    dB = _in_wider(B, 1040 + 16, -1)[:, :1040]
+    Cbuf = torch.full((264, 136 + 4), 9, dtype=I32, device="cuda")
+    sptg.gemm(dA, dB, C=Cbuf[:, :136], stream_k=stream_k, splits=7 if stream_k == 2 else 0)
+    torch.cuda.synchronize()
+    assert sptg.device_error() == 0
+    assert (Cbuf[:, 136:].cpu() == 9).all()
+    assert_int_parity(Cbuf[:, :136].cpu().contiguous(), A, B)
+
+
+def test_leading_dimensions_zero_k():
+    Cbuf = torch.full((40, 72), 3.0, dtype=F32, device="cuda")
+    A = torch.zeros(40, 0, dtype=F16, device="cuda")
+    B = torch.zeros(64, 0, dtype=F16, device="cuda")
+    sptg.gemm(A, B, C=Cbuf[:, :64])
+    torch.cuda.synchronize()
+    assert (Cbuf[:, :64].cpu() == 0).all() and (Cbuf[:, 64:].cpu() == 3).all()
+
+
 # ------------------------------------------------------------ stream / errors
 def test_async_on_a_side_stream():
     A, B = make_inputs(512, 512, 512, "f16", "uniform", 21)
