@@ -555,6 +555,10 @@ def main(argv=None):
     ap.add_argument("--trace", action="store_true",
                     help="add one traced call's in-kernel timeline to the JSON line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default=None, metavar="DTYPE_PAIR",
+                    help="time M = N = K over --sizes for one dtype pair (one JSON line per size; "
+                         "no end-to-end or CPU legs)")
+    ap.add_argument("--sizes", default="512,1024,2048,4096,8192")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -565,6 +569,18 @@ def main(argv=None):
                      "int8" if pair.startswith("s8") else "uniform", 1.0, 1)
     else:
         w = WORKLOADS[args.workload]
+    if args.sweep:
+        from workloads import Workload
+        args.no_e2e = args.no_cpu_baseline = True
+        for size in (int(x) for x in args.sizes.split(",")):
+            sw = Workload(f"{args.sweep}_{size}x{size}x{size}", size, size, size, args.sweep,
+                          "int8" if args.sweep.startswith("s8") else "uniform", 1.0, 1)
+            # about 50 ms of timed work per size at ~1.5 PFLOP/s
+            args.steps = int(min(2000, max(20, 0.05 / (2.0 * size ** 3 / 1.5e15))))
+            line = run_ours(args, sw)
+            if line is not None:
+                print(json.dumps(line), flush=True)
+        return
     if args.stream:
         line = run_stream(args)
     else:

@@ -32,14 +32,19 @@ bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v) {
   }
 }
 
-template <int MN, bool BF, int OUT, int KSUB>
-KernelVariant make_skinny_cluster() {
+template <int MN, int ST, bool BF, int OUT, int KSUB>
+KernelVariant make_skinny_cluster_at() {
   constexpr int OB = OutTraits<OUT>::bytes;
-  constexpr int ST = skinny_cluster_stages<MN, OB, KSUB>();
   KernelVariant v{reinterpret_cast<const void*>(&skinny_cluster_gemm_kernel<MN, ST, BF, OUT, KSUB>),
                   MN, ST, SkinnyClusterLayout<MN, ST, OB, KSUB>::SMEM_BYTES, false};
   v.ksub = KSUB;
   return v;
+}
+
+template <int MN, bool BF, int OUT, int KSUB>
+KernelVariant make_skinny_cluster() {
+  return make_skinny_cluster_at<MN, skinny_cluster_stages<MN, OutTraits<OUT>::bytes, KSUB>(), BF,
+                                OUT, KSUB>();
 }
 
 // MMA N = 64 at the deepest ring next to the receive buffer, for every float
@@ -56,7 +61,17 @@ bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, KernelVarian
   else if (out_kind == OUT_F32 && in_bf16) c = make_skinny_cluster<64, true, OUT_F32, K>();
   else if (out_kind == OUT_F32 && !in_bf16) c = make_skinny_cluster<64, false, OUT_F32, K>();
   else return false;
-  if (stages != 0 && stages != c.stages) return false;
+  if (stages != 0 && stages != c.stages) {
+    // shallower rings of the bfloat16 -> bfloat16 variant, for the
+    // pipelining ablation of the memory-bound shape
+    if (!(out_kind == OUT_BF16 && in_bf16)) return false;
+    switch (stages) {
+      case 1: c = make_skinny_cluster_at<64, 1, true, OUT_BF16, K>(); break;
+      case 2: c = make_skinny_cluster_at<64, 2, true, OUT_BF16, K>(); break;
+      case 3: c = make_skinny_cluster_at<64, 3, true, OUT_BF16, K>(); break;
+      default: return false;
+    }
+  }
   *v = c;
   return true;
 }

@@ -432,11 +432,15 @@ void plan_stream_k(int T, int W, int KT, int mode, int* sk_tiles, int* sk_worker
 
 // Tile shape and schedule: one CTA (128 x BN) or a CTA pair (256 x BN) per
 // tile, data-parallel or with a partial last round cut along K. The estimate
-// is rounds x (tile rows x BN) x workers / measured rate, with rounds =
-// ceil(tiles / workers) for the data-parallel schedule and tiles / workers
-// + 0.3 with stream-K (the cut tiles' partial writes and reductions, as
-// measured on 4096 x 4096 x 4096). The cheapest estimate wins; ties keep the
-// wider tile and the data-parallel schedule.
+// is in microseconds: a worker (one SM or one CTA pair) does a K-tile of its
+// tile in t_k = 2 x rows x BN x 64 / (rate / workers), with the measured
+// per-width rate; the data-parallel schedule takes ceil(tiles / workers)
+// rounds of K-tiles, the stream-K one tiles / workers rounds plus a fixed
+// 6 us for the partial writes and reductions (as measured on 4096^3 and
+// 1024^3). The cheapest estimate wins; ties keep the wider tile and the
+// data-parallel schedule.
+constexpr double kStreamKFixedUs = 6.0;
+
 void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sptg_config& cfg,
                          bool int8, int* bn_out, bool* pair_out, bool* sk_out) {
   double best = 1e300;
@@ -458,17 +462,17 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
       if (int8 && bn != 128 && bn != 160) continue;  // 3 x BN tensor-memory columns
       const int64_t T64 = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
       const int T = static_cast<int>(std::min<int64_t>(T64, INT32_MAX));
-      const double work = static_cast<double>(rows * bn) * W / (pair ? kRatePair[i] : kRateSingle[i]);
+      const double rate = (pair ? kRatePair[i] : kRateSingle[i]) * 1e6;  // FLOP per us
+      const double t_k = 2.0 * rows * bn * 64 / (rate / W);            // us per K-tile
       for (int sk = 0; sk < 2; ++sk) {
-        double rounds = static_cast<double>((T + W - 1) / W);
+        double cost = static_cast<double>((T + W - 1) / W) * KT * t_k;
         if (sk) {
           if (cfg.stream_k == 1) continue;
           int skt, skw, mc;
           plan_stream_k(T, W, KT, 0, &skt, &skw, &mc);
           if (skt == 0) continue;
-          rounds = static_cast<double>(T) / W + 0.3;
+          cost = static_cast<double>(T) / W * KT * t_k + kStreamKFixedUs;
         }
-        const double cost = rounds * work;
         if (cost < best) {
           best = cost;
           *bn_out = bn;

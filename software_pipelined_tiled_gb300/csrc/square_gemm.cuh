@@ -626,8 +626,8 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       // row r0 + (f / 8) % nr, 32-column block f / (8 nr). A warp reads
       // 64-byte runs of the partials and writes whole row segments of C.
       const int total = nr * (BN / 4);
-      constexpr int CH = 4;  // groups per contributor in flight
-      constexpr int CB = 4;  // contributors in flight
+      constexpr int CH = 8;  // groups per contributor in flight
+      constexpr int CB = 2;  // contributors in flight
       const int row0 = mt * L::TILE_M + static_cast<int>(rank) * BM;
 #pragma unroll 1
       for (int f0 = 0; f0 < total; f0 += 128 * CH) {

@@ -185,6 +185,26 @@ def test_stage_count_does_not_change_the_arithmetic(stages):
     assert torch.equal(ref, got)
 
 
+@pytest.mark.parametrize("stages", [1, 2, 3, 4, 5])
+def test_long_k_ablation_rings_match(stages):
+    # the shallower rings of the 256-wide bfloat16 pair tile give the bits of
+    # the default ring
+    A, B = make_inputs(512, 512, 2048, "bf16", "normal", 14)
+    ref = run(A, B, F32, bn=256, cta_pair=2, stream_k=1)
+    got = run(A, B, F32, bn=256, cta_pair=2, stream_k=1, stages=stages)
+    assert f"stages={stages}" in sptg.last_config()
+    assert torch.equal(ref, got)
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3])
+def test_skinny_cluster_ablation_rings_match(stages):
+    A, B = make_inputs(64, 2048, 4096, "bf16", "normal", 15)
+    ref = run(A, B, BF16, kernel="skinny_cluster", splits=2)
+    got = run(A, B, BF16, kernel="skinny_cluster", splits=2, stages=stages)
+    assert f"stages={stages}" in sptg.last_config()
+    assert torch.equal(ref, got)
+
+
 # --------------------------------------------------------- ragged and edges
 @pytest.mark.parametrize("M,N,K,dt,out", [
     (200, 136, 200, F16, F32),
@@ -365,7 +385,7 @@ def test_stream_k_is_deterministic_and_matches_data_parallel():
 def test_stream_k_chosen_for_a_partial_last_round():
     # 4096 x 4096 in 256 x 256 pair tiles: 256 tiles over the pairs leave a
     # partial last round, which the default schedule cuts along K
-    A, B = make_inputs(4096, 4096, 1024, "f16", "uniform", 44)
+    A, B = make_inputs(4096, 4096, 4096, "f16", "uniform", 44)
     C = run(A, B, F16)
     cfg = sptg.last_config()
     assert "pair=1" in cfg and "bn=256" in cfg and _sk_tiles() > 0, cfg
