@@ -113,10 +113,20 @@ def last_config() -> str:
     return buf.value.decode()
 
 
-def _stream_handle(stream) -> int:
+def _current_stream(device_index: int) -> int:
+    """Raw handle of PyTorch's current stream on a device."""
+    import torch
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return int(raw(device_index))
+    return torch.cuda.current_stream(device_index).cuda_stream
+
+
+def _stream_handle(stream, device_index: int | None = None) -> int:
     if stream is None:
         import torch
-        return torch.cuda.current_stream().cuda_stream
+        return _current_stream(torch.cuda.current_device() if device_index is None
+                               else device_index)
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
@@ -149,13 +159,20 @@ def gemm_skinny_noalloc_raw(M: int, N: int, K: int, dtype: str | int, A_ptr: int
     return int(load().sptg_gemm_skinny_noalloc(M, N, K, d, A_ptr, B_ptr, C_ptr, stream))
 
 
+_KEYS: dict = {}
+
+
 def _dtype_key(in_dtype, out_dtype) -> str:
+    key = _KEYS.get((in_dtype, out_dtype))
+    if key is not None:
+        return key
     import torch
     names = {torch.float16: "f16", torch.bfloat16: "bf16", torch.int8: "s8",
              torch.float32: "f32", torch.int32: "s32"}
     key = f"{names.get(in_dtype, '?')}_{names.get(out_dtype, '?')}"
     if key not in DTYPES:
         raise ValueError(f"unsupported input/output dtype pair {in_dtype} -> {out_dtype}")
+    _KEYS[(in_dtype, out_dtype)] = key
     return key
 
 
@@ -198,13 +215,15 @@ def gemm(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = No
     if config is None and (kernel or stages or bn or splits or cta_pair or stream_k):
         config = Config(KERNELS[kernel or "auto"], bn, stages, splits, 0, 0, cta_pair)
         config.stream_k = stream_k
-    args = (M, N, K, key, A.data_ptr(), lda, Bcm.data_ptr(), ldb, C.data_ptr(), ldc,
-            _stream_handle(stream), config)
-    if A.device.index == torch.cuda.current_device():
-        rc = gemm_strided_raw(*args)
+    dev = A.get_device()
+    args = (M, N, K, DTYPES[key], A.data_ptr(), lda, Bcm.data_ptr(), ldb, C.data_ptr(), ldc,
+            _stream_handle(stream, dev), ctypes.byref(config) if config is not None else None)
+    lib = _lib or load()
+    if dev == torch.cuda.current_device():
+        rc = lib.sptg_gemm_strided(*args)
     else:
-        with torch.cuda.device(A.device):
-            rc = gemm_strided_raw(*args)
+        with torch.cuda.device(dev):
+            rc = lib.sptg_gemm_strided(*args)
     if rc != 0:
         raise SptgError(rc, last_error() or status_string(rc))
     return C
