@@ -147,14 +147,17 @@ __device__ __forceinline__ bool square_segment(const SquareParams& p, int worker
   return true;
 }
 
-// Epilogue staging per warp: one block of 32 rows x 32 outputs. 4-byte
-// outputs keep two such buffers (a store can read one while the next block
-// is written), 16-bit outputs one buffer of 2 KB, which leaves room for one
-// more ring stage in the pair kernels.
+// Epilogue staging per warp: buffers of one block of 32 rows x 32 outputs,
+// used in turn, so that the tensor-copy stores of the last blocks are still
+// reading while the next ones are written. The ring is sized against the
+// minimum (two 4 KB buffers for 4-byte outputs, one 2 KB buffer for 16-bit
+// outputs, which leaves room for one more stage in the 224-wide pair
+// kernels); whatever the ring leaves over goes to more buffers, up to four.
 template <int OBYTES>
 struct EpiStaging {
   static constexpr int BUF = 32 * 32 * OBYTES;
-  static constexpr int NBUF = OBYTES == 4 ? 2 : 1;
+  static constexpr int MIN_NBUF = OBYTES == 4 ? 2 : 1;
+  static constexpr int MAX_NBUF = 4;
 };
 
 template <int BN, int STAGES, bool INT_EXACT, bool PAIR, int OBYTES = 4>
@@ -167,7 +170,14 @@ struct SquareLayout {
   static constexpr int B_STAGE = BN_CTA * BK * 2;
   static constexpr int EPI_WARPS = 4;
   static constexpr int EPI_BUF = EpiStaging<OBYTES>::BUF;
-  static constexpr int EPI_NBUF = EpiStaging<OBYTES>::NBUF;
+  static constexpr int RING_BYTES = STAGES * (A_STAGE + B_STAGE);
+  static constexpr bool staging_fits(int nbuf) {
+    return RING_BYTES + EPI_WARPS * nbuf * EPI_BUF + 256 + 1024 <= 232448;
+  }
+  static constexpr int EPI_NBUF =
+      staging_fits(EpiStaging<OBYTES>::MAX_NBUF) ? EpiStaging<OBYTES>::MAX_NBUF
+      : (staging_fits(2) && EpiStaging<OBYTES>::MIN_NBUF <= 2) ? 2
+                                                               : EpiStaging<OBYTES>::MIN_NBUF;
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_NBUF * EPI_BUF;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
@@ -190,13 +200,14 @@ struct SquareLayout {
   static_assert(!PAIR || BN_CTA % 16 == 0, "each CTA's B rows must be a multiple of 16");
   static_assert(STAGES >= 1, "at least one stage");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
+  static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
 };
 
 // Deepest ring that fits the 227 KB per-CTA budget next to the epilogue
 // staging, the barriers and the 1 KB alignment slack.
 template <int BN, bool PAIR = false, int OBYTES = 4>
 constexpr int square_max_stages() {
-  return (232448 - 1024 - 4 * EpiStaging<OBYTES>::NBUF * EpiStaging<OBYTES>::BUF - 256) /
+  return (232448 - 1024 - 4 * EpiStaging<OBYTES>::MIN_NBUF * EpiStaging<OBYTES>::BUF - 256) /
          (128 * 64 * 2 + (PAIR ? BN / 2 : BN) * 64 * 2);
 }
 
@@ -489,66 +500,87 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
           }
           if (!last_chunk) tmem_wait_st();
         } else {
-          // One block = 32 output columns of this warp's 32 rows: 128-byte
-          // rows (128-byte swizzle) for 4-byte outputs, 64-byte rows (64-byte
-          // swizzle) for 16-bit outputs; the TMA store unswizzles. The
+          // One block = 32 output columns of this warp's 32 rows. The
           // tensor-memory load of block cb+1 is in flight while block cb is
-          // converted, staged and stored.
+          // converted.
+          constexpr int NB = BN / 32;
           uint32_t v[32];
           tmem_ld_32x32b_x32(t_acc, v);
           tmem_wait_ld_regs(v);
+          if (seg.partial) {
 #pragma unroll 1
-          for (int cb = 0; cb < BN / 32; ++cb) {
-            const bool more = cb + 1 < BN / 32;
-            uint32_t nxt[32];
-            if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
-            if (seg.partial) {
+            for (int cb = 0; cb < NB; ++cb) {
+              const bool more = cb + 1 < NB;
+              uint32_t nxt[32];
+              if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
               // fp32 partial straight to scratch
 #pragma unroll
               for (int j = 0; j < 8; ++j)
                 __stcg(slot + (cb * 8 + j) * 128, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-            } else {
-              uint8_t* buf = bufs + (stores % L::EPI_NBUF) * L::EPI_BUF;
-              // the store that last used buf is done reading it
-              if (lane == 0) bulk_wait_group_read<L::EPI_NBUF - 1>();
+              if (more) {
+                tmem_wait_ld_regs(nxt);
+#pragma unroll
+                for (int i2 = 0; i2 < 32; ++i2) v[i2] = nxt[i2];
+              }
+            }
+          } else {
+            // Blocks go out in groups of G = the staging buffers of the warp:
+            // each block is converted into its own buffer (128-byte rows with
+            // 128-byte swizzle for 4-byte outputs, 64-byte rows with 64-byte
+            // swizzle for 16-bit ones), one proxy fence covers the group, and
+            // lanes 0..G-1 each issue the tensor-copy store of one block.
+            constexpr int G = L::EPI_NBUF;
+#pragma unroll 1
+            for (int cb0 = 0; cb0 < NB; cb0 += G) {
+              // every lane's earlier stores are done reading the buffers
+              bulk_wait_group_read<0>();
               __syncwarp();
-              if constexpr (OBYTES == 4) {
-                if constexpr (OUT == OUT_S32) {
+#pragma unroll 1
+              for (int g = 0; g < G; ++g) {
+                const int cb = cb0 + g;
+                if (cb < NB) {
+                  const bool more = cb + 1 < NB;
+                  uint32_t nxt[32];
+                  if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
+                  uint8_t* buf = bufs + g * L::EPI_BUF;
+                  if constexpr (OBYTES == 4) {
+                    if constexpr (OUT == OUT_S32) {
 #pragma unroll
-                  for (int i2 = 0; i2 < 32; ++i2) v[i2] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i2])));
-                }
-                uint8_t* row = buf + lane * 128;
+                      for (int i2 = 0; i2 < 32; ++i2) v[i2] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i2])));
+                    }
+                    uint8_t* row = buf + lane * 128;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const uint4 q4 = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                  *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
-                }
-              } else {
-                uint32_t w[16];
+                    for (int j = 0; j < 8; ++j) {
+                      const uint4 q4 = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                      *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
+                    }
+                  } else {
+                    uint32_t w[16];
 #pragma unroll
-                for (int i2 = 0; i2 < 16; ++i2)
-                  w[i2] = pack2<OUT>(__uint_as_float(v[2 * i2]), __uint_as_float(v[2 * i2 + 1]));
-                uint8_t* row = buf + lane * 64;
+                    for (int i2 = 0; i2 < 16; ++i2)
+                      w[i2] = pack2<OUT>(__uint_as_float(v[2 * i2]), __uint_as_float(v[2 * i2 + 1]));
+                    uint8_t* row = buf + lane * 64;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                  *reinterpret_cast<uint4*>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = q4;
+                    for (int j = 0; j < 4; ++j) {
+                      const uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                      *reinterpret_cast<uint4*>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = q4;
+                    }
+                  }
+                  if (more) {
+                    tmem_wait_ld_regs(nxt);
+#pragma unroll
+                    for (int i2 = 0; i2 < 32; ++i2) v[i2] = nxt[i2];
+                  }
                 }
               }
               fence_proxy_async_smem();
               __syncwarp();
-              if (lane == 0) {
-                // a block that starts past the matrix (ragged edge) stores nothing
-                if (c_row < p.M && nt * BN + 32 * cb < p.N)
-                  tma_store_2d(&tmC, smem_addr(buf), nt * BN + 32 * cb, c_row);
+              const int cb = cb0 + lane;
+              // a block that starts past the matrix (ragged edge) stores nothing
+              if (lane < G && cb < NB && c_row < p.M && nt * BN + 32 * cb < p.N) {
+                tma_store_2d(&tmC, smem_addr(bufs + lane * L::EPI_BUF), nt * BN + 32 * cb, c_row);
                 bulk_commit_group();
               }
-              ++stores;
-            }
-            if (more) {
-              tmem_wait_ld_regs(nxt);
-#pragma unroll
-              for (int i2 = 0; i2 < 32; ++i2) v[i2] = nxt[i2];
             }
           }
         }
@@ -576,7 +608,7 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       }
       ++notes;
     }
-    if (lane == 0) bulk_wait_group_read<0>();  // staging is free once the stores have read it
+    bulk_wait_group_read<0>();  // staging is free once every lane's stores have read it
     if (warp == 2 && lane == 0) trace_mark(p.trace, TR_EPI_DONE);
   } else if (p.sk_tiles > 0) {
     // ---------------------------------------------- stream-K reduction warps
