@@ -149,7 +149,10 @@ __global__ void __launch_bounds__(192, 1)
   // Warm L2 with this CTA's first stages while the previous kernel drains.
   // L2 is where writes become coherent, so this is safe even if that kernel
   // writes these operands: the loads proper come after the dependency wait.
+  uint64_t pol_stream = 0, pol_keep = 0;
   if (threadIdx.x == 0) {
+    pol_stream = policy_evict_first();  // B is read once
+    pol_keep = policy_evict_last();     // A is read by every CTA
     for (int kt = kt0; kt < min(kt1, kt0 + STAGES); ++kt) {
 #pragma unroll
       for (int j = 0; j < KSUB; ++j) {
@@ -166,8 +169,6 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_stream = policy_evict_first();  // B is read once
-      const uint64_t pol_keep = policy_evict_last();     // A is read by every CTA
       int issued_round[STAGES];
       for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
       bool ok = true;
@@ -175,7 +176,8 @@ __global__ void __launch_bounds__(192, 1)
       for (int kt = kt0; kt < kt1; ++kt, ++it) {
         const int s = it % STAGES;
         const uint32_t round = it / STAGES;
-        if (!wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl, WAIT_PRODUCER_EMPTY)) {
+        // in the first round every stage is free: no wait
+        if (round > 0 && !wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl, WAIT_PRODUCER_EMPTY)) {
           ok = false;
           break;
         }

@@ -294,17 +294,21 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   // the persistent work unit is a CTA, or a CTA pair in PAIR mode
   const int worker = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  // Warm L2 with the first stages of this CTA's first segment while the
-  // previous kernel drains (safe: L2 is where writes become coherent; the
-  // loads proper wait for the dependency).
+  // The producer (thread 0) works out its first segment and warms L2 with
+  // its first stages while the previous kernel drains (safe: L2 is where
+  // writes become coherent; the loads proper wait for the dependency).
+  Segment seg0;
+  bool have_seg0 = false;
+  int mt0 = 0, nt0 = 0;
+  uint64_t pol_operands = 0;
   if (threadIdx.x == 0) {
-    Segment seg;
-    if (square_segment(p, worker, workers, 0, seg)) {
-      int mt, nt;
-      tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
-      for (int kt = seg.kt0; kt < min(seg.kt1, seg.kt0 + STAGES); ++kt) {
-        tma_prefetch_l2_2d(&tmA, kt * BK, mt * L::TILE_M + static_cast<int>(rank) * BM);
-        tma_prefetch_l2_2d(&tmB, kt * BK, nt * BN + static_cast<int>(rank) * L::BN_CTA);
+    pol_operands = policy_evict_last();  // operands are re-read by other tiles
+    have_seg0 = square_segment(p, worker, workers, 0, seg0);
+    if (have_seg0) {
+      tile_coords(seg0.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt0, nt0);
+      for (int kt = seg0.kt0; kt < min(seg0.kt1, seg0.kt0 + STAGES); ++kt) {
+        tma_prefetch_l2_2d(&tmA, kt * BK, mt0 * L::TILE_M + static_cast<int>(rank) * BM);
+        tma_prefetch_l2_2d(&tmB, kt * BK, nt0 * BN + static_cast<int>(rank) * L::BN_CTA);
       }
     }
   }
@@ -318,21 +322,30 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_last();  // operands are re-read by other tiles
+      const uint64_t pol = pol_operands;
       int issued_round[STAGES];
       for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
       bool ok = true;
       uint32_t it = 0;
       Segment seg;
-      for (int i = 0; ok && square_segment(p, worker, workers, i, seg); ++i) {
+      for (int i = 0; ok; ++i) {
         int mt, nt;
-        tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+        if (i == 0) {
+          if (!have_seg0) break;
+          seg = seg0;  // worked out before the dependency wait
+          mt = mt0;
+          nt = nt0;
+        } else {
+          if (!square_segment(p, worker, workers, i, seg)) break;
+          tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+        }
         const int a_row = mt * L::TILE_M + static_cast<int>(rank) * BM;
         const int b_row = nt * BN + static_cast<int>(rank) * L::BN_CTA;
         for (int kt = seg.kt0; kt < seg.kt1; ++kt, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
-          if (!wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl, WAIT_PRODUCER_EMPTY)) {
+          // in the first round every stage is free: no wait
+          if (round > 0 && !wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl, WAIT_PRODUCER_EMPTY)) {
             ok = false;
             break;
           }
