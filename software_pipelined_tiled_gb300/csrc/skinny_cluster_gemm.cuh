@@ -25,6 +25,9 @@ namespace sptg {
 struct SkinnyClusterParams {
   int M, N, K;
   int num_n_tiles, num_k_tiles;
+  // 1: the maps are 3-D (64-element K-chunk, row, chunk index) and one copy
+  // per operand moves a stage's KSUB chunks; 0: 2-D maps, one copy per chunk
+  int load3d;
   unsigned int* error_word;
   uint64_t timeout_ns;
   int inject_stall;
@@ -154,10 +157,15 @@ __global__ void __launch_bounds__(192, 1)
     pol_stream = policy_evict_first();  // B is read once
     pol_keep = policy_evict_last();     // A is read by every CTA
     for (int kt = kt0; kt < min(kt1, kt0 + STAGES); ++kt) {
+      if (p.load3d) {
+        tma_prefetch_l2_3d(&tmBt, 0, nt * BNT, kt * KSUB);
+        tma_prefetch_l2_3d(&tmA, 0, 0, kt * KSUB);
+      } else {
 #pragma unroll
-      for (int j = 0; j < KSUB; ++j) {
-        tma_prefetch_l2_2d(&tmBt, (kt * KSUB + j) * BK, nt * BNT);
-        tma_prefetch_l2_2d(&tmA, (kt * KSUB + j) * BK, 0);
+        for (int j = 0; j < KSUB; ++j) {
+          tma_prefetch_l2_2d(&tmBt, (kt * KSUB + j) * BK, nt * BNT);
+          tma_prefetch_l2_2d(&tmA, (kt * KSUB + j) * BK, 0);
+        }
       }
     }
   }
@@ -183,12 +191,19 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (p.inject_stall && it == 1) continue;  // test hook: this stage never fills
         mbar_arrive_expect_tx(full_bar(s), L::STAGE);
+        if (p.load3d) {
+          // one copy per operand: KSUB chunks of 64 K-elements, each landing
+          // as its own 128-byte-swizzled sub-tile
+          tma_load_3d(stage_bt(s), &tmBt, full_bar(s), 0, nt * BNT, kt * KSUB, pol_stream);
+          tma_load_3d(stage_a(s), &tmA, full_bar(s), 0, 0, kt * KSUB, pol_keep);
+        } else {
 #pragma unroll
-        for (int j = 0; j < KSUB; ++j) {
-          tma_load_2d(stage_bt(s) + j * L::SUB_BT, &tmBt, full_bar(s), (kt * KSUB + j) * BK,
-                      nt * BNT, pol_stream);
-          tma_load_2d(stage_a(s) + j * L::SUB_A, &tmA, full_bar(s), (kt * KSUB + j) * BK, 0,
-                      pol_keep);
+          for (int j = 0; j < KSUB; ++j) {
+            tma_load_2d(stage_bt(s) + j * L::SUB_BT, &tmBt, full_bar(s), (kt * KSUB + j) * BK,
+                        nt * BNT, pol_stream);
+            tma_load_2d(stage_a(s) + j * L::SUB_A, &tmA, full_bar(s), (kt * KSUB + j) * BK, 0,
+                        pol_keep);
+          }
         }
         issued_round[s] = static_cast<int>(round);
         if (it == 0) trace_mark(p.trace, TR_FIRST_LOAD);

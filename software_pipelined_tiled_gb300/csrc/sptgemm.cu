@@ -272,6 +272,57 @@ int encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const voi
   return SPTG_OK;
 }
 
+// A 3-D view of a K-major operand (rows of K 16-bit elements, `pitch`
+// elements apart) as (64-element K-chunk, row, chunk index), the chunk index
+// stepping 128 bytes: one box of {64, box_rows, ksub} then lands as ksub
+// consecutive 128-byte-swizzled sub-tiles of box_rows x 64, the layout of
+// ksub separate 2-D boxes. Needs K to be a multiple of 64. Cached like the
+// 2-D maps.
+struct ChunkMapEntry {
+  const void* base = nullptr;
+  uint64_t K = 0, rows = 0, pitch = 0;
+  uint32_t box_rows = 0, ksub = 0;
+  int dt = -1;
+  CUtensorMap map;
+};
+thread_local ChunkMapEntry t_chunk_maps[8];
+thread_local int t_chunk_next = 0;
+
+int make_map_kchunks(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t K,
+                     uint64_t rows, uint64_t pitch, uint32_t box_rows, uint32_t ksub) {
+  for (const ChunkMapEntry& e : t_chunk_maps) {
+    if (e.base == base && e.K == K && e.rows == rows && e.pitch == pitch &&
+        e.box_rows == box_rows && e.ksub == ksub && e.dt == static_cast<int>(dt)) {
+      *map = e.map;
+      return SPTG_OK;
+    }
+  }
+  auto enc = tensor_map_encoder();
+  if (!enc) {
+    t_last_error = "cuTensorMapEncodeTiled is not available from the driver";
+    return SPTG_ERR_UNSUPPORTED;
+  }
+  cuuint64_t dims[3] = {64, rows, K / 64};
+  cuuint64_t strides[2] = {pitch * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, ksub};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return SPTG_ERR_ARG;
+  ChunkMapEntry& e = t_chunk_maps[t_chunk_next];
+  t_chunk_next = (t_chunk_next + 1) % 8;
+  e.base = base;
+  e.K = K;
+  e.rows = rows;
+  e.pitch = pitch;
+  e.box_rows = box_rows;
+  e.ksub = ksub;
+  e.dt = static_cast<int>(dt);
+  e.map = *map;
+  return SPTG_OK;
+}
+
 // ------------------------------------------------------------ dtype table
 struct DtypeInfo {
   int in_bytes, out_bytes;
@@ -738,10 +789,19 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   if (rc) return rc;
   if (cs > 1 && !forced && cluster_slots(dev, v, cs, di.sm_count) < n_tiles) return SPTG_ERR_CONFIG;
   CUtensorMap tb, ta, tc;
-  rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT, CU_TENSOR_MAP_SWIZZLE_128B, ldb);
-  if (rc) return rc;
-  rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.bn, CU_TENSOR_MAP_SWIZZLE_128B, lda);
-  if (rc) return rc;
+  // With several K-chunks per stage and K a multiple of 64, one 3-D copy per
+  // operand moves a whole stage; otherwise one 2-D copy per chunk.
+  int load3d = 0;
+  if (v.ksub > 1 && K % 64 == 0 &&
+      make_map_kchunks(&tb, d.in_tma, B, K, N, ldb, BNT, v.ksub) == SPTG_OK &&
+      make_map_kchunks(&ta, d.in_tma, A, K, M, lda, v.bn, v.ksub) == SPTG_OK)
+    load3d = 1;
+  if (!load3d) {
+    rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT, CU_TENSOR_MAP_SWIZZLE_128B, ldb);
+    if (rc) return rc;
+    rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, BK, v.bn, CU_TENSOR_MAP_SWIZZLE_128B, lda);
+    if (rc) return rc;
+  }
   // the output block a rank stores: v.bn rows of 128 / cs consecutive
   // outputs, unswizzled
   rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, BNT / cs, v.bn,
@@ -753,6 +813,7 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   p.K = static_cast<int>(K);
   p.num_n_tiles = n_tiles;
   p.num_k_tiles = k_tiles;
+  p.load3d = load3d;
   p.error_word = di.error_word;
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;
@@ -764,8 +825,8 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   if (e != cudaSuccess) return cuda_fail(e, "skinny_cluster_gemm launch");
   set_config(
       "kernel=skinny-cluster dtype=%s mma_m=%lld mma_n=%lld bk=%lld stages=%lld grid=%lld "
-      "cluster=%lld n_tiles=%lld k_tiles=%lld smem=%lld",
-      d.name, {BNT, v.bn, kstep, v.stages, grid, cs, n_tiles, k_tiles, v.smem});
+      "cluster=%lld n_tiles=%lld k_tiles=%lld copies_3d=%lld smem=%lld",
+      d.name, {BNT, v.bn, kstep, v.stages, grid, cs, n_tiles, k_tiles, load3d, v.smem});
   return SPTG_OK;
 }
 
