@@ -462,15 +462,19 @@ def test_async_on_a_side_stream():
     assert_float_parity(C.cpu(), A, B)
 
 
-@pytest.mark.parametrize("kernel,pair", [(1, 1), (1, 2), (2, 0), (3, 0)])
-def test_bounded_wait_reports_timeout_and_context_survives(kernel, pair):
+@pytest.mark.parametrize("kernel,pair,stream_k", [(1, 1, 0), (1, 2, 0), (1, 1, 2), (1, 2, 2),
+                                                   (2, 0, 0), (3, 0, 0)])
+def test_bounded_wait_reports_timeout_and_context_survives(kernel, pair, stream_k):
     # The producer withholds one K-tile; the consumer's wait runs out after
     # 100 ms, the kernel tears down, and the host reads SPTG_ERR_TIMEOUT.
+    # With every tile cut along K, the other CTAs' reduction warps also give
+    # up waiting for the stalled contributor.
     M = 512 if kernel == 1 else 64
     A, B = make_inputs(M, 1024, 1024, "bf16", "normal", 30)
     dA, dB = A.cuda(), B.cuda()
     C = torch.empty(M, 1024, dtype=BF16, device="cuda")
     cfg = sptg.Config(kernel, 0, 0, 2 if kernel == 3 else 4, 100, 1, pair)
+    cfg.stream_k = stream_k
     rc = sptg.gemm_raw(M, 1024, 1024, "bf16_bf16", dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
                        torch.cuda.current_stream().cuda_stream, cfg)
     assert rc == 0
