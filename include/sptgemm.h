@@ -135,6 +135,24 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, int dtype,
                       void* C, int64_t ldc, void* stream, const sptg_config* cfg);
 
 /*
+ * sptg_gemm_ex on HOST buffers: A (M x K), B (the N x K array Bcm) and C
+ * (M x N), dense, in host memory. The call enqueues on `stream` the copies of
+ * A and B to device buffers the library owns (one set per device and stream,
+ * grown on demand and freed in stream order), the product, and the copy of
+ * C back to the host, and returns without waiting. The caller keeps A, B and
+ * C alive and leaves C alone until the stream has reached this point.
+ * Page-locked (pinned) host memory makes the copies asynchronous; pageable
+ * memory works but the driver then stages it and the call may block. The
+ * pitch rules of sptg_gemm apply (SPTG_ERR_ALIGN); the pointers themselves
+ * need no alignment. The pages have no counterpart: this is the call a
+ * caller whose data lives in host memory makes, and bench.py's end-to-end
+ * measurement goes through it.
+ */
+int sptg_gemm_host(int64_t M, int64_t N, int64_t K, int dtype,
+                   const void* A, const void* B, void* C, void* stream,
+                   const sptg_config* cfg);
+
+/*
  * The software-pipelined ring on its own: out[i] = alpha * in[i] for
  * i < n, binary32, one rounding per element. This is the minimal working
  * example of "Hiding Memory Latency in CUDA: Asynchronous Loads and Software

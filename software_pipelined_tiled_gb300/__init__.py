@@ -19,7 +19,8 @@ import threading
 
 from ._build import LIB_PATH, build
 
-__all__ = ["DTYPES", "SptgError", "Config", "load", "gemm", "gemm_raw", "gemm_strided_raw",
+__all__ = ["DTYPES", "SptgError", "Config", "load", "gemm", "gemm_host", "gemm_raw",
+           "gemm_strided_raw",
            "gemm_skinny_noalloc_raw",
            "stream_scale",
            "last_config",
@@ -33,7 +34,8 @@ STATUS = {0: "SPTG_OK", -1: "SPTG_ERR_ARG", -2: "SPTG_ERR_ALIGN", -3: "SPTG_ERR_
 KERNELS = {"auto": 0, "square": 1, "skinny": 2, "skinny_cluster": 3}
 
 # the C functions every build must export (checked by the tests)
-EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_gemm_strided", "sptg_status_string", "sptg_last_error",
+EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_gemm_strided", "sptg_gemm_host",
+           "sptg_status_string", "sptg_last_error",
            "sptg_last_config", "sptg_device_error", "sptg_version", "sptg_gemm_skinny_noalloc",
            "sptg_stream_scale", "sptg_stream_scale_ex")
 
@@ -76,6 +78,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sptg_gemm_strided.argtypes = [i64, i64, i64, ctypes.c_int, vp, i64, vp, i64, vp, i64,
                                           vp, ctypes.POINTER(Config)]
         lib.sptg_gemm_strided.restype = ctypes.c_int
+        lib.sptg_gemm_host.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, vp,
+                                       ctypes.POINTER(Config)]
+        lib.sptg_gemm_host.restype = ctypes.c_int
         lib.sptg_status_string.argtypes = [ctypes.c_int]
         lib.sptg_status_string.restype = ctypes.c_char_p
         lib.sptg_last_error.argtypes = []
@@ -224,6 +229,37 @@ def gemm(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = No
     else:
         with torch.cuda.device(dev):
             rc = lib.sptg_gemm_strided(*args)
+    if rc != 0:
+        raise SptgError(rc, last_error() or status_string(rc))
+    return C
+
+
+def gemm_host(A, Bcm, C=None, out_dtype=None, stream=None, config: Config | None = None):
+    """C = A * B with A, Bcm and C in host memory (pinned for asynchronous copies).
+
+    The library copies the operands to its own device buffers, multiplies, and
+    copies C back, all enqueued on `stream` (default: the current stream);
+    the call returns without waiting.  Returns C (allocated pinned if None).
+    """
+    import torch
+    if A.dim() != 2 or Bcm.dim() != 2 or A.shape[1] != Bcm.shape[1]:
+        raise ValueError("A must be M x K and Bcm N x K")
+    if A.dtype != Bcm.dtype or A.is_cuda or Bcm.is_cuda:
+        raise ValueError("A and Bcm must be host tensors of the same dtype")
+    if not (A.is_contiguous() and Bcm.is_contiguous()):
+        raise ValueError("A and Bcm must be contiguous")
+    M, K = A.shape
+    N = Bcm.shape[0]
+    if out_dtype is None:
+        out_dtype = C.dtype if C is not None else (torch.int32 if A.dtype == torch.int8 else A.dtype)
+    key = _dtype_key(A.dtype, out_dtype)
+    if C is None:
+        C = torch.empty((M, N), dtype=out_dtype).pin_memory()
+    elif C.shape != (M, N) or C.dtype != out_dtype or C.is_cuda or not C.is_contiguous():
+        raise ValueError("C must be a contiguous M x N host tensor of the output dtype")
+    cfg = ctypes.byref(config) if config is not None else None
+    rc = int((_lib or load()).sptg_gemm_host(M, N, K, DTYPES[key], A.data_ptr(), Bcm.data_ptr(),
+                                             C.data_ptr(), _stream_handle(stream), cfg))
     if rc != 0:
         raise SptgError(rc, last_error() or status_string(rc))
     return C

@@ -195,6 +195,34 @@ int scratch_for(int dev, cudaStream_t stream, size_t data_bytes, ScratchView* ou
   return SPTG_OK;
 }
 
+// Device copies of the operands and result of a host-buffer call
+// (sptg_gemm_host), one area per (device, stream), grown on demand and freed
+// in stream order like the scratch.
+struct IoArea {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, IoArea> g_io;
+
+int io_for(int dev, cudaStream_t stream, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  IoArea& a = g_io[{dev, stream}];
+  if (a.bytes < bytes) {
+    if (a.ptr) cudaFreeAsync(a.ptr, stream);
+    a.ptr = nullptr;
+    a.bytes = 0;
+    cudaError_t e = cudaMallocAsync(&a.ptr, bytes, stream);
+    if (e != cudaSuccess) {
+      a.ptr = nullptr;
+      t_last_error = std::string("cudaMallocAsync: ") + cudaGetErrorString(e);
+      return SPTG_ERR_NOMEM;
+    }
+    a.bytes = bytes;
+  }
+  *out = a.ptr;
+  return SPTG_OK;
+}
+
 // ------------------------------------------------------------ tensor maps
 // The last tensor maps this thread encoded, keyed by everything that goes
 // into them: a call on the same buffers and shape reuses them.
@@ -1033,6 +1061,57 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, int dtype, const void* A,
 int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B,
                  void* C, void* stream, const sptg_config* cfg) {
   return sptg_gemm_strided(M, N, K, dtype, A, K, B, K, C, N, stream, cfg);
+}
+
+int sptg_gemm_host(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B,
+                   void* C, void* stream, const sptg_config* cfg) {
+  t_launches = 0;
+  DtypeInfo d;
+  if (!dtype_info(dtype, d)) {
+    t_last_error = "unknown dtype";
+    return SPTG_ERR_ARG;
+  }
+  if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) {
+    t_last_error = "dimensions must be in [0, 2^31)";
+    return SPTG_ERR_ARG;
+  }
+  if (M == 0 || N == 0) {
+    set_config("kernel=none dtype=%s (empty output)", d.name, {});
+    return SPTG_OK;
+  }
+  if (!C || (K > 0 && (!A || !B))) {
+    t_last_error = "null pointer";
+    return SPTG_ERR_ARG;
+  }
+  if ((K * d.in_bytes) % 16 != 0 || (N * d.out_bytes) % 16 != 0) {
+    t_last_error = "TMA needs 16-byte row pitches";
+    return SPTG_ERR_ALIGN;
+  }
+  int dev = 0;
+  DeviceInfo di;
+  int rc = device_info(di, dev);
+  if (rc) return rc;
+  cudaStream_t stream_h = static_cast<cudaStream_t>(stream);
+  auto pad = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+  const size_t a_bytes = static_cast<size_t>(M) * K * d.in_bytes;
+  const size_t b_bytes = static_cast<size_t>(N) * K * d.in_bytes;
+  const size_t c_bytes = static_cast<size_t>(M) * N * d.out_bytes;
+  void* base = nullptr;
+  rc = io_for(dev, stream_h, pad(a_bytes) + pad(b_bytes) + pad(c_bytes), &base);
+  if (rc) return rc;
+  char* dA = static_cast<char*>(base);
+  char* dB = dA + pad(a_bytes);
+  char* dC = dB + pad(b_bytes);
+  cudaError_t e = cudaSuccess;
+  if (a_bytes) e = cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream_h);
+  if (e == cudaSuccess && b_bytes)
+    e = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, stream_h);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (operands to the device)");
+  rc = sptg_gemm_strided(M, N, K, dtype, dA, K, dB, K, dC, N, stream, cfg);
+  if (rc) return rc;
+  e = cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, stream_h);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (result to the host)");
+  return SPTG_OK;
 }
 
 int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B, void* C,

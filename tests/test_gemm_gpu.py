@@ -451,6 +451,36 @@ def test_leading_dimensions_zero_k():
     assert (Cbuf[:, :64].cpu() == 0).all() and (Cbuf[:, 64:].cpu() == 3).all()
 
 
+# ------------------------------------------------------------ host buffers
+@pytest.mark.parametrize("it,ot", [("f16", F16), ("bf16", F32), ("s8", I32)])
+def test_host_buffers(it, ot):
+    # sptg_gemm_host: operands and result in pinned host memory, the copies
+    # enqueued by the library around the product
+    A, B = make_inputs(264, 520, 1040, it, "int8" if it == "s8" else "uniform", 70)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    C = sptg.gemm_host(hA, hB, out_dtype=ot)
+    torch.cuda.synchronize()
+    assert sptg.device_error() == 0
+    if it == "s8":
+        assert_int_parity(C.clone(), A, B)
+    else:
+        assert_float_parity(C.clone(), A, B)
+
+
+def test_host_buffers_pageable_and_two_streams():
+    A, B = make_inputs(300, 256, 512, "f16", "uniform", 71)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    C1 = torch.empty(300, 256, dtype=F32)               # pageable
+    C2 = torch.empty(300, 256, dtype=F32).pin_memory()  # pinned
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    sptg.gemm_host(A, B, C=C1, stream=s1)
+    sptg.gemm_host(hA, hB, C=C2, stream=s2)
+    torch.cuda.synchronize()
+    assert sptg.device_error() == 0
+    assert_float_parity(C1, A, B)
+    assert torch.equal(C1, C2)
+
+
 # ------------------------------------------------------------ stream / errors
 def test_async_on_a_side_stream():
     A, B = make_inputs(512, 512, 512, "f16", "uniform", 21)
