@@ -276,8 +276,11 @@ __global__ void __launch_bounds__(192, 1)
         for (int m = 0; m < MN; ++m) __stcg(slot + m * BNT + n_local, acc[m]);
         __threadfence();
         named_barrier_sync(1, 128);
-        if (threadIdx.x == 64) *last_flag = arrive_generation(p.counters + nt, p.generation, count,
-                                                              p.error_word);
+        if (threadIdx.x == 64) {
+          *last_flag = arrive_generation(p.counters + nt, p.generation, count, p.error_word);
+          // the last arrival is the last use of the counter in this call
+          if (*last_flag) atomicExch(p.counters + nt, 0ull);
+        }
         named_barrier_sync(1, 128);
         if (*last_flag) {
           // Sum the partial tiles in contributor order (increasing k), 16-byte

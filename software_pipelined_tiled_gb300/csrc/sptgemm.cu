@@ -169,10 +169,31 @@ struct ScratchView {
   unsigned int generation;  // a new non-zero tag for this call's counters
 };
 
+// Growing a stream-ordered allocation inside a CUDA graph capture would put
+// the allocation into the graph (valid only while the graph runs), so under
+// capture the area must already be large enough: a call made once on the
+// stream before capturing sizes it.
+bool stream_capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &st) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return st != cudaStreamCaptureStatusNone;
+}
+
+int capture_growth_error() {
+  t_last_error =
+      "the library's device buffers for this stream must exist before graph capture: make the "
+      "same call once on the stream first";
+  return SPTG_ERR_CONFIG;
+}
+
 int scratch_for(int dev, cudaStream_t stream, size_t data_bytes, ScratchView* out) {
   std::lock_guard<std::mutex> lk(g_mu);
   Scratch& s = g_scratch[{dev, stream}];
   const size_t need = kCounterArea + data_bytes;
+  if (s.bytes < need && stream_capturing(stream)) return capture_growth_error();
   if (s.bytes < need) {
     if (s.ptr) cudaFreeAsync(s.ptr, stream);
     s.ptr = nullptr;
@@ -207,6 +228,7 @@ std::map<std::pair<int, cudaStream_t>, IoArea> g_io;
 int io_for(int dev, cudaStream_t stream, size_t bytes, void** out) {
   std::lock_guard<std::mutex> lk(g_mu);
   IoArea& a = g_io[{dev, stream}];
+  if (a.bytes < bytes && stream_capturing(stream)) return capture_growth_error();
   if (a.bytes < bytes) {
     if (a.ptr) cudaFreeAsync(a.ptr, stream);
     a.ptr = nullptr;

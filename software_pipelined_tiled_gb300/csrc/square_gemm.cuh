@@ -641,8 +641,9 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
         int flag = 0;
         if (wait_bounded(note_full(j), use & 1u, ctl, WAIT_FIXUP_NOTE)) {
           mbar_arrive(note_empty(j));  // the notice is consumed
-          flag = wait_arrivals(p.counters + seg.sk * 2 + rank, p.generation, seg.count, ctl) ? 1
-                                                                                          : 0;
+          unsigned long long* ctr = p.counters + seg.sk * 2 + rank;
+          flag = wait_arrivals(ctr, p.generation, seg.count, ctl) ? 1 : 0;
+          if (flag) depart_generation(ctr, seg.count);
         }
         fix_flag[j] = flag;
       }

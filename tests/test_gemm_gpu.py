@@ -481,6 +481,72 @@ def test_host_buffers_pageable_and_two_streams():
     assert torch.equal(C1, C2)
 
 
+# ------------------------------------------------------------ CUDA graphs
+def _replay_three_times(call, C, A, B):
+    # one call captured in a graph and replayed: the split-K counters must be
+    # back at 0 after each replay, since every replay carries the generation
+    # the call was captured with
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call(s)  # sizes the stream's library buffers before the capture
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(s)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        C.fill_(-1)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sptg.device_error() == 0
+        assert_float_parity(C.cpu(), A, B)
+
+
+@pytest.mark.parametrize("cta_pair", [1, 2])
+def test_graph_replays_of_a_stream_k_call(cta_pair):
+    A, B = make_inputs(520, 776, 1096, "bf16", "uniform", 81)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty(520, 776, dtype=F32, device="cuda")
+    _replay_three_times(lambda s: sptg.gemm(dA, dB, C=C, stream=s, cta_pair=cta_pair,
+                                            stream_k=2, splits=5), C, A, B)
+
+
+def test_graph_replays_of_a_skinny_split_call():
+    A, B = make_inputs(48, 2048, 1024, "bf16", "normal", 82)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty(48, 2048, dtype=BF16, device="cuda")
+    _replay_three_times(lambda s: sptg.gemm(dA, dB, C=C, stream=s, kernel="skinny"), C, A, B)
+    assert "units=" in sptg.last_config()
+
+
+def test_graph_replays_of_the_allocation_free_call():
+    A, B = make_inputs(64, 4096, 2048, "bf16", "normal", 83)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty(64, 4096, dtype=BF16, device="cuda")
+
+    def call(s):
+        rc = sptg.gemm_skinny_noalloc_raw(64, 4096, 2048, "bf16_bf16", dA.data_ptr(),
+                                          dB.data_ptr(), C.data_ptr(), s.cuda_stream)
+        assert rc == 0
+    _replay_three_times(call, C, A, B)
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
+def test_graph_capture_before_the_buffers_exist_is_refused():
+    A, B = make_inputs(512, 768, 1024, "f16", "uniform", 84)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty(512, 768, dtype=F32, device="cuda")
+    s = torch.cuda.Stream()  # never used before: no scratch for it yet
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(sptg.SptgError, match="before graph capture"):
+        with torch.cuda.graph(g, stream=s):
+            sptg.gemm(dA, dB, C=C, stream=s, stream_k=2, splits=7)
+    torch.cuda.synchronize()
+    # the library and the context are fine afterwards
+    assert_float_parity(run(A, B, F32, stream_k=2, splits=7), A, B)
+
+
 # ------------------------------------------------------------ stream / errors
 def test_async_on_a_side_stream():
     A, B = make_inputs(512, 512, 512, "f16", "uniform", 21)
