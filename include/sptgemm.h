@@ -80,7 +80,7 @@ int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype,
 typedef struct {
   int kernel;   /* 0 auto, 1 square, 2 skinny swap-AB with stream-K split,
                    3 skinny swap-AB with the K split across a cluster of
-                   two CTAs (splits = cluster size, 1 or 2)                  */
+                   CTAs (splits = cluster size, 1, 2 or 4)                   */
   int bn;       /* square: tile columns (multiple of 16, 16..256)           */
   int stages;   /* shared-memory ring depth (1 = synchronous load/compute)  */
   int splits;   /* square: cap on persistent workers; skinny stream-K: CTAs

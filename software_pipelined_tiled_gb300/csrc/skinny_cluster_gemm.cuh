@@ -1,21 +1,20 @@
 // skinny_cluster_gemm.cuh -- the memory-bound skinny product (M <= 64) with
-// its K split across the two CTAs of a thread-block cluster.
+// its K split across the CTAs of a thread-block cluster (1, 2 or 4).
 //
 // Same arithmetic as skinny_gemm.cuh (swap-AB: D^T[n, m] = sum_k Bcm[n, k] *
 // A[m, k], MMA M = 128 over N, MMA N = MN over the rows of A), but the work
-// is cut along whole column tiles: one cluster of CS (1 or 2) CTAs per
+// is cut along whole column tiles: one cluster of CS (1, 2 or 4) CTAs per
 // 128-column tile, CTA rank r streaming the contiguous K-range
 // [r*KT/CS, (r+1)*KT/CS). Each CTA accumulates its range in tensor memory.
-// Then each rank finalises one half of the columns: it pushes the partial of
-// the other half straight into the peer's receive buffer (distributed shared
-// memory stores) and arrives on a barrier there, adds the half it received to
-// its own (two fp32 terms: the same bits in either order), converts, stages
-// its output block in shared memory and writes it with one tensor-copy store.
+// Then each rank finalises 128 / CS of the columns: it pushes its partial of
+// the other ranks' columns straight into their receive buffers (distributed
+// shared memory stores) and arrives on a barrier there, adds the CS partials
+// of its own columns in rank order (a fixed order), converts, stages its
+// output block in shared memory and writes it with one tensor-copy store.
 //
 // Compared with the stream-K kernel this needs no global scratch and no
-// atomics: the reduction is one push between the two SMs of a cluster. The
-// grid is (column tiles x CS) CTAs, which the host uses when that fills the
-// GPU.
+// atomics: the reduction is one push between the SMs of a cluster. The grid
+// is (column tiles x CS) CTAs, which the host uses when that fills the GPU.
 #pragma once
 
 #include "common.cuh"
@@ -45,14 +44,17 @@ struct SkinnyClusterLayout {
   static constexpr int BT_STAGE = KSUB * SUB_BT;
   static constexpr int A_STAGE = KSUB * SUB_A;
   static constexpr int STAGE = BT_STAGE + A_STAGE;
-  // receive buffer for the peer's partial: a row of MN floats for each of the
-  // 64 columns this rank finalises, plus 16 bytes so that 16-byte accesses of
-  // 8 consecutive rows hit 8 distinct bank groups
+  // receive buffer for the other ranks' partials: for each of the columns
+  // this rank finalises, a row of MN floats from each other rank (at most
+  // 3 x 32 columns, cluster of 4), plus 16 bytes per row so that 16-byte
+  // accesses of 8 consecutive rows hit 8 distinct bank groups
   static constexpr int PART_ROW = MN * 4 + 16;
+  static constexpr int RECV_ROWS = 96;  // max over cluster sizes 2 (1 x 64) and 4 (3 x 32)
   // output staging (reuses the receive buffer once it has been read): MN rows
   // of up to 128 outputs, the layout of C
   static constexpr int OUT_BYTES = MN * BNT * OBYTES;
-  static constexpr int PART_BYTES = 64 * PART_ROW > OUT_BYTES ? 64 * PART_ROW : OUT_BYTES;
+  static constexpr int PART_BYTES =
+      RECV_ROWS * PART_ROW > OUT_BYTES ? RECV_ROWS * PART_ROW : OUT_BYTES;
   static constexpr int OFF_PART = STAGES * STAGE;
   static constexpr int OFF_BAR = OFF_PART + PART_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 3;
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t cs = cluster_nctarank();  // 1 or 2
+  const uint32_t cs = cluster_nctarank();  // 1, 2 or 4
   const uint32_t rank = cluster_ctarank();
   const int nt = static_cast<int>(blockIdx.x / cs);
   const int KT = p.num_k_tiles;
@@ -130,7 +132,8 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
-    mbar_init(recv_bar, 64);  // one arrival per pushing thread of the peer
+    // one arrival per pushing thread of the other ranks: (cs - 1) x 128 / cs
+    mbar_init(recv_bar, cs > 1 ? static_cast<int>((cs - 1) * (128 / cs)) : 1);
     *abort_flag = 0;
     *failed = 0;
     fence_mbar_init();
@@ -276,31 +279,36 @@ __global__ void __launch_bounds__(192, 1)
           acc[32 * cb + i] = (kt1 > kt0) ? __uint_as_float(r[i]) : 0.0f;
       }
     }
-    // With two ranks each finalises half of the 128 columns: rank 0 columns
-    // 0-63, rank 1 columns 64-127. A warp whose 32 columns belong to the other
-    // rank pushes its partial into that rank's receive buffer (distributed
-    // shared memory stores) and arrives on its barrier (release, cluster
-    // scope: each thread covers its own stores); the two halves move at once.
-    // A rank that failed does not arrive, and the peer's bounded wait gives up.
-    const int half = q >> 1;              // which 64 columns this warp holds
-    const bool keep = (cs == 1) || (half == static_cast<int>(rank));
-    const int col = (cs == 1) ? n_local : (n_local & 63);  // column within the kept block
-    const int keep_threads = (cs == 1) ? 128 : 64;
+    // With cs ranks each finalises 128 / cs of the columns (rank r the block
+    // r * 128 / cs ..): a warp whose 32 columns belong to another rank pushes
+    // its partial into that rank's receive buffer (distributed shared memory
+    // stores, one slot per sending rank) and arrives on its barrier (release,
+    // cluster scope: each thread covers its own stores); all ranks' blocks
+    // move at once. A rank that failed does not arrive, and the owner's
+    // bounded wait gives up.
+    const int cpr = BNT / static_cast<int>(cs);  // columns each rank finalises
+    const int owner = (32 * q) / cpr;              // cs <= 4: whole warps
+    const bool keep = owner == static_cast<int>(rank);
+    const int col = n_local - owner * cpr;         // column within the owner's block
+    const int keep_threads = cpr;
     if (!keep) {
       if (mine_ok) {
-        const uint32_t dst = map_to_cta(smem_addr(part + col * L::PART_ROW), rank ^ 1u);
+        const int slot = static_cast<int>(rank) < owner ? static_cast<int>(rank)
+                                                        : static_cast<int>(rank) - 1;
+        const uint32_t dst = map_to_cta(smem_addr(part + (slot * cpr + col) * L::PART_ROW),
+                                        static_cast<uint32_t>(owner));
 #pragma unroll
         for (int i = 0; i < MN / 4; ++i)
           st_shared_cluster_f4(dst + 16 * i,
                                make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]));
-        mbar_arrive_cluster(map_to_cta(recv_bar, rank ^ 1u));
+        mbar_arrive_cluster(map_to_cta(recv_bar, static_cast<uint32_t>(owner)));
       }
     } else {
       bool ok = mine_ok;
       if (cs > 1) {
         ok = named_barrier_and(1, keep_threads,
                                ok && wait_bounded(recv_bar, 0, ctl, WAIT_EPI_TMEM_FULL));
-        if (ok) {
+        if (ok && cs == 2) {
           // two partials: their fp32 sum is the same in either order
           const uint8_t* row = part + col * L::PART_ROW;
           float4 v[MN / 4];
@@ -312,6 +320,47 @@ __global__ void __launch_bounds__(192, 1)
             acc[4 * i + 1] += v[i].y;
             acc[4 * i + 2] += v[i].z;
             acc[4 * i + 3] += v[i].w;
+          }
+        } else if (ok) {
+          // four partials added in rank order (= increasing k): a fixed
+          // order; the three received ones are loaded 4 chunks at a time
+          const int k = static_cast<int>(rank);
+#pragma unroll
+          for (int i0 = 0; i0 < MN / 4; i0 += 4) {
+            float4 t[3][4];
+#pragma unroll
+            for (int sl = 0; sl < 3; ++sl)
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                t[sl][j] = *reinterpret_cast<const float4*>(
+                    part + (sl * cpr + col) * L::PART_ROW + 16 * (i0 + j));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int i = i0 + j;
+              const float4 own = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+              // rank r's partial: this rank's own, or receive slot r (r < k) / r - 1
+              const float4 p0 = k == 0 ? own : t[0][j];
+              const float4 p1 = k == 1 ? own : (k > 1 ? t[1][j] : t[0][j]);
+              const float4 p2 = k == 2 ? own : (k > 2 ? t[2][j] : t[1][j]);
+              const float4 p3 = k == 3 ? own : t[2][j];
+              float4 s4 = p0;
+              s4.x += p1.x;
+              s4.y += p1.y;
+              s4.z += p1.z;
+              s4.w += p1.w;
+              s4.x += p2.x;
+              s4.y += p2.y;
+              s4.z += p2.z;
+              s4.w += p2.w;
+              s4.x += p3.x;
+              s4.y += p3.y;
+              s4.z += p3.z;
+              s4.w += p3.w;
+              acc[4 * i] = s4.x;
+              acc[4 * i + 1] = s4.y;
+              acc[4 * i + 2] = s4.z;
+              acc[4 * i + 3] = s4.w;
+            }
           }
         }
         named_barrier_sync(1, keep_threads);  // the receive buffer is read: reuse it for staging
@@ -336,7 +385,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         fence_proxy_async_smem();
         named_barrier_sync(1, keep_threads);
-        const int x0 = nt * BNT + (cs == 1 ? 0 : static_cast<int>(rank) * 64);
+        const int x0 = nt * BNT + static_cast<int>(rank) * cpr;
         if (col == 0 && x0 < p.N) {
           tma_store_2d(&tmC, smem_addr(stage), x0, 0);
           bulk_commit_group();

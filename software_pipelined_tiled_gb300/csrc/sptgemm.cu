@@ -815,18 +815,18 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   const int n_tiles = static_cast<int>((N + BNT - 1) / BNT);
   const int kstep = BK * v.ksub;  // K per ring stage
   const int k_tiles = static_cast<int>((K + kstep - 1) / kstep);
-  // cluster size: forced (splits), else 2 when two CTAs per column tile fit
-  // the SMs, else 1; taken only if the grid fills at least three quarters of
-  // the SMs
+  // cluster size: forced (splits), else the largest of 4, 2, 1 whose CTAs
+  // (cluster size per column tile) fit the SMs; taken only if the grid fills
+  // at least three quarters of the SMs
   int cs = 0;
   if (forced && cfg.splits > 0) {
     cs = cfg.splits;
-    if (cs > 2) {
-      t_last_error = "cluster size must be 1 or 2";
+    if (cs != 1 && cs != 2 && cs != 4) {
+      t_last_error = "cluster size must be 1, 2 or 4";
       return SPTG_ERR_CONFIG;
     }
   } else {
-    for (int c : {2, 1}) {
+    for (int c : {4, 2, 1}) {
       if (static_cast<int64_t>(n_tiles) * c <= di.sm_count && k_tiles >= 2 * c) {
         cs = c;
         break;

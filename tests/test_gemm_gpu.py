@@ -277,7 +277,8 @@ def test_skinny_split_and_ragged(M, N, K, splits):
 
 @pytest.mark.parametrize("M,N,K,cs", [
     (64, 8192, 4096, 2), (64, 4096, 2048, 2), (17, 1000, 1000, 2), (1, 2048, 1040, 2),
-    (40, 768, 520, 1), (64, 256, 64, 2), (33, 1024, 64, 1)])
+    (40, 768, 520, 1), (64, 256, 64, 2), (33, 1024, 64, 1),
+    (64, 4096, 8192, 4), (48, 1000, 1088, 4), (64, 512, 512, 4), (5, 2048, 4160, 4)])
 def test_skinny_cluster_split(M, N, K, cs):
     A, B = make_inputs(M, N, K, "bf16", "normal", M * 3 + K)
     C = run(A, B, BF16, kernel="skinny_cluster", splits=cs)
@@ -286,7 +287,7 @@ def test_skinny_cluster_split(M, N, K, cs):
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 8, 17])
-@pytest.mark.parametrize("cs", [1, 2])
+@pytest.mark.parametrize("cs", [1, 2, 4])
 def test_k_tile_marker_skinny_cluster(T, cs):
     # every rank's K-range lands in the sum exactly once
     A, B, expect = _marker_inputs(64, 1024, T * cs, dtype=BF16)
