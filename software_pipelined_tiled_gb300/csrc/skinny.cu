@@ -5,29 +5,32 @@
 
 namespace sptg {
 
-template <int MN, int ST, bool BF, int OUT>
+template <int MN, int ST, bool BF, int OUT, int KSUB>
 KernelVariant make_skinny() {
-  return {reinterpret_cast<const void*>(&skinny_gemm_kernel<MN, ST, BF, OUT>), MN, ST,
-          SkinnyLayout<MN, ST>::SMEM_BYTES, false};
+  KernelVariant v{reinterpret_cast<const void*>(&skinny_gemm_kernel<MN, ST, BF, OUT, KSUB>), MN,
+                  ST, SkinnyLayout<MN, ST, KSUB>::SMEM_BYTES, false};
+  v.ksub = KSUB;
+  return v;
 }
 
-// MMA N = 64 (up to 64 rows of A) at an 8-stage ring for every float dtype
-// pair; bfloat16 -> bfloat16 also at rings 1, 2 and 4 for the ablation.
+// MMA N = 64 (up to 64 rows of A), two 64-wide K-chunks per stage (each B
+// row read 256 contiguous bytes at a time) at a 4-stage ring for every float
+// dtype pair; bfloat16 -> bfloat16 also at rings 1, 2 and 3 for the ablation.
 bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v) {
-  const int s = stages ? stages : 8;
-  if (s == 8) {
-    if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny<64, 8, true, OUT_BF16>();
-    else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny<64, 8, false, OUT_F16>();
-    else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny<64, 8, true, OUT_F32>();
-    else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny<64, 8, false, OUT_F32>();
+  const int s = stages ? stages : 4;
+  if (s == 4) {
+    if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny<64, 4, true, OUT_BF16, 2>();
+    else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny<64, 4, false, OUT_F16, 2>();
+    else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny<64, 4, true, OUT_F32, 2>();
+    else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny<64, 4, false, OUT_F32, 2>();
     else return false;
     return true;
   }
   if (!(in_bf16 && out_kind == OUT_BF16)) return false;
   switch (s) {
-    case 1: *v = make_skinny<64, 1, true, OUT_BF16>(); return true;
-    case 2: *v = make_skinny<64, 2, true, OUT_BF16>(); return true;
-    case 4: *v = make_skinny<64, 4, true, OUT_BF16>(); return true;
+    case 1: *v = make_skinny<64, 1, true, OUT_BF16, 2>(); return true;
+    case 2: *v = make_skinny<64, 2, true, OUT_BF16, 2>(); return true;
+    case 3: *v = make_skinny<64, 3, true, OUT_BF16, 2>(); return true;
     default: return false;
   }
 }

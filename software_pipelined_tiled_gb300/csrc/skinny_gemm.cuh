@@ -45,12 +45,16 @@ struct SkinnyParams {
   unsigned long long* trace;  // optional timeline (see TraceEvent), or null
 };
 
-template <int MN, int STAGES>
+// A ring stage holds KSUB consecutive 64-wide K-chunks (each its own
+// 128-byte-swizzled sub-tile) of B^T and of A: one unit of work is one stage.
+template <int MN, int STAGES, int KSUB = 1>
 struct SkinnyLayout {
   static constexpr int BNT = 128;  // output columns per tile (MMA M)
   static constexpr int BK = 64;
-  static constexpr int BT_STAGE = BNT * BK * 2;
-  static constexpr int A_STAGE = MN * BK * 2;
+  static constexpr int SUB_BT = BNT * BK * 2;
+  static constexpr int SUB_A = MN * BK * 2;
+  static constexpr int BT_STAGE = KSUB * SUB_BT;
+  static constexpr int A_STAGE = KSUB * SUB_A;
   static constexpr int STAGE = BT_STAGE + A_STAGE;
   static constexpr int OFF_BAR = STAGES * STAGE;
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
@@ -67,11 +71,11 @@ __device__ __forceinline__ int cta_of_unit(int64_t u, int G, int64_t T) {
   return static_cast<int>(((u + 1) * G - 1) / T);
 }
 
-template <int MN, int STAGES, bool IN_BF16, int OUT>
+template <int MN, int STAGES, bool IN_BF16, int OUT, int KSUB = 1>
 __global__ void __launch_bounds__(192, 1)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmBt,
                        const __grid_constant__ CUtensorMap tmA, const SkinnyParams p) {
-  using L = SkinnyLayout<MN, STAGES>;
+  using L = SkinnyLayout<MN, STAGES, KSUB>;
   constexpr int BNT = L::BNT, BK = L::BK;
   constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, BNT, MN);
   static_assert(OUT != OUT_S32, "the skinny kernel writes float outputs");
@@ -127,8 +131,11 @@ __global__ void __launch_bounds__(192, 1)
     for (int64_t u = u_begin0; u < min(u_end0, u_begin0 + STAGES); ++u) {
       const int nt = static_cast<int>(u / p.num_k_tiles);
       const int kt = static_cast<int>(u - static_cast<int64_t>(nt) * p.num_k_tiles);
-      tma_prefetch_l2_2d(&tmBt, kt * L::BK, nt * L::BNT);
-      tma_prefetch_l2_2d(&tmA, kt * L::BK, 0);
+#pragma unroll
+      for (int j = 0; j < KSUB; ++j) {
+        tma_prefetch_l2_2d(&tmBt, (kt * KSUB + j) * L::BK, nt * L::BNT);
+        tma_prefetch_l2_2d(&tmA, (kt * KSUB + j) * L::BK, 0);
+      }
     }
   }
   // Set-up above may overlap the previous kernel in the stream; no global
@@ -163,8 +170,13 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (p.inject_stall && it == 1) continue;  // test hook: this stage never fills
         mbar_arrive_expect_tx(full_bar(s), L::STAGE);
-        tma_load_2d(stage_bt(s), &tmBt, full_bar(s), kt * BK, nt * BNT, pol_stream);
-        tma_load_2d(stage_a(s), &tmA, full_bar(s), kt * BK, 0, pol_keep);
+#pragma unroll
+        for (int j = 0; j < KSUB; ++j) {
+          tma_load_2d(stage_bt(s) + j * L::SUB_BT, &tmBt, full_bar(s), (kt * KSUB + j) * BK,
+                      nt * BNT, pol_stream);
+          tma_load_2d(stage_a(s) + j * L::SUB_A, &tmA, full_bar(s), (kt * KSUB + j) * BK, 0,
+                      pol_keep);
+        }
         issued_round[s] = static_cast<int>(round);
         if (it == 0) trace_mark(p.trace, TR_FIRST_LOAD);
           trace_ktile(p.trace, 0, it);
@@ -209,9 +221,13 @@ __global__ void __launch_bounds__(192, 1)
           if (it == 0) trace_mark(p.trace, TR_FIRST_DATA);
             trace_ktile(p.trace, 1, it);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            mma_f16(d_tmem, sdesc_k_major_sw128(stage_bt(s) + 32 * k),
-                    sdesc_k_major_sw128(stage_a(s) + 32 * k), IDESC, (v > u || k > 0) ? 1u : 0u);
+          for (int j = 0; j < KSUB; ++j) {
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              mma_f16(d_tmem, sdesc_k_major_sw128(stage_bt(s) + j * L::SUB_BT + 32 * k),
+                      sdesc_k_major_sw128(stage_a(s) + j * L::SUB_A + 32 * k), IDESC,
+                      (v > u || j > 0 || k > 0) ? 1u : 0u);
+            }
           }
           mma_commit(empty_bar(s));
         }

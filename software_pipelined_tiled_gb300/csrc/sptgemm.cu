@@ -714,6 +714,7 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
     return SPTG_ERR_CONFIG;
   }
   const int BNT = 128, BK = 64;
+  const int kstep = BK * v.ksub;  // K per ring stage (one unit of work)
   CUtensorMap tb, ta;
   // MMA operand A is the B^T tile (128 output columns x 64 k), operand B is the A tile.
   int rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, BK, BNT, CU_TENSOR_MAP_SWIZZLE_128B, ldb);
@@ -728,7 +729,7 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.num_n_tiles = static_cast<int>((N + BNT - 1) / BNT);
-  p.num_k_tiles = static_cast<int>((K + BK - 1) / BK);
+  p.num_k_tiles = static_cast<int>((K + kstep - 1) / kstep);
   const int64_t units = static_cast<int64_t>(p.num_n_tiles) * p.num_k_tiles;
   int grid = cfg.splits > 0 ? cfg.splits : di.sm_count;
   grid = static_cast<int>(std::min<int64_t>(grid, units));
@@ -794,7 +795,7 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   set_config(
       "kernel=skinny dtype=%s mma_m=%lld mma_n=%lld bk=%lld stages=%lld grid=%lld n_tiles=%lld "
       "k_tiles=%lld units=%lld max_contrib=%lld smem=%lld",
-      d.name, {BNT, v.bn, BK, v.stages, grid, p.num_n_tiles, p.num_k_tiles, (long long)units,
+      d.name, {BNT, v.bn, kstep, v.stages, grid, p.num_n_tiles, p.num_k_tiles, (long long)units,
                max_contrib, v.smem});
   return SPTG_OK;
 }

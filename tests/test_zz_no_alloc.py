@@ -58,7 +58,9 @@ def test_noalloc_matches_the_allocating_entry_on_two_calls(M, N, K):
 def test_noalloc_rejects_what_it_cannot_hold():
     stream = torch.cuda.current_stream().cuda_stream
     # a split that needs ~128 MiB of partial tiles: far beyond the fixed array
-    M, N, K = 64, 262144, 128
+    # (3 K-steps of 128 per column tile, 6144 units over the CTAs: the CTA
+    # boundaries fall inside column tiles)
+    M, N, K = 64, 262144, 384
     A = torch.zeros(M, K, dtype=BF16, device="cuda")
     B = torch.zeros(N, K, dtype=BF16, device="cuda")
     C = torch.empty(M, N, dtype=BF16, device="cuda")
