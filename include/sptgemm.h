@@ -226,6 +226,19 @@ int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype,
 /* Library ABI version (major*100 + minor). */
 int sptg_version(void);
 
+/*
+ * The square kernel's plan for a shape, computed on the host alone (no
+ * device is touched), for a GPU of `sm_count` SMs: the tile shape and the
+ * schedule sptg_gemm_ex would choose with configuration `cfg` (NULL =
+ * defaults), before any fallback for a missing ring depth. On success
+ * out[0..6] = tile columns BN, CTA pair (0/1), tiles, workers (CTAs or
+ * pairs), tiles cut along K (stream-K), workers sharing them, and the most
+ * contributors one cut tile can have. SPTG_ERR_ARG for a non-positive
+ * dimension, fewer than 2 SMs, an unknown dtype or an invalid field.
+ */
+int sptg_plan_square(int64_t M, int64_t N, int64_t K, int dtype, int sm_count,
+                     const sptg_config* cfg, int* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,7 +19,7 @@ import threading
 
 from ._build import LIB_PATH, build
 
-__all__ = ["DTYPES", "SptgError", "Config", "load", "gemm", "gemm_host", "gemm_raw",
+__all__ = ["DTYPES", "SptgError", "Config", "load", "gemm", "gemm_host", "gemm_raw", "plan_square",
            "gemm_strided_raw",
            "gemm_skinny_noalloc_raw",
            "stream_scale",
@@ -35,7 +35,7 @@ KERNELS = {"auto": 0, "square": 1, "skinny": 2, "skinny_cluster": 3}
 
 # the C functions every build must export (checked by the tests)
 EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_gemm_strided", "sptg_gemm_host",
-           "sptg_status_string", "sptg_last_error",
+           "sptg_plan_square", "sptg_status_string", "sptg_last_error",
            "sptg_last_config", "sptg_device_error", "sptg_version", "sptg_gemm_skinny_noalloc",
            "sptg_stream_scale", "sptg_stream_scale_ex")
 
@@ -96,11 +96,26 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sptg_stream_scale_ex.argtypes = [i64, ctypes.c_float, vp, vp, vp,
                                              ctypes.POINTER(Config)]
         lib.sptg_stream_scale_ex.restype = ctypes.c_int
+        lib.sptg_plan_square.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_int)]
+        lib.sptg_plan_square.restype = ctypes.c_int
         lib.sptg_version.argtypes = []
         lib.sptg_version.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
+
+
+def plan_square(M: int, N: int, K: int, dtype: str, sm_count: int,
+                config: Config | None = None) -> dict:
+    """The square kernel's plan for a shape on a GPU of sm_count SMs (host only)."""
+    out = (ctypes.c_int * 7)()
+    cfg = ctypes.byref(config) if config is not None else None
+    rc = int(load().sptg_plan_square(M, N, K, DTYPES[dtype], sm_count, cfg, out))
+    if rc != 0:
+        raise SptgError(rc, last_error() or status_string(rc))
+    keys = ("bn", "pair", "tiles", "workers", "stream_k_tiles", "stream_k_workers", "max_contrib")
+    return dict(zip(keys, list(out)))
 
 
 def status_string(status: int) -> str:

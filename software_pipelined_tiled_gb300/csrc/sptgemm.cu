@@ -922,6 +922,47 @@ extern "C" {
 
 int sptg_version(void) { return 100; }
 
+int sptg_plan_square(int64_t M, int64_t N, int64_t K, int dtype, int sm_count,
+                     const sptg_config* cfg_in, int* out) {
+  DtypeInfo d;
+  if (!out || sm_count < 2 || !dtype_info(dtype, d) || M <= 0 || N <= 0 || K <= 0 ||
+      M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) {
+    t_last_error = "invalid argument";
+    return SPTG_ERR_ARG;
+  }
+  sptg_config cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  if (cfg_in) cfg = *cfg_in;
+  if (cfg.stream_k < 0 || cfg.stream_k > 2 || cfg.cta_pair < 0 || cfg.cta_pair > 2 ||
+      cfg.bn < 0 || cfg.splits < 0) {
+    t_last_error = "invalid configuration field";
+    return SPTG_ERR_ARG;
+  }
+  int bn = 0;
+  bool pair = false, sk = false;
+  choose_square_shape(M, N, K, sm_count, cfg, d.is_int8, &bn, &pair, &sk);
+  const int64_t rows = pair ? 256 : 128;
+  const int64_t T64 = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
+  const int tiles = static_cast<int>(std::min<int64_t>(T64, INT32_MAX));
+  const int k_tiles = static_cast<int>((K + 63) / 64);
+  int workers = pair ? sm_count / 2 : sm_count;
+  if (cfg.splits > 0) workers = std::min(workers, cfg.splits);
+  int skt = 0, skw = 0, mc = 1;
+  plan_stream_k(tiles, workers, k_tiles, cfg.stream_k == 2 ? 2 : (sk ? 0 : 1), &skt, &skw, &mc);
+  if (skt == 0)
+    workers = std::min(workers, tiles);
+  else if (skt == tiles)
+    workers = skw;
+  out[0] = bn;
+  out[1] = pair ? 1 : 0;
+  out[2] = tiles;
+  out[3] = workers;
+  out[4] = skt;
+  out[5] = skw;
+  out[6] = mc;
+  return SPTG_OK;
+}
+
 const char* sptg_status_string(int status) {
   switch (status) {
     case SPTG_OK: return "ok";

@@ -1,0 +1,117 @@
+"""Host logic of the square kernel's planning, through the C ABI, on the CPU.
+
+sptg_plan_square runs the tile-shape model and the stream-K split of
+sptg_gemm_ex without touching a device. These tests check the choices the
+method depends on (a partial last round cut along K at 4096^3, small
+products left data-parallel, the int8 tile widths) and, over many random
+shapes and configurations, the invariants the kernels rely on: a cut tile
+never has more contributors than the scratch holds slots for, every
+stream-K worker gets at least 8 K-tiles, and forced settings are honoured.
+"""
+import random
+
+import pytest
+
+import software_pipelined_tiled_gb300 as sptg
+
+SM = 152  # GB300
+
+
+def plan(M, N, K, dtype="f16_f16", sm=SM, **cfg):
+    c = None
+    if cfg:
+        c = sptg.Config()
+        for k, v in cfg.items():
+            setattr(c, k, v)
+    return sptg.plan_square(M, N, K, dtype, sm, c)
+
+
+def test_headline_cuts_the_partial_last_round():
+    p = plan(4096, 4096, 4096)
+    # 256 x 256 pair tiles: 16 x 16 = 256 tiles = 3 rounds of 76 pairs + 28
+    assert (p["bn"], p["pair"], p["tiles"], p["workers"]) == (256, 1, 256, 76)
+    assert p["stream_k_tiles"] == 256 % 76 == 28
+    assert p["stream_k_workers"] == 76
+
+
+@pytest.mark.parametrize("size", [256, 512, 1024, 2048])
+def test_small_products_stay_data_parallel(size):
+    assert plan(size, size, size)["stream_k_tiles"] == 0
+
+
+def test_int8_takes_one_cta_tiles_that_fit_tensor_memory():
+    for size in (1024, 4096, 8192):
+        p = plan(size, size, size, "s8_s32")
+        assert p["pair"] == 0 and p["bn"] in (128, 160)
+    assert plan(4096, 4096, 4096, "s8_s32", cta_pair=2)["pair"] == 1
+
+
+def test_stream_k_settings():
+    assert plan(4096, 4096, 4096, stream_k=1)["stream_k_tiles"] == 0
+    p = plan(4096, 4096, 4096, stream_k=2)
+    assert p["stream_k_tiles"] == p["tiles"]
+
+
+def test_forced_fields_are_honoured():
+    for bn in (128, 160, 192, 224, 256):
+        for pair in (1, 2):
+            p = plan(3000, 5000, 700, bn=bn, cta_pair=pair)
+            assert p["bn"] == bn and p["pair"] == pair - 1
+    assert plan(4096, 4096, 4096, splits=10)["workers"] <= 10
+
+
+def test_arguments_are_checked():
+    for args in [(0, 64, 64, "f16_f16", SM), (64, 64, 64, "f16_f16", 1),
+                 (64, 64, -1, "f16_f16", SM)]:
+        with pytest.raises(sptg.SptgError):
+            sptg.plan_square(*args)
+    c = sptg.Config()
+    c.stream_k = 3
+    with pytest.raises(sptg.SptgError):
+        sptg.plan_square(64, 64, 64, "f16_f16", SM, c)
+
+
+def _owner(u, G, U):
+    # the worker whose unit range [w * U / G, (w + 1) * U / G) holds unit u
+    for w in range(G):
+        if w * U // G <= u < (w + 1) * U // G:
+            return w
+    raise AssertionError("unit without a worker")
+
+
+def test_plan_invariants_over_random_shapes():
+    rng = random.Random(7)
+    dtypes = ["f16_f16", "f16_f32", "bf16_bf16", "bf16_f32", "s8_s32"]
+    for _ in range(300):
+        M, N = rng.randint(1, 20000), rng.randint(1, 20000)
+        K = rng.randint(1, 9000)
+        dt = rng.choice(dtypes)
+        sm = rng.choice([8, 20, 100, 132, 148, 152])
+        cfg = {}
+        if rng.random() < 0.3:
+            cfg["stream_k"] = rng.choice([0, 1, 2])
+        if rng.random() < 0.3:
+            cfg["splits"] = rng.randint(1, 40)
+        if cfg.get("stream_k") == 2 and M * N > 4e7:
+            cfg["stream_k"] = 0  # every tile cut needs a counter per tile: keep it small
+        p = plan(M, N, K, dt, sm, **cfg)
+        rows = 256 if p["pair"] else 128
+        assert p["bn"] in (128, 160, 192, 224, 256)
+        if dt == "s8_s32":
+            assert p["bn"] in (128, 160)
+        assert p["tiles"] == -(-M // rows) * -(-N // p["bn"])
+        kt = -(-K // 64)
+        t, g, mc = p["stream_k_tiles"], p["stream_k_workers"], p["max_contrib"]
+        assert 0 <= t <= p["tiles"] and g <= max(p["workers"], 1)
+        if cfg.get("stream_k") == 1:
+            assert t == 0
+        if t == 0:
+            continue
+        U = t * kt
+        if g >= 2:
+            assert U // g >= 8, "every stream-K worker gets at least 8 K-tiles"
+        # contributors per cut tile never exceed the partial slots
+        if U <= 20000:
+            for sk in range(t):
+                first, last = _owner(sk * kt, g, U), _owner((sk + 1) * kt - 1, g, U)
+                assert last - first + 1 <= mc
