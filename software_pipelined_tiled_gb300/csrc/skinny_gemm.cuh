@@ -37,7 +37,7 @@ struct SkinnyParams {
   void* C;                    // row-major M x N output
   int64_t ldc;                // elements between rows of C
   float* partials;            // [n_tile][max_contrib][MN][128] fp32, or null if unsplit
-  unsigned long long* counters;  // [n_tile] (generation << 32 | arrivals)
+  unsigned long long* counters;  // [n_tile] (generation << 32 | arrivals); 0 after the call
   unsigned int generation;    // this call's tag for the counters, never 0
   unsigned int* error_word;
   uint64_t timeout_ns;

@@ -84,8 +84,11 @@ struct SquareParams {
   int sk_tiles;
   int sk_workers;
   int max_contrib;              // partial slots per (tile, CTA of the pair)
-  uint32_t* partials;           // [sk_tile][rank][contributor][128 x BN] 32-bit
-  unsigned long long* counters;  // [sk_tile * 2 + rank] (generation << 32 | arrivals)
+  // [sk_tile][rank][contributor][128 x BN] 32-bit, each 128 x BN block as
+  // 16-byte groups in the order [32-column block][4-column group][row]
+  uint32_t* partials;
+  // [sk_tile * 2 + rank]: generation << 32 | departures << 16 | arrivals
+  unsigned long long* counters;
   unsigned int generation;
   unsigned int* error_word;
   uint64_t timeout_ns;
