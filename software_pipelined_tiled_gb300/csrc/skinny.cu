@@ -50,15 +50,28 @@ KernelVariant make_skinny_cluster() {
                                 OUT, KSUB>();
 }
 
-// MMA N = 64 at the deepest ring next to the receive buffer, for every float
-// dtype pair. Two 64-wide K-chunks per stage (4 stages of 48 KB): each stage
-// then reads 256 contiguous bytes of every B row instead of 128, which
-// measured 5.6 TB/s against 5.2 TB/s for 8 stages of one chunk on
+// MMA N = 64 (M <= 64) at the deepest ring next to the receive buffer, for
+// every float dtype pair. Two 64-wide K-chunks per stage (4 stages of 48 KB):
+// each stage then reads 256 contiguous bytes of every B row instead of 128,
+// which measured 5.6 TB/s against 5.2 TB/s for 8 stages of one chunk on
 // 64 x 8192 x 8192 (4 chunks leave room for only 2 stages: 5.2 TB/s).
+// MMA N = 128 (64 < M <= 128): two chunks per stage at 3 stages of 64 KB for
+// 16-bit outputs; one chunk at 5 stages of 32 KB for fp32 outputs, whose
+// 64 KB output staging leaves no room for a third 64 KB stage.
 constexpr int kSkinnyClusterKsub = 2;
-bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v) {
+bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, int M, KernelVariant* v) {
   constexpr int K = kSkinnyClusterKsub;
   KernelVariant c;
+  if (M > 64) {
+    if (M > 128 || stages != 0) return false;
+    if (out_kind == OUT_BF16 && in_bf16) c = make_skinny_cluster<128, true, OUT_BF16, K>();
+    else if (out_kind == OUT_F16 && !in_bf16) c = make_skinny_cluster<128, false, OUT_F16, K>();
+    else if (out_kind == OUT_F32 && in_bf16) c = make_skinny_cluster<128, true, OUT_F32, 1>();
+    else if (out_kind == OUT_F32 && !in_bf16) c = make_skinny_cluster<128, false, OUT_F32, 1>();
+    else return false;
+    *v = c;
+    return true;
+  }
   if (out_kind == OUT_BF16 && in_bf16) c = make_skinny_cluster<64, true, OUT_BF16, K>();
   else if (out_kind == OUT_F16 && !in_bf16) c = make_skinny_cluster<64, false, OUT_F16, K>();
   else if (out_kind == OUT_F32 && in_bf16) c = make_skinny_cluster<64, true, OUT_F32, K>();

@@ -49,7 +49,12 @@ struct SkinnyClusterLayout {
   // 3 x 32 columns, cluster of 4), plus 16 bytes per row so that 16-byte
   // accesses of 8 consecutive rows hit 8 distinct bank groups
   static constexpr int PART_ROW = MN * 4 + 16;
-  static constexpr int RECV_ROWS = 96;  // max over cluster sizes 2 (1 x 64) and 4 (3 x 32)
+  // Largest cluster the receive buffer is sized for: 4 (3 x 32 columns from
+  // the other ranks) for MN = 64; 2 (64 columns from the peer) for wider MN,
+  // whose partial rows are twice as long.
+  static constexpr int MAX_CS = MN <= 64 ? 4 : 2;
+  // rows received at most: 1 x 64 (cluster of 2) or 3 x 32 (cluster of 4)
+  static constexpr int RECV_ROWS = MAX_CS == 4 ? 96 : 64;
   // output staging (reuses the receive buffer once it has been read): MN rows
   // of up to 128 outputs, the layout of C
   static constexpr int OUT_BYTES = MN * BNT * OBYTES;
@@ -119,6 +124,12 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t cs = cluster_nctarank();  // 1, 2 or 4
+  if (cs > static_cast<uint32_t>(L::MAX_CS)) {
+    // the receive buffer has no room for this many ranks: report, touch
+    // nothing (every CTA of the cluster leaves here, before any barrier)
+    if (threadIdx.x == 0) atomicOr(p.error_word, WAIT_PLAN);
+    return;
+  }
   const uint32_t rank = cluster_ctarank();
   const int nt = static_cast<int>(blockIdx.x / cs);
   const int KT = p.num_k_tiles;
@@ -309,17 +320,23 @@ __global__ void __launch_bounds__(192, 1)
         ok = named_barrier_and(1, keep_threads,
                                ok && wait_bounded(recv_bar, 0, ctl, WAIT_EPI_TMEM_FULL));
         if (ok && cs == 2) {
-          // two partials: their fp32 sum is the same in either order
+          // two partials: their fp32 sum is the same in either order; up to
+          // 16 loads in flight, then the adds
           const uint8_t* row = part + col * L::PART_ROW;
-          float4 v[MN / 4];
+          constexpr int G2 = MN / 4 < 16 ? MN / 4 : 16;
 #pragma unroll
-          for (int i = 0; i < MN / 4; ++i) v[i] = *reinterpret_cast<const float4*>(row + 16 * i);
+          for (int i0 = 0; i0 < MN / 4; i0 += G2) {
+            float4 v[G2];
 #pragma unroll
-          for (int i = 0; i < MN / 4; ++i) {
-            acc[4 * i] += v[i].x;
-            acc[4 * i + 1] += v[i].y;
-            acc[4 * i + 2] += v[i].z;
-            acc[4 * i + 3] += v[i].w;
+            for (int i = 0; i < G2; ++i)
+              v[i] = *reinterpret_cast<const float4*>(row + 16 * (i0 + i));
+#pragma unroll
+            for (int i = 0; i < G2; ++i) {
+              acc[4 * (i0 + i)] += v[i].x;
+              acc[4 * (i0 + i) + 1] += v[i].y;
+              acc[4 * (i0 + i) + 2] += v[i].z;
+              acc[4 * (i0 + i) + 3] += v[i].w;
+            }
           }
         } else if (ok) {
           // four partials added in rank order (= increasing k): a fixed

@@ -808,7 +808,9 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
                        void* C, int64_t ldc, cudaStream_t stream, const sptg_config& cfg,
                        bool forced) {
   KernelVariant v;
-  if (d.is_int8 || !skinny_cluster_variant(d.in_bf16, d.out_kind, cfg.stages, &v) || M > v.bn) {
+  if (d.is_int8 || !skinny_cluster_variant(d.in_bf16, d.out_kind, cfg.stages, static_cast<int>(M),
+                                           &v) ||
+      M > v.bn) {
     if (forced) t_last_error = "no cluster-split skinny variant for the requested dtype/stages/M";
     return SPTG_ERR_CONFIG;
   }
@@ -819,15 +821,20 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   // cluster size: forced (splits), else the largest of 4, 2, 1 whose CTAs
   // (cluster size per column tile) fit the SMs; taken only if the grid fills
   // at least three quarters of the SMs
+  // the receive buffer holds up to 3 x 32 columns (clusters of 4) for MMA
+  // N = 64 and 64 columns (clusters of 2) for MMA N = 128
+  const int max_cs = v.bn <= 64 ? 4 : 2;
   int cs = 0;
   if (forced && cfg.splits > 0) {
     cs = cfg.splits;
-    if (cs != 1 && cs != 2 && cs != 4) {
-      t_last_error = "cluster size must be 1, 2 or 4";
+    if ((cs != 1 && cs != 2 && cs != 4) || cs > max_cs) {
+      t_last_error = max_cs == 4 ? "cluster size must be 1, 2 or 4"
+                                 : "cluster size must be 1 or 2 for more than 64 rows";
       return SPTG_ERR_CONFIG;
     }
   } else {
     for (int c : {4, 2, 1}) {
+      if (c > max_cs) continue;
       if (static_cast<int64_t>(n_tiles) * c <= di.sm_count && k_tiles >= 2 * c) {
         cs = c;
         break;
@@ -1072,11 +1079,12 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, int dtype, const void* A,
   // Shape class: few output rows and a float type -> the memory-bound
   // swap-AB kernel; everything else -> the square tile kernel.
   int kernel = cfg.kernel;
-  if (kernel == 0 && !d.is_int8 && M <= 64 && N >= 1024) {
+  if (kernel == 0 && !d.is_int8 && M <= 128 && N >= 1024) {
     // memory-bound: the cluster split when it fills the GPU, else stream-K
+    // (up to 64 rows) or the square kernel
     rc = run_skinny_cluster(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
     if (rc != SPTG_ERR_CONFIG) return rc;
-    kernel = 2;
+    kernel = M <= 64 ? 2 : 1;
   }
   if (kernel == 0) kernel = 1;
   if (kernel == 3)

@@ -31,7 +31,8 @@ bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v);
 // Skinny kernel (in_bf16 selects bfloat16 inputs, else binary16).
 bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
 // Skinny kernel with K split inside a cluster (launched in clusters of 2-8).
-bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
+// M picks the MMA N: 64 for M <= 64, 128 for M <= 128.
+bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, int M, KernelVariant* v);
 // The streaming ring out = alpha * in (bn = tile bytes).
 KernelVariant stream_variant();
 // int8 -> binary16 widening of both operands in one launch: rows_a rows of

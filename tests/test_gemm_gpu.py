@@ -295,6 +295,38 @@ def test_k_tile_marker_skinny_cluster(T, cs):
     assert (C.to(torch.float64) == expect).all()
 
 
+@pytest.mark.parametrize("M,N,K,it,ot", [
+    (128, 8192, 4096, "bf16", BF16), (96, 8192, 2048, "f16", F16), (65, 9216, 1040, "bf16", F32),
+    (128, 8192, 2048, "f16", F32), (100, 16384, 1024, "bf16", BF16)])
+def test_skinny_cluster_up_to_128_rows(M, N, K, it, ot):
+    # 64 < M <= 128: the swap-AB kernel with MMA N = 128, chosen by default
+    A, B = make_inputs(M, N, K, it, "normal", M + N + K)
+    C = run(A, B, ot)
+    cfg = sptg.last_config()
+    assert "kernel=skinny-cluster" in cfg and "mma_n=128" in cfg, cfg
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("T", [1, 3, 8])
+@pytest.mark.parametrize("cs", [1, 2])
+def test_k_tile_marker_skinny_cluster_128_rows(T, cs):
+    A, B, expect = _marker_inputs(128, 1024, T * cs, dtype=BF16)
+    C = run(A, B, BF16, kernel="skinny_cluster", splits=cs)
+    assert "mma_n=128" in sptg.last_config()
+    assert (C.to(torch.float64) == expect).all()
+
+
+def test_skinny_cluster_128_rows_limits():
+    A, B = make_inputs(96, 2048, 1024, "bf16", "normal", 85)
+    with pytest.raises(sptg.SptgError):
+        run(A, B, BF16, kernel="skinny_cluster", splits=4)  # no room for 4 ranks
+    # too few column tiles for the cluster split: the square kernel takes it
+    A, B = make_inputs(100, 1024, 2048, "bf16", "normal", 86)
+    C = run(A, B, BF16)
+    assert "kernel=square" in sptg.last_config()
+    assert_float_parity(C, A, B)
+
+
 def test_skinny_cluster_matches_stream_k_and_is_deterministic():
     A, B = make_inputs(64, 8192, 8192, "bf16", "normal", 19)
     c1 = run(A, B, F32, kernel="skinny_cluster", splits=2)
