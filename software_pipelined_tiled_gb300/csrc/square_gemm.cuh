@@ -394,6 +394,9 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && rank == 0) {
+      const bool tracing = p.trace != nullptr;
+      const uint64_t a_desc0 = sdesc_k_major_sw128(sA);
+      const uint64_t b_desc0 = sdesc_k_major_sw128(sB);
       bool ok = true;
       uint32_t it = 0, unit = 0;
       Segment seg;
@@ -408,25 +411,35 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * BN;
           const int c1 = min(seg.kt1, c0 + kpc);
+          // The issue loop is the MMA warp's whole per-K-tile cost (clock
+          // marks: ~620 cycles with a descriptor built per MMA, above the
+          // ~590 cycles a 256 x 256 x 64 pair step takes on the tensor
+          // pipe), so it is kept lean: stage and phase counted, not divided;
+          // descriptors advanced by adds (the 14-bit start-address field
+          // cannot carry: shared addresses are below 256 KB).
+          int s = static_cast<int>(it % STAGES);
+          uint32_t phase = (it / STAGES) & 1u;
           for (int kt = c0; kt < c1; ++kt, ++it) {
-            const int s = it % STAGES;
-            const uint32_t round = it / STAGES;
-            if (!wait_bounded(full_bar(s), round & 1u, ctl, WAIT_MMA_FULL)) {
+            if (!wait_bounded(full_bar(s), phase, ctl, WAIT_MMA_FULL)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            if (it == 0) trace_mark(p.trace, TR_FIRST_DATA);
-            trace_ktile(p.trace, 1, it);
-            const uint32_t a_addr = sA + s * L::A_STAGE;
-            const uint32_t b_addr = sB + s * L::B_STAGE;
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              mma_f16_g<PAIR>(d_tmem, sdesc_k_major_sw128(a_addr + 32 * k),
-                              sdesc_k_major_sw128(b_addr + 32 * k), IDESC,
-                              (kt > c0 || k > 0) ? 1u : 0u);
+            if (tracing) {
+              if (it == 0) trace_mark(p.trace, TR_FIRST_DATA);
+              trace_ktile(p.trace, 1, it);
             }
+            const uint64_t adesc = a_desc0 + static_cast<uint64_t>((s * L::A_STAGE) >> 4);
+            const uint64_t bdesc = b_desc0 + static_cast<uint64_t>((s * L::B_STAGE) >> 4);
+            mma_f16_g<PAIR>(d_tmem, adesc, bdesc, IDESC, kt > c0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 1; k < BK / 16; ++k)  // +32 bytes (2 in descriptor units) per K = 16
+              mma_f16_g<PAIR>(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, 1u);
             mma_commit_g<PAIR>(empty_bar(s));  // stage s may be refilled (in both CTAs)
+            if (++s == STAGES) {
+              s = 0;
+              phase ^= 1u;
+            }
           }
           if (ok) mma_commit_g<PAIR>(tfull_bar(b));  // accumulator b holds the finished chunk
         }
