@@ -198,6 +198,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// True in exactly one lane of a fully converged warp (the same lane in every
+// call). The warp runs a role's loop together and the elected lane issues the
+// single-thread instructions (tensor copies, MMAs, commits).
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ------------------------------------------------------- tcgen05 / TMEM
 // The *_g<PAIR> forms take the CTA group: PAIR = false is cta_group::1 (one
 // SM), PAIR = true is cta_group::2 (an MMA spanning the two SMs of a CTA

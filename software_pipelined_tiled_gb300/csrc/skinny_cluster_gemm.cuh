@@ -188,9 +188,13 @@ __global__ void __launch_bounds__(192, 1)
 
   const WaitCtl ctl{p.timeout_ns, p.error_word, abort_flag};
 
+  // Producer and MMA issuer run as whole warps; one elected lane issues the
+  // copies, MMAs and commits (a lane alone in its warp pays a large fixed
+  // cost per loop trip).
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    {
+      const bool leader = elect_one_sync();
       int issued_round[STAGES];
       for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
       bool ok = true;
@@ -199,11 +203,14 @@ __global__ void __launch_bounds__(192, 1)
         const int s = it % STAGES;
         const uint32_t round = it / STAGES;
         // in the first round every stage is free: no wait
-        if (round > 0 && !wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl, WAIT_PRODUCER_EMPTY)) {
+        if (round > 0 && !__all_sync(0xffffffffu, wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl,
+                                                                WAIT_PRODUCER_EMPTY))) {
           ok = false;
           break;
         }
         if (p.inject_stall && it == 1) continue;  // test hook: this stage never fills
+        issued_round[s] = static_cast<int>(round);
+        if (!leader) continue;
         mbar_arrive_expect_tx(full_bar(s), L::STAGE);
         if (p.load3d) {
           // one copy per operand: KSUB chunks of 64 K-elements, each landing
@@ -219,14 +226,13 @@ __global__ void __launch_bounds__(192, 1)
                         pol_keep);
           }
         }
-        issued_round[s] = static_cast<int>(round);
         if (it == 0) trace_mark(p.trace, TR_FIRST_LOAD);
         trace_ktile(p.trace, 0, it);
       }
-      trace_mark(p.trace, TR_LAST_LOAD);
+      if (leader) trace_mark(p.trace, TR_LAST_LOAD);
       grid_launch_dependents();
       if (!ok) {
-        *failed = 1;
+        if (leader) *failed = 1;
         for (int s = 0; s < STAGES; ++s) {
           if (issued_round[s] < 0) continue;
           const uint32_t par = static_cast<uint32_t>(issued_round[s]) & 1u;
@@ -238,32 +244,39 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
+      const bool leader = elect_one_sync();
       uint32_t it = 0;
       for (int kt = kt0; kt < kt1; ++kt, ++it) {
         const int s = it % STAGES;
         const uint32_t round = it / STAGES;
-        if (!wait_bounded(full_bar(s), round & 1u, ctl, WAIT_MMA_FULL)) {
-          *failed = 1;
+        if (!__all_sync(0xffffffffu, wait_bounded(full_bar(s), round & 1u, ctl, WAIT_MMA_FULL))) {
+          if (leader) *failed = 1;
           break;
         }
         tc_fence_after();
-        if (it == 0) trace_mark(p.trace, TR_FIRST_DATA);
-        trace_ktile(p.trace, 1, it);
+        if (leader) {
+          if (it == 0) trace_mark(p.trace, TR_FIRST_DATA);
+          trace_ktile(p.trace, 1, it);
 #pragma unroll
-        for (int j = 0; j < KSUB; ++j) {
+          for (int j = 0; j < KSUB; ++j) {
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            mma_f16(tmem_base, sdesc_k_major_sw128(stage_bt(s) + j * L::SUB_BT + 32 * k),
-                    sdesc_k_major_sw128(stage_a(s) + j * L::SUB_A + 32 * k), IDESC,
-                    (kt > kt0 || j > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k) {
+              mma_f16(tmem_base, sdesc_k_major_sw128(stage_bt(s) + j * L::SUB_BT + 32 * k),
+                      sdesc_k_major_sw128(stage_a(s) + j * L::SUB_A + 32 * k), IDESC,
+                      (kt > kt0 || j > 0 || k > 0) ? 1u : 0u);
+            }
           }
+          mma_commit(empty_bar(s));
         }
-        mma_commit(empty_bar(s));
+        __syncwarp();
       }
-      trace_mark(p.trace, TR_LAST_MMA);
-      mma_commit(tfull_bar);  // also arrives when no MMA was issued (empty K-range)
-      mma_commit(drain_bar);
+      if (leader) {
+        trace_mark(p.trace, TR_LAST_MMA);
+        mma_commit(tfull_bar);  // also arrives when no MMA was issued (empty K-range)
+        mma_commit(drain_bar);
+      }
+      __syncwarp();
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < ctl.timeout_ns) {
       }

@@ -150,9 +150,13 @@ __global__ void __launch_bounds__(192, 1)
   const int64_t u_begin = static_cast<int64_t>(blockIdx.x) * T / G;
   const int64_t u_end = static_cast<int64_t>(blockIdx.x + 1) * T / G;
 
+  // Producer and MMA issuer run as whole warps; one elected lane issues the
+  // copies, MMAs and commits (a lane alone in its warp pays a large fixed
+  // cost per loop trip).
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    {
+      const bool leader = elect_one_sync();
       const uint64_t pol_stream = policy_evict_first();  // B is read once
       const uint64_t pol_keep = policy_evict_last();     // A is read by every CTA
       int issued_round[STAGES];
@@ -164,11 +168,14 @@ __global__ void __launch_bounds__(192, 1)
         const int kt = static_cast<int>(u - static_cast<int64_t>(nt) * KT);
         const int s = it % STAGES;
         const uint32_t round = it / STAGES;
-        if (!wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl, WAIT_PRODUCER_EMPTY)) {
+        if (!__all_sync(0xffffffffu,
+                        wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl, WAIT_PRODUCER_EMPTY))) {
           ok = false;
           break;
         }
         if (p.inject_stall && it == 1) continue;  // test hook: this stage never fills
+        issued_round[s] = static_cast<int>(round);
+        if (!leader) continue;
         mbar_arrive_expect_tx(full_bar(s), L::STAGE);
 #pragma unroll
         for (int j = 0; j < KSUB; ++j) {
@@ -177,11 +184,10 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d(stage_a(s) + j * L::SUB_A, &tmA, full_bar(s), (kt * KSUB + j) * BK, 0,
                       pol_keep);
         }
-        issued_round[s] = static_cast<int>(round);
         if (it == 0) trace_mark(p.trace, TR_FIRST_LOAD);
-          trace_ktile(p.trace, 0, it);
+        trace_ktile(p.trace, 0, it);
       }
-      trace_mark(p.trace, TR_LAST_LOAD);
+      if (leader) trace_mark(p.trace, TR_LAST_LOAD);
       grid_launch_dependents();  // the next kernel may start its set-up
       if (!ok) {
         for (int s = 0; s < STAGES; ++s) {
@@ -195,7 +201,8 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
+      const bool leader = elect_one_sync();
       bool ok = true;
       uint32_t it = 0, seg = 0;
       int64_t u = u_begin;
@@ -204,7 +211,8 @@ __global__ void __launch_bounds__(192, 1)
         const int64_t seg_end = min(u_end, static_cast<int64_t>(nt + 1) * KT);
         const uint32_t b = seg & 1u;
         const uint32_t use = seg >> 1;
-        if (!wait_bounded(tempty_bar(b), (use & 1u) ^ 1u, ctl, WAIT_MMA_TMEM_EMPTY)) {
+        if (!__all_sync(0xffffffffu,
+                        wait_bounded(tempty_bar(b), (use & 1u) ^ 1u, ctl, WAIT_MMA_TMEM_EMPTY))) {
           ok = false;
           break;
         }
@@ -213,30 +221,37 @@ __global__ void __launch_bounds__(192, 1)
         for (int64_t v = u; v < seg_end; ++v, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
-          if (!wait_bounded(full_bar(s), round & 1u, ctl, WAIT_MMA_FULL)) {
+          if (!__all_sync(0xffffffffu, wait_bounded(full_bar(s), round & 1u, ctl, WAIT_MMA_FULL))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (it == 0) trace_mark(p.trace, TR_FIRST_DATA);
+          if (leader) {
+            if (it == 0) trace_mark(p.trace, TR_FIRST_DATA);
             trace_ktile(p.trace, 1, it);
 #pragma unroll
-          for (int j = 0; j < KSUB; ++j) {
+            for (int j = 0; j < KSUB; ++j) {
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              mma_f16(d_tmem, sdesc_k_major_sw128(stage_bt(s) + j * L::SUB_BT + 32 * k),
-                      sdesc_k_major_sw128(stage_a(s) + j * L::SUB_A + 32 * k), IDESC,
-                      (v > u || j > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < BK / 16; ++k) {
+                mma_f16(d_tmem, sdesc_k_major_sw128(stage_bt(s) + j * L::SUB_BT + 32 * k),
+                        sdesc_k_major_sw128(stage_a(s) + j * L::SUB_A + 32 * k), IDESC,
+                        (v > u || j > 0 || k > 0) ? 1u : 0u);
+              }
             }
+            mma_commit(empty_bar(s));
           }
-          mma_commit(empty_bar(s));
+          __syncwarp();
         }
-        if (ok) mma_commit(tfull_bar(b));
+        if (ok && leader) mma_commit(tfull_bar(b));
+        __syncwarp();
         u = seg_end;
         ++seg;
       }
-      trace_mark(p.trace, TR_LAST_MMA);
-      mma_commit(drain_bar);
+      if (leader) {
+        trace_mark(p.trace, TR_LAST_MMA);
+        mma_commit(drain_bar);
+      }
+      __syncwarp();
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < ctl.timeout_ns) {
       }

@@ -297,19 +297,19 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   // the persistent work unit is a CTA, or a CTA pair in PAIR mode
   const int worker = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  // The producer (thread 0) works out its first segment and warms L2 with
-  // its first stages while the previous kernel drains (safe: L2 is where
-  // writes become coherent; the loads proper wait for the dependency).
+  // The producer warp works out its first segment and warms L2 with its
+  // first stages while the previous kernel drains (safe: L2 is where writes
+  // become coherent; the loads proper wait for the dependency).
   Segment seg0;
   bool have_seg0 = false;
   int mt0 = 0, nt0 = 0;
   uint64_t pol_operands = 0;
-  if (threadIdx.x == 0) {
+  if (warp == 0) {
     pol_operands = policy_evict_last();  // operands are re-read by other tiles
     have_seg0 = square_segment(p, worker, workers, 0, seg0);
     if (have_seg0) {
       tile_coords(seg0.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt0, nt0);
-      for (int kt = seg0.kt0; kt < min(seg0.kt1, seg0.kt0 + STAGES); ++kt) {
+      for (int kt = seg0.kt0; lane == 0 && kt < min(seg0.kt1, seg0.kt0 + STAGES); ++kt) {
         tma_prefetch_l2_2d(&tmA, kt * BK, mt0 * L::TILE_M + static_cast<int>(rank) * BM);
         tma_prefetch_l2_2d(&tmB, kt * BK, nt0 * BN + static_cast<int>(rank) * L::BN_CTA);
       }
@@ -322,9 +322,15 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
 
   const WaitCtl ctl{p.timeout_ns, p.error_word, abort_flag};
 
+  // The producer and the MMA issuer run their loops as whole warps, with one
+  // elected lane issuing the copies, MMAs and commits: a lane running alone
+  // in its warp pays a large fixed cost per loop trip (measured: ~470 cycles
+  // per K-tile at the MMA issuer whatever the tile width, against 128 per
+  // 256-wide MMA on the tensor pipe), which the converged warp does not.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    {
+      const bool leader = elect_one_sync();
       const uint64_t pol = pol_operands;
       int issued_round[STAGES];
       for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
@@ -347,12 +353,16 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
         for (int kt = seg.kt0; kt < seg.kt1; ++kt, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
-          // in the first round every stage is free: no wait
-          if (round > 0 && !wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl, WAIT_PRODUCER_EMPTY)) {
+          // in the first round every stage is free: no wait; the warp
+          // leaves a wait together (every lane polls, all must succeed)
+          if (round > 0 && !__all_sync(0xffffffffu, wait_bounded(empty_bar(s), (round & 1u) ^ 1u,
+                                                                  ctl, WAIT_PRODUCER_EMPTY))) {
             ok = false;
             break;
           }
           if (p.inject_stall && it == 1 && rank == 0) continue;  // test hook: stage never fills
+          issued_round[s] = static_cast<int>(round);
+          if (!leader) continue;
           if constexpr (PAIR) {
             // both CTAs' copies complete on the leader's barrier; the leader
             // announces the bytes of both
@@ -365,12 +375,11 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
             tma_load_2d(sA + s * L::A_STAGE, &tmA, full_bar(s), kt * BK, a_row, pol);
             tma_load_2d(sB + s * L::B_STAGE, &tmB, full_bar(s), kt * BK, b_row, pol);
           }
-          issued_round[s] = static_cast<int>(round);
           if (it == 0) trace_mark(p.trace, TR_FIRST_LOAD);
           trace_ktile(p.trace, 0, it);
         }
       }
-      trace_mark(p.trace, TR_LAST_LOAD);
+      if (leader) trace_mark(p.trace, TR_LAST_LOAD);
       grid_launch_dependents();  // the next kernel may start its set-up
       if (!ok) {
         // Let every copy already issued land before the CTA can exit.
@@ -393,8 +402,9 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && rank == 0) {
-      const bool tracing = p.trace != nullptr;
+    if (rank == 0) {
+      const bool leader = elect_one_sync();
+      const bool tracing = p.trace != nullptr && leader;
       const uint64_t a_desc0 = sdesc_k_major_sw128(sA);
       const uint64_t b_desc0 = sdesc_k_major_sw128(sB);
       bool ok = true;
@@ -404,23 +414,21 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
         for (int c0 = seg.kt0; ok && c0 < seg.kt1; c0 += kpc, ++unit) {
           const uint32_t b = unit & 1u;
           const uint32_t use = unit >> 1;
-          if (!wait_bounded(tempty_bar(b), (use & 1u) ^ 1u, ctl, WAIT_MMA_TMEM_EMPTY)) {
+          if (!__all_sync(0xffffffffu,
+                          wait_bounded(tempty_bar(b), (use & 1u) ^ 1u, ctl, WAIT_MMA_TMEM_EMPTY))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * BN;
           const int c1 = min(seg.kt1, c0 + kpc);
-          // The issue loop is the MMA warp's whole per-K-tile cost (clock
-          // marks: ~620 cycles with a descriptor built per MMA, above the
-          // ~590 cycles a 256 x 256 x 64 pair step takes on the tensor
-          // pipe), so it is kept lean: stage and phase counted, not divided;
-          // descriptors advanced by adds (the 14-bit start-address field
-          // cannot carry: shared addresses are below 256 KB).
+          // Stage and phase are counted, not divided; descriptors advance by
+          // adds (the 14-bit start-address field cannot carry: shared
+          // addresses are below 256 KB).
           int s = static_cast<int>(it % STAGES);
           uint32_t phase = (it / STAGES) & 1u;
           for (int kt = c0; kt < c1; ++kt, ++it) {
-            if (!wait_bounded(full_bar(s), phase, ctl, WAIT_MMA_FULL)) {
+            if (!__all_sync(0xffffffffu, wait_bounded(full_bar(s), phase, ctl, WAIT_MMA_FULL))) {
               ok = false;
               break;
             }
@@ -431,22 +439,29 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
             }
             const uint64_t adesc = a_desc0 + static_cast<uint64_t>((s * L::A_STAGE) >> 4);
             const uint64_t bdesc = b_desc0 + static_cast<uint64_t>((s * L::B_STAGE) >> 4);
-            mma_f16_g<PAIR>(d_tmem, adesc, bdesc, IDESC, kt > c0 ? 1u : 0u);
+            if (leader) {
+              mma_f16_g<PAIR>(d_tmem, adesc, bdesc, IDESC, kt > c0 ? 1u : 0u);
 #pragma unroll
-            for (int k = 1; k < BK / 16; ++k)  // +32 bytes (2 in descriptor units) per K = 16
-              mma_f16_g<PAIR>(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, 1u);
-            mma_commit_g<PAIR>(empty_bar(s));  // stage s may be refilled (in both CTAs)
+              for (int k = 1; k < BK / 16; ++k)  // +32 bytes (2 in descriptor units) per K = 16
+                mma_f16_g<PAIR>(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, 1u);
+              mma_commit_g<PAIR>(empty_bar(s));  // stage s may be refilled (in both CTAs)
+            }
+            __syncwarp();
             if (++s == STAGES) {
               s = 0;
               phase ^= 1u;
             }
           }
-          if (ok) mma_commit_g<PAIR>(tfull_bar(b));  // accumulator b holds the finished chunk
+          if (ok && leader) mma_commit_g<PAIR>(tfull_bar(b));  // accumulator b holds the finished chunk
+          __syncwarp();
         }
       }
-      trace_mark(p.trace, TR_LAST_MMA);
-      // Drain: every MMA issued above has completed before tensor memory is freed.
-      mma_commit_local_g<PAIR>(drain_bar);
+      if (leader) {
+        trace_mark(p.trace, TR_LAST_MMA);
+        // Drain: every MMA issued above has completed before tensor memory is freed.
+        mma_commit_local_g<PAIR>(drain_bar);
+      }
+      __syncwarp();
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < ctl.timeout_ns) {
       }
