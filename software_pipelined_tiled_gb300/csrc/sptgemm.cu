@@ -494,10 +494,10 @@ bool pick_square(const DtypeInfo& d, int bn, int stages, bool pair, KernelVarian
 // Per-FLOP rate of each tile shape measured on GB300 (binary16 8192 x 8192 x
 // 4096, TFLOPS with wave quantisation and padding divided out), for BN =
 // 256, 224, 192, 160, 128: the weights of the shape model below. Narrow
-// tiles lose more than their share: each K-tile of a stage costs about the
-// same whatever its width.
-constexpr double kRatePair[5] = {1790, 1638, 1446, 1241, 988};
-constexpr double kRateSingle[5] = {1606, 1501, 1469, 1213, 1003};
+// tiles lose more than their share: a K-tile's copies and barrier trip cost
+// about the same whatever its width.
+constexpr double kRatePair[5] = {1942, 1911, 1773, 1600, 1331};
+constexpr double kRateSingle[5] = {1654, 1548, 1670, 1567, 1262};
 constexpr int kTileWidths[5] = {256, 224, 192, 160, 128};
 
 // Stream-K part of the schedule for T tiles over W workers, KT K-tiles each:
@@ -536,11 +536,14 @@ void plan_stream_k(int T, int W, int KT, int mode, int* sk_tiles, int* sk_worker
 // is in microseconds: a worker (one SM or one CTA pair) does a K-tile of its
 // tile in t_k = 2 x rows x BN x 64 / (rate / workers), with the measured
 // per-width rate; the data-parallel schedule takes ceil(tiles / workers)
-// rounds of K-tiles, the stream-K one tiles / workers rounds plus a fixed
-// 6 us for the partial writes and reductions (as measured on 4096^3 and
-// 1024^3). The cheapest estimate wins; ties keep the wider tile and the
-// data-parallel schedule.
-constexpr double kStreamKFixedUs = 6.0;
+// rounds of K-tiles, the stream-K one tiles / workers rounds plus the cost
+// of cutting: 8 us for the partial writes and reductions and 0.1 us per
+// K-tile of the tile (fitted to stream-K against data-parallel 256 x 256
+// pair schedules at 4096^3, 8192 x 8192 x 4096, 6144^3, 12288^3 and
+// 8192 x 8192 x 16384: a data-parallel last round that is partly idle runs
+// faster than a full one, and more so the longer the K-loop). The cheapest
+// estimate wins; ties keep the wider tile and the data-parallel schedule.
+double stream_k_fixed_us(int k_tiles) { return 8.0 + 0.1 * k_tiles; }
 
 void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sptg_config& cfg,
                          bool int8, int* bn_out, bool* pair_out, bool* sk_out) {
@@ -572,7 +575,7 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
           int skt, skw, mc;
           plan_stream_k(T, W, KT, 0, &skt, &skw, &mc);
           if (skt == 0) continue;
-          cost = static_cast<double>(T) / W * KT * t_k + kStreamKFixedUs;
+          cost = static_cast<double>(T) / W * KT * t_k + stream_k_fixed_us(KT);
         }
         if (cost < best) {
           best = cost;

@@ -54,7 +54,14 @@ def test_workload_bf16_8192x8192x16384_sampled():
     w = WORKLOADS["bf16_8192x8192x16384_f32out"]
     A, B = workload_inputs(w)
     C = run(A, B, F32)
+    # 32 x 32 tiles of 256 x 256 over 76 pairs: the 36 tiles of the partial
+    # last round are cut along K; the raster (strips of 8 m-tiles) puts them
+    # in rows 6144.. and columns 6912..: sample that corner densely too
+    assert "bn=256" in sptg.last_config() and _sk_tiles() == 1024 % 76, sptg.last_config()
     rows, cols = sample_positions(w.M, w.N, 4000, seed=5)
+    extra = np.arange(6144, 8192, dtype=np.int64)
+    rows = np.concatenate([rows, extra])
+    cols = np.concatenate([cols, 6912 + extra * 37 % 1280])
     assert_float_parity(C, A, B, rows, cols)
     # a whole row and a whole column as well
     r = np.full(w.N, 4097, dtype=np.int64)
@@ -415,19 +422,17 @@ def test_stream_k_is_deterministic_and_matches_data_parallel():
     assert_float_parity(c3, A, B)
 
 
-def test_stream_k_chosen_for_a_partial_last_round():
-    # 4096 x 4096 in 256 x 256 pair tiles: 256 tiles over the pairs leave a
-    # partial last round, which the default schedule cuts along K
+def test_headline_schedule_fills_whole_rounds():
+    # 4096 x 4096 in 256 x 224 pair tiles: 16 x 19 = 304 tiles, four whole
+    # rounds of the pairs; the last tile column holds 64 of its 224 columns
     A, B = make_inputs(4096, 4096, 4096, "f16", "uniform", 44)
     C = run(A, B, F16)
     cfg = sptg.last_config()
-    assert "pair=1" in cfg and "bn=256" in cfg and _sk_tiles() > 0, cfg
+    assert "pair=1" in cfg and "bn=224" in cfg and _sk_tiles() == 0, cfg
     rows, cols = sample_positions(4096, 4096, 20000, seed=44)
-    # the stream-K tiles are the last tile indices, which the raster (strips
-    # of 8 m-tiles) puts in rows 2048.. and columns 3072..: sample them densely
-    extra = np.arange(2048, 4096, dtype=np.int64)
+    extra = np.arange(0, 4096, dtype=np.int64)
     rows = np.concatenate([rows, extra])
-    cols = np.concatenate([cols, 3072 + extra * 37 % 1024])
+    cols = np.concatenate([cols, 18 * 224 + extra % 64])
     assert_float_parity(C, A, B, rows, cols)
 
 

@@ -26,11 +26,19 @@ def plan(M, N, K, dtype="f16_f16", sm=SM, **cfg):
     return sptg.plan_square(M, N, K, dtype, sm, c)
 
 
-def test_headline_cuts_the_partial_last_round():
+def test_headline_fills_whole_rounds():
     p = plan(4096, 4096, 4096)
-    # 256 x 256 pair tiles: 16 x 16 = 256 tiles = 3 rounds of 76 pairs + 28
-    assert (p["bn"], p["pair"], p["tiles"], p["workers"]) == (256, 1, 256, 76)
-    assert p["stream_k_tiles"] == 256 % 76 == 28
+    # 256 x 224 pair tiles: 16 x 19 = 304 tiles = exactly 4 rounds of 76 pairs
+    assert (p["bn"], p["pair"], p["tiles"], p["workers"]) == (224, 1, 304, 76)
+    assert p["tiles"] % p["workers"] == 0
+    assert p["stream_k_tiles"] == 0
+
+
+def test_long_k_cuts_the_partial_last_round():
+    p = plan(8192, 8192, 16384, "bf16_f32")
+    # 256 x 256 pair tiles: 32 x 32 = 1024 tiles = 13 rounds of 76 pairs + 36
+    assert (p["bn"], p["pair"], p["tiles"], p["workers"]) == (256, 1, 1024, 76)
+    assert p["stream_k_tiles"] == 1024 % 76 == 36
     assert p["stream_k_workers"] == 76
 
 
