@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(192, 1)
   // cost per loop trip).
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    {
+    {  // the whole warp
       const bool leader = elect_one_sync();
       int issued_round[STAGES];
       for (int s = 0; s < STAGES; ++s) issued_round[s] = -1;
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    {
+    {  // the whole warp
       const bool leader = elect_one_sync();
       uint32_t it = 0;
       for (int kt = kt0; kt < kt1; ++kt, ++it) {

@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(192, 1)
   // cost per loop trip).
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    {
+    {  // the whole warp
       const bool leader = elect_one_sync();
       const uint64_t pol_stream = policy_evict_first();  // B is read once
       const uint64_t pol_keep = policy_evict_last();     // A is read by every CTA
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    {
+    {  // the whole warp
       const bool leader = elect_one_sync();
       bool ok = true;
       uint32_t it = 0, seg = 0;

@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   // 256-wide MMA on the tensor pipe), which the converged warp does not.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    {
+    {  // the whole warp
       const bool leader = elect_one_sync();
       const uint64_t pol = pol_operands;
       int issued_round[STAGES];
