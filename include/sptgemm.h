@@ -90,7 +90,10 @@ typedef struct {
   int inject_stall; /* test hook: 1 makes the producer withhold one k-tile so
                        the consumer's bounded wait runs out; 0 = off          */
   int cta_pair; /* square: 0 choose, 1 one CTA (128-row tiles), 2 a CTA pair on
-                   two SMs with the 2-SM MMA (256-row tiles)                 */
+                   two SMs with the 2-SM MMA (256-row tiles), 3 two such
+                   pairs per cluster of 4 on vertically adjacent tiles, each
+                   B row copied once and multicast to both pairs (binary16 /
+                   bfloat16 only, BN 256 or 224, data-parallel schedule)    */
   int no_overlap; /* 1: launch without programmatic dependent launch (the
                      kernel then starts only after the previous one ends)    */
   void* trace;  /* optional device buffer of SPTG_TRACE_WORDS uint64 (8-byte

@@ -7,10 +7,13 @@
 
 namespace sptg {
 
-template <int BN, int ST, bool BF, int OUT, bool IE, bool PAIR>
+template <int BN, int ST, bool BF, int OUT, bool IE, bool PAIR, bool MC = false>
 KernelVariant make_square() {
-  return {reinterpret_cast<const void*>(&square_gemm_kernel<BN, ST, BF, OUT, IE, PAIR>), BN, ST,
-          SquareLayout<BN, ST, IE, PAIR, OutTraits<OUT>::bytes>::SMEM_BYTES, PAIR, SQUARE_THREADS};
+  KernelVariant v{reinterpret_cast<const void*>(&square_gemm_kernel<BN, ST, BF, OUT, IE, PAIR, MC>),
+                  BN, ST, SquareLayout<BN, ST, IE, PAIR, OutTraits<OUT>::bytes>::SMEM_BYTES, PAIR,
+                  SQUARE_THREADS};
+  v.mc = MC;
+  return v;
 }
 
 // Tile widths BN in {256, 224, 192, 160, 128}, one CTA or a CTA pair per
@@ -19,8 +22,21 @@ KernelVariant make_square() {
 // and of BN 224 (pair) for the pipelining ablation (1 = load, then compute,
 // no overlap).
 template <bool BF, int OUT>
-bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v) {
+bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v, bool mc = false) {
   constexpr int OB = OutTraits<OUT>::bytes;
+  if (mc) {
+    // two pairs per cluster sharing B: the two widest tiles, deepest ring
+    if (!pair) return false;
+    if (bn == 256 && (stages == 0 || stages == square_max_stages<256, true, OB>())) {
+      *v = make_square<256, square_max_stages<256, true, OB>(), BF, OUT, false, true, true>();
+      return true;
+    }
+    if (bn == 224 && (stages == 0 || stages == square_max_stages<224, true, OB>())) {
+      *v = make_square<224, square_max_stages<224, true, OB>(), BF, OUT, false, true, true>();
+      return true;
+    }
+    return false;
+  }
 #define SPTG_SQ(BNV)                                                                     \
   case BNV:                                                                              \
     if (!pair && (stages == 0 || stages == square_max_stages<BNV, false, OB>())) {       \
