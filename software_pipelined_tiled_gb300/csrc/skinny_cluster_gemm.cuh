@@ -166,11 +166,13 @@ __global__ void __launch_bounds__(192, 1)
   // Warm L2 with this CTA's first stages while the previous kernel drains.
   // L2 is where writes become coherent, so this is safe even if that kernel
   // writes these operands: the loads proper come after the dependency wait.
+  // (every lane of the producer warp holds the policies: the lane elected
+  // to issue the copies need not be lane 0)
   uint64_t pol_stream = 0, pol_keep = 0;
-  if (threadIdx.x == 0) {
+  if (warp == 0) {
     pol_stream = policy_evict_first();  // B is read once
     pol_keep = policy_evict_last();     // A is read by every CTA
-    for (int kt = kt0; kt < min(kt1, kt0 + STAGES); ++kt) {
+    for (int kt = kt0; lane == 0 && kt < min(kt1, kt0 + STAGES); ++kt) {
       if (p.load3d) {
         tma_prefetch_l2_3d(&tmBt, 0, nt * BNT, kt * KSUB);
         tma_prefetch_l2_3d(&tmA, 0, 0, kt * KSUB);
