@@ -556,9 +556,6 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
   for (int pair = 0; pair < 2; ++pair) {
     if ((cfg.cta_pair == 1 && pair) || (cfg.cta_pair >= 2 && !pair)) continue;
     if (pair && M <= 128 && cfg.cta_pair < 2) continue;  // one CTA already covers all rows
-    // exact int8: one-CTA tiles measured faster (the chunk conversions of
-    // the epilogue weigh more against the pair's shorter K-loop)
-    if (pair && int8 && cfg.cta_pair < 2) continue;
     const int64_t rows = pair ? 256 : 128;
     const int W = pair ? sm_count / 2 : sm_count;
     for (int i = 0; i < 5; ++i) {
