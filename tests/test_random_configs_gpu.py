@@ -1,0 +1,74 @@
+"""Seeded random sweep over shapes, dtype pairs and forced configurations.
+
+Every case is small enough for the full oracle, so each element of C is
+checked: int8 bit-exact, float within the element-wise bound. The shapes are
+ragged (no tile multiple) within the library's 16-byte row-pitch rule, and the
+configurations cover the automatic choice, one-CTA and CTA-pair tiles of
+every width, stream-K never / chosen / every tile, two pairs sharing B, and
+both skinny kernels with their cluster sizes.
+"""
+import random
+
+import pytest
+import torch
+
+import software_pipelined_tiled_gb300 as sptg
+from gpu_helpers import assert_float_parity, assert_int_parity, run
+from workloads import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+OUT = {"f16_f16": torch.float16, "f16_f32": torch.float32, "bf16_bf16": torch.bfloat16,
+       "bf16_f32": torch.float32, "s8_s32": torch.int32}
+
+
+def _case(i):
+    rng = random.Random(1000 + i)
+    dt = rng.choice(list(OUT))
+    it = dt.split("_")[0]
+    kind = rng.choice(["auto", "single", "pair", "pair", "share_b", "skinny", "skinny_cluster"])
+    if dt == "s8_s32" and kind in ("share_b", "skinny", "skinny_cluster"):
+        kind = "pair"
+    kmul = 16 if it == "s8" else 8          # 16-byte rows of A and B
+    nmul = 4 if OUT[dt].itemsize == 4 else 8  # 16-byte rows of C
+    if kind.startswith("skinny"):
+        M = rng.randint(1, 64 if kind == "skinny" else 128)
+        N = nmul * rng.randint(1024 // nmul, 2600 // nmul)
+    else:
+        M = rng.randint(1, 700)
+        N = nmul * rng.randint(1, 700 // nmul)
+    K = kmul * rng.randint(1, 700 // kmul)
+    kw = {}
+    if kind in ("single", "pair", "share_b"):
+        kw["kernel"] = "square"
+        kw["cta_pair"] = {"single": 1, "pair": 2, "share_b": 3}[kind]
+        widths = (256, 224) if kind == "share_b" else \
+            ((160, 128) if it == "s8" else (256, 224, 192, 160, 128))
+        kw["bn"] = rng.choice(widths)
+        if kind != "share_b":
+            kw["stream_k"] = rng.choice([0, 1, 2])
+            if kw["stream_k"] == 2:
+                kw["splits"] = rng.randint(2, 40)
+    elif kind == "skinny":
+        kw["kernel"] = "skinny"
+        kw["splits"] = rng.randint(1, 64)
+    elif kind == "skinny_cluster":
+        kw["kernel"] = "skinny_cluster"
+        kw["splits"] = rng.choice([1, 2] if M > 64 else [1, 2, 4])
+    return dt, it, M, N, K, kind, kw
+
+
+@pytest.mark.parametrize("i", range(120))
+def test_random_configuration(i):
+    dt, it, M, N, K, kind, kw = _case(i)
+    A, B = make_inputs(M, N, K, it, "int8" if it == "s8" else "uniform", 2000 + i)
+    C = run(A, B, OUT[dt], **kw)
+    cfg = sptg.last_config()
+    if kind == "share_b":
+        assert "cluster_pairs=2" in cfg, cfg
+    elif "kernel=square" in cfg:
+        assert "cluster_pairs=1" in cfg, cfg
+    if it == "s8":
+        assert_int_parity(C, A, B)
+    else:
+        assert_float_parity(C, A, B)
