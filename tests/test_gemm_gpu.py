@@ -55,8 +55,9 @@ def test_workload_bf16_8192x8192x16384_sampled():
     A, B = workload_inputs(w)
     C = run(A, B, F32)
     # 32 x 32 tiles of 256 x 256 over 76 pairs: the 36 tiles of the partial
-    # last round are cut along K; the raster (strips of 8 m-tiles) puts them
-    # in rows 6144.. and columns 6912..: sample that corner densely too
+    # last round are cut along K; the raster (strips of 12 m-tiles at this K,
+    # the last strip 8) puts them in rows 6144.. and columns 6912..: sample
+    # that corner densely too
     assert "bn=256" in sptg.last_config() and _sk_tiles() == 1024 % 76, sptg.last_config()
     rows, cols = sample_positions(w.M, w.N, 4000, seed=5)
     extra = np.arange(6144, 8192, dtype=np.int64)
