@@ -234,10 +234,15 @@ int sptg_version(void);
  * device is touched), for a GPU of `sm_count` SMs: the tile shape and the
  * schedule sptg_gemm_ex would choose with configuration `cfg` (NULL =
  * defaults), before any fallback for a missing ring depth. On success
- * out[0..6] = tile columns BN, CTA pair (0/1), tiles, workers (CTAs or
- * pairs), tiles cut along K (stream-K), workers sharing them, and the most
- * contributors one cut tile can have. SPTG_ERR_ARG for a non-positive
- * dimension, fewer than 2 SMs, an unknown dtype or an invalid field.
+ * out[0..6] = tile columns BN, tile mode (0 one CTA, 1 CTA pair, 2 two
+ * pairs per cluster sharing B), tiles of the schedule (with mode 2, pairs of
+ * vertically adjacent tiles), workers (CTAs, pairs or clusters), tiles cut
+ * along K (stream-K), workers sharing them, and the most contributors one
+ * cut tile can have. The worker count assumes every SM holds one CTA; the
+ * library itself asks the device how many pairs or clusters fit. SPTG_ERR_ARG
+ * for a non-positive dimension, fewer than 2 SMs, an unknown dtype or an
+ * invalid field; SPTG_ERR_CONFIG when cta_pair = 3 asks for a width or dtype
+ * that has no shared-B form.
  */
 int sptg_plan_square(int64_t M, int64_t N, int64_t K, int dtype, int sm_count,
                      const sptg_config* cfg, int* out);
