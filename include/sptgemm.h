@@ -45,7 +45,9 @@ extern "C" {
 typedef enum {
   SPTG_F16_F32 = 0,   /* binary16 A, B -> fp32 C                 */
   SPTG_F16_F16 = 1,   /* binary16 A, B -> binary16 C (RN-even)   */
-  SPTG_S8_S32 = 2,    /* int8 A, B -> int32 C, bit-exact         */
+  SPTG_S8_S32 = 2,    /* int8 A, B -> int32 C, bit-exact while the
+                         sum fits int32 (any inputs for K < 131072);
+                         beyond, it wraps modulo 2^32               */
   SPTG_BF16_BF16 = 3, /* bfloat16 A, B -> bfloat16 C (RN-even)   */
   SPTG_BF16_F32 = 4   /* bfloat16 A, B -> fp32 C                 */
 } sptg_dtype;

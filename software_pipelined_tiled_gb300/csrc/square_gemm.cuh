@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
               tmem_ld_32x32b_x32(t_sum + 32 * cb, s);
               tmem_wait_ld_regs(s);
 #pragma unroll
-              for (int i2 = 0; i2 < 32; ++i2) v[i2] = static_cast<uint32_t>(static_cast<int32_t>(v[i2]) + static_cast<int32_t>(s[i2]));
+              for (int i2 = 0; i2 < 32; ++i2) v[i2] += s[i2];  // int32 add as unsigned: wraps, never undefined
             }
             if (!last_chunk) {
               tmem_st_32x32b_x32(t_sum + 32 * cb, v);
@@ -776,10 +776,10 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
               if (c0 + cc == 0) {
                 acc[i2] = v4[cc][i2];
               } else if constexpr (INT_EXACT) {
-                acc[i2].x = static_cast<uint32_t>(static_cast<int32_t>(acc[i2].x) + static_cast<int32_t>(v4[cc][i2].x));
-                acc[i2].y = static_cast<uint32_t>(static_cast<int32_t>(acc[i2].y) + static_cast<int32_t>(v4[cc][i2].y));
-                acc[i2].z = static_cast<uint32_t>(static_cast<int32_t>(acc[i2].z) + static_cast<int32_t>(v4[cc][i2].z));
-                acc[i2].w = static_cast<uint32_t>(static_cast<int32_t>(acc[i2].w) + static_cast<int32_t>(v4[cc][i2].w));
+                acc[i2].x += v4[cc][i2].x;  // int32 sums added as unsigned words (two's complement)
+                acc[i2].y += v4[cc][i2].y;
+                acc[i2].z += v4[cc][i2].z;
+                acc[i2].w += v4[cc][i2].w;
               } else {
                 acc[i2].x = __float_as_uint(__uint_as_float(acc[i2].x) + __uint_as_float(v4[cc][i2].x));
                 acc[i2].y = __float_as_uint(__uint_as_float(acc[i2].y) + __uint_as_float(v4[cc][i2].y));
