@@ -250,6 +250,18 @@ def test_int8_exact_every_width(bn, cta_pair):
     assert_int_parity(C, A, B)
 
 
+@pytest.mark.parametrize("K", [131056, 131072, 135168])
+def test_int8_sum_range(K):
+    # |a b| <= 2^14, so any K below 2^17 fits int32; at and beyond it the
+    # all -128 product (16384 K) wraps modulo 2^32, as an int32 accumulator does
+    A = torch.full((128, K), -128, dtype=I8)
+    B = torch.full((128, K), -128, dtype=I8)
+    C = run(A, B, I32)
+    want = 16384 * K
+    want = (want + 2**31) % 2**32 - 2**31
+    assert (C.to(torch.int64) == want).all(), (int(C[0, 0]), want)
+
+
 @pytest.mark.parametrize("K", [1024, 1040, 4096])
 def test_int8_extremes_exact(K):
     # every chunk of 1024 products reaches 2^24 exactly
