@@ -497,9 +497,9 @@ bool pick_square(const DtypeInfo& d, int bn, int stages, bool pair, KernelVarian
 // 256, 224, 192, 160, 128: the weights of the shape model below. Narrow
 // tiles lose more than their share: a K-tile's copies and barrier trip cost
 // about the same whatever its width.
-constexpr double kRatePair[5] = {1942, 1911, 1773, 1600, 1331};
-constexpr double kRateSingle[5] = {1654, 1548, 1670, 1567, 1262};
-constexpr int kTileWidths[5] = {256, 224, 192, 160, 128};
+constexpr double kRatePair[6] = {2133, 1942, 1911, 1773, 1600, 1331};
+constexpr double kRateSingle[6] = {0, 1654, 1548, 1670, 1567, 1262};
+constexpr int kTileWidths[6] = {512, 256, 224, 192, 160, 128};
 
 // Stream-K part of the schedule for T tiles over W workers, KT K-tiles each:
 // the tiles of a partial last round (mode 0, when that round is at most 90 %
@@ -546,6 +546,14 @@ void plan_stream_k(int T, int W, int KT, int mode, int* sk_tiles, int* sk_worker
 // estimate wins; ties keep the wider tile and the data-parallel schedule.
 double stream_k_fixed_us(int k_tiles) { return 8.0 + 0.1 * k_tiles; }
 
+// 256 x 512 pair tiles (two 256-column MMAs per K-step) move a quarter fewer
+// operand bytes per FLOP (the 2133 TFLOPS rate above, fitted to 8192 x 8192
+// x {8192, 16384}) but hold one accumulator, so each round also pays its
+// epilogue and refill. 4.3 us fits those two runs; 6 us also keeps 6144^3
+// on 256-wide tiles, where they measured 1.5 % faster. Measured wins:
+// 16384^3 5 %, 8192 x 8192 x 16384 2-3 %; 8192^3 and 12288^3 even.
+constexpr double kWideEpilogueUs = 6.0;
+
 void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sptg_config& cfg,
                          bool int8, int* bn_out, bool* pair_out, bool* sk_out) {
   double best = 1e300;
@@ -558,9 +566,11 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
     if (pair && M <= 128 && cfg.cta_pair < 2) continue;  // one CTA already covers all rows
     const int64_t rows = pair ? 256 : 128;
     const int W = pair ? sm_count / 2 : sm_count;
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < 6; ++i) {
       const int bn = kTileWidths[i];
       if (cfg.bn && bn != cfg.bn) continue;
+      // 512 columns: CTA pairs and float types only
+      if (bn == 512 && (!pair || int8 || cfg.cta_pair == 3)) continue;
       if (int8 && bn != 128 && bn != 160) continue;  // 3 x BN tensor-memory columns
       if (cfg.cta_pair == 3 && bn != 256 && bn != 224) continue;  // the B-sharing widths
       const int64_t T64 = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
@@ -569,6 +579,11 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
       const double t_k = 2.0 * rows * bn * 64 / (rate / W);            // us per K-tile
       for (int sk = 0; sk < 2; ++sk) {
         double cost = static_cast<double>((T + W - 1) / W) * KT * t_k;
+        if (bn == 512) {
+          // one accumulator: each round's epilogue is exposed; never cut
+          if (sk) continue;
+          cost += static_cast<double>((T + W - 1) / W) * kWideEpilogueUs;
+        }
         if (sk) {
           if (cfg.stream_k == 1 || cfg.cta_pair == 3) continue;  // B sharing: data-parallel
           int skt, skw, mc;
@@ -602,6 +617,10 @@ int plan_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, in
   int bn = 0;
   bool pair = false, sk = false;
   choose_square_shape(M, N, K, di.sm_count, cfg, d.is_int8, &bn, &pair, &sk);
+  if (cfg.bn && bn != cfg.bn) {
+    t_last_error = "the requested tile width does not exist for this dtype/pairing";
+    return SPTG_ERR_CONFIG;
+  }
   const bool mc = cfg.cta_pair == 3;
   if (mc && (!pair || !pick_square(d, bn, cfg.stages, true, &pl->v, true))) {
     t_last_error = "no B-sharing (two pairs per cluster) variant for the requested dtype/bn/stages";
@@ -659,7 +678,7 @@ int launch_square(const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N
   int rc = make_map_2d(&ta, d.in_tma, 2, A16, K, M, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B, lda);
   if (rc) return rc;
   rc = make_map_2d(&tb, d.in_tma, 2, B16, K, N, BK,
-                   pl.mc ? pl.v.bn / 4 : pl.pair ? pl.v.bn / 2 : pl.v.bn,
+                   (pl.mc || pl.v.bn > 256) ? pl.v.bn / 4 : pl.pair ? pl.v.bn / 2 : pl.v.bn,
                    CU_TENSOR_MAP_SWIZZLE_128B, ldb);
   if (rc) return rc;
   // C blocks of 32 columns x 32 rows: 128-byte rows for 4-byte outputs,
@@ -970,8 +989,8 @@ int sptg_plan_square(int64_t M, int64_t N, int64_t K, int dtype, int sm_count,
   int bn = 0;
   bool pair = false, sk = false;
   choose_square_shape(M, N, K, sm_count, cfg, d.is_int8, &bn, &pair, &sk);
-  if (cfg.cta_pair == 3 && (!pair || d.is_int8)) {
-    t_last_error = "no B-sharing (two pairs per cluster) variant for the requested dtype/bn";
+  if ((cfg.bn && bn != cfg.bn) || (cfg.cta_pair == 3 && (!pair || d.is_int8))) {
+    t_last_error = "no square-kernel tile for the requested dtype, width and pairing";
     return SPTG_ERR_CONFIG;
   }
   const bool share_b = cfg.cta_pair == 3;

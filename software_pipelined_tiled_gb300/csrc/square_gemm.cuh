@@ -190,7 +190,10 @@ struct SquareLayout {
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int BYTES_USED = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = BYTES_USED + 1024;  // slack to align the base to 1024
-  static constexpr int TMEM_NEEDED = 2 * BN + (INT_EXACT ? BN : 0);
+  // tiles wider than one MMA (BN = 512: two 256-column MMAs per K-step) keep
+  // a single accumulator: 512 columns fill tensor memory
+  static constexpr int NACC = BN > 256 ? 1 : 2;
+  static constexpr int TMEM_NEEDED = NACC * BN + (INT_EXACT ? BN : 0);
   static constexpr int TMEM_COLS = TMEM_NEEDED <= 32    ? 32
                                    : TMEM_NEEDED <= 64  ? 64
                                    : TMEM_NEEDED <= 128 ? 128
@@ -199,7 +202,8 @@ struct SquareLayout {
   // bytes that complete one stage's "full" barrier (both CTAs' copies in PAIR mode)
   static constexpr uint32_t STAGE_TX = (PAIR ? 2 : 1) * (A_STAGE + B_STAGE);
   static_assert(TMEM_NEEDED <= 512, "accumulators exceed tensor memory");
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
+  static_assert(BN % 32 == 0 && BN >= 32 && (BN <= 256 || (BN == 512 && PAIR && !INT_EXACT)),
+                "BN must be a multiple of 32 in [32, 256], or 512 for float CTA pairs");
   static_assert(!PAIR || BN_CTA % 16 == 0, "each CTA's B rows must be a multiple of 16");
   static_assert(STAGES >= 1, "at least one stage");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
@@ -233,9 +237,14 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   constexpr int OBYTES = OutTraits<OUT>::bytes;
   using L = SquareLayout<BN, STAGES, INT_EXACT, PAIR, OBYTES>;
   constexpr int BM = L::BM, BK = L::BK;
-  constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, L::TILE_M, BN);
+  // one MMA covers at most 256 columns: a 512-wide tile is two halves, each
+  // half's B rows split between the CTAs of the pair like a 256-wide tile's
+  constexpr int NH = BN > 256 ? 2 : 1;
+  constexpr int MMA_N = BN / NH;
+  constexpr int NACC = L::NACC;
+  constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, L::TILE_M, MMA_N);
   static_assert(!INT_EXACT || OUT == OUT_S32, "exact integer mode writes int32");
-  static_assert(!MC || (PAIR && !INT_EXACT), "B sharing pairs two CTA pairs");
+  static_assert(!MC || (PAIR && !INT_EXACT && NH == 1), "B sharing pairs two CTA pairs");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -326,9 +335,10 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       if constexpr (MC) mt0 = 2 * mt0 + static_cast<int>(pidx);
       for (int kt = seg0.kt0; lane == 0 && kt < min(seg0.kt1, seg0.kt0 + STAGES); ++kt) {
         tma_prefetch_l2_2d(&tmA, kt * BK, mt0 * L::TILE_M + static_cast<int>(rank) * BM);
-        tma_prefetch_l2_2d(&tmB, kt * BK,
-                           nt0 * BN + static_cast<int>(rank) * L::BN_CTA +
-                               static_cast<int>(pidx) * B_ROWS);
+        for (int h = 0; h < NH; ++h)
+          tma_prefetch_l2_2d(&tmB, kt * BK,
+                             nt0 * BN + h * MMA_N + static_cast<int>(rank) * (L::BN_CTA / NH) +
+                                 static_cast<int>(pidx) * B_ROWS);
       }
     }
   }
@@ -387,7 +397,14 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
             if (rank == 0) mbar_arrive_expect_tx(full_bar(s), L::STAGE_TX);
             const uint32_t leader_full = map_to_cta(full_bar(s), leader_crank);
             tma_load_2d_pair(sA + s * L::A_STAGE, &tmA, leader_full, kt * BK, a_row, pol);
-            if constexpr (MC) {
+            if constexpr (NH == 2) {
+              // this CTA's rows of each 256-column half, one box per half
+#pragma unroll
+              for (int h = 0; h < NH; ++h)
+                tma_load_2d_pair(sB + s * L::B_STAGE + h * (MMA_N / 2) * (BK * 2), &tmB, leader_full,
+                                 kt * BK, nt * BN + h * MMA_N + static_cast<int>(rank) * (MMA_N / 2),
+                                 pol);
+            } else if constexpr (MC) {
               // to this CTA and its counterpart in the other pair (cluster
               // ranks rank and rank + 2); each copy counts at its own pair
               tma_load_2d_pair_mc(sB + s * L::B_STAGE + pidx * (B_ROWS * BK * 2), &tmB, leader_full,
@@ -437,8 +454,8 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       Segment seg;
       for (int i = 0; ok && square_segment(p, worker, workers, i, seg); ++i) {
         for (int c0 = seg.kt0; ok && c0 < seg.kt1; c0 += kpc, ++unit) {
-          const uint32_t b = unit & 1u;
-          const uint32_t use = unit >> 1;
+          const uint32_t b = NACC == 2 ? (unit & 1u) : 0u;
+          const uint32_t use = NACC == 2 ? (unit >> 1) : unit;
           if (!__all_sync(0xffffffffu,
                           wait_bounded(tempty_bar(b), (use & 1u) ^ 1u, ctl, WAIT_MMA_TMEM_EMPTY))) {
             ok = false;
@@ -465,10 +482,15 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
             const uint64_t adesc = a_desc0 + static_cast<uint64_t>((s * L::A_STAGE) >> 4);
             const uint64_t bdesc = b_desc0 + static_cast<uint64_t>((s * L::B_STAGE) >> 4);
             if (leader) {
-              mma_f16_g<PAIR>(d_tmem, adesc, bdesc, IDESC, kt > c0 ? 1u : 0u);
 #pragma unroll
-              for (int k = 1; k < BK / 16; ++k)  // +32 bytes (2 in descriptor units) per K = 16
-                mma_f16_g<PAIR>(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, 1u);
+              for (int h = 0; h < NH; ++h) {  // each 256-column half of a 512-wide tile
+                const uint64_t bd = bdesc + static_cast<uint64_t>((h * (MMA_N / 2) * (BK * 2)) >> 4);
+                const uint32_t dt = d_tmem + h * MMA_N;
+                mma_f16_g<PAIR>(dt, adesc, bd, IDESC, kt > c0 ? 1u : 0u);
+#pragma unroll
+                for (int k = 1; k < BK / 16; ++k)  // +32 bytes (2 in descriptor units) per K = 16
+                  mma_f16_g<PAIR>(dt, adesc + 2 * k, bd + 2 * k, IDESC, 1u);
+              }
               // stage s may be refilled (in both CTAs; with MC in all four,
               // whose producers also write into this pair's stage)
               if constexpr (MC)
@@ -524,8 +546,8 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
                ((static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib + seg.j) * (32 * BN) +
                32 * q + lane;
       for (int c = 0; c < n_chunks; ++c, ++unit) {
-        const uint32_t b = unit & 1u;
-        const uint32_t use = unit >> 1;
+        const uint32_t b = NACC == 2 ? (unit & 1u) : 0u;
+        const uint32_t use = NACC == 2 ? (unit >> 1) : unit;
         // every lane waits, and the warp leaves together: the tensor-memory
         // loads below are warp-collective
         ok = __all_sync(0xffffffffu, wait_bounded(tfull_bar(b), use & 1u, ctl, WAIT_EPI_TMEM_FULL));

@@ -37,6 +37,12 @@ bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v, bool 
     }
     return false;
   }
+  if (bn == 512) {
+    // 256 x 512 CTA-pair tiles: two 256-column MMAs per K-step, one accumulator
+    if (!pair || (stages != 0 && stages != square_max_stages<512, true, OB>())) return false;
+    *v = make_square<512, square_max_stages<512, true, OB>(), BF, OUT, false, true>();
+    return true;
+  }
 #define SPTG_SQ(BNV)                                                                     \
   case BNV:                                                                              \
     if (!pair && (stages == 0 || stages == square_max_stages<BNV, false, OB>())) {       \

@@ -54,15 +54,13 @@ def test_workload_bf16_8192x8192x16384_sampled():
     w = WORKLOADS["bf16_8192x8192x16384_f32out"]
     A, B = workload_inputs(w)
     C = run(A, B, F32)
-    # 32 x 32 tiles of 256 x 256 over 76 pairs: the 36 tiles of the partial
-    # last round are cut along K; the raster (strips of 12 m-tiles at this K,
-    # the last strip 8) puts them in rows 6144.. and columns 6912..: sample
-    # that corner densely too
-    assert "bn=256" in sptg.last_config() and _sk_tiles() == 1024 % 76, sptg.last_config()
+    # 32 x 16 tiles of 256 x 512 over 76 pairs, data-parallel: sample one
+    # whole tile densely too (both 256-column halves of each CTA's rows)
+    assert "bn=512" in sptg.last_config() and _sk_tiles() == 0, sptg.last_config()
     rows, cols = sample_positions(w.M, w.N, 4000, seed=5)
-    extra = np.arange(6144, 8192, dtype=np.int64)
-    rows = np.concatenate([rows, extra])
-    cols = np.concatenate([cols, 6912 + extra * 37 % 1280])
+    extra = np.arange(2560, 2816, dtype=np.int64)
+    rows = np.concatenate([rows, np.repeat(extra, 16)])
+    cols = np.concatenate([cols, np.tile(np.arange(4096, 4608, 32, dtype=np.int64), 256) + np.repeat(extra, 16) % 32])
     assert_float_parity(C, A, B, rows, cols)
     # a whole row and a whole column as well
     r = np.full(w.N, 4097, dtype=np.int64)
@@ -447,6 +445,33 @@ def test_headline_schedule_fills_whole_rounds():
     rows = np.concatenate([rows, extra])
     cols = np.concatenate([cols, 18 * 224 + extra % 64])
     assert_float_parity(C, A, B, rows, cols)
+
+
+# ------------------------------------------------ 256 x 512 CTA-pair tiles
+@pytest.mark.parametrize("M,N,K,it,ot,stream_k", [
+    (768, 1096, 520, "f16", F16, 1),     # ragged N: the last tile holds 72 of 512 columns
+    (512, 1536, 1024, "bf16", F32, 0),
+    (300, 2048, 2080, "bf16", BF16, 2),  # every tile cut along K: 512-wide partials
+    (256, 512, 64, "f16", F32, 1),       # one tile, one K-tile
+])
+def test_wide_pair_tiles_parity(M, N, K, it, ot, stream_k):
+    # two 256-column MMAs per K-step into one 512-column accumulator; each
+    # CTA copies its 128 rows of each half of the tile's B
+    A, B = make_inputs(M, N, K, it, "uniform", 71)
+    kw = {"splits": 5} if stream_k == 2 else {}
+    C = run(A, B, ot, kernel="square", cta_pair=2, bn=512, stream_k=stream_k, **kw)
+    cfg = sptg.last_config()
+    assert "bn=512" in cfg and "pair=1" in cfg, cfg
+    assert_float_parity(C, A, B)
+
+
+def test_wide_tiles_need_a_float_pair():
+    A, B = make_inputs(256, 512, 64, "f16", "uniform", 72)
+    with pytest.raises(sptg.SptgError):
+        run(A, B, F32, kernel="square", cta_pair=1, bn=512)
+    A, B = make_inputs(256, 512, 64, "s8", "int8", 72)
+    with pytest.raises(sptg.SptgError):
+        run(A, B, I32, kernel="square", cta_pair=2, bn=512)
 
 
 # -------------------------------------------- two pairs per cluster sharing B

@@ -36,8 +36,19 @@ def test_headline_fills_whole_rounds():
     assert p["stream_k_tiles"] == 0
 
 
-def test_long_k_cuts_the_partial_last_round():
+def test_long_k_takes_wide_pair_tiles():
+    # 256 x 512 pair tiles (one accumulator, a quarter fewer copied bytes per
+    # FLOP): 32 x 16 = 512 tiles = 6.7 rounds of 76 pairs, never cut along K
     p = plan(8192, 8192, 16384, "bf16_f32")
+    assert (p["bn"], p["pair"], p["tiles"], p["workers"]) == (512, 1, 512, 76)
+    assert p["stream_k_tiles"] == 0
+    # short K-loops keep the double-buffered accumulators
+    assert plan(8192, 8192, 4096)["bn"] == 256
+    assert plan(16384, 16384, 4096, "bf16_bf16")["bn"] == 256
+
+
+def test_long_k_at_256_columns_cuts_the_partial_last_round():
+    p = plan(8192, 8192, 16384, "bf16_f32", bn=256)
     # 256 x 256 pair tiles: 32 x 32 = 1024 tiles = 13 rounds of 76 pairs + 36
     assert (p["bn"], p["pair"], p["tiles"], p["workers"]) == (256, 1, 1024, 76)
     assert p["stream_k_tiles"] == 1024 % 76 == 36
@@ -73,6 +84,11 @@ def test_forced_fields_are_honoured():
         for pair in (1, 2):
             p = plan(3000, 5000, 700, bn=bn, cta_pair=pair)
             assert p["bn"] == bn and p["pair"] == pair - 1
+    assert plan(3000, 5000, 700, bn=512, cta_pair=2)["bn"] == 512
+    for args, cfg in [((3000, 5000, 700), {"bn": 512, "cta_pair": 1}),
+                      ((3000, 5000, 704, "s8_s32"), {"bn": 512})]:
+        with pytest.raises(sptg.SptgError):
+            plan(*args, **cfg)
     assert plan(4096, 4096, 4096, splits=10)["workers"] <= 10
 
 
@@ -112,7 +128,9 @@ def test_plan_invariants_over_random_shapes():
             cfg["stream_k"] = 0  # every tile cut needs a counter per tile: keep it small
         p = plan(M, N, K, dt, sm, **cfg)
         rows = 256 if p["pair"] else 128
-        assert p["bn"] in (128, 160, 192, 224, 256)
+        assert p["bn"] in (128, 160, 192, 224, 256, 512)
+        if p["bn"] == 512:
+            assert p["pair"] == 1 and dt != "s8_s32" and p["stream_k_tiles"] == 0
         if dt == "s8_s32":
             assert p["bn"] in (128, 160)
         assert p["tiles"] == -(-M // rows) * -(-N // p["bn"])

@@ -43,9 +43,10 @@ def _case(i):
         kw["kernel"] = "square"
         kw["cta_pair"] = {"single": 1, "pair": 2, "share_b": 3}[kind]
         widths = (256, 224) if kind == "share_b" else \
-            ((160, 128) if it == "s8" else (256, 224, 192, 160, 128))
+            ((160, 128) if it == "s8" else (256, 224, 192, 160, 128)
+             + ((512,) if kind == "pair" else ()))
         kw["bn"] = rng.choice(widths)
-        if kind != "share_b":
+        if kind != "share_b" and kw["bn"] != 512:
             kw["stream_k"] = rng.choice([0, 1, 2])
             if kw["stream_k"] == 2:
                 kw["splits"] = rng.randint(2, 40)
