@@ -40,6 +40,15 @@
 // on both CTAs' "empty" and "tmem_full" barriers; both CTAs' epilogue warps
 // release the accumulator on the leader's "tmem_empty" barrier.
 //
+// A pair tile may be 512 wide (BN = 512): each K-step is then two 256-column
+// MMAs into the two halves of one 512-column accumulator (tensor memory holds
+// no second one, so that tile's epilogue does not overlap the next K-loop),
+// and each CTA copies its 128 rows of each half's B. Per FLOP this moves a
+// quarter fewer operand bytes than 256-wide tiles, which pays on long
+// K-loops. MC mode (opt-in) puts two pairs in a cluster of four on
+// vertically adjacent tiles that need the same B rows: each CTA copies half
+// of its B rows and multicasts them to its counterpart in the other pair.
+//
 // Work schedule (stream-K + data-parallel). With T tiles and W workers (CTAs,
 // or CTA pairs), T mod W tiles would leave a last round with most SMs idle.
 // Those tiles are instead cut along K into one contiguous range of
