@@ -549,9 +549,8 @@ def main(argv=None):
     ap.add_argument("--bn", type=int, default=0, help="force the square tile width")
     ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
                     help="0 choose, 1 square, 2 skinny stream-K, 3 skinny cluster split")
-    ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2, 3],
-                    help="square kernel: 0 choose, 1 one CTA per tile, 2 CTA pair (2-SM MMA), "
-                         "3 two pairs per cluster sharing B copies")
+    ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
+                    help="square kernel: 0 choose, 1 one CTA per tile, 2 CTA pair (2-SM MMA)")
     ap.add_argument("--stream-k", type=int, default=0, choices=[0, 1, 2],
                     help="square kernel: 0 stream-K for a partial last round, 1 never, 2 always")
     ap.add_argument("--no-e2e", action="store_true")

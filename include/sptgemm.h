@@ -49,7 +49,12 @@ typedef enum {
                          sum fits int32 (any inputs for K < 131072);
                          beyond, it wraps modulo 2^32               */
   SPTG_BF16_BF16 = 3, /* bfloat16 A, B -> bfloat16 C (RN-even)   */
-  SPTG_BF16_F32 = 4   /* bfloat16 A, B -> fp32 C                 */
+  SPTG_BF16_F32 = 4,  /* bfloat16 A, B -> fp32 C                 */
+  /* range markers, not dtypes: they make sptg_dtype span every 32-bit int,
+     so any value a caller passes is representable and is rejected with
+     SPTG_ERR_ARG unless it names one of the pairs above */
+  SPTG_DTYPE_RANGE_MIN_ = -2147483647 - 1,
+  SPTG_DTYPE_RANGE_MAX_ = 2147483647
 } sptg_dtype;
 
 enum {
@@ -75,7 +80,7 @@ enum {
  * Alignment: A, B, C 16-byte aligned; K * sizeof(input) and
  * N * sizeof(output) multiples of 16 bytes.  Otherwise SPTG_ERR_ALIGN.
  */
-int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype,
+int sptg_gemm(int64_t M, int64_t N, int64_t K, sptg_dtype dtype,
               const void* A, const void* B, void* C, void* stream);
 
 /* Kernel selection for sptg_gemm_ex; fields left at 0 mean "choose". */
@@ -83,7 +88,8 @@ typedef struct {
   int kernel;   /* 0 auto, 1 square, 2 skinny swap-AB with stream-K split,
                    3 skinny swap-AB with the K split across a cluster of
                    CTAs (splits = cluster size, 1, 2 or 4)                   */
-  int bn;       /* square: tile columns (multiple of 16, 16..256)           */
+  int bn;       /* square: tile columns, one of 128, 160, 192, 224, 256, or
+                   512 for float CTA pairs (int8: 128 or 160)               */
   int stages;   /* shared-memory ring depth (1 = synchronous load/compute)  */
   int splits;   /* square: cap on persistent workers; skinny stream-K: CTAs
                    sharing the work (0 = SM count); skinny cluster: cluster
@@ -92,10 +98,8 @@ typedef struct {
   int inject_stall; /* test hook: 1 makes the producer withhold one k-tile so
                        the consumer's bounded wait runs out; 0 = off          */
   int cta_pair; /* square: 0 choose, 1 one CTA (128-row tiles), 2 a CTA pair on
-                   two SMs with the 2-SM MMA (256-row tiles), 3 two such
-                   pairs per cluster of 4 on vertically adjacent tiles, each
-                   B row copied once and multicast to both pairs (binary16 /
-                   bfloat16 only, BN 256 or 224, data-parallel schedule)    */
+                   two SMs with the 2-SM MMA (256-row tiles); every CTA
+                   copies its own operand tiles (no multicast copies)       */
   int no_overlap; /* 1: launch without programmatic dependent launch (the
                      kernel then starts only after the previous one ends)    */
   void* trace;  /* optional device buffer of SPTG_TRACE_WORDS uint64 (8-byte
@@ -115,7 +119,7 @@ typedef struct {
 #define SPTG_TRACE_WORDS (8 * 1024 + 2 * 64)
 
 /* sptg_gemm with an explicit configuration (NULL = sptg_gemm). */
-int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype,
+int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, sptg_dtype dtype,
                  const void* A, const void* B, void* C, void* stream,
                  const sptg_config* cfg);
 
@@ -135,7 +139,7 @@ int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype,
  * 2^31 (SPTG_ERR_ARG). Elements between N and ldc of a row of C are never
  * written. lda = ldb = K and ldc = N give sptg_gemm_ex.
  */
-int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, int dtype,
+int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype,
                       const void* A, int64_t lda, const void* B, int64_t ldb,
                       void* C, int64_t ldc, void* stream, const sptg_config* cfg);
 
@@ -153,7 +157,7 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, int dtype,
  * caller whose data lives in host memory makes, and bench.py's end-to-end
  * measurement goes through it.
  */
-int sptg_gemm_host(int64_t M, int64_t N, int64_t K, int dtype,
+int sptg_gemm_host(int64_t M, int64_t N, int64_t K, sptg_dtype dtype,
                    const void* A, const void* B, void* C, void* stream,
                    const sptg_config* cfg);
 
@@ -225,7 +229,7 @@ int sptg_device_error(void* stream);
  */
 #define SPTG_NOALLOC_PARTIAL_BYTES (8u << 20)
 #define SPTG_NOALLOC_COUNTER_BYTES (64u << 10)
-int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype,
+int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, sptg_dtype dtype,
                              const void* A, const void* B, void* C, void* stream);
 
 /* Library ABI version (major*100 + minor). */
@@ -236,17 +240,15 @@ int sptg_version(void);
  * device is touched), for a GPU of `sm_count` SMs: the tile shape and the
  * schedule sptg_gemm_ex would choose with configuration `cfg` (NULL =
  * defaults), before any fallback for a missing ring depth. On success
- * out[0..6] = tile columns BN, tile mode (0 one CTA, 1 CTA pair, 2 two
- * pairs per cluster sharing B), tiles of the schedule (with mode 2, pairs of
- * vertically adjacent tiles), workers (CTAs, pairs or clusters), tiles cut
- * along K (stream-K), workers sharing them, and the most contributors one
- * cut tile can have. The worker count assumes every SM holds one CTA; the
- * library itself asks the device how many pairs or clusters fit. SPTG_ERR_ARG
- * for a non-positive dimension, fewer than 2 SMs, an unknown dtype or an
- * invalid field; SPTG_ERR_CONFIG when cta_pair = 3 asks for a width or dtype
- * that has no shared-B form.
+ * out[0..6] = tile columns BN, tile mode (0 one CTA, 1 CTA pair), tiles of
+ * the schedule, workers (CTAs or pairs), tiles cut along K (stream-K),
+ * workers sharing them, and the most contributors one cut tile can have. The
+ * worker count assumes every SM holds one CTA; the library itself asks the
+ * device how many pairs fit. SPTG_ERR_ARG for a non-positive dimension, fewer
+ * than 2 SMs, an unknown dtype or an invalid field; SPTG_ERR_CONFIG when a
+ * forced width does not exist for the dtype and pairing.
  */
-int sptg_plan_square(int64_t M, int64_t N, int64_t K, int dtype, int sm_count,
+int sptg_plan_square(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, int sm_count,
                      const sptg_config* cfg, int* out);
 
 #ifdef __cplusplus

@@ -198,22 +198,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// The same load multicast to the CTAs of `cta_mask` (cluster ranks): the
-// tile lands at `dst`'s offset in each of them, and each destination's bytes
-// complete on the barrier at `cluster_bar`'s offset in the leader (even rank)
-// of that destination's pair (`cluster_bar` addresses the issuing pair's
-// leader).
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map,
-                                                    uint32_t cluster_bar, int32_t c0, int32_t c1,
-                                                    uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "h"(cta_mask),
-      "l"(policy)
-      : "memory");
-}
-
 // True in exactly one lane of a fully converged warp (the same lane in every
 // call). The warp runs a role's loop together and the elected lane issues the
 // single-thread instructions (tensor copies, MMAs, commits).
@@ -297,16 +281,6 @@ __device__ __forceinline__ void mma_commit_g(uint32_t bar) {
                      bar)
                  : "memory");
   }
-}
-
-// 2-SM commit whose arrival goes to the barrier at `bar`'s offset in every
-// CTA of `cta_mask` (cluster ranks).
-__device__ __forceinline__ void mma_commit_pair_mask(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
 }
 
 // Arrives on this CTA's `bar` only (used for the final drain).

@@ -427,7 +427,7 @@ cudaError_t launch_variant(const KernelVariant& v, int grid, cudaStream_t stream
   int n = 0;
   if (v.pair || cluster > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = v.mc ? 4 : v.pair ? 2 : cluster;
+    attr[n].val.clusterDim.x = v.pair ? 2 : cluster;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -479,15 +479,14 @@ int pair_slots(int dev, const KernelVariant& v, int sm_count) {
 }
 
 // ------------------------------------------------------------ square path
-bool pick_square(const DtypeInfo& d, int bn, int stages, bool pair, KernelVariant* v,
-                 bool mc = false) {
-  if (d.is_int8) return !mc && square_variant_s8(bn, stages, pair, v);
+bool pick_square(const DtypeInfo& d, int bn, int stages, bool pair, KernelVariant* v) {
+  if (d.is_int8) return square_variant_s8(bn, stages, pair, v);
   switch (d.out_kind) {
-    case OUT_F16: return !d.in_bf16 && square_variant_f16_f16(bn, stages, pair, v, mc);
-    case OUT_BF16: return d.in_bf16 && square_variant_bf16_bf16(bn, stages, pair, v, mc);
+    case OUT_F16: return !d.in_bf16 && square_variant_f16_f16(bn, stages, pair, v);
+    case OUT_BF16: return d.in_bf16 && square_variant_bf16_bf16(bn, stages, pair, v);
     case OUT_F32:
-      return d.in_bf16 ? square_variant_bf16_f32(bn, stages, pair, v, mc)
-                       : square_variant_f16_f32(bn, stages, pair, v, mc);
+      return d.in_bf16 ? square_variant_bf16_f32(bn, stages, pair, v)
+                       : square_variant_f16_f32(bn, stages, pair, v);
     default: return false;
   }
 }
@@ -562,17 +561,16 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
   *sk_out = false;
   const int KT = static_cast<int>((K + 63) / 64);
   for (int pair = 0; pair < 2; ++pair) {
-    if ((cfg.cta_pair == 1 && pair) || (cfg.cta_pair >= 2 && !pair)) continue;
-    if (pair && M <= 128 && cfg.cta_pair < 2) continue;  // one CTA already covers all rows
+    if ((cfg.cta_pair == 1 && pair) || (cfg.cta_pair == 2 && !pair)) continue;
+    if (pair && M <= 128 && cfg.cta_pair != 2) continue;  // one CTA already covers all rows
     const int64_t rows = pair ? 256 : 128;
     const int W = pair ? sm_count / 2 : sm_count;
     for (int i = 0; i < 6; ++i) {
       const int bn = kTileWidths[i];
       if (cfg.bn && bn != cfg.bn) continue;
       // 512 columns: CTA pairs and float types only
-      if (bn == 512 && (!pair || int8 || cfg.cta_pair == 3)) continue;
+      if (bn == 512 && (!pair || int8)) continue;
       if (int8 && bn != 128 && bn != 160) continue;  // 3 x BN tensor-memory columns
-      if (cfg.cta_pair == 3 && bn != 256 && bn != 224) continue;  // the B-sharing widths
       const int64_t T64 = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
       const int T = static_cast<int>(std::min<int64_t>(T64, INT32_MAX));
       const double rate = (pair ? kRatePair[i] : kRateSingle[i]) * 1e6;  // FLOP per us
@@ -585,7 +583,7 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
           cost += static_cast<double>((T + W - 1) / W) * kWideEpilogueUs;
         }
         if (sk) {
-          if (cfg.stream_k == 1 || cfg.cta_pair == 3) continue;  // B sharing: data-parallel
+          if (cfg.stream_k == 1) continue;
           int skt, skw, mc;
           plan_stream_k(T, W, KT, 0, &skt, &skw, &mc);
           if (skt == 0) continue;
@@ -605,8 +603,6 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
 struct SquarePlan {
   KernelVariant v;
   bool pair;
-  bool mc;           // two pairs per cluster sharing B (cluster of 4)
-  int sched_m_tiles;  // tile rows of the schedule (with mc: pairs of tile rows)
   int tile_m, m_tiles, n_tiles, k_tiles, workers, grid;
   int sk_tiles, sk_workers, max_contrib;
   size_t partial_bytes;  // scratch for the stream-K partial tiles (0: none)
@@ -621,12 +617,7 @@ int plan_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, in
     t_last_error = "the requested tile width does not exist for this dtype/pairing";
     return SPTG_ERR_CONFIG;
   }
-  const bool mc = cfg.cta_pair == 3;
-  if (mc && (!pair || !pick_square(d, bn, cfg.stages, true, &pl->v, true))) {
-    t_last_error = "no B-sharing (two pairs per cluster) variant for the requested dtype/bn/stages";
-    return SPTG_ERR_CONFIG;
-  }
-  if (!mc && !pick_square(d, bn, cfg.stages, pair, &pl->v)) {
+  if (!pick_square(d, bn, cfg.stages, pair, &pl->v)) {
     // a forced ring depth may exist for the other tile mode only
     if (cfg.cta_pair == 0 && pick_square(d, bn, cfg.stages, !pair, &pl->v)) {
       pair = !pair;
@@ -638,28 +629,21 @@ int plan_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, in
   int rc = ensure_smem(dev, pl->v.fn, pl->v.smem);
   if (rc) return rc;
   pl->pair = pair;
-  pl->mc = mc;
   pl->tile_m = pair ? 256 : 128;
   pl->m_tiles = static_cast<int>((M + pl->tile_m - 1) / pl->tile_m);
   pl->n_tiles = static_cast<int>((N + pl->v.bn - 1) / pl->v.bn);
   pl->k_tiles = static_cast<int>((K + 63) / 64);
-  // with mc a schedule tile is two vertically adjacent tiles (the second
-  // one past the matrix when m_tiles is odd: its rows read zeros, store
-  // nothing, and its pair still copies its half of the shared B rows)
-  pl->sched_m_tiles = mc ? (pl->m_tiles + 1) / 2 : pl->m_tiles;
-  const int tiles = pl->sched_m_tiles * pl->n_tiles;
-  int workers = mc ? cluster_slots(dev, pl->v, 4, di.sm_count)
-                   : pair ? pair_slots(dev, pl->v, di.sm_count) : di.sm_count;
+  const int tiles = pl->m_tiles * pl->n_tiles;
+  int workers = pair ? pair_slots(dev, pl->v, di.sm_count) : di.sm_count;
   if (cfg.splits > 0) workers = std::min(workers, cfg.splits);
-  // the partial-tile slots and counters are per pair: no stream-K with mc
-  plan_stream_k(tiles, workers, pl->k_tiles, cfg.stream_k == 2 && !mc ? 2 : (sk && !mc ? 0 : 1),
-                &pl->sk_tiles, &pl->sk_workers, &pl->max_contrib);
+  plan_stream_k(tiles, workers, pl->k_tiles, cfg.stream_k == 2 ? 2 : (sk ? 0 : 1), &pl->sk_tiles,
+                &pl->sk_workers, &pl->max_contrib);
   if (pl->sk_tiles == 0)
     workers = std::min(workers, tiles);
   else if (pl->sk_tiles == tiles)
     workers = pl->sk_workers;  // no data-parallel tiles: idle workers are not launched
   pl->workers = workers;
-  pl->grid = mc ? 4 * workers : pair ? 2 * workers : workers;
+  pl->grid = pair ? 2 * workers : workers;
   pl->partial_bytes =
       static_cast<size_t>(pl->sk_tiles) * 2 * pl->max_contrib * 128 * pl->v.bn * 4;
   if (static_cast<size_t>(pl->sk_tiles) * 2 * sizeof(unsigned long long) > kCounterArea) {
@@ -678,7 +662,7 @@ int launch_square(const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N
   int rc = make_map_2d(&ta, d.in_tma, 2, A16, K, M, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B, lda);
   if (rc) return rc;
   rc = make_map_2d(&tb, d.in_tma, 2, B16, K, N, BK,
-                   (pl.mc || pl.v.bn > 256) ? pl.v.bn / 4 : pl.pair ? pl.v.bn / 2 : pl.v.bn,
+                   pl.v.bn > 256 ? pl.v.bn / 4 : pl.pair ? pl.v.bn / 2 : pl.v.bn,
                    CU_TENSOR_MAP_SWIZZLE_128B, ldb);
   if (rc) return rc;
   // C blocks of 32 columns x 32 rows: 128-byte rows for 4-byte outputs,
@@ -693,7 +677,7 @@ int launch_square(const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N
   p.K = static_cast<int>(K);
   p.C_out = C;
   p.ldc = ldc;
-  p.num_m_tiles = pl.sched_m_tiles;
+  p.num_m_tiles = pl.m_tiles;
   p.num_n_tiles = pl.n_tiles;
   p.num_k_tiles = pl.k_tiles;
   p.k_tiles_per_chunk = d.is_int8 ? 1024 / BK : pl.k_tiles;
@@ -701,8 +685,8 @@ int launch_square(const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N
   // on 4096^3 .. 16384 x 16384 x 4096 and 8192 x 8192 x 16384: 16-row strips
   // are best up to K = 4096 (0.6-1.8 % over 8), 12-row strips are never
   // worse than 8 beyond (16 loses 2-3 % there: the strip's A rows outgrow
-  // L2). With two pairs per cluster a schedule row is two tile rows.
-  p.group_m = (K <= 4096 ? 16 : 12) / (pl.mc ? 2 : 1);
+  // L2).
+  p.group_m = K <= 4096 ? 16 : 12;
   p.sk_tiles = pl.sk_tiles;
   p.sk_workers = pl.sk_workers;
   p.max_contrib = pl.max_contrib;
@@ -720,10 +704,10 @@ int launch_square(const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N
   set_config(
       "kernel=square dtype=%s tile_m=%lld bn=%lld bk=%lld stages=%lld pair=%lld grid=%lld "
       "tiles=%lld k_tiles=%lld chunk_k_tiles=%lld stream_k_tiles=%lld stream_k_workers=%lld "
-      "smem=%lld cluster_pairs=%lld",
+      "smem=%lld",
       d.name, {pl.tile_m, pl.v.bn, BK, pl.v.stages, pl.pair ? 1 : 0, pl.grid,
                static_cast<long long>(pl.m_tiles) * pl.n_tiles, pl.k_tiles, p.k_tiles_per_chunk,
-               pl.sk_tiles, pl.sk_workers, pl.v.smem, pl.mc ? 2 : 1});
+               pl.sk_tiles, pl.sk_workers, pl.v.smem});
   return SPTG_OK;
 }
 
@@ -970,7 +954,7 @@ extern "C" {
 
 int sptg_version(void) { return 100; }
 
-int sptg_plan_square(int64_t M, int64_t N, int64_t K, int dtype, int sm_count,
+int sptg_plan_square(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, int sm_count,
                      const sptg_config* cfg_in, int* out) {
   DtypeInfo d;
   if (!out || sm_count < 2 || !dtype_info(dtype, d) || M <= 0 || N <= 0 || K <= 0 ||
@@ -981,7 +965,7 @@ int sptg_plan_square(int64_t M, int64_t N, int64_t K, int dtype, int sm_count,
   sptg_config cfg;
   memset(&cfg, 0, sizeof(cfg));
   if (cfg_in) cfg = *cfg_in;
-  if (cfg.stream_k < 0 || cfg.stream_k > 2 || cfg.cta_pair < 0 || cfg.cta_pair > 3 ||
+  if (cfg.stream_k < 0 || cfg.stream_k > 2 || cfg.cta_pair < 0 || cfg.cta_pair > 2 ||
       cfg.bn < 0 || cfg.splits < 0) {
     t_last_error = "invalid configuration field";
     return SPTG_ERR_ARG;
@@ -989,26 +973,24 @@ int sptg_plan_square(int64_t M, int64_t N, int64_t K, int dtype, int sm_count,
   int bn = 0;
   bool pair = false, sk = false;
   choose_square_shape(M, N, K, sm_count, cfg, d.is_int8, &bn, &pair, &sk);
-  if ((cfg.bn && bn != cfg.bn) || (cfg.cta_pair == 3 && (!pair || d.is_int8))) {
+  if (cfg.bn && bn != cfg.bn) {
     t_last_error = "no square-kernel tile for the requested dtype, width and pairing";
     return SPTG_ERR_CONFIG;
   }
-  const bool share_b = cfg.cta_pair == 3;
-  const int64_t rows = share_b ? 512 : pair ? 256 : 128;  // schedule tile rows
+  const int64_t rows = pair ? 256 : 128;  // tile rows
   const int64_t T64 = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
   const int tiles = static_cast<int>(std::min<int64_t>(T64, INT32_MAX));
   const int k_tiles = static_cast<int>((K + 63) / 64);
-  int workers = share_b ? sm_count / 4 : pair ? sm_count / 2 : sm_count;
+  int workers = pair ? sm_count / 2 : sm_count;
   if (cfg.splits > 0) workers = std::min(workers, cfg.splits);
   int skt = 0, skw = 0, mc = 1;
-  plan_stream_k(tiles, workers, k_tiles, share_b ? 1 : cfg.stream_k == 2 ? 2 : (sk ? 0 : 1), &skt,
-                &skw, &mc);
+  plan_stream_k(tiles, workers, k_tiles, cfg.stream_k == 2 ? 2 : (sk ? 0 : 1), &skt, &skw, &mc);
   if (skt == 0)
     workers = std::min(workers, tiles);
   else if (skt == tiles)
     workers = skw;
   out[0] = bn;
-  out[1] = share_b ? 2 : pair ? 1 : 0;
+  out[1] = pair ? 1 : 0;
   out[2] = tiles;
   out[3] = workers;
   out[4] = skt;
@@ -1065,7 +1047,7 @@ int sptg_device_error(void* stream) {
   return SPTG_OK;
 }
 
-int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, int dtype, const void* A, int64_t lda,
+int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const void* A, int64_t lda,
                       const void* B, int64_t ldb, void* C, int64_t ldc, void* stream,
                       const sptg_config* cfg_in) {
   t_launches = 0;
@@ -1083,7 +1065,7 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, int dtype, const void* A,
   }
   if (cfg.kernel < 0 || cfg.kernel > 3 || cfg.stages < 0 || cfg.bn < 0 || cfg.splits < 0 ||
       cfg.timeout_ms < 0 || (cfg.inject_stall != 0 && cfg.inject_stall != 1) ||
-      cfg.cta_pair < 0 || cfg.cta_pair > 3 || (cfg.no_overlap != 0 && cfg.no_overlap != 1) ||
+      cfg.cta_pair < 0 || cfg.cta_pair > 2 || (cfg.no_overlap != 0 && cfg.no_overlap != 1) ||
       cfg.stream_k < 0 || cfg.stream_k > 2 ||
       (cfg.trace && (reinterpret_cast<uintptr_t>(cfg.trace) & 7u))) {
     t_last_error = "invalid configuration field";
@@ -1177,12 +1159,12 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, int dtype, const void* A,
                        0);
 }
 
-int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B,
+int sptg_gemm_ex(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const void* A, const void* B,
                  void* C, void* stream, const sptg_config* cfg) {
   return sptg_gemm_strided(M, N, K, dtype, A, K, B, K, C, N, stream, cfg);
 }
 
-int sptg_gemm_host(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B,
+int sptg_gemm_host(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const void* A, const void* B,
                    void* C, void* stream, const sptg_config* cfg) {
   t_launches = 0;
   DtypeInfo d;
@@ -1233,7 +1215,7 @@ int sptg_gemm_host(int64_t M, int64_t N, int64_t K, int dtype, const void* A, co
   return SPTG_OK;
 }
 
-int sptg_gemm(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B, void* C,
+int sptg_gemm(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const void* A, const void* B, void* C,
               void* stream) {
   return sptg_gemm_ex(M, N, K, dtype, A, B, C, stream, nullptr);
 }
@@ -1307,7 +1289,7 @@ int sptg_stream_scale(int64_t n, float alpha, const float* in, float* out, void*
   return sptg_stream_scale_ex(n, alpha, in, out, stream, nullptr);
 }
 
-int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, int dtype, const void* A,
+int sptg_gemm_skinny_noalloc(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const void* A,
                              const void* B, void* C, void* stream) {
   t_launches = 0;
   DtypeInfo d;

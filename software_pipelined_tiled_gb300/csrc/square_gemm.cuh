@@ -45,9 +45,7 @@
 // no second one, so that tile's epilogue does not overlap the next K-loop),
 // and each CTA copies its 128 rows of each half's B. Per FLOP this moves a
 // quarter fewer operand bytes than 256-wide tiles, which pays on long
-// K-loops. MC mode (opt-in) puts two pairs in a cluster of four on
-// vertically adjacent tiles that need the same B rows: each CTA copies half
-// of its B rows and multicasts them to its counterpart in the other pair.
+// K-loops.
 //
 // Work schedule (stream-K + data-parallel). With T tiles and W workers (CTAs,
 // or CTA pairs), T mod W tiles would leave a last round with most SMs idle.
@@ -237,8 +235,7 @@ __device__ __forceinline__ void store_c4(void* C, int64_t idx, uint4 bits) {
   }
 }
 
-template <int BN, int STAGES, bool IN_BF16, int OUT, bool INT_EXACT, bool PAIR = false,
-          bool MC = false>
+template <int BN, int STAGES, bool IN_BF16, int OUT, bool INT_EXACT, bool PAIR = false>
 __global__ void __launch_bounds__(SQUARE_THREADS, 1)
     square_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -253,7 +250,6 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   constexpr int NACC = L::NACC;
   constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, L::TILE_M, MMA_N);
   static_assert(!INT_EXACT || OUT == OUT_S32, "exact integer mode writes int32");
-  static_assert(!MC || (PAIR && !INT_EXACT && NH == 1), "B sharing pairs two CTA pairs");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -278,19 +274,14 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // CTA rank within the pair (0 = leader, which issues the MMAs). With MC a
-  // cluster holds two pairs (cluster ranks 0-1 and 2-3) working on vertically
-  // adjacent tiles that share their B tile: each CTA copies half of its B rows
-  // and multicasts them to the CTA of the same rank in the other pair.
-  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
-  const uint32_t rank = crank & 1u;
-  const uint32_t pidx = MC ? (crank >> 1) : 0u;  // which pair of the cluster
-  const uint32_t leader_crank = crank & ~1u;     // cluster rank of this pair's leader
+  // CTA rank within the pair (0 = leader, which issues the MMAs)
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const uint32_t leader_crank = 0u;  // cluster rank of the pair's leader
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), MC ? 2 : 1);  // MC: both pairs read the B rows of stage s
+      mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -320,15 +311,10 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int kpc = p.k_tiles_per_chunk;
-  // the persistent work unit is a CTA, a CTA pair in PAIR mode, or a cluster
-  // of two pairs with MC (its tiles then index pairs of vertically adjacent
-  // tiles: tile row mt of the schedule is rows 2 mt + pidx of the matrix)
-  constexpr int WSHIFT = MC ? 2 : (PAIR ? 1 : 0);
+  // the persistent work unit is a CTA, or a CTA pair in PAIR mode
+  constexpr int WSHIFT = PAIR ? 1 : 0;
   const int worker = static_cast<int>(blockIdx.x >> WSHIFT);
   const int workers = static_cast<int>(gridDim.x >> WSHIFT);
-  // B rows this CTA copies: its BN_CTA rows of the tile, or with MC the half
-  // of them that belongs to its pair (multicast to the other pair too)
-  constexpr int B_ROWS = MC ? L::BN_CTA / 2 : L::BN_CTA;
   // The producer warp works out its first segment and warms L2 with its
   // first stages while the previous kernel drains (safe: L2 is where writes
   // become coherent; the loads proper wait for the dependency).
@@ -341,13 +327,11 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
     have_seg0 = square_segment(p, worker, workers, 0, seg0);
     if (have_seg0) {
       tile_coords(seg0.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt0, nt0);
-      if constexpr (MC) mt0 = 2 * mt0 + static_cast<int>(pidx);
       for (int kt = seg0.kt0; lane == 0 && kt < min(seg0.kt1, seg0.kt0 + STAGES); ++kt) {
         tma_prefetch_l2_2d(&tmA, kt * BK, mt0 * L::TILE_M + static_cast<int>(rank) * BM);
         for (int h = 0; h < NH; ++h)
           tma_prefetch_l2_2d(&tmB, kt * BK,
-                             nt0 * BN + h * MMA_N + static_cast<int>(rank) * (L::BN_CTA / NH) +
-                                 static_cast<int>(pidx) * B_ROWS);
+                             nt0 * BN + h * MMA_N + static_cast<int>(rank) * (L::BN_CTA / NH));
       }
     }
   }
@@ -383,10 +367,9 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
         } else {
           if (!square_segment(p, worker, workers, i, seg)) break;
           tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
-          if constexpr (MC) mt = 2 * mt + static_cast<int>(pidx);
         }
         const int a_row = mt * L::TILE_M + static_cast<int>(rank) * BM;
-        const int b_row = nt * BN + static_cast<int>(rank) * L::BN_CTA + static_cast<int>(pidx) * B_ROWS;
+        const int b_row = nt * BN + static_cast<int>(rank) * L::BN_CTA;
         for (int kt = seg.kt0; kt < seg.kt1; ++kt, ++it) {
           const int s = it % STAGES;
           const uint32_t round = it / STAGES;
@@ -413,11 +396,6 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
                 tma_load_2d_pair(sB + s * L::B_STAGE + h * (MMA_N / 2) * (BK * 2), &tmB, leader_full,
                                  kt * BK, nt * BN + h * MMA_N + static_cast<int>(rank) * (MMA_N / 2),
                                  pol);
-            } else if constexpr (MC) {
-              // to this CTA and its counterpart in the other pair (cluster
-              // ranks rank and rank + 2); each copy counts at its own pair
-              tma_load_2d_pair_mc(sB + s * L::B_STAGE + pidx * (B_ROWS * BK * 2), &tmB, leader_full,
-                                  kt * BK, b_row, static_cast<uint16_t>(0x5u << rank), pol);
             } else {
               tma_load_2d_pair(sB + s * L::B_STAGE, &tmB, leader_full, kt * BK, b_row, pol);
             }
@@ -500,12 +478,8 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
                 for (int k = 1; k < BK / 16; ++k)  // +32 bytes (2 in descriptor units) per K = 16
                   mma_f16_g<PAIR>(dt, adesc + 2 * k, bd + 2 * k, IDESC, 1u);
               }
-              // stage s may be refilled (in both CTAs; with MC in all four,
-              // whose producers also write into this pair's stage)
-              if constexpr (MC)
-                mma_commit_pair_mask(empty_bar(s), 0xF);
-              else
-                mma_commit_g<PAIR>(empty_bar(s));
+              // stage s may be refilled (in both CTAs of a pair)
+              mma_commit_g<PAIR>(empty_bar(s));
             }
             __syncwarp();
             if (++s == STAGES) {
@@ -513,12 +487,8 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
               phase ^= 1u;
             }
           }
-          if (ok && leader) {  // accumulator b holds the finished chunk
-            if constexpr (MC)
-              mma_commit_pair_mask(tfull_bar(b), static_cast<uint16_t>(0x3u << leader_crank));
-            else
-              mma_commit_g<PAIR>(tfull_bar(b));
-          }
+          if (ok && leader)  // accumulator b holds the finished chunk
+            mma_commit_g<PAIR>(tfull_bar(b));
           __syncwarp();
         }
       }
@@ -543,7 +513,6 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
     for (int i = 0; ok && square_segment(p, worker, workers, i, seg); ++i) {
       int mt, nt;
       tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
-      if constexpr (MC) mt = 2 * mt + static_cast<int>(pidx);
       const int c_row = mt * L::TILE_M + static_cast<int>(rank) * BM + 32 * q;
       const int n_chunks = (seg.kt1 - seg.kt0 + kpc - 1) / kpc;
       // A partial segment's 32-bit values go to its scratch slot as 16-byte
@@ -755,7 +724,6 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       __threadfence();
       int mt, nt;
       tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
-      if constexpr (MC) mt = 2 * mt + static_cast<int>(pidx);
       const uint4* base = reinterpret_cast<const uint4*>(p.partials) +
                           (static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib * (32 * BN);
       // This contributor's rows: the first and the last contributor of a

@@ -7,13 +7,11 @@
 
 namespace sptg {
 
-template <int BN, int ST, bool BF, int OUT, bool IE, bool PAIR, bool MC = false>
+template <int BN, int ST, bool BF, int OUT, bool IE, bool PAIR>
 KernelVariant make_square() {
-  KernelVariant v{reinterpret_cast<const void*>(&square_gemm_kernel<BN, ST, BF, OUT, IE, PAIR, MC>),
-                  BN, ST, SquareLayout<BN, ST, IE, PAIR, OutTraits<OUT>::bytes>::SMEM_BYTES, PAIR,
-                  SQUARE_THREADS};
-  v.mc = MC;
-  return v;
+  return KernelVariant{reinterpret_cast<const void*>(&square_gemm_kernel<BN, ST, BF, OUT, IE, PAIR>),
+                       BN, ST, SquareLayout<BN, ST, IE, PAIR, OutTraits<OUT>::bytes>::SMEM_BYTES,
+                       PAIR, SQUARE_THREADS};
 }
 
 // Tile widths BN in {256, 224, 192, 160, 128}, one CTA or a CTA pair per
@@ -22,21 +20,8 @@ KernelVariant make_square() {
 // and of BN 224 (pair) for the pipelining ablation (1 = load, then compute,
 // no overlap).
 template <bool BF, int OUT>
-bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v, bool mc = false) {
+bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v) {
   constexpr int OB = OutTraits<OUT>::bytes;
-  if (mc) {
-    // two pairs per cluster sharing B: the two widest tiles, deepest ring
-    if (!pair) return false;
-    if (bn == 256 && (stages == 0 || stages == square_max_stages<256, true, OB>())) {
-      *v = make_square<256, square_max_stages<256, true, OB>(), BF, OUT, false, true, true>();
-      return true;
-    }
-    if (bn == 224 && (stages == 0 || stages == square_max_stages<224, true, OB>())) {
-      *v = make_square<224, square_max_stages<224, true, OB>(), BF, OUT, false, true, true>();
-      return true;
-    }
-    return false;
-  }
   if (bn == 512) {
     // 256 x 512 CTA-pair tiles: two 256-column MMAs per K-step, one accumulator
     if (!pair || (stages != 0 && stages != square_max_stages<512, true, OB>())) return false;

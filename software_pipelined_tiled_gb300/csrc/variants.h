@@ -18,19 +18,14 @@ struct KernelVariant {
   bool pair;       // square: 2-SM CTA-pair variant (cluster of 2)
   int threads = 192;  // CTA size
   int ksub = 1;       // skinny cluster: 64-wide K-chunks per ring stage
-  bool mc = false;    // square: two CTA pairs per cluster sharing B (cluster of 4)
 };
 
 // Square kernel for binary16 inputs (out_kind OUT_F16 or OUT_F32).
-bool square_variant_f16_f16(int bn, int stages, bool pair, KernelVariant* v,
-                          bool mc = false);
-bool square_variant_f16_f32(int bn, int stages, bool pair, KernelVariant* v,
-                          bool mc = false);
+bool square_variant_f16_f16(int bn, int stages, bool pair, KernelVariant* v);
+bool square_variant_f16_f32(int bn, int stages, bool pair, KernelVariant* v);
 // Square kernel for bfloat16 inputs (out_kind OUT_BF16 or OUT_F32).
-bool square_variant_bf16_bf16(int bn, int stages, bool pair, KernelVariant* v,
-                          bool mc = false);
-bool square_variant_bf16_f32(int bn, int stages, bool pair, KernelVariant* v,
-                          bool mc = false);
+bool square_variant_bf16_bf16(int bn, int stages, bool pair, KernelVariant* v);
+bool square_variant_bf16_f32(int bn, int stages, bool pair, KernelVariant* v);
 // Square kernel in exact-integer mode (int8 operands widened to binary16).
 bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v);
 // Skinny kernel (in_bf16 selects bfloat16 inputs, else binary16).

@@ -474,42 +474,6 @@ def test_wide_tiles_need_a_float_pair():
         run(A, B, I32, kernel="square", cta_pair=2, bn=512)
 
 
-# -------------------------------------------- two pairs per cluster sharing B
-@pytest.mark.parametrize("M,N,K,it,ot,bn", [
-    (768, 1000, 520, "f16", F16, 224),     # 3 tile rows: the last schedule row is half past M
-    (512, 768, 1024, "bf16", F32, 256),
-    (1280, 456, 200, "bf16", BF16, 224),   # ragged N and K
-    (256, 512, 64, "f16", F32, 256),       # one tile row, one K-tile
-])
-def test_b_sharing_pairs_parity(M, N, K, it, ot, bn):
-    # two CTA pairs per cluster of 4 work on vertically adjacent tiles; each
-    # copies half of the tile's B rows and multicasts it to the other pair
-    A, B = make_inputs(M, N, K, it, "uniform", 61)
-    C = run(A, B, ot, kernel="square", cta_pair=3, bn=bn)
-    cfg = sptg.last_config()
-    assert "cluster_pairs=2" in cfg and f"bn={bn}" in cfg and _sk_tiles() == 0, cfg
-    assert_float_parity(C, A, B)
-
-
-def test_b_sharing_pairs_many_rounds_sampled():
-    # 4096 x 4096 in 256 x 224 tiles: 152 schedule tiles = 4 rounds of the
-    # 38 clusters; the last tile column holds 64 of its 224 columns
-    A, B = make_inputs(4096, 4096, 4096, "f16", "uniform", 62)
-    C = run(A, B, F16, kernel="square", cta_pair=3)
-    assert "cluster_pairs=2" in sptg.last_config(), sptg.last_config()
-    rows, cols = sample_positions(4096, 4096, 20000, seed=62)
-    extra = np.arange(0, 4096, dtype=np.int64)
-    rows = np.concatenate([rows, extra])
-    cols = np.concatenate([cols, 18 * 224 + extra % 64])
-    assert_float_parity(C, A, B, rows, cols)
-
-
-def test_b_sharing_pairs_refuses_int8():
-    A, B = make_inputs(512, 512, 512, "s8", "int8", 63)
-    with pytest.raises(sptg.SptgError):
-        run(A, B, I32, kernel="square", cta_pair=3)
-
-
 # ------------------------------------------------------------ leading dimensions
 def _in_wider(X, pitch, fill):
     """X placed in the leading columns of a rows x pitch device buffer."""
@@ -693,8 +657,8 @@ def test_bounded_wait_reports_timeout_and_context_survives(kernel, pair, stream_
     assert_float_parity(C, A, B)
 
 
-@pytest.mark.parametrize("kernel,cta_pair", [("square", 1), ("square", 2), ("square", 3),
-                                             ("skinny", 0), ("skinny_cluster", 0)])
+@pytest.mark.parametrize("kernel,cta_pair", [("square", 1), ("square", 2), ("skinny", 0),
+                                             ("skinny_cluster", 0)])
 def test_timeline_trace_is_ordered(kernel, cta_pair):
     # the optional in-kernel timeline: per CTA the events come in pipeline
     # order, and CTA 0's K-tiles are consumed after they were issued

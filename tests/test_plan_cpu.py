@@ -4,8 +4,8 @@ sptg_plan_square runs the tile-shape model and the stream-K split of
 sptg_gemm_ex without touching a device. These tests check the choices the
 method depends on (whole rounds of 256 x 224 pair tiles at 4096^3, a
 partial last round cut along K for a long K-loop, small products left
-data-parallel, the int8 tile widths, the schedule of two pairs sharing B
-rows) and, over many random
+data-parallel, the int8 tile widths, no cluster-sharing mode) and, over
+many random
 shapes and configurations, the invariants the kernels rely on: a cut tile
 never has more contributors than the scratch holds slots for, every
 stream-K worker gets at least 8 K-tiles, and forced settings are honoured.
@@ -151,17 +151,8 @@ def test_plan_invariants_over_random_shapes():
                 assert last - first + 1 <= mc
 
 
-def test_b_sharing_pairs_schedule_pairs_of_tile_rows():
-    # 4096^3 in 256 x 224 tiles: 16 tile rows -> 8 schedule rows of two,
-    # 19 columns, 152 schedule tiles over 38 clusters of two pairs
-    p = plan(4096, 4096, 4096, cta_pair=3)
-    assert (p["bn"], p["pair"], p["tiles"], p["workers"]) == (224, 2, 152, 38)
-    assert p["stream_k_tiles"] == 0
-    # an odd number of tile rows rounds up; no stream-K even when asked for
-    p = plan(4096 + 256, 8192, 16384, "bf16_f32", cta_pair=3, stream_k=2)
-    assert p["pair"] == 2 and p["bn"] in (224, 256) and p["stream_k_tiles"] == 0
-    assert p["tiles"] == 9 * ((8192 + p["bn"] - 1) // p["bn"])
-    # only the two widest float tiles have the shared-B form
-    for args, cfg in [((8192, 8192, 4096), {"bn": 192}), ((4096, 4096, 4096, "s8_s32"), {})]:
+def test_no_multicast_mode():
+    # every CTA copies its own operand tiles: there is no cluster-sharing mode
+    for cfg in ({"cta_pair": 3}, {"cta_pair": -1}):
         with pytest.raises(sptg.SptgError):
-            plan(*args, cta_pair=3, **cfg)
+            plan(4096, 4096, 4096, **cfg)

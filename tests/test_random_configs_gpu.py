@@ -4,8 +4,7 @@ Every case is small enough for the full oracle, so each element of C is
 checked: int8 bit-exact, float within the element-wise bound. The shapes are
 ragged (no tile multiple) within the library's 16-byte row-pitch rule, and the
 configurations cover the automatic choice, one-CTA and CTA-pair tiles of
-every width, stream-K never / chosen / every tile, two pairs sharing B, and
-both skinny kernels with their cluster sizes.
+every width, stream-K never / chosen / every tile, and both skinny kernels with their cluster sizes.
 """
 import random
 
@@ -26,8 +25,8 @@ def _case(i):
     rng = random.Random(1000 + i)
     dt = rng.choice(list(OUT))
     it = dt.split("_")[0]
-    kind = rng.choice(["auto", "single", "pair", "pair", "share_b", "skinny", "skinny_cluster"])
-    if dt == "s8_s32" and kind in ("share_b", "skinny", "skinny_cluster"):
+    kind = rng.choice(["auto", "single", "pair", "pair", "pair", "skinny", "skinny_cluster"])
+    if dt == "s8_s32" and kind in ("skinny", "skinny_cluster"):
         kind = "pair"
     kmul = 16 if it == "s8" else 8          # 16-byte rows of A and B
     nmul = 4 if OUT[dt].itemsize == 4 else 8  # 16-byte rows of C
@@ -39,14 +38,13 @@ def _case(i):
         N = nmul * rng.randint(1, 700 // nmul)
     K = kmul * rng.randint(1, 700 // kmul)
     kw = {}
-    if kind in ("single", "pair", "share_b"):
+    if kind in ("single", "pair"):
         kw["kernel"] = "square"
-        kw["cta_pair"] = {"single": 1, "pair": 2, "share_b": 3}[kind]
-        widths = (256, 224) if kind == "share_b" else \
-            ((160, 128) if it == "s8" else (256, 224, 192, 160, 128)
-             + ((512,) if kind == "pair" else ()))
+        kw["cta_pair"] = {"single": 1, "pair": 2}[kind]
+        widths = ((160, 128) if it == "s8" else (256, 224, 192, 160, 128)
+                  + ((512,) if kind == "pair" else ()))
         kw["bn"] = rng.choice(widths)
-        if kind != "share_b" and kw["bn"] != 512:
+        if kw["bn"] != 512:
             kw["stream_k"] = rng.choice([0, 1, 2])
             if kw["stream_k"] == 2:
                 kw["splits"] = rng.randint(2, 40)
@@ -65,10 +63,8 @@ def test_random_configuration(i):
     A, B = make_inputs(M, N, K, it, "int8" if it == "s8" else "uniform", 2000 + i)
     C = run(A, B, OUT[dt], **kw)
     cfg = sptg.last_config()
-    if kind == "share_b":
-        assert "cluster_pairs=2" in cfg, cfg
-    elif "kernel=square" in cfg:
-        assert "cluster_pairs=1" in cfg, cfg
+    if kind in ("single", "pair"):
+        assert f"pair={int(kind == 'pair')}" in cfg, cfg
     if it == "s8":
         assert_int_parity(C, A, B)
     else:
