@@ -29,7 +29,6 @@ enum WaitSite : unsigned int {
   WAIT_PLAN = 1u << 5,  // not a wait: a launch whose scratch plan does not fit
   WAIT_FIXUP_NOTE = 1u << 6,  // reduction warps: notice of a written partial tile
   WAIT_FIXUP_SLOT = 1u << 7,  // epilogue: a free notice slot
-  WAIT_FIXUP_PEERS = 1u << 8,  // reduction warps: the other contributors' arrivals
 };
 
 // Optional timeline: with a trace buffer, chosen threads stamp %globaltimer
@@ -151,12 +150,12 @@ __device__ __forceinline__ void store_out4(void* C, int64_t idx, float4 v) {
 
 // Counts one arrival at a tile's split-K counter and returns whether it was the
 // last of `count`. The 64-bit counter holds (call generation << 32 |
-// departures << 16 | arrivals): a value left by an earlier call (or by one
-// that gave up) carries another generation and is replaced, so no call has to
-// clear the counters first. A call that finishes with a counter sets it back
-// to 0 (a CUDA graph replays a call with the generation it was captured
-// with, so the next replay must not find this call's count). The
-// compare-and-swap retries only when another contributor got in first.
+// arrivals): a value left by an earlier call (or by one that gave up) carries
+// another generation and is replaced, so no call has to clear the counters
+// first. The last arrival sets the counter back to 0 (a CUDA graph replays a
+// call with the generation it was captured with, so the next replay must not
+// find this call's count). The compare-and-swap retries only when another
+// contributor got in first.
 __device__ __forceinline__ int arrive_generation(unsigned long long* ctr, unsigned int gen,
                                                  int count, unsigned int* error_word) {
   unsigned long long cur = atomicAdd(ctr, 0ull);
@@ -170,34 +169,6 @@ __device__ __forceinline__ int arrive_generation(unsigned long long* ctr, unsign
   }
   atomicOr(error_word, WAIT_PLAN);
   return 0;
-}
-
-// Waits, for at most ctl.timeout_ns, until the counter holds `count`
-// arrivals of generation `gen` (see arrive_generation); false on time-out
-// (site WAIT_FIXUP_PEERS) or when another role raised the abort flag.
-__device__ __forceinline__ bool wait_arrivals(const unsigned long long* ctr, unsigned int gen,
-                                              int count, const WaitCtl& ctl) {
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
-    if (static_cast<unsigned int>(v >> 32) == gen && static_cast<int>(v & 0xffffull) == count)
-      return true;
-    if (*ctl.abort_flag) return false;
-    if (global_timer_ns() - t0 > ctl.timeout_ns) {
-      *ctl.abort_flag = 1;
-      atomicOr(ctl.error_word, WAIT_FIXUP_PEERS);
-      return false;
-    }
-    __nanosleep(100);
-  }
-}
-
-// Counts one departure of a contributor that has seen all `count` arrivals;
-// the last to leave sets the counter back to 0 (see arrive_generation).
-__device__ __forceinline__ void depart_generation(unsigned long long* ctr, int count) {
-  const unsigned long long prev = atomicAdd(ctr, 1ull << 16);
-  if (static_cast<int>((prev >> 16) & 0xffffull) + 1 == count) atomicExch(ctr, 0ull);
 }
 
 // Tile index -> (m tile, n tile). Tiles are visited in column strips of

@@ -54,15 +54,16 @@
 // tiles follow round robin, every worker the same number. A worker whose range
 // covers only part of a tile's K writes its fp32 (int32 in INT_EXACT mode)
 // partial tile to scratch and counts its arrival (an atomic counter tagged
-// with the call's generation). Once all of a tile's contributors have
-// arrived, each contributor adds up its share of the rows over all partials
-// in contributor order (= increasing k, a fixed order) and writes C. The
-// epilogue writes the partial, counts the arrival and posts a notice; four
-// reduction warps of their own take the wait and the sum, so the
+// with the call's generation). The contributor whose arrival completes the
+// count adds up all partials of its rows in contributor order (= increasing
+// k, a fixed order, so the result does not depend on which one came last) and
+// writes C; the others go on at once. No CTA ever waits for another, so the
+// schedule needs no co-residency of the grid: a CTA that becomes resident
+// only after others have finished (the GPU shared with other work) still
+// completes the product. The epilogue writes the partial, counts the arrival
+// and posts a notice; four reduction warps of their own take the sum, so the
 // accumulators keep draining and the K-loop of the next tiles never waits
-// for a reduction. The wait needs every CTA of the grid resident at once,
-// which the persistent grid (one CTA, or pair, per SM slot) is; it is
-// bounded like every other wait.
+// for a reduction.
 //
 // INT_EXACT mode computes an int8 product exactly on the fp16 tensor path: the
 // inputs are int8 values held as binary16 (exact), every product is an integer
@@ -195,7 +196,7 @@ struct SquareLayout {
   static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 4;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int BYTES_USED = OFF_MISC + 16;
+  static constexpr int BYTES_USED = OFF_MISC + 24;
   static constexpr int SMEM_BYTES = BYTES_USED + 1024;  // slack to align the base to 1024
   // tiles wider than one MMA (BN = 512: two 256-column MMAs per K-step) keep
   // a single accumulator: 512 columns fill tensor memory
@@ -214,7 +215,7 @@ struct SquareLayout {
   static_assert(!PAIR || BN_CTA % 16 == 0, "each CTA's B rows must be a multiple of 16");
   static_assert(STAGES >= 1, "at least one stage");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
-  static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
+  static_assert(NUM_BARS * 8 + 24 <= 256, "barrier area");
 };
 
 // Deepest ring that fits the 227 KB per-CTA budget next to the epilogue
@@ -271,6 +272,8 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   // the reduction warps' decision per notice (two slots, alternating)
   volatile int* fix_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
+  // per notice: 1 if this CTA's arrival completed the tile (it reduces it)
+  volatile int* note_last = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -675,16 +678,21 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       }
       if (!ok || !seg.partial) continue;
       // The partial is written: every writer makes its stores visible at GPU
-      // scope, then one thread counts the arrival at the tile's counter (at
-      // once, so that no contributor waits on another's reductions) and
-      // posts the notice to the reduction warps.
+      // scope, then one thread counts the arrival at the tile's counter and
+      // posts a notice to the reduction warps saying whether this arrival
+      // completed the tile.
       __threadfence();
       named_barrier_sync(1, 128);
       if (threadIdx.x == 64) {
-        arrive_generation(p.counters + seg.sk * 2 + rank, p.generation, seg.count, p.error_word);
+        unsigned long long* ctr = p.counters + seg.sk * 2 + rank;
+        const int last = arrive_generation(ctr, p.generation, seg.count, p.error_word);
+        // the last arrival is the counter's last use in this call
+        if (last) atomicExch(ctr, 0ull);
         const uint32_t j = notes & 1u, use = notes >> 1;
-        if (wait_bounded(note_empty(j), (use & 1u) ^ 1u, ctl, WAIT_FIXUP_SLOT))
+        if (wait_bounded(note_empty(j), (use & 1u) ^ 1u, ctl, WAIT_FIXUP_SLOT)) {
+          note_last[j] = last;
           mbar_arrive(note_full(j));
+        }
       }
       ++notes;
     }
@@ -693,10 +701,9 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
   } else if (p.sk_tiles > 0) {
     // ---------------------------------------------- stream-K reduction warps
     // For each partial tile this CTA wrote (the epilogue's notices, in
-    // segment order): wait until all the tile's contributors have arrived,
-    // then add up this contributor's share of this CTA's 128 rows over all
-    // partials in contributor order and write it to C. Every contributor so
-    // reduces a part of the tile, and no CTA carries a whole reduction.
+    // segment order): if this CTA's arrival completed the tile, add up this
+    // CTA's 128 rows over all partials in contributor order and write them to
+    // C; otherwise another contributor does.
     const int tid = threadIdx.x - 192;  // 0..127
     uint32_t notes = 0;
     bool ok = true;
@@ -705,39 +712,30 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       if (!seg.partial) continue;
       const uint32_t j = notes & 1u, use = notes >> 1;
       if (tid == 0) {
-        int flag = 0;
+        int flag = -1;  // -1: gave up waiting for the notice
         if (wait_bounded(note_full(j), use & 1u, ctl, WAIT_FIXUP_NOTE)) {
+          flag = note_last[j];
           mbar_arrive(note_empty(j));  // the notice is consumed
-          unsigned long long* ctr = p.counters + seg.sk * 2 + rank;
-          flag = wait_arrivals(ctr, p.generation, seg.count, ctl) ? 1 : 0;
-          if (flag) depart_generation(ctr, seg.count);
         }
         fix_flag[j] = flag;
       }
       named_barrier_sync(2, 128);
       const int flag = fix_flag[j];
       ++notes;
-      if (!flag) {
+      if (flag < 0) {
         ok = false;
         break;
       }
+      if (flag == 0) continue;  // a later contributor reduces this tile
       __threadfence();
       int mt, nt;
       tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
       const uint4* base = reinterpret_cast<const uint4*>(p.partials) +
                           (static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib * (32 * BN);
-      // This contributor's rows: the first and the last contributor of a
-      // tile usually hold a cut of another tile as well, so they take a half
-      // share each and the ones in between a whole share (in half shares:
-      // [0, 1), [1, 3), [3, 5), ..., [2 count - 3, 2 count - 2)).
-      const int halves = 2 * seg.count - 2;
-      const int h0 = seg.j == 0 ? 0 : 2 * seg.j - 1;
-      const int h1 = seg.j == seg.count - 1 ? halves : 2 * seg.j + 1;
-      const int r0 = 128 * h0 / halves;
-      const int nr = 128 * h1 / halves - r0;
-      // Flat index f over this share: group g = f % 8 of four columns,
-      // row r0 + (f / 8) % nr, 32-column block f / (8 nr). A warp reads
-      // 64-byte runs of the partials and writes whole row segments of C.
+      // Flat index f over the CTA's 128 rows: group g = f % 8 of four
+      // columns, row (f / 8) % 128, 32-column block f / (8 * 128). A warp
+      // reads 64-byte runs of the partials and writes whole row segments of C.
+      constexpr int nr = 128;
       const int total = nr * (BN / 4);
       constexpr int CH = 8;  // groups per contributor in flight
       constexpr int CB = 2;  // contributors in flight
@@ -749,8 +747,8 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
         for (int i2 = 0; i2 < CH; ++i2) {
           const int f = f0 + tid + 128 * i2;
           const int rest = f >> 3;
-          const int cb = rest / max(nr, 1);
-          idx[i2] = f < total ? ((cb * 8 + (f & 7)) * 128 + r0 + (rest - cb * nr)) : -1;
+          const int cb = rest / nr;
+          idx[i2] = f < total ? ((cb * 8 + (f & 7)) * 128 + (rest - cb * nr)) : -1;
         }
         uint4 acc[CH];
 #pragma unroll 1

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import software_pipelined_tiled_gb300 as sptg
 from gpu_helpers import (assert_float_parity, assert_int_parity, run, sample_positions)
 from workloads import WORKLOADS, make_inputs, workload_inputs
@@ -20,19 +21,22 @@ F16, BF16, F32, I8, I32 = torch.float16, torch.bfloat16, torch.float32, torch.in
 
 
 # ----------------------------------------------------------------- workloads
+# Float workloads meet the unmodified bound |C - C_ref| <= 1e-3 sum_k |A_ik B_kj|
+# itself (plain=True): their K is large enough that the output rounding of a
+# 16-bit C stays well inside it. Each prints its max |err| / (1e-3 sum|AB|).
 def test_workload_f16_256_f32out():
     w = WORKLOADS["f16_256x256x256_f32out"]
     A, B = workload_inputs(w)
     C = run(A, B, F32)
     assert "kernel=square" in sptg.last_config()
-    assert_float_parity(C, A, B)
+    print(w.name, "max |err| / (1e-3 sum|ab|) =", assert_float_parity(C, A, B, plain=True))
 
 
 def test_workload_f16_4096_f16out():
     w = WORKLOADS["f16_4096x4096x4096_f16out"]
     A, B = workload_inputs(w)
     C = run(A, B, F16)
-    assert_float_parity(C, A, B)
+    print(w.name, "max |err| / (1e-3 sum|ab|) =", assert_float_parity(C, A, B, plain=True))
 
 
 def test_workload_s8_4096_bit_exact():
@@ -47,7 +51,7 @@ def test_workload_bf16_skinny():
     A, B = workload_inputs(w)
     C = run(A, B, BF16)
     assert "kernel=skinny" in sptg.last_config()
-    assert_float_parity(C, A, B)
+    print(w.name, "max |err| / (1e-3 sum|ab|) =", assert_float_parity(C, A, B, plain=True))
 
 
 def test_workload_bf16_8192x8192x16384_sampled():
@@ -61,12 +65,22 @@ def test_workload_bf16_8192x8192x16384_sampled():
     extra = np.arange(2560, 2816, dtype=np.int64)
     rows = np.concatenate([rows, np.repeat(extra, 16)])
     cols = np.concatenate([cols, np.tile(np.arange(4096, 4608, 32, dtype=np.int64), 256) + np.repeat(extra, 16) % 32])
-    assert_float_parity(C, A, B, rows, cols)
+    assert_float_parity(C, A, B, rows, cols, plain=True)
     # a whole row and a whole column as well
     r = np.full(w.N, 4097, dtype=np.int64)
-    assert_float_parity(C, A, B, r, np.arange(w.N, dtype=np.int64))
+    assert_float_parity(C, A, B, r, np.arange(w.N, dtype=np.int64), plain=True)
     c = np.full(w.M, 8191, dtype=np.int64)
-    assert_float_parity(C, A, B, np.arange(w.M, dtype=np.int64), c)
+    assert_float_parity(C, A, B, np.arange(w.M, dtype=np.int64), c, plain=True)
+
+
+@pytest.mark.slow
+def test_workload_bf16_8192x8192x16384_every_element():
+    # all 67 M outputs against the oracle (about a minute of CPU time on the
+    # host's cores)
+    w = WORKLOADS["bf16_8192x8192x16384_f32out"]
+    A, B = workload_inputs(w)
+    C = run(A, B, F32)
+    print(w.name, "max |err| / (1e-3 sum|ab|) =", assert_float_parity(C, A, B, plain=True))
 
 
 # ---------------------------------------------------------- pipeline structure
@@ -132,8 +146,10 @@ def test_cta_pair_operand_halves_are_not_swapped():
     Bcm = (torch.arange(N).unsqueeze(1) + 1).to(F32).expand(N, K).contiguous() / 256
     A, Bcm = A.to(F16), Bcm.to(F16)
     C = run(A, Bcm, F32, cta_pair=2, bn=224)
-    expect = (A.to(torch.float64) @ Bcm.to(torch.float64).t()).to(F32)
-    assert torch.equal(C, expect)
+    # every product and partial sum is a multiple of 2^-16 below 2^6: exact in
+    # fp32, so the result must equal the oracle's sum exactly
+    ref, _ = oracle.gemm_float(A, Bcm, oracle.IN_F16)
+    assert np.array_equal(C.to(torch.float64).numpy(), ref)
 
 
 @pytest.mark.parametrize("stages", [1, 2, 3, 4, 5, 6])
@@ -141,7 +157,10 @@ def test_cta_pair_stage_count_does_not_change_the_arithmetic(stages):
     A, B = make_inputs(512, 448, 640, "f16", "uniform", 13)
     ref = run(A, B, F16, bn=224, cta_pair=2)
     got = run(A, B, F16, stages=stages, bn=224, cta_pair=2)
+    assert f"stages={stages}" in sptg.last_config() and "pair=1" in sptg.last_config()
     assert torch.equal(ref, got)
+    # and against the oracle: a fault shared by every ring depth shows here
+    assert_float_parity(got, A, B)
 
 
 @pytest.mark.parametrize("T", [1, 2, 7, 8, 9, 17])
@@ -188,7 +207,9 @@ def test_stage_count_does_not_change_the_arithmetic(stages):
     A, B = make_inputs(384, 512, 1024, "f16", "uniform", 12)
     ref = run(A, B, F16, bn=224, cta_pair=1)
     got = run(A, B, F16, stages=stages, bn=224, cta_pair=1)
+    assert f"stages={stages}" in sptg.last_config()
     assert torch.equal(ref, got)
+    assert_float_parity(got, A, B)
 
 
 @pytest.mark.parametrize("stages", [1, 2, 3, 4, 5])
@@ -200,6 +221,7 @@ def test_long_k_ablation_rings_match(stages):
     got = run(A, B, F32, bn=256, cta_pair=2, stream_k=1, stages=stages)
     assert f"stages={stages}" in sptg.last_config()
     assert torch.equal(ref, got)
+    assert_float_parity(got, A, B)
 
 
 @pytest.mark.parametrize("stages", [1, 2, 3])
@@ -209,6 +231,7 @@ def test_skinny_cluster_ablation_rings_match(stages):
     got = run(A, B, BF16, kernel="skinny_cluster", splits=2, stages=stages)
     assert f"stages={stages}" in sptg.last_config()
     assert torch.equal(ref, got)
+    assert_float_parity(got, A, B)
 
 
 # --------------------------------------------------------- ragged and edges
@@ -635,12 +658,12 @@ def test_async_on_a_side_stream():
 
 
 @pytest.mark.parametrize("kernel,pair,stream_k", [(1, 1, 0), (1, 2, 0), (1, 1, 2), (1, 2, 2),
-                                                   (1, 3, 0), (2, 0, 0), (3, 0, 0)])
+                                                   (2, 0, 0), (3, 0, 0)])
 def test_bounded_wait_reports_timeout_and_context_survives(kernel, pair, stream_k):
     # The producer withholds one K-tile; the consumer's wait runs out after
     # 100 ms, the kernel tears down, and the host reads SPTG_ERR_TIMEOUT.
-    # With every tile cut along K, the other CTAs' reduction warps also give
-    # up waiting for the stalled contributor.
+    # With every tile cut along K, the other contributors of the stalled
+    # CTA's tiles count their arrival and go on: none of them waits for it.
     M = 512 if kernel == 1 else 64
     A, B = make_inputs(M, 1024, 1024, "bf16", "normal", 30)
     dA, dB = A.cuda(), B.cuda()

@@ -42,17 +42,27 @@ def test_noalloc_matches_the_allocating_entry_on_two_calls(M, N, K):
     assert sptg.device_error() == 0
     existing = ref_gpu.cpu().to(torch.float64).numpy()
     ref, bound = _bound(A, B, BF16)
-    for call in range(2):
-        out = torch.full((M, N), float("nan"), dtype=BF16, device="cuda")
+    # The calls below go to a new stream, for which the allocating entry
+    # points hold no cached scratch: had this entry point asked for scratch
+    # after all, it would have to allocate some, and the device's free memory
+    # would drop. The outputs are allocated before the free memory is read.
+    side = torch.cuda.Stream()
+    outs = [torch.full((M, N), float("nan"), dtype=BF16, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for call, out in enumerate(outs):
         rc = sptg.gemm_skinny_noalloc_raw(M, N, K, "bf16_bf16", dA.data_ptr(), dB.data_ptr(),
-                                          out.data_ptr(), stream)
+                                          out.data_ptr(), side.cuda_stream)
         assert rc == 0, sptg.last_error()
-        torch.cuda.synchronize()
-        assert sptg.device_error() == 0
+        side.synchronize()
+        assert sptg.device_error(side) == 0
         got = out.cpu().to(torch.float64).numpy()
         assert np.isfinite(got).all(), f"call {call}: output not fully written"
         assert (np.abs(got - existing) <= bound).all(), f"call {call}: differs from sptg_gemm"
         assert (np.abs(got - ref) <= bound).all(), f"call {call}: outside the oracle bound"
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before, f"device memory changed by {free_before - free_after} bytes"
 
 
 def test_noalloc_rejects_what_it_cannot_hold():
