@@ -18,6 +18,15 @@ host->device copies of A and B and the device->host copy of C inside the
 timed region. `cpu_baseline` is the CPU oracle (fp64 triple loop) timed on the
 host cores on a bounded sample of the same workload.
 
+`parity` compares the output of the last timed step with the oracle on the
+rows of that sample (all rows when the oracle finishes them in time).
+
+`workloads` adds the other four workloads, each timed on its own in the same
+way (its own rotating sets, warm-up, CUDA events), with its roofline, the
+oracle on a bounded sample (a few seconds) and a parity verdict on its own
+output: every element where the oracle covers all rows, else every element
+of the sampled rows plus 4096 random positions. --no-workloads skips them.
+
 --impl reference times that oracle as the reference arm on the same
 workload, each step a bounded sample (a block of output rows).
 """
@@ -37,7 +46,7 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from workloads import WORKLOADS, TORCH_DTYPE, workload_inputs  # noqa: E402
+from workloads import WORKLOADS, WORKLOAD_ORDER, TORCH_DTYPE, workload_inputs  # noqa: E402
 
 DEFAULT_WORKLOAD = "f16_4096x4096x4096_f16out"
 L2_BYTES = 129 * 10 ** 6
@@ -183,19 +192,82 @@ def oracle_sample(w, A, B, target_s: float = 12.0):
     return rows, oracle.threads()
 
 
-def cpu_baseline(w, A, B, target_s: float = 12.0):
+def oracle_rows(w, A, B, rows: int):
+    """The oracle on output rows 0..rows-1: (seconds, result); the result is
+    (C_ref, sum_k |A_ik B_kj|) in fp64 for float inputs, the int64 C for int8."""
     import oracle
-    rows, cores = oracle_sample(w, A, B, target_s)
     t0 = time.perf_counter()
     if w.in_type == "s8":
-        oracle.gemm_s8(A[:rows], B)
+        res = oracle.gemm_s8(A[:rows], B)
     else:
-        oracle.gemm_float(A[:rows], B, {"f16": oracle.IN_F16, "bf16": oracle.IN_BF16}[w.in_type])
-    dt = time.perf_counter() - t0
+        res = oracle.gemm_float(A[:rows], B, {"f16": oracle.IN_F16, "bf16": oracle.IN_BF16}[w.in_type])
+    return time.perf_counter() - t0, res
+
+
+def cpu_baseline(w, A, B, target_s: float = 12.0):
+    """The oracle timed on a leading block of output rows (about target_s
+    seconds); returns (cpu_baseline record, rows, oracle result)."""
+    rows, cores = oracle_sample(w, A, B, target_s)
+    dt, res = oracle_rows(w, A, B, rows)
     _, unit = metric_for(w)
-    return {"value": 2.0 * rows * w.N * w.K / dt / 1e12, "unit": unit, "cores": cores,
-            "kind": "oracle",
-            "sample": f"output rows 0..{rows - 1} of {w.M} ({rows}x{w.N}x{w.K}), {dt:.1f} s"}
+    rec = {"value": 2.0 * rows * w.N * w.K / dt / 1e12, "unit": unit, "cores": cores,
+           "kind": "oracle",
+           "sample": f"output rows 0..{rows - 1} of {w.M} ({rows}x{w.N}x{w.K}), {dt:.1f} s"}
+    return rec, rows, res
+
+
+# The element-wise bar of the float workloads: |C - C_ref| <= 1e-3 sum_k |A_ik B_kj|
+# for the fp32-accumulated sum, plus the round-to-nearest of a 16-bit output
+# (unit roundoff u); int8 results must equal the oracle's.
+PARITY_TOL = 1e-3
+OUT_U = {"f32": 0.0, "f16": 2.0 ** -11, "bf16": 2.0 ** -8}
+
+
+def parity_verdict(w, C, A, B, rows: int, res, n_random: int = 0):
+    """Compares this run's own output C (host tensor) with the oracle: every
+    element of rows 0..rows-1 (res is the oracle's result for them) and
+    n_random uniformly drawn positions of the whole matrix."""
+    import numpy as np
+    import oracle
+    checked = "every element" if rows == w.M else f"every element of rows 0..{rows - 1}"
+    if n_random:
+        g = np.random.default_rng(w.seed)
+        r = g.integers(0, w.M, n_random).astype(np.int64)
+        c = g.integers(0, w.N, n_random).astype(np.int64)
+        checked += f" + {n_random} random positions"
+    if w.in_type == "s8":
+        got = C[:rows].to(torch.int64).numpy()
+        bad = int((got != res).sum())
+        n = got.size
+        if n_random:
+            ref_r = oracle.gemm_s8_at(A, B, r, c)
+            bad += int((C.to(torch.int64).numpy()[r, c] != ref_r).sum())
+            n += n_random
+        return {"checked": checked, "elements": int(n), "rule": "bit-exact", "ok": bad == 0,
+                "mismatches": bad}
+    ref, S = res
+    u = OUT_U[w.out_type]
+    full = C.to(torch.float64).numpy()
+    gots, refs, sums = [full[:rows]], [ref], [S]
+    if n_random:
+        it = {"f16": oracle.IN_F16, "bf16": oracle.IN_BF16}[w.in_type]
+        ref_r, S_r = oracle.gemm_float_at(A, B, it, r, c)
+        gots.append(full[r, c])
+        refs.append(ref_r)
+        sums.append(S_r)
+    worst, worst_plain, bad, n = 0.0, 0.0, 0, 0
+    tiny = np.finfo(np.float64).tiny
+    for got, rf, sm in zip(gots, refs, sums):
+        err = np.abs(got - rf)
+        bound = PARITY_TOL * sm + u * (np.abs(rf) + PARITY_TOL * sm)
+        bad += int((~(err <= bound)).sum())
+        n += err.size
+        worst = max(worst, float((err / np.maximum(bound, tiny)).max()))
+        worst_plain = max(worst_plain, float((err / np.maximum(PARITY_TOL * sm, tiny)).max()))
+    return {"checked": checked, "elements": int(n),
+            "rule": "|C - C_ref| <= 1e-3 sum|ab| + u (|C_ref| + 1e-3 sum|ab|)", "ok": bad == 0,
+            "outside": bad, "max_err_over_bound": worst,
+            "max_err_over_1e-3_sum_abs": worst_plain}
 
 
 # ------------------------------------------------------------- GPU leg
@@ -313,6 +385,8 @@ def run_ours(args, w):
     value = job_throughput(w.flops, world, ms_per_step) * 1e3 / 1e12
     if sptg.device_error() != 0:
         raise RuntimeError("kernel reported a timed-out wait in the timed region")
+    # the output of the last timed step, for the parity verdict
+    C_check = Cs[(args.steps - 1) % n_sets].cpu() if rank == 0 else None
 
     # ---- end to end through the public API from pinned host memory
     # Each step is one sptg_gemm_host call on pinned host buffers: the copy of
@@ -353,38 +427,31 @@ def run_ours(args, w):
                "d2h_bytes_per_step": hCs[0].numel() * hCs[0].element_size(),
                "ms_per_step": e_ms, "api": "sptg_gemm_host, steps alternating over 2 streams"}
 
+    # ---- the other workloads, each timed on its own (all ranks), with its
+    # roofline, the oracle on a bounded sample and a parity verdict (rank 0)
+    extras = {}
+    if not args.no_workloads and not args.shape:
+        for name in WORKLOAD_ORDER:
+            if name != w.name:
+                entry = run_workload(args, WORKLOADS[name], rank, world, local, sptg)
+                if entry is not None:
+                    extras[name] = entry
+
     if rank != 0:
         return None
 
-    peaks, peak_src = measured_peaks()
-    bound = bound_for(w)
     clocks = sampler.summary()
-    # The timed region runs the kernel back to back. Once that drives the GPU
-    # into its power cap (or lasts over a second) the sustained figure, taken
-    # under the same cap, is the matching denominator; else the burst one.
-    sustained = ms > 1000.0 or "sw_power_cap" in clocks.get("reasons", [])
-    if bound == "tensor":
-        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-        achieved = w.flops / (ms_per_step * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak,
-                "peak_source": f"{peak_src} bf16 {'sustained' if sustained else 'burst'} "
-                               f"(binary16 runs at the bfloat16 rate)"}
-    else:
-        peak = peaks["hbm_gbs"]
-        achieved = set_bytes / (ms_per_step * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth"}
-    roof["traffic"] = recorded_traffic(kernel_name, w.name)
-    roof["algorithmic_bytes"] = set_bytes
-    roof["kernel"] = kernel_name
+    roof = roofline(w, ms_per_step, ms, clocks, kernel_name, set_bytes)
 
     tl = None
     if args.trace:
         fields = (args.kernel, args.bn, args.stages, 0, 0, 0, args.cta_pair, int(args.no_overlap),
                   args.stream_k)
         tl = timeline(sptg, As[0], Bs[0], Cs[0], fields)
-    cpu = None if args.no_cpu_baseline else cpu_baseline(w, A, B)
+    cpu, parity = None, None
+    if not args.no_cpu_baseline:
+        cpu, rows, res = cpu_baseline(w, A, B)
+        parity = parity_verdict(w, C_check, A, B, rows, res)
     line = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -394,7 +461,7 @@ def run_ours(args, w):
                    "l2": f"{n_sets} rotating input/output sets of {set_bytes / 2**20:.0f} MiB "
                          f"(> L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roof, "cpu_baseline": cpu, "parity": parity, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
         "launch": {"mode": "cuda-graph" if graph is not None else "stream",
                    "host_us_per_step": host_us,
@@ -402,7 +469,134 @@ def run_ours(args, w):
     }
     if tl is not None:
         line["timeline"] = tl
+    if extras:
+        line["workloads"] = extras
     return line
+
+
+# NVIDIA's published dense (no 2:4 sparsity) FP16/BF16 tensor peaks for one
+# Blackwell Ultra GPU, in TFLOP/s: the HGX B300 board lists 36 PFLOPS with
+# sparsity for 8 GPUs, the GB300 NVL72 rack 360 PFLOPS with sparsity for 72;
+# halving for sparsity gives 2.25 and 2.5 PFLOPS dense per GPU. The int8 path
+# runs on the binary16 tensor pipe (sm_103a has no tcgen05 int8 MMA), so the
+# same figures bound it.
+DENSE_SPEC_TFLOPS = {"hgx_b300": 2250.0, "gb300_nvl72": 2500.0}
+
+
+def roofline(w, ms_per_step, timed_ms, clocks, kernel_name, set_bytes):
+    """The roofline record of one timed workload (achieved = algorithmic work
+    per launch / the launch's event-timed average duration)."""
+    peaks, peak_src = measured_peaks()
+    bound = bound_for(w)
+    # The timed region runs the kernel back to back. Once that drives the GPU
+    # into its power cap (or lasts over a second) the sustained figure, taken
+    # under the same cap, is the matching denominator; else the burst one.
+    sustained = timed_ms > 1000.0 or "sw_power_cap" in clocks.get("reasons", [])
+    if bound == "tensor":
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        achieved = w.flops / (ms_per_step * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_source": f"{peak_src} bf16 {'sustained' if sustained else 'burst'} "
+                               f"(binary16 and the int8 path run at the bfloat16 rate)",
+                "frac_dense_spec": achieved / DENSE_SPEC_TFLOPS["hgx_b300"],
+                "frac_dense_spec_nvl72": achieved / DENSE_SPEC_TFLOPS["gb300_nvl72"],
+                "dense_spec_tflops": dict(DENSE_SPEC_TFLOPS)}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = set_bytes / (ms_per_step * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth"}
+    roof["traffic"] = recorded_traffic(kernel_name, w.name)
+    roof["algorithmic_bytes"] = set_bytes
+    roof["kernel"] = kernel_name
+    return roof
+
+
+WORKLOAD_ORACLE_S = 4.0  # oracle seconds per additional workload
+WORKLOAD_MIN_MS = 20.0   # shortest timed region of an additional workload
+
+
+def run_workload(args, w, rank, world, local, sptg):
+    """One additional workload: its own inputs in rotating device sets (> L2),
+    W warm-up steps, then a timed region of back-to-back steps (at least
+    args.steps, more for tiny products so that it lasts WORKLOAD_MIN_MS),
+    CUDA events on the launching stream, max over ranks. Rank 0 adds the
+    roofline, the oracle on a bounded sample of output rows and a parity
+    verdict on the output of the last timed step."""
+    dev = torch.device("cuda", local)
+    A, B = workload_inputs(w)
+    out_dtype = TORCH_DTYPE[w.out_type]
+    set_bytes = algorithmic_bytes(w)
+    n_sets = max(2, -(-3 * L2_BYTES // set_bytes) + 1)
+    As = [A.to(dev) for _ in range(n_sets)]
+    Bs = [B.to(dev) for _ in range(n_sets)]
+    Cs = [torch.empty(w.M, w.N, dtype=out_dtype, device=dev) for _ in range(n_sets)]
+    stream = torch.cuda.current_stream()
+
+    def run(n):
+        for i in range(n):
+            j = i % n_sets
+            sptg.gemm(As[j], Bs[j], C=Cs[j])
+
+    run(args.warmup)
+    torch.cuda.synchronize()
+    if sptg.device_error() != 0:
+        raise RuntimeError(f"{w.name}: a kernel reported a timed-out wait during warm-up")
+    kernel_cfg = sptg.last_config()
+    launches_per_step = int(kernel_cfg.split("launches=")[-1].split()[0])
+    kernel_name = kernel_cfg.split()[0].split("=")[1]
+    # size the timed region: one probe batch of args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(args.steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    probe_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    steps = args.steps
+    if probe_ms < WORKLOAD_MIN_MS:
+        steps = int(min(20000, -(-args.steps * WORKLOAD_MIN_MS // max(probe_ms, 1e-3))))
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    run(steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if rank == 0:
+        sampler.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    if sptg.device_error() != 0:
+        raise RuntimeError(f"{w.name}: a kernel reported a timed-out wait in the timed region")
+    if rank != 0:
+        return None
+    ms_per_step = ms / steps
+    metric, unit = metric_for(w)
+    C = Cs[(steps - 1) % n_sets].cpu()
+    del As, Bs, Cs
+    clocks = sampler.summary()
+    entry = {"metric": metric, "value": job_throughput(w.flops, world, ms_per_step) * 1e3 / 1e12,
+             "unit": unit, "ms_per_step": ms_per_step, "steps": steps, "warmup": args.warmup,
+             "dtype": w.in_type,
+             "config": {"M": w.M, "N": w.N, "K": w.K, "dtype_pair": w.dtype,
+                        "distribution": w.dist, "seed": w.seed, "kernel": kernel_cfg,
+                        "l2": f"{n_sets} rotating input/output sets of "
+                              f"{set_bytes / 2**20:.1f} MiB (> L2)"},
+             "roofline": roofline(w, ms_per_step, ms, clocks, kernel_name, set_bytes),
+             "gpu_launches": launches_per_step * steps, "clocks": clocks}
+    if bound_for(w) == "hbm":
+        entry["gbs"] = entry["roofline"]["achieved"]
+    if w.M * w.N <= 256 * 256:
+        entry["roofline"]["note"] = "latency-bound: the product is two output tiles"
+    if not args.no_cpu_baseline:
+        cpu, rows, res = cpu_baseline(w, A, B, target_s=WORKLOAD_ORACLE_S)
+        entry["cpu_baseline"] = cpu
+        entry["parity"] = parity_verdict(w, C, A, B, rows, res,
+                                         n_random=0 if rows == w.M else 4096)
+    return entry
 
 
 TRACE_EVENTS = ["setup", "first_load", "first_data", "last_load", "last_mma", "epi_done",
@@ -563,6 +757,8 @@ def main(argv=None):
     ap.add_argument("--trace", action="store_true",
                     help="add one traced call's in-kernel timeline to the JSON line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time the chosen workload only (not the other four as well)")
     ap.add_argument("--sweep", default=None, metavar="DTYPE_PAIR",
                     help="time M = N = K over --sizes for one dtype pair (one JSON line per size; "
                          "no end-to-end or CPU legs)")
@@ -579,7 +775,7 @@ def main(argv=None):
         w = WORKLOADS[args.workload]
     if args.sweep:
         from workloads import Workload
-        args.no_e2e = args.no_cpu_baseline = True
+        args.no_e2e = args.no_cpu_baseline = args.no_workloads = True
         for size in (int(x) for x in args.sizes.split(",")):
             sw = Workload(f"{args.sweep}_{size}x{size}x{size}", size, size, size, args.sweep,
                           "int8" if args.sweep.startswith("s8") else "uniform", 1.0, 1)
