@@ -263,7 +263,8 @@ def test_int8_exact_cta_pair(M, N, K):
     assert_int_parity(C, A, B)
 
 
-@pytest.mark.parametrize("bn,cta_pair", [(160, 1), (160, 2), (128, 1), (128, 2)])
+@pytest.mark.parametrize("cta_pair", [1, 2])
+@pytest.mark.parametrize("bn", [160, 128])
 def test_int8_exact_every_width(bn, cta_pair):
     A, B = make_inputs(520, 488, 3136, "s8", "int8", 50 + bn)
     C = run(A, B, I32, bn=bn, cta_pair=cta_pair)
@@ -432,11 +433,13 @@ def test_k_tile_marker_stream_k(T, splits):
         assert (C.to(torch.float64) == expect).all()
 
 
+@pytest.mark.parametrize("bn", [128, 160])
 @pytest.mark.parametrize("cta_pair", [1, 2])
-def test_stream_k_int8_exact(cta_pair):
-    # cuts fall inside the 1024-product chunks; the int32 partials add exactly
+def test_stream_k_int8_exact(cta_pair, bn):
+    # cuts fall inside the 1024-product chunks, and a contributor's piece spans
+    # several chunks; the int32 partials add exactly
     A, B = make_inputs(512, 384, 4160, "s8", "int8", 42)
-    C = run(A, B, I32, cta_pair=cta_pair, stream_k=2, splits=6)
+    C = run(A, B, I32, cta_pair=cta_pair, stream_k=2, splits=6, bn=bn)
     assert _sk_tiles() > 0
     assert_int_parity(C, A, B)
     A = torch.full((130, 4096), -128, dtype=I8)
