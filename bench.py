@@ -310,6 +310,78 @@ def job_throughput(units_per_rank: float, world: int, ms_max: float) -> float:
     return world * units_per_rank / ms_max
 
 
+def _page_numa_node(ptr: int):
+    """NUMA node of the page holding host address ptr (Linux move_pages query), or None."""
+    import ctypes
+    import platform
+    nr = {"aarch64": 239, "x86_64": 279}.get(platform.machine())
+    if nr is None:
+        return None
+    libc = ctypes.CDLL(None, use_errno=True)
+    pages = (ctypes.c_void_p * 1)(ptr)
+    status = (ctypes.c_int * 1)(-1)
+    if libc.syscall(nr, 0, 1, pages, None, status, 0) != 0:
+        return None
+    return int(status[0])
+
+
+def host_link(h_in, h_out, dev, reps: int = 8):
+    """Copy rates of the host link with the end-to-end leg's own pinned buffers
+    (GB/s, CUDA events): host->device alone, device->host alone, and both at
+    once on two streams; plus where the buffers' pages and the GPU sit."""
+    import glob
+    d_in = torch.empty(h_in.numel() * h_in.element_size(), dtype=torch.uint8, device=dev)
+    d_out = torch.empty(h_out.numel() * h_out.element_size(), dtype=torch.uint8, device=dev)
+    hi = h_in.view(-1).view(torch.uint8)
+    ho = h_out.view(-1).view(torch.uint8)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream()
+        e0.record(cur)
+        s1.wait_stream(cur)
+        s2.wait_stream(cur)
+        for _ in range(reps):
+            fn()
+        cur.wait_stream(s1)
+        cur.wait_stream(s2)
+        e1.record(cur)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3
+
+    def up():
+        with torch.cuda.stream(s1):
+            d_in.copy_(hi, non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s2):
+            ho.copy_(d_out, non_blocking=True)
+
+    def both():
+        up()
+        down()
+
+    t_up, t_down, t_both = timed(up), timed(down), timed(both)
+    nin, nout = d_in.numel(), d_out.numel()
+    gpu_node = None
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        addr = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{addr}/numa_node") as f:
+            gpu_node = int(f.read())
+    except Exception:
+        gpu_node = None
+    return {"h2d_gbs": nin * reps / t_up / 1e9, "d2h_gbs": nout * reps / t_down / 1e9,
+            "both_gbs": (nin + nout) * reps / t_both / 1e9,
+            "numa_nodes": len(glob.glob("/sys/devices/system/node/node[0-9]*")),
+            "gpu_numa_node": gpu_node,
+            "pinned_in_page_node": _page_numa_node(h_in.data_ptr()),
+            "pinned_out_page_node": _page_numa_node(h_out.data_ptr())}
+
+
 def run_ours(args, w):
     import software_pipelined_tiled_gb300 as sptg
 
@@ -422,10 +494,19 @@ def run_ours(args, w):
             raise RuntimeError("kernel reported a timed-out wait in the end-to-end leg")
         e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
         isz = A.element_size()
+        h2d = (A.numel() + B.numel()) * isz
+        d2h = hCs[0].numel() * hCs[0].element_size()
         e2e = {"value": world * w.flops / (e_ms * 1e-3) / 1e12, "unit": unit,
-               "h2d_bytes_per_step": (A.numel() + B.numel()) * isz,
-               "d2h_bytes_per_step": hCs[0].numel() * hCs[0].element_size(),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms, "api": "sptg_gemm_host, steps alternating over 2 streams"}
+        link = host_link(hA, hCs[0], dev)
+        # the step's copies alone, at the link's measured rates: each direction
+        # on its own, and both directions sharing the link
+        bound_ms = max(h2d / link["h2d_gbs"], d2h / link["d2h_gbs"],
+                       (h2d + d2h) / link["both_gbs"]) / 1e6
+        link["copy_bound_ms_per_step"] = bound_ms
+        link["e2e_over_copy_bound"] = e_ms / bound_ms
+        e2e["host_link"] = link
 
     # ---- the other workloads, each timed on its own (all ranks), with its
     # roofline, the oracle on a bounded sample and a parity verdict (rank 0)

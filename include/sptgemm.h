@@ -89,7 +89,7 @@ typedef struct {
                    3 skinny swap-AB with the K split across a cluster of
                    CTAs (splits = cluster size, 1, 2 or 4)                   */
   int bn;       /* square: tile columns, one of 128, 160, 192, 224, 256, or
-                   512 for float CTA pairs (int8: 128 or 160)               */
+                   512 for float CTA pairs                                   */
   int stages;   /* shared-memory ring depth (1 = synchronous load/compute)  */
   int splits;   /* square: cap on persistent workers; skinny stream-K: CTAs
                    sharing the work (0 = SM count); skinny cluster: cluster

@@ -570,7 +570,6 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
       if (cfg.bn && bn != cfg.bn) continue;
       // 512 columns: CTA pairs and float types only
       if (bn == 512 && (!pair || int8)) continue;
-      if (int8 && bn != 128 && bn != 160) continue;  // 3 x BN tensor-memory columns
       const int64_t T64 = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
       const int T = static_cast<int>(std::min<int64_t>(T64, INT32_MAX));
       const double rate = (pair ? kRatePair[i] : kRateSingle[i]) * 1e6;  // FLOP per us

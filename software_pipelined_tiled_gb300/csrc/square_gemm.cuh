@@ -16,6 +16,7 @@
 //              stage 32-row blocks in shared memory and store them with the
 //              tensor-copy engine; then hand the accumulator back.
 //   warps 6-9  stream-K reduction (below); idle when no tile is cut.
+//   (INT_EXACT: 12 warps, 2-9 epilogue and 10-11 reduction, see below.)
 //
 // This is the producer/consumer ring of "Hiding Memory Latency in CUDA:
 // Asynchronous Loads and Software Pipelines" (sections 5, 6 and 11): stage =
@@ -69,16 +70,27 @@
 // inputs are int8 values held as binary16 (exact), every product is an integer
 // of magnitude <= 2^14 and every partial sum of at most 1024 products is an
 // integer of magnitude <= 2^24, which fp32 holds exactly.  The K-loop is cut
-// into chunks of 1024; each chunk's fp32 accumulator is converted to int32 and
-// added to an int32 running sum kept in tensor memory.
+// into chunks of 1024 products, each accumulated in one of the two
+// accumulators in turn; eight epilogue warps convert each chunk to int32 and
+// add it to a running sum in their registers (two warps per lane quadrant,
+// half of the columns each), so tensor memory holds only the two accumulators
+// and int8 takes the float tile widths up to 256.
 #pragma once
 
 #include "common.cuh"
 
 namespace sptg {
 
-// Threads of a square-kernel CTA: producer, MMA, 4 epilogue, 4 reduction warps.
+// Threads of a square-kernel CTA: producer, MMA, 4 epilogue, 4 reduction
+// warps; in exact-integer mode producer, MMA, 8 epilogue, 2 reduction warps.
 constexpr int SQUARE_THREADS = 320;
+constexpr int SQUARE_THREADS_INT = 384;
+// first thread and number of threads of the stream-K reduction warps
+template <bool INT_EXACT>
+struct ReductionWarps {
+  static constexpr int FIRST = INT_EXACT ? 320 : 192;
+  static constexpr int COUNT = INT_EXACT ? 64 : 128;
+};
 
 struct SquareParams {
   int M, N, K;
@@ -103,6 +115,33 @@ struct SquareParams {
   int inject_stall;  // test hook: withhold the load of the second K-tile
   unsigned long long* trace;  // optional timeline (see TraceEvent), or null
 };
+
+template <int N>
+struct IntConst {
+  static constexpr int value = N;
+};
+
+// Exact-integer epilogue: reads NBLK blocks of 32 fp32 columns of this
+// thread's accumulator row (exact integers, |v| <= 2^24), converts them to
+// int32 and assigns (FIRST) or adds them to the running sums (as unsigned
+// words: the int32 sum wraps modulo 2^32). 16 columns per tensor-memory load.
+template <bool FIRST, int NBLK>
+__device__ __forceinline__ void int_chunk_sums(uint32_t (&sum)[32 * NBLK], uint32_t t_acc) {
+#pragma unroll
+  for (int j = 0; j < 2 * NBLK; ++j) {
+    uint32_t t[16];
+    tmem_ld_32x32b_x16(t_acc + 16 * j, t);
+    tmem_wait_ld_regs16(t);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint32_t x = static_cast<uint32_t>(__float2int_rn(__uint_as_float(t[e])));
+      if constexpr (FIRST)
+        sum[16 * j + e] = x;
+      else
+        sum[16 * j + e] += x;
+    }
+  }
+}
 
 // One piece of a worker's work: K-tiles [kt0, kt1) of tile `tile`. A partial
 // segment (not all of K) belongs to stream-K tile `sk`, whose contributors are
@@ -164,10 +203,13 @@ __device__ __forceinline__ bool square_segment(const SquareParams& p, int worker
 // minimum (two 4 KB buffers for 4-byte outputs, one 2 KB buffer for 16-bit
 // outputs, which leaves room for one more stage in the 224-wide pair
 // kernels); whatever the ring leaves over goes to more buffers, up to four.
-template <int OBYTES>
+// The exact-integer epilogue has twice the warps (eight) and one 4 KB buffer
+// each at least: the same 32 KB.
+template <int OBYTES, bool INT_EXACT = false>
 struct EpiStaging {
+  static constexpr int WARPS = INT_EXACT ? 8 : 4;
   static constexpr int BUF = 32 * 32 * OBYTES;
-  static constexpr int MIN_NBUF = OBYTES == 4 ? 2 : 1;
+  static constexpr int MIN_NBUF = INT_EXACT ? 1 : OBYTES == 4 ? 2 : 1;
   static constexpr int MAX_NBUF = 4;
 };
 
@@ -179,16 +221,16 @@ struct SquareLayout {
   static constexpr int BK = 64;  // 64 16-bit elements = one 128-byte swizzle row
   static constexpr int A_STAGE = BM * BK * 2;
   static constexpr int B_STAGE = BN_CTA * BK * 2;
-  static constexpr int EPI_WARPS = 4;
-  static constexpr int EPI_BUF = EpiStaging<OBYTES>::BUF;
+  using Epi = EpiStaging<OBYTES, INT_EXACT>;
+  static constexpr int EPI_WARPS = Epi::WARPS;
+  static constexpr int EPI_BUF = Epi::BUF;
   static constexpr int RING_BYTES = STAGES * (A_STAGE + B_STAGE);
   static constexpr bool staging_fits(int nbuf) {
     return RING_BYTES + EPI_WARPS * nbuf * EPI_BUF + 256 + 1024 <= 232448;
   }
-  static constexpr int EPI_NBUF =
-      staging_fits(EpiStaging<OBYTES>::MAX_NBUF) ? EpiStaging<OBYTES>::MAX_NBUF
-      : (staging_fits(2) && EpiStaging<OBYTES>::MIN_NBUF <= 2) ? 2
-                                                               : EpiStaging<OBYTES>::MIN_NBUF;
+  static constexpr int EPI_NBUF = staging_fits(Epi::MAX_NBUF)                   ? Epi::MAX_NBUF
+                                  : (staging_fits(2) && Epi::MIN_NBUF <= 2) ? 2
+                                                                            : Epi::MIN_NBUF;
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_NBUF * EPI_BUF;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
@@ -201,30 +243,28 @@ struct SquareLayout {
   // tiles wider than one MMA (BN = 512: two 256-column MMAs per K-step) keep
   // a single accumulator: 512 columns fill tensor memory
   static constexpr int NACC = BN > 256 ? 1 : 2;
-  static constexpr int TMEM_NEEDED = NACC * BN + (INT_EXACT ? BN : 0);
+  static constexpr int TMEM_NEEDED = NACC * BN;
   static constexpr int TMEM_COLS = TMEM_NEEDED <= 32    ? 32
                                    : TMEM_NEEDED <= 64  ? 64
                                    : TMEM_NEEDED <= 128 ? 128
                                    : TMEM_NEEDED <= 256 ? 256
                                                         : 512;
+  // exact-integer epilogue: 32-column blocks of the first and second warp of a
+  // lane quadrant
+  static constexpr int INT_NB0 = (BN + 63) / 64;
+  static constexpr int INT_NB1 = BN / 32 - INT_NB0;
   // bytes that complete one stage's "full" barrier (both CTAs' copies in PAIR mode)
   static constexpr uint32_t STAGE_TX = (PAIR ? 2 : 1) * (A_STAGE + B_STAGE);
   static_assert(TMEM_NEEDED <= 512, "accumulators exceed tensor memory");
   static_assert(BN % 32 == 0 && BN >= 32 && (BN <= 256 || (BN == 512 && PAIR && !INT_EXACT)),
                 "BN must be a multiple of 32 in [32, 256], or 512 for float CTA pairs");
+  static_assert(!INT_EXACT || (BN >= 64 && BN <= 256),
+                "the exact-integer epilogue keeps at most 128 columns per thread");
   static_assert(!PAIR || BN_CTA % 16 == 0, "each CTA's B rows must be a multiple of 16");
   static_assert(STAGES >= 1, "at least one stage");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
   static_assert(NUM_BARS * 8 + 24 <= 256, "barrier area");
 };
-
-// Deepest ring that fits the 227 KB per-CTA budget next to the epilogue
-// staging, the barriers and the 1 KB alignment slack.
-template <int BN, bool PAIR = false, int OBYTES = 4>
-constexpr int square_max_stages() {
-  return (232448 - 1024 - 4 * EpiStaging<OBYTES>::MIN_NBUF * EpiStaging<OBYTES>::BUF - 256) /
-         (128 * 64 * 2 + (PAIR ? BN / 2 : BN) * 64 * 2);
-}
 
 template <int OUT>
 __device__ __forceinline__ void store_c4(void* C, int64_t idx, uint4 bits) {
@@ -236,8 +276,94 @@ __device__ __forceinline__ void store_c4(void* C, int64_t idx, uint4 bits) {
   }
 }
 
+// Deepest ring that fits the 227 KB per-CTA budget next to the epilogue
+// staging, the barriers and the 1 KB alignment slack.
+template <int BN, bool PAIR = false, int OBYTES = 4, bool INT_EXACT = false>
+constexpr int square_max_stages() {
+  using E = EpiStaging<OBYTES, INT_EXACT>;
+  return (232448 - 1024 - E::WARPS * E::MIN_NBUF * E::BUF - 256) /
+         (128 * 64 * 2 + (PAIR ? BN / 2 : BN) * 64 * 2);
+}
+
+// Adds up a cut tile's partials of this CTA's 128 rows in contributor order
+// (a fixed order: increasing k) and writes them to C, with NT threads (tid in
+// [0, NT)). base points at the tile's first partial slot of this CTA.
+// Flat index f over the 128 rows: group g = f % 8 of four columns, row
+// (f / 8) % 128, 32-column block f / (8 * 128). A warp reads 64-byte runs of
+// the partials and writes whole row segments of C.
+template <int BN, int OUT, bool INT_EXACT, int NT>
+__device__ __forceinline__ void reduce_cut_tile(const SquareParams& p, const uint4* base, int count,
+                                                int row0, int col0, int tid) {
+  constexpr int nr = 128;
+  constexpr int total = nr * (BN / 4);
+  // groups per contributor in flight (fewer with 256 threads, which run beside
+  // the exact-integer epilogue's running sums), contributors in flight
+  constexpr int CH = NT >= 256 ? 4 : 8;
+  constexpr int CB = 2;
+#pragma unroll 1
+  for (int f0 = 0; f0 < total; f0 += NT * CH) {
+    int idx[CH];
+#pragma unroll
+    for (int i2 = 0; i2 < CH; ++i2) {
+      const int f = f0 + tid + NT * i2;
+      const int rest = f >> 3;
+      const int cb = rest / nr;
+      idx[i2] = f < total ? ((cb * 8 + (f & 7)) * 128 + (rest - cb * nr)) : -1;
+    }
+    uint4 acc[CH];
+#pragma unroll 1
+    for (int c0 = 0; c0 < count; c0 += CB) {
+      // CB contributors' groups are loaded together, then added in order
+      uint4 v4[CB][CH];
+#pragma unroll
+      for (int cc = 0; cc < CB; ++cc) {
+        if (c0 + cc < count) {
+          const uint4* pj = base + static_cast<int64_t>(c0 + cc) * (32 * BN);
+#pragma unroll
+          for (int i2 = 0; i2 < CH; ++i2)
+            if (idx[i2] >= 0) v4[cc][i2] = __ldcg(pj + idx[i2]);
+        }
+      }
+#pragma unroll
+      for (int cc = 0; cc < CB; ++cc) {
+        if (c0 + cc >= count) break;
+#pragma unroll
+        for (int i2 = 0; i2 < CH; ++i2) {
+          if (idx[i2] < 0) continue;
+          if (c0 + cc == 0) {
+            acc[i2] = v4[cc][i2];
+          } else if constexpr (INT_EXACT) {
+            acc[i2].x += v4[cc][i2].x;  // int32 sums added as unsigned words (two's complement)
+            acc[i2].y += v4[cc][i2].y;
+            acc[i2].z += v4[cc][i2].z;
+            acc[i2].w += v4[cc][i2].w;
+          } else {
+            acc[i2].x = __float_as_uint(__uint_as_float(acc[i2].x) + __uint_as_float(v4[cc][i2].x));
+            acc[i2].y = __float_as_uint(__uint_as_float(acc[i2].y) + __uint_as_float(v4[cc][i2].y));
+            acc[i2].z = __float_as_uint(__uint_as_float(acc[i2].z) + __uint_as_float(v4[cc][i2].z));
+            acc[i2].w = __float_as_uint(__uint_as_float(acc[i2].w) + __uint_as_float(v4[cc][i2].w));
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i2 = 0; i2 < CH; ++i2) {
+      if (idx[i2] < 0) continue;
+      const int g = idx[i2] >> 7;  // cb * 8 + group
+      const int r = row0 + (idx[i2] & 127);
+      const int col = col0 + 4 * g;
+      if (r < p.M && col < p.N) {
+        if constexpr (INT_EXACT || OUT == OUT_S32)
+          store_c4<OUT_S32>(p.C_out, static_cast<int64_t>(r) * p.ldc + col, acc[i2]);
+        else
+          store_c4<OUT>(p.C_out, static_cast<int64_t>(r) * p.ldc + col, acc[i2]);
+      }
+    }
+  }
+}
+
 template <int BN, int STAGES, bool IN_BF16, int OUT, bool INT_EXACT, bool PAIR = false>
-__global__ void __launch_bounds__(SQUARE_THREADS, 1)
+__global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREADS, 1)
     square_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const SquareParams p) {
@@ -505,12 +631,146 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < ctl.timeout_ns) {
       }
     }
-  } else if (warp < 6) {
+  } else if (INT_EXACT && warp < 10) {
+    // ------------------------------------------------ exact-integer epilogue
+    if constexpr (INT_EXACT) {
+      // Warps 2-9. A chunk's accumulator holds exact integers (|v| <= 2^24);
+      // each thread converts its row's values to int32 and adds them to a
+      // running sum in its registers (int32 sums wrap modulo 2^32), so the
+      // accumulator goes back to the MMA warp as soon as it is read and tensor
+      // memory holds just the two accumulators. Each lane quadrant has two
+      // warps: warps 2-5 keep the first 32 * INT_NB0 columns, warps 6-9 the
+      // rest (at most 128 registers of sum per thread). After a segment's last
+      // chunk the sum goes to C through the tensor-copy store, or, for a piece
+      // of a tile cut along K, to its scratch slot, with a notice to the two
+      // reduction warps (warps 10-11) as in the float epilogue.
+      const int q = warp & 3;  // tensor-memory lane quadrant this warp may access
+      const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+      const int grp = (warp - 2) >> 2;
+      const int etid = static_cast<int>(threadIdx.x) - 64;  // 0..255
+      uint8_t* bufs = epi_buf + (warp - 2) * L::EPI_NBUF * L::EPI_BUF;
+      auto run = [&](auto nblk) {
+        constexpr int NBLK = decltype(nblk)::value;
+        const int cb0 = grp == 0 ? 0 : L::INT_NB0;  // this warp's first 32-column block
+        uint32_t sum[32 * NBLK];
+        uint32_t unit = 0, stores = 0, notes = 0;
+        bool ok = true;
+        Segment seg;
+        for (int i = 0; ok && square_segment(p, worker, workers, i, seg); ++i) {
+          int mt, nt;
+          tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+          const int c_row = mt * L::TILE_M + static_cast<int>(rank) * BM + 32 * q;
+          const int n_chunks = (seg.kt1 - seg.kt0 + kpc - 1) / kpc;
+          // One chunk: wait for its accumulator, convert and add it into the
+          // registers, hand the accumulator back. The first chunk of a segment
+          // assigns the sums (peeled, so they are dead between segments).
+          auto wait_chunk = [&](uint32_t& bb) {
+            bb = unit & 1u;
+            const uint32_t use = unit >> 1;
+            ++unit;
+            // the eight warps leave the wait with one decision
+            const bool got = named_barrier_and(
+                1, 256,
+                __all_sync(0xffffffffu, wait_bounded(tfull_bar(bb), use & 1u, ctl, WAIT_EPI_TMEM_FULL)));
+            if (got) tc_fence_after();
+            return got;
+          };
+          auto release_chunk = [&](uint32_t bb) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (PAIR)
+                mbar_arrive_cluster(map_to_cta(tempty_bar(bb), leader_crank));  // the leader's barrier
+              else
+                mbar_arrive(tempty_bar(bb));
+            }
+          };
+          // (a failed first wait leaves the segment loop at once: no path
+          // reaches a read of the sums without passing the assignment)
+          uint32_t b = 0;
+          if (!wait_chunk(b)) {
+            ok = false;
+            break;
+          }
+          int_chunk_sums<true, NBLK>(sum, tmem_base + lane_base + b * BN + 32 * cb0);
+          release_chunk(b);
+          for (int c = 1; c < n_chunks; ++c) {
+            if (!wait_chunk(b)) {
+              ok = false;
+              break;
+            }
+            int_chunk_sums<false, NBLK>(sum, tmem_base + lane_base + b * BN + 32 * cb0);
+            release_chunk(b);
+          }
+          if (!ok) break;
+          if (seg.partial) {
+            // 16-byte groups in the order [32-column block][group of 4 columns][row]
+            uint4* slot = reinterpret_cast<uint4*>(p.partials) +
+                          ((static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib + seg.j) * (32 * BN) +
+                          32 * q + lane;
+  #pragma unroll
+            for (int j = 0; j < NBLK; ++j)
+  #pragma unroll
+              for (int g = 0; g < 8; ++g)
+                __stcg(slot + ((cb0 + j) * 8 + g) * 128,
+                       make_uint4(sum[32 * j + 4 * g], sum[32 * j + 4 * g + 1], sum[32 * j + 4 * g + 2],
+                                  sum[32 * j + 4 * g + 3]));
+            // visible at GPU scope, then one thread counts the arrival and
+            // posts a notice to the reduction warps saying whether this arrival
+            // completed the tile
+            __threadfence();
+            named_barrier_sync(1, 256);
+            if (etid == 0) {
+              unsigned long long* ctr = p.counters + seg.sk * 2 + rank;
+              const int last = arrive_generation(ctr, p.generation, seg.count, p.error_word);
+              if (last) atomicExch(ctr, 0ull);  // the counter's last use in this call
+              const uint32_t j = notes & 1u, use = notes >> 1;
+              if (wait_bounded(note_empty(j), (use & 1u) ^ 1u, ctl, WAIT_FIXUP_SLOT)) {
+                note_last[j] = last;
+                mbar_arrive(note_full(j));
+              }
+            }
+            ++notes;
+          } else {
+            // one 32-column block at a time through this warp's staging
+            // buffers (128-byte rows, 128-byte swizzle), a tensor-copy store each
+  #pragma unroll
+            for (int j = 0; j < NBLK; ++j) {
+              uint8_t* buf = bufs + (stores % L::EPI_NBUF) * L::EPI_BUF;
+              if (lane == 0) bulk_wait_group_read<L::EPI_NBUF - 1>();
+              __syncwarp();
+              uint8_t* row = buf + lane * 128;
+  #pragma unroll
+              for (int g = 0; g < 8; ++g)
+                *reinterpret_cast<uint4*>(row + ((g ^ (lane & 7)) << 4)) =
+                    make_uint4(sum[32 * j + 4 * g], sum[32 * j + 4 * g + 1], sum[32 * j + 4 * g + 2],
+                               sum[32 * j + 4 * g + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                // a block that starts past the matrix (ragged edge) stores nothing
+                const int col = nt * BN + 32 * (cb0 + j);
+                if (c_row < p.M && col < p.N) tma_store_2d(&tmC, smem_addr(buf), col, c_row);
+                bulk_commit_group();
+              }
+              ++stores;
+            }
+          }
+        }
+        bulk_wait_group_read<0>();  // staging is free once the stores have read it
+        if (warp == 2 && lane == 0) trace_mark(p.trace, TR_EPI_DONE);
+      };
+      if (grp == 0)
+        run(IntConst<L::INT_NB0>{});
+      else
+        run(IntConst<L::INT_NB1>{});
+    }
+  } else if (!INT_EXACT && warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quadrant this warp may access
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     uint8_t* bufs = epi_buf + (warp - 2) * L::EPI_NBUF * L::EPI_BUF;
-    uint32_t stores = 0, unit = 0, notes = 0;
+    uint32_t unit = 0, notes = 0;
     bool ok = true;
     Segment seg;
     for (int i = 0; ok && square_segment(p, worker, workers, i, seg); ++i) {
@@ -535,135 +795,86 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t t_acc = tmem_base + lane_base + b * BN;
-        const bool last_chunk = (c == n_chunks - 1);
-
-        if constexpr (INT_EXACT) {
-          const uint32_t t_sum = tmem_base + lane_base + 2 * BN;
+        // One block = 32 output columns of this warp's 32 rows. The
+        // tensor-memory load of block cb+1 is in flight while block cb is
+        // converted.
+        constexpr int NB = BN / 32;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(t_acc, v);
+        tmem_wait_ld_regs(v);
+        if (seg.partial) {
 #pragma unroll 1
-          for (int cb = 0; cb < BN / 32; ++cb) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(t_acc + 32 * cb, v);
-            tmem_wait_ld_regs(v);
+          for (int cb = 0; cb < NB; ++cb) {
+            const bool more = cb + 1 < NB;
+            uint32_t nxt[32];
+            if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
+            // fp32 partial straight to scratch
 #pragma unroll
-            for (int i2 = 0; i2 < 32; ++i2) v[i2] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i2])));
-            if (c > 0) {
-              uint32_t s[32];
-              tmem_ld_32x32b_x32(t_sum + 32 * cb, s);
-              tmem_wait_ld_regs(s);
+            for (int j = 0; j < 8; ++j)
+              __stcg(slot + (cb * 8 + j) * 128, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            if (more) {
+              tmem_wait_ld_regs(nxt);
 #pragma unroll
-              for (int i2 = 0; i2 < 32; ++i2) v[i2] += s[i2];  // int32 add as unsigned: wraps, never undefined
-            }
-            if (!last_chunk) {
-              tmem_st_32x32b_x32(t_sum + 32 * cb, v);
-            } else if (seg.partial) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                __stcg(slot + (cb * 8 + j) * 128, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-            } else {
-              // 32 int32 columns = one 128-byte row block
-              uint8_t* buf = bufs + (stores % L::EPI_NBUF) * L::EPI_BUF;
-              if (lane == 0) bulk_wait_group_read<L::EPI_NBUF - 1>();
-              __syncwarp();
-              uint8_t* row = buf + lane * 128;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                uint4 w = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = w;
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                // a block that starts past the matrix (ragged edge) stores nothing
-                if (c_row < p.M && nt * BN + 32 * cb < p.N)
-                  tma_store_2d(&tmC, smem_addr(buf), nt * BN + 32 * cb, c_row);
-                bulk_commit_group();
-              }
-              ++stores;
+              for (int i2 = 0; i2 < 32; ++i2) v[i2] = nxt[i2];
             }
           }
-          if (!last_chunk) tmem_wait_st();
         } else {
-          // One block = 32 output columns of this warp's 32 rows. The
-          // tensor-memory load of block cb+1 is in flight while block cb is
-          // converted.
-          constexpr int NB = BN / 32;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(t_acc, v);
-          tmem_wait_ld_regs(v);
-          if (seg.partial) {
+          // Blocks go out in groups of G = the staging buffers of the warp:
+          // each block is converted into its own buffer (128-byte rows with
+          // 128-byte swizzle for 4-byte outputs, 64-byte rows with 64-byte
+          // swizzle for 16-bit ones), one proxy fence covers the group, and
+          // lanes 0..G-1 each issue the tensor-copy store of one block.
+          constexpr int G = L::EPI_NBUF;
 #pragma unroll 1
-            for (int cb = 0; cb < NB; ++cb) {
-              const bool more = cb + 1 < NB;
-              uint32_t nxt[32];
-              if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
-              // fp32 partial straight to scratch
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                __stcg(slot + (cb * 8 + j) * 128, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-              if (more) {
-                tmem_wait_ld_regs(nxt);
-#pragma unroll
-                for (int i2 = 0; i2 < 32; ++i2) v[i2] = nxt[i2];
-              }
-            }
-          } else {
-            // Blocks go out in groups of G = the staging buffers of the warp:
-            // each block is converted into its own buffer (128-byte rows with
-            // 128-byte swizzle for 4-byte outputs, 64-byte rows with 64-byte
-            // swizzle for 16-bit ones), one proxy fence covers the group, and
-            // lanes 0..G-1 each issue the tensor-copy store of one block.
-            constexpr int G = L::EPI_NBUF;
+          for (int cb0 = 0; cb0 < NB; cb0 += G) {
+            // every lane's earlier stores are done reading the buffers
+            bulk_wait_group_read<0>();
+            __syncwarp();
 #pragma unroll 1
-            for (int cb0 = 0; cb0 < NB; cb0 += G) {
-              // every lane's earlier stores are done reading the buffers
-              bulk_wait_group_read<0>();
-              __syncwarp();
-#pragma unroll 1
-              for (int g = 0; g < G; ++g) {
-                const int cb = cb0 + g;
-                if (cb < NB) {
-                  const bool more = cb + 1 < NB;
-                  uint32_t nxt[32];
-                  if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
-                  uint8_t* buf = bufs + g * L::EPI_BUF;
-                  if constexpr (OBYTES == 4) {
-                    if constexpr (OUT == OUT_S32) {
+            for (int g = 0; g < G; ++g) {
+              const int cb = cb0 + g;
+              if (cb < NB) {
+                const bool more = cb + 1 < NB;
+                uint32_t nxt[32];
+                if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
+                uint8_t* buf = bufs + g * L::EPI_BUF;
+                if constexpr (OBYTES == 4) {
+                  if constexpr (OUT == OUT_S32) {
 #pragma unroll
-                      for (int i2 = 0; i2 < 32; ++i2) v[i2] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i2])));
-                    }
-                    uint8_t* row = buf + lane * 128;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                      const uint4 q4 = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                      *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
-                    }
-                  } else {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i2 = 0; i2 < 16; ++i2)
-                      w[i2] = pack2<OUT>(__uint_as_float(v[2 * i2]), __uint_as_float(v[2 * i2 + 1]));
-                    uint8_t* row = buf + lane * 64;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                      const uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                      *reinterpret_cast<uint4*>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = q4;
-                    }
+                    for (int i2 = 0; i2 < 32; ++i2) v[i2] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i2])));
                   }
-                  if (more) {
-                    tmem_wait_ld_regs(nxt);
+                  uint8_t* row = buf + lane * 128;
 #pragma unroll
-                    for (int i2 = 0; i2 < 32; ++i2) v[i2] = nxt[i2];
+                  for (int j = 0; j < 8; ++j) {
+                    const uint4 q4 = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
+                  }
+                } else {
+                  uint32_t w[16];
+#pragma unroll
+                  for (int i2 = 0; i2 < 16; ++i2)
+                    w[i2] = pack2<OUT>(__uint_as_float(v[2 * i2]), __uint_as_float(v[2 * i2 + 1]));
+                  uint8_t* row = buf + lane * 64;
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    *reinterpret_cast<uint4*>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = q4;
                   }
                 }
+                if (more) {
+                  tmem_wait_ld_regs(nxt);
+#pragma unroll
+                  for (int i2 = 0; i2 < 32; ++i2) v[i2] = nxt[i2];
+                }
               }
-              fence_proxy_async_smem();
-              __syncwarp();
-              const int cb = cb0 + lane;
-              // a block that starts past the matrix (ragged edge) stores nothing
-              if (lane < G && cb < NB && c_row < p.M && nt * BN + 32 * cb < p.N) {
-                tma_store_2d(&tmC, smem_addr(bufs + lane * L::EPI_BUF), nt * BN + 32 * cb, c_row);
-                bulk_commit_group();
-              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int cb = cb0 + lane;
+            // a block that starts past the matrix (ragged edge) stores nothing
+            if (lane < G && cb < NB && c_row < p.M && nt * BN + 32 * cb < p.N) {
+              tma_store_2d(&tmC, smem_addr(bufs + lane * L::EPI_BUF), nt * BN + 32 * cb, c_row);
+              bulk_commit_group();
             }
           }
         }
@@ -704,7 +915,8 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
     // segment order): if this CTA's arrival completed the tile, add up this
     // CTA's 128 rows over all partials in contributor order and write them to
     // C; otherwise another contributor does.
-    const int tid = threadIdx.x - 192;  // 0..127
+    constexpr int NT = ReductionWarps<INT_EXACT>::COUNT;
+    const int tid = static_cast<int>(threadIdx.x) - ReductionWarps<INT_EXACT>::FIRST;  // 0..NT-1
     uint32_t notes = 0;
     bool ok = true;
     Segment seg;
@@ -719,7 +931,7 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
         }
         fix_flag[j] = flag;
       }
-      named_barrier_sync(2, 128);
+      named_barrier_sync(2, NT);
       const int flag = fix_flag[j];
       ++notes;
       if (flag < 0) {
@@ -732,74 +944,8 @@ __global__ void __launch_bounds__(SQUARE_THREADS, 1)
       tile_coords(seg.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
       const uint4* base = reinterpret_cast<const uint4*>(p.partials) +
                           (static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib * (32 * BN);
-      // Flat index f over the CTA's 128 rows: group g = f % 8 of four
-      // columns, row (f / 8) % 128, 32-column block f / (8 * 128). A warp
-      // reads 64-byte runs of the partials and writes whole row segments of C.
-      constexpr int nr = 128;
-      const int total = nr * (BN / 4);
-      constexpr int CH = 8;  // groups per contributor in flight
-      constexpr int CB = 2;  // contributors in flight
-      const int row0 = mt * L::TILE_M + static_cast<int>(rank) * BM;
-#pragma unroll 1
-      for (int f0 = 0; f0 < total; f0 += 128 * CH) {
-        int idx[CH];
-#pragma unroll
-        for (int i2 = 0; i2 < CH; ++i2) {
-          const int f = f0 + tid + 128 * i2;
-          const int rest = f >> 3;
-          const int cb = rest / nr;
-          idx[i2] = f < total ? ((cb * 8 + (f & 7)) * 128 + (rest - cb * nr)) : -1;
-        }
-        uint4 acc[CH];
-#pragma unroll 1
-        for (int c0 = 0; c0 < seg.count; c0 += CB) {
-          // CB contributors' groups are loaded together, then added in order
-          uint4 v4[CB][CH];
-#pragma unroll
-          for (int cc = 0; cc < CB; ++cc) {
-            if (c0 + cc < seg.count) {
-              const uint4* pj = base + static_cast<int64_t>(c0 + cc) * (32 * BN);
-#pragma unroll
-              for (int i2 = 0; i2 < CH; ++i2)
-                if (idx[i2] >= 0) v4[cc][i2] = __ldcg(pj + idx[i2]);
-            }
-          }
-#pragma unroll
-          for (int cc = 0; cc < CB; ++cc) {
-            if (c0 + cc >= seg.count) break;
-#pragma unroll
-            for (int i2 = 0; i2 < CH; ++i2) {
-              if (idx[i2] < 0) continue;
-              if (c0 + cc == 0) {
-                acc[i2] = v4[cc][i2];
-              } else if constexpr (INT_EXACT) {
-                acc[i2].x += v4[cc][i2].x;  // int32 sums added as unsigned words (two's complement)
-                acc[i2].y += v4[cc][i2].y;
-                acc[i2].z += v4[cc][i2].z;
-                acc[i2].w += v4[cc][i2].w;
-              } else {
-                acc[i2].x = __float_as_uint(__uint_as_float(acc[i2].x) + __uint_as_float(v4[cc][i2].x));
-                acc[i2].y = __float_as_uint(__uint_as_float(acc[i2].y) + __uint_as_float(v4[cc][i2].y));
-                acc[i2].z = __float_as_uint(__uint_as_float(acc[i2].z) + __uint_as_float(v4[cc][i2].z));
-                acc[i2].w = __float_as_uint(__uint_as_float(acc[i2].w) + __uint_as_float(v4[cc][i2].w));
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int i2 = 0; i2 < CH; ++i2) {
-          if (idx[i2] < 0) continue;
-          const int g = idx[i2] >> 7;  // cb * 8 + group
-          const int r = row0 + (idx[i2] & 127);
-          const int col = nt * BN + 4 * g;
-          if (r < p.M && col < p.N) {
-            if constexpr (INT_EXACT || OUT == OUT_S32)
-              store_c4<OUT_S32>(p.C_out, static_cast<int64_t>(r) * p.ldc + col, acc[i2]);
-            else
-              store_c4<OUT>(p.C_out, static_cast<int64_t>(r) * p.ldc + col, acc[i2]);
-          }
-        }
-      }
+      reduce_cut_tile<BN, OUT, INT_EXACT, NT>(p, base, seg.count,
+                                           mt * L::TILE_M + static_cast<int>(rank) * BM, nt * BN, tid);
       if (tid == 0) trace_mark(p.trace, TR_FIXUP_DONE);
     }
   }

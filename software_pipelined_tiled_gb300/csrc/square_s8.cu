@@ -1,6 +1,7 @@
 // square_s8.cu -- the square kernel in exact-integer mode (int8 operands held
-// as binary16, fp32 chunk accumulators of at most 1024 products, int32 sums),
-// and the int8 -> binary16 widening kernel it runs after.
+// as binary16, fp32 chunk accumulators of at most 1024 products, int32 sums in
+// the epilogue's registers), and the int8 -> binary16 widening kernel it runs
+// after.
 #include <cstring>
 
 #include "convert.cuh"
@@ -8,23 +9,27 @@
 
 namespace sptg {
 
-// Tile widths 128 and 160: two accumulators and the int32 running sum,
-// 3 x BN tensor-memory columns, fit the 512 columns up to BN = 160.
+// Tile widths 128-256 in steps of 32, one CTA or a CTA pair, each at the
+// deepest ring that fits: tensor memory holds the two accumulators of a float
+// tile, and the epilogue keeps the int32 sums in registers.
 bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v) {
-#define SPTG_S8(BNV)                                                                      \
-  if (bn == BNV) {                                                                        \
-    if (!pair && (stages == 0 || stages == square_max_stages<BNV, false, 4>())) {          \
-      *v = make_square<BNV, square_max_stages<BNV, false, 4>(), false, OUT_S32, true, false>(); \
-      return true;                                                                        \
-    }                                                                                     \
-    if (pair && (stages == 0 || stages == square_max_stages<BNV, true, 4>())) {            \
-      *v = make_square<BNV, square_max_stages<BNV, true, 4>(), false, OUT_S32, true, true>();   \
-      return true;                                                                        \
-    }                                                                                     \
-    return false;                                                                         \
+#define SPTG_S8(BNV)                                                                           \
+  if (bn == BNV) {                                                                             \
+    if (!pair && (stages == 0 || stages == square_max_stages<BNV, false, 4, true>())) {         \
+      *v = make_square<BNV, square_max_stages<BNV, false, 4, true>(), false, OUT_S32, true, false>(); \
+      return true;                                                                             \
+    }                                                                                          \
+    if (pair && (stages == 0 || stages == square_max_stages<BNV, true, 4, true>())) {           \
+      *v = make_square<BNV, square_max_stages<BNV, true, 4, true>(), false, OUT_S32, true, true>();   \
+      return true;                                                                             \
+    }                                                                                          \
+    return false;                                                                              \
   }
   SPTG_S8(128)
   SPTG_S8(160)
+  SPTG_S8(192)
+  SPTG_S8(224)
+  SPTG_S8(256)
 #undef SPTG_S8
   return false;
 }

@@ -11,7 +11,7 @@ template <int BN, int ST, bool BF, int OUT, bool IE, bool PAIR>
 KernelVariant make_square() {
   return KernelVariant{reinterpret_cast<const void*>(&square_gemm_kernel<BN, ST, BF, OUT, IE, PAIR>),
                        BN, ST, SquareLayout<BN, ST, IE, PAIR, OutTraits<OUT>::bytes>::SMEM_BYTES,
-                       PAIR, SQUARE_THREADS};
+                       PAIR, IE ? SQUARE_THREADS_INT : SQUARE_THREADS};
 }
 
 // Tile widths BN in {256, 224, 192, 160, 128}, one CTA or a CTA pair per

@@ -264,7 +264,7 @@ def test_int8_exact_cta_pair(M, N, K):
 
 
 @pytest.mark.parametrize("cta_pair", [1, 2])
-@pytest.mark.parametrize("bn", [160, 128])
+@pytest.mark.parametrize("bn", [256, 224, 192, 160, 128])
 def test_int8_exact_every_width(bn, cta_pair):
     A, B = make_inputs(520, 488, 3136, "s8", "int8", 50 + bn)
     C = run(A, B, I32, bn=bn, cta_pair=cta_pair)
@@ -433,7 +433,7 @@ def test_k_tile_marker_stream_k(T, splits):
         assert (C.to(torch.float64) == expect).all()
 
 
-@pytest.mark.parametrize("bn", [128, 160])
+@pytest.mark.parametrize("bn", [128, 160, 224, 256])
 @pytest.mark.parametrize("cta_pair", [1, 2])
 def test_stream_k_int8_exact(cta_pair, bn):
     # cuts fall inside the 1024-product chunks, and a contributor's piece spans

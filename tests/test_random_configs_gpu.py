@@ -41,8 +41,7 @@ def _case(i):
     if kind in ("single", "pair"):
         kw["kernel"] = "square"
         kw["cta_pair"] = {"single": 1, "pair": 2}[kind]
-        widths = ((160, 128) if it == "s8" else (256, 224, 192, 160, 128)
-                  + ((512,) if kind == "pair" else ()))
+        widths = (256, 224, 192, 160, 128) + ((512,) if kind == "pair" and it != "s8" else ())
         kw["bn"] = rng.choice(widths)
         if kw["bn"] != 512:
             kw["stream_k"] = rng.choice([0, 1, 2])
