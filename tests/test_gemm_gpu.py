@@ -614,6 +614,45 @@ def test_graph_replays_of_a_stream_k_call(cta_pair):
                                             stream_k=2, splits=5), C, A, B)
 
 
+@pytest.mark.parametrize("stream_k", [0, 2])
+def test_graph_replays_of_an_int8_call_with_new_inputs(stream_k):
+    # The captured call widens the int8 operands into the stream's scratch and
+    # multiplies them; every replay gets new inputs, which the replay must
+    # widen again (and, when tiles are cut along K, count and reduce anew).
+    M, N, K = 520, 456, 2080
+    dA = torch.empty(M, K, dtype=I8, device="cuda")
+    dB = torch.empty(N, K, dtype=I8, device="cuda")
+    C = torch.empty(M, N, dtype=I32, device="cuda")
+    s = torch.cuda.Stream()
+    kw = {"stream_k": 2, "splits": 7} if stream_k else {}
+
+    def call():
+        sptg.gemm(dA, dB, C=C, stream=s, **kw)
+
+    A, B = make_inputs(M, N, K, "s8", "int8", 90)
+    dA.copy_(A)
+    dB.copy_(B)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        call()  # sizes the stream's scratch before the capture
+    s.synchronize()
+    assert_int_parity(C.cpu(), A, B)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    torch.cuda.synchronize()
+    for r in range(3):
+        A, B = make_inputs(M, N, K, "s8", "int8", 91 + r)
+        dA.copy_(A)
+        dB.copy_(B)
+        C.fill_(0)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sptg.device_error() == 0
+        assert_int_parity(C.cpu(), A, B)
+
+
 def test_graph_replays_of_a_skinny_split_call():
     A, B = make_inputs(48, 2048, 1024, "bf16", "normal", 82)
     dA, dB = A.cuda(), B.cuda()
