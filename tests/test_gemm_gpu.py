@@ -722,6 +722,25 @@ def test_bounded_wait_reports_timeout_and_context_survives(kernel, pair, stream_
     assert_float_parity(C, A, B)
 
 
+@pytest.mark.parametrize("cta_pair,stream_k", [(1, 0), (2, 0), (1, 2), (2, 2)])
+def test_bounded_wait_int8_reports_timeout_and_context_survives(cta_pair, stream_k):
+    # the exact-integer kernel's eight epilogue warps and two reduction warps
+    # leave together when the producer withholds a K-tile
+    M, N, K = 512, 448, 2080
+    A, B = make_inputs(M, N, K, "s8", "int8", 33)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty(M, N, dtype=I32, device="cuda")
+    cfg = sptg.Config(1, 224, 0, 4, 100, 1, cta_pair)
+    cfg.stream_k = stream_k
+    rc = sptg.gemm_raw(M, N, K, "s8_s32", dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
+                       torch.cuda.current_stream().cuda_stream, cfg)
+    assert rc == 0
+    assert sptg.device_error() == -5
+    assert sptg.device_error() == 0
+    C = run(A, B, I32, cta_pair=cta_pair, stream_k=stream_k, splits=4 if stream_k else 0)
+    assert_int_parity(C, A, B)
+
+
 @pytest.mark.parametrize("kernel,cta_pair", [("square", 1), ("square", 2), ("skinny", 0),
                                              ("skinny_cluster", 0)])
 def test_timeline_trace_is_ordered(kernel, cta_pair):
