@@ -544,6 +544,35 @@ def test_leading_dimensions_int8(stream_k):
     assert_int_parity(Cbuf[:, :136].cpu().contiguous(), A, B)
 
 
+@pytest.mark.parametrize("it,ot,M,N,K,kw", [
+    ("f16", F32, 300, 264, 520, {"kernel": "square", "cta_pair": 1}),
+    ("bf16", BF16, 300, 456, 1096, {"kernel": "square", "cta_pair": 2}),
+    ("bf16", F32, 300, 1040, 520, {"kernel": "square", "cta_pair": 2, "bn": 512}),
+    ("f16", F16, 520, 776, 1096, {"kernel": "square", "cta_pair": 2, "stream_k": 2, "splits": 5}),
+    ("s8", I32, 264, 136, 1040, {}),
+    ("s8", I32, 264, 456, 2080, {"cta_pair": 2, "stream_k": 2, "splits": 6}),
+    ("bf16", BF16, 48, 2048, 1024, {"kernel": "skinny"}),
+    ("bf16", F32, 40, 2056, 2048, {"kernel": "skinny_cluster", "splits": 2}),
+])
+def test_rows_outside_c_stay_untouched(it, ot, M, N, K, kw):
+    # C is rows 8 .. 8 + M of a taller buffer filled with a sentinel: a store
+    # past row M (a tile's rows beyond the matrix) or before row 0 would land
+    # in those guard rows
+    A, B = make_inputs(M, N, K, it, "int8" if it == "s8" else "uniform", 62 + M)
+    sentinel = 77
+    Cbuf = torch.full((M + 48, N), sentinel, dtype=ot, device="cuda")
+    C = Cbuf[8:8 + M]
+    sptg.gemm(A.cuda(), B.cuda(), C=C, **kw)
+    torch.cuda.synchronize()
+    assert sptg.device_error() == 0
+    guard = torch.cat([Cbuf[:8], Cbuf[8 + M:]]).cpu().to(torch.float64)
+    assert (guard == sentinel).all()
+    if it == "s8":
+        assert_int_parity(C.cpu(), A, B)
+    else:
+        assert_float_parity(C.cpu(), A, B)
+
+
 def test_leading_dimensions_zero_k():
     Cbuf = torch.full((40, 72), 3.0, dtype=F32, device="cuda")
     A = torch.zeros(40, 0, dtype=F16, device="cuda")
