@@ -107,7 +107,7 @@ struct SquareParams {
   // [sk_tile][rank][contributor][128 x BN] 32-bit, each 128 x BN block as
   // 16-byte groups in the order [32-column block][4-column group][row]
   uint32_t* partials;
-  // [sk_tile * 2 + rank]: generation << 32 | departures << 16 | arrivals
+  // [sk_tile * 2 + rank]: generation << 32 | arrivals (0 between calls)
   unsigned long long* counters;
   unsigned int generation;
   unsigned int* error_word;
