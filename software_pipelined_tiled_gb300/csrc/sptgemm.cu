@@ -1134,9 +1134,9 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
     if (rc) return rc;
     void* A16 = ws.data;
     void* B16 = static_cast<char*>(ws.data) + a_pad;
-    const int64_t na = M * (K / 16), nb = N * (K / 16);
-    // two 256-thread blocks per SM, each thread with eight loads in flight
-    const int blocks = static_cast<int>(std::min<int64_t>((na + nb + 255) / 256, 2 * di.sm_count));
+    const int64_t na = M * (K / 8), nb = N * (K / 8);
+    // four 256-thread blocks per SM, each thread with eight loads in flight
+    const int blocks = static_cast<int>(std::min<int64_t>((na + nb + 255) / 256, 4 * di.sm_count));
     // A plain launch: under programmatic overlap its blocks would sit on the
     // SMs beside the previous GEMM's CTAs, which measured 14 us slower per
     // call on 4096^3. The GEMM that follows still overlaps this kernel's tail.

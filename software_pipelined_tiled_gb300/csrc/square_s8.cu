@@ -38,15 +38,15 @@ cudaError_t launch_s8_to_f16(const void* srcA, int64_t lda, int64_t rows_a, cons
                              int64_t ldb, int64_t rows_b, int64_t K, void* dstA, void* dstB,
                              int blocks, cudaStream_t stream, bool overlap_previous) {
   WidenParams p;
-  p.srcA = static_cast<const int4*>(srcA);
-  p.srcB = static_cast<const int4*>(srcB);
+  p.srcA = static_cast<const int2*>(srcA);
+  p.srcB = static_cast<const int2*>(srcB);
   p.dstA = static_cast<uint4*>(dstA);
   p.dstB = static_cast<uint4*>(dstB);
-  p.lda16 = lda / 16;
-  p.ldb16 = ldb / 16;
-  p.k16 = K / 16;
-  p.na16 = rows_a * p.k16;
-  p.nb16 = rows_b * p.k16;
+  p.lda8 = lda / 8;
+  p.ldb8 = ldb / 8;
+  p.k8 = K / 8;
+  p.na8 = rows_a * p.k8;
+  p.nb8 = rows_b * p.k8;
   cudaLaunchConfig_t lc;
   memset(&lc, 0, sizeof(lc));
   lc.gridDim = dim3(blocks, 1, 1);
