@@ -15,7 +15,8 @@
 //              tensor memory (each warp owns 32 of the 128 lanes), convert,
 //              stage 32-row blocks in shared memory and store them with the
 //              tensor-copy engine; then hand the accumulator back.
-//   warps 6-9  stream-K reduction (below); idle when no tile is cut.
+//   warps 6-9  stream-K reduction (below); when no tile is cut, they store
+//              half of the CTA's last tile instead.
 //   (INT_EXACT: 12 warps, 2-9 epilogue and 10-11 reduction, see below.)
 //
 // This is the producer/consumer ring of "Hiding Memory Latency in CUDA:
@@ -238,7 +239,7 @@ struct SquareLayout {
   static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + 4;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int BYTES_USED = OFF_MISC + 24;
+  static constexpr int BYTES_USED = OFF_MISC + 40;
   static constexpr int SMEM_BYTES = BYTES_USED + 1024;  // slack to align the base to 1024
   // tiles wider than one MMA (BN = 512: two 256-column MMAs per K-step) keep
   // a single accumulator: 512 columns fill tensor memory
@@ -249,6 +250,13 @@ struct SquareLayout {
                                    : TMEM_NEEDED <= 128 ? 128
                                    : TMEM_NEEDED <= 256 ? 256
                                                         : 512;
+  // The CTA's last tile (no tile cut along K, two accumulators): the epilogue
+  // warps store its first LAST_NB0 32-column blocks, the otherwise idle
+  // reduction warps the rest, staged in the ring (free by then), when the
+  // ring holds their buffers.
+  static constexpr int LAST_NB0 = (BN / 32 + 1) / 2;
+  static constexpr bool LAST_SPLIT =
+      !INT_EXACT && NACC == 2 && BN / 32 > 1 && RING_BYTES >= 4 * (BN / 32 - LAST_NB0) * EPI_BUF;
   // exact-integer epilogue: 32-column blocks of the first and second warp of a
   // lane quadrant
   static constexpr int INT_NB0 = (BN + 63) / 64;
@@ -263,7 +271,7 @@ struct SquareLayout {
   static_assert(!PAIR || BN_CTA % 16 == 0, "each CTA's B rows must be a multiple of 16");
   static_assert(STAGES >= 1, "at least one stage");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
-  static_assert(NUM_BARS * 8 + 24 <= 256, "barrier area");
+  static_assert(NUM_BARS * 8 + 40 <= 256, "barrier area");
 };
 
 template <int OUT>
@@ -273,6 +281,38 @@ __device__ __forceinline__ void store_c4(void* C, int64_t idx, uint4 bits) {
   } else {
     store_out4<OUT>(C, idx, make_float4(__uint_as_float(bits.x), __uint_as_float(bits.y),
                                         __uint_as_float(bits.z), __uint_as_float(bits.w)));
+  }
+}
+
+// One block of 32 outputs of this lane's row into a staging buffer of the
+// epilogue: 128-byte rows with 128-byte swizzle for 4-byte outputs, 64-byte
+// rows with 64-byte swizzle for 16-bit ones (round to nearest even), the
+// layout the C tensor map's store reads.
+template <int OUT>
+__device__ __forceinline__ void stage_block(uint8_t* buf, const uint32_t (&v)[32], uint32_t lane) {
+  if constexpr (OutTraits<OUT>::bytes == 4) {
+    uint8_t* row = buf + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint4 q4 = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      if constexpr (OUT == OUT_S32)
+        q4 = make_uint4(static_cast<uint32_t>(__float2int_rn(__uint_as_float(q4.x))),
+                        static_cast<uint32_t>(__float2int_rn(__uint_as_float(q4.y))),
+                        static_cast<uint32_t>(__float2int_rn(__uint_as_float(q4.z))),
+                        static_cast<uint32_t>(__float2int_rn(__uint_as_float(q4.w))));
+      *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
+    }
+  } else {
+    uint32_t w[16];
+#pragma unroll
+    for (int i2 = 0; i2 < 16; ++i2)
+      w[i2] = pack2<OUT>(__uint_as_float(v[2 * i2]), __uint_as_float(v[2 * i2 + 1]));
+    uint8_t* row = buf + lane * 64;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      *reinterpret_cast<uint4*>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = q4;
+    }
   }
 }
 
@@ -400,6 +440,9 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
   volatile int* fix_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
   // per notice: 1 if this CTA's arrival completed the tile (it reduces it)
   volatile int* note_last = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 16);
+  // the CTA's last tile for the reduction warps that help store it: m tile,
+  // n tile, accumulator
+  volatile int* last_tile = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 24);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -786,6 +829,12 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
         slot = reinterpret_cast<uint4*>(p.partials) +
                ((static_cast<int64_t>(seg.sk) * 2 + rank) * p.max_contrib + seg.j) * (32 * BN) +
                32 * q + lane;
+      // the CTA's last tile shares its blocks with the reduction warps
+      bool split = false;
+      if constexpr (L::LAST_SPLIT) {
+        Segment nxt;
+        split = p.sk_tiles == 0 && !square_segment(p, worker, workers, i + 1, nxt);
+      }
       for (int c = 0; c < n_chunks; ++c, ++unit) {
         const uint32_t b = NACC == 2 ? (unit & 1u) : 0u;
         const uint32_t use = NACC == 2 ? (unit >> 1) : unit;
@@ -795,10 +844,16 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
         if (!ok) break;
         tc_fence_after();
         const uint32_t t_acc = tmem_base + lane_base + b * BN;
+        if (split && threadIdx.x == 64) {
+          last_tile[0] = mt;
+          last_tile[1] = nt;
+          last_tile[2] = static_cast<int>(b);
+          mbar_arrive(note_full(0));  // the helpers may start
+        }
         // One block = 32 output columns of this warp's 32 rows. The
         // tensor-memory load of block cb+1 is in flight while block cb is
         // converted.
-        constexpr int NB = BN / 32;
+        const int NB = split ? L::LAST_NB0 : BN / 32;
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_acc, v);
         tmem_wait_ld_regs(v);
@@ -837,30 +892,7 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
                 const bool more = cb + 1 < NB;
                 uint32_t nxt[32];
                 if (more) tmem_ld_32x32b_x32(t_acc + 32 * (cb + 1), nxt);
-                uint8_t* buf = bufs + g * L::EPI_BUF;
-                if constexpr (OBYTES == 4) {
-                  if constexpr (OUT == OUT_S32) {
-#pragma unroll
-                    for (int i2 = 0; i2 < 32; ++i2) v[i2] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i2])));
-                  }
-                  uint8_t* row = buf + lane * 128;
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    const uint4 q4 = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = q4;
-                  }
-                } else {
-                  uint32_t w[16];
-#pragma unroll
-                  for (int i2 = 0; i2 < 16; ++i2)
-                    w[i2] = pack2<OUT>(__uint_as_float(v[2 * i2]), __uint_as_float(v[2 * i2 + 1]));
-                  uint8_t* row = buf + lane * 64;
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    const uint4 q4 = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                    *reinterpret_cast<uint4*>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = q4;
-                  }
-                }
+                stage_block<OUT>(bufs + g * L::EPI_BUF, v, lane);
                 if (more) {
                   tmem_wait_ld_regs(nxt);
 #pragma unroll
@@ -947,6 +979,46 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
       reduce_cut_tile<BN, OUT, INT_EXACT, NT>(p, base, seg.count,
                                            mt * L::TILE_M + static_cast<int>(rank) * BM, nt * BN, tid);
       if (tid == 0) trace_mark(p.trace, TR_FIXUP_DONE);
+    }
+  } else if constexpr (L::LAST_SPLIT) {
+    // ------------------------------------------ last-tile epilogue helpers
+    // With no tile cut along K the reduction warps have nothing to do. The
+    // CTA's last tile has no K-loop after it to hide its epilogue behind, so
+    // they store the second half of its 32-column blocks while the epilogue
+    // warps store the first: warp 6 + j takes the rows of lane quadrant
+    // (6 + j) mod 4. Their staging is the ring, which neither the copies nor
+    // the MMAs use once that tile's accumulator is complete (the notice comes
+    // after the epilogue warps have seen it complete).
+    Segment s0;
+    if (square_segment(p, worker, workers, 0, s0)) {
+      const bool got = __all_sync(0xffffffffu, wait_bounded(note_full(0), 0, ctl, WAIT_FIXUP_NOTE));
+      if (got) {
+        const int mt = last_tile[0], nt = last_tile[1];
+        const uint32_t b = static_cast<uint32_t>(last_tile[2]);
+        tc_fence_after();
+        const int q = warp & 3;
+        const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
+        const int c_row = mt * L::TILE_M + static_cast<int>(rank) * BM + 32 * q;
+        constexpr int NB1 = BN / 32 - L::LAST_NB0;
+        uint8_t* bufs = smem + L::OFF_A + (warp - 6) * NB1 * L::EPI_BUF;
+        fence_proxy_async_smem();  // the ring's async-proxy use is over
+#pragma unroll 1
+        for (int j = 0; j < NB1; ++j) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_acc + 32 * (L::LAST_NB0 + j), v);
+          tmem_wait_ld_regs(v);
+          stage_block<OUT>(bufs + j * L::EPI_BUF, v, lane);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int cb = L::LAST_NB0 + lane;
+        // a block that starts past the matrix (ragged edge) stores nothing
+        if (lane < NB1 && c_row < p.M && nt * BN + 32 * cb < p.N) {
+          tma_store_2d(&tmC, smem_addr(bufs + lane * L::EPI_BUF), nt * BN + 32 * cb, c_row);
+          bulk_commit_group();
+        }
+        bulk_wait_group_read<0>();
+      }
     }
   }
 
