@@ -206,11 +206,14 @@ __device__ __forceinline__ bool square_segment(const SquareParams& p, int worker
 // kernels); whatever the ring leaves over goes to more buffers, up to four.
 // The exact-integer epilogue has twice the warps (eight) and one 4 KB buffer
 // each at least: the same 32 KB.
-template <int OBYTES, bool INT_EXACT = false>
+// Tiles 512 wide (one accumulator, never cut along K) also drain with eight
+// warps, the reduction warps storing half of every tile's blocks: their
+// epilogue is not overlapped with a K-loop.
+template <int OBYTES, bool INT_EXACT = false, bool WIDE = false>
 struct EpiStaging {
-  static constexpr int WARPS = INT_EXACT ? 8 : 4;
+  static constexpr int WARPS = (INT_EXACT || WIDE) ? 8 : 4;
   static constexpr int BUF = 32 * 32 * OBYTES;
-  static constexpr int MIN_NBUF = INT_EXACT ? 1 : OBYTES == 4 ? 2 : 1;
+  static constexpr int MIN_NBUF = (INT_EXACT || WIDE) ? 1 : OBYTES == 4 ? 2 : 1;
   static constexpr int MAX_NBUF = 4;
 };
 
@@ -222,7 +225,7 @@ struct SquareLayout {
   static constexpr int BK = 64;  // 64 16-bit elements = one 128-byte swizzle row
   static constexpr int A_STAGE = BM * BK * 2;
   static constexpr int B_STAGE = BN_CTA * BK * 2;
-  using Epi = EpiStaging<OBYTES, INT_EXACT>;
+  using Epi = EpiStaging<OBYTES, INT_EXACT, (BN > 256)>;
   static constexpr int EPI_WARPS = Epi::WARPS;
   static constexpr int EPI_BUF = Epi::BUF;
   static constexpr int RING_BYTES = STAGES * (A_STAGE + B_STAGE);
@@ -320,7 +323,7 @@ __device__ __forceinline__ void stage_block(uint8_t* buf, const uint32_t (&v)[32
 // staging, the barriers and the 1 KB alignment slack.
 template <int BN, bool PAIR = false, int OBYTES = 4, bool INT_EXACT = false>
 constexpr int square_max_stages() {
-  using E = EpiStaging<OBYTES, INT_EXACT>;
+  using E = EpiStaging<OBYTES, INT_EXACT, (BN > 256)>;
   return (232448 - 1024 - E::WARPS * E::MIN_NBUF * E::BUF - 256) /
          (128 * 64 * 2 + (PAIR ? BN / 2 : BN) * 64 * 2);
 }
@@ -457,7 +460,11 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), (PAIR ? 2 : 1) * L::EPI_WARPS);
+      // (a 512-wide tile cut along K, a test setting, drains with four warps:
+      // the other four reduce)
+      mbar_init(tempty_bar(b), (PAIR ? 2 : 1) *
+                                   ((!INT_EXACT && L::EPI_WARPS == 8 && p.sk_tiles > 0) ? 4
+                                                                                         : L::EPI_WARPS));
     }
     mbar_init(drain_bar, 1);
     for (int j = 0; j < 2; ++j) {
@@ -808,11 +815,16 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
       else
         run(IntConst<L::INT_NB1>{});
     }
-  } else if (!INT_EXACT && warp < 6) {
+  } else if (!INT_EXACT &&
+             (warp < 6 || (L::EPI_WARPS == 8 && warp < 10 && p.sk_tiles == 0))) {
     // ------------------------------------------------------------ epilogue
+    // (eight warps for 512-wide tiles when none is cut along K: warps 2-5
+    // store the first half of a tile's 32-column blocks, warps 6-9 the second)
+    const bool wide8 = L::EPI_WARPS == 8 && p.sk_tiles == 0;
     const int q = warp & 3;  // tensor-memory lane quadrant this warp may access
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     uint8_t* bufs = epi_buf + (warp - 2) * L::EPI_NBUF * L::EPI_BUF;
+    const int cb_first = wide8 ? ((warp - 2) >> 2) * (BN / 64) : 0;
     uint32_t unit = 0, notes = 0;
     bool ok = true;
     Segment seg;
@@ -843,7 +855,7 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
         ok = __all_sync(0xffffffffu, wait_bounded(tfull_bar(b), use & 1u, ctl, WAIT_EPI_TMEM_FULL));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t t_acc = tmem_base + lane_base + b * BN;
+        const uint32_t t_acc = tmem_base + lane_base + b * BN + 32 * cb_first;
         if (split && threadIdx.x == 64) {
           last_tile[0] = mt;
           last_tile[1] = nt;
@@ -853,7 +865,7 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
         // One block = 32 output columns of this warp's 32 rows. The
         // tensor-memory load of block cb+1 is in flight while block cb is
         // converted.
-        const int NB = split ? L::LAST_NB0 : BN / 32;
+        const int NB = split ? L::LAST_NB0 : (wide8 ? BN / 64 : BN / 32);
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_acc, v);
         tmem_wait_ld_regs(v);
@@ -866,7 +878,8 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
             // fp32 partial straight to scratch
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              __stcg(slot + (cb * 8 + j) * 128, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+              __stcg(slot + ((cb_first + cb) * 8 + j) * 128,
+                     make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
             if (more) {
               tmem_wait_ld_regs(nxt);
 #pragma unroll
@@ -903,9 +916,10 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
             fence_proxy_async_smem();
             __syncwarp();
             const int cb = cb0 + lane;
+            const int col = nt * BN + 32 * (cb_first + cb);
             // a block that starts past the matrix (ragged edge) stores nothing
-            if (lane < G && cb < NB && c_row < p.M && nt * BN + 32 * cb < p.N) {
-              tma_store_2d(&tmC, smem_addr(bufs + lane * L::EPI_BUF), nt * BN + 32 * cb, c_row);
+            if (lane < G && cb < NB && c_row < p.M && col < p.N) {
+              tma_store_2d(&tmC, smem_addr(bufs + lane * L::EPI_BUF), col, c_row);
               bulk_commit_group();
             }
           }
