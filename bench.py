@@ -571,15 +571,23 @@ def roofline(w, ms_per_step, timed_ms, clocks, kernel_name, set_bytes):
     per launch / the launch's event-timed average duration)."""
     peaks, peak_src = measured_peaks()
     bound = bound_for(w)
-    # The timed region runs the kernel back to back. Once that drives the GPU
-    # into its power cap (or lasts over a second) the sustained figure, taken
-    # under the same cap, is the matching denominator; else the burst one.
-    sustained = timed_ms > 1000.0 or "sw_power_cap" in clocks.get("reasons", [])
+    # The timed region runs the kernel back to back. Once that lasts over a
+    # second, or the power cap pulled the SM clock down (median under load
+    # below 90 % of its maximum), the sustained figure, taken under the same
+    # cap at lowered clocks, is the matching denominator; else the burst one.
+    # A cap that is flagged while the clock stays at its maximum does not
+    # slow the kernel, so the burst figure stays.
+    sm, sm_max = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    clock_dropped = bool(sm and sm_max and sm < 0.9 * sm_max)
+    sustained = timed_ms > 1000.0 or ("sw_power_cap" in clocks.get("reasons", [])
+                                      and clock_dropped)
     if bound == "tensor":
         peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
         achieved = w.flops / (ms_per_step * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
+                "frac_burst": achieved / peaks["bf16_tflops"],
+                "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
                 "peak_source": f"{peak_src} bf16 {'sustained' if sustained else 'burst'} "
                                f"(binary16 and the int8 path run at the bfloat16 rate)",
                 "frac_dense_spec": achieved / DENSE_SPEC_TFLOPS["hgx_b300"],
@@ -751,6 +759,124 @@ def timeline(sptg, A, B, C, cfg_fields):
     return out
 
 
+VERSUS_SHAPES = ("4096,4096,4096,f16_f16;2048,2048,2048,f16_f16;8192,8192,4096,f16_f16;"
+                 "6144,6144,6144,f16_f16;8192,8192,8192,bf16_bf16;8192,8192,16384,bf16_bf16;"
+                 "8192,8192,16384,bf16_f32;16384,16384,4096,bf16_bf16;4096,4096,4096,s8_s32;"
+                 "64,8192,8192,bf16_bf16;128,8192,8192,bf16_bf16;64,16384,4096,bf16_bf16")
+
+
+def torch_product(pair: str):
+    """The PyTorch call that computes the same product, and its name.
+
+    Same-type outputs use torch.matmul; a 16-bit product with a binary32
+    output uses torch.mm's out_dtype where this PyTorch has it; int8 uses
+    torch._int_mm (int32 output).  None where PyTorch has no such call.
+    """
+    in_t, out_t = pair.split("_")
+    if in_t == "s8":
+        return (lambda A, Bcm, C: torch._int_mm(A, Bcm.t(), out=C)), "torch._int_mm"
+    if in_t == out_t:
+        return (lambda A, Bcm, C: torch.matmul(A, Bcm.t(), out=C)), "torch.matmul"
+    return (lambda A, Bcm, C: torch.mm(A, Bcm.t(), out_dtype=torch.float32, out=C)), \
+        "torch.mm(out_dtype=float32)"
+
+
+def run_versus_torch(args):
+    """This library against PyTorch's own GEMM on the same inputs and outputs.
+
+    Per shape: inputs drawn as the workloads draw them (uniform, seed 3; int8
+    over its whole range), rotated over device sets whose total is above L2.
+    Each side runs `iters` back-to-back calls between CUDA events, five
+    times, medians kept; the order is ours, PyTorch, ours, PyTorch and the
+    better median of each side is reported.  One JSON line per shape.
+    """
+    import statistics
+    import software_pipelined_tiled_gb300 as sptg
+    from workloads import DTYPE_PAIRS, make_inputs
+
+    sptg.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, iters, n_sets):
+        meds = []
+        for _ in range(5):
+            for i in range(3):
+                fn(i % n_sets)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for i in range(iters):
+                fn(i % n_sets)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            meds.append(e0.elapsed_time(e1) * 1e3 / iters)
+        return statistics.median(meds)
+
+    sampler = ClockSampler(0)
+    sampler.start()
+    lines = []
+    for spec in args.shapes.split(";"):
+        m, n, k, pair = spec.split(",")
+        M, N, K = int(m), int(n), int(k)
+        in_t, out_t = DTYPE_PAIRS[pair]
+        A, B = make_inputs(M, N, K, in_t, "int8" if in_t == "s8" else "uniform", 3)
+        el_in, el_out = A.element_size(), torch.empty((), dtype=TORCH_DTYPE[out_t]).element_size()
+        set_bytes = (M * K + N * K) * el_in + M * N * el_out
+        n_sets = max(2, -(-3 * L2_BYTES // set_bytes) + 1)
+        As = [A.to(dev) for _ in range(n_sets)]
+        Bs = [B.to(dev) for _ in range(n_sets)]
+        Cs = [torch.empty(M, N, dtype=TORCH_DTYPE[out_t], device=dev) for _ in range(n_sets)]
+        est_s = max(2.0 * M * N * K / 1.5e15, set_bytes / 5e12)
+        iters = int(min(2000, max(10, 0.03 / est_s)))
+        theirs_fn, theirs_name = torch_product(pair)
+
+        def ours(j):
+            sptg.gemm(As[j], Bs[j], C=Cs[j])
+
+        def theirs(j):
+            theirs_fn(As[j], Bs[j], Cs[j])
+
+        try:
+            theirs(0)
+            torch.cuda.synchronize()
+        except (RuntimeError, TypeError) as e:
+            theirs_fn = None
+            theirs_note = f"{theirs_name} unavailable: {str(e).splitlines()[0][:120]}"
+        t_ours = [timed(ours, iters, n_sets)]
+        t_theirs = []
+        if theirs_fn is not None:
+            t_theirs.append(timed(theirs, iters, n_sets))
+        t_ours.append(timed(ours, iters, n_sets))
+        if theirs_fn is not None:
+            t_theirs.append(timed(theirs, iters, n_sets))
+        if sptg.device_error() != 0:
+            raise RuntimeError("kernel reported a timed-out wait")
+        us_ours = min(t_ours)
+        us_theirs = min(t_theirs) if t_theirs else None
+        flops = 2.0 * M * N * K
+        line = {"shape": [M, N, K], "dtype": pair, "iters": iters, "sets": n_sets,
+                "ours_us": round(us_ours, 3), "ours_tflops": round(flops / us_ours / 1e6, 1),
+                "ours_config": sptg.last_config(),
+                "torch_call": theirs_name, "torch_us": None, "torch_tflops": None,
+                "torch_us_over_ours": None}
+        if us_theirs is not None:
+            line.update(torch_us=round(us_theirs, 3),
+                        torch_tflops=round(flops / us_theirs / 1e6, 1),
+                        torch_us_over_ours=round(us_theirs / us_ours, 3))
+        else:
+            line["torch_note"] = theirs_note
+        lines.append(line)
+        del As, Bs, Cs
+        torch.cuda.empty_cache()
+    sampler.stop()
+    clocks = sampler.summary()
+    for line in lines:
+        line["clocks"] = clocks
+        line["torch_version"] = torch.__version__
+    return lines
+
+
 def run_stream(args):
     """The streaming ring on its own (out = alpha * in, binary32): HBM roofline probe."""
     import software_pipelined_tiled_gb300 as sptg
@@ -853,8 +979,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--stages", type=int, default=0, help="force the ring depth (ablation)")
     ap.add_argument("--bn", type=int, default=0, help="force the square tile width")
-    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
-                    help="0 choose, 1 square, 2 skinny stream-K, 3 skinny cluster split")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3, 4, 5],
+                    help="0 choose, 1 square, 2 skinny stream-K, 3 skinny cluster split, "
+                         "4 skinny column strips (M <= 64), 5 skinny CTA pairs (M <= 64)")
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="square kernel: 0 choose, 1 one CTA per tile, 2 CTA pair (2-SM MMA)")
     ap.add_argument("--stream-k", type=int, default=0, choices=[0, 1, 2],
@@ -875,6 +1002,10 @@ def main(argv=None):
                     help="time M = N = K over --sizes for one dtype pair (one JSON line per size; "
                          "no end-to-end or CPU legs)")
     ap.add_argument("--sizes", default="512,1024,2048,4096,8192")
+    ap.add_argument("--versus-torch", action="store_true",
+                    help="time this library beside PyTorch's own GEMM over --shapes "
+                         "(one JSON line per shape)")
+    ap.add_argument("--shapes", default=VERSUS_SHAPES, metavar="M,N,K,PAIR;...")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -896,6 +1027,10 @@ def main(argv=None):
             line = run_ours(args, sw)
             if line is not None:
                 print(json.dumps(line), flush=True)
+        return
+    if args.versus_torch:
+        for line in run_versus_torch(args):
+            print(json.dumps(line), flush=True)
         return
     if args.stream:
         line = run_stream(args)

@@ -31,7 +31,8 @@ DTYPES = {"f16_f32": 0, "f16_f16": 1, "s8_s32": 2, "bf16_bf16": 3, "bf16_f32": 4
 STATUS = {0: "SPTG_OK", -1: "SPTG_ERR_ARG", -2: "SPTG_ERR_ALIGN", -3: "SPTG_ERR_UNSUPPORTED",
           -4: "SPTG_ERR_LAUNCH", -5: "SPTG_ERR_TIMEOUT", -6: "SPTG_ERR_NOMEM",
           -7: "SPTG_ERR_CONFIG"}
-KERNELS = {"auto": 0, "square": 1, "skinny": 2, "skinny_cluster": 3}
+KERNELS = {"auto": 0, "square": 1, "skinny": 2, "skinny_cluster": 3, "skinny_rows": 4,
+           "skinny_pair": 5}
 
 # the C functions every build must export (checked by the tests)
 EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_gemm_strided", "sptg_gemm_host",

@@ -1,6 +1,10 @@
-// skinny.cu -- instantiations of the skinny (swap-AB, stream-K) kernel.
+// skinny.cu -- instantiations of the skinny kernels (swap-AB stream-K,
+// swap-AB cluster split, swap-AB CTA pairs, and one CTA per strip of output
+// columns).
 #include "skinny_cluster_gemm.cuh"
 #include "skinny_gemm.cuh"
+#include "skinny_pair_gemm.cuh"
+#include "skinny_rows_gemm.cuh"
 #include "variants.h"
 
 namespace sptg {
@@ -89,6 +93,46 @@ bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, int M, Kerne
     }
   }
   *v = c;
+  return true;
+}
+
+// One CTA per strip of output columns (M <= 64): two 64-wide K-chunks per
+// stage, the ring depth and strip width set per call.
+constexpr int kSkinnyRowsKsub = 2;
+template <bool BF, int OUT>
+KernelVariant make_skinny_rows() {
+  KernelVariant v{reinterpret_cast<const void*>(&skinny_rows_gemm_kernel<BF, OUT, kSkinnyRowsKsub>),
+                  64, 0, 0, false};
+  v.ksub = kSkinnyRowsKsub;
+  return v;
+}
+
+bool skinny_rows_variant(bool in_bf16, int out_kind, KernelVariant* v) {
+  if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny_rows<true, OUT_BF16>();
+  else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny_rows<false, OUT_F16>();
+  else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny_rows<true, OUT_F32>();
+  else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny_rows<false, OUT_F32>();
+  else return false;
+  return true;
+}
+
+// CTA pairs with the 2-SM MMA (M <= 64): two 64-wide K-chunks per stage, the
+// ring depth and each CTA's column count set per call.
+constexpr int kSkinnyPairKsub = 2;
+template <bool BF, int OUT>
+KernelVariant make_skinny_pair() {
+  KernelVariant v{reinterpret_cast<const void*>(&skinny_pair_gemm_kernel<BF, OUT, kSkinnyPairKsub>),
+                  64, skinny_pair_max_stages<kSkinnyPairKsub>(), 0, true};
+  v.ksub = kSkinnyPairKsub;
+  return v;
+}
+
+bool skinny_pair_variant(bool in_bf16, int out_kind, KernelVariant* v) {
+  if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny_pair<true, OUT_BF16>();
+  else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny_pair<false, OUT_F16>();
+  else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny_pair<true, OUT_F32>();
+  else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny_pair<false, OUT_F32>();
+  else return false;
   return true;
 }
 

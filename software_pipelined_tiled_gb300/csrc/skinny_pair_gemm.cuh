@@ -1,0 +1,321 @@
+// skinny_pair_gemm.cuh -- the memory-bound skinny product (M <= 64) on CTA
+// pairs with the 2-SM tensor-core instruction, K never split.
+//
+// Swap-AB as in skinny_gemm.cuh: D^T[n, m] = sum_k Bcm[n, k] * A[m, k]. A pair
+// of CTAs (a cluster of two) owns 2 * n_cta consecutive output columns; CTA
+// rank r loads the n_cta rows of Bcm of its own columns (into a 64-row operand
+// tile; rows past n_cta are never stored) and the 32 rows 32r ... 32r + 31 of A.
+// The leader's tcgen05.mma.cta_group::2 (M = 128 over the pair's columns, N =
+// 64 over the rows of A) reads both CTAs' shared memory, so each SM copies
+// only half of A per K-chunk, and each CTA's tensor memory receives the sums
+// of its own columns over the whole of K. Nothing is exchanged between SMs
+// after the K-loop: each CTA converts its 64 x n_cta block of C, stages it in
+// shared memory (the ring, idle by then) and writes it with one tensor copy.
+//
+// Per SM a K-chunk moves (n_cta + 32) x 128 bytes, against (n_cta + 64) x 128
+// for one CTA per strip (skinny_rows_gemm.cuh) and (128 + 64) x 128 for half a
+// K-range of a 128-column tile (skinny_cluster_gemm.cuh, which then exchanges
+// partial sums). The host picks n_cta so that the pairs cover the SMs about
+// once (8192 columns over 152 SMs: 56 per CTA, 74 pairs).
+//
+// Copies of both CTAs complete on the leader's "full" barrier; the leader's
+// commits arrive on both CTAs' "empty" and "tmem_full" barriers.
+//
+// Tensor-memory layout of the accumulator (cta_group::2, M = 128, N = 64):
+// each CTA holds its 64 rows of D with the N side split in halves: row i's
+// sums for the rows 0-31 of A lie in lane i, those for the rows 32-63 in lane
+// 64 + i, each half in columns 0-31.
+#pragma once
+
+#include "common.cuh"
+
+namespace sptg {
+
+struct SkinnyPairParams {
+  int M, N, K;
+  int n_cta;        // output columns per CTA: a multiple of 8, 8 ... 64
+  int num_k_tiles;  // ring stages' worth of K: ceil(K / (64 * KSUB))
+  int stages;       // ring depth, 1 ... SKINNY_PAIR_MAX_STAGES
+  int load3d;       // 1: one 3-D copy per operand and stage; 0: 2-D per chunk
+  unsigned int* error_word;
+  uint64_t timeout_ns;
+  int inject_stall;
+  unsigned long long* trace;
+};
+
+constexpr int SKINNY_PAIR_MAX_STAGES = 16;
+// barriers (2 per stage + 2) and misc words after the ring
+constexpr int SKINNY_PAIR_BAR_BYTES = (2 * SKINNY_PAIR_MAX_STAGES + 2) * 8 + 16;
+constexpr int SKINNY_PAIR_RING_BUDGET = 232448 - 1024 - SKINNY_PAIR_BAR_BYTES;
+
+constexpr int SKINNY_PAIR_SUB_B = 64 * 128;  // one 64-wide K-chunk of a CTA's Bcm rows
+constexpr int SKINNY_PAIR_SUB_A = 32 * 128;  // one K-chunk of a CTA's 32 rows of A
+
+template <int KSUB>
+struct SkinnyPairLayout {
+  static constexpr int SUB_B = SKINNY_PAIR_SUB_B;  // room for one 64-row operand tile per chunk
+  static constexpr int SUB_A = SKINNY_PAIR_SUB_A;
+  static constexpr int STAGE = KSUB * (SUB_B + SUB_A);
+  static_assert(STAGE % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+  // C staging (in stage 0 once the K-loop is over): 64 rows of up to 64 fp32
+  static_assert(64 * 64 * 4 <= STAGE, "the output block must fit one stage");
+};
+
+template <int KSUB>
+constexpr int skinny_pair_max_stages() {
+  return SKINNY_PAIR_RING_BUDGET / SkinnyPairLayout<KSUB>::STAGE < SKINNY_PAIR_MAX_STAGES
+             ? SKINNY_PAIR_RING_BUDGET / SkinnyPairLayout<KSUB>::STAGE
+             : SKINNY_PAIR_MAX_STAGES;
+}
+
+template <bool IN_BF16, int OUT, int KSUB>
+__global__ void __launch_bounds__(192, 1)
+    skinny_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmC,
+                            const SkinnyPairParams p) {
+  using L = SkinnyPairLayout<KSUB>;
+  constexpr int BK = 64;
+  constexpr int OBYTES = OutTraits<OUT>::bytes;
+  constexpr uint32_t TMEM_COLS = 64;
+  // kind::f16, fp32 accumulation, M = 128 (the pair), N = 64
+  constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, 128, 64);
+  static_assert(OUT != OUT_S32, "float outputs only");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const int S = p.stages;
+  const uint32_t bar0 = sbase + static_cast<uint32_t>(S * L::STAGE);
+  auto stage_b = [&](int s) { return sbase + static_cast<uint32_t>(s * L::STAGE); };
+  auto stage_a = [&](int s) { return stage_b(s) + KSUB * L::SUB_B; };
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (SKINNY_PAIR_MAX_STAGES + s); };
+  const uint32_t tfull_bar = bar0 + 8u * (2 * SKINNY_PAIR_MAX_STAGES);
+  const uint32_t drain_bar = tfull_bar + 8u;
+  uint8_t* misc = smem + S * L::STAGE + (2 * SKINNY_PAIR_MAX_STAGES + 2) * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  volatile int* failed = reinterpret_cast<volatile int*>(misc + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 = leader, which issues the MMAs
+  const int n_cta = p.n_cta;
+  // this CTA's first output column
+  const int n_base = static_cast<int>(blockIdx.x >> 1) * 2 * n_cta + static_cast<int>(rank) * n_cta;
+  const int KT = p.num_k_tiles;
+  // bytes that complete one stage's "full" barrier: both CTAs' copies
+  const uint32_t stage_tx = 2u * KSUB * static_cast<uint32_t>((n_cta + 32) * 128);
+  // A K-chunk of this CTA's Bcm rows fills n_cta rows; the chunks of a stage
+  // lie back to back (as one 3-D copy writes them), so the MMA's 64-row
+  // operand tile of chunk j starts at j * n_cta rows and its rows past n_cta
+  // (the next chunk's, or unused ones) only reach sums that are never stored.
+  const int sub_b = n_cta * 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *failed = 0;
+    fence_mbar_init();
+    prefetch_tensor_map(&tmB);
+    prefetch_tensor_map(&tmA);
+    prefetch_tensor_map(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc_g<true>(smem_addr(tmem_slot), TMEM_COLS);
+    tmem_relinquish_g<true>();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers exist before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // Warm L2 with this CTA's first stages of Bcm while the previous kernel
+  // drains (safe: L2 is where writes become coherent; the loads proper wait
+  // for the dependency).
+  uint64_t pol_stream = 0, pol_keep = 0;
+  if (warp == 0) {
+    pol_stream = policy_evict_first();  // Bcm is read once
+    pol_keep = policy_evict_last();     // A is read by every pair
+    for (int kt = 0; lane == 0 && kt < min(KT, S); ++kt) {
+      if (p.load3d) {
+        tma_prefetch_l2_3d(&tmB, 0, n_base, kt * KSUB);
+      } else {
+#pragma unroll
+        for (int j = 0; j < KSUB; ++j) tma_prefetch_l2_2d(&tmB, (kt * KSUB + j) * BK, n_base);
+      }
+    }
+  }
+  grid_dependency_wait();
+  if (threadIdx.x == 0) trace_mark(p.trace, TR_SETUP);
+
+  const WaitCtl ctl{p.timeout_ns, p.error_word, abort_flag};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const bool leader = elect_one_sync();
+    int issued_round[SKINNY_PAIR_MAX_STAGES];
+    for (int s = 0; s < SKINNY_PAIR_MAX_STAGES; ++s) issued_round[s] = -1;
+    bool ok = true;
+    int s = 0;
+    uint32_t round = 0;
+    for (int kt = 0; kt < KT; ++kt) {
+      // in the first round every stage is free: no wait
+      if (round > 0 && !__all_sync(0xffffffffu, wait_bounded(empty_bar(s), (round & 1u) ^ 1u, ctl,
+                                                              WAIT_PRODUCER_EMPTY))) {
+        ok = false;
+        break;
+      }
+      if (!(p.inject_stall && kt == 1 && rank == 0)) {  // test hook: this stage never fills
+        issued_round[s] = static_cast<int>(round);
+        if (leader) {
+          // both CTAs' copies complete on the leader's barrier; the leader
+          // announces the bytes of both
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), stage_tx);
+          const uint32_t leader_full = map_to_cta(full_bar(s), 0u);
+          if (p.load3d) {
+            tma_load_3d_pair(stage_b(s), &tmB, leader_full, 0, n_base, kt * KSUB, pol_stream);
+            tma_load_3d_pair(stage_a(s), &tmA, leader_full, 0, 32 * static_cast<int>(rank),
+                             kt * KSUB, pol_keep);
+          } else {
+#pragma unroll
+            for (int j = 0; j < KSUB; ++j) {
+              tma_load_2d_pair(stage_b(s) + j * sub_b, &tmB, leader_full, (kt * KSUB + j) * BK,
+                               n_base, pol_stream);
+              tma_load_2d_pair(stage_a(s) + j * L::SUB_A, &tmA, leader_full, (kt * KSUB + j) * BK,
+                               32 * static_cast<int>(rank), pol_keep);
+            }
+          }
+          if (kt == 0) trace_mark(p.trace, TR_FIRST_LOAD);
+          trace_ktile(p.trace, 0, static_cast<uint32_t>(kt));
+        }
+      }
+      if (++s == S) {
+        s = 0;
+        ++round;
+      }
+    }
+    if (leader) trace_mark(p.trace, TR_LAST_LOAD);
+    grid_launch_dependents();
+    if (!ok) {
+      if (leader) *failed = 1;
+      if (rank == 0) {
+        // let every copy already issued land before the CTA can exit
+        for (int t = 0; t < S; ++t) {
+          if (issued_round[t] < 0) continue;
+          const uint32_t par = static_cast<uint32_t>(issued_round[t]) & 1u;
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(full_bar(t), par) && global_timer_ns() - t0 < ctl.timeout_ns) {
+          }
+        }
+      } else {
+        // the copies complete on the leader's barriers, which this CTA
+        // cannot wait on: give them a fixed 100 us to land
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 100000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (rank == 0) {
+      const bool leader = elect_one_sync();
+      int s = 0;
+      uint32_t round = 0;
+      for (int kt = 0; kt < KT; ++kt) {
+        if (!__all_sync(0xffffffffu, wait_bounded(full_bar(s), round & 1u, ctl, WAIT_MMA_FULL))) {
+          if (leader) *failed = 1;
+          break;
+        }
+        tc_fence_after();
+        if (leader) {
+          if (kt == 0) trace_mark(p.trace, TR_FIRST_DATA);
+          trace_ktile(p.trace, 1, static_cast<uint32_t>(kt));
+#pragma unroll
+          for (int j = 0; j < KSUB; ++j) {
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              mma_f16_g<true>(tmem_base, sdesc_k_major_sw128(stage_b(s) + j * sub_b + 32 * k),
+                              sdesc_k_major_sw128(stage_a(s) + j * L::SUB_A + 32 * k), IDESC,
+                              (kt > 0 || j > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit_g<true>(empty_bar(s));  // stage s may be refilled in both CTAs
+        }
+        __syncwarp();
+        if (++s == S) {
+          s = 0;
+          ++round;
+        }
+      }
+      if (leader) {
+        trace_mark(p.trace, TR_LAST_MMA);
+        mma_commit_g<true>(tfull_bar);  // both CTAs' accumulators are complete
+        mma_commit_local_g<true>(drain_bar);
+      }
+      __syncwarp();
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < ctl.timeout_ns) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // warps 2-5: the warp of lane quarter q (= warp % 4) reads lanes
+    // 32q ... 32q + 31, which hold the CTA's columns 32 (q % 2) ... + 31, each
+    // with the sums for the 32 rows of A from 32 (q / 2) on
+    const int q = warp & 3;
+    const int col = 32 * (q & 1) + lane;  // column within the CTA's block
+    const int m0 = 32 * (q >> 1);         // first row of A this warp's sums belong to
+    const bool have_col = col < n_cta;
+    const bool done = __all_sync(0xffffffffu, wait_bounded(tfull_bar, 0, ctl, WAIT_EPI_TMEM_FULL));
+    const bool ok = named_barrier_and(1, 128, done && !*failed);
+    if (ok) {
+      tc_fence_after();
+      // stage the 64 x n_cta block of C (row m holds consecutive outputs) in
+      // ring stage 0, free once every MMA has completed
+      uint8_t* stage = smem;
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * q) << 16), r);
+      tmem_wait_ld_regs(r);
+      if (have_col) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int m = m0 + i;
+          const float v = __uint_as_float(r[i]);
+          if constexpr (OBYTES == 4) {
+            reinterpret_cast<float*>(stage)[m * n_cta + col] = v;
+          } else if constexpr (OUT == OUT_F16) {
+            reinterpret_cast<__half*>(stage)[m * n_cta + col] = __float2half_rn(v);
+          } else {
+            reinterpret_cast<__nv_bfloat16*>(stage)[m * n_cta + col] = __float2bfloat16_rn(v);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1, 128);
+      // rows past M and columns past N clip
+      if (threadIdx.x == 64 && n_base < p.N) {
+        tma_store_2d(&tmC, smem_addr(stage), n_base, 0);
+        bulk_commit_group();
+        bulk_wait_group_read<0>();  // the staging may go once the copy has read it
+      }
+    }
+    if (threadIdx.x == 64) trace_mark(p.trace, TR_EPI_DONE);
+  }
+
+  tc_fence_before();
+  cluster_sync();  // neither CTA leaves while the pair's MMAs may still read it
+  if (threadIdx.x == 0) trace_mark(p.trace, TR_EXIT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_g<true>(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace sptg

@@ -24,6 +24,8 @@
 
 #include "skinny_cluster_gemm.cuh"  // SkinnyClusterParams
 #include "skinny_gemm.cuh"  // SkinnyParams
+#include "skinny_pair_gemm.cuh"  // SkinnyPairParams
+#include "skinny_rows_gemm.cuh"  // SkinnyRowsParams
 #include "square_gemm.cuh"  // SquareParams
 #include "stream_scale.cuh"  // StreamParams
 #include "variants.h"
@@ -912,6 +914,180 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   return SPTG_OK;
 }
 
+// The skinny product (M <= 64) with one CTA per strip of n_tile output
+// columns over the whole of K: no split, nothing exchanged. The strip width is
+// forced (bn) or the multiple of 8 that covers N with at most one strip per
+// SM; the ring is as deep as shared memory allows (or forced by stages).
+// Returns SPTG_ERR_CONFIG (and launches nothing) when the shape does not suit
+// it -- strips narrower than 32 columns, more strips than SMs, or fewer than
+// three quarters of the SMs busy -- so that the caller can try the others.
+int run_skinny_rows(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N,
+                    int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                    int64_t ldc, cudaStream_t stream, const sptg_config& cfg, bool forced) {
+  KernelVariant v;
+  if (d.is_int8 || M > 64 || !skinny_rows_variant(d.in_bf16, d.out_kind, &v)) {
+    if (forced) t_last_error = "the column-strip skinny kernel takes float products with M <= 64";
+    return SPTG_ERR_CONFIG;
+  }
+  int64_t nt = cfg.bn;
+  if (forced && nt > 0) {
+    if (nt % 8 != 0 || nt < 8 || nt > SKINNY_ROWS_MAX_NT) {
+      t_last_error = "column-strip width (bn) must be a multiple of 8 from 8 to 128";
+      return SPTG_ERR_CONFIG;
+    }
+  } else {
+    nt = ((N + di.sm_count - 1) / di.sm_count + 7) / 8 * 8;
+    if (nt < 8) nt = 8;
+  }
+  const int64_t strips = (N + nt - 1) / nt;
+  if (!forced && (nt < 32 || nt > SKINNY_ROWS_MAX_NT || strips > di.sm_count ||
+                  strips * 4 < 3 * static_cast<int64_t>(di.sm_count)))
+    return SPTG_ERR_CONFIG;
+  if (nt > SKINNY_ROWS_MAX_NT) {
+    t_last_error = "N needs column strips wider than 128 on this GPU";
+    return SPTG_ERR_CONFIG;
+  }
+  const int ksub = v.ksub;
+  const int stage_bytes = static_cast<int>(ksub * (64 + nt) * 128);
+  int stages = cfg.stages ? cfg.stages : SKINNY_ROWS_RING_BUDGET / stage_bytes;
+  if (stages > SKINNY_ROWS_MAX_STAGES) stages = SKINNY_ROWS_MAX_STAGES;
+  if (stages < 1 || stages * stage_bytes > SKINNY_ROWS_RING_BUDGET) {
+    t_last_error = "ring depth out of range for the column-strip skinny kernel";
+    return SPTG_ERR_CONFIG;
+  }
+  const int smem = stages * stage_bytes + SKINNY_ROWS_BAR_BYTES + 1024;
+  int rc = ensure_smem(dev, v.fn, 232448);
+  if (rc) return rc;
+  CUtensorMap ta, tb;
+  const int kstep = 64 * ksub;
+  int load3d = 0;
+  if (K % 64 == 0 &&
+      make_map_kchunks(&ta, d.in_tma, A, K, M, lda, 64, ksub) == SPTG_OK &&
+      make_map_kchunks(&tb, d.in_tma, B, K, N, ldb, static_cast<uint32_t>(nt), ksub) == SPTG_OK)
+    load3d = 1;
+  if (!load3d) {
+    rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, lda);
+    if (rc) return rc;
+    rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, 64, static_cast<uint32_t>(nt),
+                     CU_TENSOR_MAP_SWIZZLE_128B, ldb);
+    if (rc) return rc;
+  }
+  SkinnyRowsParams p;
+  p.C = C;
+  p.ldc = ldc;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.n_tile = static_cast<int>(nt);
+  p.num_k_tiles = static_cast<int>((K + kstep - 1) / kstep);
+  p.stages = stages;
+  p.stage_bytes = stage_bytes;
+  p.load3d = load3d;
+  p.error_word = di.error_word;
+  p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
+  p.inject_stall = cfg.inject_stall;
+  p.trace = static_cast<unsigned long long*>(cfg.trace);
+  v.stages = stages;
+  v.smem = smem;
+  const int grid = static_cast<int>(strips);
+  void* args[] = {&ta, &tb, &p};
+  cudaError_t e = launch_variant(v, grid, stream, args, !cfg.no_overlap);
+  ++t_launches;
+  if (e != cudaSuccess) return cuda_fail(e, "skinny_rows_gemm launch");
+  set_config(
+      "kernel=skinny-rows dtype=%s mma_m=%lld mma_n=%lld bk=%lld stages=%lld grid=%lld "
+      "k_tiles=%lld copies_3d=%lld smem=%lld",
+      d.name, {64, nt, kstep, stages, grid, p.num_k_tiles, load3d, smem});
+  return SPTG_OK;
+}
+
+// The skinny product (M <= 64) on CTA pairs with the 2-SM MMA, K never split:
+// each pair owns 2 * n_cta output columns. n_cta is forced (bn) or the
+// multiple of 8 that covers N with at most one CTA per SM; the ring is as
+// deep as shared memory allows (or forced by stages). Returns SPTG_ERR_CONFIG
+// (and launches nothing) when the shape does not suit it -- more than 64
+// columns per CTA, more CTAs than SMs, or fewer than three quarters of the
+// SMs busy -- so that the caller can try the others.
+int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N,
+                    int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                    int64_t ldc, cudaStream_t stream, const sptg_config& cfg, bool forced) {
+  KernelVariant v;
+  if (d.is_int8 || M > 64 || !skinny_pair_variant(d.in_bf16, d.out_kind, &v)) {
+    if (forced) t_last_error = "the CTA-pair skinny kernel takes float products with M <= 64";
+    return SPTG_ERR_CONFIG;
+  }
+  int64_t nc = cfg.bn;
+  if (forced && nc > 0) {
+    if (nc % 8 != 0 || nc < 8 || nc > 64) {
+      t_last_error = "columns per CTA (bn) must be a multiple of 8 from 8 to 64";
+      return SPTG_ERR_CONFIG;
+    }
+  } else {
+    nc = ((N + di.sm_count - 1) / di.sm_count + 7) / 8 * 8;
+    if (nc < 8) nc = 8;
+  }
+  const int64_t pairs = (N + 2 * nc - 1) / (2 * nc);
+  if (!forced && (nc > 64 || 2 * pairs > di.sm_count ||
+                  8 * pairs < 3 * static_cast<int64_t>(di.sm_count)))
+    return SPTG_ERR_CONFIG;
+  if (nc > 64) {
+    t_last_error = "N needs more than 64 columns per CTA on this GPU";
+    return SPTG_ERR_CONFIG;
+  }
+  const int ksub = v.ksub;
+  const int stage_bytes = ksub * (SKINNY_PAIR_SUB_B + SKINNY_PAIR_SUB_A);
+  const int stages = cfg.stages ? cfg.stages : v.stages;
+  if (stages < 1 || stages > v.stages) {
+    t_last_error = "ring depth out of range for the CTA-pair skinny kernel";
+    return SPTG_ERR_CONFIG;
+  }
+  const int smem = stages * stage_bytes + SKINNY_PAIR_BAR_BYTES + 1024;
+  int rc = ensure_smem(dev, v.fn, 232448);
+  if (rc) return rc;
+  CUtensorMap tb, ta, tc;
+  const int kstep = 64 * ksub;
+  int load3d = 0;
+  if (K % 64 == 0 &&
+      make_map_kchunks(&tb, d.in_tma, B, K, N, ldb, static_cast<uint32_t>(nc), ksub) == SPTG_OK &&
+      make_map_kchunks(&ta, d.in_tma, A, K, M, lda, 32, ksub) == SPTG_OK)
+    load3d = 1;
+  if (!load3d) {
+    rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, 64, static_cast<uint32_t>(nc),
+                     CU_TENSOR_MAP_SWIZZLE_128B, ldb);
+    if (rc) return rc;
+    rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B, lda);
+    if (rc) return rc;
+  }
+  // the block a CTA stores: 64 rows of n_cta consecutive outputs, unswizzled
+  rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, static_cast<uint32_t>(nc), 64,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, ldc);
+  if (rc) return rc;
+  SkinnyPairParams p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.n_cta = static_cast<int>(nc);
+  p.num_k_tiles = static_cast<int>((K + kstep - 1) / kstep);
+  p.stages = stages;
+  p.load3d = load3d;
+  p.error_word = di.error_word;
+  p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
+  p.inject_stall = cfg.inject_stall;
+  p.trace = static_cast<unsigned long long*>(cfg.trace);
+  v.stages = stages;
+  v.smem = smem;
+  const int grid = static_cast<int>(2 * pairs);
+  void* args[] = {&tb, &ta, &tc, &p};
+  cudaError_t e = launch_variant(v, grid, stream, args, !cfg.no_overlap);
+  ++t_launches;
+  if (e != cudaSuccess) return cuda_fail(e, "skinny_pair_gemm launch");
+  set_config(
+      "kernel=skinny-pair dtype=%s mma_m=128 mma_n=64 cols_per_cta=%lld bk=%lld stages=%lld "
+      "grid=%lld pairs=%lld k_tiles=%lld copies_3d=%lld smem=%lld",
+      d.name, {nc, kstep, stages, grid, pairs, p.num_k_tiles, load3d, smem});
+  return SPTG_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ------------------------------------------------------ allocation-free entry
@@ -1062,7 +1238,7 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
     t_last_error = "dimensions must be in [0, 2^31)";
     return SPTG_ERR_ARG;
   }
-  if (cfg.kernel < 0 || cfg.kernel > 3 || cfg.stages < 0 || cfg.bn < 0 || cfg.splits < 0 ||
+  if (cfg.kernel < 0 || cfg.kernel > 5 || cfg.stages < 0 || cfg.bn < 0 || cfg.splits < 0 ||
       cfg.timeout_ms < 0 || (cfg.inject_stall != 0 && cfg.inject_stall != 1) ||
       cfg.cta_pair < 0 || cfg.cta_pair > 2 || (cfg.no_overlap != 0 && cfg.no_overlap != 1) ||
       cfg.stream_k < 0 || cfg.stream_k > 2 ||
@@ -1108,13 +1284,20 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
   // swap-AB kernel; everything else -> the square tile kernel.
   int kernel = cfg.kernel;
   if (kernel == 0 && !d.is_int8 && M <= 128 && N >= 1024) {
-    // memory-bound: the cluster split when it fills the GPU, else stream-K
-    // (up to 64 rows) or the square kernel
+    // memory-bound: up to 64 rows one CTA per column strip when the strips
+    // fill the GPU, else the cluster split when it does, else stream-K (up
+    // to 64 rows) or the square kernel
+    rc = run_skinny_rows(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
+    if (rc != SPTG_ERR_CONFIG) return rc;
     rc = run_skinny_cluster(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
     if (rc != SPTG_ERR_CONFIG) return rc;
     kernel = M <= 64 ? 2 : 1;
   }
   if (kernel == 0) kernel = 1;
+  if (kernel == 4)
+    return run_skinny_rows(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, true);
+  if (kernel == 5)
+    return run_skinny_pair(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, true);
   if (kernel == 3)
     return run_skinny_cluster(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, true);
   if (kernel == 2) return run_skinny(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg);

@@ -33,6 +33,12 @@ bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
 // Skinny kernel with K split inside a cluster (launched in clusters of 2-8).
 // M picks the MMA N: 64 for M <= 64, 128 for M <= 128.
 bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, int M, KernelVariant* v);
+// Skinny kernel with one CTA per strip of output columns (M <= 64, 64-row
+// MMA): bn = 64, stages and smem are chosen per call (0 here).
+bool skinny_rows_variant(bool in_bf16, int out_kind, KernelVariant* v);
+// Skinny kernel on CTA pairs with the 2-SM MMA (M <= 64): stages = the
+// deepest ring that fits; the ring depth and column count are set per call.
+bool skinny_pair_variant(bool in_bf16, int out_kind, KernelVariant* v);
 // The streaming ring out = alpha * in (bn = tile bytes).
 KernelVariant stream_variant();
 // int8 -> binary16 widening of both operands in one launch: rows_a rows of

@@ -88,7 +88,7 @@ def test_argument_errors_before_device_work(lib):
 
 def test_invalid_config_fields(lib):
     ok16 = 1 << 20
-    for cfg in (sptg.Config(4, 0, 0, 0, 0, 0), sptg.Config(0, -1, 0, 0, 0, 0),
+    for cfg in (sptg.Config(6, 0, 0, 0, 0, 0), sptg.Config(0, -1, 0, 0, 0, 0),
                 sptg.Config(0, 0, -2, 0, 0, 0), sptg.Config(0, 0, 0, 0, -5, 0),
                 sptg.Config(0, 0, 0, 0, 0, 7), sptg.Config(0, 0, 0, 0, 0, 0, 4)):
         assert lib.sptg_gemm_ex(4, 8, 16, 1, ok16, ok16, ok16, None, ctypes.byref(cfg)) == -1

@@ -10,7 +10,7 @@ import torch
 
 import bench
 import oracle
-from workloads import Workload, make_inputs
+from workloads import DTYPE_PAIRS, Workload, make_inputs
 
 
 def _exact_float(A, B):
@@ -71,9 +71,18 @@ def test_roofline_arithmetic():
     assert r["frac_dense_spec"] == pytest.approx(r["achieved"] / 2250.0)
     assert r["frac_dense_spec_nvl72"] == pytest.approx(r["achieved"] / 2500.0)
     assert r["algorithmic_bytes"] == 3 * 4096 * 4096 * 2
-    # a timed region over a second (or under the power cap) takes the sustained peak
+    # a timed region over a second takes the sustained peak
     r = bench.roofline(w, 0.08, 2000.0, {"reasons": []}, "square", bench.algorithmic_bytes(w))
     assert r["peak"] == peaks["bf16_tflops_sustained"]
+    assert r["frac_burst"] == pytest.approx(r["achieved"] / peaks["bf16_tflops"])
+    # so does a power cap that pulled the SM clock down ...
+    capped = {"reasons": ["sw_power_cap"], "sm_mhz": 1500.0, "sm_max_mhz": 2070.0}
+    r = bench.roofline(w, 0.08, 20.0, capped, "square", bench.algorithmic_bytes(w))
+    assert r["peak"] == peaks["bf16_tflops_sustained"]
+    # ... but not a cap flagged while the clock stayed at its maximum
+    flagged = {"reasons": ["sw_power_cap"], "sm_mhz": 2070.0, "sm_max_mhz": 2070.0}
+    r = bench.roofline(w, 0.08, 20.0, flagged, "square", bench.algorithmic_bytes(w))
+    assert r["peak"] == peaks["bf16_tflops"]
     # the skinny product is bound by HBM: achieved = (A + B + C bytes) / time
     w = Workload("bf16_skinny_64x8192x8192_bf16out", 64, 8192, 8192, "bf16_bf16", "normal", 1.0, 4)
     b = bench.algorithmic_bytes(w)
@@ -86,3 +95,19 @@ def test_roofline_arithmetic():
 def test_job_throughput_counts_every_rank():
     # units of all ranks over the slowest rank's time
     assert bench.job_throughput(10.0, 4, 2.0) == pytest.approx(20.0)
+
+
+def test_versus_torch_calls():
+    # the PyTorch call timed beside each dtype pair computes the same product
+    assert bench.torch_product("f16_f16")[1] == "torch.matmul"
+    assert bench.torch_product("bf16_bf16")[1] == "torch.matmul"
+    assert bench.torch_product("bf16_f32")[1] == "torch.mm(out_dtype=float32)"
+    assert bench.torch_product("s8_s32")[1] == "torch._int_mm"
+    A = torch.randn(8, 16, dtype=torch.float32)
+    Bcm = torch.randn(4, 16, dtype=torch.float32)
+    C = torch.empty(8, 4)
+    bench.torch_product("f32_f32")[0](A, Bcm, C)
+    assert torch.allclose(C, A @ Bcm.t())
+    for spec in bench.VERSUS_SHAPES.split(";"):
+        m, n, k, pair = spec.split(",")
+        assert int(m) > 0 and int(n) > 0 and int(k) > 0 and pair in DTYPE_PAIRS

@@ -337,6 +337,144 @@ def test_k_tile_marker_skinny_cluster(T, cs):
     assert (C.to(torch.float64) == expect).all()
 
 
+# One CTA per strip of output columns over the whole of K (M <= 64): strip
+# widths from 8 to 128, ragged last strips (N not a multiple of the width),
+# K not a multiple of the 128-wide stage (half-empty last stage, 2-D copies
+# when K is not a multiple of 64), rows past M, all four float dtype pairs.
+@pytest.mark.parametrize("M,N,K,nt,it,ot", [
+    (64, 8192, 4096, 0, "bf16", BF16), (64, 8192, 1024, 56, "bf16", F32),
+    (1, 2048, 1040, 16, "f16", F16), (17, 1000, 1000, 48, "f16", F32),
+    (33, 4096, 520, 128, "bf16", BF16), (64, 256, 64, 8, "bf16", BF16),
+    (48, 9216, 2056, 0, "f16", F16), (5, 1000, 4160, 120, "bf16", F32),
+    (64, 1024, 8200, 32, "f16", F32)])
+def test_skinny_rows(M, N, K, nt, it, ot):
+    A, B = make_inputs(M, N, K, it, "normal", M * 5 + K)
+    C = run(A, B, ot, kernel="skinny_rows", bn=nt)
+    cfg = sptg.last_config()
+    assert "kernel=skinny-rows" in cfg, cfg
+    if nt:
+        assert f"mma_n={nt} " in cfg, cfg
+    assert_float_parity(C, A, B)
+
+
+def test_skinny_rows_is_the_default_for_the_memory_bound_shape():
+    # 64 x 8192 x 8192: strips of at most one per SM, the whole of K each
+    A, B = make_inputs(64, 8192, 8192, "bf16", "normal", 44)
+    C = run(A, B, BF16)
+    cfg = sptg.last_config()
+    assert "kernel=skinny-rows" in cfg, cfg
+    grid = int(cfg.split("grid=")[1].split()[0])
+    nt = int(cfg.split("mma_n=")[1].split()[0])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert nt % 8 == 0 and grid == -(-8192 // nt) and 3 * sms <= 4 * grid <= 4 * sms
+    print(cfg, "max |err| / (1e-3 sum|ab|) =", assert_float_parity(C, A, B, plain=True))
+    # deterministic: no split, no reduction order to vary
+    assert torch.equal(C, run(A, B, BF16))
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 8, 17])
+@pytest.mark.parametrize("stages", [0, 1, 2, 3])
+def test_k_tile_marker_skinny_rows(T, stages):
+    # every K-chunk lands in the sum exactly once, whatever the ring depth;
+    # an odd T leaves the second chunk of the last stage empty
+    A, B, expect = _marker_inputs(64, 1024, T, dtype=BF16)
+    C = run(A, B, F32, kernel="skinny_rows", bn=64, stages=stages)
+    if stages:
+        assert f"stages={stages}" in sptg.last_config()
+    assert (C.to(torch.float64) == expect).all()
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+def test_skinny_rows_ablation_rings_match(stages):
+    A, B = make_inputs(64, 2048, 4096, "bf16", "normal", 16)
+    ref = run(A, B, BF16, kernel="skinny_rows", bn=56)
+    got = run(A, B, BF16, kernel="skinny_rows", bn=56, stages=stages)
+    assert f"stages={stages}" in sptg.last_config()
+    assert torch.equal(ref, got)
+    assert_float_parity(got, A, B)
+
+
+def test_skinny_rows_limits():
+    A, B = make_inputs(65, 2048, 1024, "bf16", "normal", 87)
+    with pytest.raises(sptg.SptgError):
+        run(A, B, BF16, kernel="skinny_rows")  # more than 64 rows
+    A, B = make_inputs(64, 2048, 1024, "bf16", "normal", 88)
+    for bad in (12, 136):
+        with pytest.raises(sptg.SptgError):
+            run(A, B, BF16, kernel="skinny_rows", bn=bad)
+    with pytest.raises(sptg.SptgError):
+        run(A, B, BF16, kernel="skinny_rows", bn=128, stages=5)  # 5 x 48 KB > the budget
+    A, B = make_inputs(64, 2048, 1024, "s8", "int8", 89)
+    with pytest.raises(sptg.SptgError):
+        run(A, B, I32, kernel="skinny_rows")
+
+
+# CTA pairs with the 2-SM MMA over the whole of K (M <= 64): columns per CTA
+# from 8 to 64, ragged last pairs (a CTA whose columns all lie past N), rows of
+# A past 32 (the second CTA's half of the MMA's N side) and past M, K not a
+# multiple of the stage, all four float dtype pairs.
+@pytest.mark.parametrize("M,N,K,nc,it,ot", [
+    (64, 8192, 4096, 0, "bf16", BF16), (64, 8192, 1024, 56, "bf16", F32),
+    (1, 2048, 1040, 16, "f16", F16), (17, 1000, 1000, 48, "f16", F32),
+    (33, 4096, 520, 64, "bf16", BF16), (64, 256, 64, 8, "bf16", BF16),
+    (48, 9216, 2056, 0, "f16", F16), (5, 1000, 4160, 40, "bf16", F32),
+    (64, 1024, 8200, 32, "f16", F32), (40, 200, 640, 64, "bf16", F32)])
+def test_skinny_pair(M, N, K, nc, it, ot):
+    A, B = make_inputs(M, N, K, it, "normal", M * 11 + K)
+    C = run(A, B, ot, kernel="skinny_pair", bn=nc)
+    cfg = sptg.last_config()
+    assert "kernel=skinny-pair" in cfg, cfg
+    if nc:
+        assert f"cols_per_cta={nc} " in cfg, cfg
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 8, 17])
+@pytest.mark.parametrize("stages", [0, 1, 2, 3])
+def test_k_tile_marker_skinny_pair(T, stages):
+    A, B, expect = _marker_inputs(64, 1024, T, dtype=BF16)
+    C = run(A, B, F32, kernel="skinny_pair", bn=56, stages=stages)
+    if stages:
+        assert f"stages={stages}" in sptg.last_config()
+    assert (C.to(torch.float64) == expect).all()
+
+
+def test_skinny_pair_places_every_row_and_column():
+    # A[m, k] = m + 1 and Bcm[n, k] = n % 61 + 1: C[m, n] = K (m + 1)(n % 61 + 1),
+    # exact, so a row or column of the accumulator read from the wrong place
+    # cannot go unseen
+    M, N, K = 64, 2000, 128
+    A = (torch.arange(M, dtype=torch.float32) + 1).repeat(K, 1).t().contiguous().to(BF16)
+    Bcm = (torch.arange(N) % 61 + 1).to(torch.float32).repeat(K, 1).t().contiguous().to(BF16)
+    expect = K * torch.outer(torch.arange(M, dtype=torch.float64) + 1,
+                             (torch.arange(N) % 61 + 1).to(torch.float64))
+    for nc in (8, 40, 56, 64):
+        C = run(A, Bcm, F32, kernel="skinny_pair", bn=nc)
+        assert torch.equal(C.to(torch.float64), expect), nc
+
+
+@pytest.mark.parametrize("stages", [1, 2, 4, 9])
+def test_skinny_pair_ablation_rings_match(stages):
+    A, B = make_inputs(64, 2048, 4096, "bf16", "normal", 17)
+    ref = run(A, B, BF16, kernel="skinny_pair", bn=40)
+    got = run(A, B, BF16, kernel="skinny_pair", bn=40, stages=stages)
+    assert f"stages={stages}" in sptg.last_config()
+    assert torch.equal(ref, got)
+    assert_float_parity(got, A, B)
+
+
+def test_skinny_pair_limits():
+    A, B = make_inputs(65, 2048, 1024, "bf16", "normal", 90)
+    with pytest.raises(sptg.SptgError):
+        run(A, B, BF16, kernel="skinny_pair")  # more than 64 rows
+    A, B = make_inputs(64, 2048, 1024, "bf16", "normal", 91)
+    for bad in (12, 72):
+        with pytest.raises(sptg.SptgError):
+            run(A, B, BF16, kernel="skinny_pair", bn=bad)
+    with pytest.raises(sptg.SptgError):
+        run(A, B, BF16, kernel="skinny_pair", stages=10)  # 10 x 24 KB > the budget
+
+
 @pytest.mark.parametrize("M,N,K,it,ot", [
     (128, 8192, 4096, "bf16", BF16), (96, 8192, 2048, "f16", F16), (65, 9216, 1040, "bf16", F32),
     (128, 8192, 2048, "f16", F32), (100, 16384, 1024, "bf16", BF16)])
@@ -729,7 +867,7 @@ def test_async_on_a_side_stream():
 
 
 @pytest.mark.parametrize("kernel,pair,stream_k", [(1, 1, 0), (1, 2, 0), (1, 1, 2), (1, 2, 2),
-                                                   (2, 0, 0), (3, 0, 0)])
+                                                   (2, 0, 0), (3, 0, 0), (4, 0, 0), (5, 0, 0)])
 def test_bounded_wait_reports_timeout_and_context_survives(kernel, pair, stream_k):
     # The producer withholds one K-tile; the consumer's wait runs out after
     # 100 ms, the kernel tears down, and the host reads SPTG_ERR_TIMEOUT.
@@ -747,7 +885,8 @@ def test_bounded_wait_reports_timeout_and_context_survives(kernel, pair, stream_
     assert sptg.device_error() == -5
     assert sptg.device_error() == 0  # the word was cleared
     # the context still works
-    C = run(A, B, BF16, kernel={1: "square", 2: "skinny", 3: "skinny_cluster"}[kernel])
+    C = run(A, B, BF16, kernel={1: "square", 2: "skinny", 3: "skinny_cluster",
+                                4: "skinny_rows", 5: "skinny_pair"}[kernel])
     assert_float_parity(C, A, B)
 
 
@@ -771,7 +910,8 @@ def test_bounded_wait_int8_reports_timeout_and_context_survives(cta_pair, stream
 
 
 @pytest.mark.parametrize("kernel,cta_pair", [("square", 1), ("square", 2), ("skinny", 0),
-                                             ("skinny_cluster", 0)])
+                                             ("skinny_cluster", 0), ("skinny_rows", 0),
+                                             ("skinny_pair", 0)])
 def test_timeline_trace_is_ordered(kernel, cta_pair):
     # the optional in-kernel timeline: per CTA the events come in pipeline
     # order, and CTA 0's K-tiles are consumed after they were issued

@@ -4,7 +4,8 @@ Every case is small enough for the full oracle, so each element of C is
 checked: int8 bit-exact, float within the element-wise bound. The shapes are
 ragged (no tile multiple) within the library's 16-byte row-pitch rule, and the
 configurations cover the automatic choice, one-CTA and CTA-pair tiles of
-every width, stream-K never / chosen / every tile, and both skinny kernels with their cluster sizes.
+every width, stream-K never / chosen / every tile, and the three skinny kernels with their
+cluster sizes, strip widths and ring depths.
 """
 import random
 
@@ -68,3 +69,41 @@ def test_random_configuration(i):
         assert_int_parity(C, A, B)
     else:
         assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_random_skinny_rows(i):
+    # the column-strip skinny kernel: any strip width (multiple of 8 up to
+    # 128), any ring depth that fits, ragged N and K, rows 1 ... 64
+    rng = random.Random(5000 + i)
+    dt = rng.choice(["f16_f16", "f16_f32", "bf16_bf16", "bf16_f32"])
+    it = dt.split("_")[0]
+    nmul = 4 if OUT[dt].itemsize == 4 else 8
+    M = rng.randint(1, 64)
+    N = nmul * rng.randint(8 // nmul, 2600 // nmul)
+    K = 8 * rng.randint(1, 1400 // 8)
+    nt = 8 * rng.randint(1, 16)
+    stages = rng.randint(0, 4)
+    A, B = make_inputs(M, N, K, it, "uniform", 6000 + i)
+    C = run(A, B, OUT[dt], kernel="skinny_rows", bn=nt, stages=stages)
+    assert "kernel=skinny-rows" in sptg.last_config()
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_random_skinny_pair(i):
+    # the CTA-pair skinny kernel: any column count per CTA (multiple of 8 up
+    # to 64), any ring depth that fits, ragged N and K, rows 1 ... 64
+    rng = random.Random(7000 + i)
+    dt = rng.choice(["f16_f16", "f16_f32", "bf16_bf16", "bf16_f32"])
+    it = dt.split("_")[0]
+    nmul = 4 if OUT[dt].itemsize == 4 else 8
+    M = rng.randint(1, 64)
+    N = nmul * rng.randint(8 // nmul, 2600 // nmul)
+    K = 8 * rng.randint(1, 1400 // 8)
+    nc = 8 * rng.randint(1, 8)
+    stages = rng.randint(0, 9)
+    A, B = make_inputs(M, N, K, it, "uniform", 8000 + i)
+    C = run(A, B, OUT[dt], kernel="skinny_pair", bn=nc, stages=stages)
+    assert "kernel=skinny-pair" in sptg.last_config()
+    assert_float_parity(C, A, B)
