@@ -36,6 +36,7 @@ struct SkinnyPairParams {
   int n_cta;        // output columns per CTA: a multiple of 8, 8 ... 64
   int num_k_tiles;  // ring stages' worth of K: ceil(K / (64 * KSUB))
   int stages;       // ring depth, 1 ... SKINNY_PAIR_MAX_STAGES
+  int stage_bytes;  // skinny_pair_stage_bytes(KSUB, n_cta)
   int load3d;       // 1: one 3-D copy per operand and stage; 0: 2-D per chunk
   unsigned int* error_word;
   uint64_t timeout_ns;
@@ -48,24 +49,19 @@ constexpr int SKINNY_PAIR_MAX_STAGES = 16;
 constexpr int SKINNY_PAIR_BAR_BYTES = (2 * SKINNY_PAIR_MAX_STAGES + 2) * 8 + 16;
 constexpr int SKINNY_PAIR_RING_BUDGET = 232448 - 1024 - SKINNY_PAIR_BAR_BYTES;
 
-constexpr int SKINNY_PAIR_SUB_B = 64 * 128;  // one 64-wide K-chunk of a CTA's Bcm rows
+constexpr int SKINNY_PAIR_SUB_B = 64 * 128;  // the MMA's 64-row operand tile of Bcm rows
 constexpr int SKINNY_PAIR_SUB_A = 32 * 128;  // one K-chunk of a CTA's 32 rows of A
 
-template <int KSUB>
-struct SkinnyPairLayout {
-  static constexpr int SUB_B = SKINNY_PAIR_SUB_B;  // room for one 64-row operand tile per chunk
-  static constexpr int SUB_A = SKINNY_PAIR_SUB_A;
-  static constexpr int STAGE = KSUB * (SUB_B + SUB_A);
-  static_assert(STAGE % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
-  // C staging (in stage 0 once the K-loop is over): 64 rows of up to 64 fp32
-  static_assert(64 * 64 * 4 <= STAGE, "the output block must fit one stage");
-};
-
-template <int KSUB>
-constexpr int skinny_pair_max_stages() {
-  return SKINNY_PAIR_RING_BUDGET / SkinnyPairLayout<KSUB>::STAGE < SKINNY_PAIR_MAX_STAGES
-             ? SKINNY_PAIR_RING_BUDGET / SkinnyPairLayout<KSUB>::STAGE
-             : SKINNY_PAIR_MAX_STAGES;
+// One ring stage: the KSUB K-chunks of this CTA's n_cta rows of Bcm back to
+// back (as one 3-D copy writes them) -- the MMA reads a 64-row tile from the
+// start of each, so the region holds (KSUB - 1) packed chunks and one full
+// tile -- then the KSUB chunks of its 32 rows of A. A multiple of 1024 bytes
+// (n_cta is a multiple of 8), which keeps every chunk on the swizzle pattern.
+__host__ __device__ constexpr int skinny_pair_b_region(int ksub, int n_cta) {
+  return (ksub - 1) * n_cta * 128 + SKINNY_PAIR_SUB_B;
+}
+__host__ __device__ constexpr int skinny_pair_stage_bytes(int ksub, int n_cta) {
+  return skinny_pair_b_region(ksub, n_cta) + ksub * SKINNY_PAIR_SUB_A;
 }
 
 template <bool IN_BF16, int OUT, int KSUB>
@@ -74,27 +70,31 @@ __global__ void __launch_bounds__(192, 1)
                             const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmC,
                             const SkinnyPairParams p) {
-  using L = SkinnyPairLayout<KSUB>;
   constexpr int BK = 64;
   constexpr int OBYTES = OutTraits<OUT>::bytes;
   constexpr uint32_t TMEM_COLS = 64;
   // kind::f16, fp32 accumulation, M = 128 (the pair), N = 64
   constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, 128, 64);
   static_assert(OUT != OUT_S32, "float outputs only");
+  // C staging (in stage 0 once the K-loop is over): 64 rows of up to 64 outputs
+  static_assert(64 * 64 * OBYTES <= skinny_pair_stage_bytes(KSUB, 8),
+                "the output block must fit the smallest stage");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const int S = p.stages;
-  const uint32_t bar0 = sbase + static_cast<uint32_t>(S * L::STAGE);
-  auto stage_b = [&](int s) { return sbase + static_cast<uint32_t>(s * L::STAGE); };
-  auto stage_a = [&](int s) { return stage_b(s) + KSUB * L::SUB_B; };
+  const int n_cta = p.n_cta;
+  const uint32_t bar0 = sbase + static_cast<uint32_t>(S * p.stage_bytes);
+  auto stage_b = [&](int s) { return sbase + static_cast<uint32_t>(s * p.stage_bytes); };
+  const uint32_t a_off = static_cast<uint32_t>(skinny_pair_b_region(KSUB, n_cta));
+  auto stage_a = [&](int s) { return stage_b(s) + a_off; };
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (SKINNY_PAIR_MAX_STAGES + s); };
   const uint32_t tfull_bar = bar0 + 8u * (2 * SKINNY_PAIR_MAX_STAGES);
   const uint32_t drain_bar = tfull_bar + 8u;
-  uint8_t* misc = smem + S * L::STAGE + (2 * SKINNY_PAIR_MAX_STAGES + 2) * 8;
+  uint8_t* misc = smem + S * p.stage_bytes + (2 * SKINNY_PAIR_MAX_STAGES + 2) * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   volatile int* failed = reinterpret_cast<volatile int*>(misc + 8);
@@ -102,16 +102,15 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0 = leader, which issues the MMAs
-  const int n_cta = p.n_cta;
   // this CTA's first output column
   const int n_base = static_cast<int>(blockIdx.x >> 1) * 2 * n_cta + static_cast<int>(rank) * n_cta;
   const int KT = p.num_k_tiles;
   // bytes that complete one stage's "full" barrier: both CTAs' copies
   const uint32_t stage_tx = 2u * KSUB * static_cast<uint32_t>((n_cta + 32) * 128);
   // A K-chunk of this CTA's Bcm rows fills n_cta rows; the chunks of a stage
-  // lie back to back (as one 3-D copy writes them), so the MMA's 64-row
-  // operand tile of chunk j starts at j * n_cta rows and its rows past n_cta
-  // (the next chunk's, or unused ones) only reach sums that are never stored.
+  // lie back to back, so the MMA's 64-row operand tile of chunk j starts at
+  // j * n_cta rows and its rows past n_cta (the next chunk's, or unused ones)
+  // only reach sums that are never stored.
   const int sub_b = n_cta * 128;
 
   if (threadIdx.x == 0) {
@@ -188,8 +187,8 @@ __global__ void __launch_bounds__(192, 1)
             for (int j = 0; j < KSUB; ++j) {
               tma_load_2d_pair(stage_b(s) + j * sub_b, &tmB, leader_full, (kt * KSUB + j) * BK,
                                n_base, pol_stream);
-              tma_load_2d_pair(stage_a(s) + j * L::SUB_A, &tmA, leader_full, (kt * KSUB + j) * BK,
-                               32 * static_cast<int>(rank), pol_keep);
+              tma_load_2d_pair(stage_a(s) + j * SKINNY_PAIR_SUB_A, &tmA, leader_full,
+                               (kt * KSUB + j) * BK, 32 * static_cast<int>(rank), pol_keep);
             }
           }
           if (kt == 0) trace_mark(p.trace, TR_FIRST_LOAD);
@@ -242,8 +241,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
               mma_f16_g<true>(tmem_base, sdesc_k_major_sw128(stage_b(s) + j * sub_b + 32 * k),
-                              sdesc_k_major_sw128(stage_a(s) + j * L::SUB_A + 32 * k), IDESC,
-                              (kt > 0 || j > 0 || k > 0) ? 1u : 0u);
+                              sdesc_k_major_sw128(stage_a(s) + j * SKINNY_PAIR_SUB_A + 32 * k),
+                              IDESC, (kt > 0 || j > 0 || k > 0) ? 1u : 0u);
             }
           }
           mma_commit_g<true>(empty_bar(s));  // stage s may be refilled in both CTAs

@@ -866,6 +866,10 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
         break;
       }
     }
+    if (cs == 0 && forced) {
+      t_last_error = "no cluster size fits: the 128-column tiles outnumber the SMs";
+      return SPTG_ERR_CONFIG;
+    }
     if (cs == 0 || (!forced && static_cast<int64_t>(n_tiles) * cs * 4 < 3 * di.sm_count))
       return SPTG_ERR_CONFIG;
   }
@@ -1035,9 +1039,10 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
     return SPTG_ERR_CONFIG;
   }
   const int ksub = v.ksub;
-  const int stage_bytes = ksub * (SKINNY_PAIR_SUB_B + SKINNY_PAIR_SUB_A);
-  const int stages = cfg.stages ? cfg.stages : v.stages;
-  if (stages < 1 || stages > v.stages) {
+  const int stage_bytes = skinny_pair_stage_bytes(ksub, static_cast<int>(nc));
+  const int max_stages = std::min(SKINNY_PAIR_MAX_STAGES, SKINNY_PAIR_RING_BUDGET / stage_bytes);
+  const int stages = cfg.stages ? cfg.stages : max_stages;
+  if (stages < 1 || stages > max_stages) {
     t_last_error = "ring depth out of range for the CTA-pair skinny kernel";
     return SPTG_ERR_CONFIG;
   }
@@ -1069,6 +1074,7 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   p.n_cta = static_cast<int>(nc);
   p.num_k_tiles = static_cast<int>((K + kstep - 1) / kstep);
   p.stages = stages;
+  p.stage_bytes = stage_bytes;
   p.load3d = load3d;
   p.error_word = di.error_word;
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
@@ -1284,11 +1290,22 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
   // swap-AB kernel; everything else -> the square tile kernel.
   int kernel = cfg.kernel;
   if (kernel == 0 && !d.is_int8 && M <= 128 && N >= 1024) {
-    // memory-bound: up to 64 rows one CTA per column strip when the strips
-    // fill the GPU, else the cluster split when it does, else stream-K (up
-    // to 64 rows) or the square kernel
-    rc = run_skinny_rows(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
-    if (rc != SPTG_ERR_CONFIG) return rc;
+    // Memory-bound. Up to 64 rows, with c = N / SMs rounded up to a multiple
+    // of 8 (the output columns one SM would own): the K-loop unsplit on CTA
+    // pairs for 32 <= c <= 64, one CTA per column strip for c > 64; else the
+    // cluster split when it fills the GPU, else stream-K (up to 64 rows) or
+    // the square kernel. Measured with 64 rows on 152 SMs (bfloat16, K =
+    // 8192): N = 2048-3072 cluster split, 4096-9216 pairs, 10240-19456
+    // strips, wider stream-K.
+    const int64_t c = ((N + di.sm_count - 1) / di.sm_count + 7) / 8 * 8;
+    if (M <= 64 && c >= 32 && c <= 64) {
+      rc = run_skinny_pair(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
+      if (rc != SPTG_ERR_CONFIG) return rc;
+    }
+    if (M <= 64 && c > 64) {
+      rc = run_skinny_rows(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
+      if (rc != SPTG_ERR_CONFIG) return rc;
+    }
     rc = run_skinny_cluster(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
     if (rc != SPTG_ERR_CONFIG) return rc;
     kernel = M <= 64 ? 2 : 1;
