@@ -116,26 +116,39 @@ bool skinny_rows_variant(bool in_bf16, int out_kind, KernelVariant* v) {
   return true;
 }
 
-// CTA pairs with the 2-SM MMA (M <= 64): four 64-wide K-chunks per stage, so
-// each stage reads 512 contiguous bytes of every Bcm row (64 x 8192 x 8192:
-// 22.6 us against 23.3 us with two chunks at twice the ring depth, 36.9 us
-// with one); the ring depth and each CTA's column count are set per call.
-constexpr int kSkinnyPairKsub = 4;
-template <bool BF, int OUT>
+// CTA pairs with the 2-SM MMA over the whole of K. Up to 64 rows (MN = 64):
+// four 64-wide K-chunks per stage, so each stage reads 512 contiguous bytes of
+// every Bcm row (64 x 8192 x 8192: 22.6 us against 23.3 us with two chunks at
+// twice the ring depth, 36.9 us with one). 65-128 rows (MN = 128), whose rows
+// of A take twice the room: two chunks per stage (128 x 8192 x 8192: 25.2 us
+// against 26.4 us with four chunks at 3 stages), four up to 40 columns per CTA
+// (128 x 4096 x 8192: 17.5 against 22.3 us). The ring depth and each CTA's
+// column count are set per call.
+template <int MN, bool BF, int OUT, int KS>
 KernelVariant make_skinny_pair() {
-  KernelVariant v{reinterpret_cast<const void*>(&skinny_pair_gemm_kernel<BF, OUT, kSkinnyPairKsub>),
-                  64, 0, 0, true};
-  v.ksub = kSkinnyPairKsub;
+  KernelVariant v{reinterpret_cast<const void*>(&skinny_pair_gemm_kernel<MN, BF, OUT, KS>), MN, 0,
+                  0, true};
+  v.ksub = KS;
   return v;
 }
 
-bool skinny_pair_variant(bool in_bf16, int out_kind, KernelVariant* v) {
-  if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny_pair<true, OUT_BF16>();
-  else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny_pair<false, OUT_F16>();
-  else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny_pair<true, OUT_F32>();
-  else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny_pair<false, OUT_F32>();
+template <int MN, int KS>
+bool skinny_pair_variant_mn(bool in_bf16, int out_kind, KernelVariant* v) {
+  if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny_pair<MN, true, OUT_BF16, KS>();
+  else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny_pair<MN, false, OUT_F16, KS>();
+  else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny_pair<MN, true, OUT_F32, KS>();
+  else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny_pair<MN, false, OUT_F32, KS>();
   else return false;
   return true;
+}
+
+bool skinny_pair_variant(bool in_bf16, int out_kind, int M, int n_cta, KernelVariant* v) {
+  if (M <= 64) return skinny_pair_variant_mn<64, 4>(in_bf16, out_kind, v);
+  if (M <= 128) {
+    if (n_cta <= 40) return skinny_pair_variant_mn<128, 4>(in_bf16, out_kind, v);
+    return skinny_pair_variant_mn<128, 2>(in_bf16, out_kind, v);
+  }
+  return false;
 }
 
 }  // namespace sptg

@@ -1,30 +1,31 @@
-// skinny_pair_gemm.cuh -- the memory-bound skinny product (M <= 64) on CTA
+// skinny_pair_gemm.cuh -- the memory-bound skinny product (M <= 128) on CTA
 // pairs with the 2-SM tensor-core instruction, K never split.
 //
-// Swap-AB as in skinny_gemm.cuh: D^T[n, m] = sum_k Bcm[n, k] * A[m, k]. A pair
-// of CTAs (a cluster of two) owns 2 * n_cta consecutive output columns; CTA
-// rank r loads the n_cta rows of Bcm of its own columns (into a 64-row operand
-// tile; rows past n_cta are never stored) and the 32 rows 32r ... 32r + 31 of A.
-// The leader's tcgen05.mma.cta_group::2 (M = 128 over the pair's columns, N =
-// 64 over the rows of A) reads both CTAs' shared memory, so each SM copies
-// only half of A per K-chunk, and each CTA's tensor memory receives the sums
-// of its own columns over the whole of K. Nothing is exchanged between SMs
-// after the K-loop: each CTA converts its 64 x n_cta block of C, stages it in
-// shared memory (the ring, idle by then) and writes it with one tensor copy.
+// Swap-AB as in skinny_gemm.cuh: D^T[n, m] = sum_k Bcm[n, k] * A[m, k]. The
+// MMA's N side covers MN = 64 or 128 rows of A. A pair of CTAs (a cluster of
+// two) owns 2 * n_cta consecutive output columns; CTA rank r loads the n_cta
+// rows of Bcm of its own columns (into a 64-row operand tile; rows past n_cta
+// are never stored) and the MN / 2 rows r * MN / 2 ... of A. The leader's
+// tcgen05.mma.cta_group::2 (M = 128 over the pair's columns, N = MN over the
+// rows of A) reads both CTAs' shared memory, so each SM copies only half of
+// A per K-chunk, and each CTA's tensor memory receives the sums of its own
+// columns over the whole of K. Nothing is exchanged between SMs after the
+// K-loop: each CTA converts its MN x n_cta block of C, stages it in shared
+// memory (the ring, idle by then) and writes it with one tensor copy.
 //
-// Per SM a K-chunk moves (n_cta + 32) x 128 bytes, against (n_cta + 64) x 128
-// for one CTA per strip (skinny_rows_gemm.cuh) and (128 + 64) x 128 for half a
-// K-range of a 128-column tile (skinny_cluster_gemm.cuh, which then exchanges
-// partial sums). The host picks n_cta so that the pairs cover the SMs about
-// once (8192 columns over 152 SMs: 56 per CTA, 74 pairs).
+// Per SM a K-chunk moves (n_cta + MN / 2) x 128 bytes, against (n_cta + 64)
+// x 128 for one CTA per strip (skinny_rows_gemm.cuh, MN = 64) and (128 + MN)
+// x 128 for half a K-range of a 128-column tile (skinny_cluster_gemm.cuh,
+// which then exchanges partial sums). The host picks n_cta so that the pairs
+// cover the SMs about once (8192 columns over 152 SMs: 56 per CTA, 74 pairs).
 //
 // Copies of both CTAs complete on the leader's "full" barrier; the leader's
 // commits arrive on both CTAs' "empty" and "tmem_full" barriers.
 //
-// Tensor-memory layout of the accumulator (cta_group::2, M = 128, N = 64):
+// Tensor-memory layout of the accumulator (cta_group::2, M = 128, N = MN):
 // each CTA holds its 64 rows of D with the N side split in halves: row i's
-// sums for the rows 0-31 of A lie in lane i, those for the rows 32-63 in lane
-// 64 + i, each half in columns 0-31.
+// sums for the rows 0 ... MN/2 - 1 of A lie in lane i, those for the rows
+// MN/2 ... MN - 1 in lane 64 + i, each half in columns 0 ... MN/2 - 1.
 #pragma once
 
 #include "common.cuh"
@@ -36,7 +37,7 @@ struct SkinnyPairParams {
   int n_cta;        // output columns per CTA: a multiple of 8, 8 ... 64
   int num_k_tiles;  // ring stages' worth of K: ceil(K / (64 * KSUB))
   int stages;       // ring depth, 1 ... SKINNY_PAIR_MAX_STAGES
-  int stage_bytes;  // skinny_pair_stage_bytes(KSUB, n_cta)
+  int stage_bytes;  // skinny_pair_stage_bytes(KSUB, n_cta, MN)
   int load3d;       // 1: one 3-D copy per operand and stage; 0: 2-D per chunk
   unsigned int* error_word;
   uint64_t timeout_ns;
@@ -50,21 +51,23 @@ constexpr int SKINNY_PAIR_BAR_BYTES = (2 * SKINNY_PAIR_MAX_STAGES + 2) * 8 + 16;
 constexpr int SKINNY_PAIR_RING_BUDGET = 232448 - 1024 - SKINNY_PAIR_BAR_BYTES;
 
 constexpr int SKINNY_PAIR_SUB_B = 64 * 128;  // the MMA's 64-row operand tile of Bcm rows
-constexpr int SKINNY_PAIR_SUB_A = 32 * 128;  // one K-chunk of a CTA's 32 rows of A
+// one K-chunk of a CTA's MN / 2 rows of A
+__host__ __device__ constexpr int skinny_pair_sub_a(int mn) { return mn / 2 * 128; }
 
 // One ring stage: the KSUB K-chunks of this CTA's n_cta rows of Bcm back to
 // back (as one 3-D copy writes them) -- the MMA reads a 64-row tile from the
 // start of each, so the region holds (KSUB - 1) packed chunks and one full
-// tile -- then the KSUB chunks of its 32 rows of A. A multiple of 1024 bytes
-// (n_cta is a multiple of 8), which keeps every chunk on the swizzle pattern.
+// tile -- then the KSUB chunks of its MN / 2 rows of A. A multiple of 1024
+// bytes (n_cta is a multiple of 8), which keeps every chunk on the swizzle
+// pattern.
 __host__ __device__ constexpr int skinny_pair_b_region(int ksub, int n_cta) {
   return (ksub - 1) * n_cta * 128 + SKINNY_PAIR_SUB_B;
 }
-__host__ __device__ constexpr int skinny_pair_stage_bytes(int ksub, int n_cta) {
-  return skinny_pair_b_region(ksub, n_cta) + ksub * SKINNY_PAIR_SUB_A;
+__host__ __device__ constexpr int skinny_pair_stage_bytes(int ksub, int n_cta, int mn) {
+  return skinny_pair_b_region(ksub, n_cta) + ksub * skinny_pair_sub_a(mn);
 }
 
-template <bool IN_BF16, int OUT, int KSUB>
+template <int MN, bool IN_BF16, int OUT, int KSUB>
 __global__ void __launch_bounds__(192, 1)
     skinny_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmA,
@@ -72,13 +75,18 @@ __global__ void __launch_bounds__(192, 1)
                             const SkinnyPairParams p) {
   constexpr int BK = 64;
   constexpr int OBYTES = OutTraits<OUT>::bytes;
-  constexpr uint32_t TMEM_COLS = 64;
-  // kind::f16, fp32 accumulation, M = 128 (the pair), N = 64
-  constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, 128, 64);
+  constexpr int HALF = MN / 2;  // rows of A each CTA copies
+  constexpr int SUB_A = skinny_pair_sub_a(MN);
+  constexpr uint32_t TMEM_COLS = 64;  // holds HALF <= 64 columns
+  // kind::f16, fp32 accumulation, M = 128 (the pair), N = MN
+  constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, 128, MN);
+  static_assert(MN == 64 || MN == 128, "MN must be 64 or 128");
   static_assert(OUT != OUT_S32, "float outputs only");
-  // C staging (in stage 0 once the K-loop is over): 64 rows of up to 64 outputs
-  static_assert(64 * 64 * OBYTES <= skinny_pair_stage_bytes(KSUB, 8),
-                "the output block must fit the smallest stage");
+  // C staging (in stage 0 once the K-loop is over): MN rows of n_cta outputs;
+  // both sides grow linearly with n_cta, so the ends 8 and 64 bound it
+  static_assert(MN * 8 * OBYTES <= skinny_pair_stage_bytes(KSUB, 8, MN) &&
+                    MN * 64 * OBYTES <= skinny_pair_stage_bytes(KSUB, 64, MN),
+                "the output block must fit one stage");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -106,7 +114,7 @@ __global__ void __launch_bounds__(192, 1)
   const int n_base = static_cast<int>(blockIdx.x >> 1) * 2 * n_cta + static_cast<int>(rank) * n_cta;
   const int KT = p.num_k_tiles;
   // bytes that complete one stage's "full" barrier: both CTAs' copies
-  const uint32_t stage_tx = 2u * KSUB * static_cast<uint32_t>((n_cta + 32) * 128);
+  const uint32_t stage_tx = 2u * KSUB * static_cast<uint32_t>((n_cta + HALF) * 128);
   // A K-chunk of this CTA's Bcm rows fills n_cta rows; the chunks of a stage
   // lie back to back, so the MMA's 64-row operand tile of chunk j starts at
   // j * n_cta rows and its rows past n_cta (the next chunk's, or unused ones)
@@ -180,15 +188,15 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t leader_full = map_to_cta(full_bar(s), 0u);
           if (p.load3d) {
             tma_load_3d_pair(stage_b(s), &tmB, leader_full, 0, n_base, kt * KSUB, pol_stream);
-            tma_load_3d_pair(stage_a(s), &tmA, leader_full, 0, 32 * static_cast<int>(rank),
+            tma_load_3d_pair(stage_a(s), &tmA, leader_full, 0, HALF * static_cast<int>(rank),
                              kt * KSUB, pol_keep);
           } else {
 #pragma unroll
             for (int j = 0; j < KSUB; ++j) {
               tma_load_2d_pair(stage_b(s) + j * sub_b, &tmB, leader_full, (kt * KSUB + j) * BK,
                                n_base, pol_stream);
-              tma_load_2d_pair(stage_a(s) + j * SKINNY_PAIR_SUB_A, &tmA, leader_full,
-                               (kt * KSUB + j) * BK, 32 * static_cast<int>(rank), pol_keep);
+              tma_load_2d_pair(stage_a(s) + j * SUB_A, &tmA, leader_full, (kt * KSUB + j) * BK,
+                               HALF * static_cast<int>(rank), pol_keep);
             }
           }
           if (kt == 0) trace_mark(p.trace, TR_FIRST_LOAD);
@@ -241,7 +249,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
               mma_f16_g<true>(tmem_base, sdesc_k_major_sw128(stage_b(s) + j * sub_b + 32 * k),
-                              sdesc_k_major_sw128(stage_a(s) + j * SKINNY_PAIR_SUB_A + 32 * k),
+                              sdesc_k_major_sw128(stage_a(s) + j * SUB_A + 32 * k),
                               IDESC, (kt > 0 || j > 0 || k > 0) ? 1u : 0u);
             }
           }
@@ -267,32 +275,35 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ epilogue
     // warps 2-5: the warp of lane quarter q (= warp % 4) reads lanes
     // 32q ... 32q + 31, which hold the CTA's columns 32 (q % 2) ... + 31, each
-    // with the sums for the 32 rows of A from 32 (q / 2) on
+    // with the sums for the MN / 2 rows of A from (MN / 2)(q / 2) on
     const int q = warp & 3;
     const int col = 32 * (q & 1) + lane;  // column within the CTA's block
-    const int m0 = 32 * (q >> 1);         // first row of A this warp's sums belong to
+    const int m0 = HALF * (q >> 1);       // first row of A this warp's sums belong to
     const bool have_col = col < n_cta;
     const bool done = __all_sync(0xffffffffu, wait_bounded(tfull_bar, 0, ctl, WAIT_EPI_TMEM_FULL));
     const bool ok = named_barrier_and(1, 128, done && !*failed);
     if (ok) {
       tc_fence_after();
-      // stage the 64 x n_cta block of C (row m holds consecutive outputs) in
+      // stage the MN x n_cta block of C (row m holds consecutive outputs) in
       // ring stage 0, free once every MMA has completed
       uint8_t* stage = smem;
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * q) << 16), r);
-      tmem_wait_ld_regs(r);
-      if (have_col) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int m = m0 + i;
-          const float v = __uint_as_float(r[i]);
-          if constexpr (OBYTES == 4) {
-            reinterpret_cast<float*>(stage)[m * n_cta + col] = v;
-          } else if constexpr (OUT == OUT_F16) {
-            reinterpret_cast<__half*>(stage)[m * n_cta + col] = __float2half_rn(v);
-          } else {
-            reinterpret_cast<__nv_bfloat16*>(stage)[m * n_cta + col] = __float2bfloat16_rn(v);
+      for (int cb = 0; cb < HALF; cb += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + cb, r);
+        tmem_wait_ld_regs(r);
+        if (have_col) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int m = m0 + cb + i;
+            const float v = __uint_as_float(r[i]);
+            if constexpr (OBYTES == 4) {
+              reinterpret_cast<float*>(stage)[m * n_cta + col] = v;
+            } else if constexpr (OUT == OUT_F16) {
+              reinterpret_cast<__half*>(stage)[m * n_cta + col] = __float2half_rn(v);
+            } else {
+              reinterpret_cast<__nv_bfloat16*>(stage)[m * n_cta + col] = __float2bfloat16_rn(v);
+            }
           }
         }
       }

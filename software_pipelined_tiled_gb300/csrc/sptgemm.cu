@@ -832,7 +832,7 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
 int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N,
                        int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                        void* C, int64_t ldc, cudaStream_t stream, const sptg_config& cfg,
-                       bool forced) {
+                       bool forced, bool fill = true) {
   KernelVariant v;
   if (d.is_int8 || !skinny_cluster_variant(d.in_bf16, d.out_kind, cfg.stages, static_cast<int>(M),
                                            &v) ||
@@ -846,7 +846,7 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
   const int k_tiles = static_cast<int>((K + kstep - 1) / kstep);
   // cluster size: forced (splits), else the largest of 4, 2, 1 whose CTAs
   // (cluster size per column tile) fit the SMs; taken only if the grid fills
-  // at least three quarters of the SMs
+  // at least three quarters of the SMs (unless `fill` is false)
   // the receive buffer holds up to 3 x 32 columns (clusters of 4) for MMA
   // N = 64 and 64 columns (clusters of 2) for MMA N = 128
   const int max_cs = v.bn <= 64 ? 4 : 2;
@@ -870,7 +870,7 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
       t_last_error = "no cluster size fits: the 128-column tiles outnumber the SMs";
       return SPTG_ERR_CONFIG;
     }
-    if (cs == 0 || (!forced && static_cast<int64_t>(n_tiles) * cs * 4 < 3 * di.sm_count))
+    if (cs == 0 || (!forced && fill && static_cast<int64_t>(n_tiles) * cs * 4 < 3 * di.sm_count))
       return SPTG_ERR_CONFIG;
   }
   int rc = ensure_smem(dev, v.fn, v.smem);
@@ -1005,19 +1005,19 @@ int run_skinny_rows(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   return SPTG_OK;
 }
 
-// The skinny product (M <= 64) on CTA pairs with the 2-SM MMA, K never split:
+// The skinny product (M <= 128) on CTA pairs with the 2-SM MMA, K never split:
 // each pair owns 2 * n_cta output columns. n_cta is forced (bn) or the
 // multiple of 8 that covers N with at most one CTA per SM; the ring is as
 // deep as shared memory allows (or forced by stages). Returns SPTG_ERR_CONFIG
 // (and launches nothing) when the shape does not suit it -- more than 64
-// columns per CTA, more CTAs than SMs, or fewer than three quarters of the
-// SMs busy -- so that the caller can try the others.
+// columns per CTA, more CTAs than SMs, or (with `fill`) fewer than three
+// quarters of the SMs busy -- so that the caller can try the others.
 int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N,
                     int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-                    int64_t ldc, cudaStream_t stream, const sptg_config& cfg, bool forced) {
-  KernelVariant v;
-  if (d.is_int8 || M > 64 || !skinny_pair_variant(d.in_bf16, d.out_kind, &v)) {
-    if (forced) t_last_error = "the CTA-pair skinny kernel takes float products with M <= 64";
+                    int64_t ldc, cudaStream_t stream, const sptg_config& cfg, bool forced,
+                    bool fill = true) {
+  if (d.is_int8 || M > 128) {
+    if (forced) t_last_error = "the CTA-pair skinny kernel takes float products with M <= 128";
     return SPTG_ERR_CONFIG;
   }
   int64_t nc = cfg.bn;
@@ -1032,14 +1032,20 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   }
   const int64_t pairs = (N + 2 * nc - 1) / (2 * nc);
   if (!forced && (nc > 64 || 2 * pairs > di.sm_count ||
-                  8 * pairs < 3 * static_cast<int64_t>(di.sm_count)))
+                  (fill && 8 * pairs < 3 * static_cast<int64_t>(di.sm_count))))
     return SPTG_ERR_CONFIG;
   if (nc > 64) {
     t_last_error = "N needs more than 64 columns per CTA on this GPU";
     return SPTG_ERR_CONFIG;
   }
+  KernelVariant v;
+  if (!skinny_pair_variant(d.in_bf16, d.out_kind, static_cast<int>(M), static_cast<int>(nc), &v)) {
+    if (forced) t_last_error = "no CTA-pair skinny variant for the requested dtype";
+    return SPTG_ERR_CONFIG;
+  }
+  const int mn = v.bn;  // rows of A on the MMA's N side: 64 or 128
   const int ksub = v.ksub;
-  const int stage_bytes = skinny_pair_stage_bytes(ksub, static_cast<int>(nc));
+  const int stage_bytes = skinny_pair_stage_bytes(ksub, static_cast<int>(nc), mn);
   const int max_stages = std::min(SKINNY_PAIR_MAX_STAGES, SKINNY_PAIR_RING_BUDGET / stage_bytes);
   const int stages = cfg.stages ? cfg.stages : max_stages;
   if (stages < 1 || stages > max_stages) {
@@ -1054,18 +1060,18 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   int load3d = 0;
   if (K % 64 == 0 &&
       make_map_kchunks(&tb, d.in_tma, B, K, N, ldb, static_cast<uint32_t>(nc), ksub) == SPTG_OK &&
-      make_map_kchunks(&ta, d.in_tma, A, K, M, lda, 32, ksub) == SPTG_OK)
+      make_map_kchunks(&ta, d.in_tma, A, K, M, lda, mn / 2, ksub) == SPTG_OK)
     load3d = 1;
   if (!load3d) {
     rc = make_map_2d(&tb, d.in_tma, 2, B, K, N, 64, static_cast<uint32_t>(nc),
                      CU_TENSOR_MAP_SWIZZLE_128B, ldb);
     if (rc) return rc;
-    rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B, lda);
+    rc = make_map_2d(&ta, d.in_tma, 2, A, K, M, 64, mn / 2, CU_TENSOR_MAP_SWIZZLE_128B, lda);
     if (rc) return rc;
   }
-  // the block a CTA stores: 64 rows of n_cta consecutive outputs, unswizzled
-  rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, static_cast<uint32_t>(nc), 64,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, ldc);
+  // the block a CTA stores: mn rows of n_cta consecutive outputs, unswizzled
+  rc = make_map_2d(&tc, d.out_tma, d.out_bytes, C, N, M, static_cast<uint32_t>(nc),
+                   static_cast<uint32_t>(mn), CU_TENSOR_MAP_SWIZZLE_NONE, ldc);
   if (rc) return rc;
   SkinnyPairParams p;
   p.M = static_cast<int>(M);
@@ -1088,9 +1094,9 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   ++t_launches;
   if (e != cudaSuccess) return cuda_fail(e, "skinny_pair_gemm launch");
   set_config(
-      "kernel=skinny-pair dtype=%s mma_m=128 mma_n=64 cols_per_cta=%lld bk=%lld stages=%lld "
+      "kernel=skinny-pair dtype=%s mma_m=128 mma_n=%lld cols_per_cta=%lld bk=%lld stages=%lld "
       "grid=%lld pairs=%lld k_tiles=%lld copies_3d=%lld smem=%lld",
-      d.name, {nc, kstep, stages, grid, pairs, p.num_k_tiles, load3d, smem});
+      d.name, {mn, nc, kstep, stages, grid, pairs, p.num_k_tiles, load3d, smem});
   return SPTG_OK;
 }
 
@@ -1290,23 +1296,35 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
   // swap-AB kernel; everything else -> the square tile kernel.
   int kernel = cfg.kernel;
   if (kernel == 0 && !d.is_int8 && M <= 128 && N >= 1024) {
-    // Memory-bound. Up to 64 rows, with c = N / SMs rounded up to a multiple
-    // of 8 (the output columns one SM would own): the K-loop unsplit on CTA
-    // pairs for 32 <= c <= 64, one CTA per column strip for c > 64; else the
-    // cluster split when it fills the GPU, else stream-K (up to 64 rows) or
-    // the square kernel. Measured with 64 rows on 152 SMs (bfloat16, K =
-    // 8192): N = 2048-3072 cluster split, 4096-9216 pairs, 10240-19456
-    // strips, wider stream-K.
+    // Memory-bound. With c = N / SMs rounded up to a multiple of 8 (the
+    // output columns one SM would own):
+    //  - up to 64 rows: CTA pairs over the whole of K for 32 <= c <= 64, one
+    //    CTA per column strip for 64 < c <= 128, the cluster split for
+    //    c < 32 even where its grid leaves SMs idle (its short K-ranges and
+    //    the 4-CTA exchange beat stream-K there) unless K is long, else the
+    //    cluster split when it fills the GPU, else stream-K;
+    //  - 65-128 rows: CTA pairs for c <= 64 even where they leave SMs idle,
+    //    else the cluster split when it fills the GPU, else the square
+    //    kernel.
+    // Measured on 152 SMs (bfloat16, K = 8192 unless given), us:
+    //   64 rows: N = 1024 cluster 12.9 (stream-K 24.1, pairs 15.1); 2048 13.3
+    //   (17.4, 15.3); 3072 14.8 (16.9, 15.7); 4096-9216 pairs (5120: 16.7
+    //   against cluster 19.6); 10240-19456 strips; wider stream-K; K = 32768,
+    //   N = 1024-2048: stream-K 30-31, cluster 31-32, pairs 49;
+    //   128 rows: N = 1536 pairs 16.1 (square 66.1); 4096 17.3 (square
+    //   63.7); 8192 24.5-25.2 (cluster 27.7).
     const int64_t c = ((N + di.sm_count - 1) / di.sm_count + 7) / 8 * 8;
-    if (M <= 64 && c >= 32 && c <= 64) {
-      rc = run_skinny_pair(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
+    if (c <= 64 && (M > 64 || c >= 32)) {
+      rc = run_skinny_pair(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false,
+                           /*fill=*/M <= 64);
       if (rc != SPTG_ERR_CONFIG) return rc;
     }
     if (M <= 64 && c > 64) {
       rc = run_skinny_rows(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
       if (rc != SPTG_ERR_CONFIG) return rc;
     }
-    rc = run_skinny_cluster(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
+    rc = run_skinny_cluster(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false,
+                            /*fill=*/!(M <= 64 && c < 32 && K <= 16384));
     if (rc != SPTG_ERR_CONFIG) return rc;
     kernel = M <= 64 ? 2 : 1;
   }

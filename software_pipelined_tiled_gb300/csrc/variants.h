@@ -36,9 +36,10 @@ bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, int M, Kerne
 // Skinny kernel with one CTA per strip of output columns (M <= 64, 64-row
 // MMA): bn = 64, stages and smem are chosen per call (0 here).
 bool skinny_rows_variant(bool in_bf16, int out_kind, KernelVariant* v);
-// Skinny kernel on CTA pairs with the 2-SM MMA (M <= 64): the ring depth,
-// stage size and column count are set per call (0 here).
-bool skinny_pair_variant(bool in_bf16, int out_kind, KernelVariant* v);
+// Skinny kernel on CTA pairs with the 2-SM MMA (M <= 128, n_cta output
+// columns per CTA): bn = MMA N (64 or 128 rows of A), ksub = K-chunks per
+// stage; the ring depth and stage size are set per call (0 here).
+bool skinny_pair_variant(bool in_bf16, int out_kind, int M, int n_cta, KernelVariant* v);
 // The streaming ring out = alpha * in (bn = tile bytes).
 KernelVariant stream_variant();
 // int8 -> binary16 widening of both operands in one launch: rows_a rows of

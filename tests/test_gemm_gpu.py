@@ -419,7 +419,12 @@ def test_skinny_rows_limits():
     (1, 2048, 1040, 16, "f16", F16), (17, 1000, 1000, 48, "f16", F32),
     (33, 4096, 520, 64, "bf16", BF16), (64, 256, 64, 8, "bf16", BF16),
     (48, 9216, 2056, 0, "f16", F16), (5, 1000, 4160, 40, "bf16", F32),
-    (64, 1024, 8200, 32, "f16", F32), (40, 200, 640, 64, "bf16", F32)])
+    (64, 1024, 8200, 32, "f16", F32), (40, 200, 640, 64, "bf16", F32),
+    (8, 136, 256, 64, "f16", F16),  # the second CTA of the last pair lies wholly past N
+    # 65-128 rows: the MMA's N side covers 128 rows of A, 64 copied per CTA
+    (128, 8192, 2048, 0, "bf16", BF16), (65, 1000, 1040, 48, "f16", F32),
+    (100, 4096, 520, 64, "bf16", BF16), (128, 200, 640, 8, "f16", F16),
+    (96, 2056, 4160, 40, "bf16", F32)])
 def test_skinny_pair(M, N, K, nc, it, ot):
     A, B = make_inputs(M, N, K, it, "normal", M * 11 + K)
     C = run(A, B, ot, kernel="skinny_pair", bn=nc)
@@ -446,27 +451,30 @@ def test_skinny_pair_is_the_default_for_the_memory_bound_workload():
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 17])
 @pytest.mark.parametrize("stages", [0, 1, 2, 3])
-def test_k_tile_marker_skinny_pair(T, stages):
+@pytest.mark.parametrize("M", [64, 128])
+def test_k_tile_marker_skinny_pair(T, stages, M):
     # every K-chunk lands in the sum exactly once; T not a multiple of the
-    # stage's four chunks leaves the last stage partly empty
-    A, B, expect = _marker_inputs(64, 1024, T, dtype=BF16)
+    # stage's chunks leaves the last stage partly empty
+    A, B, expect = _marker_inputs(M, 1024, T, dtype=BF16)
     C = run(A, B, F32, kernel="skinny_pair", bn=56, stages=stages)
     if stages:
         assert f"stages={stages}" in sptg.last_config()
     assert (C.to(torch.float64) == expect).all()
 
 
-def test_skinny_pair_places_every_row_and_column():
+@pytest.mark.parametrize("M", [64, 128])
+def test_skinny_pair_places_every_row_and_column(M):
     # A[m, k] = m + 1 and Bcm[n, k] = n % 61 + 1: C[m, n] = K (m + 1)(n % 61 + 1),
     # exact, so a row or column of the accumulator read from the wrong place
     # cannot go unseen
-    M, N, K = 64, 2000, 128
+    N, K = 2000, 128
     A = (torch.arange(M, dtype=torch.float32) + 1).repeat(K, 1).t().contiguous().to(BF16)
     Bcm = (torch.arange(N) % 61 + 1).to(torch.float32).repeat(K, 1).t().contiguous().to(BF16)
     expect = K * torch.outer(torch.arange(M, dtype=torch.float64) + 1,
                              (torch.arange(N) % 61 + 1).to(torch.float64))
     for nc in (8, 40, 56, 64):
         C = run(A, Bcm, F32, kernel="skinny_pair", bn=nc)
+        assert f"mma_n={M} " in sptg.last_config()
         assert torch.equal(C.to(torch.float64), expect), nc
 
 
@@ -481,9 +489,9 @@ def test_skinny_pair_ablation_rings_match(stages):
 
 
 def test_skinny_pair_limits():
-    A, B = make_inputs(65, 2048, 1024, "bf16", "normal", 90)
+    A, B = make_inputs(129, 2048, 1024, "bf16", "normal", 90)
     with pytest.raises(sptg.SptgError):
-        run(A, B, BF16, kernel="skinny_pair")  # more than 64 rows
+        run(A, B, BF16, kernel="skinny_pair")  # more than 128 rows
     A, B = make_inputs(64, 2048, 1024, "bf16", "normal", 91)
     for bad in (12, 72):
         with pytest.raises(sptg.SptgError):
@@ -496,11 +504,40 @@ def test_skinny_pair_limits():
     (128, 8192, 4096, "bf16", BF16), (96, 8192, 2048, "f16", F16), (65, 9216, 1040, "bf16", F32),
     (128, 8192, 2048, "f16", F32), (100, 16384, 1024, "bf16", BF16)])
 def test_skinny_cluster_up_to_128_rows(M, N, K, it, ot):
-    # 64 < M <= 128: the swap-AB kernel with MMA N = 128, chosen by default
+    # 64 < M <= 128: the cluster split with MMA N = 128 (the default only past
+    # 64 columns per SM; the CTA pairs take narrower outputs)
     A, B = make_inputs(M, N, K, it, "normal", M + N + K)
-    C = run(A, B, ot)
+    C = run(A, B, ot, kernel="skinny_cluster")
     cfg = sptg.last_config()
     assert "kernel=skinny-cluster" in cfg and "mma_n=128" in cfg, cfg
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("M,N,K,kernel", [
+    (64, 1024, 8192, "kernel=skinny-cluster"), (40, 3072, 4096, "kernel=skinny-cluster"),
+    (64, 1024, 32768, "kernel=skinny "), (64, 6144, 2048, "kernel=skinny-pair"),
+    (64, 12288, 2048, "kernel=skinny-rows"), (64, 32768, 1024, "kernel=skinny ")])
+def test_default_kernel_up_to_64_rows(M, N, K, kernel):
+    # narrow outputs: the cluster split even with SMs idle (stream-K for long
+    # K); 32-64 columns per SM: CTA pairs; 65-128: strips; wider: stream-K
+    A, B = make_inputs(M, N, K, "bf16", "normal", M + N + 1)
+    C = run(A, B, BF16)
+    assert sptg.last_config().startswith(kernel), sptg.last_config()
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("M,N,K,ot", [(128, 8192, 8192, BF16), (96, 4096, 4096, F32),
+                                      (65, 1024, 2048, BF16), (100, 16384, 1024, BF16),
+                                      (128, 1536, 4096, F32)])
+def test_default_kernel_up_to_128_rows(M, N, K, ot):
+    # CTA pairs with MMA N = 128 up to 64 columns per SM, the cluster split past
+    A, B = make_inputs(M, N, K, "bf16", "normal", M + N)
+    C = run(A, B, ot)
+    cfg = sptg.last_config()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    wide = -(-N // sms) > 64
+    assert ("kernel=skinny-cluster" if wide else "kernel=skinny-pair") in cfg, cfg
+    assert "mma_n=128" in cfg, cfg
     assert_float_parity(C, A, B)
 
 
@@ -517,10 +554,10 @@ def test_skinny_cluster_128_rows_limits():
     A, B = make_inputs(96, 2048, 1024, "bf16", "normal", 85)
     with pytest.raises(sptg.SptgError):
         run(A, B, BF16, kernel="skinny_cluster", splits=4)  # no room for 4 ranks
-    # too few column tiles for the cluster split: the square kernel takes it
+    # too few column tiles for the cluster split: CTA pairs over the whole of K
     A, B = make_inputs(100, 1024, 2048, "bf16", "normal", 86)
     C = run(A, B, BF16)
-    assert "kernel=square" in sptg.last_config()
+    assert "kernel=skinny-pair" in sptg.last_config()
     assert_float_parity(C, A, B)
 
 
@@ -669,6 +706,10 @@ def _in_wider(X, pitch, fill):
     ("square", 384, 512, 1024, "f16", F16, {"cta_pair": 1, "stream_k": 2, "splits": 7}),
     ("skinny", 48, 2048, 1024, "bf16", BF16, {}),
     ("skinny_cluster", 64, 4096, 2048, "f16", F16, {"splits": 2}),
+    ("skinny_pair", 64, 4096, 2048, "bf16", F32, {"bn": 56}),
+    ("skinny_pair", 33, 1000, 1096, "f16", F16, {"bn": 24}),
+    ("skinny_rows", 64, 4096, 2048, "f16", F16, {"bn": 72}),
+    ("skinny_rows", 17, 2056, 1096, "bf16", F32, {"bn": 128}),
 ])
 def test_leading_dimensions(kernel, M, N, K, it, ot, extra):
     # A, Bcm and C as column slices of wider buffers: the tiles are read and
@@ -708,6 +749,8 @@ def test_leading_dimensions_int8(stream_k):
     ("s8", I32, 264, 456, 2080, {"cta_pair": 2, "stream_k": 2, "splits": 6}),
     ("bf16", BF16, 48, 2048, 1024, {"kernel": "skinny"}),
     ("bf16", F32, 40, 2056, 2048, {"kernel": "skinny_cluster", "splits": 2}),
+    ("bf16", BF16, 40, 2056, 2048, {"kernel": "skinny_pair", "bn": 64}),
+    ("f16", F32, 5, 1000, 1040, {"kernel": "skinny_rows", "bn": 40}),
 ])
 def test_rows_outside_c_stay_untouched(it, ot, M, N, K, kw):
     # C is rows 8 .. 8 + M of a taller buffer filled with a sentinel: a store
