@@ -96,24 +96,34 @@ bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, int M, Kerne
   return true;
 }
 
-// One CTA per strip of output columns (M <= 64): two 64-wide K-chunks per
-// stage, the ring depth and strip width set per call.
-constexpr int kSkinnyRowsKsub = 2;
-template <bool BF, int OUT>
+// One CTA per strip of output columns (M <= 64), the ring depth and strip
+// width set per call: two 64-wide K-chunks per stage up to 160 columns (a ring
+// of 4 or more stages), one chunk past that, where two leave room for only
+// 2-3 stages (64 x 24576 x 4096, 168 columns: 31.8 us at 7 stages of one
+// chunk against 32.3 us at 3 of two; 64 x 38912 x 2048, 256 columns: 25.6
+// against 27.7 us; 64 x 19456 x 4096, 128 columns: 25.1 us with two chunks
+// against 25.7 us with one).
+template <bool BF, int OUT, int KS>
 KernelVariant make_skinny_rows() {
-  KernelVariant v{reinterpret_cast<const void*>(&skinny_rows_gemm_kernel<BF, OUT, kSkinnyRowsKsub>),
-                  64, 0, 0, false};
-  v.ksub = kSkinnyRowsKsub;
+  KernelVariant v{reinterpret_cast<const void*>(&skinny_rows_gemm_kernel<BF, OUT, KS>), 64, 0, 0,
+                  false};
+  v.ksub = KS;
   return v;
 }
 
-bool skinny_rows_variant(bool in_bf16, int out_kind, KernelVariant* v) {
-  if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny_rows<true, OUT_BF16>();
-  else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny_rows<false, OUT_F16>();
-  else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny_rows<true, OUT_F32>();
-  else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny_rows<false, OUT_F32>();
+template <int KS>
+bool skinny_rows_variant_k(bool in_bf16, int out_kind, KernelVariant* v) {
+  if (out_kind == OUT_BF16 && in_bf16) *v = make_skinny_rows<true, OUT_BF16, KS>();
+  else if (out_kind == OUT_F16 && !in_bf16) *v = make_skinny_rows<false, OUT_F16, KS>();
+  else if (out_kind == OUT_F32 && in_bf16) *v = make_skinny_rows<true, OUT_F32, KS>();
+  else if (out_kind == OUT_F32 && !in_bf16) *v = make_skinny_rows<false, OUT_F32, KS>();
   else return false;
   return true;
+}
+
+bool skinny_rows_variant(bool in_bf16, int out_kind, int n_tile, KernelVariant* v) {
+  return n_tile > 160 ? skinny_rows_variant_k<1>(in_bf16, out_kind, v)
+                      : skinny_rows_variant_k<2>(in_bf16, out_kind, v);
 }
 
 // CTA pairs with the 2-SM MMA over the whole of K. Up to 64 rows (MN = 64):

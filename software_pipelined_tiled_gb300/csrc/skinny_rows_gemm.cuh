@@ -4,8 +4,8 @@
 // C = A * B with A (M x K, M <= 64) and B given as Bcm (N x K). The MMA's M
 // side is the 64 rows of A (rows past M are zero-filled by the copies and
 // never stored); its N side is a strip of n_tile output columns, a multiple
-// of 8 chosen by the host so that the strips cover the SMs about once
-// (8192 columns over 152 SMs: strips of 56, 147 CTAs). Each CTA streams its
+// of 8 up to 256 chosen by the host so that the strips cover the SMs about
+// once (16384 columns over 152 SMs: strips of 112, 147 CTAs). Each CTA streams its
 // n_tile rows of Bcm over the whole of K through a TMA ring whose stages hold
 // KSUB consecutive 64-wide K-chunks of A and of Bcm, accumulates in tensor
 // memory, and its four epilogue warps store the 64 x n_tile block straight
@@ -29,7 +29,7 @@ struct SkinnyRowsParams {
   void* C;
   int64_t ldc;          // row pitch of C, elements
   int M, N, K;
-  int n_tile;           // output columns per CTA: a multiple of 8, 8 ... 128
+  int n_tile;           // output columns per CTA: a multiple of 8, 8 ... 256
   int num_k_tiles;      // ring stages' worth of K: ceil(K / (64 * KSUB))
   int stages;           // ring depth, 1 ... SKINNY_ROWS_MAX_STAGES
   int stage_bytes;      // KSUB * (64 + n_tile) * 128, a multiple of 1024
@@ -41,7 +41,7 @@ struct SkinnyRowsParams {
 };
 
 constexpr int SKINNY_ROWS_MAX_STAGES = 16;
-constexpr int SKINNY_ROWS_MAX_NT = 128;
+constexpr int SKINNY_ROWS_MAX_NT = 256;
 // barriers (2 per stage + 2) and misc words after the ring
 constexpr int SKINNY_ROWS_BAR_BYTES = (2 * SKINNY_ROWS_MAX_STAGES + 2) * 8 + 16;
 // the largest ring the shared memory holds, after 1 KB of alignment slack
@@ -98,7 +98,8 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   volatile int* failed = reinterpret_cast<volatile int*>(misc + 8);
   // tensor-memory columns: a power of two >= 32 that holds the strip
-  const uint32_t tmem_cols = nt_cols <= 32 ? 32u : nt_cols <= 64 ? 64u : 128u;
+  const uint32_t tmem_cols =
+      nt_cols <= 32 ? 32u : nt_cols <= 64 ? 64u : nt_cols <= 128 ? 128u : 256u;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;

@@ -921,22 +921,22 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
 // The skinny product (M <= 64) with one CTA per strip of n_tile output
 // columns over the whole of K: no split, nothing exchanged. The strip width is
 // forced (bn) or the multiple of 8 that covers N with at most one strip per
-// SM; the ring is as deep as shared memory allows (or forced by stages).
-// Returns SPTG_ERR_CONFIG (and launches nothing) when the shape does not suit
-// it -- strips narrower than 32 columns, more strips than SMs, or fewer than
-// three quarters of the SMs busy -- so that the caller can try the others.
+// SM (up to 256); the ring is as deep as shared memory allows (or forced by
+// stages). Returns SPTG_ERR_CONFIG (and launches nothing) when the shape does
+// not suit it -- strips narrower than 32 columns, more strips than SMs, or
+// fewer than three quarters of the SMs busy -- so that the caller can try the
+// others.
 int run_skinny_rows(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N,
                     int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                     int64_t ldc, cudaStream_t stream, const sptg_config& cfg, bool forced) {
-  KernelVariant v;
-  if (d.is_int8 || M > 64 || !skinny_rows_variant(d.in_bf16, d.out_kind, &v)) {
+  if (d.is_int8 || M > 64) {
     if (forced) t_last_error = "the column-strip skinny kernel takes float products with M <= 64";
     return SPTG_ERR_CONFIG;
   }
   int64_t nt = cfg.bn;
   if (forced && nt > 0) {
     if (nt % 8 != 0 || nt < 8 || nt > SKINNY_ROWS_MAX_NT) {
-      t_last_error = "column-strip width (bn) must be a multiple of 8 from 8 to 128";
+      t_last_error = "column-strip width (bn) must be a multiple of 8 from 8 to 256";
       return SPTG_ERR_CONFIG;
     }
   } else {
@@ -948,7 +948,12 @@ int run_skinny_rows(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
                   strips * 4 < 3 * static_cast<int64_t>(di.sm_count)))
     return SPTG_ERR_CONFIG;
   if (nt > SKINNY_ROWS_MAX_NT) {
-    t_last_error = "N needs column strips wider than 128 on this GPU";
+    t_last_error = "N needs column strips wider than 256 on this GPU";
+    return SPTG_ERR_CONFIG;
+  }
+  KernelVariant v;
+  if (!skinny_rows_variant(d.in_bf16, d.out_kind, static_cast<int>(nt), &v)) {
+    if (forced) t_last_error = "no column-strip skinny variant for the requested dtype";
     return SPTG_ERR_CONFIG;
   }
   const int ksub = v.ksub;
@@ -1299,7 +1304,7 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
     // Memory-bound. With c = N / SMs rounded up to a multiple of 8 (the
     // output columns one SM would own):
     //  - up to 64 rows: CTA pairs over the whole of K for 32 <= c <= 64, one
-    //    CTA per column strip for 64 < c <= 128, the cluster split for
+    //    CTA per column strip for 64 < c <= 256, the cluster split for
     //    c < 32 even where its grid leaves SMs idle (its short K-ranges and
     //    the 4-CTA exchange beat stream-K there) unless K is long, else the
     //    cluster split when it fills the GPU, else stream-K;
@@ -1309,8 +1314,9 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
     // Measured on 152 SMs (bfloat16, K = 8192 unless given), us:
     //   64 rows: N = 1024 cluster 12.9 (stream-K 24.1, pairs 15.1); 2048 13.3
     //   (17.4, 15.3); 3072 14.8 (16.9, 15.7); 4096-9216 pairs (5120: 16.7
-    //   against cluster 19.6); 10240-19456 strips; wider stream-K; K = 32768,
-    //   N = 1024-2048: stream-K 30-31, cluster 31-32, pairs 49;
+    //   against cluster 19.6); 10240-38912 strips (32768 x 4096: 40.7
+    //   against stream-K 45.2); wider stream-K; K = 32768, N = 1024-2048:
+    //   stream-K 30-31, cluster 31-32, pairs 49;
     //   128 rows: N = 1536 pairs 16.1 (square 66.1); 4096 17.3 (square
     //   63.7); 8192 24.5-25.2 (cluster 27.7).
     const int64_t c = ((N + di.sm_count - 1) / di.sm_count + 7) / 8 * 8;

@@ -33,9 +33,10 @@ bool skinny_variant(bool in_bf16, int out_kind, int stages, KernelVariant* v);
 // Skinny kernel with K split inside a cluster (launched in clusters of 2-8).
 // M picks the MMA N: 64 for M <= 64, 128 for M <= 128.
 bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, int M, KernelVariant* v);
-// Skinny kernel with one CTA per strip of output columns (M <= 64, 64-row
-// MMA): bn = 64, stages and smem are chosen per call (0 here).
-bool skinny_rows_variant(bool in_bf16, int out_kind, KernelVariant* v);
+// Skinny kernel with one CTA per strip of n_tile output columns (M <= 64,
+// 64-row MMA): bn = 64, ksub = K-chunks per stage; stages and smem are
+// chosen per call (0 here).
+bool skinny_rows_variant(bool in_bf16, int out_kind, int n_tile, KernelVariant* v);
 // Skinny kernel on CTA pairs with the 2-SM MMA (M <= 128, n_cta output
 // columns per CTA): bn = MMA N (64 or 128 rows of A), ksub = K-chunks per
 // stage; the ring depth and stage size are set per call (0 here).

@@ -346,7 +346,10 @@ def test_k_tile_marker_skinny_cluster(T, cs):
     (1, 2048, 1040, 16, "f16", F16), (17, 1000, 1000, 48, "f16", F32),
     (33, 4096, 520, 128, "bf16", BF16), (64, 256, 64, 8, "bf16", BF16),
     (48, 9216, 2056, 0, "f16", F16), (5, 1000, 4160, 120, "bf16", F32),
-    (64, 1024, 8200, 32, "f16", F32)])
+    (64, 1024, 8200, 32, "f16", F32),
+    # strips past 160 columns (one K-chunk per stage) up to 256
+    (64, 32768, 1024, 0, "bf16", BF16), (17, 5000, 1040, 256, "f16", F32),
+    (40, 3000, 2056, 168, "bf16", F32), (64, 2048, 520, 200, "f16", F16)])
 def test_skinny_rows(M, N, K, nt, it, ot):
     A, B = make_inputs(M, N, K, it, "normal", M * 5 + K)
     C = run(A, B, ot, kernel="skinny_rows", bn=nt)
@@ -375,11 +378,13 @@ def test_skinny_rows_is_the_default_for_wide_outputs():
 
 @pytest.mark.parametrize("T", [1, 2, 3, 8, 17])
 @pytest.mark.parametrize("stages", [0, 1, 2, 3])
-def test_k_tile_marker_skinny_rows(T, stages):
+@pytest.mark.parametrize("nt", [64, 192])
+def test_k_tile_marker_skinny_rows(T, stages, nt):
     # every K-chunk lands in the sum exactly once, whatever the ring depth;
-    # an odd T leaves the second chunk of the last stage empty
+    # an odd T leaves the second chunk of the last stage empty (two chunks per
+    # stage up to 160 columns, one past that)
     A, B, expect = _marker_inputs(64, 1024, T, dtype=BF16)
-    C = run(A, B, F32, kernel="skinny_rows", bn=64, stages=stages)
+    C = run(A, B, F32, kernel="skinny_rows", bn=nt, stages=stages)
     if stages:
         assert f"stages={stages}" in sptg.last_config()
     assert (C.to(torch.float64) == expect).all()
@@ -400,7 +405,7 @@ def test_skinny_rows_limits():
     with pytest.raises(sptg.SptgError):
         run(A, B, BF16, kernel="skinny_rows")  # more than 64 rows
     A, B = make_inputs(64, 2048, 1024, "bf16", "normal", 88)
-    for bad in (12, 136):
+    for bad in (12, 264):
         with pytest.raises(sptg.SptgError):
             run(A, B, BF16, kernel="skinny_rows", bn=bad)
     with pytest.raises(sptg.SptgError):
@@ -516,10 +521,11 @@ def test_skinny_cluster_up_to_128_rows(M, N, K, it, ot):
 @pytest.mark.parametrize("M,N,K,kernel", [
     (64, 1024, 8192, "kernel=skinny-cluster"), (40, 3072, 4096, "kernel=skinny-cluster"),
     (64, 1024, 32768, "kernel=skinny "), (64, 6144, 2048, "kernel=skinny-pair"),
-    (64, 12288, 2048, "kernel=skinny-rows"), (64, 32768, 1024, "kernel=skinny ")])
+    (64, 12288, 2048, "kernel=skinny-rows"), (64, 32768, 1024, "kernel=skinny-rows"),
+    (64, 40960, 1024, "kernel=skinny ")])
 def test_default_kernel_up_to_64_rows(M, N, K, kernel):
     # narrow outputs: the cluster split even with SMs idle (stream-K for long
-    # K); 32-64 columns per SM: CTA pairs; 65-128: strips; wider: stream-K
+    # K); 32-64 columns per SM: CTA pairs; 65-256: strips; wider: stream-K
     A, B = make_inputs(M, N, K, "bf16", "normal", M + N + 1)
     C = run(A, B, BF16)
     assert sptg.last_config().startswith(kernel), sptg.last_config()
