@@ -555,6 +555,16 @@ double stream_k_fixed_us(int k_tiles) { return 8.0 + 0.1 * k_tiles; }
 // 16384^3 5 %, 8192 x 8192 x 16384 2-3 %; 8192^3 and 12288^3 even.
 constexpr double kWideEpilogueUs = 6.0;
 
+// A CTA pair costs a fixed extra over its K-loop rate: the cluster launch,
+// the pair's barrier and tensor-memory set-up and teardown, and a tail its
+// halved B traffic cannot pay back within one round. Products of one round
+// (CUDA-graph replay, binary16, us, single / pair): 256^3 3.71 / 4.23,
+// 512^3 4.71 / 5.04, 1024^3 6.72 / 7.17, 1536^3 9.30 / 10.62, 1024 x 1024 x
+// 4096 17.50 / 17.84, 1024 x 4096 x 1024 9.62 / 10.22, 2048^3 15.40 / 15.17;
+// the rate model alone put the pair 0.05-1.8 us ahead in all of them. 1.4 us
+// makes it pick the faster mode in each.
+constexpr double kPairFixedUs = 1.4;
+
 void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sptg_config& cfg,
                          bool int8, int* bn_out, bool* pair_out, bool* sk_out) {
   double best = 1e300;
@@ -577,7 +587,7 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
       const double rate = (pair ? kRatePair[i] : kRateSingle[i]) * 1e6;  // FLOP per us
       const double t_k = 2.0 * rows * bn * 64 / (rate / W);            // us per K-tile
       for (int sk = 0; sk < 2; ++sk) {
-        double cost = static_cast<double>((T + W - 1) / W) * KT * t_k;
+        double cost = static_cast<double>((T + W - 1) / W) * KT * t_k + (pair ? kPairFixedUs : 0.0);
         if (bn == 512) {
           // one accumulator: each round's epilogue is exposed; never cut
           if (sk) continue;
@@ -588,7 +598,8 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
           int skt, skw, mc;
           plan_stream_k(T, W, KT, 0, &skt, &skw, &mc);
           if (skt == 0) continue;
-          cost = static_cast<double>(T) / W * KT * t_k + stream_k_fixed_us(KT);
+          cost = static_cast<double>(T) / W * KT * t_k + stream_k_fixed_us(KT) +
+                 (pair ? kPairFixedUs : 0.0);
         }
         if (cost < best) {
           best = cost;
