@@ -975,7 +975,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--shape", default=None,
-                    help="M,N,K,dtype_pair: time another shape (uniform inputs, seed 1)")
+                    help="M,N,K,dtype_pair: time another shape (seed 1, values per --dist)")
+    ap.add_argument("--dist", default=None, choices=["uniform", "normal", "int8", "zeros"],
+                    help="--shape inputs: 2 U[0,1) - 1 (default for floats), N(0,1), every "
+                         "int8 value (default for int8), or all zero")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--stages", type=int, default=0, help="force the ring depth (ablation)")
     ap.add_argument("--bn", type=int, default=0, help="force the square tile width")
@@ -1012,8 +1015,9 @@ def main(argv=None):
     if args.shape:
         from workloads import Workload
         m, n, k, pair = args.shape.split(",")
-        w = Workload(f"{pair}_{m}x{n}x{k}", int(m), int(n), int(k), pair,
-                     "int8" if pair.startswith("s8") else "uniform", 1.0, 1)
+        dist = args.dist or ("int8" if pair.startswith("s8") else "uniform")
+        w = Workload(f"{pair}_{m}x{n}x{k}" + (f"_{dist}" if args.dist else ""), int(m), int(n),
+                     int(k), pair, dist, 1.0, 1)
     else:
         w = WORKLOADS[args.workload]
     if args.sweep:

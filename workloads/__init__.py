@@ -11,7 +11,9 @@ Recipe (the same for every workload):
 * ``uniform``: ``2 * U[0, 1) - 1`` in float32, then rounded to the input type
   with round-to-nearest-even (``Tensor.to``);
 * ``normal``: ``std * N(0, 1)`` in float32, then rounded the same way;
-* ``int8``: ``randint(-128, 128)``, i.e. every integer in [-128, 127].
+* ``int8``: ``randint(-128, 128)``, i.e. every integer in [-128, 127];
+* ``zeros``: all zero (no random draws), for measurements of how the
+  values themselves affect the GPU's clock.
 """
 from __future__ import annotations
 
@@ -80,6 +82,8 @@ def _draw(g: torch.Generator, shape, in_type: str, dist: str, scale: float) -> t
         if in_type != "s8":
             raise ValueError("int8 draws need an s8 input type")
         return torch.randint(-128, 128, shape, generator=g, dtype=torch.int8)
+    if dist == "zeros":
+        return torch.zeros(shape, dtype=TORCH_DTYPE[in_type])
     if dist == "uniform":
         x = torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0
     elif dist == "normal":
