@@ -95,7 +95,7 @@ typedef struct {
   int bn;       /* square: tile columns, one of 128, 160, 192, 224, 256, or
                    512 for float CTA pairs; skinny column strips (kernel 4):
                    a multiple of 8 from 8 to 256; skinny CTA pairs (kernel
-                   5): a multiple of 8 from 8 to 64                          */
+                   5): a multiple of 8 from 8 to 128                         */
   int stages;   /* shared-memory ring depth (1 = synchronous load/compute)  */
   int splits;   /* square: cap on persistent workers; skinny stream-K: CTAs
                    sharing the work (0 = SM count); skinny cluster: cluster

@@ -132,8 +132,9 @@ bool skinny_rows_variant(bool in_bf16, int out_kind, int n_tile, KernelVariant* 
 // twice the ring depth, 36.9 us with one). 65-128 rows (MN = 128), whose rows
 // of A take twice the room: two chunks per stage (128 x 8192 x 8192: 25.2 us
 // against 26.4 us with four chunks at 3 stages), four up to 40 columns per CTA
-// (128 x 4096 x 8192: 17.5 against 22.3 us). The ring depth and each CTA's
-// column count are set per call.
+// (128 x 4096 x 8192: 17.5 against 22.3 us). Past 64 columns per CTA (two
+// 64-row blocks of Bcm rows, two MMAs per K-step) two chunks per stage for
+// either MN. The ring depth and each CTA's column count are set per call.
 template <int MN, bool BF, int OUT, int KS>
 KernelVariant make_skinny_pair() {
   KernelVariant v{reinterpret_cast<const void*>(&skinny_pair_gemm_kernel<MN, BF, OUT, KS>), MN, 0,
@@ -153,7 +154,11 @@ bool skinny_pair_variant_mn(bool in_bf16, int out_kind, KernelVariant* v) {
 }
 
 bool skinny_pair_variant(bool in_bf16, int out_kind, int M, int n_cta, KernelVariant* v) {
-  if (M <= 64) return skinny_pair_variant_mn<64, 4>(in_bf16, out_kind, v);
+  if (M <= 64) {
+    // past 64 columns four chunks would leave room for only 2-3 stages
+    if (n_cta <= 64) return skinny_pair_variant_mn<64, 4>(in_bf16, out_kind, v);
+    return skinny_pair_variant_mn<64, 2>(in_bf16, out_kind, v);
+  }
   if (M <= 128) {
     if (n_cta <= 40) return skinny_pair_variant_mn<128, 4>(in_bf16, out_kind, v);
     return skinny_pair_variant_mn<128, 2>(in_bf16, out_kind, v);

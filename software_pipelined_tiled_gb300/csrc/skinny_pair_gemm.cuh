@@ -3,9 +3,10 @@
 //
 // Swap-AB as in skinny_gemm.cuh: D^T[n, m] = sum_k Bcm[n, k] * A[m, k]. The
 // MMA's N side covers MN = 64 or 128 rows of A. A pair of CTAs (a cluster of
-// two) owns 2 * n_cta consecutive output columns; CTA rank r loads the n_cta
-// rows of Bcm of its own columns (into a 64-row operand tile; rows past n_cta
-// are never stored) and the MN / 2 rows r * MN / 2 ... of A. The leader's
+// two) owns 2 * n_cta consecutive output columns (n_cta <= 128); CTA rank r
+// loads the n_cta rows of Bcm of its own columns (in blocks of 64 rows, one
+// MMA each; rows past n_cta are never stored) and the MN / 2 rows
+// r * MN / 2 ... of A. The leader's
 // tcgen05.mma.cta_group::2 (M = 128 over the pair's columns, N = MN over the
 // rows of A) reads both CTAs' shared memory, so each SM copies only half of
 // A per K-chunk, and each CTA's tensor memory receives the sums of its own
@@ -34,7 +35,7 @@ namespace sptg {
 
 struct SkinnyPairParams {
   int M, N, K;
-  int n_cta;        // output columns per CTA: a multiple of 8, 8 ... 64
+  int n_cta;        // output columns per CTA: a multiple of 8, 8 ... 128
   int num_k_tiles;  // ring stages' worth of K: ceil(K / (64 * KSUB))
   int stages;       // ring depth, 1 ... SKINNY_PAIR_MAX_STAGES
   int stage_bytes;  // skinny_pair_stage_bytes(KSUB, n_cta, MN)
@@ -55,13 +56,14 @@ constexpr int SKINNY_PAIR_SUB_B = 64 * 128;  // the MMA's 64-row operand tile of
 __host__ __device__ constexpr int skinny_pair_sub_a(int mn) { return mn / 2 * 128; }
 
 // One ring stage: the KSUB K-chunks of this CTA's n_cta rows of Bcm back to
-// back (as one 3-D copy writes them) -- the MMA reads a 64-row tile from the
-// start of each, so the region holds (KSUB - 1) packed chunks and one full
-// tile -- then the KSUB chunks of its MN / 2 rows of A. A multiple of 1024
-// bytes (n_cta is a multiple of 8), which keeps every chunk on the swizzle
-// pattern.
+// back (as one 3-D copy writes them) -- the MMAs read 64-row tiles from the
+// start of each (one per 64-row block), so the region holds (KSUB - 1) packed
+// chunks and the blocks of one more -- then the KSUB chunks of its MN / 2 rows
+// of A. A multiple of 1024 bytes (n_cta is a multiple of 8), which keeps
+// every chunk on the swizzle pattern.
+__host__ __device__ constexpr int skinny_pair_blocks(int n_cta) { return (n_cta + 63) / 64; }
 __host__ __device__ constexpr int skinny_pair_b_region(int ksub, int n_cta) {
-  return (ksub - 1) * n_cta * 128 + SKINNY_PAIR_SUB_B;
+  return (ksub - 1) * n_cta * 128 + skinny_pair_blocks(n_cta) * SKINNY_PAIR_SUB_B;
 }
 __host__ __device__ constexpr int skinny_pair_stage_bytes(int ksub, int n_cta, int mn) {
   return skinny_pair_b_region(ksub, n_cta) + ksub * skinny_pair_sub_a(mn);
@@ -77,16 +79,10 @@ __global__ void __launch_bounds__(192, 1)
   constexpr int OBYTES = OutTraits<OUT>::bytes;
   constexpr int HALF = MN / 2;  // rows of A each CTA copies
   constexpr int SUB_A = skinny_pair_sub_a(MN);
-  constexpr uint32_t TMEM_COLS = 64;  // holds HALF <= 64 columns
   // kind::f16, fp32 accumulation, M = 128 (the pair), N = MN
   constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, 128, MN);
   static_assert(MN == 64 || MN == 128, "MN must be 64 or 128");
   static_assert(OUT != OUT_S32, "float outputs only");
-  // C staging (in stage 0 once the K-loop is over): MN rows of n_cta outputs;
-  // both sides grow linearly with n_cta, so the ends 8 and 64 bound it
-  static_assert(MN * 8 * OBYTES <= skinny_pair_stage_bytes(KSUB, 8, MN) &&
-                    MN * 64 * OBYTES <= skinny_pair_stage_bytes(KSUB, 64, MN),
-                "the output block must fit one stage");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -120,6 +116,10 @@ __global__ void __launch_bounds__(192, 1)
   // j * n_cta rows and its rows past n_cta (the next chunk's, or unused ones)
   // only reach sums that are never stored.
   const int sub_b = n_cta * 128;
+  // 64-row blocks of the CTA's columns: one MMA (and one accumulator of HALF
+  // tensor-memory columns) each
+  const int nblk = skinny_pair_blocks(n_cta);
+  const uint32_t tmem_cols = nblk * HALF <= 32 ? 32u : nblk * HALF <= 64 ? 64u : 128u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tensor_map(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc_g<true>(smem_addr(tmem_slot), TMEM_COLS);
+    tmem_alloc_g<true>(smem_addr(tmem_slot), tmem_cols);
     tmem_relinquish_g<true>();
   }
   tc_fence_before();
@@ -246,11 +246,15 @@ __global__ void __launch_bounds__(192, 1)
           trace_ktile(p.trace, 1, static_cast<uint32_t>(kt));
 #pragma unroll
           for (int j = 0; j < KSUB; ++j) {
+            for (int h = 0; h < nblk; ++h) {
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              mma_f16_g<true>(tmem_base, sdesc_k_major_sw128(stage_b(s) + j * sub_b + 32 * k),
-                              sdesc_k_major_sw128(stage_a(s) + j * SUB_A + 32 * k),
-                              IDESC, (kt > 0 || j > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < BK / 16; ++k) {
+                mma_f16_g<true>(tmem_base + h * HALF,
+                                sdesc_k_major_sw128(stage_b(s) + j * sub_b + h * SKINNY_PAIR_SUB_B +
+                                                    32 * k),
+                                sdesc_k_major_sw128(stage_a(s) + j * SUB_A + 32 * k), IDESC,
+                                (kt > 0 || j > 0 || k > 0) ? 1u : 0u);
+              }
             }
           }
           mma_commit_g<true>(empty_bar(s));  // stage s may be refilled in both CTAs
@@ -274,35 +278,40 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     // warps 2-5: the warp of lane quarter q (= warp % 4) reads lanes
-    // 32q ... 32q + 31, which hold the CTA's columns 32 (q % 2) ... + 31, each
-    // with the sums for the MN / 2 rows of A from (MN / 2)(q / 2) on
+    // 32q ... 32q + 31, which hold the columns 64h + 32 (q % 2) ... + 31 of
+    // block h (in tensor-memory columns h * MN / 2 ...), each with the sums
+    // for the MN / 2 rows of A from (MN / 2)(q / 2) on
     const int q = warp & 3;
-    const int col = 32 * (q & 1) + lane;  // column within the CTA's block
-    const int m0 = HALF * (q >> 1);       // first row of A this warp's sums belong to
-    const bool have_col = col < n_cta;
+    const int m0 = HALF * (q >> 1);  // first row of A this warp's sums belong to
     const bool done = __all_sync(0xffffffffu, wait_bounded(tfull_bar, 0, ctl, WAIT_EPI_TMEM_FULL));
     const bool ok = named_barrier_and(1, 128, done && !*failed);
     if (ok) {
       tc_fence_after();
-      // stage the MN x n_cta block of C (row m holds consecutive outputs) in
-      // ring stage 0, free once every MMA has completed
+      // stage the MN x n_cta block of C (row m holds consecutive outputs) at
+      // the start of the ring, free once every MMA has completed (the host
+      // checks that the ring holds it)
       uint8_t* stage = smem;
+      for (int h = 0; h < nblk; ++h) {
+        const int col = 64 * h + 32 * (q & 1) + lane;  // column within the CTA's block
+        const bool have_col = col < n_cta;
 #pragma unroll
-      for (int cb = 0; cb < HALF; cb += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + cb, r);
-        tmem_wait_ld_regs(r);
-        if (have_col) {
+        for (int cb = 0; cb < HALF; cb += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + h * HALF + cb,
+                             r);
+          tmem_wait_ld_regs(r);
+          if (have_col) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int m = m0 + cb + i;
-            const float v = __uint_as_float(r[i]);
-            if constexpr (OBYTES == 4) {
-              reinterpret_cast<float*>(stage)[m * n_cta + col] = v;
-            } else if constexpr (OUT == OUT_F16) {
-              reinterpret_cast<__half*>(stage)[m * n_cta + col] = __float2half_rn(v);
-            } else {
-              reinterpret_cast<__nv_bfloat16*>(stage)[m * n_cta + col] = __float2bfloat16_rn(v);
+            for (int i = 0; i < 32; ++i) {
+              const int m = m0 + cb + i;
+              const float v = __uint_as_float(r[i]);
+              if constexpr (OBYTES == 4) {
+                reinterpret_cast<float*>(stage)[m * n_cta + col] = v;
+              } else if constexpr (OUT == OUT_F16) {
+                reinterpret_cast<__half*>(stage)[m * n_cta + col] = __float2half_rn(v);
+              } else {
+                reinterpret_cast<__nv_bfloat16*>(stage)[m * n_cta + col] = __float2bfloat16_rn(v);
+              }
             }
           }
         }
@@ -324,7 +333,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) trace_mark(p.trace, TR_EXIT);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc_g<true>(tmem_base, TMEM_COLS);
+    tmem_dealloc_g<true>(tmem_base, tmem_cols);
   }
 }
 

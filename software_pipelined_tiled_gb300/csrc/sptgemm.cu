@@ -1025,7 +1025,7 @@ int run_skinny_rows(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
 // each pair owns 2 * n_cta output columns. n_cta is forced (bn) or the
 // multiple of 8 that covers N with at most one CTA per SM; the ring is as
 // deep as shared memory allows (or forced by stages). Returns SPTG_ERR_CONFIG
-// (and launches nothing) when the shape does not suit it -- more than 64
+// (and launches nothing) when the shape does not suit it -- more than 128
 // columns per CTA, more CTAs than SMs, or (with `fill`) fewer than three
 // quarters of the SMs busy -- so that the caller can try the others.
 int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N,
@@ -1038,8 +1038,8 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   }
   int64_t nc = cfg.bn;
   if (forced && nc > 0) {
-    if (nc % 8 != 0 || nc < 8 || nc > 64) {
-      t_last_error = "columns per CTA (bn) must be a multiple of 8 from 8 to 64";
+    if (nc % 8 != 0 || nc < 8 || nc > 128) {
+      t_last_error = "columns per CTA (bn) must be a multiple of 8 from 8 to 128";
       return SPTG_ERR_CONFIG;
     }
   } else {
@@ -1047,11 +1047,11 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
     if (nc < 8) nc = 8;
   }
   const int64_t pairs = (N + 2 * nc - 1) / (2 * nc);
-  if (!forced && (nc > 64 || 2 * pairs > di.sm_count ||
+  if (!forced && (nc > 128 || 2 * pairs > di.sm_count ||
                   (fill && 8 * pairs < 3 * static_cast<int64_t>(di.sm_count))))
     return SPTG_ERR_CONFIG;
-  if (nc > 64) {
-    t_last_error = "N needs more than 64 columns per CTA on this GPU";
+  if (nc > 128) {
+    t_last_error = "N needs more than 128 columns per CTA on this GPU";
     return SPTG_ERR_CONFIG;
   }
   KernelVariant v;
@@ -1066,6 +1066,11 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   const int stages = cfg.stages ? cfg.stages : max_stages;
   if (stages < 1 || stages > max_stages) {
     t_last_error = "ring depth out of range for the CTA-pair skinny kernel";
+    return SPTG_ERR_CONFIG;
+  }
+  // the epilogue stages the CTA's mn x nc block of C in the ring
+  if (static_cast<int64_t>(mn) * nc * d.out_bytes > static_cast<int64_t>(stages) * stage_bytes) {
+    t_last_error = "the CTA-pair skinny kernel's output block does not fit this ring depth";
     return SPTG_ERR_CONFIG;
   }
   const int smem = stages * stage_bytes + SKINNY_PAIR_BAR_BYTES + 1024;
@@ -1319,9 +1324,9 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
     //    c < 32 even where its grid leaves SMs idle (its short K-ranges and
     //    the 4-CTA exchange beat stream-K there) unless K is long, else the
     //    cluster split when it fills the GPU, else stream-K;
-    //  - 65-128 rows: CTA pairs for c <= 64 even where they leave SMs idle,
-    //    else the cluster split when it fills the GPU, else the square
-    //    kernel.
+    //  - 65-128 rows: CTA pairs for c <= 128 (two 64-column blocks per CTA
+    //    past 64) even where they leave SMs idle, else the cluster split when
+    //    it fills the GPU, else the square kernel.
     // Measured on 152 SMs (bfloat16, K = 8192 unless given), us:
     //   64 rows: N = 1024 cluster 12.9 (stream-K 24.1, pairs 15.1); 2048 13.3
     //   (17.4, 15.3); 3072 14.8 (16.9, 15.7); 4096-9216 pairs (5120: 16.7
@@ -1329,9 +1334,12 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
     //   against stream-K 45.2); wider stream-K; K = 32768, N = 1024-2048:
     //   stream-K 30-31, cluster 31-32, pairs 49;
     //   128 rows: N = 1536 pairs 16.1 (square 66.1); 4096 17.3 (square
-    //   63.7); 8192 24.5-25.2 (cluster 27.7).
+    //   63.7); 8192 24.5-25.2 (cluster 27.7); 10240 34.9 (square 36.5);
+    //   96 x 14336: 40.3 (square 44.3); 16384-19456 K = 4096 level with the
+    //   cluster split. Up to 64 rows the strips beat pairs past c = 64
+    //   (10240: 29.2 against 31.9).
     const int64_t c = ((N + di.sm_count - 1) / di.sm_count + 7) / 8 * 8;
-    if (c <= 64 && (M > 64 || c >= 32)) {
+    if ((M > 64 && c <= 128) || (c >= 32 && c <= 64)) {
       rc = run_skinny_pair(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false,
                            /*fill=*/M <= 64);
       if (rc != SPTG_ERR_CONFIG) return rc;

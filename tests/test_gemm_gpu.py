@@ -429,7 +429,11 @@ def test_skinny_rows_limits():
     # 65-128 rows: the MMA's N side covers 128 rows of A, 64 copied per CTA
     (128, 8192, 2048, 0, "bf16", BF16), (65, 1000, 1040, 48, "f16", F32),
     (100, 4096, 520, 64, "bf16", BF16), (128, 200, 640, 8, "f16", F16),
-    (96, 2056, 4160, 40, "bf16", F32)])
+    (96, 2056, 4160, 40, "bf16", F32),
+    # past 64 columns per CTA: two 64-row blocks, two MMAs per K-step
+    (64, 16384, 1024, 0, "bf16", BF16), (100, 12288, 520, 88, "f16", F32),
+    (5, 2000, 1040, 128, "bf16", F32), (128, 1000, 2056, 72, "bf16", BF16),
+    (33, 3000, 4104, 120, "f16", F16)])
 def test_skinny_pair(M, N, K, nc, it, ot):
     A, B = make_inputs(M, N, K, it, "normal", M * 11 + K)
     C = run(A, B, ot, kernel="skinny_pair", bn=nc)
@@ -477,7 +481,7 @@ def test_skinny_pair_places_every_row_and_column(M):
     Bcm = (torch.arange(N) % 61 + 1).to(torch.float32).repeat(K, 1).t().contiguous().to(BF16)
     expect = K * torch.outer(torch.arange(M, dtype=torch.float64) + 1,
                              (torch.arange(N) % 61 + 1).to(torch.float64))
-    for nc in (8, 40, 56, 64):
+    for nc in (8, 40, 56, 64, 72, 128):
         C = run(A, Bcm, F32, kernel="skinny_pair", bn=nc)
         assert f"mma_n={M} " in sptg.last_config()
         assert torch.equal(C.to(torch.float64), expect), nc
@@ -498,7 +502,7 @@ def test_skinny_pair_limits():
     with pytest.raises(sptg.SptgError):
         run(A, B, BF16, kernel="skinny_pair")  # more than 128 rows
     A, B = make_inputs(64, 2048, 1024, "bf16", "normal", 91)
-    for bad in (12, 72):
+    for bad in (12, 136):
         with pytest.raises(sptg.SptgError):
             run(A, B, BF16, kernel="skinny_pair", bn=bad)
     with pytest.raises(sptg.SptgError):
@@ -534,16 +538,18 @@ def test_default_kernel_up_to_64_rows(M, N, K, kernel):
 
 @pytest.mark.parametrize("M,N,K,ot", [(128, 8192, 8192, BF16), (96, 4096, 4096, F32),
                                       (65, 1024, 2048, BF16), (100, 16384, 1024, BF16),
-                                      (128, 1536, 4096, F32)])
+                                      (128, 1536, 4096, F32), (128, 24576, 1024, BF16)])
 def test_default_kernel_up_to_128_rows(M, N, K, ot):
-    # CTA pairs with MMA N = 128 up to 64 columns per SM, the cluster split past
+    # CTA pairs with MMA N = 128 up to 128 columns per SM; past that the
+    # 128-column tiles outnumber the SMs, so the square kernel takes it
     A, B = make_inputs(M, N, K, "bf16", "normal", M + N)
     C = run(A, B, ot)
     cfg = sptg.last_config()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    wide = -(-N // sms) > 64
-    assert ("kernel=skinny-cluster" if wide else "kernel=skinny-pair") in cfg, cfg
-    assert "mma_n=128" in cfg, cfg
+    if -(-N // sms) > 128:
+        assert cfg.startswith("kernel=square"), cfg
+    else:
+        assert "kernel=skinny-pair" in cfg and "mma_n=128" in cfg, cfg
     assert_float_parity(C, A, B)
 
 
