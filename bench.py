@@ -984,7 +984,7 @@ def main(argv=None):
     ap.add_argument("--bn", type=int, default=0, help="force the square tile width")
     ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3, 4, 5],
                     help="0 choose, 1 square, 2 skinny stream-K, 3 skinny cluster split, "
-                         "4 skinny column strips (M <= 64), 5 skinny CTA pairs (M <= 128)")
+                         "4 skinny column strips (M <= 64), 5 skinny CTA pairs (M <= 256)")
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="square kernel: 0 choose, 1 one CTA per tile, 2 CTA pair (2-SM MMA)")
     ap.add_argument("--stream-k", type=int, default=0, choices=[0, 1, 2],

@@ -90,7 +90,7 @@ typedef struct {
                    CTAs (splits = cluster size, 1, 2 or 4), 4 skinny
                    (M <= 64, float) with one CTA per strip of output columns
                    over the whole of K (bn = strip width), 5 skinny swap-AB
-                   (M <= 128, float) on CTA pairs with the 2-SM MMA over the
+                   (M <= 256, float) on CTA pairs with the 2-SM MMA over the
                    whole of K (bn = output columns per CTA)                  */
   int bn;       /* square: tile columns, one of 128, 160, 192, 224, 256, or
                    512 for float CTA pairs; skinny column strips (kernel 4):

@@ -134,7 +134,8 @@ bool skinny_rows_variant(bool in_bf16, int out_kind, int n_tile, KernelVariant* 
 // against 26.4 us with four chunks at 3 stages), four up to 40 columns per CTA
 // (128 x 4096 x 8192: 17.5 against 22.3 us). Past 64 columns per CTA (two
 // 64-row blocks of Bcm rows, two MMAs per K-step) two chunks per stage for
-// either MN. The ring depth and each CTA's column count are set per call.
+// either MN. 129-256 rows (MN = 256): two chunks per stage. The ring depth
+// and each CTA's column count are set per call.
 template <int MN, bool BF, int OUT, int KS>
 KernelVariant make_skinny_pair() {
   KernelVariant v{reinterpret_cast<const void*>(&skinny_pair_gemm_kernel<MN, BF, OUT, KS>), MN, 0,
@@ -163,6 +164,7 @@ bool skinny_pair_variant(bool in_bf16, int out_kind, int M, int n_cta, KernelVar
     if (n_cta <= 40) return skinny_pair_variant_mn<128, 4>(in_bf16, out_kind, v);
     return skinny_pair_variant_mn<128, 2>(in_bf16, out_kind, v);
   }
+  if (M <= 256) return skinny_pair_variant_mn<256, 2>(in_bf16, out_kind, v);
   return false;
 }
 

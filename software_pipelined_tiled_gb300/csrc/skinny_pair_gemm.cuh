@@ -1,8 +1,8 @@
-// skinny_pair_gemm.cuh -- the memory-bound skinny product (M <= 128) on CTA
+// skinny_pair_gemm.cuh -- the memory-bound skinny product (M <= 256) on CTA
 // pairs with the 2-SM tensor-core instruction, K never split.
 //
 // Swap-AB as in skinny_gemm.cuh: D^T[n, m] = sum_k Bcm[n, k] * A[m, k]. The
-// MMA's N side covers MN = 64 or 128 rows of A. A pair of CTAs (a cluster of
+// MMA's N side covers MN = 64, 128 or 256 rows of A. A pair of CTAs (a cluster of
 // two) owns 2 * n_cta consecutive output columns (n_cta <= 128); CTA rank r
 // loads the n_cta rows of Bcm of its own columns (in blocks of 64 rows, one
 // MMA each; rows past n_cta are never stored) and the MN / 2 rows
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(192, 1)
   constexpr int SUB_A = skinny_pair_sub_a(MN);
   // kind::f16, fp32 accumulation, M = 128 (the pair), N = MN
   constexpr uint32_t IDESC = idesc_f16_f32acc(IN_BF16, 128, MN);
-  static_assert(MN == 64 || MN == 128, "MN must be 64 or 128");
+  static_assert(MN == 64 || MN == 128 || MN == 256, "MN must be 64, 128 or 256");
   static_assert(OUT != OUT_S32, "float outputs only");
 
   extern __shared__ uint8_t smem_raw[];
@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(192, 1)
   // 64-row blocks of the CTA's columns: one MMA (and one accumulator of HALF
   // tensor-memory columns) each
   const int nblk = skinny_pair_blocks(n_cta);
-  const uint32_t tmem_cols = nblk * HALF <= 32 ? 32u : nblk * HALF <= 64 ? 64u : 128u;
+  const uint32_t tmem_cols =
+      nblk * HALF <= 32 ? 32u : nblk * HALF <= 64 ? 64u : nblk * HALF <= 128 ? 128u : 256u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {

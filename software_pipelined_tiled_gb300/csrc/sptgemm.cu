@@ -1021,7 +1021,7 @@ int run_skinny_rows(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   return SPTG_OK;
 }
 
-// The skinny product (M <= 128) on CTA pairs with the 2-SM MMA, K never split:
+// The skinny product (M <= 256) on CTA pairs with the 2-SM MMA, K never split:
 // each pair owns 2 * n_cta output columns. n_cta is forced (bn) or the
 // multiple of 8 that covers N with at most one CTA per SM; the ring is as
 // deep as shared memory allows (or forced by stages). Returns SPTG_ERR_CONFIG
@@ -1032,8 +1032,8 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
                     int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                     int64_t ldc, cudaStream_t stream, const sptg_config& cfg, bool forced,
                     bool fill = true) {
-  if (d.is_int8 || M > 128) {
-    if (forced) t_last_error = "the CTA-pair skinny kernel takes float products with M <= 128";
+  if (d.is_int8 || M > 256) {
+    if (forced) t_last_error = "the CTA-pair skinny kernel takes float products with M <= 256";
     return SPTG_ERR_CONFIG;
   }
   int64_t nc = cfg.bn;
@@ -1316,7 +1316,7 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
   // Shape class: few output rows and a float type -> the memory-bound
   // swap-AB kernel; everything else -> the square tile kernel.
   int kernel = cfg.kernel;
-  if (kernel == 0 && !d.is_int8 && M <= 128 && N >= 1024) {
+  if (kernel == 0 && !d.is_int8 && M <= 256 && N >= 1024) {
     // Memory-bound. With c = N / SMs rounded up to a multiple of 8 (the
     // output columns one SM would own):
     //  - up to 64 rows: CTA pairs over the whole of K for 32 <= c <= 64, one
@@ -1326,7 +1326,9 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
     //    cluster split when it fills the GPU, else stream-K;
     //  - 65-128 rows: CTA pairs for c <= 128 (two 64-column blocks per CTA
     //    past 64) even where they leave SMs idle, else the cluster split when
-    //    it fills the GPU, else the square kernel.
+    //    it fills the GPU, else the square kernel;
+    //  - 129-256 rows: CTA pairs with MMA N = 256 for c <= 64, else the
+    //    square kernel.
     // Measured on 152 SMs (bfloat16, K = 8192 unless given), us:
     //   64 rows: N = 1024 cluster 12.9 (stream-K 24.1, pairs 15.1); 2048 13.3
     //   (17.4, 15.3); 3072 14.8 (16.9, 15.7); 4096-9216 pairs (5120: 16.7
@@ -1337,9 +1339,11 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
     //   63.7); 8192 24.5-25.2 (cluster 27.7); 10240 34.9 (square 36.5);
     //   96 x 14336: 40.3 (square 44.3); 16384-19456 K = 4096 level with the
     //   cluster split. Up to 64 rows the strips beat pairs past c = 64
-    //   (10240: 29.2 against 31.9).
+    //   (10240: 29.2 against 31.9). 256 rows: N = 4096 (K = 4096) 16.4
+    //   (square 18.0), 8192 32.4-33.4 (square 34.4), 16384 (K = 4096) 31.5
+    //   (square 28.0: three stages fit); 160 rows x 8192: 31.4 (34.1).
     const int64_t c = ((N + di.sm_count - 1) / di.sm_count + 7) / 8 * 8;
-    if ((M > 64 && c <= 128) || (c >= 32 && c <= 64)) {
+    if ((M > 64 && M <= 128 && c <= 128) || (M > 128 && c <= 64) || (c >= 32 && c <= 64)) {
       rc = run_skinny_pair(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false,
                            /*fill=*/M <= 64);
       if (rc != SPTG_ERR_CONFIG) return rc;

@@ -37,9 +37,9 @@ bool skinny_cluster_variant(bool in_bf16, int out_kind, int stages, int M, Kerne
 // 64-row MMA): bn = 64, ksub = K-chunks per stage; stages and smem are
 // chosen per call (0 here).
 bool skinny_rows_variant(bool in_bf16, int out_kind, int n_tile, KernelVariant* v);
-// Skinny kernel on CTA pairs with the 2-SM MMA (M <= 128, n_cta <= 128
-// output columns per CTA): bn = MMA N (64 or 128 rows of A), ksub = K-chunks
-// per stage; the ring depth and stage size are set per call (0 here).
+// Skinny kernel on CTA pairs with the 2-SM MMA (M <= 256, n_cta <= 128
+// output columns per CTA): bn = MMA N (64, 128 or 256 rows of A), ksub =
+// K-chunks per stage; the ring depth and stage size are set per call (0 here).
 bool skinny_pair_variant(bool in_bf16, int out_kind, int M, int n_cta, KernelVariant* v);
 // The streaming ring out = alpha * in (bn = tile bytes).
 KernelVariant stream_variant();

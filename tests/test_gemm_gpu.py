@@ -433,7 +433,10 @@ def test_skinny_rows_limits():
     # past 64 columns per CTA: two 64-row blocks, two MMAs per K-step
     (64, 16384, 1024, 0, "bf16", BF16), (100, 12288, 520, 88, "f16", F32),
     (5, 2000, 1040, 128, "bf16", F32), (128, 1000, 2056, 72, "bf16", BF16),
-    (33, 3000, 4104, 120, "f16", F16)])
+    (33, 3000, 4104, 120, "f16", F16),
+    # 129-256 rows: the MMA's N side covers 256 rows of A, 128 copied per CTA
+    (256, 2048, 1024, 0, "bf16", BF16), (200, 1000, 1040, 72, "f16", F32),
+    (129, 4096, 520, 128, "bf16", F32), (256, 8192, 2048, 0, "f16", F16)])
 def test_skinny_pair(M, N, K, nc, it, ot):
     A, B = make_inputs(M, N, K, it, "normal", M * 11 + K)
     C = run(A, B, ot, kernel="skinny_pair", bn=nc)
@@ -460,18 +463,23 @@ def test_skinny_pair_is_the_default_for_the_memory_bound_workload():
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 17])
 @pytest.mark.parametrize("stages", [0, 1, 2, 3])
-@pytest.mark.parametrize("M", [64, 128])
+@pytest.mark.parametrize("M", [64, 128, 256])
 def test_k_tile_marker_skinny_pair(T, stages, M):
     # every K-chunk lands in the sum exactly once; T not a multiple of the
     # stage's chunks leaves the last stage partly empty
     A, B, expect = _marker_inputs(M, 1024, T, dtype=BF16)
+    if M == 256 and stages == 1:
+        # one 47 KB stage cannot hold the 256 x 56 fp32 output block: refused
+        with pytest.raises(sptg.SptgError):
+            run(A, B, F32, kernel="skinny_pair", bn=56, stages=stages)
+        return
     C = run(A, B, F32, kernel="skinny_pair", bn=56, stages=stages)
     if stages:
         assert f"stages={stages}" in sptg.last_config()
     assert (C.to(torch.float64) == expect).all()
 
 
-@pytest.mark.parametrize("M", [64, 128])
+@pytest.mark.parametrize("M", [64, 128, 256])
 def test_skinny_pair_places_every_row_and_column(M):
     # A[m, k] = m + 1 and Bcm[n, k] = n % 61 + 1: C[m, n] = K (m + 1)(n % 61 + 1),
     # exact, so a row or column of the accumulator read from the wrong place
@@ -498,9 +506,9 @@ def test_skinny_pair_ablation_rings_match(stages):
 
 
 def test_skinny_pair_limits():
-    A, B = make_inputs(129, 2048, 1024, "bf16", "normal", 90)
+    A, B = make_inputs(257, 2048, 1024, "bf16", "normal", 90)
     with pytest.raises(sptg.SptgError):
-        run(A, B, BF16, kernel="skinny_pair")  # more than 128 rows
+        run(A, B, BF16, kernel="skinny_pair")  # more than 256 rows
     A, B = make_inputs(64, 2048, 1024, "bf16", "normal", 91)
     for bad in (12, 136):
         with pytest.raises(sptg.SptgError):
@@ -538,18 +546,22 @@ def test_default_kernel_up_to_64_rows(M, N, K, kernel):
 
 @pytest.mark.parametrize("M,N,K,ot", [(128, 8192, 8192, BF16), (96, 4096, 4096, F32),
                                       (65, 1024, 2048, BF16), (100, 16384, 1024, BF16),
-                                      (128, 1536, 4096, F32), (128, 24576, 1024, BF16)])
-def test_default_kernel_up_to_128_rows(M, N, K, ot):
-    # CTA pairs with MMA N = 128 up to 128 columns per SM; past that the
-    # 128-column tiles outnumber the SMs, so the square kernel takes it
+                                      (128, 1536, 4096, F32), (128, 24576, 1024, BF16),
+                                      (256, 8192, 2048, BF16), (160, 4096, 1024, F32),
+                                      (256, 16384, 1024, BF16)])
+def test_default_kernel_up_to_256_rows(M, N, K, ot):
+    # CTA pairs with MMA N = 128 up to 128 columns per SM (past that the
+    # 128-column tiles outnumber the SMs, so the square kernel takes it);
+    # 129-256 rows: pairs with MMA N = 256 up to 64 columns per SM
     A, B = make_inputs(M, N, K, "bf16", "normal", M + N)
     C = run(A, B, ot)
     cfg = sptg.last_config()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    if -(-N // sms) > 128:
+    c = -(-N // sms)
+    if c > (128 if M <= 128 else 64):
         assert cfg.startswith("kernel=square"), cfg
     else:
-        assert "kernel=skinny-pair" in cfg and "mma_n=128" in cfg, cfg
+        assert "kernel=skinny-pair" in cfg and f"mma_n={128 if M <= 128 else 256}" in cfg, cfg
     assert_float_parity(C, A, B)
 
 
