@@ -67,7 +67,8 @@ enum {
   SPTG_ERR_UNSUPPORTED = -3, /* no CUDA device of compute capability 10.3    */
   SPTG_ERR_LAUNCH = -4,      /* a CUDA runtime error; see sptg_last_error()  */
   SPTG_ERR_TIMEOUT = -5,     /* a kernel gave up a bounded wait (reported by
-                                sptg_device_error)                            */
+                                sptg_device_error); C's contents are then
+                                unspecified                                   */
   SPTG_ERR_NOMEM = -6,       /* scratch memory could not be allocated        */
   SPTG_ERR_CONFIG = -7       /* a forced configuration does not fit          */
 };

@@ -2,17 +2,17 @@
 // pairs with the 2-SM tensor-core instruction, K never split.
 //
 // Swap-AB as in skinny_gemm.cuh: D^T[n, m] = sum_k Bcm[n, k] * A[m, k]. The
-// MMA's N side covers MN = 64, 128 or 256 rows of A. A pair of CTAs (a cluster of
-// two) owns 2 * n_cta consecutive output columns (n_cta <= 128); CTA rank r
-// loads the n_cta rows of Bcm of its own columns (in blocks of 64 rows, one
-// MMA each; rows past n_cta are never stored) and the MN / 2 rows
-// r * MN / 2 ... of A. The leader's
-// tcgen05.mma.cta_group::2 (M = 128 over the pair's columns, N = MN over the
-// rows of A) reads both CTAs' shared memory, so each SM copies only half of
-// A per K-chunk, and each CTA's tensor memory receives the sums of its own
-// columns over the whole of K. Nothing is exchanged between SMs after the
-// K-loop: each CTA converts its MN x n_cta block of C, stages it in shared
-// memory (the ring, idle by then) and writes it with one tensor copy.
+// MMA's N side covers MN = 64, 128 or 256 rows of A. A pair of CTAs (a
+// cluster of two) owns 2 * n_cta consecutive output columns (n_cta <= 128).
+// CTA rank r loads the n_cta rows of Bcm of its own columns, in blocks of 64
+// rows (one MMA each; rows past n_cta are never stored), and the MN / 2 rows
+// r * MN / 2 ... of A. The leader's tcgen05.mma.cta_group::2 (M = 128 over
+// the pair's 64-column blocks, N = MN over the rows of A) reads both CTAs'
+// shared memory, so each SM copies only half of A per K-chunk, and each CTA's
+// tensor memory receives the sums of its own columns over the whole of K.
+// Nothing is exchanged between SMs after the K-loop: each CTA converts its
+// MN x n_cta block of C, stages it in shared memory (the ring, idle by then)
+// and writes it with one tensor copy.
 //
 // Per SM a K-chunk moves (n_cta + MN / 2) x 128 bytes, against (n_cta + 64)
 // x 128 for one CTA per strip (skinny_rows_gemm.cuh, MN = 64) and (128 + MN)
@@ -23,10 +23,11 @@
 // Copies of both CTAs complete on the leader's "full" barrier; the leader's
 // commits arrive on both CTAs' "empty" and "tmem_full" barriers.
 //
-// Tensor-memory layout of the accumulator (cta_group::2, M = 128, N = MN):
+// Tensor-memory layout of an accumulator (cta_group::2, M = 128, N = MN):
 // each CTA holds its 64 rows of D with the N side split in halves: row i's
 // sums for the rows 0 ... MN/2 - 1 of A lie in lane i, those for the rows
-// MN/2 ... MN - 1 in lane 64 + i, each half in columns 0 ... MN/2 - 1.
+// MN/2 ... MN - 1 in lane 64 + i, each half in MN / 2 columns. Block h of a
+// CTA's columns takes the columns h * MN / 2 ... of tensor memory.
 #pragma once
 
 #include "common.cuh"
@@ -107,7 +108,8 @@ __global__ void __launch_bounds__(192, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0 = leader, which issues the MMAs
   // this CTA's first output column
-  const int n_base = static_cast<int>(blockIdx.x >> 1) * 2 * n_cta + static_cast<int>(rank) * n_cta;
+  const int n_base =
+      static_cast<int>(blockIdx.x >> 1) * 2 * n_cta + static_cast<int>(rank) * n_cta;
   const int KT = p.num_k_tiles;
   // bytes that complete one stage's "full" barrier: both CTAs' copies
   const uint32_t stage_tx = 2u * KSUB * static_cast<uint32_t>((n_cta + HALF) * 128);
