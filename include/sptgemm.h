@@ -258,6 +258,24 @@ int sptg_version(void);
 int sptg_plan_square(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, int sm_count,
                      const sptg_config* cfg, int* out);
 
+/*
+ * The whole kernel choice sptg_gemm_ex would make for a shape with
+ * configuration `cfg` (NULL = defaults) on a GPU of `sm_count` SMs, computed
+ * on the host alone (no device is touched). On success out[0..5] = kernel
+ * (1 square, 2 skinny stream-K, 3 skinny cluster split, 4 skinny column
+ * strips, 5 skinny CTA pairs -- the sptg_config.kernel numbering), tile width
+ * (square: BN; 2 and 3: 128; 4: strip width; 5: output columns per CTA),
+ * CTAs launched, CTAs per cluster (1, 2 or 4), the rows of A on a skinny
+ * MMA's N side (64, 128 or 256; 0 for the square kernel) and, for the square
+ * kernel, the tiles cut along K. Assumes every SM holds one CTA and every
+ * cluster of the chosen size fits the GPU (the library asks the device; a
+ * cluster split it cannot place goes to stream-K or the square kernel).
+ * Errors as for sptg_plan_square; SPTG_ERR_CONFIG when a forced kernel does
+ * not take the shape.
+ */
+int sptg_plan(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, int sm_count,
+              const sptg_config* cfg, int* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,7 +36,7 @@ KERNELS = {"auto": 0, "square": 1, "skinny": 2, "skinny_cluster": 3, "skinny_row
 
 # the C functions every build must export (checked by the tests)
 EXPORTS = ("sptg_gemm", "sptg_gemm_ex", "sptg_gemm_strided", "sptg_gemm_host",
-           "sptg_plan_square", "sptg_status_string", "sptg_last_error",
+           "sptg_plan_square", "sptg_plan", "sptg_status_string", "sptg_last_error",
            "sptg_last_config", "sptg_device_error", "sptg_version", "sptg_gemm_skinny_noalloc",
            "sptg_stream_scale", "sptg_stream_scale_ex")
 
@@ -100,6 +100,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sptg_plan_square.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                          ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_int)]
         lib.sptg_plan_square.restype = ctypes.c_int
+        lib.sptg_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                  ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_int)]
+        lib.sptg_plan.restype = ctypes.c_int
         lib.sptg_version.argtypes = []
         lib.sptg_version.restype = ctypes.c_int
         if path is None:
@@ -117,6 +120,21 @@ def plan_square(M: int, N: int, K: int, dtype: str, sm_count: int,
         raise SptgError(rc, last_error() or status_string(rc))
     keys = ("bn", "pair", "tiles", "workers", "stream_k_tiles", "stream_k_workers", "max_contrib")
     return dict(zip(keys, list(out)))
+
+
+def plan(M: int, N: int, K: int, dtype: str, sm_count: int,
+         config: Config | None = None) -> dict:
+    """The kernel sptg_gemm would choose for a shape on a GPU of sm_count SMs (host only)."""
+    out = (ctypes.c_int * 6)()
+    cfg = ctypes.byref(config) if config is not None else None
+    rc = int(load().sptg_plan(M, N, K, DTYPES[dtype], sm_count, cfg, out))
+    if rc != 0:
+        raise SptgError(rc, last_error() or status_string(rc))
+    names = {v: k for k, v in KERNELS.items()}
+    keys = ("kernel", "width", "grid", "cluster", "mma_n", "stream_k_tiles")
+    d = dict(zip(keys, list(out)))
+    d["kernel"] = names[d["kernel"]]
+    return d
 
 
 def status_string(status: int) -> str:

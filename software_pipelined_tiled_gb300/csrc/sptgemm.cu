@@ -837,6 +837,155 @@ int run_skinny(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, int
   return SPTG_OK;
 }
 
+// ------------------------------------------------- skinny kernel geometry
+// Host-only decisions of the skinny kernels, shared by the launches below and
+// by sptg_plan. Each returns SPTG_ERR_CONFIG when the shape does not suit the
+// kernel (with t_last_error set when the kernel was forced).
+
+// Output columns one SM would own: N / SMs rounded up to a multiple of 8.
+int64_t columns_per_sm(int64_t N, int sm_count) {
+  const int64_t c = ((N + sm_count - 1) / sm_count + 7) / 8 * 8;
+  return c < 8 ? 8 : c;
+}
+
+// CTA pairs: output columns per CTA (forced bn, else columns_per_sm) and
+// pairs. Unforced, at most 128 columns per CTA and one CTA per SM, and (with
+// `fill`) at least three quarters of the SMs busy.
+int pair_geometry(int64_t N, int sm_count, const sptg_config& cfg, bool forced, bool fill,
+                  int64_t* nc_out, int64_t* pairs_out) {
+  int64_t nc = cfg.bn;
+  if (forced && nc > 0) {
+    if (nc % 8 != 0 || nc < 8 || nc > 128) {
+      t_last_error = "columns per CTA (bn) must be a multiple of 8 from 8 to 128";
+      return SPTG_ERR_CONFIG;
+    }
+  } else {
+    nc = columns_per_sm(N, sm_count);
+  }
+  const int64_t pairs = (N + 2 * nc - 1) / (2 * nc);
+  if (!forced && (nc > 128 || 2 * pairs > sm_count ||
+                  (fill && 8 * pairs < 3 * static_cast<int64_t>(sm_count))))
+    return SPTG_ERR_CONFIG;
+  if (nc > 128) {
+    t_last_error = "N needs more than 128 columns per CTA on this GPU";
+    return SPTG_ERR_CONFIG;
+  }
+  *nc_out = nc;
+  *pairs_out = pairs;
+  return SPTG_OK;
+}
+
+// Column strips: strip width (forced bn, else columns_per_sm) and strips.
+// Unforced, 32 to 256 columns, at most one strip per SM and at least three
+// quarters of the SMs busy.
+int rows_geometry(int64_t N, int sm_count, const sptg_config& cfg, bool forced, int64_t* nt_out,
+                  int64_t* strips_out) {
+  int64_t nt = cfg.bn;
+  if (forced && nt > 0) {
+    if (nt % 8 != 0 || nt < 8 || nt > SKINNY_ROWS_MAX_NT) {
+      t_last_error = "column-strip width (bn) must be a multiple of 8 from 8 to 256";
+      return SPTG_ERR_CONFIG;
+    }
+  } else {
+    nt = columns_per_sm(N, sm_count);
+  }
+  const int64_t strips = (N + nt - 1) / nt;
+  if (!forced && (nt < 32 || nt > SKINNY_ROWS_MAX_NT || strips > sm_count ||
+                  strips * 4 < 3 * static_cast<int64_t>(sm_count)))
+    return SPTG_ERR_CONFIG;
+  if (nt > SKINNY_ROWS_MAX_NT) {
+    t_last_error = "N needs column strips wider than 256 on this GPU";
+    return SPTG_ERR_CONFIG;
+  }
+  *nt_out = nt;
+  *strips_out = strips;
+  return SPTG_OK;
+}
+
+// Cluster split of variant v: 128-column tiles, K-steps of 64 * v.ksub and
+// the cluster size -- forced (splits), else the largest of 4, 2, 1 whose CTAs
+// (cluster size per column tile) fit the SMs, taken only if the grid fills at
+// least three quarters of the SMs (unless `fill` is false). The receive
+// buffer holds up to 3 x 32 columns (clusters of 4) for MMA N = 64 and 64
+// columns (clusters of 2) for MMA N = 128.
+int cluster_geometry(int64_t N, int64_t K, const KernelVariant& v, int sm_count,
+                     const sptg_config& cfg, bool forced, bool fill, int* n_tiles_out,
+                     int* k_tiles_out, int* cs_out) {
+  const int n_tiles = static_cast<int>((N + 127) / 128);
+  const int kstep = 64 * v.ksub;
+  const int k_tiles = static_cast<int>((K + kstep - 1) / kstep);
+  const int max_cs = v.bn <= 64 ? 4 : 2;
+  int cs = 0;
+  if (forced && cfg.splits > 0) {
+    cs = cfg.splits;
+    if ((cs != 1 && cs != 2 && cs != 4) || cs > max_cs) {
+      t_last_error = max_cs == 4 ? "cluster size must be 1, 2 or 4"
+                                 : "cluster size must be 1 or 2 for more than 64 rows";
+      return SPTG_ERR_CONFIG;
+    }
+  } else {
+    for (int c : {4, 2, 1}) {
+      if (c > max_cs) continue;
+      if (static_cast<int64_t>(n_tiles) * c <= sm_count && k_tiles >= 2 * c) {
+        cs = c;
+        break;
+      }
+    }
+    if (cs == 0 && forced) {
+      t_last_error = "no cluster size fits: the 128-column tiles outnumber the SMs";
+      return SPTG_ERR_CONFIG;
+    }
+    if (cs == 0 || (!forced && fill && static_cast<int64_t>(n_tiles) * cs * 4 < 3 * sm_count))
+      return SPTG_ERR_CONFIG;
+  }
+  *n_tiles_out = n_tiles;
+  *k_tiles_out = k_tiles;
+  *cs_out = cs;
+  return SPTG_OK;
+}
+
+// The automatic choice for a memory-bound shape (float, M <= 256, N >= 1024):
+// the kernels to try in order (5 CTA pairs, 4 column strips, 3 cluster split),
+// each with whether its grid must fill three quarters of the SMs; if none
+// takes the shape, stream-K (M <= 64) or the square kernel does. With c =
+// columns_per_sm(N):
+//  - up to 64 rows: CTA pairs over the whole of K for 32 <= c <= 64, one CTA
+//    per column strip for 64 < c <= 256, the cluster split for c < 32 even
+//    where its grid leaves SMs idle (its short K-ranges and the 4-CTA
+//    exchange beat stream-K there) unless K is long, else the cluster split
+//    when it fills the GPU, else stream-K;
+//  - 65-128 rows: CTA pairs for c <= 128 (two 64-column blocks per CTA past
+//    64) even where they leave SMs idle, else the cluster split when it
+//    fills the GPU, else the square kernel;
+//  - 129-256 rows: CTA pairs with MMA N = 256 for c <= 64, else the square
+//    kernel.
+// Measured on 152 SMs (bfloat16, K = 8192 unless given), us:
+//   64 rows: N = 1024 cluster 12.9 (stream-K 24.1, pairs 15.1); 2048 13.3
+//   (17.4, 15.3); 3072 14.8 (16.9, 15.7); 4096-9216 pairs (5120: 16.7
+//   against cluster 19.6); 10240-38912 strips (32768 x 4096: 40.7
+//   against stream-K 45.2); wider stream-K; K = 32768, N = 1024-2048:
+//   stream-K 30-31, cluster 31-32, pairs 49;
+//   128 rows: N = 1536 pairs 16.1 (square 66.1); 4096 17.3 (square
+//   63.7); 8192 24.5-25.2 (cluster 27.7); 10240 34.9 (square 36.5);
+//   96 x 14336: 40.3 (square 44.3); 16384-19456 K = 4096 level with the
+//   cluster split. Up to 64 rows the strips beat pairs past c = 64
+//   (10240: 29.2 against 31.9). 256 rows: N = 4096 (K = 4096) 16.4
+//   (square 18.0), 8192 32.4-33.4 (square 34.4), 16384 (K = 4096) 31.5
+//   (square 28.0: three stages fit); 160 rows x 8192: 31.4 (34.1).
+struct SkinnyTry {
+  int kernel;
+  bool fill;
+};
+int skinny_order(int64_t M, int64_t N, int64_t K, int sm_count, SkinnyTry out[3]) {
+  const int64_t c = columns_per_sm(N, sm_count);
+  int n = 0;
+  if ((M > 64 && M <= 128 && c <= 128) || (M > 128 && c <= 64) || (c >= 32 && c <= 64))
+    out[n++] = {5, M <= 64};
+  if (M <= 64 && c > 64) out[n++] = {4, true};
+  out[n++] = {3, !(M <= 64 && c < 32 && K <= 16384)};
+  return n;
+}
+
 // The skinny product with K split inside clusters: one cluster of `cs` CTAs
 // per 128-column tile. Returns SPTG_ERR_CONFIG (and launches nothing) when
 // the shape does not suit it, so that the caller can use the stream-K kernel.
@@ -852,39 +1001,11 @@ int run_skinny_cluster(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_
     return SPTG_ERR_CONFIG;
   }
   const int BNT = 128, BK = 64;
-  const int n_tiles = static_cast<int>((N + BNT - 1) / BNT);
   const int kstep = BK * v.ksub;  // K per ring stage
-  const int k_tiles = static_cast<int>((K + kstep - 1) / kstep);
-  // cluster size: forced (splits), else the largest of 4, 2, 1 whose CTAs
-  // (cluster size per column tile) fit the SMs; taken only if the grid fills
-  // at least three quarters of the SMs (unless `fill` is false)
-  // the receive buffer holds up to 3 x 32 columns (clusters of 4) for MMA
-  // N = 64 and 64 columns (clusters of 2) for MMA N = 128
-  const int max_cs = v.bn <= 64 ? 4 : 2;
-  int cs = 0;
-  if (forced && cfg.splits > 0) {
-    cs = cfg.splits;
-    if ((cs != 1 && cs != 2 && cs != 4) || cs > max_cs) {
-      t_last_error = max_cs == 4 ? "cluster size must be 1, 2 or 4"
-                                 : "cluster size must be 1 or 2 for more than 64 rows";
-      return SPTG_ERR_CONFIG;
-    }
-  } else {
-    for (int c : {4, 2, 1}) {
-      if (c > max_cs) continue;
-      if (static_cast<int64_t>(n_tiles) * c <= di.sm_count && k_tiles >= 2 * c) {
-        cs = c;
-        break;
-      }
-    }
-    if (cs == 0 && forced) {
-      t_last_error = "no cluster size fits: the 128-column tiles outnumber the SMs";
-      return SPTG_ERR_CONFIG;
-    }
-    if (cs == 0 || (!forced && fill && static_cast<int64_t>(n_tiles) * cs * 4 < 3 * di.sm_count))
-      return SPTG_ERR_CONFIG;
-  }
-  int rc = ensure_smem(dev, v.fn, v.smem);
+  int n_tiles = 0, k_tiles = 0, cs = 0;
+  int rc = cluster_geometry(N, K, v, di.sm_count, cfg, forced, fill, &n_tiles, &k_tiles, &cs);
+  if (rc) return rc;
+  rc = ensure_smem(dev, v.fn, v.smem);
   if (rc) return rc;
   if (cs > 1 && !forced && cluster_slots(dev, v, cs, di.sm_count) < n_tiles) return SPTG_ERR_CONFIG;
   CUtensorMap tb, ta, tc;
@@ -944,24 +1065,9 @@ int run_skinny_rows(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
     if (forced) t_last_error = "the column-strip skinny kernel takes float products with M <= 64";
     return SPTG_ERR_CONFIG;
   }
-  int64_t nt = cfg.bn;
-  if (forced && nt > 0) {
-    if (nt % 8 != 0 || nt < 8 || nt > SKINNY_ROWS_MAX_NT) {
-      t_last_error = "column-strip width (bn) must be a multiple of 8 from 8 to 256";
-      return SPTG_ERR_CONFIG;
-    }
-  } else {
-    nt = ((N + di.sm_count - 1) / di.sm_count + 7) / 8 * 8;
-    if (nt < 8) nt = 8;
-  }
-  const int64_t strips = (N + nt - 1) / nt;
-  if (!forced && (nt < 32 || nt > SKINNY_ROWS_MAX_NT || strips > di.sm_count ||
-                  strips * 4 < 3 * static_cast<int64_t>(di.sm_count)))
-    return SPTG_ERR_CONFIG;
-  if (nt > SKINNY_ROWS_MAX_NT) {
-    t_last_error = "N needs column strips wider than 256 on this GPU";
-    return SPTG_ERR_CONFIG;
-  }
+  int64_t nt = 0, strips = 0;
+  int rc = rows_geometry(N, di.sm_count, cfg, forced, &nt, &strips);
+  if (rc) return rc;
   KernelVariant v;
   if (!skinny_rows_variant(d.in_bf16, d.out_kind, static_cast<int>(nt), &v)) {
     if (forced) t_last_error = "no column-strip skinny variant for the requested dtype";
@@ -976,7 +1082,7 @@ int run_skinny_rows(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
     return SPTG_ERR_CONFIG;
   }
   const int smem = stages * stage_bytes + SKINNY_ROWS_BAR_BYTES + 1024;
-  int rc = ensure_smem(dev, v.fn, 232448);
+  rc = ensure_smem(dev, v.fn, 232448);
   if (rc) return rc;
   CUtensorMap ta, tb;
   const int kstep = 64 * ksub;
@@ -1036,24 +1142,9 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
     if (forced) t_last_error = "the CTA-pair skinny kernel takes float products with M <= 256";
     return SPTG_ERR_CONFIG;
   }
-  int64_t nc = cfg.bn;
-  if (forced && nc > 0) {
-    if (nc % 8 != 0 || nc < 8 || nc > 128) {
-      t_last_error = "columns per CTA (bn) must be a multiple of 8 from 8 to 128";
-      return SPTG_ERR_CONFIG;
-    }
-  } else {
-    nc = ((N + di.sm_count - 1) / di.sm_count + 7) / 8 * 8;
-    if (nc < 8) nc = 8;
-  }
-  const int64_t pairs = (N + 2 * nc - 1) / (2 * nc);
-  if (!forced && (nc > 128 || 2 * pairs > di.sm_count ||
-                  (fill && 8 * pairs < 3 * static_cast<int64_t>(di.sm_count))))
-    return SPTG_ERR_CONFIG;
-  if (nc > 128) {
-    t_last_error = "N needs more than 128 columns per CTA on this GPU";
-    return SPTG_ERR_CONFIG;
-  }
+  int64_t nc = 0, pairs = 0;
+  int rc = pair_geometry(N, di.sm_count, cfg, forced, fill, &nc, &pairs);
+  if (rc) return rc;
   KernelVariant v;
   if (!skinny_pair_variant(d.in_bf16, d.out_kind, static_cast<int>(M), static_cast<int>(nc), &v)) {
     if (forced) t_last_error = "no CTA-pair skinny variant for the requested dtype";
@@ -1074,7 +1165,7 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
     return SPTG_ERR_CONFIG;
   }
   const int smem = stages * stage_bytes + SKINNY_PAIR_BAR_BYTES + 1024;
-  int rc = ensure_smem(dev, v.fn, 232448);
+  rc = ensure_smem(dev, v.fn, 232448);
   if (rc) return rc;
   CUtensorMap tb, ta, tc;
   const int kstep = 64 * ksub;
@@ -1207,6 +1298,101 @@ int sptg_plan_square(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, int sm_c
   return SPTG_OK;
 }
 
+int sptg_plan(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, int sm_count,
+              const sptg_config* cfg_in, int* out) {
+  DtypeInfo d;
+  if (!out || sm_count < 2 || !dtype_info(dtype, d) || M <= 0 || N <= 0 || K <= 0 ||
+      M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) {
+    t_last_error = "invalid argument";
+    return SPTG_ERR_ARG;
+  }
+  sptg_config cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  if (cfg_in) cfg = *cfg_in;
+  if (cfg.kernel < 0 || cfg.kernel > 5 || cfg.stream_k < 0 || cfg.stream_k > 2 ||
+      cfg.cta_pair < 0 || cfg.cta_pair > 2 || cfg.bn < 0 || cfg.splits < 0 || cfg.stages < 0) {
+    t_last_error = "invalid configuration field";
+    return SPTG_ERR_ARG;
+  }
+  for (int i = 0; i < 6; ++i) out[i] = 0;
+  auto set = [&](int kernel, int64_t width, int64_t grid, int cluster, int mma_n, int cut) -> int {
+    out[0] = kernel;
+    out[1] = static_cast<int>(width);
+    out[2] = static_cast<int>(std::min<int64_t>(grid, INT32_MAX));
+    out[3] = cluster;
+    out[4] = mma_n;
+    out[5] = cut;
+    return SPTG_OK;
+  };
+  auto pair = [&](bool forced, bool fill) -> int {
+    if (d.is_int8 || M > 256) {
+      if (forced) t_last_error = "the CTA-pair skinny kernel takes float products with M <= 256";
+      return SPTG_ERR_CONFIG;
+    }
+    int64_t nc = 0, pairs = 0;
+    int rc = pair_geometry(N, sm_count, cfg, forced, fill, &nc, &pairs);
+    if (rc) return rc;
+    KernelVariant v;
+    if (!skinny_pair_variant(d.in_bf16, d.out_kind, static_cast<int>(M), static_cast<int>(nc), &v))
+      return SPTG_ERR_CONFIG;
+    return set(5, nc, 2 * pairs, 2, v.bn, 0);
+  };
+  auto rows = [&](bool forced) -> int {
+    if (d.is_int8 || M > 64) {
+      if (forced) t_last_error = "the column-strip skinny kernel takes float products with M <= 64";
+      return SPTG_ERR_CONFIG;
+    }
+    int64_t nt = 0, strips = 0;
+    int rc = rows_geometry(N, sm_count, cfg, forced, &nt, &strips);
+    if (rc) return rc;
+    return set(4, nt, strips, 1, 64, 0);
+  };
+  auto cluster = [&](bool forced, bool fill) -> int {
+    KernelVariant v;
+    if (d.is_int8 ||
+        !skinny_cluster_variant(d.in_bf16, d.out_kind, cfg.stages, static_cast<int>(M), &v) ||
+        M > v.bn) {
+      if (forced) t_last_error = "no cluster-split skinny variant for the requested dtype/stages/M";
+      return SPTG_ERR_CONFIG;
+    }
+    int n_tiles = 0, k_tiles = 0, cs = 0;
+    int rc = cluster_geometry(N, K, v, sm_count, cfg, forced, fill, &n_tiles, &k_tiles, &cs);
+    if (rc) return rc;
+    return set(3, 128, static_cast<int64_t>(n_tiles) * cs, cs, v.bn, 0);
+  };
+  int kernel = cfg.kernel;
+  if (kernel == 0 && !d.is_int8 && M <= 256 && N >= 1024) {
+    SkinnyTry order[3];
+    const int n_try = skinny_order(M, N, K, sm_count, order);
+    for (int t = 0; t < n_try; ++t) {
+      const int rc = order[t].kernel == 5   ? pair(false, order[t].fill)
+                     : order[t].kernel == 4 ? rows(false)
+                                            : cluster(false, order[t].fill);
+      if (rc != SPTG_ERR_CONFIG) return rc;
+    }
+    kernel = M <= 64 ? 2 : 1;
+  }
+  if (kernel == 0) kernel = 1;
+  if (kernel == 3) return cluster(true, true);
+  if (kernel == 4) return rows(true);
+  if (kernel == 5) return pair(true, true);
+  if (kernel == 2) {
+    KernelVariant v;
+    if (d.is_int8 || !skinny_variant(d.in_bf16, d.out_kind, cfg.stages, &v) || M > v.bn) {
+      t_last_error = "no skinny-kernel variant for the requested dtype/stages/M";
+      return SPTG_ERR_CONFIG;
+    }
+    const int64_t n_tiles = (N + 127) / 128, kstep = 64 * v.ksub;
+    const int64_t units = n_tiles * ((K + kstep - 1) / kstep);
+    const int64_t grid = std::min<int64_t>(cfg.splits > 0 ? cfg.splits : sm_count, units);
+    return set(2, 128, grid, 1, v.bn, 0);
+  }
+  int sq[7];
+  const int rc = sptg_plan_square(M, N, K, dtype, sm_count, &cfg, sq);
+  if (rc) return rc;
+  return set(1, sq[0], static_cast<int64_t>(sq[3]) * (sq[1] ? 2 : 1), sq[1] ? 2 : 1, 0, sq[4]);
+}
+
 const char* sptg_status_string(int status) {
   switch (status) {
     case SPTG_OK: return "ok";
@@ -1317,44 +1503,20 @@ int sptg_gemm_strided(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, const v
   // swap-AB kernel; everything else -> the square tile kernel.
   int kernel = cfg.kernel;
   if (kernel == 0 && !d.is_int8 && M <= 256 && N >= 1024) {
-    // Memory-bound. With c = N / SMs rounded up to a multiple of 8 (the
-    // output columns one SM would own):
-    //  - up to 64 rows: CTA pairs over the whole of K for 32 <= c <= 64, one
-    //    CTA per column strip for 64 < c <= 256, the cluster split for
-    //    c < 32 even where its grid leaves SMs idle (its short K-ranges and
-    //    the 4-CTA exchange beat stream-K there) unless K is long, else the
-    //    cluster split when it fills the GPU, else stream-K;
-    //  - 65-128 rows: CTA pairs for c <= 128 (two 64-column blocks per CTA
-    //    past 64) even where they leave SMs idle, else the cluster split when
-    //    it fills the GPU, else the square kernel;
-    //  - 129-256 rows: CTA pairs with MMA N = 256 for c <= 64, else the
-    //    square kernel.
-    // Measured on 152 SMs (bfloat16, K = 8192 unless given), us:
-    //   64 rows: N = 1024 cluster 12.9 (stream-K 24.1, pairs 15.1); 2048 13.3
-    //   (17.4, 15.3); 3072 14.8 (16.9, 15.7); 4096-9216 pairs (5120: 16.7
-    //   against cluster 19.6); 10240-38912 strips (32768 x 4096: 40.7
-    //   against stream-K 45.2); wider stream-K; K = 32768, N = 1024-2048:
-    //   stream-K 30-31, cluster 31-32, pairs 49;
-    //   128 rows: N = 1536 pairs 16.1 (square 66.1); 4096 17.3 (square
-    //   63.7); 8192 24.5-25.2 (cluster 27.7); 10240 34.9 (square 36.5);
-    //   96 x 14336: 40.3 (square 44.3); 16384-19456 K = 4096 level with the
-    //   cluster split. Up to 64 rows the strips beat pairs past c = 64
-    //   (10240: 29.2 against 31.9). 256 rows: N = 4096 (K = 4096) 16.4
-    //   (square 18.0), 8192 32.4-33.4 (square 34.4), 16384 (K = 4096) 31.5
-    //   (square 28.0: three stages fit); 160 rows x 8192: 31.4 (34.1).
-    const int64_t c = ((N + di.sm_count - 1) / di.sm_count + 7) / 8 * 8;
-    if ((M > 64 && M <= 128 && c <= 128) || (M > 128 && c <= 64) || (c >= 32 && c <= 64)) {
-      rc = run_skinny_pair(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false,
-                           /*fill=*/M <= 64);
+    // memory-bound: the kernels skinny_order lists, in turn
+    SkinnyTry order[3];
+    const int n_try = skinny_order(M, N, K, di.sm_count, order);
+    for (int t = 0; t < n_try; ++t) {
+      if (order[t].kernel == 5)
+        rc = run_skinny_pair(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false,
+                             order[t].fill);
+      else if (order[t].kernel == 4)
+        rc = run_skinny_rows(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
+      else
+        rc = run_skinny_cluster(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false,
+                                order[t].fill);
       if (rc != SPTG_ERR_CONFIG) return rc;
     }
-    if (M <= 64 && c > 64) {
-      rc = run_skinny_rows(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false);
-      if (rc != SPTG_ERR_CONFIG) return rc;
-    }
-    rc = run_skinny_cluster(dev, di, d, M, N, K, A, lda, B, ldb, C, ldc, stream_h, cfg, false,
-                            /*fill=*/!(M <= 64 && c < 32 && K <= 16384));
-    if (rc != SPTG_ERR_CONFIG) return rc;
     kernel = M <= 64 ? 2 : 1;
   }
   if (kernel == 0) kernel = 1;

@@ -939,6 +939,26 @@ def test_graph_capture_before_the_buffers_exist_is_refused():
     assert_float_parity(run(A, B, F32, stream_k=2, splits=7), A, B)
 
 
+# ------------------------------------------------------- host-only plan
+@pytest.mark.parametrize("M,N,K", [
+    (64, 8192, 4096), (64, 16384, 1024), (64, 1024, 8192), (64, 1024, 32768), (40, 3072, 4096),
+    (64, 40960, 1024), (128, 8192, 2048), (256, 4096, 1024), (256, 16384, 1024),
+    (1024, 1024, 1024), (4096, 4096, 1024)])
+def test_plan_matches_the_launch(M, N, K):
+    # sptg_plan, computed on the host alone, names the kernel and grid the
+    # call then launches
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = sptg.plan(M, N, K, "bf16_bf16", sms)
+    A, B = make_inputs(M, N, K, "bf16", "normal", 5)
+    run(A, B, BF16)
+    cfg = sptg.last_config()
+    prefix = {"square": "kernel=square ", "skinny": "kernel=skinny ",
+              "skinny_cluster": "kernel=skinny-cluster ", "skinny_rows": "kernel=skinny-rows ",
+              "skinny_pair": "kernel=skinny-pair "}[p["kernel"]]
+    assert cfg.startswith(prefix), (p, cfg)
+    assert int(cfg.split("grid=")[1].split()[0]) == p["grid"], (p, cfg)
+
+
 # ------------------------------------------------------------ stream / errors
 def test_async_on_a_side_stream():
     A, B = make_inputs(512, 512, 512, "f16", "uniform", 21)
