@@ -337,7 +337,8 @@ struct ChunkMapEntry {
   int dt = -1;
   CUtensorMap map;
 };
-thread_local ChunkMapEntry t_chunk_maps[8];
+constexpr int kChunkMapCache = 32;  // as many as the 2-D maps: rotating operand sets hit
+thread_local ChunkMapEntry t_chunk_maps[kChunkMapCache];
 thread_local int t_chunk_next = 0;
 
 int make_map_kchunks(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t K,
@@ -363,7 +364,7 @@ int make_map_kchunks(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return SPTG_ERR_ARG;
   ChunkMapEntry& e = t_chunk_maps[t_chunk_next];
-  t_chunk_next = (t_chunk_next + 1) % 8;
+  t_chunk_next = (t_chunk_next + 1) % kChunkMapCache;
   e.base = base;
   e.K = K;
   e.rows = rows;
