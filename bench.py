@@ -125,27 +125,42 @@ class ClockSampler:
         self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, pw, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
+                clk = float(f[1])
                 mx = float(f[2])
             except ValueError:
                 continue
+            try:
+                power = float(f[3])
+            except ValueError:
+                power = None
+            sm.append(clk)
+            pw.append(power)
             for name, val in zip(names, f[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
-        sm_sorted = sorted(sm)
-        # the median over samples taken under load
-        loaded = [x for x in sm_sorted if x > 0.3 * (mx or x)] or sm_sorted
+        # The median over samples taken under load: those drawing at least half
+        # the run's highest power (an idle GPU sits at its maximum clock, so
+        # the samples before and after the timed region would otherwise hide a
+        # clock the power cap pulled down), else those above 30 % of the
+        # maximum clock when no power figure was read.
+        known = [p for p in pw if p is not None]
+        if known:
+            top = max(known)
+            loaded = sorted(c for c, p in zip(sm, pw) if p is not None and p >= 0.5 * top)
+        else:
+            loaded = sorted(c for c in sm if c > 0.3 * (mx or c))
+        loaded = loaded or sorted(sm)
         return {"sm_mhz": loaded[len(loaded) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_under_load": len(loaded)}
 
 
 def sources_hash():

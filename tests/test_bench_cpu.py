@@ -111,3 +111,27 @@ def test_versus_torch_calls():
     for spec in bench.VERSUS_SHAPES.split(";"):
         m, n, k, pair = spec.split(",")
         assert int(m) > 0 and int(n) > 0 and int(k) > 0 and pair in DTYPE_PAIRS
+
+
+def test_clock_summary_counts_samples_under_load():
+    # idle samples before and after the timed region read the maximum clock;
+    # only those drawing at least half the run's highest power count
+    s = bench.ClockSampler(0)
+    idle = "0, 2070, 2070, 180.0, 0x0, Not Active, Not Active, Not Active, Not Active"
+    busy = "0, {c}, 2070, {p}, 0x4, Not Active, Not Active, Not Active, Active"
+    s.lines = [idle, idle, idle, busy.format(c=1500, p=1390.0), busy.format(c=1480, p=1395.0),
+               busy.format(c=1520, p=1380.0), idle]
+    r = s.summary()
+    assert r["sm_mhz"] == 1500 and r["sm_max_mhz"] == 2070
+    assert r["reasons"] == ["sw_power_cap"] and r["samples"] == 7 and r["samples_under_load"] == 3
+    # the roofline then takes the sustained peak: the cap pulled the clock down
+    peaks, _ = bench.measured_peaks()
+    w = Workload("f16_4096x4096x4096_f16out", 4096, 4096, 4096, "f16_f16", "uniform", 1.0, 2)
+    assert bench.roofline(w, 0.08, 100.0, r, "square",
+                          bench.algorithmic_bytes(w))["peak"] == peaks["bf16_tflops_sustained"]
+    # no power figure: the clock filter of before
+    s.lines = ["0, 2070, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 1900, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 300, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active"]
+    r = s.summary()
+    assert r["sm_mhz"] == 2070 and r["samples_under_load"] == 2
