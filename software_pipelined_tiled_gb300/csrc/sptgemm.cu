@@ -1252,7 +1252,7 @@ int noalloc_scratch(int dev, unsigned char** out) {
 // ================================================================ C ABI
 extern "C" {
 
-int sptg_version(void) { return 100; }
+int sptg_version(void) { return 101; }  // 1.01: sptg_plan, skinny kernels 4 and 5
 
 int sptg_plan_square(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, int sm_count,
                      const sptg_config* cfg_in, int* out) {

@@ -53,7 +53,7 @@ def test_dtype_and_status_values_match_header():
 
 
 def test_version_and_status_strings(lib):
-    assert lib.sptg_version() == 100
+    assert lib.sptg_version() == 101
     for code in sptg.STATUS:
         assert sptg.status_string(code) and sptg.status_string(code) != "unknown status"
     assert sptg.status_string(12345) == "unknown status"
