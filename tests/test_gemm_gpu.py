@@ -805,15 +805,21 @@ def test_leading_dimensions_zero_k():
 
 
 # ------------------------------------------------------------ host buffers
-@pytest.mark.parametrize("it,ot", [("f16", F16), ("bf16", F32), ("s8", I32)])
-def test_host_buffers(it, ot):
+@pytest.mark.parametrize("M,N,K,it,ot,kernel", [
+    (264, 520, 1040, "f16", F16, "square"), (264, 520, 1040, "bf16", F32, "square"),
+    (264, 520, 1040, "s8", I32, "square"),
+    # the skinny kernels behind the host-buffer entry point as well
+    (64, 8192, 2048, "bf16", BF16, "skinny-pair"), (64, 16384, 1024, "f16", F16, "skinny-rows"),
+    (40, 3072, 2048, "bf16", F32, "skinny-cluster"), (128, 4096, 1024, "bf16", BF16, "skinny-pair")])
+def test_host_buffers(M, N, K, it, ot, kernel):
     # sptg_gemm_host: operands and result in pinned host memory, the copies
     # enqueued by the library around the product
-    A, B = make_inputs(264, 520, 1040, it, "int8" if it == "s8" else "uniform", 70)
+    A, B = make_inputs(M, N, K, it, "int8" if it == "s8" else "uniform", 70)
     hA, hB = A.pin_memory(), B.pin_memory()
     C = sptg.gemm_host(hA, hB, out_dtype=ot)
     torch.cuda.synchronize()
     assert sptg.device_error() == 0
+    assert sptg.last_config().startswith(f"kernel={kernel} "), sptg.last_config()
     if it == "s8":
         assert_int_parity(C.clone(), A, B)
     else:
