@@ -918,6 +918,40 @@ def test_graph_replays_of_a_skinny_split_call():
     assert "units=" in sptg.last_config()
 
 
+@pytest.mark.parametrize("M,N,K,kernel", [(64, 8192, 2048, "skinny-pair"),
+                                           (128, 4096, 1024, "skinny-pair"),
+                                           (64, 16384, 1024, "skinny-rows"),
+                                           (40, 3072, 2048, "skinny-cluster")])
+def test_graph_replays_of_the_skinny_kernels_with_new_inputs(M, N, K, kernel):
+    # captured once, replayed with new operands copied into the same buffers
+    dA = torch.empty(M, K, dtype=BF16, device="cuda")
+    dB = torch.empty(N, K, dtype=BF16, device="cuda")
+    C = torch.empty(M, N, dtype=BF16, device="cuda")
+    s = torch.cuda.Stream()
+    A, B = make_inputs(M, N, K, "bf16", "normal", 84)
+    dA.copy_(A)
+    dB.copy_(B)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        sptg.gemm(dA, dB, C=C, stream=s)
+    s.synchronize()
+    assert sptg.last_config().startswith(f"kernel={kernel} "), sptg.last_config()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sptg.gemm(dA, dB, C=C, stream=s)
+    torch.cuda.synchronize()
+    for r in range(3):
+        A, B = make_inputs(M, N, K, "bf16", "normal", 85 + r)
+        dA.copy_(A)
+        dB.copy_(B)
+        C.fill_(0)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert sptg.device_error() == 0
+        assert_float_parity(C.cpu(), A, B)
+
+
 def test_graph_replays_of_the_allocation_free_call():
     A, B = make_inputs(64, 4096, 2048, "bf16", "normal", 83)
     dA, dB = A.cuda(), B.cuda()
