@@ -93,8 +93,9 @@ typedef struct {
                    over the whole of K (bn = strip width), 5 skinny swap-AB
                    (M <= 256, float) on CTA pairs with the 2-SM MMA over the
                    whole of K (bn = output columns per CTA)                  */
-  int bn;       /* square: tile columns, one of 128, 160, 192, 224, 256, or
-                   512 for float CTA pairs; skinny column strips (kernel 4):
+  int bn;       /* square: tile columns, 112 to 256 in steps of 16 for
+                   float types (int8: 128, 160, 192, 224 or 256), or 512 for
+                   float CTA pairs; skinny column strips (kernel 4):
                    a multiple of 8 from 8 to 256; skinny CTA pairs (kernel
                    5): a multiple of 8 from 8 to 128                         */
   int stages;   /* shared-memory ring depth (1 = synchronous load/compute)  */

@@ -148,6 +148,29 @@ __device__ __forceinline__ void store_out4(void* C, int64_t idx, float4 v) {
   }
 }
 
+// Stores 8 (16-bit outputs) or 4 (fp32) consecutive outputs of one row from
+// fp32 values; `n_valid` of them lie inside C (all when n_valid >= the group).
+template <int OUT>
+__device__ __forceinline__ void store_row_group(void* row_ptr, int col, const float* v,
+                                                int n_valid) {
+  if constexpr (OUT == OUT_F32) {
+    float* dst = static_cast<float*>(row_ptr) + col;
+    if (n_valid >= 4) {
+      *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+      for (int i = 0; i < n_valid; ++i) dst[i] = v[i];
+    }
+  } else {
+    uint16_t* dst = static_cast<uint16_t*>(row_ptr) + col;
+    if (n_valid >= 8) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(pack2<OUT>(v[0], v[1]), pack2<OUT>(v[2], v[3]),
+                                                  pack2<OUT>(v[4], v[5]), pack2<OUT>(v[6], v[7]));
+    } else {
+      for (int i = 0; i < n_valid; ++i) store_out<OUT>(dst, i, v[i]);
+    }
+  }
+}
+
 // Counts one arrival at a tile's split-K counter and returns whether it was the
 // last of `count`. The 64-bit counter holds (call generation << 32 |
 // arrivals): a value left by an earlier call (or by one that gave up) carries

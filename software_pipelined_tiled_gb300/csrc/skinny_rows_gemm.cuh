@@ -47,29 +47,6 @@ constexpr int SKINNY_ROWS_BAR_BYTES = (2 * SKINNY_ROWS_MAX_STAGES + 2) * 8 + 16;
 // the largest ring the shared memory holds, after 1 KB of alignment slack
 constexpr int SKINNY_ROWS_RING_BUDGET = 232448 - 1024 - SKINNY_ROWS_BAR_BYTES;
 
-// Stores 8 (16-bit outputs) or 4 (fp32) consecutive outputs of one row from
-// fp32 values; `n_valid` of them lie inside C (all when n_valid >= the group).
-template <int OUT>
-__device__ __forceinline__ void store_row_group(void* row_ptr, int col, const float* v,
-                                                int n_valid) {
-  if constexpr (OUT == OUT_F32) {
-    float* dst = static_cast<float*>(row_ptr) + col;
-    if (n_valid >= 4) {
-      *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-    } else {
-      for (int i = 0; i < n_valid; ++i) dst[i] = v[i];
-    }
-  } else {
-    uint16_t* dst = static_cast<uint16_t*>(row_ptr) + col;
-    if (n_valid >= 8) {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(pack2<OUT>(v[0], v[1]), pack2<OUT>(v[2], v[3]),
-                                                  pack2<OUT>(v[4], v[5]), pack2<OUT>(v[6], v[7]));
-    } else {
-      for (int i = 0; i < n_valid; ++i) store_out<OUT>(dst, i, v[i]);
-    }
-  }
-}
-
 template <bool IN_BF16, int OUT, int KSUB>
 __global__ void __launch_bounds__(192, 1)
     skinny_rows_gemm_kernel(const __grid_constant__ CUtensorMap tmA,

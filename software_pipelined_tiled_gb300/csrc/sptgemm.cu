@@ -495,13 +495,16 @@ bool pick_square(const DtypeInfo& d, int bn, int stages, bool pair, KernelVarian
 }
 
 // Per-FLOP rate of each tile shape measured on GB300 (binary16 8192 x 8192 x
-// 4096, TFLOPS with wave quantisation and padding divided out), for BN =
-// 256, 224, 192, 160, 128: the weights of the shape model below. Narrow
+// 4096 data-parallel, TFLOPS with wave quantisation and padding divided out:
+// rounds x workers x tile FLOPs / time), for BN = 512 (pairs only) and 256
+// down to 112 in steps of 16: the weights of the shape model below. Narrow
 // tiles lose more than their share: a K-tile's copies and barrier trip cost
-// about the same whatever its width.
-constexpr double kRatePair[6] = {2133, 1942, 1911, 1773, 1600, 1331};
-constexpr double kRateSingle[6] = {0, 1654, 1548, 1670, 1567, 1262};
-constexpr int kTileWidths[6] = {512, 256, 224, 192, 160, 128};
+// about the same whatever its width. (The 512 entry was measured on another
+// box and scaled by the ratio of the two boxes' 256-wide pair rates.)
+constexpr int kNumWidths = 11;
+constexpr int kTileWidths[kNumWidths] = {512, 256, 240, 224, 208, 192, 176, 160, 144, 128, 112};
+constexpr double kRatePair[kNumWidths] = {2103, 1915, 1889, 1875, 1829, 1729, 1648, 1558, 1434, 1312, 1189};
+constexpr double kRateSingle[kNumWidths] = {0, 1684, 1639, 1613, 1684, 1669, 1557, 1507, 1414, 1224, 1138};
 
 // Stream-K part of the schedule for T tiles over W workers, KT K-tiles each:
 // the tiles of a partial last round (mode 0, when that round is at most 90 %
@@ -578,11 +581,12 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
     if (pair && M <= 128 && cfg.cta_pair != 2) continue;  // one CTA already covers all rows
     const int64_t rows = pair ? 256 : 128;
     const int W = pair ? sm_count / 2 : sm_count;
-    for (int i = 0; i < 6; ++i) {
+    for (int i = 0; i < kNumWidths; ++i) {
       const int bn = kTileWidths[i];
       if (cfg.bn && bn != cfg.bn) continue;
-      // 512 columns: CTA pairs and float types only
+      // 512 columns: CTA pairs and float types only; int8 in 32-column steps
       if (bn == 512 && (!pair || int8)) continue;
+      if (int8 && bn % 32 != 0) continue;
       const int64_t T64 = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
       const int T = static_cast<int>(std::min<int64_t>(T64, INT32_MAX));
       const double rate = (pair ? kRatePair[i] : kRateSingle[i]) * 1e6;  // FLOP per us

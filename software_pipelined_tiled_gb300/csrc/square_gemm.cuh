@@ -247,7 +247,13 @@ struct SquareLayout {
   // tiles wider than one MMA (BN = 512: two 256-column MMAs per K-step) keep
   // a single accumulator: 512 columns fill tensor memory
   static constexpr int NACC = BN > 256 ? 1 : 2;
-  static constexpr int TMEM_NEEDED = NACC * BN;
+  // The epilogue moves whole blocks of 32 columns; a float tile may end in a
+  // block of 16 (BN = 112, 144, ..., 240), stored straight from registers.
+  static constexpr int NB_FULL = BN / 32;
+  static constexpr bool HALF_BLOCK = BN % 32 != 0;
+  // tensor-memory columns from one accumulator to the next (a multiple of 32)
+  static constexpr int ACC_COLS = (BN + 31) / 32 * 32;
+  static constexpr int TMEM_NEEDED = NACC == 2 ? 2 * ACC_COLS : BN;
   static constexpr int TMEM_COLS = TMEM_NEEDED <= 32    ? 32
                                    : TMEM_NEEDED <= 64  ? 64
                                    : TMEM_NEEDED <= 128 ? 128
@@ -257,9 +263,10 @@ struct SquareLayout {
   // warps store its first LAST_NB0 32-column blocks, the otherwise idle
   // reduction warps the rest, staged in the ring (free by then), when the
   // ring holds their buffers.
-  static constexpr int LAST_NB0 = (BN / 32 + 1) / 2;
+  // (a last 16-column block stays with the epilogue warps)
+  static constexpr int LAST_NB0 = (NB_FULL + 1) / 2;
   static constexpr bool LAST_SPLIT =
-      !INT_EXACT && NACC == 2 && BN / 32 > 1 && RING_BYTES >= 4 * (BN / 32 - LAST_NB0) * EPI_BUF;
+      !INT_EXACT && NACC == 2 && NB_FULL > 1 && RING_BYTES >= 4 * (NB_FULL - LAST_NB0) * EPI_BUF;
   // exact-integer epilogue: 32-column blocks of the first and second warp of a
   // lane quadrant
   static constexpr int INT_NB0 = (BN + 63) / 64;
@@ -267,11 +274,15 @@ struct SquareLayout {
   // bytes that complete one stage's "full" barrier (both CTAs' copies in PAIR mode)
   static constexpr uint32_t STAGE_TX = (PAIR ? 2 : 1) * (A_STAGE + B_STAGE);
   static_assert(TMEM_NEEDED <= 512, "accumulators exceed tensor memory");
-  static_assert(BN % 32 == 0 && BN >= 32 && (BN <= 256 || (BN == 512 && PAIR && !INT_EXACT)),
-                "BN must be a multiple of 32 in [32, 256], or 512 for float CTA pairs");
+  static_assert((BN % 32 == 0 && BN >= 32 && BN <= 256) ||
+                    (BN % 16 == 0 && BN >= 48 && BN <= 256 && !INT_EXACT) ||
+                    (BN == 512 && PAIR && !INT_EXACT),
+                "BN must be a multiple of 32 in [32, 256], of 16 for float tiles, or 512 for "
+                "float CTA pairs");
   static_assert(!INT_EXACT || (BN >= 64 && BN <= 256),
                 "the exact-integer epilogue keeps at most 128 columns per thread");
-  static_assert(!PAIR || BN_CTA % 16 == 0, "each CTA's B rows must be a multiple of 16");
+  // the 2-SM MMA with M = 256 takes N in steps of 16: half a step per CTA
+  static_assert(!PAIR || BN_CTA % 8 == 0, "each CTA's B rows must be a multiple of 8");
   static_assert(STAGES >= 1, "at least one stage");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
   static_assert(NUM_BARS * 8 + 40 <= 256, "barrier area");
@@ -332,13 +343,15 @@ constexpr int square_max_stages() {
 // (a fixed order: increasing k) and writes them to C, with NT threads (tid in
 // [0, NT)). base points at the tile's first partial slot of this CTA.
 // Flat index f over the 128 rows: group g = f % 8 of four columns, row
-// (f / 8) % 128, 32-column block f / (8 * 128). A warp reads 64-byte runs of
+// (f / 8) % 128, 32-column block f / (8 * 128); past the whole blocks, a last
+// 16-column block takes g = f % 4, row f / 4. A warp reads 64-byte runs of
 // the partials and writes whole row segments of C.
 template <int BN, int OUT, bool INT_EXACT, int NT>
 __device__ __forceinline__ void reduce_cut_tile(const SquareParams& p, const uint4* base, int count,
                                                 int row0, int col0, int tid) {
   constexpr int nr = 128;
   constexpr int total = nr * (BN / 4);
+  constexpr int full = nr * 8 * (BN / 32);  // the groups of whole 32-column blocks
   // groups per contributor in flight (fewer with 256 threads, which run beside
   // the exact-integer epilogue's running sums), contributors in flight
   constexpr int CH = NT >= 256 ? 4 : 8;
@@ -349,9 +362,15 @@ __device__ __forceinline__ void reduce_cut_tile(const SquareParams& p, const uin
 #pragma unroll
     for (int i2 = 0; i2 < CH; ++i2) {
       const int f = f0 + tid + NT * i2;
-      const int rest = f >> 3;
-      const int cb = rest / nr;
-      idx[i2] = f < total ? ((cb * 8 + (f & 7)) * 128 + (rest - cb * nr)) : -1;
+      if (f < full) {
+        const int rest = f >> 3;
+        const int cb = rest / nr;
+        idx[i2] = (cb * 8 + (f & 7)) * 128 + (rest - cb * nr);
+      } else if (f < total) {
+        idx[i2] = ((BN / 32) * 8 + ((f - full) & 3)) * 128 + ((f - full) >> 2);
+      } else {
+        idx[i2] = -1;
+      }
     }
     uint4 acc[CH];
 #pragma unroll 1
@@ -628,7 +647,7 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + b * BN;
+          const uint32_t d_tmem = tmem_base + b * L::ACC_COLS;
           const int c1 = min(seg.kt1, c0 + kpc);
           // Stage and phase are counted, not divided; descriptors advance by
           // adds (the 14-bit start-address field cannot carry: shared
@@ -742,14 +761,14 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
             ok = false;
             break;
           }
-          int_chunk_sums<true, NBLK>(sum, tmem_base + lane_base + b * BN + 32 * cb0);
+          int_chunk_sums<true, NBLK>(sum, tmem_base + lane_base + b * L::ACC_COLS + 32 * cb0);
           release_chunk(b);
           for (int c = 1; c < n_chunks; ++c) {
             if (!wait_chunk(b)) {
               ok = false;
               break;
             }
-            int_chunk_sums<false, NBLK>(sum, tmem_base + lane_base + b * BN + 32 * cb0);
+            int_chunk_sums<false, NBLK>(sum, tmem_base + lane_base + b * L::ACC_COLS + 32 * cb0);
             release_chunk(b);
           }
           if (!ok) break;
@@ -855,7 +874,7 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
         ok = __all_sync(0xffffffffu, wait_bounded(tfull_bar(b), use & 1u, ctl, WAIT_EPI_TMEM_FULL));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t t_acc = tmem_base + lane_base + b * BN + 32 * cb_first;
+        const uint32_t t_acc = tmem_base + lane_base + b * L::ACC_COLS + 32 * cb_first;
         if (split && threadIdx.x == 64) {
           last_tile[0] = mt;
           last_tile[1] = nt;
@@ -865,7 +884,7 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
         // One block = 32 output columns of this warp's 32 rows. The
         // tensor-memory load of block cb+1 is in flight while block cb is
         // converted.
-        const int NB = split ? L::LAST_NB0 : (wide8 ? BN / 64 : BN / 32);
+        const int NB = split ? L::LAST_NB0 : (wide8 ? BN / 64 : L::NB_FULL);
         uint32_t v[32];
         tmem_ld_32x32b_x32(t_acc, v);
         tmem_wait_ld_regs(v);
@@ -921,6 +940,35 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
             if (lane < G && cb < NB && c_row < p.M && col < p.N) {
               tma_store_2d(&tmC, smem_addr(bufs + lane * L::EPI_BUF), col, c_row);
               bulk_commit_group();
+            }
+          }
+        }
+        if constexpr (L::HALF_BLOCK) {
+          // The tile's last 16 columns: each lane's row goes out from its
+          // registers (N * sizeof(out) is a multiple of 16 bytes, so a group
+          // of 8 16-bit or 4 fp32 outputs lies wholly inside or outside C),
+          // or, for a partial segment, to the scratch slot's last groups.
+          uint32_t h[16];
+          tmem_ld_32x32b_x16(t_acc + 32 * L::NB_FULL, h);
+          tmem_wait_ld_regs16(h);
+          if (seg.partial) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              __stcg(slot + (L::NB_FULL * 8 + j) * 128,
+                     make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]));
+          } else {
+            const int row = c_row + lane;
+            const int col = nt * BN + 32 * L::NB_FULL;
+            if (row < p.M && col < p.N) {
+              float f[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(h[j]);
+              void* row_ptr = static_cast<uint8_t*>(p.C_out) +
+                              (static_cast<int64_t>(row) * p.ldc) * OBYTES;
+              constexpr int GRP = OBYTES == 4 ? 4 : 8;
+#pragma unroll
+              for (int g = 0; g < 16 / GRP; ++g)
+                if (col + GRP * g < p.N) store_row_group<OUT>(row_ptr, col + GRP * g, f + GRP * g, GRP);
             }
           }
         }
@@ -1011,9 +1059,9 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
         const uint32_t b = static_cast<uint32_t>(last_tile[2]);
         tc_fence_after();
         const int q = warp & 3;
-        const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
+        const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * L::ACC_COLS;
         const int c_row = mt * L::TILE_M + static_cast<int>(rank) * BM + 32 * q;
-        constexpr int NB1 = BN / 32 - L::LAST_NB0;
+        constexpr int NB1 = L::NB_FULL - L::LAST_NB0;
         uint8_t* bufs = smem + L::OFF_A + (warp - 6) * NB1 * L::EPI_BUF;
         fence_proxy_async_smem();  // the ring's async-proxy use is over
 #pragma unroll 1

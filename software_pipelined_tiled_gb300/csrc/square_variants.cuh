@@ -14,7 +14,7 @@ KernelVariant make_square() {
                        PAIR, IE ? SQUARE_THREADS_INT : SQUARE_THREADS};
 }
 
-// Tile widths BN in {256, 224, 192, 160, 128}, one CTA or a CTA pair per
+// Tile widths BN from 112 to 256 in steps of 16, one CTA or a CTA pair per
 // tile, each at the deepest ring that fits (square_max_stages). For
 // binary16 -> binary16 also the shallower rings of BN 256 and 224 (one CTA)
 // and of BN 224 (pair) for the pipelining ablation (1 = load, then compute,
@@ -41,10 +41,15 @@ bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v) {
     break;
   switch (bn) {
     SPTG_SQ(256)
+    SPTG_SQ(240)
     SPTG_SQ(224)
+    SPTG_SQ(208)
     SPTG_SQ(192)
+    SPTG_SQ(176)
     SPTG_SQ(160)
+    SPTG_SQ(144)
     SPTG_SQ(128)
+    SPTG_SQ(112)
     default:
       return false;
   }

@@ -104,7 +104,10 @@ def test_k_tile_marker_square(T, stages, bn):
     assert (C.to(torch.float64) == expect).all()
 
 
-@pytest.mark.parametrize("bn", [256, 224, 192, 160, 128])
+FLOAT_WIDTHS = [256, 240, 224, 208, 192, 176, 160, 144, 128, 112]
+
+
+@pytest.mark.parametrize("bn", FLOAT_WIDTHS)
 @pytest.mark.parametrize("pair", ["f16_f32", "f16_f16", "bf16_bf16", "bf16_f32"])
 def test_every_tile_width(bn, pair):
     it, ot = pair.split("_")
@@ -126,7 +129,7 @@ def test_k_tile_marker_cta_pair(T, bn):
     assert (C.to(torch.float64) == expect).all()
 
 
-@pytest.mark.parametrize("bn", [256, 224, 192, 160, 128])
+@pytest.mark.parametrize("bn", FLOAT_WIDTHS)
 @pytest.mark.parametrize("pair", ["f16_f32", "f16_f16", "bf16_bf16", "bf16_f32"])
 def test_every_tile_width_cta_pair(bn, pair):
     it, ot = pair.split("_")
@@ -136,6 +139,69 @@ def test_every_tile_width_cta_pair(bn, pair):
     C = run(A, B, dt[ot], kernel="square", bn=bn, cta_pair=2)
     assert f"bn={bn}" in sptg.last_config() and "pair=1" in sptg.last_config()
     assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("bn", [112, 176, 240])
+@pytest.mark.parametrize("cta_pair", [1, 2])
+@pytest.mark.parametrize("it,ot,N", [("f16", F16, 1000), ("bf16", BF16, 696), ("bf16", F32, 692),
+                                     ("f16", F32, 1056)])
+def test_half_block_tiles_over_several_rounds(bn, cta_pair, it, ot, N):
+    # widths ending in a 16-column block (stored from registers) on three
+    # workers, so each holds several tiles and both accumulators take turns;
+    # N = 696 / 692 end inside the last tile's 16-column block (one group of
+    # 8 bfloat16 / 4 fp32 outputs in C, the rest past N), 1056 is a multiple
+    # of 176 (every tile whole)
+    A, B = make_inputs(700, N, 200, it, "uniform", bn + cta_pair)
+    C = run(A, B, ot, kernel="square", bn=bn, cta_pair=cta_pair, splits=3, stream_k=1)
+    cfg = sptg.last_config()
+    assert f"bn={bn}" in cfg and f"pair={cta_pair - 1}" in cfg, cfg
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("bn", [112, 176, 240])
+@pytest.mark.parametrize("cta_pair", [1, 2])
+def test_half_block_tiles_cut_along_k(bn, cta_pair):
+    # every tile cut along K: the last 16 columns of each partial go to the
+    # scratch slot's last groups and come back through the reduction
+    A, B = make_inputs(520, 776, 1096, "bf16", "uniform", 42 + bn)
+    C = run(A, B, F32, kernel="square", bn=bn, cta_pair=cta_pair, stream_k=2, splits=5)
+    assert _sk_tiles() > 0 and f"bn={bn}" in sptg.last_config()
+    assert_float_parity(C, A, B)
+    A, B = make_inputs(300, 528, 2000, "f16", "uniform", 43 + bn)
+    C = run(A, B, F16, kernel="square", bn=bn, cta_pair=cta_pair, stream_k=2, splits=7)
+    assert _sk_tiles() > 0
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("bn", [112, 176])
+def test_half_block_columns_are_placed(bn):
+    # each column of B distinct, A the identity block: C[i, j] = B[j, i]
+    # exactly, so a 16-column block written to the wrong columns or rows shows
+    M, N, K = 256, 3 * bn, 256
+    A = torch.eye(M, K, dtype=F16)
+    Bcm = ((torch.arange(N).unsqueeze(1) * 7 + torch.arange(K).unsqueeze(0)) % 1024).to(F16)
+    for cta_pair in (1, 2):
+        C = run(A, Bcm, F32, kernel="square", bn=bn, cta_pair=cta_pair, splits=1, stream_k=1)
+        assert f"bn={bn}" in sptg.last_config()
+        assert torch.equal(C, Bcm.t().to(F32)[:M])
+
+
+def test_mid_rows_default_tiles():
+    # 768 x 8192 x 8192 takes 256 x 176 pair tiles by default: sampled
+    # outputs, a whole row, and the 16-column block that ends tile column 45
+    # (the last tile column holds only 96 columns)
+    M, N, K = 768, 8192, 8192
+    A, B = make_inputs(M, N, K, "bf16", "normal", 46)
+    C = run(A, B, BF16)
+    cfg = sptg.last_config()
+    assert "bn=176" in cfg and "pair=1" in cfg, cfg
+    rows, cols = sample_positions(M, N, 3000, seed=46)
+    tail = np.arange(45 * 176 + 160, 46 * 176, dtype=np.int64)
+    rows = np.concatenate([rows, np.repeat(np.arange(0, M, 37, dtype=np.int64), 16)])
+    cols = np.concatenate([cols, np.tile(tail, len(range(0, M, 37)))])
+    assert_float_parity(C, A, B, rows, cols)
+    r = np.full(N, 513, dtype=np.int64)
+    assert_float_parity(C, A, B, r, np.arange(N, dtype=np.int64))
 
 
 def test_cta_pair_operand_halves_are_not_swapped():

@@ -47,6 +47,19 @@ def test_long_k_takes_wide_pair_tiles():
     assert plan(16384, 16384, 4096, "bf16_bf16")["bn"] == 256
 
 
+def test_widths_in_steps_of_16_fill_rounds():
+    # 768 x 8192: 256 x 176 pair tiles, 3 x 47 = 141 tiles in two rounds of 76
+    # pairs (256-wide tiles: 96 tiles, 1.26 rounds)
+    p = plan(768, 8192, 8192, "bf16_bf16")
+    assert (p["bn"], p["pair"], p["tiles"], p["stream_k_tiles"]) == (176, 1, 141, 0)
+    # 256^3: six single-CTA tiles of 128 x 112 (four of 128 x 128 before)
+    p = plan(256, 256, 256, "f16_f32")
+    assert (p["bn"], p["pair"], p["tiles"]) == (112, 0, 6)
+    # 512 x 4096 x 4096: 4 x 37 = 148 single-CTA tiles of 128 x 112, one round
+    p = plan(512, 4096, 4096)
+    assert (p["bn"], p["pair"], p["tiles"], p["workers"]) == (112, 0, 148, 148)
+
+
 def test_long_k_at_256_columns_cuts_the_partial_last_round():
     p = plan(8192, 8192, 16384, "bf16_f32", bn=256)
     # 256 x 256 pair tiles: 32 x 32 = 1024 tiles = 13 rounds of 76 pairs + 36
@@ -79,11 +92,20 @@ def test_stream_k_settings():
     assert p["stream_k_tiles"] == p["tiles"]
 
 
+FLOAT_WIDTHS = tuple(range(112, 257, 16))
+
+
 def test_forced_fields_are_honoured():
-    for bn in (128, 160, 192, 224, 256):
+    for bn in FLOAT_WIDTHS:
         for pair in (1, 2):
             p = plan(3000, 5000, 700, bn=bn, cta_pair=pair)
             assert p["bn"] == bn and p["pair"] == pair - 1
+    # int8 tiles in steps of 32 columns only
+    for bn in (128, 160, 192, 224, 256):
+        assert plan(3000, 5000, 704, "s8_s32", bn=bn)["bn"] == bn
+    for bn in (112, 144, 176, 208, 240, 96):
+        with pytest.raises(sptg.SptgError):
+            plan(3000, 5000, 704, "s8_s32", bn=bn)
     assert plan(3000, 5000, 700, bn=512, cta_pair=2)["bn"] == 512
     for args, cfg in [((3000, 5000, 700), {"bn": 512, "cta_pair": 1}),
                       ((3000, 5000, 704, "s8_s32"), {"bn": 512})]:
@@ -128,11 +150,11 @@ def test_plan_invariants_over_random_shapes():
             cfg["stream_k"] = 0  # every tile cut needs a counter per tile: keep it small
         p = plan(M, N, K, dt, sm, **cfg)
         rows = 256 if p["pair"] else 128
-        assert p["bn"] in (128, 160, 192, 224, 256, 512)
+        assert p["bn"] in FLOAT_WIDTHS + (512,)
         if p["bn"] == 512:
             assert p["pair"] == 1 and dt != "s8_s32" and p["stream_k_tiles"] == 0
         if dt == "s8_s32":
-            assert p["bn"] != 512
+            assert p["bn"] != 512 and p["bn"] % 32 == 0
         assert p["tiles"] == -(-M // rows) * -(-N // p["bn"])
         kt = -(-K // 64)
         t, g, mc = p["stream_k_tiles"], p["stream_k_workers"], p["max_contrib"]

@@ -43,6 +43,8 @@ def _case(i):
         kw["kernel"] = "square"
         kw["cta_pair"] = {"single": 1, "pair": 2}[kind]
         widths = (256, 224, 192, 160, 128) + ((512,) if kind == "pair" and it != "s8" else ())
+        if it != "s8":
+            widths += (240, 208, 176, 144, 112)
         kw["bn"] = rng.choice(widths)
         if kw["bn"] != 512:
             kw["stream_k"] = rng.choice([0, 1, 2])
