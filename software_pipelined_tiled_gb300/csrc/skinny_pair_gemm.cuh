@@ -30,6 +30,8 @@
 // CTA's columns takes the columns h * MN / 2 ... of tensor memory.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace sptg {
@@ -41,6 +43,7 @@ struct SkinnyPairParams {
   int stages;       // ring depth, 1 ... SKINNY_PAIR_MAX_STAGES
   int stage_bytes;  // skinny_pair_stage_bytes(KSUB, n_cta, MN)
   int load3d;       // 1: one 3-D copy per operand and stage; 0: 2-D per chunk
+  int k_rotate;     // 1: pair i starts its K-loop at chunk i * num_k_tiles / pairs
   unsigned int* error_word;
   uint64_t timeout_ns;
   int inject_stall;
@@ -111,6 +114,17 @@ __global__ void __launch_bounds__(192, 1)
   const int n_base =
       static_cast<int>(blockIdx.x >> 1) * 2 * n_cta + static_cast<int>(rank) * n_cta;
   const int KT = p.num_k_tiles;
+  // With k_rotate the pairs start their K-loops at evenly spaced chunks and
+  // wrap around, so that at any moment they read different columns of A and
+  // different K-ranges of their Bcm rows (the sum's order over K differs
+  // from pair to pair; each column's order is fixed by the launch).
+  const int k_rot = p.k_rotate ? static_cast<int>((static_cast<int64_t>(blockIdx.x >> 1) * KT) /
+                                                  static_cast<int64_t>(gridDim.x >> 1))
+                               : 0;
+  auto kchunk = [&](int kt) {  // the chunk a pair copies at loop position kt
+    const int c = kt + k_rot;
+    return c >= KT ? c - KT : c;
+  };
   // bytes that complete one stage's "full" barrier: both CTAs' copies
   const uint32_t stage_tx = 2u * KSUB * static_cast<uint32_t>((n_cta + HALF) * 128);
   // A K-chunk of this CTA's Bcm rows fills n_cta rows; the chunks of a stage
@@ -154,11 +168,12 @@ __global__ void __launch_bounds__(192, 1)
     pol_stream = policy_evict_first();  // Bcm is read once
     pol_keep = policy_evict_last();     // A is read by every pair
     for (int kt = 0; lane == 0 && kt < min(KT, S); ++kt) {
+      const int kc = kchunk(kt);
       if (p.load3d) {
-        tma_prefetch_l2_3d(&tmB, 0, n_base, kt * KSUB);
+        tma_prefetch_l2_3d(&tmB, 0, n_base, kc * KSUB);
       } else {
 #pragma unroll
-        for (int j = 0; j < KSUB; ++j) tma_prefetch_l2_2d(&tmB, (kt * KSUB + j) * BK, n_base);
+        for (int j = 0; j < KSUB; ++j) tma_prefetch_l2_2d(&tmB, (kc * KSUB + j) * BK, n_base);
       }
     }
   }
@@ -189,16 +204,17 @@ __global__ void __launch_bounds__(192, 1)
           // announces the bytes of both
           if (rank == 0) mbar_arrive_expect_tx(full_bar(s), stage_tx);
           const uint32_t leader_full = map_to_cta(full_bar(s), 0u);
+          const int kc = kchunk(kt);
           if (p.load3d) {
-            tma_load_3d_pair(stage_b(s), &tmB, leader_full, 0, n_base, kt * KSUB, pol_stream);
+            tma_load_3d_pair(stage_b(s), &tmB, leader_full, 0, n_base, kc * KSUB, pol_stream);
             tma_load_3d_pair(stage_a(s), &tmA, leader_full, 0, HALF * static_cast<int>(rank),
-                             kt * KSUB, pol_keep);
+                             kc * KSUB, pol_keep);
           } else {
 #pragma unroll
             for (int j = 0; j < KSUB; ++j) {
-              tma_load_2d_pair(stage_b(s) + j * sub_b, &tmB, leader_full, (kt * KSUB + j) * BK,
+              tma_load_2d_pair(stage_b(s) + j * sub_b, &tmB, leader_full, (kc * KSUB + j) * BK,
                                n_base, pol_stream);
-              tma_load_2d_pair(stage_a(s) + j * SUB_A, &tmA, leader_full, (kt * KSUB + j) * BK,
+              tma_load_2d_pair(stage_a(s) + j * SUB_A, &tmA, leader_full, (kc * KSUB + j) * BK,
                                HALF * static_cast<int>(rank), pol_keep);
             }
           }
@@ -236,38 +252,51 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------------------------------------------------- MMA issuer
     if (rank == 0) {
       const bool leader = elect_one_sync();
-      int s = 0;
-      uint32_t round = 0;
-      for (int kt = 0; kt < KT; ++kt) {
-        if (!__all_sync(0xffffffffu, wait_bounded(full_bar(s), round & 1u, ctl, WAIT_MMA_FULL))) {
-          if (leader) *failed = 1;
-          break;
-        }
-        tc_fence_after();
-        if (leader) {
-          if (kt == 0) trace_mark(p.trace, TR_FIRST_DATA);
-          trace_ktile(p.trace, 1, static_cast<uint32_t>(kt));
+      // The K-loop with each stage's MMAs as straight-line code, compiled
+      // for one and for two 64-row blocks (n_cta <= 128) and chosen once: a
+      // loop with a runtime trip count, or a branch, run by the elected lane
+      // alone costs more per stage than the MMAs it issues (64 x 4096 x 8192:
+      // 20.6 us with a runtime block loop against 15.4 us straight-line).
+      auto k_loop = [&](auto nb) {
+        constexpr int NB = decltype(nb)::value;
+        int s = 0;
+        uint32_t round = 0;
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!__all_sync(0xffffffffu, wait_bounded(full_bar(s), round & 1u, ctl, WAIT_MMA_FULL))) {
+            if (leader) *failed = 1;
+            break;
+          }
+          tc_fence_after();
+          if (leader) {
+            if (kt == 0) trace_mark(p.trace, TR_FIRST_DATA);
+            trace_ktile(p.trace, 1, static_cast<uint32_t>(kt));
 #pragma unroll
-          for (int j = 0; j < KSUB; ++j) {
-            for (int h = 0; h < nblk; ++h) {
+            for (int j = 0; j < KSUB; ++j) {
 #pragma unroll
-              for (int k = 0; k < BK / 16; ++k) {
-                mma_f16_g<true>(tmem_base + h * HALF,
-                                sdesc_k_major_sw128(stage_b(s) + j * sub_b + h * SKINNY_PAIR_SUB_B +
-                                                    32 * k),
-                                sdesc_k_major_sw128(stage_a(s) + j * SUB_A + 32 * k), IDESC,
-                                (kt > 0 || j > 0 || k > 0) ? 1u : 0u);
+              for (int h = 0; h < NB; ++h) {
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                  mma_f16_g<true>(tmem_base + h * HALF,
+                                  sdesc_k_major_sw128(stage_b(s) + j * sub_b +
+                                                      h * SKINNY_PAIR_SUB_B + 32 * k),
+                                  sdesc_k_major_sw128(stage_a(s) + j * SUB_A + 32 * k), IDESC,
+                                  (kt > 0 || j > 0 || k > 0) ? 1u : 0u);
+                }
               }
             }
+            mma_commit_g<true>(empty_bar(s));  // stage s may be refilled in both CTAs
           }
-          mma_commit_g<true>(empty_bar(s));  // stage s may be refilled in both CTAs
+          __syncwarp();
+          if (++s == S) {
+            s = 0;
+            ++round;
+          }
         }
-        __syncwarp();
-        if (++s == S) {
-          s = 0;
-          ++round;
-        }
-      }
+      };
+      if (nblk == 1)
+        k_loop(std::integral_constant<int, 1>{});
+      else
+        k_loop(std::integral_constant<int, 2>{});
       if (leader) {
         trace_mark(p.trace, TR_LAST_MMA);
         mma_commit_g<true>(tfull_bar);  // both CTAs' accumulators are complete

@@ -1199,6 +1199,12 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   p.stages = stages;
   p.stage_bytes = stage_bytes;
   p.load3d = load3d;
+  // Staggered K-loops (see the kernel) for loops of 64 stages or more
+  // (same box, us, without / with: 64 x 8192 x 16384 43.7 / 42.2, 128 x 8192
+  // x 8192 25.15 / 24.65, 96 x 14336 x 8192 38.9 / 38.2, 256 x 8192 x 8192
+  // 32.2 / 31.8); at 32 stages it measured level or 0.5 % slower (64 x 8192 x
+  // 8192 22.06 / 22.13, 64 x 4096 x 8192 15.7 / 15.7).
+  p.k_rotate = p.num_k_tiles >= 64 ? 1 : 0;
   p.error_word = di.error_word;
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;
@@ -1212,8 +1218,8 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   if (e != cudaSuccess) return cuda_fail(e, "skinny_pair_gemm launch");
   set_config(
       "kernel=skinny-pair dtype=%s mma_m=128 mma_n=%lld cols_per_cta=%lld bk=%lld stages=%lld "
-      "grid=%lld pairs=%lld k_tiles=%lld copies_3d=%lld smem=%lld",
-      d.name, {mn, nc, kstep, stages, grid, pairs, p.num_k_tiles, load3d, smem});
+      "grid=%lld pairs=%lld k_tiles=%lld copies_3d=%lld k_rotate=%lld smem=%lld",
+      d.name, {mn, nc, kstep, stages, grid, pairs, p.num_k_tiles, load3d, p.k_rotate, smem});
   return SPTG_OK;
 }
 

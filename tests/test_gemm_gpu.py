@@ -545,6 +545,32 @@ def test_k_tile_marker_skinny_pair(T, stages, M):
     assert (C.to(torch.float64) == expect).all()
 
 
+@pytest.mark.parametrize("M,N,T,nc", [(64, 1024, 260, 56), (128, 2048, 260, 32),
+                                      (256, 1000, 129, 40), (64, 4000, 257, 120)])
+def test_k_tile_marker_skinny_pair_staggered(M, N, T, nc):
+    # 64 stages or more: the pairs start their K-loops at staggered chunks and
+    # wrap around; every K-chunk must still land in each sum exactly once
+    # (T K-tiles of 64, the last stage partly empty, its chunk somewhere in
+    # the middle of most pairs' loops); binary16 holds the markers up to 2048
+    # exactly (bfloat16 only up to 256)
+    A, B, expect = _marker_inputs(M, N, T, dtype=F16)
+    C = run(A, B, F32, kernel="skinny_pair", bn=nc)
+    cfg = sptg.last_config()
+    assert "k_rotate=1" in cfg, cfg
+    assert (C.to(torch.float64) == expect).all()
+
+
+@pytest.mark.parametrize("M,N,K,it,ot", [(64, 4096, 16392, "bf16", BF16),
+                                         (128, 8192, 8200, "f16", F32),
+                                         (96, 6000, 16384, "bf16", F32)])
+def test_skinny_pair_staggered_parity(M, N, K, it, ot):
+    A, B = make_inputs(M, N, K, it, "normal", M + K)
+    C = run(A, B, ot, kernel="skinny_pair")
+    assert "k_rotate=1" in sptg.last_config(), sptg.last_config()
+    assert_float_parity(C, A, B)
+    assert torch.equal(C, run(A, B, ot, kernel="skinny_pair"))  # the same order every call
+
+
 @pytest.mark.parametrize("M", [64, 128, 256])
 def test_skinny_pair_places_every_row_and_column(M):
     # A[m, k] = m + 1 and Bcm[n, k] = n % 61 + 1: C[m, n] = K (m + 1)(n % 61 + 1),
