@@ -34,6 +34,7 @@ struct SkinnyRowsParams {
   int stages;           // ring depth, 1 ... SKINNY_ROWS_MAX_STAGES
   int stage_bytes;      // KSUB * (64 + n_tile) * 128, a multiple of 1024
   int load3d;           // 1: one 3-D copy per operand and stage; 0: 2-D per chunk
+  int k_rotate;         // 1: strip i starts its K-loop at chunk i * num_k_tiles / strips
   unsigned int* error_word;
   uint64_t timeout_ns;
   int inject_stall;
@@ -82,6 +83,17 @@ __global__ void __launch_bounds__(192, 1)
   const int lane = threadIdx.x & 31;
   const int n0 = static_cast<int>(blockIdx.x) * nt_cols;  // first output column
   const int KT = p.num_k_tiles;
+  // With k_rotate the strips start their K-loops at evenly spaced chunks and
+  // wrap around, so that at any moment they read different columns of A and
+  // different K-ranges of their Bcm rows (each column's order over K is
+  // fixed by the launch).
+  const int k_rot = p.k_rotate ? static_cast<int>((static_cast<int64_t>(blockIdx.x) * KT) /
+                                                  static_cast<int64_t>(gridDim.x))
+                               : 0;
+  auto kchunk = [&](int kt) {  // the chunk a strip copies at loop position kt
+    const int c = kt + k_rot;
+    return c >= KT ? c - KT : c;
+  };
   // kind::f16, fp32 accumulation, M = 64, N = n_tile
   const uint32_t idesc = idesc_f16_f32acc(IN_BF16, 64, nt_cols);
 
@@ -114,11 +126,12 @@ __global__ void __launch_bounds__(192, 1)
     pol_stream = policy_evict_first();  // Bcm is read once
     pol_keep = policy_evict_last();     // A is read by every CTA
     for (int kt = 0; lane == 0 && kt < min(KT, S); ++kt) {
+      const int kc = kchunk(kt);
       if (p.load3d) {
-        tma_prefetch_l2_3d(&tmB, 0, n0, kt * KSUB);
+        tma_prefetch_l2_3d(&tmB, 0, n0, kc * KSUB);
       } else {
 #pragma unroll
-        for (int j = 0; j < KSUB; ++j) tma_prefetch_l2_2d(&tmB, (kt * KSUB + j) * BK, n0);
+        for (int j = 0; j < KSUB; ++j) tma_prefetch_l2_2d(&tmB, (kc * KSUB + j) * BK, n0);
       }
     }
   }
@@ -146,15 +159,16 @@ __global__ void __launch_bounds__(192, 1)
         issued_round[s] = static_cast<int>(round);
         if (leader) {
           mbar_arrive_expect_tx(full_bar(s), static_cast<uint32_t>(p.stage_bytes));
+          const int kc = kchunk(kt);
           if (p.load3d) {
-            tma_load_3d(stage_a(s), &tmA, full_bar(s), 0, 0, kt * KSUB, pol_keep);
-            tma_load_3d(stage_b(s), &tmB, full_bar(s), 0, n0, kt * KSUB, pol_stream);
+            tma_load_3d(stage_a(s), &tmA, full_bar(s), 0, 0, kc * KSUB, pol_keep);
+            tma_load_3d(stage_b(s), &tmB, full_bar(s), 0, n0, kc * KSUB, pol_stream);
           } else {
 #pragma unroll
             for (int j = 0; j < KSUB; ++j) {
-              tma_load_2d(stage_a(s) + j * SUB_A, &tmA, full_bar(s), (kt * KSUB + j) * BK, 0,
+              tma_load_2d(stage_a(s) + j * SUB_A, &tmA, full_bar(s), (kc * KSUB + j) * BK, 0,
                           pol_keep);
-              tma_load_2d(stage_b(s) + j * sub_b, &tmB, full_bar(s), (kt * KSUB + j) * BK, n0,
+              tma_load_2d(stage_b(s) + j * sub_b, &tmB, full_bar(s), (kc * KSUB + j) * BK, n0,
                           pol_stream);
             }
           }

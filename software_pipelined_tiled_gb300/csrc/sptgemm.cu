@@ -1114,6 +1114,12 @@ int run_skinny_rows(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   p.stages = stages;
   p.stage_bytes = stage_bytes;
   p.load3d = load3d;
+  // Staggered K-loops (see the kernel) for K >= 8192 over 64 stages or more
+  // (same box, us, without / with: 64 x 16384 x 8192 41.3 / 40.1, 64 x 12288
+  // x 16384 67.4 / 65.6, 64 x 24576 x 8192 60.5 / 59.6; 64 x 16384 x 4096
+  // 21.6 / 21.4; at K = 4096 over 64 one-chunk stages 0.35 % slower: 64 x
+  // 32768 x 4096 40.15 / 40.3, 32 x 32000 x 4096 39.0 / 39.1).
+  p.k_rotate = (K >= 8192 && p.num_k_tiles >= 64) ? 1 : 0;
   p.error_word = di.error_word;
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;
@@ -1127,8 +1133,8 @@ int run_skinny_rows(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   if (e != cudaSuccess) return cuda_fail(e, "skinny_rows_gemm launch");
   set_config(
       "kernel=skinny-rows dtype=%s mma_m=%lld mma_n=%lld bk=%lld stages=%lld grid=%lld "
-      "k_tiles=%lld copies_3d=%lld smem=%lld",
-      d.name, {64, nt, kstep, stages, grid, p.num_k_tiles, load3d, smem});
+      "k_tiles=%lld copies_3d=%lld k_rotate=%lld smem=%lld",
+      d.name, {64, nt, kstep, stages, grid, p.num_k_tiles, load3d, p.k_rotate, smem});
   return SPTG_OK;
 }
 
@@ -1199,12 +1205,12 @@ int run_skinny_pair(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M
   p.stages = stages;
   p.stage_bytes = stage_bytes;
   p.load3d = load3d;
-  // Staggered K-loops (see the kernel) for loops of 64 stages or more
-  // (same box, us, without / with: 64 x 8192 x 16384 43.7 / 42.2, 128 x 8192
+  // Staggered K-loops (see the kernel) for loops of 64 stages or more, as
+  // for the strip kernel (same box, us, without / with: 64 x 8192 x 16384 43.7 / 42.2, 128 x 8192
   // x 8192 25.15 / 24.65, 96 x 14336 x 8192 38.9 / 38.2, 256 x 8192 x 8192
   // 32.2 / 31.8); at 32 stages it measured level or 0.5 % slower (64 x 8192 x
   // 8192 22.06 / 22.13, 64 x 4096 x 8192 15.7 / 15.7).
-  p.k_rotate = p.num_k_tiles >= 64 ? 1 : 0;
+  p.k_rotate = (K >= 8192 && p.num_k_tiles >= 64) ? 1 : 0;
   p.error_word = di.error_word;
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;

@@ -456,6 +456,31 @@ def test_k_tile_marker_skinny_rows(T, stages, nt):
     assert (C.to(torch.float64) == expect).all()
 
 
+@pytest.mark.parametrize("T,nt", [(129, 64), (129, 192), (130, 112)])
+def test_k_tile_marker_skinny_rows_staggered(T, nt):
+    # K >= 8192 over 64 stages or more: the strips start their K-loops at
+    # staggered chunks and wrap around; every K-chunk must still land in each
+    # sum exactly once (binary16 markers: exact up to 2048)
+    A, B, expect = _marker_inputs(64, 2000, T, dtype=F16)
+    C = run(A, B, F32, kernel="skinny_rows", bn=nt)
+    assert "k_rotate=1" in sptg.last_config(), sptg.last_config()
+    assert (C.to(torch.float64) == expect).all()
+
+
+@pytest.mark.parametrize("M,N,K,it,ot", [(64, 16384, 8200, "bf16", BF16),
+                                         (40, 30000, 8192, "f16", F32)])
+def test_skinny_rows_staggered_parity(M, N, K, it, ot):
+    A, B = make_inputs(M, N, K, it, "normal", M + N)
+    C = run(A, B, ot)
+    cfg = sptg.last_config()
+    assert "kernel=skinny-rows" in cfg and "k_rotate=1" in cfg, cfg
+    rows, cols = sample_positions(M, N, 6000, seed=M)
+    assert_float_parity(C, A, B, rows, cols)
+    r = np.full(N, M - 1, dtype=np.int64)
+    assert_float_parity(C, A, B, r, np.arange(N, dtype=np.int64))
+    assert torch.equal(C, run(A, B, ot))  # the same order every call
+
+
 @pytest.mark.parametrize("stages", [1, 2, 3, 4])
 def test_skinny_rows_ablation_rings_match(stages):
     A, B = make_inputs(64, 2048, 4096, "bf16", "normal", 16)
