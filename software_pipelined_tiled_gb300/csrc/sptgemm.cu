@@ -714,6 +714,7 @@ int launch_square(const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N
   p.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms > 0 ? cfg.timeout_ms : 2000) * 1000000ull;
   p.inject_stall = cfg.inject_stall;
   p.trace = static_cast<unsigned long long*>(cfg.trace);
+  p.b_once = pl.m_tiles == 1 ? 1 : 0;
   void* args[] = {&ta, &tb, &tc, &p};
   cudaError_t e = launch_variant(pl.v, pl.grid, stream, args, !cfg.no_overlap);
   ++t_launches;
