@@ -482,16 +482,34 @@ int pair_slots(int dev, const KernelVariant& v, int sm_count) {
 }
 
 // ------------------------------------------------------------ square path
-bool pick_square(const DtypeInfo& d, int bn, int stages, bool pair, KernelVariant* v) {
-  if (d.is_int8) return square_variant_s8(bn, stages, pair, v);
+bool pick_square(const DtypeInfo& d, int bn, int stages, bool pair, KernelVariant* v,
+                 int kch = 1) {
+  if (d.is_int8) return kch == 1 && square_variant_s8(bn, stages, pair, v);
   switch (d.out_kind) {
-    case OUT_F16: return !d.in_bf16 && square_variant_f16_f16(bn, stages, pair, v);
-    case OUT_BF16: return d.in_bf16 && square_variant_bf16_bf16(bn, stages, pair, v);
+    case OUT_F16: return !d.in_bf16 && square_variant_f16_f16(bn, stages, pair, v, kch);
+    case OUT_BF16: return d.in_bf16 && square_variant_bf16_bf16(bn, stages, pair, v, kch);
     case OUT_F32:
-      return d.in_bf16 ? square_variant_bf16_f32(bn, stages, pair, v)
-                       : square_variant_f16_f32(bn, stages, pair, v);
+      return d.in_bf16 ? square_variant_bf16_f32(bn, stages, pair, v, kch)
+                       : square_variant_f16_f32(bn, stages, pair, v, kch);
     default: return false;
   }
+}
+
+// 64-wide K-chunks per ring stage of a square tile: two for float CTA pairs
+// over K-loops of 32 K-chunks or more whose two-chunk ring still holds four
+// stages (up to 176 columns with 16-bit C, 128 with fp32 C), one elsewhere
+// and with a forced ring depth. Narrow pair tiles pay a stage's barrier trips
+// and MMA issue for little tensor work; two chunks halve that per FLOP. Same
+// box, us, one / two chunks: 768 x 8192 x 8192 bfloat16 on 256 x 176 pairs
+// 65.9 / 61.0, 256 x 8192 x 8192 on 256 x 112 pairs 34.9 / 31.1; with three
+// stages it lost (4096^3 on 256 x 224 pairs 78.0 / 80.2, 512 x 8192 x 8192 on
+// 256 x 224 pairs 40.9 / 44.3), and single CTAs, whose rings are half as
+// deep, lost most (384 x 8192 x 8192 on 128 x 176 tiles, two stages: 40.2 /
+// 52.8).
+int square_kch(const DtypeInfo& d, int bn, bool pair, int64_t K, const sptg_config& cfg) {
+  if (d.is_int8 || !pair || cfg.stages != 0 || (K + 63) / 64 < 32) return 1;
+  KernelVariant v2;
+  return (pick_square(d, bn, 0, true, &v2, 2) && v2.stages >= 4) ? 2 : 1;
 }
 
 // Per-FLOP rate of each tile shape measured on GB300 (binary16 8192 x 8192 x
@@ -620,6 +638,7 @@ void choose_square_shape(int64_t M, int64_t N, int64_t K, int sm_count, const sp
 struct SquarePlan {
   KernelVariant v;
   bool pair;
+  int kch;  // 64-wide K-chunks per ring stage
   int tile_m, m_tiles, n_tiles, k_tiles, workers, grid;
   int sk_tiles, sk_workers, max_contrib;
   size_t partial_bytes;  // scratch for the stream-K partial tiles (0: none)
@@ -634,22 +653,26 @@ int plan_square(int dev, const DeviceInfo& di, const DtypeInfo& d, int64_t M, in
     t_last_error = "the requested tile width does not exist for this dtype/pairing";
     return SPTG_ERR_CONFIG;
   }
-  if (!pick_square(d, bn, cfg.stages, pair, &pl->v)) {
+  int kch = square_kch(d, bn, pair, K, cfg);
+  if (!pick_square(d, bn, cfg.stages, pair, &pl->v, kch)) {
     // a forced ring depth may exist for the other tile mode only
-    if (cfg.cta_pair == 0 && pick_square(d, bn, cfg.stages, !pair, &pl->v)) {
+    if (cfg.cta_pair == 0 && pick_square(d, bn, cfg.stages, !pair, &pl->v, kch)) {
       pair = !pair;
+    } else if (kch != 1 && pick_square(d, bn, cfg.stages, pair, &pl->v, 1)) {
+      kch = 1;
     } else {
       t_last_error = "no square-kernel variant for the requested bn/stages/pairing";
       return SPTG_ERR_CONFIG;
     }
   }
+  pl->kch = pl->v.ksub;
   int rc = ensure_smem(dev, pl->v.fn, pl->v.smem);
   if (rc) return rc;
   pl->pair = pair;
   pl->tile_m = pair ? 256 : 128;
   pl->m_tiles = static_cast<int>((M + pl->tile_m - 1) / pl->tile_m);
   pl->n_tiles = static_cast<int>((N + pl->v.bn - 1) / pl->v.bn);
-  pl->k_tiles = static_cast<int>((K + 63) / 64);
+  pl->k_tiles = static_cast<int>((K + 64 * pl->kch - 1) / (64 * pl->kch));  // ring stages
   const int tiles = pl->m_tiles * pl->n_tiles;
   int workers = pair ? pair_slots(dev, pl->v, di.sm_count) : di.sm_count;
   if (cfg.splits > 0) workers = std::min(workers, cfg.splits);
@@ -722,10 +745,10 @@ int launch_square(const DeviceInfo& di, const DtypeInfo& d, int64_t M, int64_t N
   set_config(
       "kernel=square dtype=%s tile_m=%lld bn=%lld bk=%lld stages=%lld pair=%lld grid=%lld "
       "tiles=%lld k_tiles=%lld chunk_k_tiles=%lld stream_k_tiles=%lld stream_k_workers=%lld "
-      "smem=%lld",
+      "kch=%lld smem=%lld",
       d.name, {pl.tile_m, pl.v.bn, BK, pl.v.stages, pl.pair ? 1 : 0, pl.grid,
                static_cast<long long>(pl.m_tiles) * pl.n_tiles, pl.k_tiles, p.k_tiles_per_chunk,
-               pl.sk_tiles, pl.sk_workers, pl.v.smem});
+               pl.sk_tiles, pl.sk_workers, pl.kch, pl.v.smem});
   return SPTG_OK;
 }
 
@@ -1297,7 +1320,8 @@ int sptg_plan_square(int64_t M, int64_t N, int64_t K, sptg_dtype dtype, int sm_c
   const int64_t rows = pair ? 256 : 128;  // tile rows
   const int64_t T64 = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
   const int tiles = static_cast<int>(std::min<int64_t>(T64, INT32_MAX));
-  const int k_tiles = static_cast<int>((K + 63) / 64);
+  const int kch = square_kch(d, bn, pair, K, cfg);  // as the launch: stages of kch K-chunks
+  const int k_tiles = static_cast<int>((K + 64 * kch - 1) / (64 * kch));
   int workers = pair ? sm_count / 2 : sm_count;
   if (cfg.splits > 0) workers = std::min(workers, cfg.splits);
   int skt = 0, skw = 0, mc = 1;

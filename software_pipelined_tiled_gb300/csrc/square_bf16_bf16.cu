@@ -3,8 +3,8 @@
 
 namespace sptg {
 
-bool square_variant_bf16_bf16(int bn, int stages, bool pair, KernelVariant* v) {
-  return square_float_variant<true, OUT_BF16>(bn, stages, pair, v);
+bool square_variant_bf16_bf16(int bn, int stages, bool pair, KernelVariant* v, int kch) {
+  return square_float_variant<true, OUT_BF16>(bn, stages, pair, v, kch);
 }
 
 }  // namespace sptg

@@ -3,8 +3,8 @@
 
 namespace sptg {
 
-bool square_variant_f16_f16(int bn, int stages, bool pair, KernelVariant* v) {
-  return square_float_variant<false, OUT_F16>(bn, stages, pair, v);
+bool square_variant_f16_f16(int bn, int stages, bool pair, KernelVariant* v, int kch) {
+  return square_float_variant<false, OUT_F16>(bn, stages, pair, v, kch);
 }
 
 }  // namespace sptg

@@ -218,14 +218,18 @@ struct EpiStaging {
   static constexpr int MAX_NBUF = 4;
 };
 
-template <int BN, int STAGES, bool INT_EXACT, bool PAIR, int OBYTES = 4>
+template <int BN, int STAGES, bool INT_EXACT, bool PAIR, int OBYTES = 4, int KCH = 1>
 struct SquareLayout {
   static constexpr int BM = 128;         // rows of A (and of C) per CTA
   static constexpr int TILE_M = PAIR ? 256 : 128;
   static constexpr int BN_CTA = PAIR ? BN / 2 : BN;  // rows of B per CTA
   static constexpr int BK = 64;  // 64 16-bit elements = one 128-byte swizzle row
-  static constexpr int A_STAGE = BM * BK * 2;
-  static constexpr int B_STAGE = BN_CTA * BK * 2;
+  // A ring stage holds KCH consecutive 64-wide K-chunks of each operand
+  // (chunk j of A at j * A_CHUNK, of B at j * B_CHUNK within the stage)
+  static constexpr int A_CHUNK = BM * BK * 2;
+  static constexpr int B_CHUNK = BN_CTA * BK * 2;
+  static constexpr int A_STAGE = KCH * A_CHUNK;
+  static constexpr int B_STAGE = KCH * B_CHUNK;
   using Epi = EpiStaging<OBYTES, INT_EXACT, (BN > 256)>;
   static constexpr int EPI_WARPS = Epi::WARPS;
   static constexpr int EPI_BUF = Epi::BUF;
@@ -285,6 +289,8 @@ struct SquareLayout {
   // the 2-SM MMA with M = 256 takes N in steps of 16: half a step per CTA
   static_assert(!PAIR || BN_CTA % 8 == 0, "each CTA's B rows must be a multiple of 8");
   static_assert(STAGES >= 1, "at least one stage");
+  static_assert(KCH == 1 || (KCH == 2 && !INT_EXACT && BN <= 256),
+                "two K-chunks per stage: float tiles up to 256 wide");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
   static_assert(NUM_BARS * 8 + 40 <= 256, "barrier area");
 };
@@ -333,11 +339,11 @@ __device__ __forceinline__ void stage_block(uint8_t* buf, const uint32_t (&v)[32
 
 // Deepest ring that fits the 227 KB per-CTA budget next to the epilogue
 // staging, the barriers and the 1 KB alignment slack.
-template <int BN, bool PAIR = false, int OBYTES = 4, bool INT_EXACT = false>
+template <int BN, bool PAIR = false, int OBYTES = 4, bool INT_EXACT = false, int KCH = 1>
 constexpr int square_max_stages() {
   using E = EpiStaging<OBYTES, INT_EXACT, (BN > 256)>;
   return (232448 - 1024 - E::WARPS * E::MIN_NBUF * E::BUF - 256) /
-         (128 * 64 * 2 + (PAIR ? BN / 2 : BN) * 64 * 2);
+         (KCH * (128 * 64 * 2 + (PAIR ? BN / 2 : BN) * 64 * 2));
 }
 
 // Adds up a cut tile's partials of this CTA's 128 rows in contributor order
@@ -425,13 +431,13 @@ __device__ __forceinline__ void reduce_cut_tile(const SquareParams& p, const uin
   }
 }
 
-template <int BN, int STAGES, bool IN_BF16, int OUT, bool INT_EXACT, bool PAIR = false>
+template <int BN, int STAGES, bool IN_BF16, int OUT, bool INT_EXACT, bool PAIR = false, int KCH = 1>
 __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREADS, 1)
     square_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const SquareParams p) {
   constexpr int OBYTES = OutTraits<OUT>::bytes;
-  using L = SquareLayout<BN, STAGES, INT_EXACT, PAIR, OBYTES>;
+  using L = SquareLayout<BN, STAGES, INT_EXACT, PAIR, OBYTES, KCH>;
   constexpr int BM = L::BM, BK = L::BK;
   // one MMA covers at most 256 columns: a 512-wide tile is two halves, each
   // half's B rows split between the CTAs of the pair like a 256-wide tile's
@@ -527,10 +533,12 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
     if (have_seg0) {
       tile_coords(seg0.tile, p.num_m_tiles, p.num_n_tiles, p.group_m, mt0, nt0);
       for (int kt = seg0.kt0; lane == 0 && kt < min(seg0.kt1, seg0.kt0 + STAGES); ++kt) {
-        tma_prefetch_l2_2d(&tmA, kt * BK, mt0 * L::TILE_M + static_cast<int>(rank) * BM);
-        for (int h = 0; h < NH; ++h)
-          tma_prefetch_l2_2d(&tmB, kt * BK,
-                             nt0 * BN + h * MMA_N + static_cast<int>(rank) * (L::BN_CTA / NH));
+        for (int j = 0; j < KCH; ++j) {
+          tma_prefetch_l2_2d(&tmA, (kt * KCH + j) * BK, mt0 * L::TILE_M + static_cast<int>(rank) * BM);
+          for (int h = 0; h < NH; ++h)
+            tma_prefetch_l2_2d(&tmB, (kt * KCH + j) * BK,
+                               nt0 * BN + h * MMA_N + static_cast<int>(rank) * (L::BN_CTA / NH));
+        }
       }
     }
   }
@@ -590,8 +598,17 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
             // announces the bytes of both
             if (rank == 0) mbar_arrive_expect_tx(full_bar(s), L::STAGE_TX);
             const uint32_t leader_full = map_to_cta(full_bar(s), leader_crank);
-            tma_load_2d_pair(sA + s * L::A_STAGE, &tmA, leader_full, kt * BK, a_row, pol);
-            if constexpr (NH == 2) {
+            if constexpr (KCH > 1) {
+              // KCH consecutive K-chunks of each operand (tiles up to 256 wide)
+#pragma unroll
+              for (int j = 0; j < KCH; ++j) {
+                tma_load_2d_pair(sA + s * L::A_STAGE + j * L::A_CHUNK, &tmA, leader_full,
+                                 (kt * KCH + j) * BK, a_row, pol);
+                tma_load_2d_pair(sB + s * L::B_STAGE + j * L::B_CHUNK, &tmB, leader_full,
+                                 (kt * KCH + j) * BK, b_row, pol_b);
+              }
+            } else if constexpr (NH == 2) {
+              tma_load_2d_pair(sA + s * L::A_STAGE, &tmA, leader_full, kt * BK, a_row, pol);
               // this CTA's rows of each 256-column half, one box per half
 #pragma unroll
               for (int h = 0; h < NH; ++h)
@@ -599,12 +616,18 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
                                  kt * BK, nt * BN + h * MMA_N + static_cast<int>(rank) * (MMA_N / 2),
                                  pol_b);
             } else {
+              tma_load_2d_pair(sA + s * L::A_STAGE, &tmA, leader_full, kt * BK, a_row, pol);
               tma_load_2d_pair(sB + s * L::B_STAGE, &tmB, leader_full, kt * BK, b_row, pol_b);
             }
           } else {
             mbar_arrive_expect_tx(full_bar(s), L::STAGE_TX);
-            tma_load_2d(sA + s * L::A_STAGE, &tmA, full_bar(s), kt * BK, a_row, pol);
-            tma_load_2d(sB + s * L::B_STAGE, &tmB, full_bar(s), kt * BK, b_row, pol_b);
+#pragma unroll
+            for (int j = 0; j < KCH; ++j) {
+              tma_load_2d(sA + s * L::A_STAGE + j * L::A_CHUNK, &tmA, full_bar(s),
+                          (kt * KCH + j) * BK, a_row, pol);
+              tma_load_2d(sB + s * L::B_STAGE + j * L::B_CHUNK, &tmB, full_bar(s),
+                          (kt * KCH + j) * BK, b_row, pol_b);
+            }
           }
           if (it == 0) trace_mark(p.trace, TR_FIRST_LOAD);
           trace_ktile(p.trace, 0, it);
@@ -672,13 +695,18 @@ __global__ void __launch_bounds__(INT_EXACT ? SQUARE_THREADS_INT : SQUARE_THREAD
             const uint64_t bdesc = b_desc0 + static_cast<uint64_t>((s * L::B_STAGE) >> 4);
             if (leader) {
 #pragma unroll
-              for (int h = 0; h < NH; ++h) {  // each 256-column half of a 512-wide tile
-                const uint64_t bd = bdesc + static_cast<uint64_t>((h * (MMA_N / 2) * (BK * 2)) >> 4);
-                const uint32_t dt = d_tmem + h * MMA_N;
-                mma_f16_g<PAIR>(dt, adesc, bd, IDESC, kt > c0 ? 1u : 0u);
+              for (int j = 0; j < KCH; ++j) {  // each 64-wide K-chunk of the stage
+                const uint64_t aj = adesc + static_cast<uint64_t>((j * L::A_CHUNK) >> 4);
 #pragma unroll
-                for (int k = 1; k < BK / 16; ++k)  // +32 bytes (2 in descriptor units) per K = 16
-                  mma_f16_g<PAIR>(dt, adesc + 2 * k, bd + 2 * k, IDESC, 1u);
+                for (int h = 0; h < NH; ++h) {  // each 256-column half of a 512-wide tile
+                  const uint64_t bd = bdesc + static_cast<uint64_t>((j * L::B_CHUNK) >> 4) +
+                                      static_cast<uint64_t>((h * (MMA_N / 2) * (BK * 2)) >> 4);
+                  const uint32_t dt = d_tmem + h * MMA_N;
+                  mma_f16_g<PAIR>(dt, aj, bd, IDESC, (kt > c0 || j > 0) ? 1u : 0u);
+#pragma unroll
+                  for (int k = 1; k < BK / 16; ++k)  // +32 bytes (2 in descriptor units) per K = 16
+                    mma_f16_g<PAIR>(dt, aj + 2 * k, bd + 2 * k, IDESC, 1u);
+                }
               }
               // stage s may be refilled (in both CTAs of a pair)
               mma_commit_g<PAIR>(empty_bar(s));

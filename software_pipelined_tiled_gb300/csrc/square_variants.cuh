@@ -7,11 +7,14 @@
 
 namespace sptg {
 
-template <int BN, int ST, bool BF, int OUT, bool IE, bool PAIR>
+template <int BN, int ST, bool BF, int OUT, bool IE, bool PAIR, int KCH = 1>
 KernelVariant make_square() {
-  return KernelVariant{reinterpret_cast<const void*>(&square_gemm_kernel<BN, ST, BF, OUT, IE, PAIR>),
-                       BN, ST, SquareLayout<BN, ST, IE, PAIR, OutTraits<OUT>::bytes>::SMEM_BYTES,
-                       PAIR, IE ? SQUARE_THREADS_INT : SQUARE_THREADS};
+  KernelVariant v{
+      reinterpret_cast<const void*>(&square_gemm_kernel<BN, ST, BF, OUT, IE, PAIR, KCH>), BN, ST,
+      SquareLayout<BN, ST, IE, PAIR, OutTraits<OUT>::bytes, KCH>::SMEM_BYTES, PAIR,
+      IE ? SQUARE_THREADS_INT : SQUARE_THREADS};
+  v.ksub = KCH;
+  return v;
 }
 
 // Tile widths BN from 112 to 256 in steps of 16, one CTA or a CTA pair per
@@ -20,8 +23,35 @@ KernelVariant make_square() {
 // and of BN 224 (pair) for the pipelining ablation (1 = load, then compute,
 // no overlap).
 template <bool BF, int OUT>
-bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v) {
+bool square_float_variant(int bn, int stages, bool pair, KernelVariant* v, int kch = 1) {
   constexpr int OB = OutTraits<OUT>::bytes;
+  if (kch == 2) {
+    // two 64-wide K-chunks per ring stage, at the deepest ring that fits
+    if (stages != 0) return false;
+#define SPTG_SQ2(BNV)                                                                           \
+  case BNV:                                                                                     \
+    if (pair)                                                                                   \
+      *v = make_square<BNV, square_max_stages<BNV, true, OB, false, 2>(), BF, OUT, false, true, 2>(); \
+    else                                                                                        \
+      *v = make_square<BNV, square_max_stages<BNV, false, OB, false, 2>(), BF, OUT, false, false, 2>(); \
+    return true;
+    switch (bn) {
+      SPTG_SQ2(256)
+      SPTG_SQ2(240)
+      SPTG_SQ2(224)
+      SPTG_SQ2(208)
+      SPTG_SQ2(192)
+      SPTG_SQ2(176)
+      SPTG_SQ2(160)
+      SPTG_SQ2(144)
+      SPTG_SQ2(128)
+      SPTG_SQ2(112)
+      default:
+        return false;
+    }
+#undef SPTG_SQ2
+  }
+  if (kch != 1) return false;
   if (bn == 512) {
     // 256 x 512 CTA-pair tiles: two 256-column MMAs per K-step, one accumulator
     if (!pair || (stages != 0 && stages != square_max_stages<512, true, OB>())) return false;

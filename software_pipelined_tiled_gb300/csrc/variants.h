@@ -17,15 +17,17 @@ struct KernelVariant {
   int smem;        // dynamic shared memory per CTA, bytes
   bool pair;       // square: 2-SM CTA-pair variant (cluster of 2)
   int threads = 192;  // CTA size
-  int ksub = 1;       // skinny cluster: 64-wide K-chunks per ring stage
+  int ksub = 1;       // 64-wide K-chunks per ring stage (skinny kernels, square kernel)
 };
 
-// Square kernel for binary16 inputs (out_kind OUT_F16 or OUT_F32).
-bool square_variant_f16_f16(int bn, int stages, bool pair, KernelVariant* v);
-bool square_variant_f16_f32(int bn, int stages, bool pair, KernelVariant* v);
+// Square kernel for binary16 inputs (out_kind OUT_F16 or OUT_F32); kch =
+// 64-wide K-chunks per ring stage (1, or 2 for the deepest rings of tiles up
+// to 256 wide).
+bool square_variant_f16_f16(int bn, int stages, bool pair, KernelVariant* v, int kch = 1);
+bool square_variant_f16_f32(int bn, int stages, bool pair, KernelVariant* v, int kch = 1);
 // Square kernel for bfloat16 inputs (out_kind OUT_BF16 or OUT_F32).
-bool square_variant_bf16_bf16(int bn, int stages, bool pair, KernelVariant* v);
-bool square_variant_bf16_f32(int bn, int stages, bool pair, KernelVariant* v);
+bool square_variant_bf16_bf16(int bn, int stages, bool pair, KernelVariant* v, int kch = 1);
+bool square_variant_bf16_f32(int bn, int stages, bool pair, KernelVariant* v, int kch = 1);
 // Square kernel in exact-integer mode (int8 operands widened to binary16).
 bool square_variant_s8(int bn, int stages, bool pair, KernelVariant* v);
 // Skinny kernel (in_bf16 selects bfloat16 inputs, else binary16).

@@ -173,6 +173,53 @@ def test_half_block_tiles_cut_along_k(bn, cta_pair):
     assert_float_parity(C, A, B)
 
 
+@pytest.mark.parametrize("bn,it,ot", [(112, "f16", F16), (176, "f16", F16), (144, "bf16", BF16),
+                                      (128, "bf16", F32), (112, "bf16", F32)])
+def test_two_chunk_stages(bn, it, ot):
+    # CTA pairs over K-loops of 32 K-chunks or more take two 64-wide K-chunks
+    # per ring stage where that ring still holds four stages; K = 2056 leaves
+    # the last stage's second chunk wholly past K (zero-filled)
+    A, B = make_inputs(300, 680, 2056, it, "uniform", bn + 3)
+    C = run(A, B, ot, kernel="square", bn=bn, cta_pair=2, splits=7, stream_k=1)
+    cfg = sptg.last_config()
+    assert "kch=2" in cfg and f"bn={bn}" in cfg and "pair=1" in cfg, cfg
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("bn,cta_pair,ot", [(176, 2, F32), (192, 2, F16), (176, 1, F16),
+                                            (112, 1, F16)])
+def test_one_chunk_stages_where_two_leave_a_shallow_ring(bn, cta_pair, ot):
+    # fp32 C at 176 columns and 192-wide pairs would keep three two-chunk
+    # stages, single CTAs two or three: one chunk per stage there
+    A, B = make_inputs(300, 680, 2056, "f16", "uniform", bn + 5)
+    C = run(A, B, ot, kernel="square", bn=bn, cta_pair=cta_pair)
+    assert "kch=1" in sptg.last_config(), sptg.last_config()
+    assert_float_parity(C, A, B)
+
+
+@pytest.mark.parametrize("T", [32, 33, 47])
+def test_k_tile_marker_two_chunk_stages(T):
+    # both chunks of every stage land in the sum exactly once (T odd: the
+    # last stage holds one chunk inside K); three pairs over several tiles
+    A, B, expect = _marker_inputs(512, 896, T)
+    C = run(A, B, F32, kernel="square", bn=112, cta_pair=2, splits=3, stream_k=1)
+    assert "kch=2" in sptg.last_config(), sptg.last_config()
+    assert (C.to(torch.float64) == expect).all()
+
+
+def test_two_chunk_stages_cut_along_k():
+    # stream-K over stages of two K-chunks: the cut falls between stages
+    A, B = make_inputs(520, 776, 4104, "bf16", "uniform", 62)
+    C = run(A, B, F32, kernel="square", bn=112, cta_pair=2, stream_k=2, splits=5)
+    assert _sk_tiles() > 0 and "kch=2" in sptg.last_config(), sptg.last_config()
+    assert_float_parity(C, A, B)
+    # a forced ring depth keeps one chunk per stage (the deepest one-chunk
+    # ring of a 112-wide pair tile with fp32 C: 8 stages)
+    C = run(A, B, F32, kernel="square", bn=112, cta_pair=2, stages=8)
+    assert "kch=1" in sptg.last_config() and "stages=8" in sptg.last_config()
+    assert_float_parity(C, A, B)
+
+
 @pytest.mark.parametrize("bn", [112, 176])
 def test_half_block_columns_are_placed(bn):
     # each column of B distinct, A the identity block: C[i, j] = B[j, i]
