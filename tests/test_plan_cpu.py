@@ -178,3 +178,25 @@ def test_no_multicast_mode():
     for cfg in ({"cta_pair": 3}, {"cta_pair": -1}):
         with pytest.raises(sptg.SptgError):
             plan(4096, 4096, 4096, **cfg)
+
+
+def test_two_chunk_stages_count_in_the_stream_k_split():
+    # Float CTA pairs over K-loops of 32 K-chunks or more whose two-chunk ring
+    # keeps four stages take two 64-wide K-chunks per stage, and the stream-K
+    # split counts in stages: one cut tile over every pair, at least 8 stages
+    # (16 K-chunks) each. 176-wide pairs with 16-bit C qualify; with fp32 C
+    # (three two-chunk stages) and single CTAs they keep one chunk per stage.
+    K = 64 * 600  # 600 K-chunks, 300 two-chunk stages
+    for dtype, pair, chunks in [("f16_f16", 2, 2), ("bf16_bf16", 2, 2), ("f16_f32", 2, 1),
+                                ("bf16_f32", 2, 1), ("f16_f16", 1, 1)]:
+        p = plan(256 if pair == 2 else 128, 176, K, dtype, bn=176, cta_pair=pair, stream_k=2)
+        assert p["stream_k_tiles"] == p["tiles"] == 1
+        stages = -(-K // (64 * chunks))
+        workers = SM // 2 if pair == 2 else SM
+        assert p["stream_k_workers"] == min(workers, stages // 8), (dtype, pair)
+    # a short K-loop (fewer than 32 K-chunks) keeps one chunk per stage
+    p = plan(256, 176, 64 * 31, "f16_f16", bn=176, cta_pair=2, stream_k=2)
+    assert p["stream_k_workers"] == min(SM // 2, 31 // 8)
+    # int8 never takes two chunks (its exact sums are cut every 1024 products)
+    p = plan(256, 192, 64 * 600, "s8_s32", bn=192, cta_pair=2, stream_k=2)
+    assert p["stream_k_workers"] == min(SM // 2, 600 // 8)
